@@ -1,0 +1,168 @@
+"""Pins the oracle's amax, current-scale rules and the four quantisation
+granularities against closed forms, invariants and brute force."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle as o
+
+
+def _enc_err_bound(fmt, p):
+    """half the spacing of the format around |p| (p already scaled, |p| <= fmax)"""
+    a = abs(float(p))
+    if fmt == o.E4M3:
+        e = max(math.floor(math.log2(a)) if a > 0 else -6, -6)
+        return 2.0 ** (e - 3) / 2
+    e = max(math.floor(math.log2(a)) if a > 0 else -14, -14)
+    return 2.0 ** (e - 2) / 2
+
+
+def test_amax_brute_force_and_nan():
+    rng = np.random.default_rng(0)
+    for n in [1, 2, 7, 128, 1000]:
+        x = rng.standard_normal(n).astype(np.float32)
+        assert o.amax(x) == np.max(np.abs(x))
+    assert o.amax(np.zeros(5, np.float32)) == 0.0
+    assert o.amax(np.float32([-3.0, 2.0])) == 3.0
+    assert math.isnan(o.amax(np.float32([1.0, np.nan, 5.0])))
+
+
+@pytest.mark.parametrize("fmt", [o.E4M3, o.E5M2])
+def test_current_scale_closed_forms(fmt):
+    fm = o.fmax(fmt)
+    m, s = o.current_scale(fm / 4, fmt)
+    assert m == 4.0 and s == 0.25
+    m, s = o.current_scale(fm, fmt)
+    assert m == 1.0 and s == 1.0
+    for bad in [0.0, math.inf, math.nan]:
+        assert o.current_scale(bad, fmt) == (1.0, 1.0)
+    m, s = o.current_scale(3.0, fmt)
+    assert m == np.float32(fm) / np.float32(3.0) and s == np.float32(3.0) / np.float32(fm)
+
+
+@pytest.mark.parametrize("fmt", [o.E4M3, o.E5M2])
+def test_tensor_current_invariants(fmt):
+    rng = np.random.default_rng(1 + fmt)
+    x = (rng.standard_normal((64, 96)) * 3).astype(np.float32)
+    q, a, s, sat = o.quantize_tensor_current(x, fmt)
+    maxc = 0x7E if fmt == o.E4M3 else 0x7B
+    i = np.unravel_index(np.argmax(np.abs(x)), x.shape)
+    assert q[i] & 0x7F == maxc                       # the amax element lands on +-fmax
+    assert sat == 0
+    m, _ = o.current_scale(a, fmt)
+    deq = o.decode_array(fmt, q)
+    p = x.astype(np.float32) * m
+    for (r, c) in [(0, 0), (5, 7), (63, 95), i]:
+        assert abs(deq[r, c] - float(p[r, c])) <= _enc_err_bound(fmt, p[r, c])
+    assert np.all(np.sign(deq) * np.sign(x) >= 0)  # sign kept
+
+
+@pytest.mark.parametrize("fmt", [o.E4M3, o.E5M2])
+def test_power_of_two_rescale_is_exact(fmt):
+    """Multiplying a tensor by 2^k multiplies its step s by 2^k and leaves the
+    codes unchanged (the rule is scale-equivariant in binary)."""
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((4, 256)).astype(np.float32)
+    for gran_fn in [o.quantize_tile1x128, o.quantize_mx32]:
+        q0, s0, *_ = gran_fn(x, fmt)
+        q1, s1, *_ = gran_fn(x * np.float32(8.0), fmt)
+        assert np.array_equal(q0, q1)
+        if gran_fn is o.quantize_mx32:
+            assert np.array_equal(s1.astype(int), s0.astype(int) + 3)
+        else:
+            assert np.array_equal(s1, s0 * np.float32(8.0))
+
+
+def test_tile_outlier_only_spoils_its_own_tile():
+    """Week 14 absmax bullet: with per-block scales an outlier only hurts its
+    own block.  A 1x128 tile with an outlier changes codes in that tile only."""
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((3, 512)).astype(np.float32)
+    q0, s0, a0, _ = o.quantize_tile1x128(x, o.E4M3)
+    y = x.copy()
+    y[1, 300] = 1000.0
+    q1, s1, a1, _ = o.quantize_tile1x128(y, o.E4M3)
+    diff = np.argwhere(q0 != q1)
+    assert len(diff) > 0
+    assert set(map(tuple, np.unique(np.stack([diff[:, 0], diff[:, 1] // 128], 1), axis=0))) == {(1, 2)}
+    assert np.array_equal(np.argwhere(s0 != s1), np.array([[1, 2]]))
+    assert a1[1, 2] == 1000.0
+
+
+def test_tile_layout_rows_and_columns():
+    """Scale layout s[r][c/128]: a tile whose values are all v gets s = v/448
+    and every code is 0x7E; other tiles keep their own scale."""
+    x = np.zeros((2, 384), np.float32)
+    x[0, 0:128] = 3.0
+    x[0, 128:256] = -5.0
+    x[1, 256:384] = 0.5
+    q, s, a, _ = o.quantize_tile1x128(x, o.E4M3)
+    assert s.shape == (2, 3)
+    assert s[0, 0] == np.float32(3.0) / np.float32(448.0)
+    assert s[0, 1] == np.float32(5.0) / np.float32(448.0)
+    assert s[1, 2] == np.float32(0.5) / np.float32(448.0)
+    assert s[0, 2] == 1.0 and s[1, 0] == 1.0       # all-zero tiles
+    assert np.all(q[0, 0:128] == 0x7E) and np.all(q[0, 128:256] == 0xFE)
+    assert np.all(q[1, 256:] == 0x7E) and np.all(q[1, :256] == 0)
+
+
+def test_block128_layout_and_outlier():
+    rng = np.random.default_rng(6)
+    x = (rng.standard_normal((256, 384)) * 0.02).astype(np.float32)
+    q0, s0, a0, _ = o.quantize_block128(x, o.E4M3)
+    assert s0.shape == (2, 3)
+    for bi in range(2):
+        for bj in range(3):
+            blk = x[bi * 128:(bi + 1) * 128, bj * 128:(bj + 1) * 128]
+            assert a0[bi, bj] == np.max(np.abs(blk))
+            assert s0[bi, bj] == np.float32(np.max(np.abs(blk))) / np.float32(448.0)
+    y = x.copy()
+    y[130, 5] = 7.0                                     # block (1, 0)
+    q1, s1, _, _ = o.quantize_block128(y, o.E4M3)
+    changed = {(int(r) // 128, int(c) // 128) for r, c in np.argwhere(q0 != q1)}
+    assert changed == {(1, 0)}
+    assert np.array_equal(np.argwhere(s0 != s1), np.array([[1, 0]]))
+
+
+@pytest.mark.parametrize("fmt", [o.E4M3, o.E5M2])
+def test_mx_exponent_special_cases(fmt):
+    emax = 8 if fmt == o.E4M3 else 15
+    fm = o.fmax(fmt)
+    for k in range(-20, 21):
+        assert o.mx_scale_code(fm * 2.0 ** k, fmt) == 127 + k          # amax exactly fmax*2^k
+        assert o.mx_scale_code(2.0 ** (emax + k), fmt) == 127 + k      # 1.0 * 2^(emax+k)
+        just_above = float(np.nextafter(np.float32(fm * 2.0 ** k), np.float32(np.inf)))
+        assert o.mx_scale_code(just_above, fmt) == 128 + k             # bumps by one
+    assert o.mx_scale_code(0.0, fmt) == 127
+    assert o.mx_scale_code(math.nan, fmt) == 0xFF
+    assert o.mx_scale_code(math.inf, fmt) == 0xFF
+    assert o.mx_scale_code(1e-45, fmt) == 0                            # clamped at 2^-127
+    assert o.mx_scale_code(3e38, fmt) <= 254
+
+
+@pytest.mark.parametrize("fmt", [o.E4M3, o.E5M2])
+def test_mx_never_saturates_and_is_minimal(fmt):
+    rng = np.random.default_rng(8)
+    x = (rng.standard_normal((16, 256)) * 2.0 ** rng.integers(-30, 30, (16, 1))).astype(np.float32)
+    x[3, 17] *= 100.0
+    q, e, a, sat = o.quantize_mx32(x, fmt)
+    assert sat == 0
+    fm = o.fmax(fmt)
+    for r in range(16):
+        for t in range(8):
+            amax = float(np.max(np.abs(x[r, 32 * t:32 * t + 32])))
+            k = int(e[r, t]) - 127
+            assert amax <= fm * 2.0 ** k                     # fits
+            assert amax > fm * 2.0 ** (k - 1)                # smallest such power of two
+            deq = o.decode_array(fmt, q[r, 32 * t:32 * t + 32]) * 2.0 ** k
+            xs = x[r, 32 * t:32 * t + 32].astype(np.float64)
+            bound = np.array([_enc_err_bound(fmt, v * 2.0 ** -k) for v in xs]) * 2.0 ** k
+            assert np.all(np.abs(deq - xs) <= bound)
+
+
+def test_sat_count_and_clipping():
+    x = np.float32([1.0, 500.0, -448.0, 449.0, -1e6])
+    q, sat = o.quantize_with_multiplier(x, 1.0, o.E4M3)
+    assert sat == 3
+    assert q.tolist() == [o.encode(o.E4M3, 1.0), 0x7E, 0xFE, 0x7E, 0xFE]
