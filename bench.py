@@ -1,0 +1,458 @@
+#!/usr/bin/env python
+"""Benchmark of the FP8 scaled-linear hot path on GB300.
+
+One step = one pass of the whole path over one batch of the large FFN
+training step (M = 16384 tokens, 4096 -> 14336 and 14336 -> 4096 linears,
+HYBRID per-tensor delayed scaling, amax history 16): for each linear,
+quantize x and W (E4M3, with transposed copies), forward GEMM, quantize dy
+(E5M2, with transposed copy), dgrad GEMM, wgrad GEMM; then the end-of-step
+scale update of all six tensor roles.  Every step runs in this library's
+kernels through its C ABI.
+
+Metric: FP8 linear TFLOP/s = GEMM FLOPs (2MNK per GEMM, six per step) per
+second of the whole step (quantize + GEMM + scale update), with the inputs
+resident in HBM; plus quantize GB/s, each against its roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain reference implementation of
+the same arithmetic) on a bounded sample of the same workload.  Several GPUs
+run independent replicas (the path has no exchange step on one node).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from scaled_quantize_gemm_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "FP8 linear TFLOP/s (quant+GEMM) and quantize GB/s, as % of roofline"
+UNIT = "TFLOP/s"
+H = 16
+WK = wl.WORKLOADS[5]
+SAMPLE_TOKENS = 128      # CPU oracle sample: the same step at 128 tokens
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "of measured"
+    except Exception:
+        return 6800.0, 1900.0, "of fallback"
+
+
+# ---------------------------------------------------------------- distributed
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _barrier_max(value: float, ws: int, device) -> float:
+    if ws == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        rows = []
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[6:10]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(float(r[4]) for r in rows if r[4].replace(".", "").isdigit())
+                if any(r[4].replace(".", "").isdigit() for r in rows) else None}
+
+
+# ---------------------------------------------------------------- our arm
+class FFNStep:
+    """Device buffers and the timed step of workload 5."""
+
+    def __init__(self, device, n_input_sets: int):
+        import scaled_quantize_gemm_gb300 as sq
+        self.sq = sq
+        self.dev = device
+        M = WK.tokens
+        self.M = M
+        self.lin = [(l.in_features, l.out_features) for l in WK.linears]      # (K, N)
+        self.W = [wl.linear_w(5, li, N, K, device) for li, (K, N) in enumerate(self.lin)]
+        self.inputs = []
+        for s in range(n_input_sets):
+            per = []
+            for li, (K, N) in enumerate(self.lin):
+                per.append((wl.linear_x(5, li, s, M, K, device), wl.linear_dy(5, li, s, M, N, device)))
+            self.inputs.append(per)
+        u8 = dict(dtype=torch.uint8, device=device)
+        self.buf = []
+        for li, (K, N) in enumerate(self.lin):
+            self.buf.append(dict(
+                qx=torch.empty((M, K), **u8), qxT=torch.empty((K, M), **u8),
+                qw=torch.empty((N, K), **u8), qwT=torch.empty((K, N), **u8),
+                qdy=torch.empty((M, N), **u8), qdyT=torch.empty((N, M), **u8),
+                y=torch.empty((M, N), dtype=torch.bfloat16, device=device),
+                dx=torch.empty((M, K), dtype=torch.bfloat16, device=device),
+                dw=torch.empty((N, K), dtype=torch.float32, device=device),
+                ws=torch.empty(sq.fp8_linear_workspace_bytes(M, N, K), **u8)))
+        self.states = torch.empty(6 * (H + 2), dtype=torch.float32, device=device)
+        self.formats = [sq.E4M3, sq.E4M3, sq.E5M2] * 2
+        sq.fp8_scale_init(self.states, 6, H)
+
+    def st(self, i):
+        return self.states[i * (H + 2):(i + 1) * (H + 2)]
+
+    def s(self, i):
+        return self.states[i * (H + 2) + H + 1:i * (H + 2) + H + 2]
+
+    def gemm_flops_per_step(self):
+        M = self.M
+        return sum(3 * 2 * M * N * K for (K, N) in self.lin)
+
+    def quant_bytes_per_step(self):
+        # bf16 read + code write + transposed code write, per element
+        M = self.M
+        return sum(4 * (M * K + N * K + M * N) for (K, N) in self.lin)
+
+    def step(self, s: int, ev=None):
+        """One pass of the hot path through the granular C-ABI calls; `ev`
+        (a list) receives (kind, start_event, end_event) per call."""
+        sq = self.sq
+        inp = self.inputs[s % len(self.inputs)]
+
+        def rec(kind, fn):
+            if ev is None:
+                fn()
+                return
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            ev.append((kind, a, b))
+
+        for li, (K, N) in enumerate(self.lin):
+            x, dy = inp[li]
+            B = self.buf[li]
+            sx, sw, sd = 3 * li, 3 * li + 1, 3 * li + 2
+            rec("quant", lambda: sq.fp8_quantize(x, sq.E4M3, sq.TENSOR, B["qx"], qT=B["qxT"],
+                                                 delayed_state=self.st(sx), history_len=H))
+            rec("quant", lambda: sq.fp8_quantize(self.W[li], sq.E4M3, sq.TENSOR, B["qw"], qT=B["qwT"],
+                                                 delayed_state=self.st(sw), history_len=H))
+            rec("gemm", lambda: sq.fp8_gemm(B["qx"], sq.E4M3, self.s(sx), sq.TENSOR,
+                                            B["qw"], sq.E4M3, self.s(sw), sq.TENSOR, B["y"]))
+            rec("quant", lambda: sq.fp8_quantize(dy, sq.E5M2, sq.TENSOR, B["qdy"], qT=B["qdyT"],
+                                                 delayed_state=self.st(sd), history_len=H))
+            rec("gemm", lambda: sq.fp8_gemm(B["qdy"], sq.E5M2, self.s(sd), sq.TENSOR,
+                                            B["qwT"], sq.E4M3, self.s(sw), sq.TENSOR, B["dx"]))
+            rec("gemm", lambda: sq.fp8_gemm(B["qdyT"], sq.E5M2, self.s(sd), sq.TENSOR,
+                                            B["qxT"], sq.E4M3, self.s(sx), sq.TENSOR, B["dw"]))
+        rec("update", lambda: sq.fp8_update_scale(self.states, 6, H, self.formats))
+
+    KERNELS_PER_STEP = 13   # 6 casts + 6 GEMMs + 1 scale update
+
+    def e2e_step(self, host_inputs, dev_in, states_host):
+        """The same step through the linear-layer API with host buffers: the
+        step's x and dy arrive from pinned host memory, the step's scale state
+        goes back to the host."""
+        sq = self.sq
+        for li, (K, N) in enumerate(self.lin):
+            xh, dyh = host_inputs[li]
+            xd, dyd = dev_in[li]
+            B = self.buf[li]
+            xd.copy_(xh, non_blocking=True)
+            dyd.copy_(dyh, non_blocking=True)
+            sq.fp8_linear_fwd(xd, self.W[li], B["y"], B["ws"], x_state=self.st(3 * li),
+                              w_state=self.st(3 * li + 1), history_len=H)
+            sq.fp8_linear_bwd(dyd, B["dx"], B["dw"], B["ws"], K, dy_state=self.st(3 * li + 2), history_len=H)
+        sq.fp8_update_scale(self.states, 6, H, self.formats)
+        states_host.copy_(self.states, non_blocking=True)
+
+
+def run_ours(args, ws, rank, local):
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    hbm_peak, bf16_peak, peak_src = _peaks()
+    fp8_peak = 2.0 * bf16_peak          # dense FP8 = 2 x dense BF16 (nominal ratio 4.5 / 2.25)
+
+    b = FFNStep(device, n_input_sets=min(WK.steps, max(2, args.steps + args.warmup)))
+    for s in range(args.warmup):
+        b.step(s)
+    torch.cuda.synchronize()
+    rc = b.sq.fp8_device_status(True)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} after warm-up")
+
+    clocks = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.3 if clocks and clocks.proc else 0.0)
+    ev = []
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for s in range(args.steps):
+        b.step(args.warmup + s, ev)
+    t1.record()
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop() if clocks else None
+    total_ms = _barrier_max(t0.elapsed_time(t1), ws, device)
+    rc = b.sq.fp8_device_status(True)
+    if rc != 0:
+        raise RuntimeError(f"device status {rc} after the timed steps")
+
+    ms_step = total_ms / args.steps
+    flops = b.gemm_flops_per_step()
+    value = ws * flops / (ms_step * 1e-3) / 1e12
+    per = {"gemm": [], "quant": [], "update": []}
+    for kind, a, e in ev:
+        per[kind].append(a.elapsed_time(e))
+    gemm_ms = statistics.mean(per["gemm"])
+    gemm_flops_launch = flops / 6
+    achieved = gemm_flops_launch / (gemm_ms * 1e-3) / 1e12
+    quant_ms_step = sum(per["quant"]) / args.steps
+    qbytes = b.quant_bytes_per_step()
+    quant_gbs = qbytes / (quant_ms_step * 1e-3) / 1e9
+    # the largest cast: x of the second linear / dy of the first (16384 x 14336)
+    big = [per["quant"][i] for i in range(len(per["quant"])) if i % 6 in (2, 3)]
+    big_bytes = 4 * WK.tokens * 14336
+    big_gbs = big_bytes / (statistics.mean(big) * 1e-3) / 1e9
+
+    # ---- end to end through the linear API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_sets = []
+        for s in range(2):
+            host_sets.append([(x.to("cpu").pin_memory(), dy.to("cpu").pin_memory())
+                              for (x, dy) in b.inputs[s % len(b.inputs)]])
+        dev_in = [(torch.empty_like(x), torch.empty_like(dy)) for (x, dy) in b.inputs[0]]
+        states_host = torch.empty(b.states.shape, dtype=torch.float32).pin_memory()
+        h2d = sum(x.numel() * x.element_size() + dy.numel() * dy.element_size() for (x, dy) in host_sets[0])
+        d2h = states_host.numel() * 4
+        for s in range(args.warmup):
+            b.e2e_step(host_sets[s % 2], dev_in, states_host)
+        torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for s in range(args.steps):
+            b.e2e_step(host_sets[s % 2], dev_in, states_host)
+        e1.record()
+        torch.cuda.synchronize()
+        e2e_ms = _barrier_max(e0.elapsed_time(e1), ws, device) / args.steps
+        e2e = {"value": round(ws * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "api": "fp8_linear_fwd / fp8_linear_bwd / fp8_update_scale, pinned host x and dy in, "
+                      "scale states out"}
+        if b.sq.fp8_device_status(True) != 0:
+            raise RuntimeError("device status error in the end-to-end leg")
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(budget_s=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp8", "data": "synthetic",
+            "config": {"workload": WK.name, "tokens": WK.tokens,
+                       "linears": [f"{K}->{N}" for (K, N) in b.lin], "history_len": H,
+                       "recipe": "HYBRID per-tensor delayed (E4M3 fwd, E5M2 grads), amax_compute_algo=max",
+                       "outputs": "y bf16, dx bf16, dW fp32",
+                       "l2": "no flush: every step reads inputs larger than L2 (128-470 MB each, 10 rotating "
+                             "seeded batches)",
+                       "parallelism": f"replicas x{ws}"},
+            "clocks": clk,
+            "e2e": e2e,
+            "gpu_launches": b.KERNELS_PER_STEP * args.steps,
+            "roofline": {"bound": "tensor", "kernel": "k_gemm_tensor (tcgen05 kind::f8f6f4, 128x256 tile)",
+                         "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                         "frac": round(achieved / fp8_peak, 4), "traffic": None,
+                         "peak_source": f"2 x bf16_tflops {peak_src} (dense FP8 = 2 x dense BF16)",
+                         "flops_per_launch": gemm_flops_launch, "launch_ms": round(gemm_ms, 4)},
+            "roofline_quantize": {"bound": "hbm", "kernel": "k_cast_tensor_T (16384 x 14336 casts)",
+                                  "achieved": round(big_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                                  "frac": round(big_gbs / hbm_peak, 4), "traffic": None,
+                                  "peak_source": f"hbm_gbs {peak_src}",
+                                  "bytes_per_launch": big_bytes},
+            "quantize": {"GB_per_s_all_casts": round(quant_gbs, 1), "ms_per_step": round(quant_ms_step, 4),
+                         "bytes_per_step": qbytes},
+            "gemm": {"ms_per_step": round(sum(per["gemm"]) / args.steps, 4),
+                     "tflops_per_s": round(achieved, 1)},
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ---------------------------------------------------------------- CPU oracle
+def _oracle_sample_inputs(step: int):
+    """The workload's step at SAMPLE_TOKENS tokens (same recipe, CPU-drawn)."""
+    out = []
+    for li, lin in enumerate(WK.linears):
+        K, N = lin.in_features, lin.out_features
+        x = wl.linear_x(5, li, step, SAMPLE_TOKENS, K, "cpu").float().numpy()
+        dy = wl.linear_dy(5, li, step, SAMPLE_TOKENS, N, "cpu").float().numpy()
+        out.append((x, dy))
+    return out
+
+
+def _oracle_weights():
+    return [wl.linear_w(5, li, l.out_features, l.in_features, "cpu").float().numpy()
+            for li, l in enumerate(WK.linears)]
+
+
+def oracle_sample_step(o, weights, inputs, states):
+    """One step of the workload through the CPU oracle at SAMPLE_TOKENS
+    tokens: quantize x, W, dy (delayed), forward, dgrad, wgrad, update.
+    Returns the GEMM FLOPs processed."""
+    flops = 0
+    for li, (x, dy) in enumerate(inputs):
+        sx, sw, sd = states[3 * li], states[3 * li + 1], states[3 * li + 2]
+        qx, fx, qw, fw, _ = o.linear_fwd_delayed(x, weights[li], sx, sw)
+        o.linear_bwd_delayed(dy, sd, o.E5M2, qx, fx, qw, fw)
+        M, K = x.shape
+        N = weights[li].shape[0]
+        flops += 3 * 2 * M * N * K
+    for i, st in enumerate(states):
+        o.update_scale(st, o.E5M2 if i % 3 == 2 else o.E4M3)
+    return flops
+
+
+def cpu_baseline(budget_s: float = 20.0):
+    import oracle as o
+    o.build()
+    weights = _oracle_weights()
+    states = [o.state_init(H) for _ in range(6)]
+    inputs = [_oracle_sample_inputs(s) for s in range(2)]
+    oracle_sample_step(o, weights, inputs[0], states)        # warm (build, page-in)
+    t = time.perf_counter()
+    flops, n = 0, 0
+    while True:
+        flops += oracle_sample_step(o, weights, inputs[n % 2], states)
+        n += 1
+        if time.perf_counter() - t > budget_s or n >= 50:
+            break
+    dt = time.perf_counter() - t
+    return {"value": round(flops / dt / 1e12, 6), "unit": UNIT, "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": f"{n} steps of the FFN workload at {SAMPLE_TOKENS} tokens (full 4096x14336 weights "
+                      f"quantised every step), {dt:.1f} s"}
+
+
+def run_reference(args, ws, rank, local):
+    if rank != 0:
+        return
+    import oracle as o
+    o.build()
+    weights = _oracle_weights()
+    states = [o.state_init(H) for _ in range(6)]
+    inputs = [_oracle_sample_inputs(s) for s in range(2)]
+    for s in range(args.warmup):
+        oracle_sample_step(o, weights, inputs[s % 2], states)
+    t = time.perf_counter()
+    flops = 0
+    for s in range(args.steps):
+        flops += oracle_sample_step(o, weights, inputs[s % 2], states)
+    dt = time.perf_counter() - t
+    value = flops / dt / 1e12
+    cores = len(os.sched_getaffinity(0))
+    sample = f"each step = the FFN workload at {SAMPLE_TOKENS} tokens with full weights"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+        "data": "synthetic",
+        "config": {"workload": WK.name, "tokens": SAMPLE_TOKENS, "parallelism": "CPU, rank 0 only"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = _dist()
+    if args.impl == "reference":
+        run_reference(args, ws, rank, local)
+    else:
+        run_ours(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    main()

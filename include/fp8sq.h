@@ -1,0 +1,232 @@
+/*
+ * fp8sq.h -- C ABI of the GB300 (sm_103a) FP8 scaled-linear library.
+ *
+ * The path: amax -> scale (current or delayed) -> saturating round-to-
+ * nearest-even cast to E4M3 / E5M2 -> FP8 GEMM with fp32 accumulation and a
+ * dequantising epilogue, for the forward, dgrad and wgrad products of a
+ * linear layer y = x W^T.
+ *
+ * Sources, cited by page title and section:
+ *   [TS]  "Transformer Scaling" (lab.mindcaptain.ai, reading 06): Part 01
+ *         (scale maps a tensor into FP8's range using amax; delayed vs
+ *         current scaling; HYBRID = E4M3 forward, E5M2 gradients), core
+ *         vocabulary (amax, delayed scaling), worked example.
+ *   [W14] "Week 14. Scaling laws, precision, parallelism": absmax bullet
+ *         (x ~ q * scale, scale from max|x|; per tensor / block; 1x128
+ *         activation tiles and 128x128 weight blocks; MX blocks of 32), FP8
+ *         bullet (E4M3 max 448, E5M2 max 57344; matmuls in FP8), accumulation
+ *         precision bullet (wide accumulator, fp32 promotion at intervals).
+ *   [TE]  "Accelerating Transformer Training with NVIDIA Transformer Engine":
+ *         DelayedScaling(HYBRID, amax_history_len=16, amax_compute_algo=max),
+ *         te.Linear, the fp8_meta scale / amax_history dump.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named as device pointers are caller-owned device memory; the
+ *    library allocates nothing and keeps no state between calls except a
+ *    per-device cache of the SM count and a sticky device error word.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *    only enqueues work on it and returns; the caller synchronises.
+ *  - Matrices are row-major with row pitch = number of columns.
+ *  - Return value: FP8SQ_OK (0) or a negative FP8SQ_ERR_* code.  Arguments
+ *    are validated before anything is enqueued, so an error return means
+ *    nothing was launched (except FP8SQ_ERR_CUDA from a failed launch).
+ *    fp8_last_error() gives a message for the calling thread's last error.
+ *    Nothing aborts, traps or prints.
+ *  - Only sm_103 devices are accepted (FP8SQ_ERR_WRONG_ARCH otherwise).
+ */
+#ifndef FP8SQ_H
+#define FP8SQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define FP8SQ_API __attribute__((visibility("default")))
+#else
+#define FP8SQ_API
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define FP8SQ_OK 0
+#define FP8SQ_ERR_INVALID_ARG -1  /* null pointer, negative size, bad enum */
+#define FP8SQ_ERR_UNSUPPORTED -2  /* shape / granularity combination not supported */
+#define FP8SQ_ERR_MISALIGNED -3   /* a pointer is not 16-byte aligned */
+#define FP8SQ_ERR_WRONG_ARCH -4   /* current device is not sm_103 */
+#define FP8SQ_ERR_CUDA -5         /* a CUDA runtime / driver call failed */
+#define FP8SQ_ERR_TIMEOUT -6      /* a bounded device-side wait ran out */
+
+/* ---- enumerations ---------------------------------------------------- */
+/* [W14] FP8 bullet: E4M3 (max 448, no infinities, S.1111.111 = NaN) and
+ * E5M2 (max 57344, IEEE-like with infinities). */
+#define FP8SQ_E4M3 0
+#define FP8SQ_E5M2 1
+
+/* element types of inputs and outputs */
+#define FP8SQ_BF16 0
+#define FP8SQ_F32 1
+
+/* scaling units ([W14] absmax bullet) */
+#define FP8SQ_TENSOR 0         /* one scale per tensor                          */
+#define FP8SQ_TILE_1x128 1     /* one scale per 128 consecutive values of a row */
+#define FP8SQ_BLOCK_128x128 2  /* one scale per 128x128 block                   */
+#define FP8SQ_MX32 3           /* one power-of-two (E8M0) scale per 32 values   */
+
+/* amax history reduction ([TE] amax_compute_algo) */
+#define FP8SQ_AMAX_MAX 0
+#define FP8SQ_AMAX_MOST_RECENT 1
+
+/* recipes ([TS] Part 01 / [TE] Format.HYBRID; [W14] "E4M3 is enough
+ * everywhere" with fine-grained scaling) */
+#define FP8SQ_RECIPE_HYBRID 0     /* x, W in E4M3; dY in E5M2 */
+#define FP8SQ_RECIPE_E4M3 1       /* everything in E4M3       */
+
+/*
+ * Delayed-scaling state of one tensor role ([TS] core vocabulary "Delayed
+ * Scaling"; [TE] fp8_meta amax_history and scale): a block of
+ * FP8SQ_STATE_FLOATS(H) fp32 values in device memory,
+ *     [0 .. H-1]  amax history, newest first (index 0 = the current step)
+ *     [H]         m, the multiplier applied before the cast (fmax / a)
+ *     [H + 1]     s, the dequantisation step (a / fmax)
+ * where a is the history's reduction.  Several states may be packed back to
+ * back (state i at offset i * FP8SQ_STATE_FLOATS(H)).
+ */
+#define FP8SQ_STATE_FLOATS(H) ((H) + 2)
+
+/* ---- 1. amax ------------------------------------------------------------
+ * [TS] core vocabulary: amax = the maximum absolute value of a tensor.
+ * Computes max|x| of every scaling unit of x[rows][cols] (x: bf16 or fp32).
+ *   gran TENSOR:       amax_out[0]
+ *   gran TILE_1x128:   amax_out[rows][cols/128]   (cols % 128 == 0)
+ *   gran BLOCK_128x128 amax_out[rows/128][cols/128] (rows, cols % 128 == 0)
+ *   gran MX32:         amax_out[rows][cols/32]    (cols % 32 == 0)
+ * A NaN in a unit gives a NaN amax.  x must be 16-byte aligned; for TENSOR
+ * any size is accepted (rows * cols == 0 gives 0).
+ */
+FP8SQ_API int fp8_amax(const void* x, int x_dtype, int64_t rows, int64_t cols, int gran,
+                       float* amax_out, void* stream);
+
+/* ---- 2. scale state -------------------------------------------------------
+ * fp8_scale_init: sets n_states packed states to history = 0, m = s = 1.
+ * fp8_update_scale: the end-of-step update of delayed scaling ([TS] core
+ * vocabulary; [TE] DelayedScaling).  For every state i: a = max over the
+ * history (algo MAX) or its newest entry (MOST_RECENT); if a is finite and
+ * > 0 then m = fmax/a and s = a/fmax (one fp32 division each, fmax from
+ * formats[i]), otherwise m and s are kept; then the history rolls by one
+ * (entry j takes entry j-1) and entry 0 becomes 0.
+ * formats: HOST array of n_states FP8SQ_E4M3 / FP8SQ_E5M2 (copied at call).
+ * n_states <= 1024, 1 <= history_len <= 4096.
+ */
+FP8SQ_API int fp8_scale_init(float* states, int n_states, int history_len, void* stream);
+FP8SQ_API int fp8_update_scale(float* states, int n_states, int history_len, const int* formats,
+                               int algo, void* stream);
+
+/* ---- 3. quantize ------------------------------------------------------------
+ * q = sat_RNE_fp8(fp32(x) * m) for every element, m taken from the element's
+ * scaling unit ([W14] absmax bullet; [TS] worked example: the multiplier
+ * 448/240 maps 120 to 224 and a spike of 300 clips at 448).
+ *
+ *   x         device, bf16 or fp32 [rows][cols], 16-byte aligned
+ *   format    FP8SQ_E4M3 / FP8SQ_E5M2 (satfinite: |x*m| >= fmax and +-inf
+ *             give +-fmax; NaN gives a NaN code; -0 and negative values that
+ *             round to zero give 0x80)
+ *   gran, delayed_state:
+ *     TENSOR + delayed_state != NULL: delayed scaling.  m = state[H]; the
+ *       tensor's amax is max-combined into state[0] (atomic, so several
+ *       tensors may share a role).  scales_out is ignored.
+ *     TENSOR + delayed_state == NULL: current scaling, two passes (amax,
+ *       then cast).  amax_out (1 float) and scales_out (1 float, receives
+ *       s = amax/fmax) are REQUIRED.  m = fmax/amax (amax 0 or non-finite:
+ *       m = s = 1).
+ *     TILE_1x128 / BLOCK_128x128: current scaling per unit, one pass;
+ *       scales_out f32 [rows][cols/128] / [rows/128][cols/128] receives s.
+ *     MX32: one pass; scales_out u8 [rows][cols/32] receives the E8M0 code
+ *       e + 127 of the smallest power of two 2^e with amax <= fmax * 2^e
+ *       (clamped to [-127, 127]; amax 0 -> 127; non-finite -> 0xFF with
+ *       m = 1); m = 2^-e.
+ *   q         device u8 [rows][cols], 16-byte aligned
+ *   qT        device u8 [cols][rows] (the transposed codes, same scale) or
+ *             NULL; TENSOR only, needs rows % 16 == 0 and cols % 16 == 0
+ *   amax_out  device f32 per unit (layout as fp8_amax) or NULL (see above)
+ *   sat_count device u64 or NULL: the number of elements with |x*m| > fmax
+ *             (they clip) is ADDED to it.
+ *   history_len  H of delayed_state (ignored when it is NULL)
+ */
+FP8SQ_API int fp8_quantize(const void* x, int x_dtype, int64_t rows, int64_t cols, int format,
+                           int gran, float* delayed_state, int history_len, uint8_t* q,
+                           uint8_t* qT, void* scales_out, float* amax_out,
+                           unsigned long long* sat_count, void* stream);
+
+/* ---- 4. GEMM ----------------------------------------------------------------
+ * D[m][n] = epi( sum_k Ahat[m][k] * Bhat[n][k] ) with Ahat = dec(qA) * sA,
+ * Bhat = dec(qB) * sB ([W14] FP8 bullet: matmuls run in FP8 with a wider
+ * accumulator; x ~ q * scale).  Accumulation is fp32 in tensor memory;
+ * epi multiplies by the scales, adds bias[n] if given, and rounds to the
+ * output type (bf16: round-to-nearest-even).
+ *   A  device u8 [M][K] (K contiguous), B device u8 [N][K] (K contiguous);
+ *      both 16-byte aligned.  a_format / b_format each E4M3 or E5M2
+ *      (E5M2 x E4M3 is the HYBRID dgrad / wgrad pairing).
+ *   (a_gran, b_gran) pairs:
+ *     (TENSOR, TENSOR): a_scale, b_scale = device f32[1] each (s).
+ *     (TILE_1x128, BLOCK_128x128): a_scale f32 [M][K/128], b_scale f32
+ *       [N/128][K/128]; partial sums over each 128-wide K block are promoted
+ *       to fp32 registers with sA * sB ([W14] accumulation bullet:
+ *       promotion to fp32 at fixed intervals); K % 128 == 0.
+ *     (MX32, MX32): a_scale u8 E8M0 [M][K/32], b_scale u8 [N][K/32]
+ *       (layout of fp8_quantize MX32); K % 128 == 0.
+ *   D  device [M][N], bf16 or f32, 16-byte aligned; bias device f32 [N] or NULL.
+ *   Shapes: M >= 0, N % 8 == 0, K % 16 == 0 (TENSOR) / % 128 (others).
+ *   K == 0 writes epi(0).
+ */
+FP8SQ_API int fp8_gemm(const uint8_t* A, int a_format, const void* a_scale, int a_gran,
+                       const uint8_t* B, int b_format, const void* b_scale, int b_gran,
+                       int64_t M, int64_t N, int64_t K, const float* bias, void* D, int d_dtype,
+                       void* stream);
+
+/* ---- 5. linear layer ---------------------------------------------------------
+ * [TE] te.Linear under fp8_autocast; [TS] Part 01 (HYBRID).
+ * Forward  y[M][N]  = x[M][K] W[N][K]^T      (x, W quantised in E4M3)
+ * Backward dx[M][K] = dy[M][N] W             (dy in E5M2 under HYBRID)
+ *          dW[N][K] = dy^T x                 (fp32 output, the master-weight
+ *                                              precision of [W14] FP8 bullet)
+ * x, w, dy: device bf16.  y: bf16 or f32.  dx: bf16.  dw: f32.
+ * gran TENSOR: delayed scaling when x_state / w_state / dy_state are given
+ *   (each a state block of history_len), current scaling when all are NULL.
+ *   The forward keeps the codes of x and W (and their transposes) in the
+ *   workspace; the backward reads them and adds dy's codes.
+ * gran TILE_1x128: x in 1x128 tiles, W in 128x128 blocks, current scaling,
+ *   forward only.   gran MX32: x and W in MX-32 blocks, forward only.
+ * workspace: device, >= fp8_linear_workspace_bytes(M, N, K, gran), 256-byte
+ *   aligned; the same workspace must be passed to the matching backward.
+ * Shapes: M, N, K % 128 == 0 (TENSOR: M % 16, N % 16, K % 16).
+ */
+FP8SQ_API size_t fp8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int gran);
+FP8SQ_API int fp8_linear_fwd(const void* x, const void* w, int64_t M, int64_t N, int64_t K,
+                             int gran, int recipe, float* x_state, float* w_state,
+                             int history_len, void* workspace, size_t ws_bytes,
+                             const float* bias, void* y, int y_dtype, void* stream);
+FP8SQ_API int fp8_linear_bwd(const void* dy, int64_t M, int64_t N, int64_t K, int recipe,
+                             float* dy_state, int history_len, void* workspace, size_t ws_bytes,
+                             void* dx, float* dw, void* stream);
+
+/* ---- 6. diagnostics --------------------------------------------------------
+ * fp8_device_status: synchronises the current device and returns
+ *   FP8SQ_ERR_TIMEOUT if any bounded device-side wait of this library ran out
+ *   since the last clear (the kernel that hit it wrote nothing further and
+ *   returned), FP8SQ_OK otherwise.  clear != 0 resets the word.  While the
+ *   word is set, GEMM kernels return early without computing.
+ * fp8_last_error: message for the calling thread's last non-zero status
+ *   (static thread-local storage; never NULL).
+ * fp8_abi_version: 1.
+ */
+FP8SQ_API int fp8_device_status(int clear);
+FP8SQ_API const char* fp8_last_error(void);
+FP8SQ_API int fp8_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FP8SQ_H */

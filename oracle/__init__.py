@@ -277,6 +277,40 @@ def epilogue(r: np.ndarray, out_bf16: bool) -> np.ndarray:
     return bf16_round_array_fast(f) if out_bf16 else f
 
 
+# ---------------------------------------------------------------- linear layer
+# y = x W^T with per-tensor delayed scaling under the HYBRID recipe
+# ("Transformer Scaling", Part 01: E4M3 for forward weights/activations, E5M2
+# for gradients; Transformer Engine tutorial: te.Linear under fp8_autocast).
+# Backward: dx = dy W (contraction over N), dW = dy^T x (contraction over M).
+# Per-tensor codes transpose exactly, so the transposed operands are the
+# transposes of the forward codes.
+def linear_fwd_delayed(x, w, x_state, w_state):
+    """-> (qx, sx, qw, sw, R) with R = xhat what^T in float64; the states'
+    history slot 0 records the amaxes (in place)."""
+    H = x_state.size - 2
+    sx, sw = np.float32(x_state[H + 1]), np.float32(w_state[H + 1])
+    qx, _ = quantize_delayed(x, E4M3, x_state)
+    qw, _ = quantize_delayed(w, E4M3, w_state)
+    r = gemm_ref(dequantize(qx, E4M3, GRAN_TENSOR, sx), dequantize(qw, E4M3, GRAN_TENSOR, sw))
+    return qx, sx, qw, sw, r
+
+
+def linear_bwd_delayed(dy, dy_state, dy_fmt, qx, sx, qw, sw, rows=None, wrows=None):
+    """-> (qdy, sdy, dX, dW) in float64.  rows / wrows: optional row subsets
+    of dX (over M) and dW (over N) to evaluate (sampled checks)."""
+    H = dy_state.size - 2
+    sdy = np.float32(dy_state[H + 1])
+    qdy, _ = quantize_delayed(dy, dy_fmt, dy_state)
+    dyh = dequantize(qdy, dy_fmt, GRAN_TENSOR, sdy)
+    xh = dequantize(qx, E4M3, GRAN_TENSOR, sx)
+    wh = dequantize(qw, E4M3, GRAN_TENSOR, sw)
+    a = dyh if rows is None else dyh[rows]
+    dX = gemm_ref(a, wh.T)
+    at = dyh.T if wrows is None else dyh.T[wrows]
+    dW = gemm_ref(at, xh.T)
+    return qdy, sdy, dX, dW
+
+
 # ---------------------------------------------------------------- worked-example helpers
 def int8_absmax(x):
     a = _f32(x)

@@ -114,12 +114,13 @@ float orc_f32_from_bf16(uint16_t h)
 float orc_amax(const float* x, int64_t n)
 {
     float m = 0.0f;
+    int any_nan = 0;
+    #pragma omp parallel for reduction(max:m) reduction(|:any_nan) schedule(static) if(n > 65536)
     for (int64_t i = 0; i < n; ++i) {
-        if (isnan(x[i])) return NAN;
-        float a = fabsf(x[i]);
-        if (a > m) m = a;
+        if (isnan(x[i])) any_nan = 1;
+        else if (fabsf(x[i]) > m) m = fabsf(x[i]);
     }
-    return m;
+    return any_nan ? NAN : m;
 }
 
 /* max of two amaxes with NaN propagation */
@@ -158,6 +159,7 @@ static int64_t quant_run(const float* x, int64_t n, int64_t stride, float m, int
 {
     float fmax = (float)orc_fmax(fmt);
     int64_t sat = 0;
+    #pragma omp parallel for reduction(+:sat) schedule(static) if(n > 65536)
     for (int64_t i = 0; i < n; ++i) {
         float p = x[i * stride] * m;
         if (fabsf(p) > fmax) ++sat;

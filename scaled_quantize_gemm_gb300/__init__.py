@@ -1,0 +1,165 @@
+"""Python binding of the sm_103a FP8 scaled-linear library (libfp8sq.so).
+
+Argument marshalling only: every function forwards torch tensors' device
+pointers and the current CUDA stream to the extern "C" entry point of the
+same name declared in ``include/fp8sq.h``; all of the path's arithmetic runs
+in the library's CUDA kernels.  There is no fallback: if the library has not
+been built (``__graft_entry__.build()``) the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+E4M3, E5M2 = 0, 1
+BF16, F32 = 0, 1
+TENSOR, TILE_1x128, BLOCK_128x128, MX32 = 0, 1, 2, 3
+AMAX_MAX, AMAX_MOST_RECENT = 0, 1
+RECIPE_HYBRID, RECIPE_E4M3 = 0, 1
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WRONG_ARCH, ERR_CUDA, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libfp8sq.so")
+HEADER = os.path.join(os.path.dirname(HERE), "include", "fp8sq.h")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class Fp8Error(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"[{code}] {msg}")
+        self.code = code
+
+
+def state_floats(history_len: int) -> int:
+    return history_len + 2
+
+
+def lib() -> ctypes.CDLL:
+    """Load libfp8sq.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                                   "(the FP8 path has no fallback)")
+            L = ctypes.CDLL(LIB_PATH)
+            c = ctypes
+            P, I, I64, Z = c.c_void_p, c.c_int, c.c_int64, c.c_size_t
+            sig = {
+                "fp8_abi_version": (I, []),
+                "fp8_last_error": (c.c_char_p, []),
+                "fp8_device_status": (I, [I]),
+                "fp8_amax": (I, [P, I, I64, I64, I, P, P]),
+                "fp8_scale_init": (I, [P, I, I, P]),
+                "fp8_update_scale": (I, [P, I, I, P, I, P]),
+                "fp8_quantize": (I, [P, I, I64, I64, I, I, P, I, P, P, P, P, P, P]),
+                "fp8_gemm": (I, [P, I, P, I, P, I, P, I, I64, I64, I64, P, P, I, P]),
+                "fp8_linear_workspace_bytes": (Z, [I64, I64, I64, I]),
+                "fp8_linear_fwd": (I, [P, P, I64, I64, I64, I, I, P, P, I, P, Z, P, P, I, P]),
+                "fp8_linear_bwd": (I, [P, I64, I64, I64, I, P, I, P, Z, P, P, P]),
+            }
+            for name, (res, args) in sig.items():
+                f = getattr(L, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = L
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(code: int):
+    if code != OK:
+        raise Fp8Error(code, lib().fp8_last_error().decode())
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+# ---------------------------------------------------------------- entry points
+def fp8_amax(x, gran: int, amax_out, stream=None) -> None:
+    R, C = (x.shape[0], x.shape[1]) if x.dim() == 2 else (1, x.numel())
+    _check(lib().fp8_amax(_ptr(x), _dtype_code(x), R, C, gran, _ptr(amax_out), _stream(stream)))
+
+
+def fp8_scale_init(states, n_states: int, history_len: int, stream=None) -> None:
+    _check(lib().fp8_scale_init(_ptr(states), n_states, history_len, _stream(stream)))
+
+
+def fp8_update_scale(states, n_states: int, history_len: int, formats, algo: int = AMAX_MAX,
+                     stream=None) -> None:
+    arr = (ctypes.c_int * max(1, n_states))(*formats)
+    _check(lib().fp8_update_scale(_ptr(states), n_states, history_len, arr, algo, _stream(stream)))
+
+
+def fp8_quantize(x, format: int, gran: int, q, qT=None, scales_out=None, amax_out=None,
+                 delayed_state=None, history_len: int = 0, sat_count=None, stream=None) -> None:
+    R, C = (x.shape[0], x.shape[1]) if x.dim() == 2 else (1, x.numel())
+    _check(lib().fp8_quantize(_ptr(x), _dtype_code(x), R, C, format, gran, _ptr(delayed_state), history_len,
+                              _ptr(q), _ptr(qT), _ptr(scales_out), _ptr(amax_out), _ptr(sat_count),
+                              _stream(stream)))
+
+
+def fp8_gemm(A, a_format: int, a_scale, a_gran: int, B, b_format: int, b_scale, b_gran: int,
+             D, bias=None, M: int = None, N: int = None, K: int = None, stream=None) -> None:
+    M = A.shape[0] if M is None else M
+    K = A.shape[1] if K is None else K
+    N = B.shape[0] if N is None else N
+    _check(lib().fp8_gemm(_ptr(A), a_format, _ptr(a_scale), a_gran, _ptr(B), b_format, _ptr(b_scale), b_gran,
+                          M, N, K, _ptr(bias), _ptr(D), _dtype_code(D), _stream(stream)))
+
+
+def fp8_linear_workspace_bytes(M: int, N: int, K: int, gran: int = TENSOR) -> int:
+    return int(lib().fp8_linear_workspace_bytes(M, N, K, gran))
+
+
+def fp8_linear_fwd(x, w, y, workspace, gran: int = TENSOR, recipe: int = RECIPE_HYBRID,
+                   x_state=None, w_state=None, history_len: int = 0, bias=None, stream=None) -> None:
+    M, K = x.shape
+    N = w.shape[0]
+    _check(lib().fp8_linear_fwd(_ptr(x), _ptr(w), M, N, K, gran, recipe, _ptr(x_state), _ptr(w_state),
+                                history_len, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                _ptr(bias), _ptr(y), _dtype_code(y), _stream(stream)))
+
+
+def fp8_linear_bwd(dy, dx, dw, workspace, K: int, recipe: int = RECIPE_HYBRID, dy_state=None,
+                   history_len: int = 0, stream=None) -> None:
+    M, N = dy.shape
+    _check(lib().fp8_linear_bwd(_ptr(dy), M, N, K, recipe, _ptr(dy_state), history_len, _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _ptr(dx), _ptr(dw),
+                                _stream(stream)))
+
+
+def fp8_device_status(clear: bool = True) -> int:
+    return lib().fp8_device_status(1 if clear else 0)
+
+
+def declared_symbols() -> list:
+    """Names of the entry points declared FP8SQ_API in include/fp8sq.h."""
+    import re
+    txt = open(HEADER).read()
+    return re.findall(r"FP8SQ_API\s+[\w\s\*]+?\b(fp8_\w+)\s*\(", txt)

@@ -1,0 +1,453 @@
+// api.cu -- the extern "C" boundary declared in include/fp8sq.h.
+// Validates every argument on the host before anything is enqueued, checks
+// that the current device is sm_103, then hands off to the launchers.
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cuda_runtime.h>
+
+#include "../../include/fp8sq.h"
+#include "internal.h"
+
+namespace {
+
+thread_local char g_msg[512] = "no error";
+
+int fail(int code, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+struct DevInfo {
+    int checked = 0, ok = 0, sms = 0, major = 0, minor = 0;
+};
+DevInfo g_dev[64];
+
+// current device must be sm_103; returns its SM count through *sms
+int check_device(int* sms)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return fail(FP8SQ_ERR_CUDA, "no usable CUDA device (%s)", cudaGetErrorString(e));
+    }
+    DevInfo& d = g_dev[dev];
+    if (!d.checked) {
+        if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(FP8SQ_ERR_CUDA, "cannot query device %d", dev);
+        }
+        d.ok = (d.major == 10 && d.minor == 3);
+        d.checked = 1;
+    }
+    if (!d.ok) return fail(FP8SQ_ERR_WRONG_ARCH, "device %d is sm_%d%d; this library is built for sm_103a only", dev, d.major, d.minor);
+    *sms = d.sms;
+    return FP8SQ_OK;
+}
+
+int cuda_status(cudaError_t e, const char* what)
+{
+    if (e == cudaSuccess) return FP8SQ_OK;
+    cudaGetLastError();
+    return fail(FP8SQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool valid_format(int f) { return f == FP8SQ_E4M3 || f == FP8SQ_E5M2; }
+bool valid_dtype(int d) { return d == FP8SQ_BF16 || d == FP8SQ_F32; }
+bool valid_gran(int g) { return g >= FP8SQ_TENSOR && g <= FP8SQ_MX32; }
+
+const int64_t kMaxDim = (int64_t)1 << 31;  // GEMM / TMA coordinates are 32-bit
+
+// per-unit layout checks shared by amax and quantize
+int check_units(int gran, int64_t rows, int64_t cols)
+{
+    if (gran == FP8SQ_TILE_1x128 && cols % 128)
+        return fail(FP8SQ_ERR_UNSUPPORTED, "1x128 tiles need cols %% 128 == 0 (cols = %lld)", (long long)cols);
+    if (gran == FP8SQ_BLOCK_128x128 && (rows % 128 || cols % 128))
+        return fail(FP8SQ_ERR_UNSUPPORTED, "128x128 blocks need rows, cols %% 128 == 0 (%lld x %lld)", (long long)rows, (long long)cols);
+    if (gran == FP8SQ_MX32 && cols % 32)
+        return fail(FP8SQ_ERR_UNSUPPORTED, "MX-32 blocks need cols %% 32 == 0 (cols = %lld)", (long long)cols);
+    return FP8SQ_OK;
+}
+
+// workspace layout of the linear layer (offsets in bytes, 256-byte aligned)
+struct WsLayout {
+    size_t qx = 0, qxT = 0, qw = 0, qwT = 0, qdy = 0, qdyT = 0, sx = 0, sw = 0, scal = 0, total = 0;
+};
+size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
+WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int gran)
+{
+    WsLayout L;
+    size_t off = 0;
+    auto take = [&](size_t bytes) { size_t o = off; off += al256(bytes); return o; };
+    L.qx = take((size_t)(M * K));
+    L.qw = take((size_t)(N * K));
+    if (gran == FP8SQ_TENSOR) {
+        L.qxT = take((size_t)(M * K));
+        L.qwT = take((size_t)(N * K));
+        L.qdy = take((size_t)(M * N));
+        L.qdyT = take((size_t)(M * N));
+        L.scal = take(8 * sizeof(float));   // sx, sw, sdy, ax, aw, ady
+    } else if (gran == FP8SQ_TILE_1x128) {
+        L.sx = take((size_t)(M * (K / 128)) * sizeof(float));
+        L.sw = take((size_t)((N / 128) * (K / 128)) * sizeof(float));
+    } else {
+        L.sx = take((size_t)(M * (K / 32)));
+        L.sw = take((size_t)(N * (K / 32)));
+    }
+    L.total = off;
+    return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+FP8SQ_API int fp8_abi_version(void) { return 1; }
+
+FP8SQ_API const char* fp8_last_error(void) { return g_msg; }
+
+FP8SQ_API int fp8_device_status(int clear)
+{
+    int v = fp8sq::read_device_error(clear);
+    if (v < 0) return fail(FP8SQ_ERR_CUDA, "cannot read the device error word");
+    if (v) return fail(FP8SQ_ERR_TIMEOUT, "a bounded device-side wait ran out");
+    return FP8SQ_OK;
+}
+
+FP8SQ_API int fp8_amax(const void* x, int x_dtype, int64_t rows, int64_t cols, int gran, float* amax_out,
+                       void* stream)
+{
+    if (!x || !amax_out) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_amax: null pointer");
+    if (!valid_dtype(x_dtype) || !valid_gran(gran)) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_amax: bad dtype or granularity");
+    if (rows < 0 || cols < 0) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_amax: negative size");
+    if (!aligned16(x)) return fail(FP8SQ_ERR_MISALIGNED, "fp8_amax: x must be 16-byte aligned");
+    if (!aligned4(amax_out)) return fail(FP8SQ_ERR_MISALIGNED, "fp8_amax: amax_out must be 4-byte aligned");
+    int r = check_units(gran, rows, cols);
+    if (r) return r;
+    int sms;
+    if ((r = check_device(&sms))) return r;
+    fp8sq::QuantArgs a;
+    a.x = x;
+    a.x_dtype = x_dtype;
+    a.rows = rows;
+    a.cols = cols;
+    a.gran = gran;
+    a.amax = amax_out;
+    return cuda_status(fp8sq::launch_amax(a, static_cast<cudaStream_t>(stream), sms), "fp8_amax launch");
+}
+
+FP8SQ_API int fp8_scale_init(float* states, int n_states, int history_len, void* stream)
+{
+    if (!states) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_scale_init: null states");
+    if (n_states < 0 || history_len < 1 || history_len > 4096)
+        return fail(FP8SQ_ERR_INVALID_ARG, "fp8_scale_init: bad n_states / history_len");
+    if (!aligned4(states)) return fail(FP8SQ_ERR_MISALIGNED, "fp8_scale_init: states must be 4-byte aligned");
+    int sms, r;
+    if ((r = check_device(&sms))) return r;
+    return cuda_status(fp8sq::launch_scale_init(states, n_states, history_len, static_cast<cudaStream_t>(stream)),
+                       "fp8_scale_init launch");
+}
+
+FP8SQ_API int fp8_update_scale(float* states, int n_states, int history_len, const int* formats, int algo,
+                               void* stream)
+{
+    if (!states || !formats) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_update_scale: null pointer");
+    if (n_states < 0 || n_states > 1024 || history_len < 1 || history_len > 4096)
+        return fail(FP8SQ_ERR_INVALID_ARG, "fp8_update_scale: bad n_states / history_len");
+    if (algo != FP8SQ_AMAX_MAX && algo != FP8SQ_AMAX_MOST_RECENT)
+        return fail(FP8SQ_ERR_INVALID_ARG, "fp8_update_scale: bad algo");
+    for (int i = 0; i < n_states; ++i)
+        if (!valid_format(formats[i])) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_update_scale: bad format of state %d", i);
+    if (!aligned4(states)) return fail(FP8SQ_ERR_MISALIGNED, "fp8_update_scale: states must be 4-byte aligned");
+    int sms, r;
+    if ((r = check_device(&sms))) return r;
+    return cuda_status(
+        fp8sq::launch_update_scale(states, n_states, history_len, formats, algo, static_cast<cudaStream_t>(stream)),
+        "fp8_update_scale launch");
+}
+
+static int validate_quantize(const void* x, int x_dtype, int64_t rows, int64_t cols, int format, int gran,
+                             const float* state, int H, const uint8_t* q, const uint8_t* qT, const void* scales,
+                             const float* amax_out)
+{
+    if (!x || !q) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize: null x or q");
+    if (!valid_dtype(x_dtype) || !valid_format(format) || !valid_gran(gran))
+        return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize: bad dtype, format or granularity");
+    if (rows < 0 || cols < 0) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize: negative size");
+    if (rows >= kMaxDim || cols >= kMaxDim) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_quantize: dimension too large");
+    if (!aligned16(x) || !aligned16(q) || (qT && !aligned16(qT)))
+        return fail(FP8SQ_ERR_MISALIGNED, "fp8_quantize: x, q, qT must be 16-byte aligned");
+    if ((scales && !aligned4(scales)) || (amax_out && !aligned4(amax_out)) || (state && !aligned4(state)))
+        return fail(FP8SQ_ERR_MISALIGNED, "fp8_quantize: scale / amax / state buffers must be 4-byte aligned");
+    int r = check_units(gran, rows, cols);
+    if (r) return r;
+    if (gran == FP8SQ_TENSOR) {
+        if (state && (H < 1 || H > 4096)) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize: bad history_len");
+        if (!state && (!amax_out || !scales))
+            return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize: current per-tensor scaling needs amax_out and scales_out");
+        if (qT && (rows % 16 || cols % 16))
+            return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_quantize: a transposed copy needs rows, cols %% 16 == 0");
+    } else {
+        if (state) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_quantize: delayed scaling is per tensor only");
+        if (qT) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_quantize: a transposed copy is per tensor only");
+        if (!scales) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize: scales_out is required for this granularity");
+    }
+    return FP8SQ_OK;
+}
+
+FP8SQ_API int fp8_quantize(const void* x, int x_dtype, int64_t rows, int64_t cols, int format, int gran,
+                           float* delayed_state, int history_len, uint8_t* q, uint8_t* qT, void* scales_out,
+                           float* amax_out, unsigned long long* sat_count, void* stream)
+{
+    int r = validate_quantize(x, x_dtype, rows, cols, format, gran, delayed_state, history_len, q, qT, scales_out,
+                              amax_out);
+    if (r) return r;
+    if (sat_count && (reinterpret_cast<uintptr_t>(sat_count) & 7u))
+        return fail(FP8SQ_ERR_MISALIGNED, "fp8_quantize: sat_count must be 8-byte aligned");
+    int sms;
+    if ((r = check_device(&sms))) return r;
+    fp8sq::QuantArgs a;
+    a.x = x;
+    a.x_dtype = x_dtype;
+    a.rows = rows;
+    a.cols = cols;
+    a.format = format;
+    a.gran = gran;
+    a.state = delayed_state;
+    a.history_len = history_len;
+    a.q = q;
+    a.qT = qT;
+    a.scales = scales_out;
+    a.amax = amax_out;
+    a.sat = sat_count;
+    return cuda_status(fp8sq::launch_quantize(a, static_cast<cudaStream_t>(stream), sms), "fp8_quantize launch");
+}
+
+static int validate_gemm(const uint8_t* A, int a_format, const void* a_scale, int a_gran, const uint8_t* B,
+                         int b_format, const void* b_scale, int b_gran, int64_t M, int64_t N, int64_t K,
+                         const float* bias, const void* D, int d_dtype, int* mode)
+{
+    if (!A || !B || !D || !a_scale || !b_scale) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_gemm: null pointer");
+    if (!valid_format(a_format) || !valid_format(b_format) || !valid_dtype(d_dtype))
+        return fail(FP8SQ_ERR_INVALID_ARG, "fp8_gemm: bad format or output dtype");
+    if (M < 0 || N < 0 || K < 0) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_gemm: negative size");
+    if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_gemm: dimension too large");
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D))
+        return fail(FP8SQ_ERR_MISALIGNED, "fp8_gemm: A, B, D must be 16-byte aligned");
+    if (!aligned4(a_scale) || !aligned4(b_scale) || (bias && !aligned4(bias)))
+        return fail(FP8SQ_ERR_MISALIGNED, "fp8_gemm: scales / bias must be 4-byte aligned");
+    if (N % 8) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_gemm: N %% 8 != 0");
+    if (a_gran == FP8SQ_TENSOR && b_gran == FP8SQ_TENSOR) {
+        if (K % 16) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_gemm: K %% 16 != 0");
+        *mode = 0;
+    } else if (a_gran == FP8SQ_TILE_1x128 && b_gran == FP8SQ_BLOCK_128x128) {
+        if (K % 128) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_gemm: 1x128 x 128x128 scaling needs K %% 128 == 0");
+        *mode = 1;
+    } else if (a_gran == FP8SQ_MX32 && b_gran == FP8SQ_MX32) {
+        if (K % 128) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_gemm: MX scaling needs K %% 128 == 0");
+        *mode = 2;
+    } else {
+        return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_gemm: unsupported scale granularity pair (%d, %d)", a_gran, b_gran);
+    }
+    return FP8SQ_OK;
+}
+
+FP8SQ_API int fp8_gemm(const uint8_t* A, int a_format, const void* a_scale, int a_gran, const uint8_t* B,
+                       int b_format, const void* b_scale, int b_gran, int64_t M, int64_t N, int64_t K,
+                       const float* bias, void* D, int d_dtype, void* stream)
+{
+    int mode = 0;
+    int r = validate_gemm(A, a_format, a_scale, a_gran, B, b_format, b_scale, b_gran, M, N, K, bias, D, d_dtype, &mode);
+    if (r) return r;
+    int sms;
+    if ((r = check_device(&sms))) return r;
+    fp8sq::GemmArgs g;
+    g.A = A;
+    g.B = B;
+    g.a_format = a_format;
+    g.b_format = b_format;
+    g.mode = mode;
+    g.a_scale = a_scale;
+    g.b_scale = b_scale;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.bias = bias;
+    g.D = D;
+    g.d_dtype = d_dtype;
+    const char* why = nullptr;
+    cudaError_t e = fp8sq::launch_gemm(g, static_cast<cudaStream_t>(stream), sms, &why);
+    if (e == cudaErrorNotSupported) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_gemm: %s", why ? why : "not supported");
+    if (e != cudaSuccess && why) {
+        cudaGetLastError();
+        return fail(FP8SQ_ERR_CUDA, "fp8_gemm: %s", why);
+    }
+    return cuda_status(e, "fp8_gemm launch");
+}
+
+FP8SQ_API size_t fp8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int gran)
+{
+    if (M < 0 || N < 0 || K < 0 || !(gran == FP8SQ_TENSOR || gran == FP8SQ_TILE_1x128 || gran == FP8SQ_MX32)) return 0;
+    return ws_layout(M, N, K, gran).total;
+}
+
+static int check_linear_shape(int64_t M, int64_t N, int64_t K, int gran, const void* ws, size_t ws_bytes)
+{
+    if (M < 0 || N < 0 || K < 0) return fail(FP8SQ_ERR_INVALID_ARG, "linear: negative size");
+    if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) return fail(FP8SQ_ERR_UNSUPPORTED, "linear: dimension too large");
+    if (gran == FP8SQ_TENSOR) {
+        if (M % 16 || N % 16 || K % 16) return fail(FP8SQ_ERR_UNSUPPORTED, "linear: per-tensor needs M, N, K %% 16 == 0");
+    } else if (gran == FP8SQ_TILE_1x128 || gran == FP8SQ_MX32) {
+        if (M % 128 || N % 128 || K % 128) return fail(FP8SQ_ERR_UNSUPPORTED, "linear: block scaling needs M, N, K %% 128 == 0");
+    } else {
+        return fail(FP8SQ_ERR_INVALID_ARG, "linear: granularity must be TENSOR, TILE_1x128 or MX32");
+    }
+    if (!ws) return fail(FP8SQ_ERR_INVALID_ARG, "linear: null workspace");
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(FP8SQ_ERR_MISALIGNED, "linear: workspace must be 256-byte aligned");
+    if (ws_bytes < ws_layout(M, N, K, gran).total) return fail(FP8SQ_ERR_INVALID_ARG, "linear: workspace too small");
+    return FP8SQ_OK;
+}
+
+FP8SQ_API int fp8_linear_fwd(const void* x, const void* w, int64_t M, int64_t N, int64_t K, int gran, int recipe,
+                             float* x_state, float* w_state, int history_len, void* workspace, size_t ws_bytes,
+                             const float* bias, void* y, int y_dtype, void* stream)
+{
+    if (!x || !w || !y) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_linear_fwd: null pointer");
+    if (recipe != FP8SQ_RECIPE_HYBRID && recipe != FP8SQ_RECIPE_E4M3) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_linear_fwd: bad recipe");
+    if (!valid_dtype(y_dtype)) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_linear_fwd: bad y dtype");
+    int r = check_linear_shape(M, N, K, gran, workspace, ws_bytes);
+    if (r) return r;
+    const bool delayed = x_state || w_state;
+    if (delayed && (!x_state || !w_state)) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_linear_fwd: give both x_state and w_state, or neither");
+    if (delayed && gran != FP8SQ_TENSOR) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_linear_fwd: delayed scaling is per tensor only");
+    if (delayed && (history_len < 1 || history_len > 4096)) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_linear_fwd: bad history_len");
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return fail(FP8SQ_ERR_MISALIGNED, "fp8_linear_fwd: x, w, y must be 16-byte aligned");
+    if ((bias && !aligned4(bias)) || (x_state && !aligned4(x_state)) || (w_state && !aligned4(w_state)))
+        return fail(FP8SQ_ERR_MISALIGNED, "fp8_linear_fwd: bias / states must be 4-byte aligned");
+    int sms;
+    if ((r = check_device(&sms))) return r;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const WsLayout L = ws_layout(M, N, K, gran);
+    const int H = history_len;
+
+    fp8sq::QuantArgs qa;
+    qa.x_dtype = fp8sq::kBF16;
+    qa.format = fp8sq::kE4M3;
+    fp8sq::GemmArgs g;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.bias = bias;
+    g.D = y;
+    g.d_dtype = y_dtype;
+    g.A = ws + L.qx;
+    g.B = ws + L.qw;
+    if (gran == FP8SQ_TENSOR) {
+        float* scal = reinterpret_cast<float*>(ws + L.scal);   // sx, sw, sdy, ax, aw, ady
+        // x
+        qa.x = x; qa.rows = M; qa.cols = K; qa.gran = fp8sq::kTensor;
+        qa.q = ws + L.qx; qa.qT = ws + L.qxT;
+        qa.state = x_state; qa.history_len = H;
+        qa.scales = &scal[0]; qa.amax = delayed ? nullptr : &scal[3];
+        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: quantize x"))) return r;
+        // W
+        qa.x = w; qa.rows = N; qa.cols = K;
+        qa.q = ws + L.qw; qa.qT = ws + L.qwT;
+        qa.state = w_state;
+        qa.scales = &scal[1]; qa.amax = delayed ? nullptr : &scal[4];
+        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: quantize w"))) return r;
+        if (delayed) {
+            // keep the dequantisation steps used now for the backward pass
+            if ((r = cuda_status(cudaMemcpyAsync(&scal[0], x_state + H + 1, sizeof(float), cudaMemcpyDeviceToDevice, st), "fp8_linear_fwd: copy s_x"))) return r;
+            if ((r = cuda_status(cudaMemcpyAsync(&scal[1], w_state + H + 1, sizeof(float), cudaMemcpyDeviceToDevice, st), "fp8_linear_fwd: copy s_w"))) return r;
+        }
+        g.mode = 0;
+        g.a_scale = &scal[0];
+        g.b_scale = &scal[1];
+        g.a_format = g.b_format = fp8sq::kE4M3;
+    } else if (gran == FP8SQ_TILE_1x128) {
+        qa.x = x; qa.rows = M; qa.cols = K; qa.gran = fp8sq::kTile;
+        qa.q = ws + L.qx; qa.scales = ws + L.sx;
+        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: quantize x"))) return r;
+        qa.x = w; qa.rows = N; qa.cols = K; qa.gran = fp8sq::kBlock;
+        qa.q = ws + L.qw; qa.scales = ws + L.sw;
+        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: quantize w"))) return r;
+        g.mode = 1;
+        g.a_scale = ws + L.sx;
+        g.b_scale = ws + L.sw;
+    } else {
+        qa.x = x; qa.rows = M; qa.cols = K; qa.gran = fp8sq::kMX;
+        qa.q = ws + L.qx; qa.scales = ws + L.sx;
+        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: quantize x"))) return r;
+        qa.x = w; qa.rows = N; qa.cols = K;
+        qa.q = ws + L.qw; qa.scales = ws + L.sw;
+        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: quantize w"))) return r;
+        g.mode = 2;
+        g.a_scale = ws + L.sx;
+        g.b_scale = ws + L.sw;
+    }
+    const char* why = nullptr;
+    cudaError_t e = fp8sq::launch_gemm(g, st, sms, &why);
+    if (e == cudaErrorNotSupported) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_linear_fwd: %s", why ? why : "GEMM not supported");
+    return cuda_status(e, why ? why : "fp8_linear_fwd: GEMM launch");
+}
+
+FP8SQ_API int fp8_linear_bwd(const void* dy, int64_t M, int64_t N, int64_t K, int recipe, float* dy_state,
+                             int history_len, void* workspace, size_t ws_bytes, void* dx, float* dw, void* stream)
+{
+    if (!dy || !dx || !dw) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_linear_bwd: null pointer");
+    if (recipe != FP8SQ_RECIPE_HYBRID && recipe != FP8SQ_RECIPE_E4M3) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_linear_bwd: bad recipe");
+    int r = check_linear_shape(M, N, K, FP8SQ_TENSOR, workspace, ws_bytes);
+    if (r) return r;
+    if (dy_state && (history_len < 1 || history_len > 4096)) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_linear_bwd: bad history_len");
+    if (!aligned16(dy) || !aligned16(dx) || !aligned16(dw)) return fail(FP8SQ_ERR_MISALIGNED, "fp8_linear_bwd: dy, dx, dw must be 16-byte aligned");
+    if (dy_state && !aligned4(dy_state)) return fail(FP8SQ_ERR_MISALIGNED, "fp8_linear_bwd: dy_state must be 4-byte aligned");
+    int sms;
+    if ((r = check_device(&sms))) return r;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const WsLayout L = ws_layout(M, N, K, FP8SQ_TENSOR);
+    float* scal = reinterpret_cast<float*>(ws + L.scal);
+    const int fdy = recipe == FP8SQ_RECIPE_HYBRID ? fp8sq::kE5M2 : fp8sq::kE4M3;
+
+    fp8sq::QuantArgs qa;
+    qa.x = dy; qa.x_dtype = fp8sq::kBF16; qa.rows = M; qa.cols = N;
+    qa.format = fdy; qa.gran = fp8sq::kTensor;
+    qa.q = ws + L.qdy; qa.qT = ws + L.qdyT;
+    qa.state = dy_state; qa.history_len = history_len;
+    qa.scales = &scal[2]; qa.amax = dy_state ? nullptr : &scal[5];
+    if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_bwd: quantize dy"))) return r;
+    if (dy_state &&
+        (r = cuda_status(cudaMemcpyAsync(&scal[2], dy_state + history_len + 1, sizeof(float), cudaMemcpyDeviceToDevice, st), "fp8_linear_bwd: copy s_dy")))
+        return r;
+
+    const char* why = nullptr;
+    // dgrad: dx[M][K] = dy[M][N] * W[N][K]   (A = dy codes, B = W^T codes [K][N])
+    fp8sq::GemmArgs g;
+    g.mode = 0;
+    g.A = ws + L.qdy; g.a_format = fdy; g.a_scale = &scal[2];
+    g.B = ws + L.qwT; g.b_format = fp8sq::kE4M3; g.b_scale = &scal[1];
+    g.M = M; g.N = K; g.K = N;
+    g.D = dx; g.d_dtype = fp8sq::kBF16;
+    if ((r = cuda_status(fp8sq::launch_gemm(g, st, sms, &why), why ? why : "fp8_linear_bwd: dgrad"))) return r;
+    // wgrad: dw[N][K] = dy^T[N][M] * x[M][K]   (A = dy^T codes [N][M], B = x^T codes [K][M])
+    g.A = ws + L.qdyT; g.a_format = fdy; g.a_scale = &scal[2];
+    g.B = ws + L.qxT; g.b_format = fp8sq::kE4M3; g.b_scale = &scal[0];
+    g.M = N; g.N = K; g.K = M;
+    g.D = dw; g.d_dtype = fp8sq::kF32;
+    return cuda_status(fp8sq::launch_gemm(g, st, sms, &why), why ? why : "fp8_linear_bwd: wgrad");
+}
+
+}  // extern "C"

@@ -1,0 +1,587 @@
+// gemm.cu -- FP8 GEMM on the sm_103a 5th-generation tensor cores.
+//
+// D[m][n] = epi(sum_k dec(A[m][k]) sA * dec(B[n][k]) sB): the "matmuls run in
+// FP8" with a wider accumulator of the week-14 page (FP8 bullet,
+// accumulation-precision bullet); x ~ q * scale from its absmax bullet.
+//
+// One persistent CTA per SM, warp-specialised:
+//   warp 0     TMA producer: 128x128 A and BNx128 B tiles (K-major, 128-byte
+//              swizzle) into a STAGES-deep shared-memory ring
+//   warp 1     allocates tensor memory; one thread issues tcgen05.mma
+//              (kind::f8f6f4, M=128, N=BN, K=32 per instruction) and
+//              tcgen05.commit to release ring slots / publish accumulators
+//   warps 2..  epilogue: tcgen05.ld the fp32 accumulator, multiply by the
+//              dequantisation scales, round, store
+// Mode 0 (per-tensor scales): two TMEM accumulators of BN columns, so the
+// epilogue of tile i overlaps the MMAs of tile i+1.
+// Mode 1 (1x128 activation tiles x 128x128 weight blocks): the MMAs of each
+// 128-wide K block write a fresh partial into one of four TMEM buffers and
+// the epilogue warps promote it into fp32 registers with sA[m][kb] *
+// sB[nb][kb] (the fixed-interval fp32 promotion of the week-14 page,
+// interval = the 128-wide scale block).
+// Every mbarrier wait is bounded (1 s): on expiry the kernel sets a device
+// error word, stops issuing work, drains what it issued and frees its
+// tensor memory before returning.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8sq {
+
+__device__ int g_dev_error = 0;
+
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per wait
+constexpr uint64_t kDrainLimitNs = 100000000ull;   // 100 ms per drain wait
+
+// Wait for phase `parity` of `bar`; false if the wait ran out or another
+// wait of this library already failed (the error word is set).
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity)
+{
+    const uint32_t a = smem_addr(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(a, parity)) return true;
+        if ((it & 255u) == 0u) {
+            if (*reinterpret_cast<volatile int*>(&g_dev_error)) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                atomicExch(&g_dev_error, 1);
+                return false;
+            }
+        }
+    }
+}
+// Drain wait used on the abort path: ignores the error word, short limit.
+__device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity)
+{
+    const uint32_t a = smem_addr(bar);
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(a, parity))
+        if (global_timer_ns() - t0 > kDrainLimitNs) return;
+}
+
+struct TileSched {
+    int num_m, num_n, group;
+    __device__ __forceinline__ void coords(int t, int& mb, int& nb) const
+    {
+        const int per_group = group * num_n;
+        const int g = t / per_group;
+        const int first = g * group;
+        const int gs = min(num_m - first, group);
+        const int r = t - g * per_group;
+        mb = first + r % gs;
+        nb = r / gs;
+    }
+};
+
+struct EpiParams {
+    int M, N, K;
+    const float* sA;     // mode 0: 1 float; mode 1: [M][K/128]
+    const float* sB;     // mode 0: 1 float; mode 1: [N/128][K/128]
+    const float* bias;   // [N] or null
+    void* D;
+};
+
+constexpr int BM = 128;
+constexpr int BK = 128;  // bytes = elements for 8-bit operands
+constexpr int A_BYTES = BM * BK;
+
+// ------------------------------------------------------------------ epilogue store
+// 32 consecutive columns of one row: v[j] is column col0 + j.
+template <bool OUT_BF16>
+__device__ __forceinline__ void store_row32(const EpiParams& p, int row, int col0, const float (&v)[32])
+{
+    if (row >= p.M) return;
+    if (OUT_BF16) {
+        __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p.D) + (int64_t)row * p.N + col0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            if (col0 + 8 * c + 8 <= p.N) {
+                uint4 w;
+                __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * c + 0], v[8 * c + 1]);
+                __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * c + 2], v[8 * c + 3]);
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * c + 4], v[8 * c + 5]);
+                __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * c + 6], v[8 * c + 7]);
+                w.x = *reinterpret_cast<uint32_t*>(&h0);
+                w.y = *reinterpret_cast<uint32_t*>(&h1);
+                w.z = *reinterpret_cast<uint32_t*>(&h2);
+                w.w = *reinterpret_cast<uint32_t*>(&h3);
+                *reinterpret_cast<uint4*>(d + 8 * c) = w;
+            }
+        }
+    } else {
+        float* d = static_cast<float*>(p.D) + (int64_t)row * p.N + col0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            if (col0 + 8 * c + 8 <= p.N) {
+                *reinterpret_cast<float4*>(d + 8 * c) = make_float4(v[8 * c], v[8 * c + 1], v[8 * c + 2], v[8 * c + 3]);
+                *reinterpret_cast<float4*>(d + 8 * c + 4) =
+                    make_float4(v[8 * c + 4], v[8 * c + 5], v[8 * c + 6], v[8 * c + 7]);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ shared layout
+template <int BN, int STAGES, int NACC>
+struct Smem {
+    static constexpr int B_BYTES = BN * BK;
+    static constexpr int STAGE = A_BYTES + B_BYTES;
+    static constexpr int BAR_OFF = STAGES * STAGE;
+    static constexpr int NBARS = 2 * STAGES + 2 * NACC + 1;
+    static constexpr int BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;  // + holder + alignment slack
+};
+
+// Common prologue: barriers, tensor memory, early exit if the error word is set.
+template <int STAGES, int NACC, int EPI_WARPS>
+__device__ __forceinline__ bool gemm_setup(uint8_t* smem, int bar_off, uint32_t tmem_cols,
+                                           const CUtensorMap* tmA, const CUtensorMap* tmB, uint32_t& tmem_base)
+{
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + bar_off);
+    uint32_t* holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 2 * NACC + 1);
+    __shared__ int s_skip;
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        s_skip = *reinterpret_cast<volatile int*>(&g_dev_error);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&bars[s], 1);            // full
+            mbar_init(&bars[STAGES + s], 1);   // empty
+        }
+        for (int b = 0; b < NACC; ++b) {
+            mbar_init(&bars[2 * STAGES + b], 1);                 // accumulator full
+            mbar_init(&bars[2 * STAGES + NACC + b], EPI_WARPS);  // accumulator empty
+        }
+        mbar_init(&bars[2 * STAGES + 2 * NACC], 1);              // drain
+        fence_mbar_init();
+        prefetch_tmap(tmA);
+        prefetch_tmap(tmB);
+    }
+    __syncthreads();
+    if (s_skip) return false;
+    if (warp == 1) {
+        tmem_alloc(holder, tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    tmem_base = *holder;
+    return true;
+}
+
+// ------------------------------------------------------------------ producer
+template <int BN, int STAGES>
+__device__ __forceinline__ void producer_loop(uint8_t* smem, uint64_t* full, uint64_t* empty,
+                                              const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                              const TileSched& sched, int num_tiles, int nkb)
+{
+    constexpr int STAGE = A_BYTES + BN * BK;
+    int stage = 0;
+    uint32_t phase = 0;
+    int issued = 0;
+    bool aborted = false;
+    for (int t = blockIdx.x; t < num_tiles && !aborted; t += gridDim.x) {
+        int mb, nb;
+        sched.coords(t, mb, nb);
+        for (int kb = 0; kb < nkb; ++kb) {
+            if (!wait_bounded(&empty[stage], phase ^ 1u)) {
+                aborted = true;
+                break;
+            }
+            uint8_t* sa = smem + stage * STAGE;
+            mbar_arrive_expect_tx(&full[stage], STAGE);
+            tma_load_2d(sa, tmA, kb * BK, mb * BM, &full[stage]);
+            tma_load_2d(sa + A_BYTES, tmB, kb * BK, nb * BN, &full[stage]);
+            ++issued;
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    if (aborted) {
+        // wait for the copies still in flight before the CTA can exit
+        int n = issued < STAGES ? issued : STAGES;
+        int s = stage;
+        uint32_t ph = phase;
+        for (int i = 0; i < n; ++i) {
+            if (--s < 0) {
+                s = STAGES - 1;
+                ph ^= 1u;
+            }
+            wait_drain(&full[s], ph);
+        }
+    }
+}
+
+// ================================================================== mode 0
+// per-tensor scales; epilogue warps 2..5
+template <int BN, int STAGES, bool OUT_BF16>
+__global__ void __launch_bounds__(192, 1)
+    k_gemm_tensor(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  EpiParams p, uint32_t idesc, TileSched sched)
+{
+    using L = Smem<BN, STAGES, 2>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+    uint64_t* empty = full + STAGES;
+    uint64_t* afull = empty + STAGES;
+    uint64_t* aempty = afull + 2;
+    uint64_t* drain = aempty + 2;
+    constexpr uint32_t TMEM_COLS = 2 * BN;
+
+    uint32_t tmem_base;
+    if (!gemm_setup<STAGES, 2, 4>(smem, L::BAR_OFF, TMEM_COLS, &tmA, &tmB, tmem_base)) return;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int num_tiles = sched.num_m * sched.num_n;
+    const int nkb = (p.K + BK - 1) / BK;
+
+    if (warp == 0) {
+        if (lane == 0) producer_loop<BN, STAGES>(smem, full, empty, &tmA, &tmB, sched, num_tiles, nkb);
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0, lt = 0;
+            uint32_t phase = 0;
+            bool aborted = false;
+            for (int t = blockIdx.x; t < num_tiles && !aborted; t += gridDim.x, ++lt) {
+                const int b = lt & 1;
+                const uint32_t u = (uint32_t)(lt >> 1);
+                if (!wait_bounded(&aempty[b], (u & 1u) ^ 1u)) {
+                    aborted = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(b * BN);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!wait_bounded(&full[stage], phase)) {
+                        aborted = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_addr(smem + stage * L::STAGE);
+                    const uint64_t da = sdesc_kmajor_sw128(sa);
+                    const uint64_t db = sdesc_kmajor_sw128(sa + A_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k)
+                        mma_f8f6f4(d, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+                    mma_commit(&empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!aborted) mma_commit(&afull[b]);
+            }
+            if (aborted) {
+                mma_commit(drain);          // completes once every issued MMA is done
+                wait_drain(drain, 0);
+            }
+        }
+    } else {
+        const int quarter = warp & 3;       // the TMEM lane quarter this warp may read
+        const float scale = __ldg(p.sA) * __ldg(p.sB);
+        int lt = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++lt) {
+            const int b = lt & 1;
+            const uint32_t u = (uint32_t)(lt >> 1);
+            const bool ok = wait_bounded(&afull[b], u & 1u);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            tc_fence_after();
+            int mb, nb;
+            sched.coords(t, mb, nb);
+            const int row = mb * BM + quarter * 32 + lane;
+            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(taddr + (uint32_t)c, r);
+                tmem_ld_wait();
+                float v[32];
+                const int col0 = nb * BN + c;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * scale;
+                if (p.bias) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (col0 + j < p.N) v[j] += __ldg(p.bias + col0 + j);
+                }
+                store_row32<OUT_BF16>(p, row, col0, v);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&aempty[b]);
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ================================================================== mode 1
+// 1x128 x 128x128 scales with per-K-block promotion; BN = 128, four TMEM
+// partial buffers, 8 epilogue warps (warps 2..9): warp w reads lane quarter
+// w % 4 and column half (w - 2) / 4.
+constexpr int kPromoBuffers = 4;
+
+template <int STAGES, bool OUT_BF16>
+__global__ void __launch_bounds__(320, 1)
+    k_gemm_promote(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   EpiParams p, uint32_t idesc, TileSched sched)
+{
+    constexpr int BN = 128;
+    constexpr int NB = kPromoBuffers;
+    using L = Smem<BN, STAGES, NB>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+    uint64_t* empty = full + STAGES;
+    uint64_t* afull = empty + STAGES;
+    uint64_t* aempty = afull + NB;
+    uint64_t* drain = aempty + NB;
+    constexpr uint32_t TMEM_COLS = NB * BN;
+
+    uint32_t tmem_base;
+    if (!gemm_setup<STAGES, NB, 8>(smem, L::BAR_OFF, TMEM_COLS, &tmA, &tmB, tmem_base)) return;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int num_tiles = sched.num_m * sched.num_n;
+    const int nkb = p.K / BK;
+
+    if (warp == 0) {
+        if (lane == 0) producer_loop<BN, STAGES>(smem, full, empty, &tmA, &tmB, sched, num_tiles, nkb);
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0, it = 0;
+            uint32_t phase = 0;
+            bool aborted = false;
+            for (int t = blockIdx.x; t < num_tiles && !aborted; t += gridDim.x) {
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const int b = it % NB;
+                    const uint32_t u = (uint32_t)(it / NB);
+                    if (!wait_bounded(&aempty[b], (u & 1u) ^ 1u) || !wait_bounded(&full[stage], phase)) {
+                        aborted = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + (uint32_t)(b * BN);
+                    const uint32_t sa = smem_addr(smem + stage * L::STAGE);
+                    const uint64_t da = sdesc_kmajor_sw128(sa);
+                    const uint64_t db = sdesc_kmajor_sw128(sa + A_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k) mma_f8f6f4(d, da + 2 * k, db + 2 * k, idesc, k != 0 ? 1u : 0u);
+                    mma_commit(&empty[stage]);
+                    mma_commit(&afull[b]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (aborted) {
+                mma_commit(drain);
+                wait_drain(drain, 0);
+            }
+        }
+    } else {
+        const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int ksb = p.K / BK;            // scale blocks along K
+        int it = 0;
+        bool ok_all = true;
+        for (int t = blockIdx.x; t < num_tiles && ok_all; t += gridDim.x) {
+            int mb, nb;
+            sched.coords(t, mb, nb);
+            const int row = mb * BM + quarter * 32 + lane;
+            const int rowc = row < p.M ? row : p.M - 1;   // clamp for the scale read
+            const float* sa_row = p.sA + (int64_t)rowc * ksb;
+            const float* sb_row = p.sB + (int64_t)nb * ksb;   // BN = 128: one weight block row
+            float acc[64];
+#pragma unroll
+            for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
+            float sc_next = __ldg(sa_row) * __ldg(sb_row);
+            for (int kb = 0; kb < nkb; ++kb, ++it) {
+                const float sc = sc_next;
+                if (kb + 1 < nkb) sc_next = __ldg(sa_row + kb + 1) * __ldg(sb_row + kb + 1);
+                const int b = it % NB;
+                const uint32_t u = (uint32_t)(it / NB);
+                const bool ok = wait_bounded(&afull[b], u & 1u);
+                if (!__all_sync(0xFFFFFFFFu, ok)) {
+                    ok_all = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr =
+                    tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * BN + half * 64);
+                uint32_t r0[32], r1[32];
+                tmem_ld_32x32b_x32(taddr, r0);
+                tmem_ld_32x32b_x32(taddr + 32, r1);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&aempty[b]);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    acc[j] = fmaf(__uint_as_float(r0[j]), sc, acc[j]);
+                    acc[32 + j] = fmaf(__uint_as_float(r1[j]), sc, acc[32 + j]);
+                }
+            }
+            if (!ok_all) break;
+            const int col0 = nb * BN + half * 64;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    v[j] = acc[32 * h + j];
+                    if (p.bias && col0 + 32 * h + j < p.N) v[j] += __ldg(p.bias + col0 + 32 * h + j);
+                }
+                store_row32<OUT_BF16>(p, row, col0 + 32 * h, v);
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ================================================================== K == 0
+template <bool OUT_BF16>
+__global__ void k_fill_bias(void* D, int64_t M, int64_t N, const float* bias)
+{
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= M * N) return;
+    float v = bias ? bias[i % N] : 0.0f;
+    if (OUT_BF16) static_cast<__nv_bfloat16*>(D)[i] = __float2bfloat16_rn(v);
+    else static_cast<float*>(D)[i] = v;
+}
+
+// ================================================================== host
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D u8 tensor [rows][inner] (inner contiguous), box box_rows x 128 bytes, 128-byte swizzle
+static bool make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner};
+    cuuint32_t box[2] = {128u, box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// instruction descriptor, kind::f8f6f4: D fp32, A/B format, both K-major, N, M = 128
+static uint32_t make_idesc(int a_fmt, int b_fmt, int n)
+{
+    uint32_t d = 0;
+    d |= 1u << 4;                       // D format: F32
+    d |= (uint32_t)a_fmt << 7;          // 0 = E4M3, 1 = E5M2
+    d |= (uint32_t)b_fmt << 10;
+    d |= (uint32_t)(n >> 3) << 17;      // N / 8
+    d |= (uint32_t)(BM >> 4) << 24;     // M / 16
+    return d;
+}
+
+template <typename KernelT>
+static cudaError_t launch_persistent(KernelT kernel, int threads, int smem_bytes, int num_tiles, int sms,
+                                     cudaStream_t st, const CUtensorMap& ta, const CUtensorMap& tb,
+                                     const EpiParams& p, uint32_t idesc, const TileSched& sched)
+{
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return e;
+    int grid = num_tiles < sms ? num_tiles : sms;
+    kernel<<<grid, threads, smem_bytes, st>>>(ta, tb, p, idesc, sched);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char** why)
+{
+    *why = nullptr;
+    if (g.M == 0 || g.N == 0) return cudaSuccess;
+    const bool bf16 = g.d_dtype == kBF16;
+    if (g.K == 0) {
+        int64_t n = g.M * g.N;
+        if (bf16) k_fill_bias<true><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(g.D, g.M, g.N, g.bias);
+        else k_fill_bias<false><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(g.D, g.M, g.N, g.bias);
+        return cudaGetLastError();
+    }
+    EpiParams p;
+    p.M = (int)g.M;
+    p.N = (int)g.N;
+    p.K = (int)g.K;
+    p.sA = static_cast<const float*>(g.a_scale);
+    p.sB = static_cast<const float*>(g.b_scale);
+    p.bias = g.bias;
+    p.D = g.D;
+    CUtensorMap ta, tb;
+    if (g.mode == 0) {
+        constexpr int BN = 256, ST = 4;
+        if (!make_tmap(&ta, g.A, g.K, g.M, BM) || !make_tmap(&tb, g.B, g.K, g.N, BN)) {
+            *why = "cuTensorMapEncodeTiled failed";
+            return cudaErrorInvalidValue;
+        }
+        TileSched sched{(int)((g.M + BM - 1) / BM), (int)((g.N + BN - 1) / BN), 16};
+        const int tiles = sched.num_m * sched.num_n;
+        const uint32_t idesc = make_idesc(g.a_format, g.b_format, BN);
+        const int smem = Smem<BN, ST, 2>::BYTES;
+        if (bf16)
+            return launch_persistent(k_gemm_tensor<BN, ST, true>, 192, smem, tiles, sms, st, ta, tb, p, idesc, sched);
+        return launch_persistent(k_gemm_tensor<BN, ST, false>, 192, smem, tiles, sms, st, ta, tb, p, idesc, sched);
+    }
+    if (g.mode == 1) {
+        constexpr int BN = 128, ST = 6;
+        if (!make_tmap(&ta, g.A, g.K, g.M, BM) || !make_tmap(&tb, g.B, g.K, g.N, BN)) {
+            *why = "cuTensorMapEncodeTiled failed";
+            return cudaErrorInvalidValue;
+        }
+        TileSched sched{(int)((g.M + BM - 1) / BM), (int)((g.N + BN - 1) / BN), 16};
+        const int tiles = sched.num_m * sched.num_n;
+        const uint32_t idesc = make_idesc(g.a_format, g.b_format, BN);
+        const int smem = Smem<BN, ST, kPromoBuffers>::BYTES;
+        if (bf16)
+            return launch_persistent(k_gemm_promote<ST, true>, 320, smem, tiles, sms, st, ta, tb, p, idesc, sched);
+        return launch_persistent(k_gemm_promote<ST, false>, 320, smem, tiles, sms, st, ta, tb, p, idesc, sched);
+    }
+    *why = "GEMM mode not built";
+    return cudaErrorNotSupported;
+}
+
+int read_device_error(int clear)
+{
+    int v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+    if (cudaMemcpyFromSymbol(&v, g_dev_error, sizeof(int)) != cudaSuccess) return -1;
+    if (clear) {
+        int z = 0;
+        if (cudaMemcpyToSymbol(g_dev_error, &z, sizeof(int)) != cudaSuccess) return -1;
+    }
+    return v;
+}
+
+}  // namespace fp8sq

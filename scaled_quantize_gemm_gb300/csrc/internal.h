@@ -1,0 +1,52 @@
+// internal.h -- host-side launcher interface between the C-ABI layer
+// (api.cu) and the kernel translation units.  Not installed, not part of the ABI.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fp8sq {
+
+enum { kE4M3 = 0, kE5M2 = 1 };
+enum { kBF16 = 0, kF32 = 1 };
+enum { kTensor = 0, kTile = 1, kBlock = 2, kMX = 3 };
+
+struct QuantArgs {
+    const void* x = nullptr;
+    int x_dtype = kBF16;
+    int64_t rows = 0, cols = 0;
+    int format = kE4M3;
+    int gran = kTensor;
+    float* state = nullptr;          // delayed state block (TENSOR only) or null
+    int history_len = 0;
+    uint8_t* q = nullptr;            // may be null only for amax-only launches
+    uint8_t* qT = nullptr;
+    void* scales = nullptr;
+    float* amax = nullptr;
+    unsigned long long* sat = nullptr;
+    const float* amax_in = nullptr;  // current per-tensor: the amax of pass 1
+};
+
+// quantize.cu
+cudaError_t launch_amax(const QuantArgs& a, cudaStream_t st, int sms);    // writes a.amax per unit
+cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st, int sms);
+cudaError_t launch_scale_init(float* states, int n, int H, cudaStream_t st);
+cudaError_t launch_update_scale(float* states, int n, int H, const int* formats, int algo, cudaStream_t st);
+
+struct GemmArgs {
+    const uint8_t* A = nullptr;
+    const uint8_t* B = nullptr;
+    int a_format = kE4M3, b_format = kE4M3;
+    int mode = 0;                    // 0 per-tensor, 1 tile x block promotion, 2 MX
+    const void* a_scale = nullptr;
+    const void* b_scale = nullptr;
+    int64_t M = 0, N = 0, K = 0;
+    const float* bias = nullptr;
+    void* D = nullptr;
+    int d_dtype = kBF16;
+};
+
+// gemm.cu
+cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char** why);
+int read_device_error(int clear);   // 0 or the device error word's value
+
+}  // namespace fp8sq

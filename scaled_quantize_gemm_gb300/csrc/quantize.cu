@@ -1,0 +1,610 @@
+// quantize.cu -- amax, scale rules and the saturating FP8 cast on sm_103a.
+//
+// All of this is HBM-bound (2 B read + 1 B written per bf16 element, +1 B for
+// a transposed copy), so the kernels are built around coalesced 128-bit
+// loads, 64-bit code stores, an in-register amax (packed bf16 absolute
+// values reduced with a 2-way unsigned max), warp shuffles and one atomic per
+// CTA.  No shared-memory staging is needed: every scaling unit lives in the
+// registers of one thread group.
+//
+// Arithmetic follows the pages' statement of the method:
+//  * amax = max|x| ("Transformer Scaling", core vocabulary), taken on the
+//    IEEE bit patterns of |x| so that a NaN propagates;
+//  * current scale m = fmax / amax, s = amax / fmax, each one IEEE fp32
+//    division ("Week 14", absmax bullet: the step comes from the current
+//    block; "Transformer Scaling" worked example: the multiplier form);
+//  * cast q = cvt.rn.satfinite(fp32(x) * m) ("Transformer Scaling" worked
+//    example: a value past the range clips at 448);
+//  * MX: one power-of-two scale per 32 values ("Week 14", absmax bullet),
+//    the smallest 2^e with amax <= fmax * 2^e;
+//  * delayed: m from the state, the tensor's amax max-combined into the
+//    newest history slot; the end-of-step update takes the history max
+//    ("Transformer Scaling", delayed scaling; the Transformer Engine
+//    tutorial's DelayedScaling recipe).
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fp8sq {
+
+template <int FMT>
+struct Fmt;
+template <>
+struct Fmt<kE4M3> {
+    static constexpr float fmax = 448.0f;
+    static constexpr int emax = 8;
+};
+template <>
+struct Fmt<kE5M2> {
+    static constexpr float fmax = 57344.0f;
+    static constexpr int emax = 15;
+};
+
+// ------------------------------------------------------------------ loads
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// 8 consecutive input elements held in registers.
+template <int DT>
+struct Vec8;
+
+template <>
+struct Vec8<kBF16> {
+    uint4 w;
+    static constexpr int bytes = 16;
+    __device__ __forceinline__ void load(const void* base, int64_t elem) { w = ld_nc_v4(static_cast<const uint16_t*>(base) + elem); }
+    __device__ __forceinline__ void zero() { w = make_uint4(0, 0, 0, 0); }
+    // fp32 bit pattern of max|x_i| (NaN-propagating: NaN bits sort above inf)
+    __device__ __forceinline__ uint32_t absmax_bits() const
+    {
+        const uint32_t k = 0x7FFF7FFFu;
+        uint32_t u = __vmaxu2(__vmaxu2(w.x & k, w.y & k), __vmaxu2(w.z & k, w.w & k));
+        return max(u & 0xFFFFu, u >> 16) << 16;
+    }
+    __device__ __forceinline__ void get(float (&f)[8]) const
+    {
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(ws[i] << 16);
+            f[2 * i + 1] = __uint_as_float(ws[i] & 0xFFFF0000u);
+        }
+    }
+};
+
+template <>
+struct Vec8<kF32> {
+    uint4 a, b;
+    static constexpr int bytes = 32;
+    __device__ __forceinline__ void load(const void* base, int64_t elem)
+    {
+        const float* p = static_cast<const float*>(base) + elem;
+        a = ld_nc_v4(p);
+        b = ld_nc_v4(p + 4);
+    }
+    __device__ __forceinline__ void zero() { a = b = make_uint4(0, 0, 0, 0); }
+    __device__ __forceinline__ uint32_t absmax_bits() const
+    {
+        const uint32_t k = 0x7FFFFFFFu;
+        uint32_t m0 = max(max(a.x & k, a.y & k), max(a.z & k, a.w & k));
+        uint32_t m1 = max(max(b.x & k, b.y & k), max(b.z & k, b.w & k));
+        return max(m0, m1);
+    }
+    __device__ __forceinline__ void get(float (&f)[8]) const
+    {
+        f[0] = __uint_as_float(a.x); f[1] = __uint_as_float(a.y);
+        f[2] = __uint_as_float(a.z); f[3] = __uint_as_float(a.w);
+        f[4] = __uint_as_float(b.x); f[5] = __uint_as_float(b.y);
+        f[6] = __uint_as_float(b.z); f[7] = __uint_as_float(b.w);
+    }
+};
+
+// ------------------------------------------------------------------ scale rules
+// current scaling: m = fmax/amax, s = amax/fmax; amax 0 or non-finite -> 1, 1
+template <int FMT>
+__device__ __forceinline__ void current_scale(uint32_t amax_bits, float& m, float& s)
+{
+    float a = __uint_as_float(amax_bits);
+    if (amax_bits != 0u && amax_bits < 0x7F800000u) {
+        m = __fdiv_rn(Fmt<FMT>::fmax, a);
+        s = __fdiv_rn(a, Fmt<FMT>::fmax);
+    } else {
+        m = 1.0f;
+        s = 1.0f;
+    }
+}
+
+// MX: E8M0 code of the smallest 2^e with amax <= fmax * 2^e, and m = 2^-e
+template <int FMT>
+__device__ __forceinline__ uint32_t mx_scale(uint32_t amax_bits, float& m)
+{
+    if (amax_bits >= 0x7F800000u) { m = 1.0f; return 0xFFu; }
+    if (amax_bits == 0u) { m = 1.0f; return 127u; }
+    int E;
+    uint32_t frac;
+    uint32_t ef = amax_bits >> 23;
+    if (ef == 0u) {                      // subnormal: normalise
+        uint32_t mant = amax_bits & 0x7FFFFFu;
+        int p = 31 - __clz(mant);        // leading one position, 0..22
+        E = p - 149;
+        frac = (mant << (23 - p)) & 0x7FFFFFu;
+    } else {
+        E = (int)ef - 127;
+        frac = amax_bits & 0x7FFFFFu;
+    }
+    int e = E - Fmt<FMT>::emax + (frac > 0x600000u ? 1 : 0);   // 1.f > 1.75
+    e = max(-127, min(127, e));
+    m = (e <= 126) ? __uint_as_float((uint32_t)(127 - e) << 23) : __uint_as_float(0x00400000u);
+    return (uint32_t)(e + 127);
+}
+
+// cast 8 values with multiplier m; returns 8 codes packed little-endian
+template <int FMT>
+__device__ __forceinline__ uint2 cast8(const float (&f)[8], float m, uint32_t& nsat)
+{
+    float p[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        p[i] = __fmul_rn(f[i], m);
+        nsat += (fabsf(p[i]) > Fmt<FMT>::fmax) ? 1u : 0u;
+    }
+    uint32_t lo = cvt_fp8x2<FMT>(p[0], p[1]) | (cvt_fp8x2<FMT>(p[2], p[3]) << 16);
+    uint32_t hi = cvt_fp8x2<FMT>(p[4], p[5]) | (cvt_fp8x2<FMT>(p[6], p[7]) << 16);
+    return make_uint2(lo, hi);
+}
+
+__device__ __forceinline__ void atomic_max_bits(float* dst, uint32_t bits)
+{
+    // |x| bit patterns order like the values (NaN above inf); skip the atomic
+    // when the stored value already covers ours.
+    unsigned int* p = reinterpret_cast<unsigned int*>(dst);
+    if (bits > *reinterpret_cast<volatile unsigned int*>(p)) atomicMax(p, bits);
+}
+
+__device__ __forceinline__ void add_sat(unsigned long long* sat, uint32_t n)
+{
+    n = __reduce_add_sync(0xFFFFFFFFu, n);
+    if ((threadIdx.x & 31) == 0 && n) atomicAdd(sat, (unsigned long long)n);
+}
+
+// block-wide max of the fp32 bit patterns; result valid in every thread
+template <int NWARPS>
+__device__ __forceinline__ uint32_t block_max_bits(uint32_t v, uint32_t* red)
+{
+    v = __reduce_max_sync(0xFFFFFFFFu, v);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    uint32_t r = red[0];
+#pragma unroll
+    for (int i = 1; i < NWARPS; ++i) r = max(r, red[i]);
+    return r;
+}
+
+// ================================================================== per-tensor
+// Pass 1 of current per-tensor scaling (and fp8_amax TENSOR): grid-stride
+// over 8-element chunks, 4 independent 128-bit loads in flight per thread.
+constexpr int kFlatThreads = 256;
+constexpr int kFlatUnroll = 4;
+
+template <int DT>
+__global__ void __launch_bounds__(kFlatThreads) k_amax_tensor(const void* __restrict__ x, int64_t n,
+                                                              float* __restrict__ amax_out)
+{
+    __shared__ uint32_t red[kFlatThreads / 32];
+    const int64_t nch = n / 8;
+    uint32_t mx = 0;
+    const int64_t stride = (int64_t)gridDim.x * kFlatThreads * kFlatUnroll;
+    for (int64_t c0 = (int64_t)blockIdx.x * kFlatThreads * kFlatUnroll; c0 < nch; c0 += stride) {
+        Vec8<DT> v[kFlatUnroll];
+#pragma unroll
+        for (int u = 0; u < kFlatUnroll; ++u) {
+            int64_t c = c0 + u * kFlatThreads + threadIdx.x;
+            if (c < nch) v[u].load(x, c * 8); else v[u].zero();
+        }
+#pragma unroll
+        for (int u = 0; u < kFlatUnroll; ++u) mx = max(mx, v[u].absmax_bits());
+    }
+    // ragged tail (n % 8 elements): block 0, first threads
+    if (blockIdx.x == 0 && threadIdx.x < (n & 7)) {
+        int64_t i = nch * 8 + threadIdx.x;
+        uint32_t b = (DT == kBF16) ? ((uint32_t)(static_cast<const uint16_t*>(x)[i] & 0x7FFFu) << 16)
+                                   : (__float_as_uint(static_cast<const float*>(x)[i]) & 0x7FFFFFFFu);
+        mx = max(mx, b);
+    }
+    uint32_t r = block_max_bits<kFlatThreads / 32>(mx, red);
+    if (threadIdx.x == 0) atomic_max_bits(amax_out, r);
+}
+
+// Cast pass of per-tensor scaling without a transposed copy.
+//   DELAYED: m = state[H]; the tensor's amax is max-combined into state[0]
+//            (and into amax_out if given).
+//   current: m, s from *amax_in; block 0 writes s.
+template <int DT, int FMT, bool DELAYED>
+__global__ void __launch_bounds__(kFlatThreads) k_cast_tensor(const void* __restrict__ x, int64_t n,
+                                                              uint8_t* __restrict__ q, float* state, int H,
+                                                              const float* amax_in, float* s_out,
+                                                              float* amax_out, unsigned long long* sat)
+{
+    __shared__ uint32_t red[kFlatThreads / 32];
+    float m, s;
+    if (DELAYED) {
+        m = state[H];
+        s = 0.0f;
+    } else {
+        current_scale<FMT>(__float_as_uint(*amax_in), m, s);
+        if (blockIdx.x == 0 && threadIdx.x == 0 && s_out) *s_out = s;
+    }
+    const int64_t nch = n / 8;
+    uint32_t mx = 0, nsat = 0;
+    const int64_t stride = (int64_t)gridDim.x * kFlatThreads * kFlatUnroll;
+    for (int64_t c0 = (int64_t)blockIdx.x * kFlatThreads * kFlatUnroll; c0 < nch; c0 += stride) {
+        Vec8<DT> v[kFlatUnroll];
+#pragma unroll
+        for (int u = 0; u < kFlatUnroll; ++u) {
+            int64_t c = c0 + u * kFlatThreads + threadIdx.x;
+            if (c < nch) v[u].load(x, c * 8); else v[u].zero();
+        }
+#pragma unroll
+        for (int u = 0; u < kFlatUnroll; ++u) {
+            int64_t c = c0 + u * kFlatThreads + threadIdx.x;
+            if (DELAYED) mx = max(mx, v[u].absmax_bits());
+            float f[8];
+            v[u].get(f);
+            uint2 codes = cast8<FMT>(f, m, nsat);
+            if (c < nch) *reinterpret_cast<uint2*>(q + c * 8) = codes;
+        }
+    }
+    if (blockIdx.x == 0 && threadIdx.x < (n & 7)) {
+        int64_t i = nch * 8 + threadIdx.x;
+        float f = (DT == kBF16) ? __uint_as_float((uint32_t)static_cast<const uint16_t*>(x)[i] << 16)
+                                : static_cast<const float*>(x)[i];
+        float p = __fmul_rn(f, m);
+        nsat += fabsf(p) > Fmt<FMT>::fmax ? 1u : 0u;
+        q[i] = (uint8_t)(cvt_fp8x2<FMT>(p, 0.0f) & 0xFFu);
+        mx = max(mx, __float_as_uint(f) & 0x7FFFFFFFu);
+    }
+    if (sat) add_sat(sat, nsat);
+    if (DELAYED) {
+        uint32_t r = block_max_bits<kFlatThreads / 32>(mx, red);
+        if (threadIdx.x == 0) {
+            atomic_max_bits(&state[0], r);
+            if (amax_out) atomic_max_bits(amax_out, r);
+        }
+    }
+}
+
+// 8x8 byte transpose: in[i] holds row i (bytes = columns 0..7); out[j] holds
+// column j (bytes = rows 0..7).  Four 4x4 transposes with byte permutes.
+__device__ __forceinline__ void transpose4x4(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
+                                             uint32_t& c0, uint32_t& c1, uint32_t& c2, uint32_t& c3)
+{
+    uint32_t t0 = __byte_perm(w0, w1, 0x5140);  // w0.b0 w1.b0 w0.b1 w1.b1
+    uint32_t t1 = __byte_perm(w2, w3, 0x5140);
+    uint32_t t2 = __byte_perm(w0, w1, 0x7362);  // w0.b2 w1.b2 w0.b3 w1.b3
+    uint32_t t3 = __byte_perm(w2, w3, 0x7362);
+    c0 = __byte_perm(t0, t1, 0x5410);
+    c1 = __byte_perm(t0, t1, 0x7632);
+    c2 = __byte_perm(t2, t3, 0x5410);
+    c3 = __byte_perm(t2, t3, 0x7632);
+}
+__device__ __forceinline__ void transpose8x8(const uint2 (&in)[8], uint2 (&out)[8])
+{
+    uint32_t a[4], b[4], c[4], d[4];
+    // rows 0-3 cols 0-3 -> cols 0-3 rows 0-3 (low words of out[0..3])
+    transpose4x4(in[0].x, in[1].x, in[2].x, in[3].x, a[0], a[1], a[2], a[3]);
+    // rows 4-7 cols 0-3 -> high words of out[0..3]
+    transpose4x4(in[4].x, in[5].x, in[6].x, in[7].x, b[0], b[1], b[2], b[3]);
+    // rows 0-3 cols 4-7 -> low words of out[4..7]
+    transpose4x4(in[0].y, in[1].y, in[2].y, in[3].y, c[0], c[1], c[2], c[3]);
+    transpose4x4(in[4].y, in[5].y, in[6].y, in[7].y, d[0], d[1], d[2], d[3]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        out[j] = make_uint2(a[j], b[j]);
+        out[4 + j] = make_uint2(c[j], d[j]);
+    }
+}
+
+// Per-tensor cast with a transposed copy: one 128x128 tile per CTA, each
+// thread an 8x8 sub-block (8 rows x one 128-bit load).  Warp layout: 4
+// column groups x 8 row groups, so every load instruction reads 64-byte
+// row segments and every code store writes whole 32-byte sectors, in both q
+// and qT.  Requires rows % 8 == 0, cols % 8 == 0.
+template <int DT, int FMT, bool DELAYED>
+__global__ void __launch_bounds__(256) k_cast_tensor_T(const void* __restrict__ x, int64_t R, int64_t C,
+                                                       uint8_t* __restrict__ q, uint8_t* __restrict__ qT,
+                                                       float* state, int H, const float* amax_in,
+                                                       float* s_out, float* amax_out,
+                                                       unsigned long long* sat)
+{
+    __shared__ uint32_t red[8];
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    const int64_t c0 = (int64_t)blockIdx.x * 128 + ((w & 3) * 4 + (l & 3)) * 8;
+    const int64_t r0 = (int64_t)blockIdx.y * 128 + ((w >> 2) * 8 + (l >> 2)) * 8;
+    float m, s;
+    if (DELAYED) {
+        m = state[H];
+        s = 0.0f;
+    } else {
+        current_scale<FMT>(__float_as_uint(*amax_in), m, s);
+        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && s_out) *s_out = s;
+    }
+    const bool ok = (r0 < R) && (c0 < C);
+    Vec8<DT> v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if (ok) v[i].load(x, (r0 + i) * C + c0); else v[i].zero();
+    }
+    uint32_t mx = 0, nsat = 0;
+    uint2 rows[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if (DELAYED) mx = max(mx, v[i].absmax_bits());
+        float f[8];
+        v[i].get(f);
+        rows[i] = cast8<FMT>(f, m, nsat);
+    }
+    if (ok) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(q + (r0 + i) * C + c0) = rows[i];
+        if (qT) {
+            uint2 cols[8];
+            transpose8x8(rows, cols);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) *reinterpret_cast<uint2*>(qT + (c0 + j) * R + r0) = cols[j];
+        }
+    } else {
+        nsat = 0;
+    }
+    if (sat) add_sat(sat, nsat);
+    if (DELAYED) {
+        uint32_t r = block_max_bits<8>(mx, red);
+        if (threadIdx.x == 0) {
+            atomic_max_bits(&state[0], r);
+            if (amax_out) atomic_max_bits(amax_out, r);
+        }
+    }
+}
+
+// ================================================================== row units
+// 1x128 tiles (UNIT = 128) and MX-32 blocks (UNIT = 32): a unit is UNIT/8
+// consecutive lanes, each holding one 128-bit chunk; units never straddle a
+// row because cols % UNIT == 0, so the tensor is treated as flat.
+// WRITE_Q = false computes the unit amaxes only (fp8_amax).
+template <int DT, int FMT, int UNIT, bool WRITE_Q>
+__global__ void __launch_bounds__(kFlatThreads) k_quant_rowunits(const void* __restrict__ x, int64_t n,
+                                                                 uint8_t* __restrict__ q, void* scales,
+                                                                 float* amax_out, unsigned long long* sat)
+{
+    constexpr int TPU = UNIT / 8;  // lanes per unit
+    const int64_t nch = n / 8;
+    uint32_t nsat = 0;
+    const int64_t stride = (int64_t)gridDim.x * kFlatThreads * kFlatUnroll;
+    for (int64_t c0 = (int64_t)blockIdx.x * kFlatThreads * kFlatUnroll; c0 < nch; c0 += stride) {
+        Vec8<DT> v[kFlatUnroll];
+#pragma unroll
+        for (int u = 0; u < kFlatUnroll; ++u) {
+            int64_t c = c0 + u * kFlatThreads + threadIdx.x;
+            if (c < nch) v[u].load(x, c * 8); else v[u].zero();
+        }
+#pragma unroll
+        for (int u = 0; u < kFlatUnroll; ++u) {
+            const int64_t c = c0 + u * kFlatThreads + threadIdx.x;
+            uint32_t a = v[u].absmax_bits();
+#pragma unroll
+            for (int o = TPU / 2; o >= 1; o >>= 1) a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+            const bool valid = c < nch;            // uniform over a unit's lanes
+            const bool leader = (threadIdx.x % TPU) == 0;
+            const int64_t unit = c / TPU;
+            if (valid && leader && amax_out) amax_out[unit] = __uint_as_float(a);
+            if (WRITE_Q) {
+                float m, s = 0.0f;
+                uint32_t code = 0;
+                if (UNIT == 32) code = mx_scale<FMT>(a, m);
+                else current_scale<FMT>(a, m, s);
+                float f[8];
+                v[u].get(f);
+                uint32_t ns = 0;
+                uint2 codes = cast8<FMT>(f, m, ns);
+                if (valid) {
+                    nsat += ns;
+                    *reinterpret_cast<uint2*>(q + c * 8) = codes;
+                    if (leader) {
+                        if (UNIT == 32) static_cast<uint8_t*>(scales)[unit] = (uint8_t)code;
+                        else static_cast<float*>(scales)[unit] = s;
+                    }
+                }
+            }
+        }
+    }
+    if (WRITE_Q && sat) add_sat(sat, nsat);
+}
+
+// ================================================================== 128x128 blocks
+// One CTA per block, 256 threads, 8x8 elements per thread (same warp layout
+// as k_cast_tensor_T); block amax through shared memory, then the cast.
+template <int DT, int FMT, bool WRITE_Q>
+__global__ void __launch_bounds__(256) k_quant_block128(const void* __restrict__ x, int64_t R, int64_t C,
+                                                        uint8_t* __restrict__ q, float* s_out,
+                                                        float* amax_out, unsigned long long* sat)
+{
+    __shared__ uint32_t red[8];
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    const int64_t c0 = (int64_t)blockIdx.x * 128 + ((w & 3) * 4 + (l & 3)) * 8;
+    const int64_t r0 = (int64_t)blockIdx.y * 128 + ((w >> 2) * 8 + (l >> 2)) * 8;
+    Vec8<DT> v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i].load(x, (r0 + i) * C + c0);
+    uint32_t mx = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mx = max(mx, v[i].absmax_bits());
+    const uint32_t a = block_max_bits<8>(mx, red);
+    const int64_t unit = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;
+    float m, s;
+    current_scale<FMT>(a, m, s);
+    if (threadIdx.x == 0) {
+        if (amax_out) amax_out[unit] = __uint_as_float(a);
+        if (WRITE_Q) s_out[unit] = s;
+    }
+    if (!WRITE_Q) return;
+    uint32_t nsat = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float f[8];
+        v[i].get(f);
+        *reinterpret_cast<uint2*>(q + (r0 + i) * C + c0) = cast8<FMT>(f, m, nsat);
+    }
+    if (sat) add_sat(sat, nsat);
+}
+
+// ================================================================== state
+__global__ void k_scale_init(float* states, int n, int H)
+{
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    int64_t total = (int64_t)n * (H + 2);
+    if (i < total) {
+        int64_t j = i % (H + 2);
+        states[i] = (j < H) ? 0.0f : 1.0f;
+    }
+}
+
+struct FormatList {
+    uint8_t f[1024];
+};
+
+__global__ void k_update_scale(float* states, int n, int H, FormatList fl, int algo)
+{
+    int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    float* st = states + (int64_t)i * (H + 2);
+    uint32_t a = __float_as_uint(st[0]) & 0x7FFFFFFFu;
+    if (algo == 0)
+        for (int j = 1; j < H; ++j) a = max(a, __float_as_uint(st[j]) & 0x7FFFFFFFu);
+    if (a != 0u && a < 0x7F800000u) {
+        float fm = fl.f[i] == kE4M3 ? Fmt<kE4M3>::fmax : Fmt<kE5M2>::fmax;
+        float af = __uint_as_float(a);
+        st[H] = __fdiv_rn(fm, af);
+        st[H + 1] = __fdiv_rn(af, fm);
+    }
+    for (int j = H - 1; j >= 1; --j) st[j] = st[j - 1];
+    st[0] = 0.0f;
+}
+
+// ================================================================== launchers
+static int flat_grid(int64_t nch, int sms)
+{
+    int64_t per_block = (int64_t)kFlatThreads * kFlatUnroll;
+    int64_t need = (nch + per_block - 1) / per_block;
+    int64_t cap = (int64_t)sms * 8;     // 8 x 256 threads resident per SM
+    int64_t g = need < cap ? need : cap;
+    return g < 1 ? 1 : (int)g;
+}
+
+template <int DT>
+static cudaError_t amax_dt(const QuantArgs& a, cudaStream_t st, int sms)
+{
+    const int64_t n = a.rows * a.cols;
+    switch (a.gran) {
+    case kTensor:
+        if (cudaMemsetAsync(a.amax, 0, sizeof(float), st) != cudaSuccess) return cudaGetLastError();
+        if (n > 0) k_amax_tensor<DT><<<flat_grid(n / 8, sms), kFlatThreads, 0, st>>>(a.x, n, a.amax);
+        break;
+    case kTile:
+        if (n > 0) k_quant_rowunits<DT, kE4M3, 128, false><<<flat_grid(n / 8, sms), kFlatThreads, 0, st>>>(a.x, n, nullptr, nullptr, a.amax, nullptr);
+        break;
+    case kMX:
+        if (n > 0) k_quant_rowunits<DT, kE4M3, 32, false><<<flat_grid(n / 8, sms), kFlatThreads, 0, st>>>(a.x, n, nullptr, nullptr, a.amax, nullptr);
+        break;
+    case kBlock:
+        if (n > 0) k_quant_block128<DT, kE4M3, false><<<dim3((unsigned)(a.cols / 128), (unsigned)(a.rows / 128)), 256, 0, st>>>(a.x, a.rows, a.cols, nullptr, nullptr, a.amax, nullptr);
+        break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_amax(const QuantArgs& a, cudaStream_t st, int sms)
+{
+    return a.x_dtype == kBF16 ? amax_dt<kBF16>(a, st, sms) : amax_dt<kF32>(a, st, sms);
+}
+
+template <int DT, int FMT>
+static cudaError_t quant_dt_fmt(const QuantArgs& a, cudaStream_t st, int sms)
+{
+    const int64_t n = a.rows * a.cols;
+    const int H = a.history_len;
+    if (a.gran == kTensor) {
+        const bool delayed = a.state != nullptr;
+        if (!delayed) {
+            // pass 1: amax into a.amax (required), pass 2 reads it
+            QuantArgs p = a;
+            p.gran = kTensor;
+            cudaError_t e = amax_dt<DT>(p, st, sms);
+            if (e != cudaSuccess) return e;
+        } else if (a.amax) {
+            if (cudaMemsetAsync(a.amax, 0, sizeof(float), st) != cudaSuccess) return cudaGetLastError();
+        }
+        float* s_out = static_cast<float*>(a.scales);
+        if (a.qT) {
+            if (n == 0) {
+                if (!delayed) k_cast_tensor<DT, FMT, false><<<1, kFlatThreads, 0, st>>>(a.x, 0, a.q, nullptr, 0, a.amax, s_out, nullptr, nullptr);
+                return cudaGetLastError();
+            }
+            dim3 grid((unsigned)((a.cols + 127) / 128), (unsigned)((a.rows + 127) / 128));
+            if (delayed)
+                k_cast_tensor_T<DT, FMT, true><<<grid, 256, 0, st>>>(a.x, a.rows, a.cols, a.q, a.qT, a.state, H, nullptr, nullptr, a.amax, a.sat);
+            else
+                k_cast_tensor_T<DT, FMT, false><<<grid, 256, 0, st>>>(a.x, a.rows, a.cols, a.q, a.qT, nullptr, 0, a.amax, s_out, nullptr, a.sat);
+        } else {
+            int g = flat_grid(n / 8, sms);
+            if (delayed)
+                k_cast_tensor<DT, FMT, true><<<g, kFlatThreads, 0, st>>>(a.x, n, a.q, a.state, H, nullptr, nullptr, a.amax, a.sat);
+            else
+                k_cast_tensor<DT, FMT, false><<<g, kFlatThreads, 0, st>>>(a.x, n, a.q, nullptr, 0, a.amax, s_out, nullptr, a.sat);
+        }
+        return cudaGetLastError();
+    }
+    if (n == 0) return cudaSuccess;
+    switch (a.gran) {
+    case kTile:
+        k_quant_rowunits<DT, FMT, 128, true><<<flat_grid(n / 8, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat);
+        break;
+    case kMX:
+        k_quant_rowunits<DT, FMT, 32, true><<<flat_grid(n / 8, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat);
+        break;
+    case kBlock:
+        k_quant_block128<DT, FMT, true><<<dim3((unsigned)(a.cols / 128), (unsigned)(a.rows / 128)), 256, 0, st>>>(a.x, a.rows, a.cols, a.q, static_cast<float*>(a.scales), a.amax, a.sat);
+        break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st, int sms)
+{
+    if (a.x_dtype == kBF16)
+        return a.format == kE4M3 ? quant_dt_fmt<kBF16, kE4M3>(a, st, sms) : quant_dt_fmt<kBF16, kE5M2>(a, st, sms);
+    return a.format == kE4M3 ? quant_dt_fmt<kF32, kE4M3>(a, st, sms) : quant_dt_fmt<kF32, kE5M2>(a, st, sms);
+}
+
+cudaError_t launch_scale_init(float* states, int n, int H, cudaStream_t st)
+{
+    int64_t total = (int64_t)n * (H + 2);
+    if (total > 0) k_scale_init<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(states, n, H);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_update_scale(float* states, int n, int H, const int* formats, int algo, cudaStream_t st)
+{
+    FormatList fl;
+    for (int i = 0; i < n; ++i) fl.f[i] = (uint8_t)formats[i];
+    if (n > 0) k_update_scale<<<(n + 127) / 128, 128, 0, st>>>(states, n, H, fl, algo);
+    return cudaGetLastError();
+}
+
+}  // namespace fp8sq

@@ -1,0 +1,59 @@
+"""Shared test helpers: tensor conversion and the GEMM tolerance check.
+
+GEMM tolerance (the 1e-3 bound on maximum relative error): for fp32 output,
+max|C - R| <= 1e-3 * max|R|, R the oracle's float64 result.  For bf16 output
+the output rounding itself is up to half a bf16 ulp (2^-9 relative), so each
+element must satisfy |C - R| <= 1e-3 * max|R| + ulp_bf16(C) / 2: C is the
+bf16 rounding of a value within the 1e-3 bound.
+"""
+import numpy as np
+import torch
+
+import oracle as o
+
+
+def np32(t: torch.Tensor) -> np.ndarray:
+    """torch (bf16/fp32, any device) -> exact float32 numpy."""
+    return t.detach().float().cpu().numpy()
+
+
+def codes(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().numpy().view(np.uint8)
+
+
+def bf16_half_ulp(c: np.ndarray) -> np.ndarray:
+    a = np.abs(c.astype(np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return 2.0 ** (e - 7) / 2
+
+
+def gemm_error(C: torch.Tensor, R: np.ndarray) -> float:
+    """max|C - R| / max|R| (the reported relative error)."""
+    c = C.detach().float().cpu().numpy().astype(np.float64)
+    den = float(np.max(np.abs(R)))
+    return float(np.max(np.abs(c - R))) / (den if den > 0 else 1.0)
+
+
+def assert_gemm_close(C: torch.Tensor, R: np.ndarray, tol: float = 1e-3):
+    c = C.detach().float().cpu().numpy().astype(np.float64)
+    assert c.shape == R.shape
+    assert np.all(np.isfinite(c)), "non-finite output"
+    scale = float(np.max(np.abs(R))) if R.size else 0.0
+    bound = tol * scale
+    if C.dtype == torch.bfloat16:
+        bound = bound + bf16_half_ulp(c)
+    err = np.abs(c - R)
+    bad = err > bound
+    if np.any(bad):
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{int(bad.sum())} elements out of tolerance; first at {tuple(i)}: "
+                             f"got {c[tuple(i)]!r}, oracle {R[tuple(i)]!r}, max|R| {scale}")
+
+
+def nan_aware_codes_equal(gpu: np.ndarray, ref: np.ndarray, fmt: int) -> bool:
+    """bit-exact, except that any NaN code matches any NaN code"""
+    table = np.array([np.isnan(o.decode(fmt, c)) for c in range(256)])
+    g_nan, r_nan = table[gpu], table[ref]
+    if not np.array_equal(g_nan, r_nan):
+        return False
+    return bool(np.array_equal(gpu[~g_nan], ref[~r_nan]))

@@ -1,0 +1,188 @@
+"""GPU parity of the tcgen05 FP8 GEMM against the oracle's float64 product of
+the dequantised operands (tolerance in tests/_helpers.py), plus closed forms
+that must come out exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as o
+import scaled_quantize_gemm_gb300 as sq
+from scaled_quantize_gemm_gb300 import workloads as wl
+
+from _helpers import assert_gemm_close, codes, gemm_error, np32
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _int_codes(rng, shape, fmt, lo, hi):
+    v = rng.integers(lo, hi + 1, shape)
+    table = {t: o.encode(fmt, float(t)) for t in range(lo, hi + 1)}
+    q = np.vectorize(table.get)(v).astype(np.uint8)
+    return v, q
+
+
+def _one(v=1.0):
+    return torch.tensor([v], dtype=torch.float32, device=DEV)
+
+
+def _gemm_t(qa, fa, sa, qb, fb, sb, out_dtype, bias=None):
+    M, N = qa.shape[0], qb.shape[0]
+    D = torch.empty((M, N), dtype=out_dtype, device=DEV)
+    sq.fp8_gemm(qa, fa, sa, sq.TENSOR, qb, fb, sb, sq.TENSOR, D, bias=bias)
+    torch.cuda.synchronize()
+    return D
+
+
+@pytest.mark.parametrize("fa,fb", [(sq.E4M3, sq.E4M3), (sq.E5M2, sq.E4M3), (sq.E4M3, sq.E5M2), (sq.E5M2, sq.E5M2)])
+def test_integer_operands_exact(fa, fb):
+    """Small integers are exact codes; with unit scales every partial sum is an
+    integer below 2^24, so fp32 accumulation must reproduce the int64 product."""
+    rng = np.random.default_rng(1)
+    M, N, K = 256, 512, 384
+    va, qa = _int_codes(rng, (M, K), fa, -8, 8)
+    vb, qb = _int_codes(rng, (N, K), fb, -8, 8)
+    D = _gemm_t(torch.from_numpy(qa).to(DEV), fa, _one(), torch.from_numpy(qb).to(DEV), fb, _one(), torch.float32)
+    exact = (va.astype(np.int64) @ vb.astype(np.int64).T).astype(np.float32)
+    assert np.array_equal(D.cpu().numpy(), exact)
+
+
+def test_identity_b():
+    rng = np.random.default_rng(2)
+    M, K = 384, 256
+    qa = rng.integers(0, 256, (M, K)).astype(np.uint8)
+    qa[(qa & 0x7F) == 0x7F] = 0x10                        # no NaN codes
+    one = o.encode(o.E4M3, 1.0)
+    qb = np.where(np.eye(K, dtype=bool), one, 0).astype(np.uint8)
+    D = _gemm_t(torch.from_numpy(qa).to(DEV), sq.E4M3, _one(0.5), torch.from_numpy(qb).to(DEV), sq.E4M3, _one(),
+                torch.float32)
+    ref = o.dequantize(qa, o.E4M3, o.GRAN_TENSOR, 0.5).astype(np.float32)
+    assert np.array_equal(D.cpu().numpy(), ref)
+
+
+def test_accumulation_width_long_k():
+    """K = 16384 with +-1, +-2 operands: sums stay below 2^24 and are exact in
+    fp32 -- a narrow accumulator (the week-14 page's 14-bit FP8 accumulator
+    note) would lose low bits here."""
+    rng = np.random.default_rng(3)
+    M, N, K = 128, 256, 16384
+    va, qa = _int_codes(rng, (M, K), o.E4M3, 0, 2)      # non-negative: the sums grow to ~2^15
+    vb, qb = _int_codes(rng, (N, K), o.E4M3, 0, 2)
+    D = _gemm_t(torch.from_numpy(qa).to(DEV), sq.E4M3, _one(), torch.from_numpy(qb).to(DEV), sq.E4M3, _one(),
+                torch.float32)
+    exact = (va.astype(np.int64) @ vb.astype(np.int64).T)
+    assert exact.max() < 2 ** 24
+    assert np.array_equal(D.cpu().numpy().astype(np.int64), exact)
+
+
+def _quant_tensor(x, fmt):
+    xd = x.to(DEV)
+    q = torch.empty(x.shape, dtype=torch.uint8, device=DEV)
+    amax = torch.zeros(1, device=DEV)
+    s = torch.zeros(1, device=DEV)
+    sq.fp8_quantize(xd, fmt, sq.TENSOR, q, scales_out=s, amax_out=amax)
+    return q, s
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (200, 136, 80), (384, 768, 1024), (1, 8, 16), (130, 264, 144)])
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+def test_per_tensor_vs_oracle(M, N, K, out):
+    a = wl.normal((M, K), 1.0, 11 + M, dtype=torch.float32)
+    b = wl.normal((N, K), 1.0, 12 + N, dtype=torch.float32)
+    qa, sa = _quant_tensor(a, sq.E4M3)
+    qb, sb = _quant_tensor(b, sq.E4M3)
+    bias = torch.randn(N, generator=torch.Generator().manual_seed(5)).to(DEV) if M == 384 else None
+    D = _gemm_t(qa, sq.E4M3, sa, qb, sq.E4M3, sb, out, bias=bias)
+    R = o.gemm_ref(o.dequantize(codes(qa), 0, 0, sa.item()), o.dequantize(codes(qb), 0, 0, sb.item()),
+                   bias=None if bias is None else bias.cpu().numpy())
+    assert_gemm_close(D, R)
+
+
+def test_w1_per_tensor_current_linear():
+    """Workload 1: A, B 256x256 fp32 with outliers of 30, per-tensor current
+    E4M3, M=N=K=256, fp32 output."""
+    a, b = wl.w1_operands()
+    qa, sa = _quant_tensor(a, sq.E4M3)
+    qb, sb = _quant_tensor(b, sq.E4M3)
+    D = _gemm_t(qa, sq.E4M3, sa, qb, sq.E4M3, sb, torch.float32)
+    rqa, _, rsa, _ = o.quantize_tensor_current(a.numpy(), o.E4M3)
+    rqb, _, rsb, _ = o.quantize_tensor_current(b.numpy(), o.E4M3)
+    assert np.array_equal(codes(qa), rqa) and np.array_equal(codes(qb), rqb)
+    R = o.gemm_ref(o.dequantize(rqa, 0, 0, rsa), o.dequantize(rqb, 0, 0, rsb))
+    assert_gemm_close(D, R)
+    assert gemm_error(D, R) < 1e-5
+
+
+def test_k_zero_and_m_zero():
+    qa = torch.empty((64, 0), dtype=torch.uint8, device=DEV)
+    qb = torch.empty((32, 0), dtype=torch.uint8, device=DEV)
+    bias = torch.arange(32, dtype=torch.float32, device=DEV)
+    D = torch.full((64, 32), 7.0, device=DEV)
+    sq.fp8_gemm(qa, 0, _one(), 0, qb, 0, _one(), 0, D, bias=bias, M=64, N=32, K=0)
+    torch.cuda.synchronize()
+    assert torch.equal(D, bias.expand(64, 32))
+    E = torch.full((0, 32), 1.0, device=DEV)
+    sq.fp8_gemm(torch.empty((0, 16), dtype=torch.uint8, device=DEV), 0, _one(), 0,
+                torch.zeros((32, 16), dtype=torch.uint8, device=DEV), 0, _one(), 0, E, M=0, N=32, K=16)
+    torch.cuda.synchronize()
+
+
+def _quant_tile_block(x, w):
+    M, K = x.shape
+    N = w.shape[0]
+    qx = torch.empty((M, K), dtype=torch.uint8, device=DEV)
+    qw = torch.empty((N, K), dtype=torch.uint8, device=DEV)
+    sx = torch.empty(M * (K // 128), dtype=torch.float32, device=DEV)
+    sw = torch.empty((N // 128) * (K // 128), dtype=torch.float32, device=DEV)
+    sq.fp8_quantize(x.to(DEV), sq.E4M3, sq.TILE_1x128, qx, scales_out=sx)
+    sq.fp8_quantize(w.to(DEV), sq.E4M3, sq.BLOCK_128x128, qw, scales_out=sw)
+    return qx, sx, qw, sw
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 384, 1024), (200, 256, 512)])
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+def test_tile_block_promotion_vs_oracle(M, N, K, out):
+    x = wl.student_t3((M, K), 21 + M)
+    w = wl.normal((N, K), 0.02, 22 + N)
+    qx, sx, qw, sw = _quant_tile_block(x, w)
+    D = torch.empty((M, N), dtype=out, device=DEV)
+    sq.fp8_gemm(qx, sq.E4M3, sx, sq.TILE_1x128, qw, sq.E4M3, sw, sq.BLOCK_128x128, D)
+    torch.cuda.synchronize()
+    R = o.gemm_ref(o.dequantize(codes(qx), 0, o.GRAN_TILE_1x128, sx.cpu().numpy().reshape(M, K // 128)),
+                   o.dequantize(codes(qw), 0, o.GRAN_BLOCK_128x128, sw.cpu().numpy().reshape(N // 128, K // 128)))
+    assert_gemm_close(D, R)
+
+
+def _sample_rows(M, n, seed):
+    return np.sort(np.random.default_rng(seed).choice(M, size=n, replace=False))
+
+
+def test_w3_full_size_sampled_rows():
+    """Workload 3 at full size (M=N=K=4096, bf16 out) in the launch
+    configuration the bench times; 256 sampled rows checked against the oracle."""
+    x, w = wl.w3_operands(DEV)
+    qx, sx, qw, sw = _quant_tile_block(x, w)
+    D = torch.empty((4096, 4096), dtype=torch.bfloat16, device=DEV)
+    sq.fp8_gemm(qx, sq.E4M3, sx, sq.TILE_1x128, qw, sq.E4M3, sw, sq.BLOCK_128x128, D)
+    torch.cuda.synchronize()
+    rows = _sample_rows(4096, 256, 3)
+    ah = o.dequantize(codes(qx[rows]), 0, o.GRAN_TILE_1x128, sx.view(4096, 32)[rows].cpu().numpy())
+    bh = o.dequantize(codes(qw), 0, o.GRAN_BLOCK_128x128, sw.view(32, 32).cpu().numpy())
+    assert_gemm_close(D[rows], o.gemm_ref(ah, bh))
+
+
+def test_w5_forward_gemm_full_size_sampled_rows():
+    """The FFN up-projection of workload 5 (M=16384, K=4096, N=14336, bf16
+    out) at full size; 128 sampled rows against the oracle."""
+    M, K, N = 16384, 4096, 14336
+    x = wl.linear_x(5, 0, 0, M, K, DEV)
+    w = wl.linear_w(5, 0, N, K, DEV)
+    qx, sx = _quant_tensor(x, sq.E4M3)
+    qw, sw = _quant_tensor(w, sq.E4M3)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    sq.fp8_gemm(qx, sq.E4M3, sx, sq.TENSOR, qw, sq.E4M3, sw, sq.TENSOR, D)
+    torch.cuda.synchronize()
+    rows = _sample_rows(M, 128, 5)
+    ah = o.dequantize(codes(qx[rows]), 0, 0, sx.item())
+    bh = o.dequantize(codes(qw), 0, 0, sw.item())
+    assert_gemm_close(D[rows], o.gemm_ref(ah, bh))

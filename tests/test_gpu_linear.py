@@ -1,0 +1,169 @@
+"""GPU parity of the FP8 linear layer (forward, dgrad, wgrad) under the
+HYBRID delayed-scaling recipe and under current / fine-grained scaling:
+histories and multipliers bit-exact every step, outputs within tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as o
+import scaled_quantize_gemm_gb300 as sq
+from scaled_quantize_gemm_gb300 import workloads as wl
+
+from _helpers import assert_gemm_close, np32
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+class Layer:
+    """device buffers of one linear layer under delayed scaling"""
+
+    def __init__(self, M, K, N, H=16):
+        self.M, self.K, self.N, self.H = M, K, N, H
+        self.states = torch.empty(3 * (H + 2), dtype=torch.float32, device=DEV)
+        sq.fp8_scale_init(self.states, 3, H)
+        self.ws = torch.empty(sq.fp8_linear_workspace_bytes(M, N, K), dtype=torch.uint8, device=DEV)
+        self.y = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+        self.dx = torch.empty((M, K), dtype=torch.bfloat16, device=DEV)
+        self.dw = torch.empty((N, K), dtype=torch.float32, device=DEV)
+
+    def st(self, i):
+        return self.states[i * (self.H + 2):(i + 1) * (self.H + 2)]
+
+    def step(self, x, w, dy):
+        sq.fp8_linear_fwd(x, w, self.y, self.ws, x_state=self.st(0), w_state=self.st(1), history_len=self.H)
+        sq.fp8_linear_bwd(dy, self.dx, self.dw, self.ws, self.K, dy_state=self.st(2), history_len=self.H)
+
+
+FORMATS = [sq.E4M3, sq.E4M3, sq.E5M2]       # x, W, dy under HYBRID
+
+
+def _oracle_step(ref, x, w, dy, rows=None, wrows=None):
+    qx, sx, qw, sw, Y = o.linear_fwd_delayed(np32(x), np32(w), ref[0], ref[1])
+    if rows is not None:
+        Y = Y[rows]
+    _, _, dX, dW = o.linear_bwd_delayed(np32(dy), ref[2], o.E5M2, qx, sx, qw, sw, rows=rows, wrows=wrows)
+    return Y, dX, dW
+
+
+@pytest.mark.parametrize("M,K,N", [(256, 384, 512), (128, 128, 128), (272, 144, 400)])
+def test_delayed_hybrid_steps(M, K, N):
+    L = Layer(M, K, N)
+    ref = [o.state_init(16) for _ in range(3)]
+    w = wl.normal((N, K), 0.02, 3).to(DEV)
+    for step in range(4):
+        x = wl.normal((M, K), 1.0 + step, 10 + step).to(DEV)
+        dy = wl.normal((M, N), 1e-3, 20 + step).to(DEV)
+        L.step(x, w, dy)
+        Y, dX, dW = _oracle_step(ref, x, w, dy)
+        sq.fp8_update_scale(L.states, 3, 16, FORMATS)
+        for r in range(3):
+            o.update_scale(ref[r], FORMATS[r])
+        torch.cuda.synchronize()
+        assert_gemm_close(L.y, Y)
+        assert_gemm_close(L.dx, dX)
+        assert_gemm_close(L.dw, dW)
+        assert L.states.cpu().numpy().tobytes() == np.concatenate(ref).tobytes(), step
+
+
+def test_current_scaling_linear():
+    M, K, N = 256, 256, 384
+    x = wl.normal((M, K), 2.0, 1).to(DEV)
+    w = wl.normal((N, K), 0.02, 2).to(DEV)
+    dy = wl.normal((M, N), 1e-3, 3).to(DEV)
+    ws = torch.empty(sq.fp8_linear_workspace_bytes(M, N, K), dtype=torch.uint8, device=DEV)
+    y = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device=DEV)
+    dw = torch.empty((N, K), dtype=torch.float32, device=DEV)
+    sq.fp8_linear_fwd(x, w, y, ws)
+    sq.fp8_linear_bwd(dy, dx, dw, ws, K, recipe=sq.RECIPE_E4M3)
+    torch.cuda.synchronize()
+    qx, _, sx, _ = o.quantize_tensor_current(np32(x), o.E4M3)
+    qw, _, sw, _ = o.quantize_tensor_current(np32(w), o.E4M3)
+    qd, _, sd, _ = o.quantize_tensor_current(np32(dy), o.E4M3)
+    xh, wh, dh = (o.dequantize(qx, 0, 0, sx), o.dequantize(qw, 0, 0, sw), o.dequantize(qd, 0, 0, sd))
+    assert_gemm_close(y, o.gemm_ref(xh, wh))
+    assert_gemm_close(dx, o.gemm_ref(dh, wh.T))
+    assert_gemm_close(dw, o.gemm_ref(dh.T, xh.T))
+
+
+def test_tile_block_linear_forward():
+    M, K, N = 256, 512, 384
+    x = wl.student_t3((M, K), 4).to(DEV)
+    w = wl.normal((N, K), 0.02, 5).to(DEV)
+    ws = torch.empty(sq.fp8_linear_workspace_bytes(M, N, K, sq.TILE_1x128), dtype=torch.uint8, device=DEV)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    sq.fp8_linear_fwd(x, w, y, ws, gran=sq.TILE_1x128)
+    torch.cuda.synchronize()
+    qx, sx, _, _ = o.quantize_tile1x128(np32(x), o.E4M3)
+    qw, sw, _, _ = o.quantize_block128(np32(w), o.E4M3)
+    R = o.gemm_ref(o.dequantize(qx, 0, o.GRAN_TILE_1x128, sx), o.dequantize(qw, 0, o.GRAN_BLOCK_128x128, sw))
+    assert_gemm_close(y, R)
+
+
+def test_w2_minigpt_20_steps():
+    """Workload 2: M = 2048 tokens (8 x 256), 768->2304, 768->3072, 3072->768,
+    HYBRID delayed scaling, H = 16, max, 20 steps with the activation std
+    drifting from 1 to 8.  All nine histories are compared bit for bit after
+    every step; outputs on 64 sampled rows (and 64 sampled dW rows) per step."""
+    wk = wl.WORKLOADS[2]
+    layers, refs, ws_ = [], [], []
+    for li, lin in enumerate(wk.linears):
+        layers.append(Layer(wk.tokens, lin.in_features, lin.out_features, wk.history_len))
+        refs.append([o.state_init(wk.history_len) for _ in range(3)])
+        ws_.append(wl.linear_w(2, li, lin.out_features, lin.in_features, DEV))
+    rng = np.random.default_rng(0)
+    for step in range(wk.steps):
+        for li, lin in enumerate(wk.linears):
+            L = layers[li]
+            x = wl.linear_x(2, li, step, wk.tokens, lin.in_features, DEV, std=wl.w2_sigma(step, wk.steps))
+            dy = wl.linear_dy(2, li, step, wk.tokens, lin.out_features, DEV)
+            L.step(x, ws_[li], dy)
+            rows = np.sort(rng.choice(wk.tokens, 64, replace=False))
+            wrows = np.sort(rng.choice(lin.out_features, 64, replace=False))
+            Y, dX, dW = _oracle_step(refs[li], x, ws_[li], dy, rows=rows, wrows=wrows)
+            torch.cuda.synchronize()
+            assert_gemm_close(L.y[rows], Y)
+            assert_gemm_close(L.dx[rows], dX)
+            assert_gemm_close(L.dw[wrows], dW)
+        for li in range(3):
+            sq.fp8_update_scale(layers[li].states, 3, wk.history_len, FORMATS)
+            for r in range(3):
+                o.update_scale(refs[li][r], FORMATS[r])
+        torch.cuda.synchronize()
+        for li in range(3):
+            assert layers[li].states.cpu().numpy().tobytes() == np.concatenate(refs[li]).tobytes(), (step, li)
+
+
+def test_w5_ffn_step_full_size():
+    """Workload 5 at full size (M = 16384, 4096 -> 14336 -> 4096), two steps of
+    forward + backward + update in the launch configuration the bench times;
+    histories bit-exact, 32 sampled rows of y, dx and dW per linear."""
+    wk = wl.WORKLOADS[5]
+    rng = np.random.default_rng(1)
+    layers, refs, ws_ = [], [], []
+    for li, lin in enumerate(wk.linears):
+        layers.append(Layer(wk.tokens, lin.in_features, lin.out_features, wk.history_len))
+        refs.append([o.state_init(wk.history_len) for _ in range(3)])
+        ws_.append(wl.linear_w(5, li, lin.out_features, lin.in_features, DEV))
+    for step in range(2):
+        for li, lin in enumerate(wk.linears):
+            L = layers[li]
+            x = wl.linear_x(5, li, step, wk.tokens, lin.in_features, DEV)
+            dy = wl.linear_dy(5, li, step, wk.tokens, lin.out_features, DEV)
+            L.step(x, ws_[li], dy)
+            rows = np.sort(rng.choice(wk.tokens, 32, replace=False))
+            wrows = np.sort(rng.choice(lin.out_features, 32, replace=False))
+            Y, dX, dW = _oracle_step(refs[li], x, ws_[li], dy, rows=rows, wrows=wrows)
+            torch.cuda.synchronize()
+            assert_gemm_close(L.y[rows], Y)
+            assert_gemm_close(L.dx[rows], dX)
+            assert_gemm_close(L.dw[wrows], dW)
+            del x, dy
+        for li in range(2):
+            sq.fp8_update_scale(layers[li].states, 3, wk.history_len, FORMATS)
+            for r in range(3):
+                o.update_scale(refs[li][r], FORMATS[r])
+        torch.cuda.synchronize()
+        for li in range(2):
+            assert layers[li].states.cpu().numpy().tobytes() == np.concatenate(refs[li]).tobytes(), (step, li)
