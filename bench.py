@@ -435,8 +435,58 @@ def run_reference(args, ws, rank, local):
     }), flush=True)
 
 
+def kernel_case(case: str, launches: int):
+    """A handful of launches of one kernel at the workload's size, for
+    profiling a single launch: 'gemm' = the 16384 x 14336 x 4096 forward GEMM
+    (k_gemm_tensor), 'cast' = the 16384 x 14336 E5M2 cast with its transposed
+    copy (k_cast_tensor_T), 'promote' = the 4096^3 1x128 x 128x128 GEMM
+    (k_gemm_promote)."""
+    import scaled_quantize_gemm_gb300 as sq
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    u8 = dict(dtype=torch.uint8, device=dev)
+    st = torch.empty(H + 2, dtype=torch.float32, device=dev)
+    sq.fp8_scale_init(st, 1, H)
+    if case == "cast":
+        M, N = WK.tokens, 14336
+        dy = wl.linear_dy(5, 0, 0, M, N, dev)
+        q, qT = torch.empty((M, N), **u8), torch.empty((N, M), **u8)
+        for _ in range(launches):
+            sq.fp8_quantize(dy, sq.E5M2, sq.TENSOR, q, qT=qT, delayed_state=st, history_len=H)
+    elif case == "gemm":
+        M, K, N = WK.tokens, 4096, 14336
+        x = wl.linear_x(5, 0, 0, M, K, dev)
+        w = wl.linear_w(5, 0, N, K, dev)
+        qx, qw = torch.empty((M, K), **u8), torch.empty((N, K), **u8)
+        sw = torch.empty(H + 2, dtype=torch.float32, device=dev)
+        sq.fp8_scale_init(sw, 1, H)
+        sq.fp8_quantize(x, sq.E4M3, sq.TENSOR, qx, delayed_state=st, history_len=H)
+        sq.fp8_quantize(w, sq.E4M3, sq.TENSOR, qw, delayed_state=sw, history_len=H)
+        del x, w
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        for _ in range(launches):
+            sq.fp8_gemm(qx, sq.E4M3, st[H + 1:], sq.TENSOR, qw, sq.E4M3, sw[H + 1:], sq.TENSOR, y)
+    elif case == "promote":
+        x, w = wl.w3_operands(dev)
+        qx, qw = torch.empty(x.shape, **u8), torch.empty(w.shape, **u8)
+        sx = torch.empty(4096 * 32, dtype=torch.float32, device=dev)
+        sw = torch.empty(32 * 32, dtype=torch.float32, device=dev)
+        sq.fp8_quantize(x, sq.E4M3, sq.TILE_1x128, qx, scales_out=sx)
+        sq.fp8_quantize(w, sq.E4M3, sq.BLOCK_128x128, qw, scales_out=sw)
+        y = torch.empty((4096, 4096), dtype=torch.bfloat16, device=dev)
+        for _ in range(launches):
+            sq.fp8_gemm(qx, sq.E4M3, sx, sq.TILE_1x128, qw, sq.E4M3, sw, sq.BLOCK_128x128, y)
+    torch.cuda.synchronize()
+    if sq.fp8_device_status(True) != 0:
+        raise RuntimeError("device status error")
+    print(f"kernel case {case}: {launches} launches ok")
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--kernel-case", choices=["gemm", "cast", "promote"], default=None,
+                    help="run a few launches of one kernel (for profiling) and exit")
+    ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
@@ -447,6 +497,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.kernel_case:
+        kernel_case(args.kernel_case, args.launches)
+        return
     ws, rank, local = _dist()
     if args.impl == "reference":
         run_reference(args, ws, rank, local)

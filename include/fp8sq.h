@@ -30,6 +30,7 @@
  *  - Return value: FP8SQ_OK (0) or a negative FP8SQ_ERR_* code.  Arguments
  *    are validated before anything is enqueued, so an error return means
  *    nothing was launched (except FP8SQ_ERR_CUDA from a failed launch).
+ *    A pointer to an operand with zero elements may be NULL.
  *    fp8_last_error() gives a message for the calling thread's last error.
  *    Nothing aborts, traps or prints.
  *  - Only sm_103 devices are accepted (FP8SQ_ERR_WRONG_ARCH otherwise).

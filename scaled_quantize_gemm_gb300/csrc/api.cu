@@ -128,7 +128,7 @@ FP8SQ_API int fp8_device_status(int clear)
 FP8SQ_API int fp8_amax(const void* x, int x_dtype, int64_t rows, int64_t cols, int gran, float* amax_out,
                        void* stream)
 {
-    if (!x || !amax_out) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_amax: null pointer");
+    if ((!x && rows * cols != 0) || !amax_out) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_amax: null pointer");
     if (!valid_dtype(x_dtype) || !valid_gran(gran)) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_amax: bad dtype or granularity");
     if (rows < 0 || cols < 0) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_amax: negative size");
     if (!aligned16(x)) return fail(FP8SQ_ERR_MISALIGNED, "fp8_amax: x must be 16-byte aligned");
@@ -181,7 +181,7 @@ static int validate_quantize(const void* x, int x_dtype, int64_t rows, int64_t c
                              const float* state, int H, const uint8_t* q, const uint8_t* qT, const void* scales,
                              const float* amax_out)
 {
-    if (!x || !q) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize: null x or q");
+    if ((!x || !q) && rows * cols != 0) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize: null x or q");
     if (!valid_dtype(x_dtype) || !valid_format(format) || !valid_gran(gran))
         return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize: bad dtype, format or granularity");
     if (rows < 0 || cols < 0) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize: negative size");
@@ -238,7 +238,10 @@ static int validate_gemm(const uint8_t* A, int a_format, const void* a_scale, in
                          int b_format, const void* b_scale, int b_gran, int64_t M, int64_t N, int64_t K,
                          const float* bias, const void* D, int d_dtype, int* mode)
 {
-    if (!A || !B || !D || !a_scale || !b_scale) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_gemm: null pointer");
+    // empty operands may come with null pointers (nothing of them is read)
+    if ((!A && M * K != 0) || (!B && N * K != 0) || (!D && M * N != 0) ||
+        ((!a_scale || !b_scale) && M * N * K != 0))
+        return fail(FP8SQ_ERR_INVALID_ARG, "fp8_gemm: null pointer");
     if (!valid_format(a_format) || !valid_format(b_format) || !valid_dtype(d_dtype))
         return fail(FP8SQ_ERR_INVALID_ARG, "fp8_gemm: bad format or output dtype");
     if (M < 0 || N < 0 || K < 0) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_gemm: negative size");
