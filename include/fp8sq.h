@@ -213,6 +213,36 @@ FP8SQ_API int fp8_linear_bwd(const void* dy, int64_t M, int64_t N, int64_t K, in
                              float* dy_state, int history_len, void* workspace, size_t ws_bytes,
                              void* dx, float* dw, void* stream);
 
+/* ---- 5b. forward linear without allocation --------------------------------
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that cannot call cudaMalloc or hand over a workspace -- code running inside
+ * a framework that owns every byte of device memory through its own pool, or
+ * a plugin called where allocating (which can synchronise the device) is not
+ * allowed.
+ *
+ * Computes y = x W^T like fp8_linear_fwd with gran TENSOR and current
+ * per-tensor scaling (x, W cast to E4M3 with m = 448/amax; y = acc * s_x *
+ * s_w + bias).  Its scratch -- the codes of x and W and four fp32 scalars --
+ * is a file-scope device array of FP8SQ_NOALLOC_SCRATCH_BYTES (32 MiB) that
+ * every GPU which loads this library holds until the process exits.  The call
+ * itself allocates nothing (no cudaMalloc, cudaFree or allocating library
+ * routine).
+ *   x  device bf16 [M][K], w device bf16 [N][K], y device bf16 / f32 [M][N],
+ *      bias device f32 [N] or NULL; x, w, y 16-byte aligned.
+ *   Needs N % 8 == 0, K % 16 == 0 and round256(M*K) + round256(N*K) + 256 <=
+ *   FP8SQ_NOALLOC_SCRATCH_BYTES; larger sizes return FP8SQ_ERR_UNSUPPORTED
+ *   with a message giving the bytes needed.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) for that device; make that first call before any
+ * stream capture.  All calls share the one array and it keeps the last
+ * call's contents (the amax slots are cleared by every call), so calls whose
+ * work overlaps on the GPU -- on different streams, or from several threads
+ * -- race on it and must be serialised by the caller.
+ */
+#define FP8SQ_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+FP8SQ_API int fp8_linear_fwd_noalloc(const void* x, const void* w, int64_t M, int64_t N, int64_t K,
+                                     const float* bias, void* y, int y_dtype, void* stream);
+
 /* ---- 6. diagnostics --------------------------------------------------------
  * fp8_device_status: synchronises the current device and returns
  *   FP8SQ_ERR_TIMEOUT if any bounded device-side wait of this library ran out

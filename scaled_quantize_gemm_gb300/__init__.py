@@ -60,6 +60,7 @@ def lib() -> ctypes.CDLL:
                 "fp8_linear_workspace_bytes": (Z, [I64, I64, I64, I]),
                 "fp8_linear_fwd": (I, [P, P, I64, I64, I64, I, I, P, P, I, P, Z, P, P, I, P]),
                 "fp8_linear_bwd": (I, [P, I64, I64, I64, I, P, I, P, Z, P, P, P]),
+                "fp8_linear_fwd_noalloc": (I, [P, P, I64, I64, I64, P, P, I, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -152,6 +153,15 @@ def fp8_linear_bwd(dy, dx, dw, workspace, K: int, recipe: int = RECIPE_HYBRID, d
     _check(lib().fp8_linear_bwd(_ptr(dy), M, N, K, recipe, _ptr(dy_state), history_len, _ptr(workspace),
                                 workspace.numel() * workspace.element_size(), _ptr(dx), _ptr(dw),
                                 _stream(stream)))
+
+
+def fp8_linear_fwd_noalloc(x, w, y, bias=None, stream=None) -> None:
+    """Forward linear with current per-tensor scaling and no allocation: the
+    scratch is the library's static device array (see include/fp8sq.h)."""
+    M, K = x.shape
+    N = w.shape[0]
+    _check(lib().fp8_linear_fwd_noalloc(_ptr(x), _ptr(w), M, N, K, _ptr(bias), _ptr(y), _dtype_code(y),
+                                        _stream(stream)))
 
 
 def fp8_device_status(clear: bool = True) -> int:

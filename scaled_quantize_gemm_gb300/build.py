@@ -13,7 +13,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libfp8sq.so")
-SOURCES = ["quantize.cu", "gemm.cu", "api.cu"]
+SOURCES = ["quantize.cu", "gemm.cu", "api.cu", "noalloc.cu"]
 HEADERS = ["ptx.cuh", "internal.h", os.path.join("..", "..", "include", "fp8sq.h")]
 
 NVCC_FLAGS = [

@@ -111,6 +111,18 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int gran)
 
 }  // namespace
 
+namespace fp8sq {
+int api_fail(int code, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return code;
+}
+int api_check_device(int* sms) { return check_device(sms); }
+}  // namespace fp8sq
+
 extern "C" {
 
 FP8SQ_API int fp8_abi_version(void) { return 1; }

@@ -49,4 +49,8 @@ struct GemmArgs {
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char** why);
 int read_device_error(int clear);   // 0 or the device error word's value
 
+// api.cu: the calling thread's error message and the sm_103 device check
+int api_fail(int code, const char* fmt, ...);
+int api_check_device(int* sms);
+
 }  // namespace fp8sq
