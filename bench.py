@@ -334,7 +334,7 @@ def run_ours(args, ws, rank, local):
                          "frac": round(achieved / fp8_peak, 4), "traffic": None,
                          "peak_source": f"2 x bf16_tflops {peak_src} (dense FP8 = 2 x dense BF16)",
                          "flops_per_launch": gemm_flops_launch, "launch_ms": round(gemm_ms, 4)},
-            "roofline_quantize": {"bound": "hbm", "kernel": "k_cast_tensor_T (16384 x 14336 casts)",
+            "roofline_quantize": {"bound": "hbm", "kernel": "k_cast_T_tma (16384 x 14336 casts)",
                                   "achieved": round(big_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                                   "frac": round(big_gbs / hbm_peak, 4), "traffic": None,
                                   "peak_source": f"hbm_gbs {peak_src}",
@@ -439,8 +439,8 @@ def kernel_case(case: str, launches: int):
     """A handful of launches of one kernel at the workload's size, for
     profiling a single launch: 'gemm' = the 16384 x 14336 x 4096 forward GEMM
     (k_gemm_tensor), 'cast' = the 16384 x 14336 E5M2 cast with its transposed
-    copy (k_cast_tensor_T), 'promote' = the 4096^3 1x128 x 128x128 GEMM
-    (k_gemm_promote)."""
+    copy (k_cast_T_tma), 'promote' = the 4096^3 1x128 x 128x128 GEMM
+    (k_gemm_promote), 'mx' = the 8192^3 MX-32 GEMM (k_gemm_mx)."""
     import scaled_quantize_gemm_gb300 as sq
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -466,6 +466,17 @@ def kernel_case(case: str, launches: int):
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         for _ in range(launches):
             sq.fp8_gemm(qx, sq.E4M3, st[H + 1:], sq.TENSOR, qw, sq.E4M3, sw[H + 1:], sq.TENSOR, y)
+    elif case == "mx":
+        a, b = wl.w4_operands(dev)
+        qa, qb = torch.empty(a.shape, **u8), torch.empty(b.shape, **u8)
+        ea = torch.empty(a.numel() // 32, **u8)
+        eb = torch.empty(b.numel() // 32, **u8)
+        sq.fp8_quantize(a, sq.E4M3, sq.MX32_TILED, qa, scales_out=ea)
+        sq.fp8_quantize(b, sq.E4M3, sq.MX32_TILED, qb, scales_out=eb)
+        del a, b
+        y = torch.empty((8192, 8192), dtype=torch.bfloat16, device=dev)
+        for _ in range(launches):
+            sq.fp8_gemm(qa, sq.E4M3, ea, sq.MX32_TILED, qb, sq.E4M3, eb, sq.MX32_TILED, y)
     elif case == "promote":
         x, w = wl.w3_operands(dev)
         qx, qw = torch.empty(x.shape, **u8), torch.empty(w.shape, **u8)
@@ -484,7 +495,7 @@ def kernel_case(case: str, launches: int):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel-case", choices=["gemm", "cast", "promote"], default=None,
+    ap.add_argument("--kernel-case", choices=["gemm", "cast", "promote", "mx"], default=None,
                     help="run a few launches of one kernel (for profiling) and exit")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--gpus", type=int, default=1)

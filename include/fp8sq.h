@@ -75,6 +75,15 @@ extern "C" {
 #define FP8SQ_TILE_1x128 1     /* one scale per 128 consecutive values of a row */
 #define FP8SQ_BLOCK_128x128 2  /* one scale per 128x128 block                   */
 #define FP8SQ_MX32 3           /* one power-of-two (E8M0) scale per 32 values   */
+#define FP8SQ_MX32_TILED 4     /* MX32 with the scales in the GEMM's tiled layout */
+
+/* Tiled MX scale layout (FP8SQ_MX32_TILED), for a tensor [rows][cols] with
+ * rows % 128 == 0 and cols % 128 == 0: the E8M0 code of row r, 32-block
+ * t = c / 32 sits at byte
+ *     ((r / 128) * (cols / 128) + t / 4) * 512
+ *       + (r % 32) * 16 + ((r / 32) % 4) * 4 + (t % 4),
+ * i.e. 512-byte chunks of 128 rows x 4 consecutive 32-blocks (128 values
+ * along K), in the order the block-scaled tensor-core MMA reads them. */
 
 /* amax history reduction ([TE] amax_compute_algo) */
 #define FP8SQ_AMAX_MAX 0
@@ -144,7 +153,8 @@ FP8SQ_API int fp8_update_scale(float* states, int n_states, int history_len, con
  *       m = s = 1).
  *     TILE_1x128 / BLOCK_128x128: current scaling per unit, one pass;
  *       scales_out f32 [rows][cols/128] / [rows/128][cols/128] receives s.
- *     MX32: one pass; scales_out u8 [rows][cols/32] receives the E8M0 code
+ *     MX32 / MX32_TILED: one pass; scales_out u8 [rows][cols/32] (MX32) or
+ *       the tiled layout above (MX32_TILED) receives the E8M0 code
  *       e + 127 of the smallest power of two 2^e with amax <= fmax * 2^e
  *       (clamped to [-127, 127]; amax 0 -> 127; non-finite -> 0xFF with
  *       m = 1); m = 2^-e.
@@ -176,8 +186,11 @@ FP8SQ_API int fp8_quantize(const void* x, int x_dtype, int64_t rows, int64_t col
  *       [N/128][K/128]; partial sums over each 128-wide K block are promoted
  *       to fp32 registers with sA * sB ([W14] accumulation bullet:
  *       promotion to fp32 at fixed intervals); K % 128 == 0.
- *     (MX32, MX32): a_scale u8 E8M0 [M][K/32], b_scale u8 [N][K/32]
- *       (layout of fp8_quantize MX32); K % 128 == 0.
+ *     (MX32_TILED, MX32_TILED): a_scale, b_scale u8 E8M0 in the tiled
+ *       layout (as written by fp8_quantize MX32_TILED), 16-byte aligned;
+ *       D = sum_k dec(qA) 2^(eA - 127) dec(qB) 2^(eB - 127) on the
+ *       block-scaled tensor-core path ([W14] absmax bullet: every 32
+ *       numbers share a scale); M, N, K % 128 == 0.
  *   D  device [M][N], bf16 or f32, 16-byte aligned; bias device f32 [N] or NULL.
  *   Shapes: M >= 0, N % 8 == 0, K % 16 == 0 (TENSOR) / % 128 (others).
  *   K == 0 writes epi(0).
@@ -199,7 +212,8 @@ FP8SQ_API int fp8_gemm(const uint8_t* A, int a_format, const void* a_scale, int 
  *   The forward keeps the codes of x and W (and their transposes) in the
  *   workspace; the backward reads them and adds dy's codes.
  * gran TILE_1x128: x in 1x128 tiles, W in 128x128 blocks, current scaling,
- *   forward only.   gran MX32: x and W in MX-32 blocks, forward only.
+ *   forward only.   gran MX32: x and W in MX-32 blocks (tiled scales in the
+ *   workspace), forward only.
  * workspace: device, >= fp8_linear_workspace_bytes(M, N, K, gran), 256-byte
  *   aligned; the same workspace must be passed to the matching backward.
  * Shapes: M, N, K % 128 == 0 (TENSOR: M % 16, N % 16, K % 16).

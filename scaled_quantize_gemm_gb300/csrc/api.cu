@@ -64,7 +64,7 @@ int cuda_status(cudaError_t e, const char* what)
 
 bool valid_format(int f) { return f == FP8SQ_E4M3 || f == FP8SQ_E5M2; }
 bool valid_dtype(int d) { return d == FP8SQ_BF16 || d == FP8SQ_F32; }
-bool valid_gran(int g) { return g >= FP8SQ_TENSOR && g <= FP8SQ_MX32; }
+bool valid_gran(int g) { return g >= FP8SQ_TENSOR && g <= FP8SQ_MX32_TILED; }
 
 const int64_t kMaxDim = (int64_t)1 << 31;  // GEMM / TMA coordinates are 32-bit
 
@@ -77,6 +77,8 @@ int check_units(int gran, int64_t rows, int64_t cols)
         return fail(FP8SQ_ERR_UNSUPPORTED, "128x128 blocks need rows, cols %% 128 == 0 (%lld x %lld)", (long long)rows, (long long)cols);
     if (gran == FP8SQ_MX32 && cols % 32)
         return fail(FP8SQ_ERR_UNSUPPORTED, "MX-32 blocks need cols %% 32 == 0 (cols = %lld)", (long long)cols);
+    if (gran == FP8SQ_MX32_TILED && (rows % 128 || cols % 128))
+        return fail(FP8SQ_ERR_UNSUPPORTED, "tiled MX-32 scales need rows, cols %% 128 == 0 (%lld x %lld)", (long long)rows, (long long)cols);
     return FP8SQ_OK;
 }
 
@@ -132,6 +134,9 @@ FP8SQ_API const char* fp8_last_error(void) { return g_msg; }
 FP8SQ_API int fp8_device_status(int clear)
 {
     int v = fp8sq::read_device_error(clear);
+    int vq = fp8sq::read_device_error_quant(clear);
+    if (v >= 0 && vq < 0) v = vq;
+    else if (v == 0) v = vq;
     if (v < 0) return fail(FP8SQ_ERR_CUDA, "cannot read the device error word");
     if (v) return fail(FP8SQ_ERR_TIMEOUT, "a bounded device-side wait ran out");
     return FP8SQ_OK;
@@ -141,7 +146,8 @@ FP8SQ_API int fp8_amax(const void* x, int x_dtype, int64_t rows, int64_t cols, i
                        void* stream)
 {
     if ((!x && rows * cols != 0) || !amax_out) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_amax: null pointer");
-    if (!valid_dtype(x_dtype) || !valid_gran(gran)) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_amax: bad dtype or granularity");
+    if (!valid_dtype(x_dtype) || !valid_gran(gran) || gran == FP8SQ_MX32_TILED)
+        return fail(FP8SQ_ERR_INVALID_ARG, "fp8_amax: bad dtype or granularity");
     if (rows < 0 || cols < 0) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_amax: negative size");
     if (!aligned16(x)) return fail(FP8SQ_ERR_MISALIGNED, "fp8_amax: x must be 16-byte aligned");
     if (!aligned4(amax_out)) return fail(FP8SQ_ERR_MISALIGNED, "fp8_amax: amax_out must be 4-byte aligned");
@@ -269,8 +275,11 @@ static int validate_gemm(const uint8_t* A, int a_format, const void* a_scale, in
     } else if (a_gran == FP8SQ_TILE_1x128 && b_gran == FP8SQ_BLOCK_128x128) {
         if (K % 128) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_gemm: 1x128 x 128x128 scaling needs K %% 128 == 0");
         *mode = 1;
-    } else if (a_gran == FP8SQ_MX32 && b_gran == FP8SQ_MX32) {
-        if (K % 128) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_gemm: MX scaling needs K %% 128 == 0");
+    } else if (a_gran == FP8SQ_MX32_TILED && b_gran == FP8SQ_MX32_TILED) {
+        if (!aligned16(a_scale) || !aligned16(b_scale))
+            return fail(FP8SQ_ERR_MISALIGNED, "fp8_gemm: tiled MX scales must be 16-byte aligned");
+        if (M % 128 || N % 128 || K % 128)
+            return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_gemm: MX scaling needs M, N, K %% 128 == 0");
         *mode = 2;
     } else {
         return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_gemm: unsupported scale granularity pair (%d, %d)", a_gran, b_gran);
@@ -403,7 +412,7 @@ FP8SQ_API int fp8_linear_fwd(const void* x, const void* w, int64_t M, int64_t N,
         g.a_scale = ws + L.sx;
         g.b_scale = ws + L.sw;
     } else {
-        qa.x = x; qa.rows = M; qa.cols = K; qa.gran = fp8sq::kMX;
+        qa.x = x; qa.rows = M; qa.cols = K; qa.gran = fp8sq::kMXTiled;
         qa.q = ws + L.qx; qa.scales = ws + L.sx;
         if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: quantize x"))) return r;
         qa.x = w; qa.rows = N; qa.cols = K;

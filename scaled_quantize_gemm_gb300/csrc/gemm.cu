@@ -35,34 +35,10 @@ namespace fp8sq {
 
 __device__ int g_dev_error = 0;
 
-constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per wait
-constexpr uint64_t kDrainLimitNs = 100000000ull;   // 100 ms per drain wait
-
-// Wait for phase `parity` of `bar`; false if the wait ran out or another
-// wait of this library already failed (the error word is set).
+// Every wait of this file reports into g_dev_error.
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity)
 {
-    const uint32_t a = smem_addr(bar);
-    if (mbar_try_wait(a, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(a, parity)) return true;
-        if ((it & 255u) == 0u) {
-            if (*reinterpret_cast<volatile int*>(&g_dev_error)) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
-                atomicExch(&g_dev_error, 1);
-                return false;
-            }
-        }
-    }
-}
-// Drain wait used on the abort path: ignores the error word, short limit.
-__device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity)
-{
-    const uint32_t a = smem_addr(bar);
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(a, parity))
-        if (global_timer_ns() - t0 > kDrainLimitNs) return;
+    return wait_bounded_err(bar, parity, &g_dev_error);
 }
 
 struct TileSched {
@@ -455,6 +431,206 @@ __global__ void __launch_bounds__(320, 1)
     }
 }
 
+// ================================================================== mode 2
+// MX-32 block scaling on the block-scaled tensor-core path
+// (tcgen05.mma kind::mxf8f6f4.block_scale, E8M0 scale factors).  Each stage
+// carries, next to the A and B tiles, the 512-byte scale chunks of its 128
+// rows x 128 K (one per 128 rows of B), copied from global memory by bulk
+// copies (the chunks are contiguous in the tiled scale layout of
+// fp8_quantize) and into tensor memory by tcgen05.cp.32x128b.warpx4.  Every
+// ring stage has its own scale-factor columns, so a stage's columns are
+// rewritten only after the MMAs that read them have completed (their
+// commit released the stage).  MMA j (K = 32 slice j of the stage) selects
+// byte j of each scale word through the descriptor's scale-factor ids.
+template <int BN, int STAGES, int NACC>
+struct MxLayout {
+    static constexpr int CH = BN / 128;                  // 128-row scale chunks of B
+    static constexpr int B_BYTES = BN * BK;
+    static constexpr int STAGE = A_BYTES + B_BYTES;
+    static constexpr int SF_STAGE = 512 * (1 + CH);
+    static constexpr int SF_OFF = STAGES * STAGE;
+    static constexpr int BAR_OFF = SF_OFF + STAGES * SF_STAGE;
+    static constexpr int NBARS = 2 * STAGES + 2 * NACC + 1;
+    static constexpr int BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
+    static constexpr int SF_COL0 = NACC * BN;            // first scale-factor TMEM column
+    static constexpr int SF_COLS = 4 * (1 + CH);         // per stage
+    static_assert(SF_COL0 + STAGES * SF_COLS <= 512, "tensor memory budget");
+};
+
+// descriptor of a 32-row x 16-byte scale chunk in shared memory (rows
+// contiguous, no swizzle; 8-row groups 128 bytes apart)
+__device__ __forceinline__ uint64_t sdesc_sf_chunk(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)(128 >> 4) << 16;
+    d |= (uint64_t)(128 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+struct MxParams {
+    const uint8_t* sfa;   // tiled E8M0 scales of A
+    const uint8_t* sfb;   // tiled E8M0 scales of B
+    int kb128;            // K / 128
+    int nchunks_b;        // N / 128
+};
+
+template <int BN, int STAGES, int NACC, bool OUT_BF16>
+__global__ void __launch_bounds__(192, 1)
+    k_gemm_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, EpiParams p,
+              uint32_t idesc, TileSched sched, MxParams mx)
+{
+    using L = MxLayout<BN, STAGES, NACC>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+    uint64_t* empty = full + STAGES;
+    uint64_t* afull = empty + STAGES;
+    uint64_t* aempty = afull + NACC;
+    uint64_t* drain = aempty + NACC;
+    uint8_t* sf_smem = smem + L::SF_OFF;
+    constexpr uint32_t TMEM_COLS = 512;
+
+    uint32_t tmem_base;
+    if (!gemm_setup<STAGES, NACC, 4>(smem, L::BAR_OFF, TMEM_COLS, &tmA, &tmB, tmem_base)) return;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int num_tiles = sched.num_m * sched.num_n;
+    const int nkb = p.K / BK;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0, issued = 0;
+            uint32_t phase = 0;
+            bool aborted = false;
+            for (int t = blockIdx.x; t < num_tiles && !aborted; t += gridDim.x) {
+                int mb, nb;
+                sched.coords(t, mb, nb);
+                int nch = mx.nchunks_b - nb * L::CH;
+                nch = nch < L::CH ? nch : L::CH;
+                const uint32_t bytes = L::STAGE + 512u * (uint32_t)(1 + nch);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!wait_bounded(&empty[stage], phase ^ 1u)) {
+                        aborted = true;
+                        break;
+                    }
+                    uint8_t* sa = smem + stage * L::STAGE;
+                    uint8_t* sf = sf_smem + stage * L::SF_STAGE;
+                    mbar_arrive_expect_tx(&full[stage], bytes);
+                    tma_load_2d(sa, &tmA, kb * BK, mb * BM, &full[stage]);
+                    tma_load_2d(sa + A_BYTES, &tmB, kb * BK, nb * BN, &full[stage]);
+                    bulk_load_1d(sf, mx.sfa + ((int64_t)mb * mx.kb128 + kb) * 512, 512, &full[stage]);
+                    for (int c = 0; c < nch; ++c)
+                        bulk_load_1d(sf + 512 * (1 + c), mx.sfb + ((int64_t)(nb * L::CH + c) * mx.kb128 + kb) * 512,
+                                     512, &full[stage]);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (aborted) {
+                int n = issued < STAGES ? issued : STAGES;
+                int s = stage;
+                uint32_t ph = phase;
+                for (int i = 0; i < n; ++i) {
+                    if (--s < 0) {
+                        s = STAGES - 1;
+                        ph ^= 1u;
+                    }
+                    wait_drain(&full[s], ph);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0, lt = 0;
+            uint32_t phase = 0;
+            bool aborted = false;
+            for (int t = blockIdx.x; t < num_tiles && !aborted; t += gridDim.x, ++lt) {
+                const int b = lt % NACC;
+                const uint32_t u = (uint32_t)(lt / NACC);
+                if (!wait_bounded(&aempty[b], (u & 1u) ^ 1u)) {
+                    aborted = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(b * BN);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!wait_bounded(&full[stage], phase)) {
+                        aborted = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_addr(smem + stage * L::STAGE);
+                    const uint32_t sf = smem_addr(sf_smem + stage * L::SF_STAGE);
+                    const uint32_t sfa_t = tmem_base + (uint32_t)(L::SF_COL0 + stage * L::SF_COLS);
+                    const uint32_t sfb_t = sfa_t + 4;
+                    tmem_cp_32x128b_warpx4(sfa_t, sdesc_sf_chunk(sf));
+#pragma unroll
+                    for (int c = 0; c < L::CH; ++c) tmem_cp_32x128b_warpx4(sfb_t + 4 * c, sdesc_sf_chunk(sf + 512 * (1 + c)));
+                    const uint64_t da = sdesc_kmajor_sw128(sa);
+                    const uint64_t db = sdesc_kmajor_sw128(sa + A_BYTES);
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k)
+                        mma_mxf8f6f4(d, da + 2 * k, db + 2 * k, idesc | ((uint32_t)k << 29) | ((uint32_t)k << 4),
+                                     sfa_t, sfb_t, (kb | k) != 0 ? 1u : 0u);
+                    mma_commit(&empty[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!aborted) mma_commit(&afull[b]);
+            }
+            if (aborted) {
+                mma_commit(drain);
+                wait_drain(drain, 0);
+            }
+        }
+    } else {
+        const int quarter = warp & 3;
+        int lt = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++lt) {
+            const int b = lt % NACC;
+            const uint32_t u = (uint32_t)(lt / NACC);
+            const bool ok = wait_bounded(&afull[b], u & 1u);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            tc_fence_after();
+            int mb, nb;
+            sched.coords(t, mb, nb);
+            const int row = mb * BM + quarter * 32 + lane;
+            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * BN);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(taddr + (uint32_t)c, r);
+                tmem_ld_wait();
+                float v[32];
+                const int col0 = nb * BN + c;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                if (p.bias) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (col0 + j < p.N) v[j] += __ldg(p.bias + col0 + j);
+                }
+                store_row32<OUT_BF16>(p, row, col0, v);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&aempty[b]);
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
 // ================================================================== K == 0
 template <bool OUT_BF16>
 __global__ void k_fill_bias(void* D, int64_t M, int64_t N, const float* bias)
@@ -481,19 +657,26 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
-// 2-D u8 tensor [rows][inner] (inner contiguous), box box_rows x 128 bytes, 128-byte swizzle
-static bool make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows)
+bool encode_tmap_2d(CUtensorMap* m, int u16, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                    uint32_t box_rows)
 {
     auto fn = encode_fn();
     if (!fn) return false;
+    const uint64_t esz = u16 ? 2 : 1;
     cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {inner};
-    cuuint32_t box[2] = {128u, box_rows};
+    cuuint64_t strides[1] = {inner * esz};
+    cuuint32_t box[2] = {box_inner, box_rows};
     cuuint32_t estr[2] = {1u, 1u};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(m, u16 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr),
+                    dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// 2-D u8 tensor [rows][inner] (inner contiguous), box box_rows x 128 bytes, 128-byte swizzle
+static bool make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_rows)
+{
+    return encode_tmap_2d(m, 0, ptr, inner, rows, 128u, box_rows);
 }
 
 // instruction descriptor, kind::f8f6f4: D fp32, A/B format, both K-major, N, M = 128
@@ -505,6 +688,20 @@ static uint32_t make_idesc(int a_fmt, int b_fmt, int n)
     d |= (uint32_t)b_fmt << 10;
     d |= (uint32_t)(n >> 3) << 17;      // N / 8
     d |= (uint32_t)(BM >> 4) << 24;     // M / 16
+    return d;
+}
+
+// instruction descriptor, kind::mxf8f6f4.block_scale: A/B format, both
+// K-major, N, E8M0 scale factors, M = 128; the scale-factor byte ids
+// (bits 4-5 for B, 29-30 for A) are or-ed in per MMA
+static uint32_t make_idesc_mx(int a_fmt, int b_fmt, int n)
+{
+    uint32_t d = 0;
+    d |= (uint32_t)a_fmt << 7;
+    d |= (uint32_t)b_fmt << 10;
+    d |= (uint32_t)(n >> 3) << 17;
+    d |= 1u << 23;                      // scale factors: UE8M0
+    d |= (uint32_t)(BM >> 4) << 24;
     return d;
 }
 
@@ -567,6 +764,25 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
         if (bf16)
             return launch_persistent(k_gemm_promote<ST, true>, 320, smem, tiles, sms, st, ta, tb, p, idesc, sched);
         return launch_persistent(k_gemm_promote<ST, false>, 320, smem, tiles, sms, st, ta, tb, p, idesc, sched);
+    }
+    if (g.mode == 2) {
+        constexpr int BN = 256, ST = 4, NACC = 1;
+        using L = MxLayout<BN, ST, NACC>;
+        if (!make_tmap(&ta, g.A, g.K, g.M, BM) || !make_tmap(&tb, g.B, g.K, g.N, BN)) {
+            *why = "cuTensorMapEncodeTiled failed";
+            return cudaErrorInvalidValue;
+        }
+        TileSched sched{(int)(g.M / BM), (int)((g.N + BN - 1) / BN), 16};
+        const int tiles = sched.num_m * sched.num_n;
+        MxParams mx{static_cast<const uint8_t*>(g.a_scale), static_cast<const uint8_t*>(g.b_scale), (int)(g.K / 128),
+                    (int)(g.N / 128)};
+        const uint32_t idesc = make_idesc_mx(g.a_format, g.b_format, BN);
+        auto kern = bf16 ? k_gemm_mx<BN, ST, NACC, true> : k_gemm_mx<BN, ST, NACC, false>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
+        if (e != cudaSuccess) return e;
+        const int grid = tiles < sms ? tiles : sms;
+        kern<<<grid, 192, L::BYTES, st>>>(ta, tb, p, idesc, sched, mx);
+        return cudaGetLastError();
     }
     *why = "GEMM mode not built";
     return cudaErrorNotSupported;

@@ -2,13 +2,14 @@
 // (api.cu) and the kernel translation units.  Not installed, not part of the ABI.
 #pragma once
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace fp8sq {
 
 enum { kE4M3 = 0, kE5M2 = 1 };
 enum { kBF16 = 0, kF32 = 1 };
-enum { kTensor = 0, kTile = 1, kBlock = 2, kMX = 3 };
+enum { kTensor = 0, kTile = 1, kBlock = 2, kMX = 3, kMXTiled = 4 };
 
 struct QuantArgs {
     const void* x = nullptr;
@@ -36,7 +37,7 @@ struct GemmArgs {
     const uint8_t* A = nullptr;
     const uint8_t* B = nullptr;
     int a_format = kE4M3, b_format = kE4M3;
-    int mode = 0;                    // 0 per-tensor, 1 tile x block promotion, 2 MX
+    int mode = 0;                    // 0 per-tensor, 1 tile x block promotion, 2 MX (tiled E8M0 scales)
     const void* a_scale = nullptr;
     const void* b_scale = nullptr;
     int64_t M = 0, N = 0, K = 0;
@@ -47,7 +48,14 @@ struct GemmArgs {
 
 // gemm.cu
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char** why);
-int read_device_error(int clear);   // 0 or the device error word's value
+int read_device_error(int clear);   // 0 or the GEMM kernels' device error word
+// 2-D tiled TMA map, 128-byte swizzle, zero fill out of bounds; u16 selects
+// 2-byte elements (else 1-byte)
+bool encode_tmap_2d(CUtensorMap* m, int u16, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                    uint32_t box_rows);
+
+// quantize.cu
+int read_device_error_quant(int clear);   // 0 or the cast kernels' device error word
 
 // api.cu: the calling thread's error message and the sm_103 device check
 int api_fail(int code, const char* fmt, ...);

@@ -75,6 +75,34 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
+// Wait for phase `parity` of `bar` for at most ~1 s.  `err` is a device
+// error word: false is returned (and *err set) when the wait runs out, and
+// also as soon as some other wait has set *err.
+__device__ __forceinline__ bool wait_bounded_err(uint64_t* bar, uint32_t parity, int* err)
+{
+    const uint32_t a = smem_addr(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(a, parity)) return true;
+        if ((it & 255u) == 0u) {
+            if (*reinterpret_cast<volatile int*>(err)) return false;
+            if (global_timer_ns() - t0 > 1000000000ull) {
+                atomicExch(err, 1);
+                return false;
+            }
+        }
+    }
+}
+// Drain wait on the abort path: ignores the error word, 100 ms limit.
+__device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity)
+{
+    const uint32_t a = smem_addr(bar);
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(a, parity))
+        if (global_timer_ns() - t0 > 100000000ull) return;
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m)
 {
@@ -143,7 +171,7 @@ __device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, u
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
             d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");

@@ -373,15 +373,184 @@ __global__ void __launch_bounds__(256) k_cast_tensor_T(const void* __restrict__ 
     }
 }
 
+// ================================================================== per-tensor, TMA-fed
+// The per-tensor cast with a transposed copy for bf16 inputs, as a persistent
+// pipeline: one CTA per SM; warp 8 streams 128x128 bf16 tiles into a
+// 6-stage shared-memory ring with TMA (two 64-column boxes per tile, 128-byte
+// swizzle, zero fill past the edges); warps 0..7 each take a 32-row x 64-column
+// quarter of a tile, eight rows x 8 columns per thread.  Lane (cg = lane % 8,
+// rg = lane / 8) reads 16-byte chunk cg of its rows, so the eight lanes of a
+// shared-memory phase hit eight different swizzled chunks (no bank
+// conflicts), and every code store (q rows, qT rows) covers whole 32-byte
+// sectors.  The amax is combined over the CTA's whole share of tiles and
+// reaches global memory with one atomic per CTA.
+__device__ int g_dev_error_q = 0;
+
+constexpr int kTStages = 6;
+constexpr int kTTile = 128 * 128 * 2;
+constexpr int kTThreads = 288;
+constexpr int kTSmem = kTStages * kTTile + 2 * kTStages * 8 + 1024;
+
+template <int FMT, bool DELAYED>
+__global__ void __launch_bounds__(kTThreads, 1)
+    k_cast_T_tma(const __grid_constant__ CUtensorMap tmX, int64_t R, int64_t C, uint8_t* __restrict__ q,
+                 uint8_t* __restrict__ qT, float* state, int H, const float* amax_in, float* s_out, float* amax_out,
+                 unsigned long long* sat)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTStages * kTTile);
+    uint64_t* empty = full + kTStages;
+    __shared__ uint32_t red[8];
+    __shared__ int s_skip;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tiles_c = (int)((C + 127) / 128);
+    const int ntiles = tiles_c * (int)((R + 127) / 128);
+    if (threadIdx.x == 0) {
+        s_skip = *reinterpret_cast<volatile int*>(&g_dev_error_q);
+        for (int i = 0; i < kTStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 8);
+        }
+        fence_mbar_init();
+        prefetch_tmap(&tmX);
+    }
+    __syncthreads();
+    if (s_skip) return;
+    uint32_t mx = 0, nsat = 0;
+    if (warp == 8) {
+        if (lane == 0) {
+            int stage = 0, issued = 0;
+            uint32_t phase = 0;
+            bool aborted = false;
+            for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+                if (!wait_bounded_err(&empty[stage], phase ^ 1u, &g_dev_error_q)) {
+                    aborted = true;
+                    break;
+                }
+                const int c0 = (t % tiles_c) * 128, r0 = (t / tiles_c) * 128;
+                uint8_t* dst = smem + stage * kTTile;
+                mbar_arrive_expect_tx(&full[stage], kTTile);
+                tma_load_2d(dst, &tmX, c0, r0, &full[stage]);
+                tma_load_2d(dst + kTTile / 2, &tmX, c0 + 64, r0, &full[stage]);
+                ++issued;
+                if (++stage == kTStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (aborted) {
+                int n = issued < kTStages ? issued : kTStages;
+                int st = stage;
+                uint32_t ph = phase;
+                for (int i = 0; i < n; ++i) {
+                    if (--st < 0) {
+                        st = kTStages - 1;
+                        ph ^= 1u;
+                    }
+                    wait_drain(&full[st], ph);
+                }
+            }
+        }
+    } else {
+        float m, s;
+        if (DELAYED) {
+            m = state[H];
+            s = 0.0f;
+        } else {
+            current_scale<FMT>(__float_as_uint(*amax_in), m, s);
+            if (blockIdx.x == 0 && threadIdx.x == 0 && s_out) *s_out = s;
+        }
+        const int h = warp >> 2, cg = lane & 7;
+        const int rloc = (warp & 3) * 32 + (lane >> 3) * 8;
+        const int cloc = h * 64 + cg * 8;
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+            const bool ok = wait_bounded_err(&full[stage], phase, &g_dev_error_q);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            const uint8_t* half = smem + stage * kTTile + h * (kTTile / 2);
+            Vec8<kBF16> v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = rloc + i;
+                v[i].w = *reinterpret_cast<const uint4*>(half + r * 128 + ((cg ^ (r & 7)) << 4));
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+            if (++stage == kTStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+            const int64_t r0 = (int64_t)(t / tiles_c) * 128 + rloc;
+            const int64_t c0 = (int64_t)(t % tiles_c) * 128 + cloc;
+            uint2 rows[8];
+            uint32_t ns = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (DELAYED) mx = max(mx, v[i].absmax_bits());
+                float f[8];
+                v[i].get(f);
+                rows[i] = cast8<FMT>(f, m, ns);
+            }
+            if (r0 < R && c0 < C) {
+                nsat += ns;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(q + (r0 + i) * C + c0) = rows[i];
+                uint2 cols[8];
+                transpose8x8(rows, cols);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) *reinterpret_cast<uint2*>(qT + (c0 + j) * R + r0) = cols[j];
+            }
+        }
+        if (sat) add_sat(sat, nsat);
+        if (DELAYED) {
+            mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+            if (lane == 0) red[warp] = mx;
+        }
+    }
+    __syncthreads();
+    if (DELAYED && threadIdx.x == 0) {
+        uint32_t r = red[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) r = max(r, red[i]);
+        atomic_max_bits(&state[0], r);
+        if (amax_out) atomic_max_bits(amax_out, r);
+    }
+}
+
+int read_device_error_quant(int clear)
+{
+    int v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+    if (cudaMemcpyFromSymbol(&v, g_dev_error_q, sizeof(int)) != cudaSuccess) return -1;
+    if (clear) {
+        int z = 0;
+        if (cudaMemcpyToSymbol(g_dev_error_q, &z, sizeof(int)) != cudaSuccess) return -1;
+    }
+    return v;
+}
+
 // ================================================================== row units
 // 1x128 tiles (UNIT = 128) and MX-32 blocks (UNIT = 32): a unit is UNIT/8
 // consecutive lanes, each holding one 128-bit chunk; units never straddle a
 // row because cols % UNIT == 0, so the tensor is treated as flat.
 // WRITE_Q = false computes the unit amaxes only (fp8_amax).
-template <int DT, int FMT, int UNIT, bool WRITE_Q>
+// MX scales: the canonical layout is u8 [rows][cols/32]; the tiled layout
+// (TILED = true) is the one the block-scaled GEMM copies straight into tensor
+// memory: 512-byte chunks of 128 rows x 4 consecutive 32-blocks, chunk
+// (r/128, t/4) at ((r/128) * (cols/128) + t/4) * 512, inside it
+// (r % 32) * 16 + ((r / 32) % 4) * 4 + t % 4.
+__device__ __forceinline__ int64_t mx_tiled_offset(int64_t r, int64_t t, int64_t cols)
+{
+    return ((r >> 7) * (cols >> 7) + (t >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (t & 3);
+}
+
+template <int DT, int FMT, int UNIT, bool WRITE_Q, bool TILED = false>
 __global__ void __launch_bounds__(kFlatThreads) k_quant_rowunits(const void* __restrict__ x, int64_t n,
                                                                  uint8_t* __restrict__ q, void* scales,
-                                                                 float* amax_out, unsigned long long* sat)
+                                                                 float* amax_out, unsigned long long* sat,
+                                                                 int64_t cols = 0)
 {
     constexpr int TPU = UNIT / 8;  // lanes per unit
     const int64_t nch = n / 8;
@@ -417,7 +586,10 @@ __global__ void __launch_bounds__(kFlatThreads) k_quant_rowunits(const void* __r
                     nsat += ns;
                     *reinterpret_cast<uint2*>(q + c * 8) = codes;
                     if (leader) {
-                        if (UNIT == 32) static_cast<uint8_t*>(scales)[unit] = (uint8_t)code;
+                        if (UNIT == 32 && TILED)
+                            static_cast<uint8_t*>(scales)[mx_tiled_offset(unit / (cols / 32), unit % (cols / 32), cols)] =
+                                (uint8_t)code;
+                        else if (UNIT == 32) static_cast<uint8_t*>(scales)[unit] = (uint8_t)code;
                         else static_cast<float*>(scales)[unit] = s;
                     }
                 }
@@ -551,6 +723,20 @@ static cudaError_t quant_dt_fmt(const QuantArgs& a, cudaStream_t st, int sms)
             if (cudaMemsetAsync(a.amax, 0, sizeof(float), st) != cudaSuccess) return cudaGetLastError();
         }
         float* s_out = static_cast<float*>(a.scales);
+        if (a.qT && DT == kBF16 && n > 0) {
+            CUtensorMap tm;
+            if (!encode_tmap_2d(&tm, 1, a.x, (uint64_t)a.cols, (uint64_t)a.rows, 64u, 128u)) return cudaErrorInvalidValue;
+            const int64_t tiles = ((a.rows + 127) / 128) * ((a.cols + 127) / 128);
+            const int grid = (int)(tiles < sms ? tiles : sms);
+            auto kern = delayed ? k_cast_T_tma<FMT, true> : k_cast_T_tma<FMT, false>;
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
+            if (e != cudaSuccess) return e;
+            if (delayed)
+                kern<<<grid, kTThreads, kTSmem, st>>>(tm, a.rows, a.cols, a.q, a.qT, a.state, H, nullptr, nullptr, a.amax, a.sat);
+            else
+                kern<<<grid, kTThreads, kTSmem, st>>>(tm, a.rows, a.cols, a.q, a.qT, nullptr, 0, a.amax, s_out, nullptr, a.sat);
+            return cudaGetLastError();
+        }
         if (a.qT) {
             if (n == 0) {
                 if (!delayed) k_cast_tensor<DT, FMT, false><<<1, kFlatThreads, 0, st>>>(a.x, 0, a.q, nullptr, 0, a.amax, s_out, nullptr, nullptr);
@@ -577,6 +763,9 @@ static cudaError_t quant_dt_fmt(const QuantArgs& a, cudaStream_t st, int sms)
         break;
     case kMX:
         k_quant_rowunits<DT, FMT, 32, true><<<flat_grid(n / 8, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat);
+        break;
+    case kMXTiled:
+        k_quant_rowunits<DT, FMT, 32, true, true><<<flat_grid(n / 8, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
         break;
     case kBlock:
         k_quant_block128<DT, FMT, true><<<dim3((unsigned)(a.cols / 128), (unsigned)(a.rows / 128)), 256, 0, st>>>(a.x, a.rows, a.cols, a.q, static_cast<float*>(a.scales), a.amax, a.sat);

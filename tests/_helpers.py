@@ -57,3 +57,12 @@ def nan_aware_codes_equal(gpu: np.ndarray, ref: np.ndarray, fmt: int) -> bool:
     if not np.array_equal(g_nan, r_nan):
         return False
     return bool(np.array_equal(gpu[~g_nan], ref[~r_nan]))
+
+
+def mx_untile(tiled: np.ndarray, R: int, C: int) -> np.ndarray:
+    """Tiled MX scale layout (include/fp8sq.h, FP8SQ_MX32_TILED) -> the
+    canonical [R][C/32] layout, by the header's index formula."""
+    r = np.arange(R)[:, None]
+    t = np.arange(C // 32)[None, :]
+    off = ((r // 128) * (C // 128) + t // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (t % 4)
+    return np.asarray(tiled).reshape(-1)[off]

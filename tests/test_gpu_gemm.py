@@ -187,3 +187,97 @@ def test_w5_forward_gemm_full_size_sampled_rows():
     ah = o.dequantize(codes(qx[rows]), 0, 0, sx.item())
     bh = o.dequantize(codes(qw), 0, 0, sw.item())
     assert_gemm_close(D[rows], o.gemm_ref(ah, bh))
+
+
+# ---------------------------------------------------------------- MX-32 block scaling
+def _quant_mx(x):
+    R, C = x.shape
+    q = torch.empty((R, C), dtype=torch.uint8, device=DEV)
+    e = torch.empty(R * C // 32, dtype=torch.uint8, device=DEV)
+    sq.fp8_quantize(x.to(DEV), sq.E4M3, sq.MX32_TILED, q, scales_out=e)
+    return q, e
+
+
+def _mx_gemm(qa, ea, qb, eb, out):
+    D = torch.empty((qa.shape[0], qb.shape[0]), dtype=out, device=DEV)
+    sq.fp8_gemm(qa, sq.E4M3, ea, sq.MX32_TILED, qb, sq.E4M3, eb, sq.MX32_TILED, D)
+    torch.cuda.synchronize()
+    return D
+
+
+def test_mx_unit_scales_integer_exact():
+    """E8M0 code 127 (= 1.0) everywhere and small-integer codes: the
+    block-scaled MMA must reproduce the int64 product exactly."""
+    rng = np.random.default_rng(7)
+    M, N, K = 256, 384, 512
+    va, qa = _int_codes(rng, (M, K), o.E4M3, -8, 8)
+    vb, qb = _int_codes(rng, (N, K), o.E4M3, -8, 8)
+    ea = torch.full((M * K // 32,), 127, dtype=torch.uint8, device=DEV)
+    eb = torch.full((N * K // 32,), 127, dtype=torch.uint8, device=DEV)
+    D = _mx_gemm(torch.from_numpy(qa).to(DEV), ea, torch.from_numpy(qb).to(DEV), eb, torch.float32)
+    assert np.array_equal(D.cpu().numpy(), (va.astype(np.int64) @ vb.astype(np.int64).T).astype(np.float32))
+
+
+def test_mx_power_of_two_scales_select_the_right_block():
+    """One non-unit scale per operand at a time: a 2^k on row r, 32-block t of
+    A must scale exactly the products of that block (checks the scale
+    factors' row and K placement in tensor memory, and the per-MMA byte id)."""
+    from _helpers import mx_untile
+    rng = np.random.default_rng(8)
+    M, N, K = 256, 256, 256
+    va, qa = _int_codes(rng, (M, K), o.E4M3, -4, 4)
+    vb, qb = _int_codes(rng, (N, K), o.E4M3, -4, 4)
+    ta = np.full((M, K // 32), 127, np.uint8)
+    tb = np.full((N, K // 32), 127, np.uint8)
+    ta[37, 5] = 129      # x4
+    ta[200, 0] = 126     # x0.5
+    ta[99, 7] = 130      # x8
+    tb[150, 3] = 128     # x2
+    tb[3, 6] = 125       # x0.25
+
+    def tile(can, R, C):
+        out = np.zeros(R * C // 32, np.uint8)
+        r = np.arange(R)[:, None]
+        t = np.arange(C // 32)[None, :]
+        off = ((r // 128) * (C // 128) + t // 4) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + (t % 4)
+        out[off] = can
+        assert np.array_equal(mx_untile(out, R, C), can)
+        return out
+
+    ea = torch.from_numpy(tile(ta, M, K)).to(DEV)
+    eb = torch.from_numpy(tile(tb, N, K)).to(DEV)
+    D = _mx_gemm(torch.from_numpy(qa).to(DEV), ea, torch.from_numpy(qb).to(DEV), eb, torch.float32)
+    ah = va * np.repeat(2.0 ** (ta.astype(np.float64) - 127), 32, axis=1)
+    bh = vb * np.repeat(2.0 ** (tb.astype(np.float64) - 127), 32, axis=1)
+    assert np.array_equal(D.cpu().numpy().astype(np.float64), ah @ bh.T)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 384, 512), (384, 256, 1024)])
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+def test_mx_vs_oracle(M, N, K, out):
+    from _helpers import mx_untile
+    a = wl.with_scaled_fraction((M, K), 1e-3, 100.0, 41 + M)
+    b = wl.with_scaled_fraction((N, K), 1e-3, 100.0, 42 + N)
+    qa, ea = _quant_mx(a)
+    qb, eb = _quant_mx(b)
+    D = _mx_gemm(qa, ea, qb, eb, out)
+    R = o.gemm_ref(o.dequantize(codes(qa), 0, o.GRAN_MX32, mx_untile(ea.cpu().numpy(), M, K)),
+                   o.dequantize(codes(qb), 0, o.GRAN_MX32, mx_untile(eb.cpu().numpy(), N, K)))
+    assert_gemm_close(D, R)
+
+
+def test_w4_mx_full_size_sampled_rows():
+    """Workload 4 at full size: A, B 8192 x 8192 with 0.1 % of entries x100,
+    MX-32 E4M3, bf16 out; 128 sampled rows against the oracle."""
+    from _helpers import mx_untile
+    a, b = wl.w4_operands(DEV)
+    qa, ea = _quant_mx(a)
+    qb, eb = _quant_mx(b)
+    del a, b
+    D = _mx_gemm(qa, ea, qb, eb, torch.bfloat16)
+    rows = _sample_rows(8192, 128, 9)
+    ea_c = mx_untile(ea.cpu().numpy(), 8192, 8192)
+    eb_c = mx_untile(eb.cpu().numpy(), 8192, 8192)
+    ah = o.dequantize(codes(qa[rows]), 0, o.GRAN_MX32, ea_c[rows])
+    bh = o.dequantize(codes(qb), 0, o.GRAN_MX32, eb_c)
+    assert_gemm_close(D[rows], o.gemm_ref(ah, bh))

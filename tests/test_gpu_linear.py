@@ -167,3 +167,17 @@ def test_w5_ffn_step_full_size():
         torch.cuda.synchronize()
         for li in range(2):
             assert layers[li].states.cpu().numpy().tobytes() == np.concatenate(refs[li]).tobytes(), (step, li)
+
+
+def test_mx_linear_forward():
+    M, K, N = 256, 512, 384
+    x = wl.with_scaled_fraction((M, K), 1e-3, 100.0, 6).to(DEV)
+    w = wl.normal((N, K), 0.02, 7).to(DEV)
+    ws = torch.empty(sq.fp8_linear_workspace_bytes(M, N, K, sq.MX32), dtype=torch.uint8, device=DEV)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    sq.fp8_linear_fwd(x, w, y, ws, gran=sq.MX32)
+    torch.cuda.synchronize()
+    qx, ex, _, _ = o.quantize_mx32(np32(x), o.E4M3)
+    qw, ew, _, _ = o.quantize_mx32(np32(w), o.E4M3)
+    R = o.gemm_ref(o.dequantize(qx, 0, o.GRAN_MX32, ex), o.dequantize(qw, 0, o.GRAN_MX32, ew))
+    assert_gemm_close(y, R)

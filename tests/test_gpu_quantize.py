@@ -258,3 +258,18 @@ def test_w5_largest_cast_full_size():
     gqt = codes(qT)
     assert np.array_equal(gqt, rq.T)
     assert st.cpu().numpy().tobytes() == ref_state.tobytes()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape", [(128, 128), (384, 512)])
+def test_mx32_tiled_scales(fmt, shape):
+    from _helpers import mx_untile
+    R, C = shape
+    x = wl.with_scaled_fraction(shape, 0.01, 100.0, 31 + R)
+    q = _u8(shape)
+    e = _u8(R * C // 32)
+    sq.fp8_quantize(x.to(DEV), fmt, sq.MX32_TILED, q, scales_out=e)
+    torch.cuda.synchronize()
+    rq, re, _, _ = o.quantize_mx32(np32(x), fmt)
+    assert np.array_equal(codes(q), rq)
+    assert np.array_equal(mx_untile(e.cpu().numpy(), R, C), re)
