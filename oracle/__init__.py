@@ -35,6 +35,7 @@ import numpy as np
 E4M3, E5M2 = 0, 1
 ALGO_MAX, ALGO_MOST_RECENT = 0, 1
 GRAN_TENSOR, GRAN_TILE_1x128, GRAN_BLOCK_128x128, GRAN_MX32 = 0, 1, 2, 3
+GRAN_TILE_128x1, GRAN_MX32_COL = 4, 5   # column units (128 or 32 consecutive rows of a column)
 FMAX = {E4M3: 448.0, E5M2: 57344.0}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -79,6 +80,8 @@ def _load():
                 "orc_quantize_tile1x128": (c.c_int64, [P, c.c_int64, c.c_int64, c.c_int, P, P, P]),
                 "orc_quantize_block128": (c.c_int64, [P, c.c_int64, c.c_int64, c.c_int, P, P, P]),
                 "orc_mx_scale_code": (c.c_uint8, [c.c_float, c.c_int]),
+                "orc_quantize_tile128x1": (c.c_int64, [P, c.c_int64, c.c_int64, c.c_int, P, P, P]),
+                "orc_quantize_mx32_col": (c.c_int64, [P, c.c_int64, c.c_int64, c.c_int, P, P, P]),
                 "orc_quantize_mx32": (c.c_int64, [P, c.c_int64, c.c_int64, c.c_int, P, P, P]),
                 "orc_state_init": (None, [P, c.c_int]),
                 "orc_quantize_delayed": (c.c_int64, [P, c.c_int64, c.c_int, P, c.c_int, P]),
@@ -225,6 +228,30 @@ def quantize_mx32(x, fmt: int):
     return q, e, am, int(sat)
 
 
+def quantize_tile128x1(x, fmt: int):
+    """column tiles: x[R][C], R % 128 == 0 -> (q [R][C], s[R/128][C], amax, n_sat)"""
+    a = _f32(x)
+    R, C = a.shape
+    assert R % 128 == 0
+    q = np.empty((R, C), dtype=np.uint8)
+    s = np.empty((R // 128, C), dtype=np.float32)
+    am = np.empty((R // 128, C), dtype=np.float32)
+    sat = _load().orc_quantize_tile128x1(_p(a), R, C, fmt, _p(q), _p(s), _p(am))
+    return q, s, am, int(sat)
+
+
+def quantize_mx32_col(x, fmt: int):
+    """column MX blocks: x[R][C], R % 32 == 0 -> (q [R][C], e8m0 [R/32][C], amax, n_sat)"""
+    a = _f32(x)
+    R, C = a.shape
+    assert R % 32 == 0
+    q = np.empty((R, C), dtype=np.uint8)
+    e = np.empty((R // 32, C), dtype=np.uint8)
+    am = np.empty((R // 32, C), dtype=np.float32)
+    sat = _load().orc_quantize_mx32_col(_p(a), R, C, fmt, _p(q), _p(e), _p(am))
+    return q, e, am, int(sat)
+
+
 # ---------------------------------------------------------------- delayed state
 def state_init(H: int) -> np.ndarray:
     st = np.empty(H + 2, dtype=np.float32)
@@ -251,7 +278,7 @@ def update_scale(state: np.ndarray, fmt: int, algo: int = ALGO_MAX) -> None:
 def dequantize(q: np.ndarray, fmt: int, gran: int, scales) -> np.ndarray:
     q = np.ascontiguousarray(q, dtype=np.uint8)
     R, C = q.shape
-    if gran == GRAN_MX32:
+    if gran in (GRAN_MX32, GRAN_MX32_COL):
         sc = np.ascontiguousarray(scales, dtype=np.uint8)
     else:
         sc = np.ascontiguousarray(np.atleast_1d(np.asarray(scales, dtype=np.float32)))
@@ -309,6 +336,46 @@ def linear_bwd_delayed(dy, dy_state, dy_fmt, qx, sx, qw, sw, rows=None, wrows=No
     at = dyh.T if wrows is None else dyh.T[wrows]
     dW = gemm_ref(at, xh.T)
     return qdy, sdy, dX, dW
+
+
+# Fine-grained scaling ("Week 14", absmax bullet: 1x128 activation tiles and
+# 128x128 weight blocks, as in DeepSeek-V3; MX blocks of 32).  Each GEMM
+# operand is quantised along that GEMM's contraction dimension: the forward
+# contracts over K (x rows, W rows), dgrad over N (dy rows; W's columns: the
+# 128x128 blocks of W^T are W's blocks transposed, and MX W is re-quantised
+# in column blocks), wgrad over the tokens M (dy and x in column units).
+def linear_fine_fwd(x, w, gran: int):
+    """gran GRAN_TILE_1x128 (x tiles, W blocks) or GRAN_MX32 -> (state, R) with
+    state holding what the backward needs (the forward's W codes / scales)."""
+    if gran == GRAN_TILE_1x128:
+        qx, sx, _, _ = quantize_tile1x128(x, E4M3)
+        qw, sw, _, _ = quantize_block128(w, E4M3)
+        r = gemm_ref(dequantize(qx, E4M3, GRAN_TILE_1x128, sx), dequantize(qw, E4M3, GRAN_BLOCK_128x128, sw))
+        return {"x": x, "qw": qw, "sw": sw, "w": w}, r
+    qx, ex, _, _ = quantize_mx32(x, E4M3)
+    qw, ew, _, _ = quantize_mx32(w, E4M3)
+    r = gemm_ref(dequantize(qx, E4M3, GRAN_MX32, ex), dequantize(qw, E4M3, GRAN_MX32, ew))
+    return {"x": x, "w": w}, r
+
+
+def linear_fine_bwd(st, dy, gran: int, dy_fmt: int = E4M3):
+    """-> (dX, dW) float64 for the fine-grained recipes."""
+    x, w = st["x"], st["w"]
+    if gran == GRAN_TILE_1x128:
+        qd, sd, _, _ = quantize_tile1x128(dy, dy_fmt)                      # along N
+        wh = dequantize(st["qw"], E4M3, GRAN_BLOCK_128x128, st["sw"])       # blocks, same codes
+        dX = gemm_ref(dequantize(qd, dy_fmt, GRAN_TILE_1x128, sd), wh.T)
+        qdc, sdc, _, _ = quantize_tile128x1(dy, dy_fmt)                    # along M
+        qxc, sxc, _, _ = quantize_tile128x1(x, E4M3)
+        dW = gemm_ref(dequantize(qdc, dy_fmt, GRAN_TILE_128x1, sdc).T, dequantize(qxc, E4M3, GRAN_TILE_128x1, sxc).T)
+        return dX, dW
+    qd, ed, _, _ = quantize_mx32(dy, dy_fmt)                               # along N
+    qwc, ewc, _, _ = quantize_mx32_col(w, E4M3)                            # W along N
+    dX = gemm_ref(dequantize(qd, dy_fmt, GRAN_MX32, ed), dequantize(qwc, E4M3, GRAN_MX32_COL, ewc).T)
+    qdc, edc, _, _ = quantize_mx32_col(dy, dy_fmt)                         # along M
+    qxc, exc, _, _ = quantize_mx32_col(x, E4M3)
+    dW = gemm_ref(dequantize(qdc, dy_fmt, GRAN_MX32_COL, edc).T, dequantize(qxc, E4M3, GRAN_MX32_COL, exc).T)
+    return dX, dW
 
 
 # ---------------------------------------------------------------- worked-example helpers

@@ -285,6 +285,55 @@ int64_t orc_quantize_mx32(const float* x, int64_t R, int64_t C, int fmt, uint8_t
 }
 
 /* ------------------------------------------------------------------------
+ * 7b. Column units, for the backward products that contract over the other
+ * dimension (dgrad over the output features, wgrad over the tokens): the
+ * same 1x128 / MX-32 rules applied to 128 (or 32) consecutive values of a
+ * COLUMN of x[R][C].  By definition these are the row units of x^T.
+ *   tile128x1: s[R/128][C] (column c, row block rb at rb*C + c)
+ *   mx32_col:  e8m0[R/32][C]
+ * Codes keep x's layout: q[r][c].
+ * ---------------------------------------------------------------------- */
+int64_t orc_quantize_tile128x1(const float* x, int64_t R, int64_t C, int fmt, uint8_t* q,
+                               float* s_out, float* amax_out)
+{
+    int64_t RB = R / 128, sat = 0;
+    #pragma omp parallel for reduction(+:sat) schedule(static)
+    for (int64_t c = 0; c < C; ++c) {
+        for (int64_t rb = 0; rb < RB; ++rb) {
+            float a = 0.0f;
+            for (int64_t r = rb * 128; r < rb * 128 + 128; ++r)
+                a = amax2(a, fabsf(x[r * C + c]));
+            float m, s;
+            orc_current_scale(a, fmt, &m, &s);
+            s_out[rb * C + c] = s;
+            if (amax_out) amax_out[rb * C + c] = a;
+            sat += quant_run(x + rb * 128 * C + c, 128, C, m, fmt, q + rb * 128 * C + c, C);
+        }
+    }
+    return sat;
+}
+
+int64_t orc_quantize_mx32_col(const float* x, int64_t R, int64_t C, int fmt, uint8_t* q,
+                              uint8_t* e8m0_out, float* amax_out)
+{
+    int64_t RB = R / 32, sat = 0;
+    #pragma omp parallel for reduction(+:sat) schedule(static)
+    for (int64_t c = 0; c < C; ++c) {
+        for (int64_t rb = 0; rb < RB; ++rb) {
+            float a = 0.0f;
+            for (int64_t r = rb * 32; r < rb * 32 + 32; ++r)
+                a = amax2(a, fabsf(x[r * C + c]));
+            uint8_t code = orc_mx_scale_code(a, fmt);
+            float m = (code == 0xFF) ? 1.0f : (float)ldexp(1.0, -((int)code - 127));
+            e8m0_out[rb * C + c] = code;
+            if (amax_out) amax_out[rb * C + c] = a;
+            sat += quant_run(x + rb * 32 * C + c, 32, C, m, fmt, q + rb * 32 * C + c, C);
+        }
+    }
+    return sat;
+}
+
+/* ------------------------------------------------------------------------
  * 8. Delayed scaling with an amax history.
  * [TS] core vocabulary: delayed scaling "uses historical amax" to set the
  * scale, avoiding a read of the tensor before the cast, at the cost of lag;
@@ -333,7 +382,8 @@ void orc_update_scale(float* state, int H, int fmt, int algo)
  * 9. Dequantisation to exact doubles: xhat = dec(q) * s(unit).  dec(q) has
  * at most 4 significant bits and s is an fp32, so the product is exact.
  * gran: 0 tensor (s[0]), 1 tile 1x128 (s[R][C/128]), 2 block 128x128
- * (s[R/128][C/128]), 3 MX-32 (E8M0 codes u8[R][C/32]).
+ * (s[R/128][C/128]), 3 MX-32 (E8M0 codes u8[R][C/32]), 4 column tile 128x1
+ * (s[R/128][C]), 5 column MX-32 (E8M0 codes u8[R/32][C]).
  * ---------------------------------------------------------------------- */
 void orc_dequantize(const uint8_t* q, int64_t R, int64_t C, int fmt, int gran,
                     const void* scales, double* out)
@@ -345,7 +395,11 @@ void orc_dequantize(const uint8_t* q, int64_t R, int64_t C, int fmt, int gran,
             if (gran == 0) s = ((const float*)scales)[0];
             else if (gran == 1) s = ((const float*)scales)[r * (C / 128) + c / 128];
             else if (gran == 2) s = ((const float*)scales)[(r / 128) * (C / 128) + c / 128];
-            else {
+            else if (gran == 4) s = ((const float*)scales)[(r / 128) * C + c];
+            else if (gran == 5) {
+                uint8_t code = ((const uint8_t*)scales)[(r / 32) * C + c];
+                s = (code == 0xFF) ? NAN : ldexp(1.0, (int)code - 127);
+            } else {
                 uint8_t code = ((const uint8_t*)scales)[r * (C / 32) + c / 32];
                 s = (code == 0xFF) ? NAN : ldexp(1.0, (int)code - 127);
             }

@@ -166,3 +166,53 @@ def test_sat_count_and_clipping():
     q, sat = o.quantize_with_multiplier(x, 1.0, o.E4M3)
     assert sat == 3
     assert q.tolist() == [o.encode(o.E4M3, 1.0), 0x7E, 0xFE, 0x7E, 0xFE]
+
+
+@pytest.mark.parametrize("fmt", [o.E4M3, o.E5M2])
+def test_column_units_are_row_units_of_the_transpose(fmt):
+    """Column tiles / column MX blocks of x are, by definition, the row units
+    of x^T: codes, scales and amaxes must agree element for element."""
+    rng = np.random.default_rng(12)
+    x = (rng.standard_normal((256, 96)) * np.exp(rng.standard_normal((1, 96)))).astype(np.float32)
+    x[5, 7] = 300.0
+    q, s, a, sat = o.quantize_tile128x1(x, fmt)
+    qt, st, at, satt = o.quantize_tile1x128(np.ascontiguousarray(x.T), fmt)
+    assert np.array_equal(q, qt.T) and np.array_equal(s, st.T) and np.array_equal(a, at.T) and sat == satt
+    q, e, a, sat = o.quantize_mx32_col(x, fmt)
+    qt, et, at, satt = o.quantize_mx32(np.ascontiguousarray(x.T), fmt)
+    assert np.array_equal(q, qt.T) and np.array_equal(e, et.T) and np.array_equal(a, at.T) and sat == satt
+
+
+def test_column_tile_layout_closed_form():
+    x = np.zeros((256, 3), np.float32)
+    x[0:128, 0] = 2.0          # column 0, row block 0
+    x[128:256, 2] = -7.0       # column 2, row block 1
+    q, s, a, _ = o.quantize_tile128x1(x, o.E4M3)
+    assert s.shape == (2, 3)
+    assert s[0, 0] == np.float32(2.0) / np.float32(448.0) and s[1, 2] == np.float32(7.0) / np.float32(448.0)
+    assert s[1, 0] == 1.0 and s[0, 2] == 1.0
+    assert np.all(q[0:128, 0] == 0x7E) and np.all(q[128:, 2] == 0xFE)
+    one = o.encode(o.E4M3, 1.0)
+    assert np.array_equal(o.dequantize(np.full((256, 3), one, np.uint8), o.E4M3, o.GRAN_TILE_128x1, s),
+                          np.repeat(s, 128, axis=0).astype(np.float64))
+    e = np.array([[120, 130], [127, 140]], np.uint8)          # [R/32][C] for R = 64, C = 2
+    assert np.array_equal(o.dequantize(np.full((64, 2), one, np.uint8), o.E4M3, o.GRAN_MX32_COL, e),
+                          np.repeat(2.0 ** (e.astype(np.float64) - 127), 32, axis=0))
+
+
+@pytest.mark.parametrize("gran", [o.GRAN_TILE_1x128, o.GRAN_MX32])
+def test_fine_grained_backward_close_to_exact(gran):
+    """The fine-grained forward / dgrad / wgrad of the oracle stay within the
+    formats' precision of the exact float64 products (a dropped transpose or
+    a mis-oriented scale would break this)."""
+    rng = np.random.default_rng(13)
+    M, K, N = 256, 384, 256
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    dy = (rng.standard_normal((M, N)) * 1e-3).astype(np.float32)
+    st, y = o.linear_fine_fwd(x, w, gran)
+    dX, dW = o.linear_fine_bwd(st, dy, gran)
+    x64, w64, d64 = x.astype(np.float64), w.astype(np.float64), dy.astype(np.float64)
+    for got, exact in ((y, x64 @ w64.T), (dX, d64 @ w64), (dW, d64.T @ x64)):
+        assert got.shape == exact.shape
+        assert np.max(np.abs(got - exact)) / np.max(np.abs(exact)) < 0.1
