@@ -76,6 +76,8 @@ extern "C" {
 #define FP8SQ_BLOCK_128x128 2  /* one scale per 128x128 block                   */
 #define FP8SQ_MX32 3           /* one power-of-two (E8M0) scale per 32 values   */
 #define FP8SQ_MX32_TILED 4     /* MX32 with the scales in the GEMM's tiled layout */
+#define FP8SQ_TILE_128x1 5     /* one scale per 128 consecutive values of a column */
+#define FP8SQ_MX32_COL_TILED 6 /* one E8M0 scale per 32 values of a column, tiled  */
 
 /* Tiled MX scale layout (FP8SQ_MX32_TILED), for a tensor [rows][cols] with
  * rows % 128 == 0 and cols % 128 == 0: the E8M0 code of row r, 32-block
@@ -158,9 +160,19 @@ FP8SQ_API int fp8_update_scale(float* states, int n_states, int history_len, con
  *       e + 127 of the smallest power of two 2^e with amax <= fmax * 2^e
  *       (clamped to [-127, 127]; amax 0 -> 127; non-finite -> 0xFF with
  *       m = 1); m = 2^-e.
+ *     TILE_128x1 / MX32_COL_TILED (column units, for the backward products
+ *       that contract over the rows of x): the same rules applied to 128
+ *       (or 32) consecutive values of each COLUMN.  Needs bf16 x, rows % 128
+ *       == 0 and cols % 16 == 0 (MX: cols % 128 == 0).  qT is required (the
+ *       transposed codes are the GEMM operand), q may be NULL.  scales_out:
+ *       f32 [rows/128][cols] (TILE_128x1), or the E8M0 codes of qT's 32-value
+ *       row blocks in the tiled layout of the [cols][rows] matrix qT
+ *       (MX32_COL_TILED).
  *   q         device u8 [rows][cols], 16-byte aligned
- *   qT        device u8 [cols][rows] (the transposed codes, same scale) or
- *             NULL; TENSOR only, needs rows % 16 == 0 and cols % 16 == 0
+ *   qT        device u8 [cols][rows] (the transposed codes) or NULL; for
+ *             TENSOR (same scale; rows, cols % 16 == 0) and BLOCK_128x128
+ *             (qT's 128x128 block scales are the transpose of scales_out),
+ *             required for the column units
  *   amax_out  device f32 per unit (layout as fp8_amax) or NULL (see above)
  *   sat_count device u64 or NULL: the number of elements with |x*m| > fmax
  *             (they clip) is ADDED to it.
@@ -186,8 +198,14 @@ FP8SQ_API int fp8_quantize(const void* x, int x_dtype, int64_t rows, int64_t col
  *       [N/128][K/128]; partial sums over each 128-wide K block are promoted
  *       to fp32 registers with sA * sB ([W14] accumulation bullet:
  *       promotion to fp32 at fixed intervals); K % 128 == 0.
- *     (MX32_TILED, MX32_TILED): a_scale, b_scale u8 E8M0 in the tiled
- *       layout (as written by fp8_quantize MX32_TILED), 16-byte aligned;
+ *     (TILE_128x1, TILE_128x1): A and B are the transposed codes qT of two
+ *       column-tile quantisations (the wgrad operands dy^T and x^T, whose
+ *       contraction runs over the original rows): a_scale f32 [K/128][M],
+ *       b_scale f32 [K/128][N]; every K block's partial is promoted with
+ *       sA[kb][m] * sB[kb][n]; K % 128 == 0.
+ *     (MX32_TILED or MX32_COL_TILED, same for B): a_scale, b_scale u8 E8M0
+ *       in the tiled layout of the operand (as written by fp8_quantize
+ *       MX32_TILED for q, or MX32_COL_TILED for qT), 16-byte aligned;
  *       D = sum_k dec(qA) 2^(eA - 127) dec(qB) 2^(eB - 127) on the
  *       block-scaled tensor-core path ([W14] absmax bullet: every 32
  *       numbers share a scale); M, N, K % 128 == 0.
@@ -211,19 +229,26 @@ FP8SQ_API int fp8_gemm(const uint8_t* A, int a_format, const void* a_scale, int 
  *   (each a state block of history_len), current scaling when all are NULL.
  *   The forward keeps the codes of x and W (and their transposes) in the
  *   workspace; the backward reads them and adds dy's codes.
- * gran TILE_1x128: x in 1x128 tiles, W in 128x128 blocks, current scaling,
- *   forward only.   gran MX32: x and W in MX-32 blocks (tiled scales in the
- *   workspace), forward only.
+ * gran TILE_1x128: x in 1x128 tiles, W in 128x128 blocks, current scaling
+ *   ([W14] absmax bullet, the DeepSeek-V3 granularity).  Backward: dy in
+ *   1x128 tiles along N for dgrad (B = W^T codes, its blocks transposed); dy
+ *   and x in 128x1 column tiles along M for wgrad (both operands promoted per
+ *   128 tokens).  The forward also casts x in column tiles for the backward.
+ * gran MX32: every operand in MX-32 blocks along its contraction dimension:
+ *   x, W along K (forward), dy along N and W along N (dgrad), dy and x along
+ *   M (wgrad); the forward also writes the column-block codes of x and W.
  * workspace: device, >= fp8_linear_workspace_bytes(M, N, K, gran), 256-byte
  *   aligned; the same workspace must be passed to the matching backward.
  * Shapes: M, N, K % 128 == 0 (TENSOR: M % 16, N % 16, K % 16).
+ * fp8_linear_bwd takes the forward's gran and workspace.  Under the HYBRID
+ * recipe dy is cast to E5M2, under RECIPE_E4M3 to E4M3.
  */
 FP8SQ_API size_t fp8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int gran);
 FP8SQ_API int fp8_linear_fwd(const void* x, const void* w, int64_t M, int64_t N, int64_t K,
                              int gran, int recipe, float* x_state, float* w_state,
                              int history_len, void* workspace, size_t ws_bytes,
                              const float* bias, void* y, int y_dtype, void* stream);
-FP8SQ_API int fp8_linear_bwd(const void* dy, int64_t M, int64_t N, int64_t K, int recipe,
+FP8SQ_API int fp8_linear_bwd(const void* dy, int64_t M, int64_t N, int64_t K, int gran, int recipe,
                              float* dy_state, int history_len, void* workspace, size_t ws_bytes,
                              void* dx, float* dw, void* stream);
 
@@ -265,7 +290,7 @@ FP8SQ_API int fp8_linear_fwd_noalloc(const void* x, const void* w, int64_t M, in
  *   word is set, GEMM kernels return early without computing.
  * fp8_last_error: message for the calling thread's last non-zero status
  *   (static thread-local storage; never NULL).
- * fp8_abi_version: 1.
+ * fp8_abi_version: 2.
  */
 FP8SQ_API int fp8_device_status(int clear);
 FP8SQ_API const char* fp8_last_error(void);

@@ -14,7 +14,7 @@ import threading
 
 E4M3, E5M2 = 0, 1
 BF16, F32 = 0, 1
-TENSOR, TILE_1x128, BLOCK_128x128, MX32, MX32_TILED = 0, 1, 2, 3, 4
+TENSOR, TILE_1x128, BLOCK_128x128, MX32, MX32_TILED, TILE_128x1, MX32_COL_TILED = 0, 1, 2, 3, 4, 5, 6
 AMAX_MAX, AMAX_MOST_RECENT = 0, 1
 RECIPE_HYBRID, RECIPE_E4M3 = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WRONG_ARCH, ERR_CUDA, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
@@ -59,7 +59,7 @@ def lib() -> ctypes.CDLL:
                 "fp8_gemm": (I, [P, I, P, I, P, I, P, I, I64, I64, I64, P, P, I, P]),
                 "fp8_linear_workspace_bytes": (Z, [I64, I64, I64, I]),
                 "fp8_linear_fwd": (I, [P, P, I64, I64, I64, I, I, P, P, I, P, Z, P, P, I, P]),
-                "fp8_linear_bwd": (I, [P, I64, I64, I64, I, P, I, P, Z, P, P, P]),
+                "fp8_linear_bwd": (I, [P, I64, I64, I64, I, I, P, I, P, Z, P, P, P]),
                 "fp8_linear_fwd_noalloc": (I, [P, P, I64, I64, I64, P, P, I, P]),
             }
             for name, (res, args) in sig.items():
@@ -147,10 +147,10 @@ def fp8_linear_fwd(x, w, y, workspace, gran: int = TENSOR, recipe: int = RECIPE_
                                 _ptr(bias), _ptr(y), _dtype_code(y), _stream(stream)))
 
 
-def fp8_linear_bwd(dy, dx, dw, workspace, K: int, recipe: int = RECIPE_HYBRID, dy_state=None,
-                   history_len: int = 0, stream=None) -> None:
+def fp8_linear_bwd(dy, dx, dw, workspace, K: int, gran: int = TENSOR, recipe: int = RECIPE_HYBRID,
+                   dy_state=None, history_len: int = 0, stream=None) -> None:
     M, N = dy.shape
-    _check(lib().fp8_linear_bwd(_ptr(dy), M, N, K, recipe, _ptr(dy_state), history_len, _ptr(workspace),
+    _check(lib().fp8_linear_bwd(_ptr(dy), M, N, K, gran, recipe, _ptr(dy_state), history_len, _ptr(workspace),
                                 workspace.numel() * workspace.element_size(), _ptr(dx), _ptr(dw),
                                 _stream(stream)))
 

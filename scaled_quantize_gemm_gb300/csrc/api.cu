@@ -64,7 +64,9 @@ int cuda_status(cudaError_t e, const char* what)
 
 bool valid_format(int f) { return f == FP8SQ_E4M3 || f == FP8SQ_E5M2; }
 bool valid_dtype(int d) { return d == FP8SQ_BF16 || d == FP8SQ_F32; }
-bool valid_gran(int g) { return g >= FP8SQ_TENSOR && g <= FP8SQ_MX32_TILED; }
+bool valid_gran(int g) { return g >= FP8SQ_TENSOR && g <= FP8SQ_MX32_COL_TILED; }
+bool column_gran(int g) { return g == FP8SQ_TILE_128x1 || g == FP8SQ_MX32_COL_TILED; }
+bool mx_tiled(int g) { return g == FP8SQ_MX32_TILED || g == FP8SQ_MX32_COL_TILED; }
 
 const int64_t kMaxDim = (int64_t)1 << 31;  // GEMM / TMA coordinates are 32-bit
 
@@ -77,16 +79,23 @@ int check_units(int gran, int64_t rows, int64_t cols)
         return fail(FP8SQ_ERR_UNSUPPORTED, "128x128 blocks need rows, cols %% 128 == 0 (%lld x %lld)", (long long)rows, (long long)cols);
     if (gran == FP8SQ_MX32 && cols % 32)
         return fail(FP8SQ_ERR_UNSUPPORTED, "MX-32 blocks need cols %% 32 == 0 (cols = %lld)", (long long)cols);
-    if (gran == FP8SQ_MX32_TILED && (rows % 128 || cols % 128))
+    if ((gran == FP8SQ_MX32_TILED || gran == FP8SQ_MX32_COL_TILED) && (rows % 128 || cols % 128))
         return fail(FP8SQ_ERR_UNSUPPORTED, "tiled MX-32 scales need rows, cols %% 128 == 0 (%lld x %lld)", (long long)rows, (long long)cols);
+    if (gran == FP8SQ_TILE_128x1 && (rows % 128 || cols % 16))
+        return fail(FP8SQ_ERR_UNSUPPORTED, "128x1 column tiles need rows %% 128 == 0 and cols %% 16 == 0 (%lld x %lld)", (long long)rows, (long long)cols);
     return FP8SQ_OK;
 }
 
 // workspace layout of the linear layer (offsets in bytes, 256-byte aligned)
 struct WsLayout {
-    size_t qx = 0, qxT = 0, qw = 0, qwT = 0, qdy = 0, qdyT = 0, sx = 0, sw = 0, scal = 0, total = 0;
+    size_t qx = 0, qxT = 0, qw = 0, qwT = 0, qdy = 0, qdyT = 0;
+    size_t sx = 0, sxT = 0, sw = 0, swT = 0, sdy = 0, sdyT = 0, scal = 0, total = 0;
 };
 size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
+// TENSOR: codes of x, W, dy and their transposes + 8 scalars.
+// TILE_1x128: x tiles [M][K/128] and column tiles [M/128][K]; W blocks and
+//   their transpose; dy tiles [M][N/128] and column tiles [M/128][N].
+// MX32: x, W, dy in row blocks and column blocks, tiled E8M0 scales.
 WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int gran)
 {
     WsLayout L;
@@ -94,18 +103,26 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int gran)
     auto take = [&](size_t bytes) { size_t o = off; off += al256(bytes); return o; };
     L.qx = take((size_t)(M * K));
     L.qw = take((size_t)(N * K));
+    L.qxT = take((size_t)(M * K));
+    L.qwT = take((size_t)(N * K));
+    L.qdy = take((size_t)(M * N));
+    L.qdyT = take((size_t)(M * N));
     if (gran == FP8SQ_TENSOR) {
-        L.qxT = take((size_t)(M * K));
-        L.qwT = take((size_t)(N * K));
-        L.qdy = take((size_t)(M * N));
-        L.qdyT = take((size_t)(M * N));
         L.scal = take(8 * sizeof(float));   // sx, sw, sdy, ax, aw, ady
     } else if (gran == FP8SQ_TILE_1x128) {
         L.sx = take((size_t)(M * (K / 128)) * sizeof(float));
+        L.sxT = take((size_t)((M / 128) * K) * sizeof(float));
         L.sw = take((size_t)((N / 128) * (K / 128)) * sizeof(float));
+        L.swT = take((size_t)((N / 128) * (K / 128)) * sizeof(float));
+        L.sdy = take((size_t)(M * (N / 128)) * sizeof(float));
+        L.sdyT = take((size_t)((M / 128) * N) * sizeof(float));
     } else {
         L.sx = take((size_t)(M * (K / 32)));
+        L.sxT = take((size_t)(M * (K / 32)));
         L.sw = take((size_t)(N * (K / 32)));
+        L.swT = take((size_t)(N * (K / 32)));
+        L.sdy = take((size_t)(M * (N / 32)));
+        L.sdyT = take((size_t)(M * (N / 32)));
     }
     L.total = off;
     return L;
@@ -127,7 +144,7 @@ int api_check_device(int* sms) { return check_device(sms); }
 
 extern "C" {
 
-FP8SQ_API int fp8_abi_version(void) { return 1; }
+FP8SQ_API int fp8_abi_version(void) { return 2; }
 
 FP8SQ_API const char* fp8_last_error(void) { return g_msg; }
 
@@ -146,7 +163,7 @@ FP8SQ_API int fp8_amax(const void* x, int x_dtype, int64_t rows, int64_t cols, i
                        void* stream)
 {
     if ((!x && rows * cols != 0) || !amax_out) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_amax: null pointer");
-    if (!valid_dtype(x_dtype) || !valid_gran(gran) || gran == FP8SQ_MX32_TILED)
+    if (!valid_dtype(x_dtype) || !valid_gran(gran) || gran == FP8SQ_MX32_TILED || column_gran(gran))
         return fail(FP8SQ_ERR_INVALID_ARG, "fp8_amax: bad dtype or granularity");
     if (rows < 0 || cols < 0) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_amax: negative size");
     if (!aligned16(x)) return fail(FP8SQ_ERR_MISALIGNED, "fp8_amax: x must be 16-byte aligned");
@@ -199,12 +216,12 @@ static int validate_quantize(const void* x, int x_dtype, int64_t rows, int64_t c
                              const float* state, int H, const uint8_t* q, const uint8_t* qT, const void* scales,
                              const float* amax_out)
 {
-    if ((!x || !q) && rows * cols != 0) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize: null x or q");
+    if ((!x || (!q && !column_gran(gran))) && rows * cols != 0) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize: null x or q");
     if (!valid_dtype(x_dtype) || !valid_format(format) || !valid_gran(gran))
         return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize: bad dtype, format or granularity");
     if (rows < 0 || cols < 0) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize: negative size");
     if (rows >= kMaxDim || cols >= kMaxDim) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_quantize: dimension too large");
-    if (!aligned16(x) || !aligned16(q) || (qT && !aligned16(qT)))
+    if (!aligned16(x) || (q && !aligned16(q)) || (qT && !aligned16(qT)))
         return fail(FP8SQ_ERR_MISALIGNED, "fp8_quantize: x, q, qT must be 16-byte aligned");
     if ((scales && !aligned4(scales)) || (amax_out && !aligned4(amax_out)) || (state && !aligned4(state)))
         return fail(FP8SQ_ERR_MISALIGNED, "fp8_quantize: scale / amax / state buffers must be 4-byte aligned");
@@ -218,8 +235,15 @@ static int validate_quantize(const void* x, int x_dtype, int64_t rows, int64_t c
             return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_quantize: a transposed copy needs rows, cols %% 16 == 0");
     } else {
         if (state) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_quantize: delayed scaling is per tensor only");
-        if (qT) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_quantize: a transposed copy is per tensor only");
+        if (qT && !(gran == FP8SQ_BLOCK_128x128 || column_gran(gran)))
+            return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_quantize: a transposed copy needs TENSOR, BLOCK_128x128 or a column granularity");
         if (!scales) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize: scales_out is required for this granularity");
+        if (column_gran(gran)) {
+            if (!qT && rows * cols != 0) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize: column granularities need qT");
+            if (x_dtype != FP8SQ_BF16) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_quantize: column granularities need bf16 input");
+            if (amax_out) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_quantize: no amax output for column granularities");
+            if (!aligned16(scales)) return fail(FP8SQ_ERR_MISALIGNED, "fp8_quantize: column-unit scales must be 16-byte aligned");
+        }
     }
     return FP8SQ_OK;
 }
@@ -275,7 +299,12 @@ static int validate_gemm(const uint8_t* A, int a_format, const void* a_scale, in
     } else if (a_gran == FP8SQ_TILE_1x128 && b_gran == FP8SQ_BLOCK_128x128) {
         if (K % 128) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_gemm: 1x128 x 128x128 scaling needs K %% 128 == 0");
         *mode = 1;
-    } else if (a_gran == FP8SQ_MX32_TILED && b_gran == FP8SQ_MX32_TILED) {
+    } else if (a_gran == FP8SQ_TILE_128x1 && b_gran == FP8SQ_TILE_128x1) {
+        if (K % 128) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_gemm: column-tile scaling needs K %% 128 == 0");
+        if (!aligned16(a_scale) || !aligned16(b_scale))
+            return fail(FP8SQ_ERR_MISALIGNED, "fp8_gemm: column-tile scales must be 16-byte aligned");
+        *mode = 3;
+    } else if (mx_tiled(a_gran) && mx_tiled(b_gran)) {
         if (!aligned16(a_scale) || !aligned16(b_scale))
             return fail(FP8SQ_ERR_MISALIGNED, "fp8_gemm: tiled MX scales must be 16-byte aligned");
         if (M % 128 || N % 128 || K % 128)
@@ -402,22 +431,32 @@ FP8SQ_API int fp8_linear_fwd(const void* x, const void* w, int64_t M, int64_t N,
         g.b_scale = &scal[1];
         g.a_format = g.b_format = fp8sq::kE4M3;
     } else if (gran == FP8SQ_TILE_1x128) {
+        // x: 1x128 tiles along K (forward) and 128x1 column tiles along M (wgrad)
         qa.x = x; qa.rows = M; qa.cols = K; qa.gran = fp8sq::kTile;
         qa.q = ws + L.qx; qa.scales = ws + L.sx;
         if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: quantize x"))) return r;
+        qa.gran = fp8sq::kTileCol; qa.q = nullptr; qa.qT = ws + L.qxT; qa.scales = ws + L.sxT;
+        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: column-quantize x"))) return r;
+        // W: 128x128 blocks, with the transposed codes and scale grid (dgrad)
         qa.x = w; qa.rows = N; qa.cols = K; qa.gran = fp8sq::kBlock;
-        qa.q = ws + L.qw; qa.scales = ws + L.sw;
+        qa.q = ws + L.qw; qa.qT = ws + L.qwT; qa.scales = ws + L.sw;
+        qa.scalesT = reinterpret_cast<float*>(ws + L.swT);
         if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: quantize w"))) return r;
         g.mode = 1;
         g.a_scale = ws + L.sx;
         g.b_scale = ws + L.sw;
     } else {
+        // x and W: MX-32 blocks along K (forward) and along their rows (backward)
         qa.x = x; qa.rows = M; qa.cols = K; qa.gran = fp8sq::kMXTiled;
         qa.q = ws + L.qx; qa.scales = ws + L.sx;
         if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: quantize x"))) return r;
-        qa.x = w; qa.rows = N; qa.cols = K;
-        qa.q = ws + L.qw; qa.scales = ws + L.sw;
+        qa.gran = fp8sq::kMXCol; qa.q = nullptr; qa.qT = ws + L.qxT; qa.scales = ws + L.sxT;
+        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: column-quantize x"))) return r;
+        qa.x = w; qa.rows = N; qa.cols = K; qa.gran = fp8sq::kMXTiled;
+        qa.q = ws + L.qw; qa.qT = nullptr; qa.scales = ws + L.sw;
         if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: quantize w"))) return r;
+        qa.gran = fp8sq::kMXCol; qa.q = nullptr; qa.qT = ws + L.qwT; qa.scales = ws + L.swT;
+        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: column-quantize w"))) return r;
         g.mode = 2;
         g.a_scale = ws + L.sx;
         g.b_scale = ws + L.sw;
@@ -428,13 +467,15 @@ FP8SQ_API int fp8_linear_fwd(const void* x, const void* w, int64_t M, int64_t N,
     return cuda_status(e, why ? why : "fp8_linear_fwd: GEMM launch");
 }
 
-FP8SQ_API int fp8_linear_bwd(const void* dy, int64_t M, int64_t N, int64_t K, int recipe, float* dy_state,
-                             int history_len, void* workspace, size_t ws_bytes, void* dx, float* dw, void* stream)
+FP8SQ_API int fp8_linear_bwd(const void* dy, int64_t M, int64_t N, int64_t K, int gran, int recipe,
+                             float* dy_state, int history_len, void* workspace, size_t ws_bytes, void* dx, float* dw,
+                             void* stream)
 {
     if (!dy || !dx || !dw) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_linear_bwd: null pointer");
     if (recipe != FP8SQ_RECIPE_HYBRID && recipe != FP8SQ_RECIPE_E4M3) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_linear_bwd: bad recipe");
-    int r = check_linear_shape(M, N, K, FP8SQ_TENSOR, workspace, ws_bytes);
+    int r = check_linear_shape(M, N, K, gran, workspace, ws_bytes);
     if (r) return r;
+    if (dy_state && gran != FP8SQ_TENSOR) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_linear_bwd: delayed scaling is per tensor only");
     if (dy_state && (history_len < 1 || history_len > 4096)) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_linear_bwd: bad history_len");
     if (!aligned16(dy) || !aligned16(dx) || !aligned16(dw)) return fail(FP8SQ_ERR_MISALIGNED, "fp8_linear_bwd: dy, dx, dw must be 16-byte aligned");
     if (dy_state && !aligned4(dy_state)) return fail(FP8SQ_ERR_MISALIGNED, "fp8_linear_bwd: dy_state must be 4-byte aligned");
@@ -442,36 +483,51 @@ FP8SQ_API int fp8_linear_bwd(const void* dy, int64_t M, int64_t N, int64_t K, in
     if ((r = check_device(&sms))) return r;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const WsLayout L = ws_layout(M, N, K, FP8SQ_TENSOR);
-    float* scal = reinterpret_cast<float*>(ws + L.scal);
+    const WsLayout L = ws_layout(M, N, K, gran);
     const int fdy = recipe == FP8SQ_RECIPE_HYBRID ? fp8sq::kE5M2 : fp8sq::kE4M3;
+    const char* why = nullptr;
 
     fp8sq::QuantArgs qa;
     qa.x = dy; qa.x_dtype = fp8sq::kBF16; qa.rows = M; qa.cols = N;
-    qa.format = fdy; qa.gran = fp8sq::kTensor;
-    qa.q = ws + L.qdy; qa.qT = ws + L.qdyT;
-    qa.state = dy_state; qa.history_len = history_len;
-    qa.scales = &scal[2]; qa.amax = dy_state ? nullptr : &scal[5];
-    if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_bwd: quantize dy"))) return r;
-    if (dy_state &&
-        (r = cuda_status(cudaMemcpyAsync(&scal[2], dy_state + history_len + 1, sizeof(float), cudaMemcpyDeviceToDevice, st), "fp8_linear_bwd: copy s_dy")))
-        return r;
-
-    const char* why = nullptr;
-    // dgrad: dx[M][K] = dy[M][N] * W[N][K]   (A = dy codes, B = W^T codes [K][N])
-    fp8sq::GemmArgs g;
-    g.mode = 0;
-    g.A = ws + L.qdy; g.a_format = fdy; g.a_scale = &scal[2];
-    g.B = ws + L.qwT; g.b_format = fp8sq::kE4M3; g.b_scale = &scal[1];
-    g.M = M; g.N = K; g.K = N;
-    g.D = dx; g.d_dtype = fp8sq::kBF16;
-    if ((r = cuda_status(fp8sq::launch_gemm(g, st, sms, &why), why ? why : "fp8_linear_bwd: dgrad"))) return r;
-    // wgrad: dw[N][K] = dy^T[N][M] * x[M][K]   (A = dy^T codes [N][M], B = x^T codes [K][M])
-    g.A = ws + L.qdyT; g.a_format = fdy; g.a_scale = &scal[2];
-    g.B = ws + L.qxT; g.b_format = fp8sq::kE4M3; g.b_scale = &scal[0];
-    g.M = N; g.N = K; g.K = M;
-    g.D = dw; g.d_dtype = fp8sq::kF32;
-    return cuda_status(fp8sq::launch_gemm(g, st, sms, &why), why ? why : "fp8_linear_bwd: wgrad");
+    qa.format = fdy;
+    fp8sq::GemmArgs dg, wg;                 // dgrad dx[M][K] = dy W; wgrad dw[N][K] = dy^T x
+    dg.M = M; dg.N = K; dg.K = N; dg.D = dx; dg.d_dtype = fp8sq::kBF16;
+    dg.A = ws + L.qdy; dg.a_format = fdy; dg.B = ws + L.qwT; dg.b_format = fp8sq::kE4M3;
+    wg.M = N; wg.N = K; wg.K = M; wg.D = dw; wg.d_dtype = fp8sq::kF32;
+    wg.A = ws + L.qdyT; wg.a_format = fdy; wg.B = ws + L.qxT; wg.b_format = fp8sq::kE4M3;
+    if (gran == FP8SQ_TENSOR) {
+        float* scal = reinterpret_cast<float*>(ws + L.scal);
+        qa.gran = fp8sq::kTensor;
+        qa.q = ws + L.qdy; qa.qT = ws + L.qdyT;
+        qa.state = dy_state; qa.history_len = history_len;
+        qa.scales = &scal[2]; qa.amax = dy_state ? nullptr : &scal[5];
+        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_bwd: quantize dy"))) return r;
+        if (dy_state &&
+            (r = cuda_status(cudaMemcpyAsync(&scal[2], dy_state + history_len + 1, sizeof(float), cudaMemcpyDeviceToDevice, st), "fp8_linear_bwd: copy s_dy")))
+            return r;
+        dg.mode = wg.mode = 0;
+        dg.a_scale = &scal[2]; dg.b_scale = &scal[1];
+        wg.a_scale = &scal[2]; wg.b_scale = &scal[0];
+    } else if (gran == FP8SQ_TILE_1x128) {
+        // dy: 1x128 tiles along N (dgrad) and 128x1 column tiles along M (wgrad)
+        qa.gran = fp8sq::kTile; qa.q = ws + L.qdy; qa.scales = ws + L.sdy;
+        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_bwd: quantize dy"))) return r;
+        qa.gran = fp8sq::kTileCol; qa.q = nullptr; qa.qT = ws + L.qdyT; qa.scales = ws + L.sdyT;
+        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_bwd: column-quantize dy"))) return r;
+        dg.mode = 1; dg.a_scale = ws + L.sdy; dg.b_scale = ws + L.swT;
+        wg.mode = 3; wg.a_scale = ws + L.sdyT; wg.b_scale = ws + L.sxT;
+    } else {
+        // dy: MX-32 blocks along N (dgrad) and along M (wgrad)
+        qa.gran = fp8sq::kMXTiled; qa.q = ws + L.qdy; qa.scales = ws + L.sdy;
+        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_bwd: quantize dy"))) return r;
+        qa.gran = fp8sq::kMXCol; qa.q = nullptr; qa.qT = ws + L.qdyT; qa.scales = ws + L.sdyT;
+        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_bwd: column-quantize dy"))) return r;
+        dg.mode = wg.mode = 2;
+        dg.a_scale = ws + L.sdy; dg.b_scale = ws + L.swT;
+        wg.a_scale = ws + L.sdyT; wg.b_scale = ws + L.sxT;
+    }
+    if ((r = cuda_status(fp8sq::launch_gemm(dg, st, sms, &why), why ? why : "fp8_linear_bwd: dgrad"))) return r;
+    return cuda_status(fp8sq::launch_gemm(wg, st, sms, &why), why ? why : "fp8_linear_bwd: wgrad");
 }
 
 }  // extern "C"

@@ -210,7 +210,9 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t* afull = empty + STAGES;
     uint64_t* aempty = afull + 2;
     uint64_t* drain = aempty + 2;
-    constexpr uint32_t TMEM_COLS = 2 * BN;
+    // two BN-column accumulators; the allocation is a power of two >= 32
+    constexpr uint32_t TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+    static_assert(2 * BN <= 512, "two accumulators must fit in tensor memory");
 
     uint32_t tmem_base;
     if (!gemm_setup<STAGES, 2, 4>(smem, L::BAR_OFF, TMEM_COLS, &tmA, &tmB, tmem_base)) return;
@@ -304,17 +306,26 @@ __global__ void __launch_bounds__(192, 1)
 
 // ================================================================== mode 1
 // 1x128 x 128x128 scales with per-K-block promotion; BN = 128, four TMEM
-// partial buffers, 8 epilogue warps (warps 2..9): warp w reads lane quarter
-// w % 4 and column half (w - 2) / 4.
+// partial buffers.  EPI epilogue warps (warps 2..EPI+1): warp w reads lane
+// quarter w % 4 and the (w - 2) / 4-th slice of 128 / (EPI / 4) columns.
+// PF is how many K blocks ahead each thread reads its combined scale
+// sA[row][kb] * sB[nb][kb] (1: the next one; 16: a register window of 16).
 constexpr int kPromoBuffers = 4;
 
-template <int STAGES, bool OUT_BF16>
-__global__ void __launch_bounds__(320, 1)
+// SM selects the scale layouts: 1 = A in 1x128 tiles sA[M][K/128] and B in
+// 128x128 blocks sB[N/128][K/128]; 3 = both operands in tiles along K with
+// K-block-major scales sA[K/128][M], sB[K/128][N] (the transposed codes of
+// column-tile quantisation), whose per-column scales reach each warp through
+// a double-buffered shared-memory slot.
+template <int STAGES, bool OUT_BF16, int EPI, int PF, int SM = 1>
+__global__ void __launch_bounds__(64 + 32 * EPI, 1)
     k_gemm_promote(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    EpiParams p, uint32_t idesc, TileSched sched)
 {
     constexpr int BN = 128;
     constexpr int NB = kPromoBuffers;
+    constexpr int COLS = BN * 4 / EPI;       // columns per epilogue warp
+    constexpr int NLD = COLS / 32;           // 32-column TMEM loads per K block
     using L = Smem<BN, STAGES, NB>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -326,7 +337,7 @@ __global__ void __launch_bounds__(320, 1)
     constexpr uint32_t TMEM_COLS = NB * BN;
 
     uint32_t tmem_base;
-    if (!gemm_setup<STAGES, NB, 8>(smem, L::BAR_OFF, TMEM_COLS, &tmA, &tmB, tmem_base)) return;
+    if (!gemm_setup<STAGES, NB, EPI>(smem, L::BAR_OFF, TMEM_COLS, &tmA, &tmB, tmem_base)) return;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int num_tiles = sched.num_m * sched.num_n;
@@ -367,9 +378,82 @@ __global__ void __launch_bounds__(320, 1)
                 wait_drain(drain, 0);
             }
         }
-    } else {
+    } else if (SM == 3) {
+        static_assert(PF == 1 && COLS == 64, "column-scale promotion uses 8 warps, next-block prefetch");
+        __shared__ float colbuf[EPI][2][COLS];
         const int quarter = warp & 3;
-        const int half = (warp - 2) >> 2;
+        const int part = (warp - 2) >> 2;
+        const int ew = warp - 2;
+        int it = 0;
+        bool ok_all = true;
+        for (int t = blockIdx.x; t < num_tiles && ok_all; t += gridDim.x) {
+            int mb, nb;
+            sched.coords(t, mb, nb);
+            const int row = mb * BM + quarter * 32 + lane;
+            const int rowc = row < p.M ? row : p.M - 1;
+            const int col0 = nb * BN + part * COLS;
+            int cl = col0 + 2 * lane;                       // this lane's two column scales
+            cl = cl < p.N - 1 ? cl : p.N - 2;
+            float acc[COLS];
+#pragma unroll
+            for (int j = 0; j < COLS; ++j) acc[j] = 0.0f;
+            float ra = __ldg(p.sA + rowc);
+            float2 cb = *reinterpret_cast<const float2*>(p.sB + cl);
+            for (int kb = 0; kb < nkb; ++kb) {
+                const float ra_cur = ra;
+                const float2 cb_cur = cb;
+                if (kb + 1 < nkb) {
+                    ra = __ldg(p.sA + (int64_t)(kb + 1) * p.M + rowc);
+                    cb = *reinterpret_cast<const float2*>(p.sB + (int64_t)(kb + 1) * p.N + cl);
+                }
+                float* buf = colbuf[ew][kb & 1];
+                *reinterpret_cast<float2*>(buf + 2 * lane) = cb_cur;
+                __syncwarp();
+                const int b = it % NB;
+                const uint32_t u = (uint32_t)(it / NB);
+                ++it;
+                const bool ok = wait_bounded(&afull[b], u & 1u);
+                if (!__all_sync(0xFFFFFFFFu, ok)) {
+                    ok_all = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr =
+                    tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * BN + part * COLS);
+                uint32_t r[NLD][32];
+#pragma unroll
+                for (int l = 0; l < NLD; ++l) tmem_ld_32x32b_x32(taddr + 32 * l, r[l]);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&aempty[b]);
+#pragma unroll
+                for (int c4 = 0; c4 < COLS / 4; ++c4) {
+                    const float4 s4 = *reinterpret_cast<const float4*>(buf + 4 * c4);
+                    const float sc[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = 4 * c4 + e;
+                        acc[c] = fmaf(__uint_as_float(r[c / 32][c % 32]), ra_cur * sc[e], acc[c]);
+                    }
+                }
+            }
+            if (!ok_all) break;
+#pragma unroll
+            for (int h = 0; h < NLD; ++h) {
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    v[j] = acc[32 * h + j];
+                    if (p.bias && col0 + 32 * h + j < p.N) v[j] += __ldg(p.bias + col0 + 32 * h + j);
+                }
+                store_row32<OUT_BF16>(p, row, col0 + 32 * h, v);
+            }
+        }
+    } else {
+        // SM == 1
+        const int quarter = warp & 3;
+        const int part = (warp - 2) >> 2;
         const int ksb = p.K / BK;            // scale blocks along K
         int it = 0;
         bool ok_all = true;
@@ -380,40 +464,55 @@ __global__ void __launch_bounds__(320, 1)
             const int rowc = row < p.M ? row : p.M - 1;   // clamp for the scale read
             const float* sa_row = p.sA + (int64_t)rowc * ksb;
             const float* sb_row = p.sB + (int64_t)nb * ksb;   // BN = 128: one weight block row
-            float acc[64];
+            float acc[COLS];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) acc[j] = 0.0f;
-            float sc_next = __ldg(sa_row) * __ldg(sb_row);
-            for (int kb = 0; kb < nkb; ++kb, ++it) {
-                const float sc = sc_next;
-                if (kb + 1 < nkb) sc_next = __ldg(sa_row + kb + 1) * __ldg(sb_row + kb + 1);
-                const int b = it % NB;
-                const uint32_t u = (uint32_t)(it / NB);
-                const bool ok = wait_bounded(&afull[b], u & 1u);
-                if (!__all_sync(0xFFFFFFFFu, ok)) {
-                    ok_all = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t taddr =
-                    tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * BN + half * 64);
-                uint32_t r0[32], r1[32];
-                tmem_ld_32x32b_x32(taddr, r0);
-                tmem_ld_32x32b_x32(taddr + 32, r1);
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&aempty[b]);
+            for (int j = 0; j < COLS; ++j) acc[j] = 0.0f;
+            float sc[PF], na[PF], nbv[PF];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    acc[j] = fmaf(__uint_as_float(r0[j]), sc, acc[j]);
-                    acc[32 + j] = fmaf(__uint_as_float(r1[j]), sc, acc[32 + j]);
+            for (int j = 0; j < PF; ++j) {
+                const int kb = j < nkb ? j : nkb - 1;
+                sc[j] = __ldg(sa_row + kb) * __ldg(sb_row + kb);
+            }
+            for (int kw = 0; kw < nkb && ok_all; kw += PF) {
+#pragma unroll
+                for (int j = 0; j < PF; ++j) {
+                    const int kb = (kw + PF + j) < nkb ? kw + PF + j : nkb - 1;
+                    na[j] = __ldg(sa_row + kb);
+                    nbv[j] = __ldg(sb_row + kb);
                 }
+#pragma unroll
+                for (int j = 0; j < PF; ++j) {
+                    if (kw + j >= nkb) break;
+                    const int b = it % NB;
+                    const uint32_t u = (uint32_t)(it / NB);
+                    ++it;
+                    const bool ok = wait_bounded(&afull[b], u & 1u);
+                    if (!__all_sync(0xFFFFFFFFu, ok)) {
+                        ok_all = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t taddr =
+                        tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * BN + part * COLS);
+                    uint32_t r[NLD][32];
+#pragma unroll
+                    for (int l = 0; l < NLD; ++l) tmem_ld_32x32b_x32(taddr + 32 * l, r[l]);
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&aempty[b]);
+#pragma unroll
+                    for (int l = 0; l < NLD; ++l)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) acc[32 * l + i] = fmaf(__uint_as_float(r[l][i]), sc[j], acc[32 * l + i]);
+                }
+#pragma unroll
+                for (int j = 0; j < PF; ++j) sc[j] = na[j] * nbv[j];
             }
             if (!ok_all) break;
-            const int col0 = nb * BN + half * 64;
+            const int col0 = nb * BN + part * COLS;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int h = 0; h < NLD; ++h) {
                 float v[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
@@ -429,6 +528,34 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);
     }
+}
+
+// launches one promotion-kernel variant (EPI epilogue warps, PF scale window,
+// SM scale layouts)
+template <int EPI, int PF, int SM = 1>
+static cudaError_t launch_promote(const GemmArgs& g, const EpiParams& p, cudaStream_t st, int sms, const char** why)
+{
+    constexpr int BN = 128, ST = 6;
+    CUtensorMap ta, tb;
+    if (!encode_tmap_2d(&ta, 0, g.A, g.K, g.M, 128u, BM) || !encode_tmap_2d(&tb, 0, g.B, g.K, g.N, 128u, BN)) {
+        *why = "cuTensorMapEncodeTiled failed";
+        return cudaErrorInvalidValue;
+    }
+    TileSched sched{(int)((g.M + BM - 1) / BM), (int)((g.N + BN - 1) / BN), 16};
+    const int tiles = sched.num_m * sched.num_n;
+    uint32_t idesc = 0;
+    idesc |= 1u << 4;
+    idesc |= (uint32_t)g.a_format << 7;
+    idesc |= (uint32_t)g.b_format << 10;
+    idesc |= (uint32_t)(BN >> 3) << 17;
+    idesc |= (uint32_t)(BM >> 4) << 24;
+    const int smem = Smem<BN, ST, kPromoBuffers>::BYTES;
+    auto kern = g.d_dtype == kBF16 ? k_gemm_promote<ST, true, EPI, PF, SM> : k_gemm_promote<ST, false, EPI, PF, SM>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int grid = tiles < sms ? tiles : sms;
+    kern<<<grid, 64 + 32 * EPI, smem, st>>>(ta, tb, p, idesc, sched);
+    return cudaGetLastError();
 }
 
 // ================================================================== mode 2
@@ -476,8 +603,8 @@ struct MxParams {
     int nchunks_b;        // N / 128
 };
 
-template <int BN, int STAGES, int NACC, bool OUT_BF16>
-__global__ void __launch_bounds__(192, 1)
+template <int BN, int STAGES, int NACC, bool OUT_BF16, int EPI = 4>
+__global__ void __launch_bounds__(64 + 32 * EPI, 1)
     k_gemm_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, EpiParams p,
               uint32_t idesc, TileSched sched, MxParams mx)
 {
@@ -493,7 +620,7 @@ __global__ void __launch_bounds__(192, 1)
     constexpr uint32_t TMEM_COLS = 512;
 
     uint32_t tmem_base;
-    if (!gemm_setup<STAGES, NACC, 4>(smem, L::BAR_OFF, TMEM_COLS, &tmA, &tmB, tmem_base)) return;
+    if (!gemm_setup<STAGES, NACC, EPI>(smem, L::BAR_OFF, TMEM_COLS, &tmA, &tmB, tmem_base)) return;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int num_tiles = sched.num_m * sched.num_n;
@@ -591,7 +718,11 @@ __global__ void __launch_bounds__(192, 1)
             }
         }
     } else {
+        // EPI / 4 warps per TMEM lane quarter split the BN columns
+        constexpr int PARTS = EPI / 4;
+        constexpr int COLS = BN / PARTS;
         const int quarter = warp & 3;
+        const int part = (warp - 2) >> 2;
         int lt = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++lt) {
             const int b = lt % NACC;
@@ -602,14 +733,15 @@ __global__ void __launch_bounds__(192, 1)
             int mb, nb;
             sched.coords(t, mb, nb);
             const int row = mb * BM + quarter * 32 + lane;
-            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * BN);
+            const uint32_t taddr =
+                tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * BN + part * COLS);
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
+            for (int c = 0; c < COLS; c += 32) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(taddr + (uint32_t)c, r);
                 tmem_ld_wait();
                 float v[32];
-                const int col0 = nb * BN + c;
+                const int col0 = nb * BN + part * COLS + c;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
                 if (p.bias) {
@@ -738,7 +870,9 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
     p.D = g.D;
     CUtensorMap ta, tb;
     if (g.mode == 0) {
-        constexpr int BN = 256, ST = 4;
+        // 128x224 tiles with a 5-stage ring (225 KB): measured faster than
+        // 128x256 x 4 stages on every FFN shape, and 224 divides 14336
+        constexpr int BN = 224, ST = 5;
         if (!make_tmap(&ta, g.A, g.K, g.M, BM) || !make_tmap(&tb, g.B, g.K, g.N, BN)) {
             *why = "cuTensorMapEncodeTiled failed";
             return cudaErrorInvalidValue;
@@ -751,20 +885,8 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
             return launch_persistent(k_gemm_tensor<BN, ST, true>, 192, smem, tiles, sms, st, ta, tb, p, idesc, sched);
         return launch_persistent(k_gemm_tensor<BN, ST, false>, 192, smem, tiles, sms, st, ta, tb, p, idesc, sched);
     }
-    if (g.mode == 1) {
-        constexpr int BN = 128, ST = 6;
-        if (!make_tmap(&ta, g.A, g.K, g.M, BM) || !make_tmap(&tb, g.B, g.K, g.N, BN)) {
-            *why = "cuTensorMapEncodeTiled failed";
-            return cudaErrorInvalidValue;
-        }
-        TileSched sched{(int)((g.M + BM - 1) / BM), (int)((g.N + BN - 1) / BN), 16};
-        const int tiles = sched.num_m * sched.num_n;
-        const uint32_t idesc = make_idesc(g.a_format, g.b_format, BN);
-        const int smem = Smem<BN, ST, kPromoBuffers>::BYTES;
-        if (bf16)
-            return launch_persistent(k_gemm_promote<ST, true>, 320, smem, tiles, sms, st, ta, tb, p, idesc, sched);
-        return launch_persistent(k_gemm_promote<ST, false>, 320, smem, tiles, sms, st, ta, tb, p, idesc, sched);
-    }
+    if (g.mode == 1) return launch_promote<8, 1>(g, p, st, sms, why);
+    if (g.mode == 3) return launch_promote<8, 1, 3>(g, p, st, sms, why);
     if (g.mode == 2) {
         constexpr int BN = 256, ST = 4, NACC = 1;
         using L = MxLayout<BN, ST, NACC>;
@@ -777,11 +899,14 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
         MxParams mx{static_cast<const uint8_t*>(g.a_scale), static_cast<const uint8_t*>(g.b_scale), (int)(g.K / 128),
                     (int)(g.N / 128)};
         const uint32_t idesc = make_idesc_mx(g.a_format, g.b_format, BN);
-        auto kern = bf16 ? k_gemm_mx<BN, ST, NACC, true> : k_gemm_mx<BN, ST, NACC, false>;
+        // one accumulator (the scale factors take the other TMEM columns), so
+        // eight epilogue warps drain it in half the time of four
+        constexpr int EPI = 8;
+        auto kern = bf16 ? k_gemm_mx<BN, ST, NACC, true, EPI> : k_gemm_mx<BN, ST, NACC, false, EPI>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
         if (e != cudaSuccess) return e;
         const int grid = tiles < sms ? tiles : sms;
-        kern<<<grid, 192, L::BYTES, st>>>(ta, tb, p, idesc, sched, mx);
+        kern<<<grid, 64 + 32 * EPI, L::BYTES, st>>>(ta, tb, p, idesc, sched, mx);
         return cudaGetLastError();
     }
     *why = "GEMM mode not built";

@@ -9,7 +9,7 @@ namespace fp8sq {
 
 enum { kE4M3 = 0, kE5M2 = 1 };
 enum { kBF16 = 0, kF32 = 1 };
-enum { kTensor = 0, kTile = 1, kBlock = 2, kMX = 3, kMXTiled = 4 };
+enum { kTensor = 0, kTile = 1, kBlock = 2, kMX = 3, kMXTiled = 4, kTileCol = 5, kMXCol = 6 };
 
 struct QuantArgs {
     const void* x = nullptr;
@@ -22,6 +22,7 @@ struct QuantArgs {
     uint8_t* q = nullptr;            // may be null only for amax-only launches
     uint8_t* qT = nullptr;
     void* scales = nullptr;
+    float* scalesT = nullptr;        // 128x128 blocks with qT: the transposed scale grid
     float* amax = nullptr;
     unsigned long long* sat = nullptr;
     const float* amax_in = nullptr;  // current per-tensor: the amax of pass 1
@@ -37,7 +38,8 @@ struct GemmArgs {
     const uint8_t* A = nullptr;
     const uint8_t* B = nullptr;
     int a_format = kE4M3, b_format = kE4M3;
-    int mode = 0;                    // 0 per-tensor, 1 tile x block promotion, 2 MX (tiled E8M0 scales)
+    int mode = 0;                    // 0 per-tensor, 1 tile x block promotion, 2 MX (tiled E8M0 scales),
+                                     // 3 column tiles x column tiles (promotion, scales [K/128][rows])
     const void* a_scale = nullptr;
     const void* b_scale = nullptr;
     int64_t M = 0, N = 0, K = 0;

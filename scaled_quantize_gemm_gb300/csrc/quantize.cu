@@ -373,6 +373,16 @@ __global__ void __launch_bounds__(256) k_cast_tensor_T(const void* __restrict__ 
     }
 }
 
+// MX scales: the canonical layout is u8 [rows][cols/32]; the tiled layout
+// (TILED = true) is the one the block-scaled GEMM copies straight into tensor
+// memory: 512-byte chunks of 128 rows x 4 consecutive 32-blocks, chunk
+// (r/128, t/4) at ((r/128) * (cols/128) + t/4) * 512, inside it
+// (r % 32) * 16 + ((r / 32) % 4) * 4 + t % 4.
+__device__ __forceinline__ int64_t mx_tiled_offset(int64_t r, int64_t t, int64_t cols)
+{
+    return ((r >> 7) * (cols >> 7) + (t >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (t & 3);
+}
+
 // ================================================================== per-tensor, TMA-fed
 // The per-tensor cast with a transposed copy for bf16 inputs, as a persistent
 // pipeline: one CTA per SM; warp 8 streams 128x128 bf16 tiles into a
@@ -519,6 +529,198 @@ __global__ void __launch_bounds__(kTThreads, 1)
     }
 }
 
+// AND of `v` over the 256 consumer threads (warps 0..7), at named barrier 1
+__device__ __forceinline__ bool consumers_all(bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 256, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
+// ================================================================== column units, TMA-fed
+// Column tiles of 128 rows (UNIT = 128, scales f32 [R/128][C]) and column MX
+// blocks of 32 rows (UNIT = 32, E8M0 scales in the tiled layout of the
+// transposed matrix [C][R]): the operands of products that contract over
+// the rows of x.  Same ring and lane map as k_cast_T_tma; each thread's
+// column maxima (8 columns x its 8 rows) are reduced over the 4 lanes that
+// share its columns (a 32-row quarter) and, for 128-row tiles, over the 4
+// quarter warps through shared memory.  Writes the transposed codes qT and,
+// when q is given, the codes in x's layout.
+template <int FMT, int UNIT>
+__global__ void __launch_bounds__(kTThreads, 1)
+    k_quant_col_tma(const __grid_constant__ CUtensorMap tmX, int64_t R, int64_t C, uint8_t* __restrict__ q,
+                    uint8_t* __restrict__ qT, void* scales, unsigned long long* sat)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTStages * kTTile);
+    uint64_t* empty = full + kTStages;
+    __shared__ uint32_t colred[2][4][64];     // [half][quarter][column], 128-row tiles only
+    __shared__ int s_skip;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tiles_c = (int)((C + 127) / 128);
+    const int ntiles = tiles_c * (int)((R + 127) / 128);
+    if (threadIdx.x == 0) {
+        s_skip = *reinterpret_cast<volatile int*>(&g_dev_error_q);
+        for (int i = 0; i < kTStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 8);
+        }
+        fence_mbar_init();
+        prefetch_tmap(&tmX);
+    }
+    __syncthreads();
+    if (s_skip) return;
+    if (warp == 8) {
+        if (lane == 0) {
+            int stage = 0, issued = 0;
+            uint32_t phase = 0;
+            bool aborted = false;
+            for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+                if (!wait_bounded_err(&empty[stage], phase ^ 1u, &g_dev_error_q)) {
+                    aborted = true;
+                    break;
+                }
+                const int c0 = (t % tiles_c) * 128, r0 = (t / tiles_c) * 128;
+                uint8_t* dst = smem + stage * kTTile;
+                mbar_arrive_expect_tx(&full[stage], kTTile);
+                tma_load_2d(dst, &tmX, c0, r0, &full[stage]);
+                tma_load_2d(dst + kTTile / 2, &tmX, c0 + 64, r0, &full[stage]);
+                ++issued;
+                if (++stage == kTStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (aborted) {
+                int n = issued < kTStages ? issued : kTStages;
+                int st = stage;
+                uint32_t ph = phase;
+                for (int i = 0; i < n; ++i) {
+                    if (--st < 0) {
+                        st = kTStages - 1;
+                        ph ^= 1u;
+                    }
+                    wait_drain(&full[st], ph);
+                }
+            }
+        }
+        return;   // the consumers synchronise among themselves (barrier 1, 256 threads)
+    }
+    const int h = warp >> 2, rq = warp & 3, cg = lane & 7, rg = lane >> 3;
+    const int rloc = rq * 32 + rg * 8;
+    const int cloc = h * 64 + cg * 8;
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t nsat = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        const bool ok = wait_bounded_err(&full[stage], phase, &g_dev_error_q);
+        if (UNIT == 128) {
+            // the 8 consumer warps meet at named barrier 1 below, so they
+            // decide together whether to go on (AND over all 256 threads)
+            if (!consumers_all(ok)) break;
+        } else if (!__all_sync(0xFFFFFFFFu, ok)) {
+            break;
+        }
+        const uint8_t* half = smem + stage * kTTile + h * (kTTile / 2);
+        Vec8<kBF16> v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = rloc + i;
+            v[i].w = *reinterpret_cast<const uint4*>(half + r * 128 + ((cg ^ (r & 7)) << 4));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
+        if (++stage == kTStages) {
+            stage = 0;
+            phase ^= 1u;
+        }
+        float f[8][8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i].get(f[i]);
+        // column maxima of the |x| bit patterns over this thread's 8 rows, then
+        // over the quarter's 32 rows (lanes cg, cg+8, cg+16, cg+24)
+        uint32_t cm[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            uint32_t a = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a = max(a, __float_as_uint(f[i][j]) & 0x7FFFFFFFu);
+            a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 8));
+            a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 16));
+            cm[j] = a;
+        }
+        if (UNIT == 128) {
+            if (rg == 0) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) colred[h][rq][cg * 8 + j] = cm[j];
+            }
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                cm[j] = max(max(colred[h][0][cg * 8 + j], colred[h][1][cg * 8 + j]),
+                            max(colred[h][2][cg * 8 + j], colred[h][3][cg * 8 + j]));
+            asm volatile("bar.sync 1, 256;" ::: "memory");   // colred is rewritten by the next tile
+        }
+        float m[8], sc[8];
+        uint32_t code[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (UNIT == 32) code[j] = mx_scale<FMT>(cm[j], m[j]);
+            else current_scale<FMT>(cm[j], m[j], sc[j]);
+        }
+        uint2 rows[8];
+        uint32_t ns = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float p[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                p[j] = __fmul_rn(f[i][j], m[j]);
+                ns += (fabsf(p[j]) > Fmt<FMT>::fmax) ? 1u : 0u;
+            }
+            rows[i].x = cvt_fp8x2<FMT>(p[0], p[1]) | (cvt_fp8x2<FMT>(p[2], p[3]) << 16);
+            rows[i].y = cvt_fp8x2<FMT>(p[4], p[5]) | (cvt_fp8x2<FMT>(p[6], p[7]) << 16);
+        }
+        const int64_t tr0 = (int64_t)(t / tiles_c) * 128;
+        const int64_t r0 = tr0 + rloc;
+        const int64_t c0 = (int64_t)(t % tiles_c) * 128 + cloc;
+        if (r0 < R && c0 < C) {
+            nsat += ns;
+            if (q) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(q + (r0 + i) * C + c0) = rows[i];
+            }
+            uint2 cols[8];
+            transpose8x8(rows, cols);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) *reinterpret_cast<uint2*>(qT + (c0 + j) * R + r0) = cols[j];
+            if (rg == 0) {
+                if (UNIT == 128) {
+                    if (rq == 0) {
+                        float* s_out = static_cast<float*>(scales) + (tr0 / 128) * C + c0;
+                        *reinterpret_cast<float4*>(s_out) = make_float4(sc[0], sc[1], sc[2], sc[3]);
+                        *reinterpret_cast<float4*>(s_out + 4) = make_float4(sc[4], sc[5], sc[6], sc[7]);
+                    }
+                } else {
+                    uint8_t* e = static_cast<uint8_t*>(scales);
+                    const int64_t t32 = (tr0 + rq * 32) / 32;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) e[mx_tiled_offset(c0 + j, t32, R)] = (uint8_t)code[j];
+                }
+            }
+        }
+    }
+    if (sat) add_sat(sat, nsat);
+}
+
 int read_device_error_quant(int clear)
 {
     int v = 0;
@@ -536,16 +738,6 @@ int read_device_error_quant(int clear)
 // consecutive lanes, each holding one 128-bit chunk; units never straddle a
 // row because cols % UNIT == 0, so the tensor is treated as flat.
 // WRITE_Q = false computes the unit amaxes only (fp8_amax).
-// MX scales: the canonical layout is u8 [rows][cols/32]; the tiled layout
-// (TILED = true) is the one the block-scaled GEMM copies straight into tensor
-// memory: 512-byte chunks of 128 rows x 4 consecutive 32-blocks, chunk
-// (r/128, t/4) at ((r/128) * (cols/128) + t/4) * 512, inside it
-// (r % 32) * 16 + ((r / 32) % 4) * 4 + t % 4.
-__device__ __forceinline__ int64_t mx_tiled_offset(int64_t r, int64_t t, int64_t cols)
-{
-    return ((r >> 7) * (cols >> 7) + (t >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (t & 3);
-}
-
 template <int DT, int FMT, int UNIT, bool WRITE_Q, bool TILED = false>
 __global__ void __launch_bounds__(kFlatThreads) k_quant_rowunits(const void* __restrict__ x, int64_t n,
                                                                  uint8_t* __restrict__ q, void* scales,
@@ -602,10 +794,13 @@ __global__ void __launch_bounds__(kFlatThreads) k_quant_rowunits(const void* __r
 // ================================================================== 128x128 blocks
 // One CTA per block, 256 threads, 8x8 elements per thread (same warp layout
 // as k_cast_tensor_T); block amax through shared memory, then the cast.
+// With qT, the block's transposed codes go to qT [C][R] and its scale to
+// sT[C/128][R/128] (the 128x128 blocks of x^T are x's blocks transposed).
 template <int DT, int FMT, bool WRITE_Q>
 __global__ void __launch_bounds__(256) k_quant_block128(const void* __restrict__ x, int64_t R, int64_t C,
                                                         uint8_t* __restrict__ q, float* s_out,
-                                                        float* amax_out, unsigned long long* sat)
+                                                        float* amax_out, unsigned long long* sat,
+                                                        uint8_t* __restrict__ qT = nullptr, float* sT = nullptr)
 {
     __shared__ uint32_t red[8];
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
@@ -624,14 +819,23 @@ __global__ void __launch_bounds__(256) k_quant_block128(const void* __restrict__
     if (threadIdx.x == 0) {
         if (amax_out) amax_out[unit] = __uint_as_float(a);
         if (WRITE_Q) s_out[unit] = s;
+        if (WRITE_Q && sT) sT[(int64_t)blockIdx.x * gridDim.y + blockIdx.y] = s;
     }
     if (!WRITE_Q) return;
     uint32_t nsat = 0;
+    uint2 rows[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         float f[8];
         v[i].get(f);
-        *reinterpret_cast<uint2*>(q + (r0 + i) * C + c0) = cast8<FMT>(f, m, nsat);
+        rows[i] = cast8<FMT>(f, m, nsat);
+        *reinterpret_cast<uint2*>(q + (r0 + i) * C + c0) = rows[i];
+    }
+    if (qT) {
+        uint2 cols[8];
+        transpose8x8(rows, cols);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) *reinterpret_cast<uint2*>(qT + (c0 + j) * R + r0) = cols[j];
     }
     if (sat) add_sat(sat, nsat);
 }
@@ -767,8 +971,20 @@ static cudaError_t quant_dt_fmt(const QuantArgs& a, cudaStream_t st, int sms)
     case kMXTiled:
         k_quant_rowunits<DT, FMT, 32, true, true><<<flat_grid(n / 8, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
         break;
+    case kTileCol:
+    case kMXCol: {
+        CUtensorMap tm;
+        if (!encode_tmap_2d(&tm, 1, a.x, (uint64_t)a.cols, (uint64_t)a.rows, 64u, 128u)) return cudaErrorInvalidValue;
+        const int64_t tiles = ((a.rows + 127) / 128) * ((a.cols + 127) / 128);
+        const int grid = (int)(tiles < sms ? tiles : sms);
+        auto kern = a.gran == kTileCol ? k_quant_col_tma<FMT, 128> : k_quant_col_tma<FMT, 32>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
+        if (e != cudaSuccess) return e;
+        kern<<<grid, kTThreads, kTSmem, st>>>(tm, a.rows, a.cols, a.q, a.qT, a.scales, a.sat);
+        break;
+    }
     case kBlock:
-        k_quant_block128<DT, FMT, true><<<dim3((unsigned)(a.cols / 128), (unsigned)(a.rows / 128)), 256, 0, st>>>(a.x, a.rows, a.cols, a.q, static_cast<float*>(a.scales), a.amax, a.sat);
+        k_quant_block128<DT, FMT, true><<<dim3((unsigned)(a.cols / 128), (unsigned)(a.rows / 128)), 256, 0, st>>>(a.x, a.rows, a.cols, a.q, static_cast<float*>(a.scales), a.amax, a.sat, a.qT, a.scalesT);
         break;
     }
     return cudaGetLastError();

@@ -22,7 +22,7 @@ def test_exports_every_declared_symbol(L):
                           "fp8_scale_init", "fp8_linear_workspace_bytes", "fp8_device_status"}
     for n in names:
         assert hasattr(L, n), n
-    assert L.fp8_abi_version() == 1
+    assert L.fp8_abi_version() == 2
 
 
 def test_null_and_enum_validation(L):
@@ -51,6 +51,11 @@ def test_quantize_validation(L):
     # transposed copy / delayed state only per tensor
     assert q(f, 0, 128, 128, 0, sq.TILE_1x128, None, 0, f, f, f, None, None, None) == sq.ERR_UNSUPPORTED
     assert q(f, 0, 128, 128, 0, sq.TILE_1x128, f, 16, f, None, f, None, None, None) == sq.ERR_UNSUPPORTED
+    # column units: qT required, bf16 only, rows % 128
+    assert q(f, 0, 256, 128, 0, sq.TILE_128x1, None, 0, None, None, f, None, None, None) == sq.ERR_INVALID_ARG
+    assert q(f, 1, 256, 128, 0, sq.TILE_128x1, None, 0, None, f, f, None, None, None) == sq.ERR_UNSUPPORTED
+    assert q(f, 0, 200, 128, 0, sq.TILE_128x1, None, 0, None, f, f, None, None, None) == sq.ERR_UNSUPPORTED
+    assert q(f, 0, 256, 96, 0, sq.MX32_COL_TILED, None, 0, None, f, f, None, None, None) == sq.ERR_UNSUPPORTED
     # missing scales for a block granularity
     assert q(f, 0, 128, 128, 0, sq.MX32, None, 0, f, None, None, None, None, None) == sq.ERR_INVALID_ARG
     # bad history length
@@ -86,7 +91,12 @@ def test_linear_validation_and_workspace(L):
     assert fwd(f, f, 256, 512, 384, 0, 0, None, None, 0, P(4096 + 16), ws, None, f, 0, None) == sq.ERR_MISALIGNED
     assert fwd(f, f, 200, 512, 384, 1, 0, None, None, 0, f, 1 << 30, None, f, 0, None) == sq.ERR_UNSUPPORTED
     bwd = L.fp8_linear_bwd
-    assert bwd(f, 256, 512, 384, 5, None, 0, f, ws, f, f, None) == sq.ERR_INVALID_ARG
+    assert bwd(f, 256, 512, 384, 0, 5, None, 0, f, ws, f, f, None) == sq.ERR_INVALID_ARG       # recipe
+    assert bwd(f, 256, 512, 384, 9, 0, None, 0, f, ws, f, f, None) == sq.ERR_INVALID_ARG       # gran
+    assert bwd(f, 256, 512, 384, 1, 0, f, 16, f, 1 << 30, f, f, None) == sq.ERR_UNSUPPORTED   # delayed + tiles
+    # the fine-grained layouts hold the column-unit codes and scales of x, W and dy too
+    assert sq.fp8_linear_workspace_bytes(256, 512, 384, sq.TILE_1x128) >= 2 * (256 * 384 + 512 * 384 + 256 * 512)
+    assert sq.fp8_linear_workspace_bytes(256, 512, 384, sq.MX32) >= 2 * (256 * 384 + 512 * 384 + 256 * 512)
 
 
 def test_update_scale_validation(L):

@@ -281,3 +281,26 @@ def test_w4_mx_full_size_sampled_rows():
     ah = o.dequantize(codes(qa[rows]), 0, o.GRAN_MX32, ea_c[rows])
     bh = o.dequantize(codes(qb), 0, o.GRAN_MX32, eb_c)
     assert_gemm_close(D[rows], o.gemm_ref(ah, bh))
+
+
+@pytest.mark.parametrize("Mt,N,K", [(256, 384, 256), (384, 256, 512)])
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+def test_column_tile_gemm_vs_oracle(Mt, N, K, out):
+    """Mode for wgrad: both operands are the transposed codes of 128x1
+    column-tile quantisations (contraction over the original rows Mt)."""
+    dy = wl.normal((Mt, N), 1e-3, 91 + Mt)
+    x = wl.student_t3((Mt, K), 92 + K)
+    qdT = torch.empty((N, Mt), dtype=torch.uint8, device=DEV)
+    qxT = torch.empty((K, Mt), dtype=torch.uint8, device=DEV)
+    sd = torch.empty((Mt // 128) * N, dtype=torch.float32, device=DEV)
+    sx = torch.empty((Mt // 128) * K, dtype=torch.float32, device=DEV)
+    sq.fp8_quantize(dy.to(DEV), sq.E5M2, sq.TILE_128x1, None, qT=qdT, scales_out=sd)
+    sq.fp8_quantize(x.to(DEV), sq.E4M3, sq.TILE_128x1, None, qT=qxT, scales_out=sx)
+    D = torch.empty((N, K), dtype=out, device=DEV)
+    sq.fp8_gemm(qdT, sq.E5M2, sd, sq.TILE_128x1, qxT, sq.E4M3, sx, sq.TILE_128x1, D)
+    torch.cuda.synchronize()
+    rqd, rsd, _, _ = o.quantize_tile128x1(np32(dy), o.E5M2)
+    rqx, rsx, _, _ = o.quantize_tile128x1(np32(x), o.E4M3)
+    R = o.gemm_ref(o.dequantize(rqd, o.E5M2, o.GRAN_TILE_128x1, rsd).T,
+                   o.dequantize(rqx, o.E4M3, o.GRAN_TILE_128x1, rsx).T)
+    assert_gemm_close(D, R)

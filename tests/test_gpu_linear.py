@@ -181,3 +181,27 @@ def test_mx_linear_forward():
     qw, ew, _, _ = o.quantize_mx32(np32(w), o.E4M3)
     R = o.gemm_ref(o.dequantize(qx, 0, o.GRAN_MX32, ex), o.dequantize(qw, 0, o.GRAN_MX32, ew))
     assert_gemm_close(y, R)
+
+
+@pytest.mark.parametrize("gran", [sq.TILE_1x128, sq.MX32])
+@pytest.mark.parametrize("recipe", [sq.RECIPE_E4M3, sq.RECIPE_HYBRID])
+def test_fine_grained_linear_forward_and_backward(gran, recipe):
+    """1x128 / 128x128 (and MX-32) forward, dgrad and wgrad, each operand
+    quantised along its own contraction dimension, against the oracle."""
+    M, K, N = 256, 384, 512
+    x = wl.student_t3((M, K), 101).to(DEV)
+    w = wl.normal((N, K), 0.02, 102).to(DEV)
+    dy = wl.normal((M, N), 1e-3, 103).to(DEV)
+    ws = torch.empty(sq.fp8_linear_workspace_bytes(M, N, K, gran), dtype=torch.uint8, device=DEV)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device=DEV)
+    dw = torch.empty((N, K), dtype=torch.float32, device=DEV)
+    sq.fp8_linear_fwd(x, w, y, ws, gran=gran)
+    sq.fp8_linear_bwd(dy, dx, dw, ws, K, gran=gran, recipe=recipe)
+    torch.cuda.synchronize()
+    og = o.GRAN_TILE_1x128 if gran == sq.TILE_1x128 else o.GRAN_MX32
+    st, Y = o.linear_fine_fwd(np32(x), np32(w), og)
+    dX, dW = o.linear_fine_bwd(st, np32(dy), og, o.E5M2 if recipe == sq.RECIPE_HYBRID else o.E4M3)
+    assert_gemm_close(y, Y)
+    assert_gemm_close(dx, dX)
+    assert_gemm_close(dw, dW)

@@ -273,3 +273,75 @@ def test_mx32_tiled_scales(fmt, shape):
     rq, re, _, _ = o.quantize_mx32(np32(x), fmt)
     assert np.array_equal(codes(q), rq)
     assert np.array_equal(mx_untile(e.cpu().numpy(), R, C), re)
+
+
+@pytest.mark.parametrize("H", [1, 1024])
+def test_history_length_variants(H):
+    """The tutorial's suggested amax_history_len=1024 (and the degenerate 1):
+    40 steps of cast + update with a spike, bit-exact against the oracle."""
+    states = torch.empty(2 * (H + 2), dtype=torch.float32, device=DEV)
+    sq.fp8_scale_init(states, 2, H)
+    ref = [o.state_init(H) for _ in range(2)]
+    fmts = [sq.E4M3, sq.E5M2]
+    g = torch.Generator().manual_seed(H)
+    for step in range(40):
+        for r in range(2):
+            x = (torch.randn((32, 256), generator=g) * (1.0 + (step % 7))).to(torch.bfloat16)
+            if step == 3:
+                x[0, 0] = 3000.0
+            q = _u8((32, 256))
+            sq.fp8_quantize(x.to(DEV), fmts[r], sq.TENSOR, q, delayed_state=states[r * (H + 2):(r + 1) * (H + 2)],
+                            history_len=H)
+            o.quantize_delayed(np32(x), fmts[r], ref[r])
+        sq.fp8_update_scale(states, 2, H, fmts)
+        for r in range(2):
+            o.update_scale(ref[r], fmts[r])
+    torch.cuda.synchronize()
+    assert states.cpu().numpy().tobytes() == np.concatenate(ref).tobytes()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape", [(256, 384), (128, 144), (384, 128)])
+def test_column_tiles_128x1(fmt, shape):
+    R, C = shape
+    x = wl.student_t3(shape, 61 + R + C)
+    x[130 % R, 5] = 900.0
+    q, qT = _u8(shape), _u8((C, R))
+    s = _f32((R // 128) * C)
+    sat = torch.zeros(1, dtype=torch.int64, device=DEV)
+    sq.fp8_quantize(x.to(DEV), fmt, sq.TILE_128x1, q, qT=qT, scales_out=s, sat_count=sat)
+    torch.cuda.synchronize()
+    rq, rs, _, rsat = o.quantize_tile128x1(np32(x), fmt)
+    assert np.array_equal(codes(q), rq)
+    assert np.array_equal(codes(qT), rq.T)
+    assert np.array_equal(s.cpu().numpy(), rs.ravel())
+    assert int(sat.item()) == rsat
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape", [(256, 384), (128, 128)])
+def test_column_mx_blocks(fmt, shape):
+    from _helpers import mx_untile
+    R, C = shape
+    x = wl.with_scaled_fraction(shape, 0.01, 100.0, 71 + R)
+    x[32:64, 3] = 0.0
+    qT = _u8((C, R))
+    e = _u8(R * C // 32)
+    sq.fp8_quantize(x.to(DEV), fmt, sq.MX32_COL_TILED, None, qT=qT, scales_out=e)
+    torch.cuda.synchronize()
+    rq, re, _, _ = o.quantize_mx32_col(np32(x), fmt)
+    assert np.array_equal(codes(qT), rq.T)
+    # the tiled scales belong to qT = [C][R]; canonical qT scales are re^T
+    assert np.array_equal(mx_untile(e.cpu().numpy(), C, R), re.T)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_block_128x128_with_transpose(fmt):
+    x = wl.normal((256, 384), 0.02, 81)
+    q, qT = _u8((256, 384)), _u8((384, 256))
+    s = _f32(6)
+    sq.fp8_quantize(x.to(DEV), fmt, sq.BLOCK_128x128, q, qT=qT, scales_out=s)
+    torch.cuda.synchronize()
+    rq, rs, _, _ = o.quantize_block128(np32(x), fmt)
+    assert np.array_equal(codes(q), rq) and np.array_equal(codes(qT), rq.T)
+    assert np.array_equal(s.cpu().numpy(), rs.ravel())
