@@ -36,6 +36,7 @@ E4M3, E5M2 = 0, 1
 ALGO_MAX, ALGO_MOST_RECENT = 0, 1
 GRAN_TENSOR, GRAN_TILE_1x128, GRAN_BLOCK_128x128, GRAN_MX32 = 0, 1, 2, 3
 GRAN_TILE_128x1, GRAN_MX32_COL = 4, 5   # column units (128 or 32 consecutive rows of a column)
+GRAN_TILE_POW2, GRAN_BLOCK_POW2 = 6, 7   # 1x128 / 128x128 units with power-of-two (E8M0) scales
 FMAX = {E4M3: 448.0, E5M2: 57344.0}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -81,6 +82,10 @@ def _load():
                 "orc_quantize_block128": (c.c_int64, [P, c.c_int64, c.c_int64, c.c_int, P, P, P]),
                 "orc_mx_scale_code": (c.c_uint8, [c.c_float, c.c_int]),
                 "orc_quantize_tile128x1": (c.c_int64, [P, c.c_int64, c.c_int64, c.c_int, P, P, P]),
+                "orc_mx_scale_code_floor": (c.c_uint8, [c.c_float, c.c_int]),
+                "orc_quantize_mx32_floor": (c.c_int64, [P, c.c_int64, c.c_int64, c.c_int, P, P]),
+                "orc_quantize_tile1x128_pow2": (c.c_int64, [P, c.c_int64, c.c_int64, c.c_int, P, P]),
+                "orc_quantize_block128_pow2": (c.c_int64, [P, c.c_int64, c.c_int64, c.c_int, P, P]),
                 "orc_quantize_mx32_col": (c.c_int64, [P, c.c_int64, c.c_int64, c.c_int, P, P, P]),
                 "orc_quantize_mx32": (c.c_int64, [P, c.c_int64, c.c_int64, c.c_int, P, P, P]),
                 "orc_state_init": (None, [P, c.c_int]),
@@ -252,6 +257,27 @@ def quantize_mx32_col(x, fmt: int):
     return q, e, am, int(sat)
 
 
+def mx_scale_code_floor(a: float, fmt: int) -> int:
+    return int(_load().orc_mx_scale_code_floor(float(np.float32(a)), fmt))
+
+
+def _e8m0_quantizer(name, shape_fn):
+    def f(x, fmt: int):
+        a = _f32(x)
+        R, C = a.shape
+        q = np.empty((R, C), dtype=np.uint8)
+        e = np.empty(shape_fn(R, C), dtype=np.uint8)
+        sat = getattr(_load(), name)(_p(a), R, C, fmt, _p(q), _p(e))
+        return q, e, int(sat)
+    return f
+
+
+# recipe variants: OCP-floor MX exponent; power-of-two 1x128 / 128x128 scales
+quantize_mx32_floor = _e8m0_quantizer("orc_quantize_mx32_floor", lambda R, C: (R, C // 32))
+quantize_tile1x128_pow2 = _e8m0_quantizer("orc_quantize_tile1x128_pow2", lambda R, C: (R, C // 128))
+quantize_block128_pow2 = _e8m0_quantizer("orc_quantize_block128_pow2", lambda R, C: (R // 128, C // 128))
+
+
 # ---------------------------------------------------------------- delayed state
 def state_init(H: int) -> np.ndarray:
     st = np.empty(H + 2, dtype=np.float32)
@@ -278,7 +304,7 @@ def update_scale(state: np.ndarray, fmt: int, algo: int = ALGO_MAX) -> None:
 def dequantize(q: np.ndarray, fmt: int, gran: int, scales) -> np.ndarray:
     q = np.ascontiguousarray(q, dtype=np.uint8)
     R, C = q.shape
-    if gran in (GRAN_MX32, GRAN_MX32_COL):
+    if gran in (GRAN_MX32, GRAN_MX32_COL, GRAN_TILE_POW2, GRAN_BLOCK_POW2):
         sc = np.ascontiguousarray(scales, dtype=np.uint8)
     else:
         sc = np.ascontiguousarray(np.atleast_1d(np.asarray(scales, dtype=np.float32)))

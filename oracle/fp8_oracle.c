@@ -265,6 +265,82 @@ uint8_t orc_mx_scale_code(float amax, int fmt)
     return (uint8_t)(e + 127);
 }
 
+/* The OCP MX convention's exponent (a recipe variant, not the pages'):
+ * e = floor(log2(amax)) - emax, so a block whose largest significand
+ * exceeds 1.75 clips at fmax.  Same clamping and special codes as above. */
+uint8_t orc_mx_scale_code_floor(float amax, int fmt)
+{
+    if (!isfinite(amax)) return 0xFF;
+    if (amax == 0.0f) return 127;
+    int emax = (fmt == ORC_E4M3) ? 8 : 15;
+    int E;
+    frexp((double)amax, &E);
+    int e = (E - 1) - emax;
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return (uint8_t)(e + 127);
+}
+
+int64_t orc_quantize_mx32_floor(const float* x, int64_t R, int64_t C, int fmt, uint8_t* q,
+                                uint8_t* e8m0_out)
+{
+    int64_t T = C / 32, sat = 0;
+    #pragma omp parallel for reduction(+:sat) schedule(static)
+    for (int64_t r = 0; r < R; ++r) {
+        for (int64_t t = 0; t < T; ++t) {
+            const float* u = x + r * C + t * 32;
+            uint8_t code = orc_mx_scale_code_floor(orc_amax(u, 32), fmt);
+            float m = (code == 0xFF) ? 1.0f : (float)ldexp(1.0, -((int)code - 127));
+            e8m0_out[r * T + t] = code;
+            sat += quant_run(u, 32, 1, m, fmt, q + r * C + t * 32, 1);
+        }
+    }
+    return sat;
+}
+
+/* Power-of-two scales for 1x128 tiles and 128x128 blocks (a recipe variant:
+ * the scale of each unit restricted to a power of two, by the same rule as
+ * the MX blocks -- the smallest 2^e with amax <= fmax * 2^e).  Output: E8M0
+ * codes, e_tile[R][C/128] / e_block[R/128][C/128]. */
+int64_t orc_quantize_tile1x128_pow2(const float* x, int64_t R, int64_t C, int fmt, uint8_t* q,
+                                    uint8_t* e_out)
+{
+    int64_t T = C / 128, sat = 0;
+    #pragma omp parallel for reduction(+:sat) schedule(static)
+    for (int64_t r = 0; r < R; ++r) {
+        for (int64_t t = 0; t < T; ++t) {
+            const float* u = x + r * C + t * 128;
+            uint8_t code = orc_mx_scale_code(orc_amax(u, 128), fmt);
+            float m = (code == 0xFF) ? 1.0f : (float)ldexp(1.0, -((int)code - 127));
+            e_out[r * T + t] = code;
+            sat += quant_run(u, 128, 1, m, fmt, q + r * C + t * 128, 1);
+        }
+    }
+    return sat;
+}
+
+int64_t orc_quantize_block128_pow2(const float* x, int64_t R, int64_t C, int fmt, uint8_t* q,
+                                   uint8_t* e_out)
+{
+    int64_t BR = R / 128, BC = C / 128, sat = 0;
+    #pragma omp parallel for reduction(+:sat) schedule(static)
+    for (int64_t bi = 0; bi < BR; ++bi) {
+        for (int64_t bj = 0; bj < BC; ++bj) {
+            float a = 0.0f;
+            for (int64_t r = 0; r < 128; ++r)
+                a = amax2(a, orc_amax(x + (bi * 128 + r) * C + bj * 128, 128));
+            uint8_t code = orc_mx_scale_code(a, fmt);
+            float m = (code == 0xFF) ? 1.0f : (float)ldexp(1.0, -((int)code - 127));
+            e_out[bi * BC + bj] = code;
+            for (int64_t r = 0; r < 128; ++r) {
+                int64_t off = (bi * 128 + r) * C + bj * 128;
+                sat += quant_run(x + off, 128, 1, m, fmt, q + off, 1);
+            }
+        }
+    }
+    return sat;
+}
+
 int64_t orc_quantize_mx32(const float* x, int64_t R, int64_t C, int fmt, uint8_t* q,
                           uint8_t* e8m0_out, float* amax_out)
 {
@@ -383,7 +459,9 @@ void orc_update_scale(float* state, int H, int fmt, int algo)
  * at most 4 significant bits and s is an fp32, so the product is exact.
  * gran: 0 tensor (s[0]), 1 tile 1x128 (s[R][C/128]), 2 block 128x128
  * (s[R/128][C/128]), 3 MX-32 (E8M0 codes u8[R][C/32]), 4 column tile 128x1
- * (s[R/128][C]), 5 column MX-32 (E8M0 codes u8[R/32][C]).
+ * (s[R/128][C]), 5 column MX-32 (E8M0 codes u8[R/32][C]), 6 power-of-two 1x128
+ * tiles (E8M0 codes u8[R][C/128]), 7 power-of-two 128x128 blocks (E8M0 codes
+ * u8[R/128][C/128]).
  * ---------------------------------------------------------------------- */
 void orc_dequantize(const uint8_t* q, int64_t R, int64_t C, int fmt, int gran,
                     const void* scales, double* out)
@@ -398,6 +476,10 @@ void orc_dequantize(const uint8_t* q, int64_t R, int64_t C, int fmt, int gran,
             else if (gran == 4) s = ((const float*)scales)[(r / 128) * C + c];
             else if (gran == 5) {
                 uint8_t code = ((const uint8_t*)scales)[(r / 32) * C + c];
+                s = (code == 0xFF) ? NAN : ldexp(1.0, (int)code - 127);
+            } else if (gran == 6 || gran == 7) {
+                uint8_t code = (gran == 6) ? ((const uint8_t*)scales)[r * (C / 128) + c / 128]
+                                           : ((const uint8_t*)scales)[(r / 128) * (C / 128) + c / 128];
                 s = (code == 0xFF) ? NAN : ldexp(1.0, (int)code - 127);
             } else {
                 uint8_t code = ((const uint8_t*)scales)[r * (C / 32) + c / 32];

@@ -216,3 +216,45 @@ def test_fine_grained_backward_close_to_exact(gran):
     for got, exact in ((y, x64 @ w64.T), (dX, d64 @ w64), (dW, d64.T @ x64)):
         assert got.shape == exact.shape
         assert np.max(np.abs(got - exact)) / np.max(np.abs(exact)) < 0.1
+
+
+@pytest.mark.parametrize("fmt", [o.E4M3, o.E5M2])
+def test_mx_floor_rule_closed_form(fmt):
+    """The floor rule is the ceiling rule minus one exactly when the block
+    maximum's significand exceeds 1.75; only then does it clip."""
+    fm = o.fmax(fmt)
+    for k in range(-10, 11):
+        exact = fm * 2.0 ** k                        # significand 1.75: same code, no clipping
+        assert o.mx_scale_code_floor(exact, fmt) == o.mx_scale_code(exact, fmt)
+        above = float(np.nextafter(np.float32(exact), np.float32(np.inf)))
+        assert o.mx_scale_code_floor(above, fmt) == o.mx_scale_code(above, fmt) - 1
+        one = 2.0 ** (k + 3)                         # significand 1.0
+        assert o.mx_scale_code_floor(one, fmt) == o.mx_scale_code(one, fmt)
+    x = np.full((1, 32), 1.0, np.float32)
+    x[0, 0] = np.float32(1.9 * 2.0 ** 5)
+    q, e, sat = o.quantize_mx32_floor(x, fmt)
+    assert sat == 1 and (q[0, 0] & 0x7F) == (0x7E if fmt == o.E4M3 else 0x7B)
+    _, _, _, sat_ceil = o.quantize_mx32(x, fmt)
+    assert sat_ceil == 0
+
+
+@pytest.mark.parametrize("fmt", [o.E4M3, o.E5M2])
+def test_pow2_tiles_and_blocks(fmt):
+    """A power-of-two 1x128 tile scale is the largest of its four MX-32 codes
+    (the code is monotone in amax); a 128x128 block's is the largest over its
+    tiles.  Codes are the cast with that exact power of two; nothing clips."""
+    rng = np.random.default_rng(14)
+    x = (rng.standard_normal((256, 384)) * np.exp(rng.standard_normal((256, 1)))).astype(np.float32)
+    x[3, 200] = 5000.0
+    q, e, sat = o.quantize_tile1x128_pow2(x, fmt)
+    _, emx, _, _ = o.quantize_mx32(x, fmt)
+    assert np.array_equal(e, emx.reshape(256, 3, 4).max(axis=2)) and sat == 0
+    for (r, t) in [(0, 0), (3, 1), (255, 2)]:
+        m = 2.0 ** -(int(e[r, t]) - 127)
+        qq, _ = o.quantize_with_multiplier(x[r, 128 * t:128 * t + 128], np.float32(m), fmt)
+        assert np.array_equal(q[r, 128 * t:128 * t + 128], qq)
+    qb, eb, satb = o.quantize_block128_pow2(x, fmt)
+    assert np.array_equal(eb, e.reshape(2, 128, 3).max(axis=1)) and satb == 0
+    one = o.encode(fmt, 1.0)
+    assert np.array_equal(o.dequantize(np.full((256, 384), one, np.uint8), fmt, o.GRAN_BLOCK_POW2, eb),
+                          np.repeat(np.repeat(2.0 ** (eb.astype(np.float64) - 127), 128, 0), 128, 1))
