@@ -78,6 +78,10 @@ extern "C" {
 #define FP8SQ_MX32_TILED 4     /* MX32 with the scales in the GEMM's tiled layout */
 #define FP8SQ_TILE_128x1 5     /* one scale per 128 consecutive values of a column */
 #define FP8SQ_MX32_COL_TILED 6 /* one E8M0 scale per 32 values of a column, tiled  */
+/* recipe variants with E8M0 scales in the tiled layout (GEMM-ready):       */
+#define FP8SQ_TILE_1x128_POW2 7     /* 1x128 tiles, power-of-two scale        */
+#define FP8SQ_BLOCK_128x128_POW2 8  /* 128x128 blocks, power-of-two scale     */
+#define FP8SQ_MX32_FLOOR_TILED 9    /* MX-32 with the OCP floor exponent rule */
 
 /* Tiled MX scale layout (FP8SQ_MX32_TILED), for a tensor [rows][cols] with
  * rows % 128 == 0 and cols % 128 == 0: the E8M0 code of row r, 32-block
@@ -168,6 +172,14 @@ FP8SQ_API int fp8_update_scale(float* states, int n_states, int history_len, con
  *       f32 [rows/128][cols] (TILE_128x1), or the E8M0 codes of qT's 32-value
  *       row blocks in the tiled layout of the [cols][rows] matrix qT
  *       (MX32_COL_TILED).
+ *     TILE_1x128_POW2 / BLOCK_128x128_POW2 / MX32_FLOOR_TILED (recipe
+ *       variants; rows, cols % 128 == 0): the unit's scale is a power of two,
+ *       written as an E8M0 code into the tiled layout above, repeated over
+ *       every 32-value block the unit covers, so the codes feed the
+ *       block-scaled GEMM.  POW2: the smallest 2^e with amax <= fmax * 2^e
+ *       (nothing clips).  FLOOR: e = floor(log2 amax) - emax, the OCP MX
+ *       convention, which clips a block whose largest significand exceeds
+ *       1.75 (sat_count counts those elements).
  *   q         device u8 [rows][cols], 16-byte aligned
  *   qT        device u8 [cols][rows] (the transposed codes) or NULL; for
  *             TENSOR (same scale; rows, cols % 16 == 0) and BLOCK_128x128
@@ -203,7 +215,8 @@ FP8SQ_API int fp8_quantize(const void* x, int x_dtype, int64_t rows, int64_t col
  *       contraction runs over the original rows): a_scale f32 [K/128][M],
  *       b_scale f32 [K/128][N]; every K block's partial is promoted with
  *       sA[kb][m] * sB[kb][n]; K % 128 == 0.
- *     (MX32_TILED or MX32_COL_TILED, same for B): a_scale, b_scale u8 E8M0
+ *     (any of MX32_TILED, MX32_COL_TILED, TILE_1x128_POW2, BLOCK_128x128_POW2,
+ *      MX32_FLOOR_TILED for each operand): a_scale, b_scale u8 E8M0
  *       in the tiled layout of the operand (as written by fp8_quantize
  *       MX32_TILED for q, or MX32_COL_TILED for qT), 16-byte aligned;
  *       D = sum_k dec(qA) 2^(eA - 127) dec(qB) 2^(eB - 127) on the

@@ -15,6 +15,7 @@ import threading
 E4M3, E5M2 = 0, 1
 BF16, F32 = 0, 1
 TENSOR, TILE_1x128, BLOCK_128x128, MX32, MX32_TILED, TILE_128x1, MX32_COL_TILED = 0, 1, 2, 3, 4, 5, 6
+TILE_1x128_POW2, BLOCK_128x128_POW2, MX32_FLOOR_TILED = 7, 8, 9
 AMAX_MAX, AMAX_MOST_RECENT = 0, 1
 RECIPE_HYBRID, RECIPE_E4M3 = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WRONG_ARCH, ERR_CUDA, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6

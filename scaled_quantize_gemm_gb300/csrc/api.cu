@@ -64,9 +64,13 @@ int cuda_status(cudaError_t e, const char* what)
 
 bool valid_format(int f) { return f == FP8SQ_E4M3 || f == FP8SQ_E5M2; }
 bool valid_dtype(int d) { return d == FP8SQ_BF16 || d == FP8SQ_F32; }
-bool valid_gran(int g) { return g >= FP8SQ_TENSOR && g <= FP8SQ_MX32_COL_TILED; }
+bool valid_gran(int g) { return g >= FP8SQ_TENSOR && g <= FP8SQ_MX32_FLOOR_TILED; }
 bool column_gran(int g) { return g == FP8SQ_TILE_128x1 || g == FP8SQ_MX32_COL_TILED; }
-bool mx_tiled(int g) { return g == FP8SQ_MX32_TILED || g == FP8SQ_MX32_COL_TILED; }
+bool e8m0_tiled(int g)
+{
+    return g == FP8SQ_MX32_TILED || g == FP8SQ_MX32_COL_TILED || g == FP8SQ_TILE_1x128_POW2 ||
+           g == FP8SQ_BLOCK_128x128_POW2 || g == FP8SQ_MX32_FLOOR_TILED;
+}
 
 const int64_t kMaxDim = (int64_t)1 << 31;  // GEMM / TMA coordinates are 32-bit
 
@@ -79,7 +83,7 @@ int check_units(int gran, int64_t rows, int64_t cols)
         return fail(FP8SQ_ERR_UNSUPPORTED, "128x128 blocks need rows, cols %% 128 == 0 (%lld x %lld)", (long long)rows, (long long)cols);
     if (gran == FP8SQ_MX32 && cols % 32)
         return fail(FP8SQ_ERR_UNSUPPORTED, "MX-32 blocks need cols %% 32 == 0 (cols = %lld)", (long long)cols);
-    if ((gran == FP8SQ_MX32_TILED || gran == FP8SQ_MX32_COL_TILED) && (rows % 128 || cols % 128))
+    if (e8m0_tiled(gran) && (rows % 128 || cols % 128))
         return fail(FP8SQ_ERR_UNSUPPORTED, "tiled MX-32 scales need rows, cols %% 128 == 0 (%lld x %lld)", (long long)rows, (long long)cols);
     if (gran == FP8SQ_TILE_128x1 && (rows % 128 || cols % 16))
         return fail(FP8SQ_ERR_UNSUPPORTED, "128x1 column tiles need rows %% 128 == 0 and cols %% 16 == 0 (%lld x %lld)", (long long)rows, (long long)cols);
@@ -163,7 +167,7 @@ FP8SQ_API int fp8_amax(const void* x, int x_dtype, int64_t rows, int64_t cols, i
                        void* stream)
 {
     if ((!x && rows * cols != 0) || !amax_out) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_amax: null pointer");
-    if (!valid_dtype(x_dtype) || !valid_gran(gran) || gran == FP8SQ_MX32_TILED || column_gran(gran))
+    if (!valid_dtype(x_dtype) || !valid_gran(gran) || gran > FP8SQ_MX32)
         return fail(FP8SQ_ERR_INVALID_ARG, "fp8_amax: bad dtype or granularity");
     if (rows < 0 || cols < 0) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_amax: negative size");
     if (!aligned16(x)) return fail(FP8SQ_ERR_MISALIGNED, "fp8_amax: x must be 16-byte aligned");
@@ -238,6 +242,8 @@ static int validate_quantize(const void* x, int x_dtype, int64_t rows, int64_t c
         if (qT && !(gran == FP8SQ_BLOCK_128x128 || column_gran(gran)))
             return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_quantize: a transposed copy needs TENSOR, BLOCK_128x128 or a column granularity");
         if (!scales) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize: scales_out is required for this granularity");
+        if (e8m0_tiled(gran) && !aligned16(scales))
+            return fail(FP8SQ_ERR_MISALIGNED, "fp8_quantize: tiled E8M0 scales must be 16-byte aligned");
         if (column_gran(gran)) {
             if (!qT && rows * cols != 0) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize: column granularities need qT");
             if (x_dtype != FP8SQ_BF16) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_quantize: column granularities need bf16 input");
@@ -304,7 +310,7 @@ static int validate_gemm(const uint8_t* A, int a_format, const void* a_scale, in
         if (!aligned16(a_scale) || !aligned16(b_scale))
             return fail(FP8SQ_ERR_MISALIGNED, "fp8_gemm: column-tile scales must be 16-byte aligned");
         *mode = 3;
-    } else if (mx_tiled(a_gran) && mx_tiled(b_gran)) {
+    } else if (e8m0_tiled(a_gran) && e8m0_tiled(b_gran)) {
         if (!aligned16(a_scale) || !aligned16(b_scale))
             return fail(FP8SQ_ERR_MISALIGNED, "fp8_gemm: tiled MX scales must be 16-byte aligned");
         if (M % 128 || N % 128 || K % 128)

@@ -9,7 +9,8 @@ namespace fp8sq {
 
 enum { kE4M3 = 0, kE5M2 = 1 };
 enum { kBF16 = 0, kF32 = 1 };
-enum { kTensor = 0, kTile = 1, kBlock = 2, kMX = 3, kMXTiled = 4, kTileCol = 5, kMXCol = 6 };
+enum { kTensor = 0, kTile = 1, kBlock = 2, kMX = 3, kMXTiled = 4, kTileCol = 5, kMXCol = 6,
+       kTilePow2 = 7, kBlockPow2 = 8, kMXFloor = 9 };
 
 struct QuantArgs {
     const void* x = nullptr;

@@ -146,6 +146,20 @@ __device__ __forceinline__ uint32_t mx_scale(uint32_t amax_bits, float& m)
     return (uint32_t)(e + 127);
 }
 
+// MX by the OCP floor rule: e = floor(log2 amax) - emax (can clip)
+template <int FMT>
+__device__ __forceinline__ uint32_t mx_scale_floor(uint32_t amax_bits, float& m)
+{
+    if (amax_bits >= 0x7F800000u) { m = 1.0f; return 0xFFu; }
+    if (amax_bits == 0u) { m = 1.0f; return 127u; }
+    uint32_t ef = amax_bits >> 23;
+    const int E = (ef == 0u) ? (31 - __clz(amax_bits & 0x7FFFFFu)) - 149 : (int)ef - 127;
+    int e = E - Fmt<FMT>::emax;
+    e = max(-127, min(127, e));
+    m = (e <= 126) ? __uint_as_float((uint32_t)(127 - e) << 23) : __uint_as_float(0x00400000u);
+    return (uint32_t)(e + 127);
+}
+
 // cast 8 values with multiplier m; returns 8 codes packed little-endian
 template <int FMT>
 __device__ __forceinline__ uint2 cast8(const float (&f)[8], float m, uint32_t& nsat)
@@ -738,7 +752,11 @@ int read_device_error_quant(int clear)
 // consecutive lanes, each holding one 128-bit chunk; units never straddle a
 // row because cols % UNIT == 0, so the tensor is treated as flat.
 // WRITE_Q = false computes the unit amaxes only (fp8_amax).
-template <int DT, int FMT, int UNIT, bool WRITE_Q, bool TILED = false>
+// RULE: 0 = current fp32 scale (1x128 tiles); 1 = E8M0, smallest power of two
+// that fits (MX-32 blocks, and power-of-two 1x128 tiles); 2 = E8M0 by the
+// OCP floor rule (MX-32 blocks).  A power-of-two 1x128 tile writes its code
+// into all four 32-blocks it covers in the tiled layout.
+template <int DT, int FMT, int UNIT, bool WRITE_Q, bool TILED = false, int RULE = (UNIT == 32 ? 1 : 0)>
 __global__ void __launch_bounds__(kFlatThreads) k_quant_rowunits(const void* __restrict__ x, int64_t n,
                                                                  uint8_t* __restrict__ q, void* scales,
                                                                  float* amax_out, unsigned long long* sat,
@@ -768,7 +786,8 @@ __global__ void __launch_bounds__(kFlatThreads) k_quant_rowunits(const void* __r
             if (WRITE_Q) {
                 float m, s = 0.0f;
                 uint32_t code = 0;
-                if (UNIT == 32) code = mx_scale<FMT>(a, m);
+                if (RULE == 1) code = mx_scale<FMT>(a, m);
+                else if (RULE == 2) code = mx_scale_floor<FMT>(a, m);
                 else current_scale<FMT>(a, m, s);
                 float f[8];
                 v[u].get(f);
@@ -778,11 +797,18 @@ __global__ void __launch_bounds__(kFlatThreads) k_quant_rowunits(const void* __r
                     nsat += ns;
                     *reinterpret_cast<uint2*>(q + c * 8) = codes;
                     if (leader) {
-                        if (UNIT == 32 && TILED)
-                            static_cast<uint8_t*>(scales)[mx_tiled_offset(unit / (cols / 32), unit % (cols / 32), cols)] =
-                                (uint8_t)code;
-                        else if (UNIT == 32) static_cast<uint8_t*>(scales)[unit] = (uint8_t)code;
-                        else static_cast<float*>(scales)[unit] = s;
+                        if (RULE == 0) {
+                            static_cast<float*>(scales)[unit] = s;
+                        } else if (TILED) {
+                            constexpr int SUB = UNIT / 32;      // 32-blocks per unit
+                            const int64_t per_row = cols / UNIT;
+                            const int64_t r = unit / per_row, t = unit % per_row;
+#pragma unroll
+                            for (int i = 0; i < SUB; ++i)
+                                static_cast<uint8_t*>(scales)[mx_tiled_offset(r, t * SUB + i, cols)] = (uint8_t)code;
+                        } else {
+                            static_cast<uint8_t*>(scales)[unit] = (uint8_t)code;
+                        }
                     }
                 }
             }
@@ -796,11 +822,15 @@ __global__ void __launch_bounds__(kFlatThreads) k_quant_rowunits(const void* __r
 // as k_cast_tensor_T); block amax through shared memory, then the cast.
 // With qT, the block's transposed codes go to qT [C][R] and its scale to
 // sT[C/128][R/128] (the 128x128 blocks of x^T are x's blocks transposed).
-template <int DT, int FMT, bool WRITE_Q>
+// POW2: the block scale is the smallest power of two that fits (E8M0); its
+// code fills the block's whole 512-byte chunk of the tiled MX layout (all 128
+// rows x four 32-blocks), so the block feeds the block-scaled GEMM directly.
+template <int DT, int FMT, bool WRITE_Q, bool POW2 = false>
 __global__ void __launch_bounds__(256) k_quant_block128(const void* __restrict__ x, int64_t R, int64_t C,
                                                         uint8_t* __restrict__ q, float* s_out,
                                                         float* amax_out, unsigned long long* sat,
-                                                        uint8_t* __restrict__ qT = nullptr, float* sT = nullptr)
+                                                        uint8_t* __restrict__ qT = nullptr, float* sT = nullptr,
+                                                        uint8_t* e_tiled = nullptr)
 {
     __shared__ uint32_t red[8];
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
@@ -814,12 +844,20 @@ __global__ void __launch_bounds__(256) k_quant_block128(const void* __restrict__
     for (int i = 0; i < 8; ++i) mx = max(mx, v[i].absmax_bits());
     const uint32_t a = block_max_bits<8>(mx, red);
     const int64_t unit = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;
-    float m, s;
-    current_scale<FMT>(a, m, s);
+    float m, s = 0.0f;
+    if (POW2) {
+        const uint32_t code = mx_scale<FMT>(a, m);
+        if (WRITE_Q) {
+            const uint16_t two = (uint16_t)(code | (code << 8));
+            reinterpret_cast<uint16_t*>(e_tiled + unit * 512)[threadIdx.x] = two;
+        }
+    } else {
+        current_scale<FMT>(a, m, s);
+    }
     if (threadIdx.x == 0) {
         if (amax_out) amax_out[unit] = __uint_as_float(a);
-        if (WRITE_Q) s_out[unit] = s;
-        if (WRITE_Q && sT) sT[(int64_t)blockIdx.x * gridDim.y + blockIdx.y] = s;
+        if (WRITE_Q && !POW2) s_out[unit] = s;
+        if (WRITE_Q && !POW2 && sT) sT[(int64_t)blockIdx.x * gridDim.y + blockIdx.y] = s;
     }
     if (!WRITE_Q) return;
     uint32_t nsat = 0;
@@ -970,6 +1008,15 @@ static cudaError_t quant_dt_fmt(const QuantArgs& a, cudaStream_t st, int sms)
         break;
     case kMXTiled:
         k_quant_rowunits<DT, FMT, 32, true, true><<<flat_grid(n / 8, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
+        break;
+    case kTilePow2:
+        k_quant_rowunits<DT, FMT, 128, true, true, 1><<<flat_grid(n / 8, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
+        break;
+    case kMXFloor:
+        k_quant_rowunits<DT, FMT, 32, true, true, 2><<<flat_grid(n / 8, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
+        break;
+    case kBlockPow2:
+        k_quant_block128<DT, FMT, true, true><<<dim3((unsigned)(a.cols / 128), (unsigned)(a.rows / 128)), 256, 0, st>>>(a.x, a.rows, a.cols, a.q, nullptr, a.amax, a.sat, nullptr, nullptr, static_cast<uint8_t*>(a.scales));
         break;
     case kTileCol:
     case kMXCol: {

@@ -304,3 +304,27 @@ def test_column_tile_gemm_vs_oracle(Mt, N, K, out):
     R = o.gemm_ref(o.dequantize(rqd, o.E5M2, o.GRAN_TILE_128x1, rsd).T,
                    o.dequantize(rqx, o.E4M3, o.GRAN_TILE_128x1, rsx).T)
     assert_gemm_close(D, R)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 384, 512), (4096, 4096, 4096)])
+def test_pow2_tiles_blocks_on_block_scaled_mma(M, N, K):
+    """Power-of-two 1x128 tiles x power-of-two 128x128 blocks run on the
+    block-scaled MMA (no promotion): parity with the oracle's product of the
+    exactly dequantised operands (sampled rows at the full workload-3 size)."""
+    x = wl.student_t3((M, K), 121 + M)
+    w = wl.normal((N, K), 0.02, 122 + N)
+    qx, qw = torch.empty((M, K), dtype=torch.uint8, device=DEV), torch.empty((N, K), dtype=torch.uint8, device=DEV)
+    ex = torch.empty(M * K // 32, dtype=torch.uint8, device=DEV)
+    ew = torch.empty(N * K // 32, dtype=torch.uint8, device=DEV)
+    sq.fp8_quantize(x.to(DEV), sq.E4M3, sq.TILE_1x128_POW2, qx, scales_out=ex)
+    sq.fp8_quantize(w.to(DEV), sq.E4M3, sq.BLOCK_128x128_POW2, qw, scales_out=ew)
+    D = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    sq.fp8_gemm(qx, sq.E4M3, ex, sq.TILE_1x128_POW2, qw, sq.E4M3, ew, sq.BLOCK_128x128_POW2, D)
+    torch.cuda.synchronize()
+    rqx, rex, _ = o.quantize_tile1x128_pow2(np32(x), o.E4M3)
+    rqw, rew, _ = o.quantize_block128_pow2(np32(w), o.E4M3)
+    assert np.array_equal(codes(qx), rqx) and np.array_equal(codes(qw), rqw)
+    rows = _sample_rows(M, min(M, 128), 11)
+    ah = o.dequantize(rqx[rows], o.E4M3, o.GRAN_TILE_POW2, rex[rows])
+    bh = o.dequantize(rqw, o.E4M3, o.GRAN_BLOCK_POW2, rew)
+    assert_gemm_close(D[rows], o.gemm_ref(ah, bh))

@@ -345,3 +345,33 @@ def test_block_128x128_with_transpose(fmt):
     rq, rs, _, _ = o.quantize_block128(np32(x), fmt)
     assert np.array_equal(codes(q), rq) and np.array_equal(codes(qT), rq.T)
     assert np.array_equal(s.cpu().numpy(), rs.ravel())
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_pow2_tiles_blocks_and_floor_mx(fmt):
+    """Recipe variants: power-of-two 1x128 tiles, power-of-two 128x128 blocks
+    and the OCP-floor MX rule, all with E8M0 codes in the tiled layout."""
+    from _helpers import mx_untile
+    R, C = 256, 384
+    x = wl.with_scaled_fraction((R, C), 0.01, 100.0, 111)
+    x[7, 40] = 1.9 * 2 ** 10                       # significand > 1.75: the floor rule clips it
+    xd = x.to(DEV)
+    xf = np32(x)
+    q, e = _u8((R, C)), _u8(R * C // 32)
+    sat = torch.zeros(1, dtype=torch.int64, device=DEV)
+    sq.fp8_quantize(xd, fmt, sq.TILE_1x128_POW2, q, scales_out=e, sat_count=sat)
+    torch.cuda.synchronize()
+    rq, re, rsat = o.quantize_tile1x128_pow2(xf, fmt)
+    assert np.array_equal(codes(q), rq) and int(sat.item()) == rsat == 0
+    assert np.array_equal(mx_untile(e.cpu().numpy(), R, C), np.repeat(re, 4, axis=1))
+    sq.fp8_quantize(xd, fmt, sq.BLOCK_128x128_POW2, q, scales_out=e)
+    torch.cuda.synchronize()
+    rq, re, _ = o.quantize_block128_pow2(xf, fmt)
+    assert np.array_equal(codes(q), rq)
+    assert np.array_equal(mx_untile(e.cpu().numpy(), R, C), np.repeat(np.repeat(re, 128, axis=0), 4, axis=1))
+    sat.zero_()
+    sq.fp8_quantize(xd, fmt, sq.MX32_FLOOR_TILED, q, scales_out=e, sat_count=sat)
+    torch.cuda.synchronize()
+    rq, re, rsat = o.quantize_mx32_floor(xf, fmt)
+    assert np.array_equal(codes(q), rq) and int(sat.item()) == rsat >= 1
+    assert np.array_equal(mx_untile(e.cpu().numpy(), R, C), re)
