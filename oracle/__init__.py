@@ -83,6 +83,7 @@ def _load():
                 "orc_mx_scale_code": (c.c_uint8, [c.c_float, c.c_int]),
                 "orc_quantize_tile128x1": (c.c_int64, [P, c.c_int64, c.c_int64, c.c_int, P, P, P]),
                 "orc_mx_scale_code_floor": (c.c_uint8, [c.c_float, c.c_int]),
+                "orc_layernorm": (None, [P, c.c_int64, c.c_int64, P, P, c.c_double, P, P, P]),
                 "orc_quantize_mx32_floor": (c.c_int64, [P, c.c_int64, c.c_int64, c.c_int, P, P]),
                 "orc_quantize_tile1x128_pow2": (c.c_int64, [P, c.c_int64, c.c_int64, c.c_int, P, P]),
                 "orc_quantize_block128_pow2": (c.c_int64, [P, c.c_int64, c.c_int64, c.c_int, P, P]),
@@ -276,6 +277,40 @@ def _e8m0_quantizer(name, shape_fn):
 quantize_mx32_floor = _e8m0_quantizer("orc_quantize_mx32_floor", lambda R, C: (R, C // 32))
 quantize_tile1x128_pow2 = _e8m0_quantizer("orc_quantize_tile1x128_pow2", lambda R, C: (R, C // 128))
 quantize_block128_pow2 = _e8m0_quantizer("orc_quantize_block128_pow2", lambda R, C: (R // 128, C // 128))
+
+
+def layernorm(x, gamma, beta=None, eps: float = 1e-5):
+    """-> (y float64 [R][K], mean float64 [R], rstd float64 [R])"""
+    a = _f32(x)
+    R, K = a.shape
+    g = _f32(gamma)
+    b = None if beta is None else _f32(beta)
+    y = np.empty((R, K), dtype=np.float64)
+    mu = np.empty(R, dtype=np.float64)
+    rs = np.empty(R, dtype=np.float64)
+    _load().orc_layernorm(_p(a), R, K, _p(g), _p(b), float(eps), _p(y), _p(mu), _p(rs))
+    return y, mu, rs
+
+
+def ln_acceptable_codes(y: np.ndarray, delta: np.ndarray, m: float, fmt: int):
+    """Codes reachable from a LayerNorm output known to within +-delta of the
+    exact y (the reduction order of an implementation is not specified):
+    (nearest code of fp32(y) * m, lowest and highest code over the interval).
+    Casting is monotone, so every code in between is reachable too."""
+    yf = y.astype(np.float32)
+    m32 = np.float32(m)
+    lo = (y - delta).astype(np.float32)
+    hi = (y + delta).astype(np.float32)
+    def enc(v):
+        q, _ = quantize_with_multiplier(v, m32, fmt)
+        return q
+    return enc(yf), enc(lo), enc(hi)
+
+
+def code_rank(q: np.ndarray) -> np.ndarray:
+    """Order-preserving integer for FP8 codes (sign-magnitude -> signed)."""
+    q = q.astype(np.int32)
+    return np.where(q & 0x80, -(q & 0x7F), q & 0x7F)
 
 
 # ---------------------------------------------------------------- delayed state

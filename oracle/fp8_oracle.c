@@ -410,6 +410,32 @@ int64_t orc_quantize_mx32_col(const float* x, int64_t R, int64_t C, int fmt, uin
 }
 
 /* ------------------------------------------------------------------------
+ * 7c. LayerNorm in front of a linear layer (the Transformer Engine
+ * tutorial's te.LayerNormLinear / te.LayerNorm; the pages give no formula,
+ * so the standard one): per row, mean = sum(x)/K, var = sum((x-mean)^2)/K,
+ * rstd = 1/sqrt(var + eps), y = (x - mean) * rstd * gamma + beta.  Computed
+ * in double; y_out is double [R][K], mu / rstd double [R].
+ * ---------------------------------------------------------------------- */
+void orc_layernorm(const float* x, int64_t R, int64_t K, const float* gamma, const float* beta, double eps,
+                   double* y_out, double* mu_out, double* rstd_out)
+{
+    #pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < R; ++r) {
+        const float* row = x + r * K;
+        double sum = 0.0;
+        for (int64_t k = 0; k < K; ++k) sum += row[k];
+        double mean = sum / (double)K;
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; ++k) ss += (row[k] - mean) * (row[k] - mean);
+        double rstd = 1.0 / sqrt(ss / (double)K + eps);
+        mu_out[r] = mean;
+        rstd_out[r] = rstd;
+        for (int64_t k = 0; k < K; ++k)
+            y_out[r * K + k] = (row[k] - mean) * rstd * (double)gamma[k] + (beta ? (double)beta[k] : 0.0);
+    }
+}
+
+/* ------------------------------------------------------------------------
  * 8. Delayed scaling with an amax history.
  * [TS] core vocabulary: delayed scaling "uses historical amax" to set the
  * scale, avoiding a read of the tensor before the cast, at the cost of lag;

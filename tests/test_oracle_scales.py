@@ -258,3 +258,34 @@ def test_pow2_tiles_and_blocks(fmt):
     one = o.encode(fmt, 1.0)
     assert np.array_equal(o.dequantize(np.full((256, 384), one, np.uint8), fmt, o.GRAN_BLOCK_POW2, eb),
                           np.repeat(np.repeat(2.0 ** (eb.astype(np.float64) - 127), 128, 0), 128, 1))
+
+
+def test_layernorm_closed_forms():
+    """Standardised output: every row has mean 0 and variance var/(var+eps)
+    before the affine part; gamma scales and beta shifts column-wise; a
+    constant row gives beta exactly."""
+    rng = np.random.default_rng(15)
+    x = (rng.standard_normal((8, 256)) * 3 + 2).astype(np.float32)
+    x[5, :] = 7.0
+    g = np.ones(256, np.float32)
+    y, mu, rs = o.layernorm(x, g, None, 1e-5)
+    assert np.allclose(mu, x.astype(np.float64).mean(axis=1), rtol=0, atol=1e-12)
+    var = x.astype(np.float64).var(axis=1)
+    assert np.allclose(rs, 1 / np.sqrt(var + 1e-5), rtol=1e-14)
+    assert np.allclose(y.mean(axis=1), 0, atol=1e-12)
+    assert np.allclose(y[:5].var(axis=1), var[:5] / (var[:5] + 1e-5), rtol=1e-12)
+    gam = rng.uniform(0.5, 2, 256).astype(np.float32)
+    bet = rng.standard_normal(256).astype(np.float32)
+    y2, _, _ = o.layernorm(x, gam, bet, 1e-5)
+    assert np.allclose(y2, y * gam + bet, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(y2[5], bet.astype(np.float64))
+
+
+def test_ln_acceptable_codes_bracket():
+    y = np.array([1.0, 67.9999, 68.0001, -3.0], dtype=np.float64)     # 68 = E4M3 midpoint of 64 and 72
+    delta = np.full(4, 1e-3)
+    near, lo, hi = o.ln_acceptable_codes(y, delta, 1.0, o.E4M3)
+    r = o.code_rank
+    assert np.all(r(lo) <= r(near)) and np.all(r(near) <= r(hi))
+    assert lo[1] != hi[1] and lo[2] != hi[2]            # ambiguous next to the midpoint
+    assert lo[0] == hi[0] and lo[3] == hi[3]            # unambiguous elsewhere
