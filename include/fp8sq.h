@@ -265,6 +265,34 @@ FP8SQ_API int fp8_linear_bwd(const void* dy, int64_t M, int64_t N, int64_t K, in
                              float* dy_state, int history_len, void* workspace, size_t ws_bytes,
                              void* dx, float* dw, void* stream);
 
+/* ---- 5a. LayerNorm fused into the cast ---------------------------------
+ * [TE] te.LayerNorm / te.LayerNormLinear: the normalisation in front of a
+ * linear layer, fused here with the amax and the FP8 cast so the bf16
+ * LayerNorm output never goes to HBM.  Per row r of x [M][K] (bf16):
+ *   mu[r] = sum(x)/K, var = sum((x - mu)^2)/K, rstd[r] = 1/sqrt(var + eps),
+ *   y = (x - mu[r]) * rstd[r] * gamma[c] + beta[c]      (fp32 arithmetic)
+ * then q = sat_RNE_fp8(y * m) with delayed per-tensor scaling: m = state[H],
+ * amax(|y|) max-combined into state[0] (as fp8_quantize TENSOR + delayed).
+ *   gamma, beta  device f32 [K] (beta may be NULL)
+ *   q            device u8 [M][K]; qT device u8 [K][M] or NULL
+ *   mu_out, rstd_out  device f32 [M], required (the LayerNorm backward needs them)
+ *   M % 16 == 0, K % 16 == 0; x, q, qT 16-byte aligned.
+ * The row statistics are fp32 reductions whose order is this library's; the
+ * codes equal those of the exact LayerNorm except where y * m lies within the
+ * reductions' rounding error of a midpoint between two codes.
+ * fp8_layernorm_linear_fwd: the same cast of x, then the per-tensor delayed
+ * linear forward of fp8_linear_fwd (W cast, GEMM) with the TENSOR workspace
+ * layout, so fp8_linear_bwd (gran TENSOR) runs the backward of the linear.
+ */
+FP8SQ_API int fp8_layernorm_quantize(const void* x, const float* gamma, const float* beta, float eps,
+                                     int64_t M, int64_t K, int format, float* delayed_state, int history_len,
+                                     uint8_t* q, uint8_t* qT, float* mu_out, float* rstd_out, void* stream);
+FP8SQ_API int fp8_layernorm_linear_fwd(const void* x, const float* gamma, const float* beta, float eps,
+                                       const void* w, int64_t M, int64_t N, int64_t K, float* x_state,
+                                       float* w_state, int history_len, void* workspace, size_t ws_bytes,
+                                       float* mu_out, float* rstd_out, const float* bias, void* y, int y_dtype,
+                                       void* stream);
+
 /* ---- 5b. forward linear without allocation --------------------------------
  * The pages have no counterpart to this entry point; it exists for callers
  * that cannot call cudaMalloc or hand over a workspace -- code running inside

@@ -62,6 +62,9 @@ def lib() -> ctypes.CDLL:
                 "fp8_linear_fwd": (I, [P, P, I64, I64, I64, I, I, P, P, I, P, Z, P, P, I, P]),
                 "fp8_linear_bwd": (I, [P, I64, I64, I64, I, I, P, I, P, Z, P, P, P]),
                 "fp8_linear_fwd_noalloc": (I, [P, P, I64, I64, I64, P, P, I, P]),
+                "fp8_layernorm_quantize": (I, [P, P, P, c.c_float, I64, I64, I, P, I, P, P, P, P, P]),
+                "fp8_layernorm_linear_fwd": (I, [P, P, P, c.c_float, P, I64, I64, I64, P, P, I, P, Z, P, P, P, P,
+                                                 I, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -154,6 +157,23 @@ def fp8_linear_bwd(dy, dx, dw, workspace, K: int, gran: int = TENSOR, recipe: in
     _check(lib().fp8_linear_bwd(_ptr(dy), M, N, K, gran, recipe, _ptr(dy_state), history_len, _ptr(workspace),
                                 workspace.numel() * workspace.element_size(), _ptr(dx), _ptr(dw),
                                 _stream(stream)))
+
+
+def fp8_layernorm_quantize(x, gamma, beta, eps: float, format: int, q, qT, mu, rstd, delayed_state,
+                           history_len: int, stream=None) -> None:
+    M, K = x.shape
+    _check(lib().fp8_layernorm_quantize(_ptr(x), _ptr(gamma), _ptr(beta), eps, M, K, format, _ptr(delayed_state),
+                                        history_len, _ptr(q), _ptr(qT), _ptr(mu), _ptr(rstd), _stream(stream)))
+
+
+def fp8_layernorm_linear_fwd(x, gamma, beta, eps: float, w, y, workspace, mu, rstd, x_state, w_state,
+                             history_len: int, bias=None, stream=None) -> None:
+    M, K = x.shape
+    N = w.shape[0]
+    _check(lib().fp8_layernorm_linear_fwd(_ptr(x), _ptr(gamma), _ptr(beta), eps, _ptr(w), M, N, K, _ptr(x_state),
+                                          _ptr(w_state), history_len, _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(), _ptr(mu), _ptr(rstd),
+                                          _ptr(bias), _ptr(y), _dtype_code(y), _stream(stream)))
 
 
 def fp8_linear_fwd_noalloc(x, w, y, bias=None, stream=None) -> None:

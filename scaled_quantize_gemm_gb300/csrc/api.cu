@@ -536,4 +536,75 @@ FP8SQ_API int fp8_linear_bwd(const void* dy, int64_t M, int64_t N, int64_t K, in
     return cuda_status(fp8sq::launch_gemm(wg, st, sms, &why), why ? why : "fp8_linear_bwd: wgrad");
 }
 
+static int validate_ln(const void* x, const float* gamma, const float* beta, int64_t M, int64_t K, int format,
+                       const float* state, int H, const uint8_t* q, const uint8_t* qT, const float* mu,
+                       const float* rstd)
+{
+    if (!x || !gamma || !q || !state || !mu || !rstd) return fail(FP8SQ_ERR_INVALID_ARG, "layernorm: null pointer");
+    if (!valid_format(format)) return fail(FP8SQ_ERR_INVALID_ARG, "layernorm: bad format");
+    if (M < 0 || K < 0) return fail(FP8SQ_ERR_INVALID_ARG, "layernorm: negative size");
+    if (M >= kMaxDim || K >= kMaxDim) return fail(FP8SQ_ERR_UNSUPPORTED, "layernorm: dimension too large");
+    if (M % 16 || K % 16) return fail(FP8SQ_ERR_UNSUPPORTED, "layernorm: needs M, K %% 16 == 0");
+    if (H < 1 || H > 4096) return fail(FP8SQ_ERR_INVALID_ARG, "layernorm: bad history_len");
+    if (!aligned16(x) || !aligned16(q) || (qT && !aligned16(qT)))
+        return fail(FP8SQ_ERR_MISALIGNED, "layernorm: x, q, qT must be 16-byte aligned");
+    if (!aligned4(gamma) || (beta && !aligned4(beta)) || !aligned4(state) || !aligned4(mu) || !aligned4(rstd))
+        return fail(FP8SQ_ERR_MISALIGNED, "layernorm: gamma, beta, state, mu, rstd must be 4-byte aligned");
+    return FP8SQ_OK;
+}
+
+FP8SQ_API int fp8_layernorm_quantize(const void* x, const float* gamma, const float* beta, float eps, int64_t M,
+                                     int64_t K, int format, float* delayed_state, int history_len, uint8_t* q,
+                                     uint8_t* qT, float* mu_out, float* rstd_out, void* stream)
+{
+    int r = validate_ln(x, gamma, beta, M, K, format, delayed_state, history_len, q, qT, mu_out, rstd_out);
+    if (r) return r;
+    int sms;
+    if ((r = check_device(&sms))) return r;
+    fp8sq::QuantArgs qa;
+    qa.x = x; qa.x_dtype = fp8sq::kBF16; qa.rows = M; qa.cols = K; qa.format = format;
+    qa.gran = fp8sq::kTensor; qa.state = delayed_state; qa.history_len = history_len; qa.q = q; qa.qT = qT;
+    return cuda_status(fp8sq::launch_layernorm_quantize(qa, gamma, beta, eps, mu_out, rstd_out,
+                                                        static_cast<cudaStream_t>(stream), sms),
+                       "fp8_layernorm_quantize launch");
+}
+
+FP8SQ_API int fp8_layernorm_linear_fwd(const void* x, const float* gamma, const float* beta, float eps, const void* w,
+                                       int64_t M, int64_t N, int64_t K, float* x_state, float* w_state,
+                                       int history_len, void* workspace, size_t ws_bytes, float* mu_out,
+                                       float* rstd_out, const float* bias, void* y, int y_dtype, void* stream)
+{
+    if (!w || !y || !w_state) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_layernorm_linear_fwd: null pointer");
+    if (!valid_dtype(y_dtype)) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_layernorm_linear_fwd: bad y dtype");
+    int r = check_linear_shape(M, N, K, FP8SQ_TENSOR, workspace, ws_bytes);
+    if (r) return r;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const WsLayout L = ws_layout(M, N, K, FP8SQ_TENSOR);
+    r = validate_ln(x, gamma, beta, M, K, FP8SQ_E4M3, x_state, history_len, ws + L.qx, ws + L.qxT, mu_out, rstd_out);
+    if (r) return r;
+    if (!aligned16(w) || !aligned16(y)) return fail(FP8SQ_ERR_MISALIGNED, "fp8_layernorm_linear_fwd: w, y must be 16-byte aligned");
+    if ((bias && !aligned4(bias)) || !aligned4(w_state)) return fail(FP8SQ_ERR_MISALIGNED, "fp8_layernorm_linear_fwd: bias / w_state alignment");
+    int sms;
+    if ((r = check_device(&sms))) return r;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int H = history_len;
+    float* scal = reinterpret_cast<float*>(ws + L.scal);
+    fp8sq::QuantArgs qa;
+    qa.x = x; qa.x_dtype = fp8sq::kBF16; qa.rows = M; qa.cols = K; qa.format = fp8sq::kE4M3;
+    qa.gran = fp8sq::kTensor; qa.state = x_state; qa.history_len = H; qa.q = ws + L.qx; qa.qT = ws + L.qxT;
+    if ((r = cuda_status(fp8sq::launch_layernorm_quantize(qa, gamma, beta, eps, mu_out, rstd_out, st, sms),
+                         "fp8_layernorm_linear_fwd: layernorm cast")))
+        return r;
+    qa.x = w; qa.rows = N; qa.cols = K; qa.state = w_state; qa.q = ws + L.qw; qa.qT = ws + L.qwT;
+    if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_layernorm_linear_fwd: quantize w"))) return r;
+    if ((r = cuda_status(cudaMemcpyAsync(&scal[0], x_state + H + 1, sizeof(float), cudaMemcpyDeviceToDevice, st), "copy s_x"))) return r;
+    if ((r = cuda_status(cudaMemcpyAsync(&scal[1], w_state + H + 1, sizeof(float), cudaMemcpyDeviceToDevice, st), "copy s_w"))) return r;
+    fp8sq::GemmArgs g;
+    g.mode = 0; g.M = M; g.N = N; g.K = K; g.bias = bias; g.D = y; g.d_dtype = y_dtype;
+    g.A = ws + L.qx; g.B = ws + L.qw; g.a_scale = &scal[0]; g.b_scale = &scal[1];
+    g.a_format = g.b_format = fp8sq::kE4M3;
+    const char* why = nullptr;
+    return cuda_status(fp8sq::launch_gemm(g, st, sms, &why), why ? why : "fp8_layernorm_linear_fwd: GEMM");
+}
+
 }  // extern "C"

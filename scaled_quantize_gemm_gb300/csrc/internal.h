@@ -34,6 +34,10 @@ cudaError_t launch_amax(const QuantArgs& a, cudaStream_t st, int sms);    // wri
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st, int sms);
 cudaError_t launch_scale_init(float* states, int n, int H, cudaStream_t st);
 cudaError_t launch_update_scale(float* states, int n, int H, const int* formats, int algo, cudaStream_t st);
+// LayerNorm of bf16 x [rows][cols] fused into the delayed per-tensor cast
+// (a.state required); writes mu, rstd [rows]
+cudaError_t launch_layernorm_quantize(const QuantArgs& a, const float* gamma, const float* beta, float eps,
+                                      float* mu, float* rstd, cudaStream_t st, int sms);
 
 struct GemmArgs {
     const uint8_t* A = nullptr;

@@ -415,11 +415,21 @@ constexpr int kTTile = 128 * 128 * 2;
 constexpr int kTThreads = 288;
 constexpr int kTSmem = kTStages * kTTile + 2 * kTStages * 8 + 1024;
 
-template <int FMT, bool DELAYED>
+// Row-wise LayerNorm folded into the cast (LN = true): x is replaced by
+// y = (x - mu[r]) * rstd[r] * gamma[c] + beta[c] before the multiplier, the
+// amax is taken over y, and the bf16 LayerNorm output never leaves the SM.
+struct LnParams {
+    const float* mu = nullptr;
+    const float* rstd = nullptr;
+    const float* gamma = nullptr;
+    const float* beta = nullptr;
+};
+
+template <int FMT, bool DELAYED, bool LN = false>
 __global__ void __launch_bounds__(kTThreads, 1)
     k_cast_T_tma(const __grid_constant__ CUtensorMap tmX, int64_t R, int64_t C, uint8_t* __restrict__ q,
                  uint8_t* __restrict__ qT, float* state, int H, const float* amax_in, float* s_out, float* amax_out,
-                 unsigned long long* sat)
+                 unsigned long long* sat, LnParams ln = LnParams())
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -508,23 +518,48 @@ __global__ void __launch_bounds__(kTThreads, 1)
             }
             const int64_t r0 = (int64_t)(t / tiles_c) * 128 + rloc;
             const int64_t c0 = (int64_t)(t % tiles_c) * 128 + cloc;
+            const bool inside = r0 < R && c0 < C;
             uint2 rows[8];
             uint32_t ns = 0;
+            if (LN) {
+                float g[8], be[8], mu[8], rs[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                if (DELAYED) mx = max(mx, v[i].absmax_bits());
-                float f[8];
-                v[i].get(f);
-                rows[i] = cast8<FMT>(f, m, ns);
+                for (int j = 0; j < 8; ++j) {
+                    g[j] = inside ? __ldg(ln.gamma + c0 + j) : 0.0f;
+                    be[j] = (inside && ln.beta) ? __ldg(ln.beta + c0 + j) : 0.0f;
+                    mu[j] = inside ? __ldg(ln.mu + r0 + j) : 0.0f;
+                    rs[j] = inside ? __ldg(ln.rstd + r0 + j) : 0.0f;
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float f[8];
+                    v[i].get(f);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        f[j] = __fmaf_rn(__fmul_rn(__fsub_rn(f[j], mu[i]), rs[i]), g[j], be[j]);
+                        if (DELAYED && inside) mx = max(mx, __float_as_uint(f[j]) & 0x7FFFFFFFu);
+                    }
+                    rows[i] = cast8<FMT>(f, m, ns);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (DELAYED) mx = max(mx, v[i].absmax_bits());
+                    float f[8];
+                    v[i].get(f);
+                    rows[i] = cast8<FMT>(f, m, ns);
+                }
             }
-            if (r0 < R && c0 < C) {
+            if (inside) {
                 nsat += ns;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(q + (r0 + i) * C + c0) = rows[i];
-                uint2 cols[8];
-                transpose8x8(rows, cols);
+                if (qT) {
+                    uint2 cols[8];
+                    transpose8x8(rows, cols);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) *reinterpret_cast<uint2*>(qT + (c0 + j) * R + r0) = cols[j];
+                    for (int j = 0; j < 8; ++j) *reinterpret_cast<uint2*>(qT + (c0 + j) * R + r0) = cols[j];
+                }
             }
         }
         if (sat) add_sat(sat, nsat);
@@ -733,6 +768,104 @@ __global__ void __launch_bounds__(kTThreads, 1)
         }
     }
     if (sat) add_sat(sat, nsat);
+}
+
+// LayerNorm statistics, one warp per row: mean = sum(x) / K and
+// var = sum((x - mean)^2) / K in fp32 (per-lane running sums, then a warp
+// tree), rstd = 1 / sqrt(var + eps) with IEEE division and square root.
+// Rows of up to 32 x 8 x LN_REG elements (4096 for LN_REG = 16) are read once
+// into registers with all loads in flight; longer rows take two passes.
+constexpr int LN_REG = 16;
+
+__global__ void __launch_bounds__(256) k_ln_stats(const uint16_t* __restrict__ x, int64_t R, int64_t K, float eps,
+                                                  float* __restrict__ mu, float* __restrict__ rstd)
+{
+    const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= R) return;
+    const uint16_t* row = x + r * K;
+    const int64_t nch = K / 8;
+    float sum = 0.0f, ss = 0.0f, mean;
+    if (nch <= 32 * LN_REG) {
+        Vec8<kBF16> v[LN_REG];
+#pragma unroll
+        for (int i = 0; i < LN_REG; ++i) {
+            const int64_t c = lane + 32 * i;
+            if (c < nch) v[i].load(row, c * 8); else v[i].zero();
+        }
+#pragma unroll
+        for (int i = 0; i < LN_REG; ++i) {
+            float f[8];
+            v[i].get(f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) sum = __fadd_rn(sum, f[j]);
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xFFFFFFFFu, sum, o));
+        mean = __fdiv_rn(sum, (float)K);
+#pragma unroll
+        for (int i = 0; i < LN_REG; ++i) {
+            if (lane + 32 * i >= nch) continue;
+            float f[8];
+            v[i].get(f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float d = __fsub_rn(f[j], mean);
+                ss = __fmaf_rn(d, d, ss);
+            }
+        }
+    } else {
+        for (int64_t c = lane; c < nch; c += 32) {
+            Vec8<kBF16> v;
+            v.load(row, c * 8);
+            float f[8];
+            v.get(f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) sum = __fadd_rn(sum, f[j]);
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xFFFFFFFFu, sum, o));
+        mean = __fdiv_rn(sum, (float)K);
+        for (int64_t c = lane; c < nch; c += 32) {
+            Vec8<kBF16> v;
+            v.load(row, c * 8);
+            float f[8];
+            v.get(f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float d = __fsub_rn(f[j], mean);
+                ss = __fmaf_rn(d, d, ss);
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, o));
+    if (lane == 0) {
+        mu[r] = mean;
+        rstd[r] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)K), eps)));
+    }
+}
+
+cudaError_t launch_layernorm_quantize(const QuantArgs& a, const float* gamma, const float* beta, float eps,
+                                      float* mu, float* rstd, cudaStream_t st, int sms)
+{
+    if (a.rows == 0 || a.cols == 0) return cudaSuccess;
+    k_ln_stats<<<(unsigned)((a.rows + 7) / 8), 256, 0, st>>>(static_cast<const uint16_t*>(a.x), a.rows, a.cols, eps, mu, rstd);
+    CUtensorMap tm;
+    if (!encode_tmap_2d(&tm, 1, a.x, (uint64_t)a.cols, (uint64_t)a.rows, 64u, 128u)) return cudaErrorInvalidValue;
+    const int64_t tiles = ((a.rows + 127) / 128) * ((a.cols + 127) / 128);
+    const int grid = (int)(tiles < sms ? tiles : sms);
+    LnParams ln;
+    ln.mu = mu;
+    ln.rstd = rstd;
+    ln.gamma = gamma;
+    ln.beta = beta;
+    auto kern = a.format == kE4M3 ? k_cast_T_tma<kE4M3, true, true> : k_cast_T_tma<kE5M2, true, true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kTThreads, kTSmem, st>>>(tm, a.rows, a.cols, a.q, a.qT, a.state, a.history_len, nullptr, nullptr,
+                                          a.amax, a.sat, ln);
+    return cudaGetLastError();
 }
 
 int read_device_error_quant(int clear)
@@ -974,9 +1107,11 @@ static cudaError_t quant_dt_fmt(const QuantArgs& a, cudaStream_t st, int sms)
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
             if (e != cudaSuccess) return e;
             if (delayed)
-                kern<<<grid, kTThreads, kTSmem, st>>>(tm, a.rows, a.cols, a.q, a.qT, a.state, H, nullptr, nullptr, a.amax, a.sat);
+                kern<<<grid, kTThreads, kTSmem, st>>>(tm, a.rows, a.cols, a.q, a.qT, a.state, H, nullptr, nullptr, a.amax, a.sat,
+                                                      LnParams());
             else
-                kern<<<grid, kTThreads, kTSmem, st>>>(tm, a.rows, a.cols, a.q, a.qT, nullptr, 0, a.amax, s_out, nullptr, a.sat);
+                kern<<<grid, kTThreads, kTSmem, st>>>(tm, a.rows, a.cols, a.q, a.qT, nullptr, 0, a.amax, s_out, nullptr, a.sat,
+                                                      LnParams());
             return cudaGetLastError();
         }
         if (a.qT) {
