@@ -62,8 +62,8 @@ KERNEL_SOURCES = {   # file, [(start marker or None = file start, end marker)]: 
                                      ("        if (a.qT && DT == kBF16 && n > 0) {", "        if (a.qT) {")]),
 }
 TRAFFIC = {
-    "k_gemm_tensor": {"sha": "6568bca905ceb172", "bytes": 952974080},
-    "k_cast_T_tma": {"sha": "0a76c44e9243e63d", "bytes": 891605760},
+    "k_gemm_tensor": {"sha": "2f94300c74f2a651", "bytes": 965291264},
+    "k_cast_T_tma": {"sha": "2c47d5eb152bb4f2", "bytes": 893085184},
 }
 
 
@@ -359,6 +359,22 @@ def run_ours(args, ws, rank, local):
         states_host = torch.empty(b.states.shape, dtype=torch.float32).pin_memory()
         h2d = sum(x.numel() * x.element_size() + dy.numel() * dy.element_size() for (x, dy) in host_sets[0])
         d2h = states_host.numel() * 4
+        # the host link alone: one step's inputs copied with nothing else running
+        dev_tmp = [(torch.empty_like(x), torch.empty_like(dy)) for (x, dy) in b.inputs[0]]
+        for _ in range(2):
+            for (xh, dyh), (xd, dyd) in zip(host_sets[0], dev_tmp):
+                xd.copy_(xh, non_blocking=True)
+                dyd.copy_(dyh, non_blocking=True)
+        torch.cuda.synchronize()
+        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        l0.record()
+        for (xh, dyh), (xd, dyd) in zip(host_sets[0], dev_tmp):
+            xd.copy_(xh, non_blocking=True)
+            dyd.copy_(dyh, non_blocking=True)
+        l1.record()
+        torch.cuda.synchronize()
+        link_gbs = h2d / (l0.elapsed_time(l1) * 1e-3) / 1e9
+        del dev_tmp
         b.e2e_run(host_sets, args.warmup, states_host)
         torch.cuda.synchronize()
         if ws > 1:
@@ -372,6 +388,8 @@ def run_ours(args, ws, rank, local):
         e2e_ms = _barrier_max(e0.elapsed_time(e1), ws, device) / args.steps
         e2e = {"value": round(ws * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "h2d_link_gbs": round(link_gbs, 1),
+               "h2d_bound_ms": round(h2d / (link_gbs * 1e9) * 1e3, 4),
                "api": "fp8_linear_fwd / fp8_linear_bwd / fp8_update_scale; each step's x and dy copied "
                       "from pinned host memory (next step's copies overlap this step's compute), scale states "
                       "read back every step"}

@@ -103,14 +103,67 @@ __device__ __forceinline__ void store_row32(const EpiParams& p, int row, int col
     }
 }
 
+// Staged TMA store of one warp's 32 rows x SC columns (SC = 32 bytes of the
+// output type: 16 bf16 or 8 fp32).  Each lane writes its row's 32 bytes into
+// the warp's 1 KB shared buffer, then lane 0 issues a bulk tensor store; the
+// tensor map clips rows and columns past the matrix.  The buffer is reused
+// only after the previous store has read it (wait_group.read 0), so skipping
+// a fully out-of-range store never lets a pending one be overwritten.  Writing
+// whole 32-byte row segments through the TMA instead of 16-byte per-lane
+// stores halves the L2 write requests and takes the stores off the LSU.
+constexpr int kStageBytes = 1024;   // per epilogue warp
+
+template <bool OUT_BF16>
+__device__ __forceinline__ void stage_store(uint8_t* buf, const CUtensorMap* tmD, const float* v, int col0, int row0,
+                                            int M, int N, int lane)
+{
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    __syncwarp();
+    uint8_t* rowp = buf + lane * 32;
+    if (OUT_BF16) {
+#pragma unroll
+        for (int q4 = 0; q4 < 2; ++q4) {
+            uint4 w4;
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * q4 + 0], v[8 * q4 + 1]);
+            __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * q4 + 2], v[8 * q4 + 3]);
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * q4 + 4], v[8 * q4 + 5]);
+            __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * q4 + 6], v[8 * q4 + 7]);
+            w4.x = *reinterpret_cast<uint32_t*>(&h0);
+            w4.y = *reinterpret_cast<uint32_t*>(&h1);
+            w4.z = *reinterpret_cast<uint32_t*>(&h2);
+            w4.w = *reinterpret_cast<uint32_t*>(&h3);
+            *reinterpret_cast<uint4*>(rowp + 16 * q4) = w4;
+        }
+    } else {
+        *reinterpret_cast<float4*>(rowp) = make_float4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<float4*>(rowp + 16) = make_float4(v[4], v[5], v[6], v[7]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && col0 < N && row0 < M) {
+        asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                         reinterpret_cast<uint64_t>(tmD)),
+                     "r"(col0), "r"(row0), "r"(smem_addr(buf))
+                     : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+}
+__device__ __forceinline__ void stage_store_drain(int lane)
+{
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
+}
+
 // ------------------------------------------------------------------ shared layout
-template <int BN, int STAGES, int NACC>
+template <int BN, int STAGES, int NACC, int EPI_STAGE_WARPS = 0>
 struct Smem {
     static constexpr int B_BYTES = BN * BK;
     static constexpr int STAGE = A_BYTES + B_BYTES;
     static constexpr int BAR_OFF = STAGES * STAGE;
     static constexpr int NBARS = 2 * STAGES + 2 * NACC + 1;
-    static constexpr int BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;  // + holder + alignment slack
+    static constexpr int STG_OFF = BAR_OFF + 512;                      // epilogue staging (1 KB per warp)
+    static constexpr int BYTES = STG_OFF + EPI_STAGE_WARPS * kStageBytes + 1024;   // + alignment slack
+    static_assert(NBARS * 8 + 16 <= 512, "barriers and the TMEM holder fit before the staging area");
 };
 
 // Common prologue: barriers, tensor memory, early exit if the error word is set.
@@ -200,9 +253,9 @@ __device__ __forceinline__ void producer_loop(uint8_t* smem, uint64_t* full, uin
 template <int BN, int STAGES, bool OUT_BF16>
 __global__ void __launch_bounds__(192, 1)
     k_gemm_tensor(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  EpiParams p, uint32_t idesc, TileSched sched)
+                  EpiParams p, uint32_t idesc, TileSched sched, const __grid_constant__ CUtensorMap tmD)
 {
-    using L = Smem<BN, STAGES, 2>;
+    using L = Smem<BN, STAGES, 2, 4>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
@@ -265,6 +318,8 @@ __global__ void __launch_bounds__(192, 1)
     } else {
         const int quarter = warp & 3;       // the TMEM lane quarter this warp may read
         const float scale = __ldg(p.sA) * __ldg(p.sB);
+        uint8_t* stg = smem + L::STG_OFF + (warp - 2) * kStageBytes;
+        constexpr int SC = OUT_BF16 ? 16 : 8;   // columns per 32-byte staged row segment
         int lt = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++lt) {
             const int b = lt & 1;
@@ -274,7 +329,7 @@ __global__ void __launch_bounds__(192, 1)
             tc_fence_after();
             int mb, nb;
             sched.coords(t, mb, nb);
-            const int row = mb * BM + quarter * 32 + lane;
+            const int row0 = mb * BM + quarter * 32;
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * BN);
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {
@@ -282,20 +337,23 @@ __global__ void __launch_bounds__(192, 1)
                 tmem_ld_32x32b_x32(taddr + (uint32_t)c, r);
                 tmem_ld_wait();
                 float v[32];
-                const int col0 = nb * BN + c;
+                const int colc = nb * BN + c;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * scale;
                 if (p.bias) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (col0 + j < p.N) v[j] += __ldg(p.bias + col0 + j);
+                        if (colc + j < p.N) v[j] += __ldg(p.bias + colc + j);
                 }
-                store_row32<OUT_BF16>(p, row, col0, v);
+#pragma unroll
+                for (int h = 0; h < 32 / SC; ++h)
+                    stage_store<OUT_BF16>(stg, &tmD, v + h * SC, colc + h * SC, row0, p.M, p.N, lane);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&aempty[b]);
         }
+        stage_store_drain(lane);
     }
     __syncthreads();
     if (warp == 1) {
@@ -578,7 +636,8 @@ struct MxLayout {
     static constexpr int SF_OFF = STAGES * STAGE;
     static constexpr int BAR_OFF = SF_OFF + STAGES * SF_STAGE;
     static constexpr int NBARS = 2 * STAGES + 2 * NACC + 1;
-    static constexpr int BYTES = BAR_OFF + NBARS * 8 + 16 + 1024;
+    static constexpr int STG_OFF = BAR_OFF + 512;        // epilogue staging, 1 KB per warp
+    static constexpr int BYTES = STG_OFF + 8 * kStageBytes + 1024;
     static constexpr int SF_COL0 = NACC * BN;            // first scale-factor TMEM column
     static constexpr int SF_COLS = 4 * (1 + CH);         // per stage
     static_assert(SF_COL0 + STAGES * SF_COLS <= 512, "tensor memory budget");
@@ -606,8 +665,9 @@ struct MxParams {
 template <int BN, int STAGES, int NACC, bool OUT_BF16, int EPI = 4>
 __global__ void __launch_bounds__(64 + 32 * EPI, 1)
     k_gemm_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, EpiParams p,
-              uint32_t idesc, TileSched sched, MxParams mx)
+              uint32_t idesc, TileSched sched, MxParams mx, const __grid_constant__ CUtensorMap tmD)
 {
+    static_assert(EPI <= 8, "staging area holds 8 warps");
     using L = MxLayout<BN, STAGES, NACC>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -723,6 +783,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
         constexpr int COLS = BN / PARTS;
         const int quarter = warp & 3;
         const int part = (warp - 2) >> 2;
+        uint8_t* stg = smem + L::STG_OFF + (warp - 2) * kStageBytes;
+        constexpr int SC = OUT_BF16 ? 16 : 8;
         int lt = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++lt) {
             const int b = lt % NACC;
@@ -732,7 +794,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
             tc_fence_after();
             int mb, nb;
             sched.coords(t, mb, nb);
-            const int row = mb * BM + quarter * 32 + lane;
+            const int row0 = mb * BM + quarter * 32;
             const uint32_t taddr =
                 tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * BN + part * COLS);
 #pragma unroll 1
@@ -749,12 +811,15 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                     for (int j = 0; j < 32; ++j)
                         if (col0 + j < p.N) v[j] += __ldg(p.bias + col0 + j);
                 }
-                store_row32<OUT_BF16>(p, row, col0, v);
+#pragma unroll
+                for (int h = 0; h < 32 / SC; ++h)
+                    stage_store<OUT_BF16>(stg, &tmD, v + h * SC, col0 + h * SC, row0, p.M, p.N, lane);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&aempty[b]);
         }
+        stage_store_drain(lane);
     }
     __syncthreads();
     if (warp == 1) {
@@ -837,6 +902,22 @@ static uint32_t make_idesc_mx(int a_fmt, int b_fmt, int n)
     return d;
 }
 
+// 2-D tensor map of the output D [M][N] for the staged epilogue stores: box
+// 32 rows x 32 bytes, no swizzle (stores clip at the matrix edge)
+static bool make_tmap_out(CUtensorMap* m, void* D, int64_t M, int64_t N, bool bf16)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const uint64_t esz = bf16 ? 2 : 4;
+    cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)(N * esz)};
+    cuuint32_t box[2] = {(cuuint32_t)(32 / esz), 32u};
+    cuuint32_t estr[2] = {1u, 1u};
+    return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, D, dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename KernelT>
 static cudaError_t launch_persistent(KernelT kernel, int threads, int smem_bytes, int num_tiles, int sms,
                                      cudaStream_t st, const CUtensorMap& ta, const CUtensorMap& tb,
@@ -877,13 +958,21 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
             *why = "cuTensorMapEncodeTiled failed";
             return cudaErrorInvalidValue;
         }
+        CUtensorMap td;
+        if (!make_tmap_out(&td, g.D, g.M, g.N, bf16)) {
+            *why = "cuTensorMapEncodeTiled failed (output)";
+            return cudaErrorInvalidValue;
+        }
         TileSched sched{(int)((g.M + BM - 1) / BM), (int)((g.N + BN - 1) / BN), 16};
         const int tiles = sched.num_m * sched.num_n;
         const uint32_t idesc = make_idesc(g.a_format, g.b_format, BN);
-        const int smem = Smem<BN, ST, 2>::BYTES;
-        if (bf16)
-            return launch_persistent(k_gemm_tensor<BN, ST, true>, 192, smem, tiles, sms, st, ta, tb, p, idesc, sched);
-        return launch_persistent(k_gemm_tensor<BN, ST, false>, 192, smem, tiles, sms, st, ta, tb, p, idesc, sched);
+        const int smem = Smem<BN, ST, 2, 4>::BYTES;
+        auto kern = bf16 ? k_gemm_tensor<BN, ST, true> : k_gemm_tensor<BN, ST, false>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        const int grid = tiles < sms ? tiles : sms;
+        kern<<<grid, 192, smem, st>>>(ta, tb, p, idesc, sched, td);
+        return cudaGetLastError();
     }
     if (g.mode == 1) return launch_promote<8, 1>(g, p, st, sms, why);
     if (g.mode == 3) return launch_promote<8, 1, 3>(g, p, st, sms, why);
@@ -905,8 +994,13 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
         auto kern = bf16 ? k_gemm_mx<BN, ST, NACC, true, EPI> : k_gemm_mx<BN, ST, NACC, false, EPI>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
         if (e != cudaSuccess) return e;
+        CUtensorMap td;
+        if (!make_tmap_out(&td, g.D, g.M, g.N, bf16)) {
+            *why = "cuTensorMapEncodeTiled failed (output)";
+            return cudaErrorInvalidValue;
+        }
         const int grid = tiles < sms ? tiles : sms;
-        kern<<<grid, 64 + 32 * EPI, L::BYTES, st>>>(ta, tb, p, idesc, sched, mx);
+        kern<<<grid, 64 + 32 * EPI, L::BYTES, st>>>(ta, tb, p, idesc, sched, mx, td);
         return cudaGetLastError();
     }
     *why = "GEMM mode not built";
