@@ -329,11 +329,18 @@ FP8SQ_API int fp8_linear_fwd_noalloc(const void* x, const void* w, int64_t M, in
  *   since the last clear (the kernel that hit it wrote nothing further and
  *   returned), FP8SQ_OK otherwise.  clear != 0 resets the word.  While the
  *   word is set, GEMM kernels return early without computing.
+ * fp8_selftest_wait_timeout: exercises that failure path on purpose, with
+ *   no fault and no hang: one thread waits, through the library's bounded
+ *   wait, on an mbarrier phase nothing completes, gives up after limit_us
+ *   (1 .. 1e6), sets the device error word and returns; *waited_out (device
+ *   int) receives 1.  fp8_device_status then reports FP8SQ_ERR_TIMEOUT until
+ *   cleared.
  * fp8_last_error: message for the calling thread's last non-zero status
  *   (static thread-local storage; never NULL).
  * fp8_abi_version: 2.
  */
 FP8SQ_API int fp8_device_status(int clear);
+FP8SQ_API int fp8_selftest_wait_timeout(int limit_us, int* waited_out, void* stream);
 FP8SQ_API const char* fp8_last_error(void);
 FP8SQ_API int fp8_abi_version(void);
 

@@ -53,6 +53,7 @@ def lib() -> ctypes.CDLL:
                 "fp8_abi_version": (I, []),
                 "fp8_last_error": (c.c_char_p, []),
                 "fp8_device_status": (I, [I]),
+                "fp8_selftest_wait_timeout": (I, [I, P, P]),
                 "fp8_amax": (I, [P, I, I64, I64, I, P, P]),
                 "fp8_scale_init": (I, [P, I, I, P]),
                 "fp8_update_scale": (I, [P, I, I, P, I, P]),
@@ -183,6 +184,10 @@ def fp8_linear_fwd_noalloc(x, w, y, bias=None, stream=None) -> None:
     N = w.shape[0]
     _check(lib().fp8_linear_fwd_noalloc(_ptr(x), _ptr(w), M, N, K, _ptr(bias), _ptr(y), _dtype_code(y),
                                         _stream(stream)))
+
+
+def fp8_selftest_wait_timeout(limit_us: int, waited_out, stream=None) -> None:
+    _check(lib().fp8_selftest_wait_timeout(limit_us, _ptr(waited_out), _stream(stream)))
 
 
 def fp8_device_status(clear: bool = True) -> int:

@@ -163,6 +163,18 @@ FP8SQ_API int fp8_device_status(int clear)
     return FP8SQ_OK;
 }
 
+FP8SQ_API int fp8_selftest_wait_timeout(int limit_us, int* waited_out, void* stream)
+{
+    if (!waited_out) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_selftest_wait_timeout: null waited_out");
+    if (limit_us < 1 || limit_us > 1000000) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_selftest_wait_timeout: limit 1 us .. 1 s");
+    if (!aligned4(waited_out)) return fail(FP8SQ_ERR_MISALIGNED, "fp8_selftest_wait_timeout: waited_out alignment");
+    int sms, r;
+    if ((r = check_device(&sms))) return r;
+    return cuda_status(fp8sq::launch_selftest_wait((uint64_t)limit_us * 1000ull, waited_out,
+                                                   static_cast<cudaStream_t>(stream)),
+                       "fp8_selftest_wait_timeout launch");
+}
+
 FP8SQ_API int fp8_amax(const void* x, int x_dtype, int64_t rows, int64_t cols, int gran, float* amax_out,
                        void* stream)
 {

@@ -828,6 +828,28 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
     }
 }
 
+// ================================================================== self-test
+// One thread waits, through the same bounded wait the GEMM kernels use, on
+// an mbarrier phase that nothing completes; the wait gives up after
+// limit_ns, sets the device error word and the kernel returns.  Lets the
+// failure path be exercised without faulting or hanging the GPU.
+__global__ void k_selftest_wait(uint64_t limit_ns, int* waited_out)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        const bool ok = wait_bounded_err(&bar, 0, &g_dev_error, limit_ns);
+        *waited_out = ok ? 0 : 1;
+    }
+}
+
+cudaError_t launch_selftest_wait(uint64_t limit_ns, int* waited_out, cudaStream_t st)
+{
+    k_selftest_wait<<<1, 32, 0, st>>>(limit_ns, waited_out);
+    return cudaGetLastError();
+}
+
 // ================================================================== K == 0
 template <bool OUT_BF16>
 __global__ void k_fill_bias(void* D, int64_t M, int64_t N, const float* bias)

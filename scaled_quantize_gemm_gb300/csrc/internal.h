@@ -56,6 +56,8 @@ struct GemmArgs {
 // gemm.cu
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char** why);
 int read_device_error(int clear);   // 0 or the GEMM kernels' device error word
+// launches a kernel whose bounded wait is made to run out (failure-path test)
+cudaError_t launch_selftest_wait(uint64_t limit_ns, int* waited_out, cudaStream_t st);
 // 2-D tiled TMA map, 128-byte swizzle, zero fill out of bounds; u16 selects
 // 2-byte elements (else 1-byte)
 bool encode_tmap_2d(CUtensorMap* m, int u16, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_inner,

@@ -78,7 +78,8 @@ __device__ __forceinline__ uint64_t global_timer_ns()
 // Wait for phase `parity` of `bar` for at most ~1 s.  `err` is a device
 // error word: false is returned (and *err set) when the wait runs out, and
 // also as soon as some other wait has set *err.
-__device__ __forceinline__ bool wait_bounded_err(uint64_t* bar, uint32_t parity, int* err)
+__device__ __forceinline__ bool wait_bounded_err(uint64_t* bar, uint32_t parity, int* err,
+                                                 uint64_t limit_ns = 1000000000ull)
 {
     const uint32_t a = smem_addr(bar);
     if (mbar_try_wait(a, parity)) return true;
@@ -87,7 +88,7 @@ __device__ __forceinline__ bool wait_bounded_err(uint64_t* bar, uint32_t parity,
         if (mbar_try_wait(a, parity)) return true;
         if ((it & 255u) == 0u) {
             if (*reinterpret_cast<volatile int*>(err)) return false;
-            if (global_timer_ns() - t0 > 1000000000ull) {
+            if (global_timer_ns() - t0 > limit_ns) {
                 atomicExch(err, 1);
                 return false;
             }
