@@ -363,27 +363,45 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 // ================================================================== mode 1
-// 1x128 x 128x128 scales with per-K-block promotion; BN = 128, four TMEM
-// partial buffers.  EPI epilogue warps (warps 2..EPI+1): warp w reads lane
-// quarter w % 4 and the (w - 2) / 4-th slice of 128 / (EPI / 4) columns.
-// PF is how many K blocks ahead each thread reads its combined scale
-// sA[row][kb] * sB[nb][kb] (1: the next one; 16: a register window of 16).
-constexpr int kPromoBuffers = 4;
+// Fine-grained scales with per-K-block promotion.  Tile 128 x BN, 512 / BN
+// TMEM partial buffers of BN columns.  Eight epilogue warps (2..9): warp w
+// reads TMEM lane quarter w % 4 and owns column half (w - 2) / 4 of the tile
+// (COLS = BN / 2 columns).  For every K block it copies its 32 x COLS fp32
+// partial out of tensor memory, frees the buffer after the last copy, and
+// adds partial x scale into its register accumulators, while the MMAs of the
+// next K blocks run into the other buffers.
+// SM selects the scale layouts:
+//   1: A in 1x128 tiles sA[M][K/128], B in 128x128 blocks sB[ceil(N/128)][K/128]
+//      (BN = 256): a warp's 128 columns are one weight block, so its scale
+//      is one number per K block, sA[row][kb] * sB[block][kb];
+//   3: both operands in tiles along K with K-block-major scales sA[K/128][M],
+//      sB[K/128][N] (the transposed codes of column-tile quantisation), BN = 128:
+//      per element sA[kb][row] * sB[kb][col]; the warp's column scales reach
+//      its lanes through a double-buffered shared-memory slot.
+// Measured at 16384 x 14336 x 4096 (bf16 out): per-row scales 1999 TFLOP/s
+// at BN 256 against 1457 at BN 128 (a 256-wide tile halves the A-operand
+// shared-memory reads per FLOP; the tensor-memory drain per FLOP is the same
+// for any width).  Per-column scales stay at BN 128: at 256 their 128
+// accumulators, the partial chunk and the scale operands exceed the 168
+// registers a thread has with ten warps, and the spills cost more than the
+// wider tile gains.  Outputs are written with direct 16-byte stores: staging
+// them through shared memory for bulk tensor stores serialises each warp's
+// stores behind the previous store's read and, with the MMAs at most two
+// K blocks ahead, stalls the tensor pipe (1371 against 1999 TFLOP/s).
+constexpr int kPromoStages(int bn) { return bn == 256 ? 4 : 6; }
 
-// SM selects the scale layouts: 1 = A in 1x128 tiles sA[M][K/128] and B in
-// 128x128 blocks sB[N/128][K/128]; 3 = both operands in tiles along K with
-// K-block-major scales sA[K/128][M], sB[K/128][N] (the transposed codes of
-// column-tile quantisation), whose per-column scales reach each warp through
-// a double-buffered shared-memory slot.
-template <int STAGES, bool OUT_BF16, int EPI, int PF, int SM = 1>
-__global__ void __launch_bounds__(64 + 32 * EPI, 1)
+template <int BN, int STAGES, bool OUT_BF16, int SM>
+__global__ void __launch_bounds__(320, 1)
     k_gemm_promote(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    EpiParams p, uint32_t idesc, TileSched sched)
 {
-    constexpr int BN = 128;
-    constexpr int NB = kPromoBuffers;
-    constexpr int COLS = BN * 4 / EPI;       // columns per epilogue warp
+    constexpr int NB = 512 / BN;             // partial buffers
+    constexpr int EPI = 8;
+    constexpr int COLS = BN / 2;             // columns per epilogue warp
     constexpr int NLD = COLS / 32;           // 32-column TMEM loads per K block
+    constexpr int CPL = COLS / 32;           // column scales per lane (SM 3)
+    static_assert(BN == 128 || BN == 256, "tile width");
+    static_assert(SM == 1 ? BN == 256 : BN == 128, "scale layout and tile width go together");
     using L = Smem<BN, STAGES, NB>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -392,7 +410,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
     uint64_t* afull = empty + STAGES;
     uint64_t* aempty = afull + NB;
     uint64_t* drain = aempty + NB;
-    constexpr uint32_t TMEM_COLS = NB * BN;
+    constexpr uint32_t TMEM_COLS = 512;
 
     uint32_t tmem_base;
     if (!gemm_setup<STAGES, NB, EPI>(smem, L::BAR_OFF, TMEM_COLS, &tmA, &tmB, tmem_base)) return;
@@ -436,37 +454,59 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                 wait_drain(drain, 0);
             }
         }
-    } else if (SM == 3) {
-        static_assert(PF == 1 && COLS == 64, "column-scale promotion uses 8 warps, next-block prefetch");
-        __shared__ float colbuf[EPI][2][COLS];
+    } else {
         const int quarter = warp & 3;
-        const int part = (warp - 2) >> 2;
+        const int part = (warp - 2) >> 2;           // column half of the tile
         const int ew = warp - 2;
+        const int ksb = p.K / BK;                   // scale blocks along K
+        const int nblk = (p.N + 127) / 128;         // weight blocks along N
+        __shared__ __align__(16) float colbuf[SM == 3 ? EPI : 1][2][SM == 3 ? COLS : 4];
         int it = 0;
         bool ok_all = true;
         for (int t = blockIdx.x; t < num_tiles && ok_all; t += gridDim.x) {
             int mb, nb;
             sched.coords(t, mb, nb);
             const int row = mb * BM + quarter * 32 + lane;
-            const int rowc = row < p.M ? row : p.M - 1;
+            const int rowc = row < p.M ? row : p.M - 1;   // clamp for the scale reads
             const int col0 = nb * BN + part * COLS;
-            int cl = col0 + 2 * lane;                       // this lane's two column scales
-            cl = cl < p.N - 1 ? cl : p.N - 2;
             float acc[COLS];
 #pragma unroll
             for (int j = 0; j < COLS; ++j) acc[j] = 0.0f;
-            float ra = __ldg(p.sA + rowc);
-            float2 cb = *reinterpret_cast<const float2*>(p.sB + cl);
+            // SM 1: sc = the K block's combined scale (one weight block per warp).
+            // SM 3: ra = the row's scale, cb = this lane's CPL column scales.
+            const float* sa_row = p.sA + (int64_t)rowc * ksb;
+            int wblk = nb * (BN / 128) + part * (COLS / 128);
+            wblk = wblk < nblk ? wblk : nblk - 1;
+            const float* sb_row = p.sB + (int64_t)wblk * ksb;
+            int cl = col0 + CPL * lane;
+            cl = cl < p.N - CPL ? cl : p.N - CPL;
+            float sc = 0.0f, ra = 0.0f;
+            float cb[CPL];
+            if constexpr (SM == 1) {
+                sc = __ldg(sa_row) * __ldg(sb_row);
+            } else {
+                ra = __ldg(p.sA + rowc);
+#pragma unroll
+                for (int j = 0; j < CPL; ++j) cb[j] = __ldg(p.sB + cl + j);
+            }
             for (int kb = 0; kb < nkb; ++kb) {
-                const float ra_cur = ra;
-                const float2 cb_cur = cb;
-                if (kb + 1 < nkb) {
-                    ra = __ldg(p.sA + (int64_t)(kb + 1) * p.M + rowc);
-                    cb = *reinterpret_cast<const float2*>(p.sB + (int64_t)(kb + 1) * p.N + cl);
+                const int kn = kb + 1 < nkb ? kb + 1 : kb;
+                float na = 0.0f, nbv = 0.0f;
+                float ncb[CPL];
+                [[maybe_unused]] const float* cbuf = nullptr;
+                if constexpr (SM == 1) {
+                    na = __ldg(sa_row + kn);
+                    nbv = __ldg(sb_row + kn);
+                } else {
+                    na = __ldg(p.sA + (int64_t)kn * p.M + rowc);
+#pragma unroll
+                    for (int j = 0; j < CPL; ++j) ncb[j] = __ldg(p.sB + (int64_t)kn * p.N + cl + j);
+                    float* w = colbuf[ew][kb & 1];
+#pragma unroll
+                    for (int j = 0; j < CPL; ++j) w[CPL * lane + j] = cb[j];
+                    __syncwarp();
+                    cbuf = w;
                 }
-                float* buf = colbuf[ew][kb & 1];
-                *reinterpret_cast<float2*>(buf + 2 * lane) = cb_cur;
-                __syncwarp();
                 const int b = it % NB;
                 const uint32_t u = (uint32_t)(it / NB);
                 ++it;
@@ -478,80 +518,23 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                 tc_fence_after();
                 const uint32_t taddr =
                     tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * BN + part * COLS);
-                uint32_t r[NLD][32];
+                if constexpr (SM == 1) {
+                    // 128 columns: one 32-column chunk in flight at a time (registers)
 #pragma unroll
-                for (int l = 0; l < NLD; ++l) tmem_ld_32x32b_x32(taddr + 32 * l, r[l]);
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&aempty[b]);
+                    for (int l = 0; l < NLD; ++l) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(taddr + 32 * l, r);
+                        tmem_ld_wait();
+                        if (l == NLD - 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&aempty[b]);
+                        }
 #pragma unroll
-                for (int c4 = 0; c4 < COLS / 4; ++c4) {
-                    const float4 s4 = *reinterpret_cast<const float4*>(buf + 4 * c4);
-                    const float sc[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c = 4 * c4 + e;
-                        acc[c] = fmaf(__uint_as_float(r[c / 32][c % 32]), ra_cur * sc[e], acc[c]);
+                        for (int i = 0; i < 32; ++i) acc[32 * l + i] = fmaf(__uint_as_float(r[i]), sc, acc[32 * l + i]);
                     }
-                }
-            }
-            if (!ok_all) break;
-#pragma unroll
-            for (int h = 0; h < NLD; ++h) {
-                float v[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    v[j] = acc[32 * h + j];
-                    if (p.bias && col0 + 32 * h + j < p.N) v[j] += __ldg(p.bias + col0 + 32 * h + j);
-                }
-                store_row32<OUT_BF16>(p, row, col0 + 32 * h, v);
-            }
-        }
-    } else {
-        // SM == 1
-        const int quarter = warp & 3;
-        const int part = (warp - 2) >> 2;
-        const int ksb = p.K / BK;            // scale blocks along K
-        int it = 0;
-        bool ok_all = true;
-        for (int t = blockIdx.x; t < num_tiles && ok_all; t += gridDim.x) {
-            int mb, nb;
-            sched.coords(t, mb, nb);
-            const int row = mb * BM + quarter * 32 + lane;
-            const int rowc = row < p.M ? row : p.M - 1;   // clamp for the scale read
-            const float* sa_row = p.sA + (int64_t)rowc * ksb;
-            const float* sb_row = p.sB + (int64_t)nb * ksb;   // BN = 128: one weight block row
-            float acc[COLS];
-#pragma unroll
-            for (int j = 0; j < COLS; ++j) acc[j] = 0.0f;
-            float sc[PF], na[PF], nbv[PF];
-#pragma unroll
-            for (int j = 0; j < PF; ++j) {
-                const int kb = j < nkb ? j : nkb - 1;
-                sc[j] = __ldg(sa_row + kb) * __ldg(sb_row + kb);
-            }
-            for (int kw = 0; kw < nkb && ok_all; kw += PF) {
-#pragma unroll
-                for (int j = 0; j < PF; ++j) {
-                    const int kb = (kw + PF + j) < nkb ? kw + PF + j : nkb - 1;
-                    na[j] = __ldg(sa_row + kb);
-                    nbv[j] = __ldg(sb_row + kb);
-                }
-#pragma unroll
-                for (int j = 0; j < PF; ++j) {
-                    if (kw + j >= nkb) break;
-                    const int b = it % NB;
-                    const uint32_t u = (uint32_t)(it / NB);
-                    ++it;
-                    const bool ok = wait_bounded(&afull[b], u & 1u);
-                    if (!__all_sync(0xFFFFFFFFu, ok)) {
-                        ok_all = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t taddr =
-                        tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * BN + part * COLS);
+                } else {
+                    // 64 columns: both chunks loaded, one wait, buffer freed before the FMAs
                     uint32_t r[NLD][32];
 #pragma unroll
                     for (int l = 0; l < NLD; ++l) tmem_ld_32x32b_x32(taddr + 32 * l, r[l]);
@@ -560,15 +543,25 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&aempty[b]);
 #pragma unroll
-                    for (int l = 0; l < NLD; ++l)
+                    for (int c4 = 0; c4 < COLS / 4; ++c4) {
+                        const float4 s4 = *reinterpret_cast<const float4*>(cbuf + 4 * c4);
+                        const float s[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) acc[32 * l + i] = fmaf(__uint_as_float(r[l][i]), sc[j], acc[32 * l + i]);
+                        for (int e = 0; e < 4; ++e) {
+                            const int c = 4 * c4 + e;
+                            acc[c] = fmaf(__uint_as_float(r[c / 32][c % 32]), ra * s[e], acc[c]);
+                        }
+                    }
                 }
+                if constexpr (SM == 1) {
+                    sc = na * nbv;
+                } else {
+                    ra = na;
 #pragma unroll
-                for (int j = 0; j < PF; ++j) sc[j] = na[j] * nbv[j];
+                    for (int j = 0; j < CPL; ++j) cb[j] = ncb[j];
+                }
             }
             if (!ok_all) break;
-            const int col0 = nb * BN + part * COLS;
 #pragma unroll
             for (int h = 0; h < NLD; ++h) {
                 float v[32];
@@ -588,12 +581,11 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
     }
 }
 
-// launches one promotion-kernel variant (EPI epilogue warps, PF scale window,
-// SM scale layouts)
-template <int EPI, int PF, int SM = 1>
+// launches the promotion kernel for scale layout SM (1: BN 256, 3: BN 128)
+template <int SM>
 static cudaError_t launch_promote(const GemmArgs& g, const EpiParams& p, cudaStream_t st, int sms, const char** why)
 {
-    constexpr int BN = 128, ST = 6;
+    constexpr int BN = SM == 1 ? 256 : 128, ST = kPromoStages(BN);
     CUtensorMap ta, tb;
     if (!encode_tmap_2d(&ta, 0, g.A, g.K, g.M, 128u, BM) || !encode_tmap_2d(&tb, 0, g.B, g.K, g.N, 128u, BN)) {
         *why = "cuTensorMapEncodeTiled failed";
@@ -607,12 +599,12 @@ static cudaError_t launch_promote(const GemmArgs& g, const EpiParams& p, cudaStr
     idesc |= (uint32_t)g.b_format << 10;
     idesc |= (uint32_t)(BN >> 3) << 17;
     idesc |= (uint32_t)(BM >> 4) << 24;
-    const int smem = Smem<BN, ST, kPromoBuffers>::BYTES;
-    auto kern = g.d_dtype == kBF16 ? k_gemm_promote<ST, true, EPI, PF, SM> : k_gemm_promote<ST, false, EPI, PF, SM>;
+    const int smem = Smem<BN, ST, 512 / BN>::BYTES;
+    auto kern = g.d_dtype == kBF16 ? k_gemm_promote<BN, ST, true, SM> : k_gemm_promote<BN, ST, false, SM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int grid = tiles < sms ? tiles : sms;
-    kern<<<grid, 64 + 32 * EPI, smem, st>>>(ta, tb, p, idesc, sched);
+    kern<<<grid, 320, smem, st>>>(ta, tb, p, idesc, sched);
     return cudaGetLastError();
 }
 
@@ -996,8 +988,8 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
         kern<<<grid, 192, smem, st>>>(ta, tb, p, idesc, sched, td);
         return cudaGetLastError();
     }
-    if (g.mode == 1) return launch_promote<8, 1>(g, p, st, sms, why);
-    if (g.mode == 3) return launch_promote<8, 1, 3>(g, p, st, sms, why);
+    if (g.mode == 1) return launch_promote<1>(g, p, st, sms, why);
+    if (g.mode == 3) return launch_promote<3>(g, p, st, sms, why);
     if (g.mode == 2) {
         constexpr int BN = 256, ST = 4, NACC = 1;
         using L = MxLayout<BN, ST, NACC>;

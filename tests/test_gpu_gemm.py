@@ -154,6 +154,24 @@ def test_tile_block_promotion_vs_oracle(M, N, K, out):
     assert_gemm_close(D, R)
 
 
+@pytest.mark.parametrize("M,N,K", [(328, 640, 512), (128, 1152, 384)])
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+def test_tile_block_promotion_bias_ragged_tiles(M, N, K, out):
+    """Promotion with bias, N % 256 == 128 (the last 256-wide tile holds one
+    weight block and columns past N) and a ragged M."""
+    x = wl.student_t3((M, K), 31 + M)
+    w = wl.normal((N, K), 0.02, 32 + N)
+    bias = wl.normal((N,), 0.5, 33 + N, dtype=torch.float32).to(DEV)
+    qx, sx, qw, sw = _quant_tile_block(x, w)
+    D = torch.empty((M, N), dtype=out, device=DEV)
+    sq.fp8_gemm(qx, sq.E4M3, sx, sq.TILE_1x128, qw, sq.E4M3, sw, sq.BLOCK_128x128, D, bias=bias)
+    torch.cuda.synchronize()
+    R = o.gemm_ref(o.dequantize(codes(qx), 0, o.GRAN_TILE_1x128, sx.cpu().numpy().reshape(M, K // 128)),
+                   o.dequantize(codes(qw), 0, o.GRAN_BLOCK_128x128, sw.cpu().numpy().reshape(N // 128, K // 128)),
+                   bias=bias.cpu().numpy())
+    assert_gemm_close(D, R)
+
+
 def _sample_rows(M, n, seed):
     return np.sort(np.random.default_rng(seed).choice(M, size=n, replace=False))
 
@@ -203,6 +221,23 @@ def _mx_gemm(qa, ea, qb, eb, out):
     sq.fp8_gemm(qa, sq.E4M3, ea, sq.MX32_TILED, qb, sq.E4M3, eb, sq.MX32_TILED, D)
     torch.cuda.synchronize()
     return D
+
+
+def test_mx_gemm_bias_vs_oracle():
+    """MX-32 GEMM with bias (fp32 out), N % 256 == 128."""
+    from _helpers import mx_untile
+    M, N, K = 256, 640, 512
+    a = wl.normal((M, K), 1.0, 41)
+    b = wl.normal((N, K), 1.0, 42)
+    bias = wl.normal((N,), 2.0, 43, dtype=torch.float32).to(DEV)
+    qa, ea = _quant_mx(a)
+    qb, eb = _quant_mx(b)
+    D = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    sq.fp8_gemm(qa, sq.E4M3, ea, sq.MX32_TILED, qb, sq.E4M3, eb, sq.MX32_TILED, D, bias=bias)
+    torch.cuda.synchronize()
+    ah = o.dequantize(codes(qa), 0, o.GRAN_MX32, mx_untile(ea.cpu().numpy(), M, K))
+    bh = o.dequantize(codes(qb), 0, o.GRAN_MX32, mx_untile(eb.cpu().numpy(), N, K))
+    assert_gemm_close(D, o.gemm_ref(ah, bh, bias=bias.cpu().numpy()))
 
 
 def test_mx_unit_scales_integer_exact():
@@ -283,13 +318,17 @@ def test_w4_mx_full_size_sampled_rows():
     assert_gemm_close(D[rows], o.gemm_ref(ah, bh))
 
 
-@pytest.mark.parametrize("Mt,N,K", [(256, 384, 256), (384, 256, 512)])
+@pytest.mark.parametrize("Mt,N,K,with_bias", [(256, 384, 256, False), (384, 256, 512, False),
+                                              (512, 208, 640, True), (128, 144, 1152, True)])
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
-def test_column_tile_gemm_vs_oracle(Mt, N, K, out):
+def test_column_tile_gemm_vs_oracle(Mt, N, K, with_bias, out):
     """Mode for wgrad: both operands are the transposed codes of 128x1
-    column-tile quantisations (contraction over the original rows Mt)."""
+    column-tile quantisations (contraction over the original rows Mt); the
+    GEMM's N (here K) ragged at the 256-wide tile, GEMM M (here N) ragged at
+    128, with and without bias."""
     dy = wl.normal((Mt, N), 1e-3, 91 + Mt)
     x = wl.student_t3((Mt, K), 92 + K)
+    bias = wl.normal((K,), 1e-3, 93 + K, dtype=torch.float32).to(DEV) if with_bias else None
     qdT = torch.empty((N, Mt), dtype=torch.uint8, device=DEV)
     qxT = torch.empty((K, Mt), dtype=torch.uint8, device=DEV)
     sd = torch.empty((Mt // 128) * N, dtype=torch.float32, device=DEV)
@@ -297,12 +336,13 @@ def test_column_tile_gemm_vs_oracle(Mt, N, K, out):
     sq.fp8_quantize(dy.to(DEV), sq.E5M2, sq.TILE_128x1, None, qT=qdT, scales_out=sd)
     sq.fp8_quantize(x.to(DEV), sq.E4M3, sq.TILE_128x1, None, qT=qxT, scales_out=sx)
     D = torch.empty((N, K), dtype=out, device=DEV)
-    sq.fp8_gemm(qdT, sq.E5M2, sd, sq.TILE_128x1, qxT, sq.E4M3, sx, sq.TILE_128x1, D)
+    sq.fp8_gemm(qdT, sq.E5M2, sd, sq.TILE_128x1, qxT, sq.E4M3, sx, sq.TILE_128x1, D, bias=bias)
     torch.cuda.synchronize()
     rqd, rsd, _, _ = o.quantize_tile128x1(np32(dy), o.E5M2)
     rqx, rsx, _, _ = o.quantize_tile128x1(np32(x), o.E4M3)
     R = o.gemm_ref(o.dequantize(rqd, o.E5M2, o.GRAN_TILE_128x1, rsd).T,
-                   o.dequantize(rqx, o.E4M3, o.GRAN_TILE_128x1, rsx).T)
+                   o.dequantize(rqx, o.E4M3, o.GRAN_TILE_128x1, rsx).T,
+                   bias=None if bias is None else bias.cpu().numpy())
     assert_gemm_close(D, R)
 
 
