@@ -50,20 +50,20 @@ SAMPLE_TOKENS = 128      # CPU oracle sample: the same step at 128 tokens
 # one ncu capture of each reported kernel, valid only while the kernel's own
 # source text (and the PTX wrappers) still hash to the recorded digest; a
 # changed kernel reports null until it is captured again.  Captured shapes:
-# k_gemm_tensor on the 16384 x 14336 x 4096 forward GEMM, k_cast_T_tma on the
+# k_gemm_tensor_pair on the 16384 x 14336 x 4096 forward GEMM, k_cast_T_tma on the
 # 16384 x 14336 cast (the captures are summarised under profiles/).
 CSRC = os.path.join(ROOT, "scaled_quantize_gemm_gb300", "csrc")
 KERNEL_SOURCES = {   # file, [(start marker or None = file start, end marker)]: helpers + kernel + launch config
-    "k_gemm_tensor": ("gemm.cu", [(None, "// ================================================================== mode 1"),
-                                  ("    if (g.mode == 0) {", "    if (g.mode == 1)")]),
+    "k_gemm_tensor_pair": ("gemm.cu", [(None, "// ================================================================== mode 1"),
+                                       ("    if (g.mode == 0) {", "    if (g.mode == 1)")]),
     "k_cast_T_tma": ("quantize.cu", [(None, "// ================================================================== per-tensor\n"),
                                      ("// ================================================================== per-tensor, TMA-fed",
                                       "// AND of `v` over the 256 consumer threads"),
                                      ("        if (a.qT && DT == kBF16 && n > 0) {", "        if (a.qT) {")]),
 }
 TRAFFIC = {
-    "k_gemm_tensor": {"sha": "bfa1f28c6d4ac95f", "bytes": 964290048},
-    "k_cast_T_tma": {"sha": "430ea2c18259f07e", "bytes": 893286144},
+    "k_gemm_tensor_pair": {"sha": "ff4d0e083e856221", "bytes": 973734144},
+    "k_cast_T_tma": {"sha": "947ebc665f936dba", "bytes": 893327616},
 }
 
 
@@ -248,7 +248,7 @@ class FFNStep:
 
     KERNELS_PER_STEP = 13   # 6 casts + 6 GEMMs + 1 scale update
 
-    def e2e_run(self, host_sets, steps: int, states_host):
+    def e2e_run(self, host_sets, steps: int, states_host, copy_ev=None):
         """`steps` steps through the linear-layer API with host buffers: each
         step's x and dy come from pinned host memory, the step's scale state
         goes back to the host.  The copies of step s+1 run on one copy stream
@@ -271,9 +271,14 @@ class FFNStep:
             hs = host_sets[s % len(host_sets)]
             copy.wait_stream(main) if s < 2 else copy.wait_event(free[buf])
             with torch.cuda.stream(copy):
+                if copy_ev is not None:
+                    copy_ev.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+                    copy_ev[-1][0].record()
                 for li, (xh, dyh) in enumerate(hs):
                     dev_in[buf][li][0].copy_(xh, non_blocking=True)
                     dev_in[buf][li][1].copy_(dyh, non_blocking=True)
+                if copy_ev is not None:
+                    copy_ev[-1][1].record()
             ready[buf].record(copy)
 
         issue_copy(0)
@@ -384,17 +389,31 @@ def run_ours(args, ws, rank, local):
         torch.cuda.synchronize()
         if ws > 1:
             torch.distributed.barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        b.e2e_run(host_sets, args.steps, states_host)
-        e1.record()
-        torch.cuda.synchronize()
-        e2e_ms = _barrier_max(e0.elapsed_time(e1), ws, device) / args.steps
+        # three timed windows of K steps each; the median window is reported
+        # (a single host-side copy stall on the shared host, seen as one copy
+        # of ~60 ms among 5.7 ms ones, would otherwise decide the number)
+        rep_ms, copy_ms = [], []
+        for _ in range(3):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            cev = []
+            if ws > 1:
+                torch.distributed.barrier()
+            torch.cuda.synchronize()
+            e0.record()
+            b.e2e_run(host_sets, args.steps, states_host, cev)
+            e1.record()
+            torch.cuda.synchronize()
+            copy_ms += [a.elapsed_time(z) for a, z in cev]
+            rep_ms.append(_barrier_max(e0.elapsed_time(e1), ws, device) / args.steps)
+        e2e_ms = statistics.median(rep_ms)
         e2e = {"value": round(_replica_throughput(flops, e2e_ms, ws), 2), "unit": UNIT,
                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "h2d_link_gbs": round(link_gbs, 1),
                "h2d_bound_ms": round(h2d / (link_gbs * 1e9) * 1e3, 4),
+               "h2d_copy_ms": {"median": round(statistics.median(copy_ms), 4), "max": round(max(copy_ms), 4)},
+               "windows_ms_per_step": [round(v, 4) for v in rep_ms],
+               "window_rule": "median of 3 timed windows of K steps",
                "api": "fp8_linear_fwd / fp8_linear_bwd / fp8_update_scale; each step's x and dy copied "
                       "from pinned host memory (next step's copies overlap this step's compute), scale states "
                       "read back every step"}
@@ -420,9 +439,9 @@ def run_ours(args, ws, rank, local):
             "clocks": clk,
             "e2e": e2e,
             "gpu_launches": b.KERNELS_PER_STEP * args.steps,
-            "roofline": {"bound": "tensor", "kernel": "k_gemm_tensor (tcgen05 kind::f8f6f4, 128x224 tile, 5 stages)",
+            "roofline": {"bound": "tensor", "kernel": "k_gemm_tensor_pair (tcgen05 .cta_group::2 kind::f8f6f4, 256x256 tile on a CTA pair, 6 stages)",
                          "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
-                         "frac": round(achieved / fp8_peak, 4), "traffic": kernel_traffic("k_gemm_tensor"),
+                         "frac": round(achieved / fp8_peak, 4), "traffic": kernel_traffic("k_gemm_tensor_pair"),
                          "traffic_shape": "16384 x 14336 x 4096 forward GEMM (one ncu capture)",
                          "peak_source": f"2 x bf16_tflops {peak_src} (dense FP8 = 2 x dense BF16)",
                          "flops_per_launch": gemm_flops_launch, "launch_ms": round(gemm_ms, 4)},
@@ -530,7 +549,7 @@ def run_reference(args, ws, rank, local):
 def kernel_case(case: str, launches: int):
     """A handful of launches of one kernel at the workload's size, for
     profiling a single launch: 'gemm' = the 16384 x 14336 x 4096 forward GEMM
-    (k_gemm_tensor), 'cast' = the 16384 x 14336 E5M2 cast with its transposed
+    (k_gemm_tensor_pair), 'cast' = the 16384 x 14336 E5M2 cast with its transposed
     copy (k_cast_T_tma), 'promote' = the 4096^3 1x128 x 128x128 GEMM
     (k_gemm_promote), 'mx' = the 8192^3 MX-32 GEMM (k_gemm_mx)."""
     import scaled_quantize_gemm_gb300 as sq
@@ -585,11 +604,153 @@ def kernel_case(case: str, launches: int):
     print(f"kernel case {case}: {launches} launches ok")
 
 
+def modes_table(reps: int = 10):
+    """Times every GEMM mode, cast and linear-layer call of the five workloads
+    (and the promotion kernels at the FFN shapes) through the C ABI: median of
+    `reps` launches after 3 warm-ups, CUDA events on the launching stream.
+    One JSON line per row; not the benchmark line."""
+    import scaled_quantize_gemm_gb300 as sq
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    hbm_peak, bf16_peak, src = _peaks()
+    fp8_peak = 2.0 * bf16_peak
+    u8 = dict(dtype=torch.uint8, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+
+    def med(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        if sq.fp8_device_status(True) != 0:
+            raise RuntimeError("device status error")
+        return statistics.median(ts)
+
+    def row(call, shape, ms, flops=None, nbytes=None):
+        r = {"call": call, "shape": shape, "us": round(ms * 1e3, 1)}
+        if flops:
+            r["TFLOP/s"] = round(flops / (ms * 1e-3) / 1e12, 1)
+            r["of_fp8_peak"] = round(r["TFLOP/s"] / fp8_peak, 3)
+        if nbytes:
+            r["GB/s"] = round(nbytes / (ms * 1e-3) / 1e9, 1)
+            r["of_hbm_peak"] = round(r["GB/s"] / hbm_peak, 3)
+        r["peak_source"] = src
+        print(json.dumps(r), flush=True)
+
+    def quant_tile_block(M, N, K, xs, ws):
+        qx, qw = torch.empty((M, K), **u8), torch.empty((N, K), **u8)
+        sx, sw = torch.empty(M * (K // 128), **f32), torch.empty((N // 128) * (K // 128), **f32)
+        sq.fp8_quantize(xs, sq.E4M3, sq.TILE_1x128, qx, scales_out=sx)
+        sq.fp8_quantize(ws, sq.E4M3, sq.BLOCK_128x128, qw, scales_out=sw)
+        return qx, sx, qw, sw
+
+    # workload 1: per-tensor current scaling, 256^3, fp32 out
+    a, b = wl.w1_operands(dev)
+    qa, qb = torch.empty((256, 256), **u8), torch.empty((256, 256), **u8)
+    sa, sb, am = torch.empty(1, **f32), torch.empty(1, **f32), torch.empty(1, **f32)
+    sq.fp8_quantize(a, sq.E4M3, sq.TENSOR, qa, scales_out=sa, amax_out=am)
+    sq.fp8_quantize(b, sq.E4M3, sq.TENSOR, qb, scales_out=sb, amax_out=am)
+    y = torch.empty((256, 256), **f32)
+    row("fp8_quantize TENSOR E4M3 current (fp32 in)", "256x256",
+        med(lambda: sq.fp8_quantize(a, sq.E4M3, sq.TENSOR, qa, scales_out=sa, amax_out=am)), nbytes=256 * 256 * 5)
+    row("fp8_gemm TENSOR x TENSOR, fp32 out", "256^3",
+        med(lambda: sq.fp8_gemm(qa, sq.E4M3, sa, sq.TENSOR, qb, sq.E4M3, sb, sq.TENSOR, y)), flops=2 * 256 ** 3)
+
+    # workload 2: MiniGPT linears, delayed scaling
+    W2 = wl.WORKLOADS[2]
+    for li, lin in enumerate(W2.linears):
+        M, K, N = W2.tokens, lin.in_features, lin.out_features
+        x, w, dy = wl.linear_x(2, li, 0, M, K, dev), wl.linear_w(2, li, N, K, dev), wl.linear_dy(2, li, 0, M, N, dev)
+        st = [torch.empty(H + 2, **f32) for _ in range(3)]
+        for i, s_ in enumerate(st):
+            sq.fp8_scale_init(s_, 1 if i < 2 else 2, H)
+        ws = torch.empty(sq.fp8_linear_workspace_bytes(M, N, K), **u8)
+        yb = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+        dw = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+        row("fp8_linear_fwd TENSOR delayed", f"{M}x{K}->{N}",
+            med(lambda: sq.fp8_linear_fwd(x, w, yb, ws, x_state=st[0], w_state=st[1], history_len=H)),
+            flops=2 * M * N * K)
+        row("fp8_linear_bwd TENSOR delayed", f"{M}x{K}->{N}",
+            med(lambda: sq.fp8_linear_bwd(dy, dx, dw, ws, K, dy_state=st[2], history_len=H)), flops=4 * M * N * K)
+
+    # workload 3 and the promotion kernels at the FFN shapes
+    for (M, N, K) in [(4096, 4096, 4096), (16384, 14336, 4096), (8192, 8192, 8192)]:
+        if M == 4096:
+            xs, wsrc = wl.w3_operands(dev)
+        else:
+            xs, wsrc = wl.student_t3((M, K), 1, dev), wl.normal((N, K), 0.02, 2, dev)
+        qx, sx, qw, sw = quant_tile_block(M, N, K, xs, wsrc)
+        if M == 4096:
+            row("fp8_quantize TILE_1x128 E4M3", "4096x4096",
+                med(lambda: sq.fp8_quantize(xs, sq.E4M3, sq.TILE_1x128, qx, scales_out=sx)),
+                nbytes=M * K * 3 + M * K // 128 * 4)
+            row("fp8_quantize BLOCK_128x128 E4M3", "4096x4096",
+                med(lambda: sq.fp8_quantize(wsrc, sq.E4M3, sq.BLOCK_128x128, qw, scales_out=sw)),
+                nbytes=N * K * 3)
+        del xs, wsrc
+        yb = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        row("fp8_gemm TILE_1x128 x BLOCK_128x128 (k_gemm_promote, 128x256 tile)", f"{M}x{N}x{K}",
+            med(lambda: sq.fp8_gemm(qx, sq.E4M3, sx, sq.TILE_1x128, qw, sq.E4M3, sw, sq.BLOCK_128x128, yb)),
+            flops=2 * M * N * K)
+        del qx, qw, yb
+        Mt = M      # column tiles: the wgrad GEMM dW[N][K] over Mt rows
+        dy, xx = wl.normal((Mt, N), 1e-3, 3, dev), wl.student_t3((Mt, K), 4, dev)
+        qdT, qxT = torch.empty((N, Mt), **u8), torch.empty((K, Mt), **u8)
+        sd, sxx = torch.empty((Mt // 128) * N, **f32), torch.empty((Mt // 128) * K, **f32)
+        sq.fp8_quantize(dy, sq.E5M2, sq.TILE_128x1, None, qT=qdT, scales_out=sd)
+        sq.fp8_quantize(xx, sq.E4M3, sq.TILE_128x1, None, qT=qxT, scales_out=sxx)
+        del dy, xx
+        yb = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+        row("fp8_gemm TILE_128x1 x TILE_128x1 (k_gemm_promote, 128x128 tile)", f"{N}x{K}x{Mt}",
+            med(lambda: sq.fp8_gemm(qdT, sq.E5M2, sd, sq.TILE_128x1, qxT, sq.E4M3, sxx, sq.TILE_128x1, yb)),
+            flops=2 * N * K * Mt)
+        del qdT, qxT, yb
+        torch.cuda.empty_cache()
+    M = N = K = 4096
+    for gran, name in [(sq.TILE_1x128, "TILE_1x128 / BLOCK_128x128"), (sq.MX32, "MX32")]:
+        x, w = wl.student_t3((M, K), 1, dev), wl.normal((N, K), 0.02, 2, dev)
+        dy = wl.normal((M, N), 1e-3, 3, dev)
+        ws = torch.empty(sq.fp8_linear_workspace_bytes(M, N, K, gran), **u8)
+        yb = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        dx = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+        dw = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+        row(f"fp8_linear_fwd {name} current", "4096^3",
+            med(lambda: sq.fp8_linear_fwd(x, w, yb, ws, gran=gran)), flops=2 * M * N * K)
+        row(f"fp8_linear_bwd {name} current", "4096^3",
+            med(lambda: sq.fp8_linear_bwd(dy, dx, dw, ws, K, gran=gran)), flops=4 * M * N * K)
+
+    # workload 4: MX-32, and the per-tensor GEMM on the same operands
+    a, b = wl.w4_operands(dev)
+    qa, qb = torch.empty(a.shape, **u8), torch.empty(b.shape, **u8)
+    ea, eb = torch.empty(a.numel() // 32, **u8), torch.empty(b.numel() // 32, **u8)
+    row("fp8_quantize MX32_TILED E4M3", "8192x8192",
+        med(lambda: sq.fp8_quantize(a, sq.E4M3, sq.MX32_TILED, qa, scales_out=ea)), nbytes=8192 * 8192 * (3 + 1 / 32))
+    sq.fp8_quantize(b, sq.E4M3, sq.MX32_TILED, qb, scales_out=eb)
+    del a, b
+    yb = torch.empty((8192, 8192), dtype=torch.bfloat16, device=dev)
+    row("fp8_gemm MX32_TILED (k_gemm_mx)", "8192^3",
+        med(lambda: sq.fp8_gemm(qa, sq.E4M3, ea, sq.MX32_TILED, qb, sq.E4M3, eb, sq.MX32_TILED, yb)),
+        flops=2 * 8192 ** 3)
+    one = torch.ones(1, **f32)
+    row("fp8_gemm TENSOR x TENSOR (k_gemm_tensor_pair)", "8192^3",
+        med(lambda: sq.fp8_gemm(qa, sq.E4M3, one, sq.TENSOR, qb, sq.E4M3, one, sq.TENSOR, yb)), flops=2 * 8192 ** 3)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--kernel-case", choices=["gemm", "cast", "promote", "mx"], default=None,
                     help="run a few launches of one kernel (for profiling) and exit")
     ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--modes", action="store_true",
+                    help="time every GEMM mode, cast and linear call of the five workloads (one JSON line each) and exit")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
@@ -600,6 +761,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.modes:
+        modes_table()
+        return
     if args.kernel_case:
         kernel_case(args.kernel_case, args.launches)
         return

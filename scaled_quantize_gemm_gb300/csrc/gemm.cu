@@ -249,13 +249,48 @@ __device__ __forceinline__ void producer_loop(uint8_t* smem, uint64_t* full, uin
 }
 
 // ================================================================== mode 0
-// per-tensor scales; epilogue warps 2..5
-template <int BN, int STAGES, bool OUT_BF16>
-__global__ void __launch_bounds__(192, 1)
-    k_gemm_tensor(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  EpiParams p, uint32_t idesc, TileSched sched, const __grid_constant__ CUtensorMap tmD)
+// Per-tensor scales on CTA pairs (tcgen05 .cta_group::2).  A cluster of two
+// CTAs computes 256 x 256 output tiles: CTA r holds A rows [128 r, 128 r + 128)
+// and B rows [128 r, 128 r + 128) of the tile in its own shared memory; the
+// even CTA (the leader) issues the M = 256 MMAs, which read both CTAs' shared
+// memory and accumulate each CTA's 128 rows into that CTA's TMEM.  Each SM
+// thus loads half of the B tile it multiplies with, which halves the B reads
+// from shared memory per FLOP against one CTA per tile.
+//   warp 0 (both CTAs): TMA producer into a 6-stage ring (32 KB per stage);
+//     the loads of both CTAs complete on the leader's full barrier, for
+//     which the leader's producer alone declares the pair's bytes.
+//   warp 1: pair-wide TMEM allocation (512 columns: two 256-column
+//     accumulators); in the leader one thread issues the MMAs and commits,
+//     multicast to both CTAs, the ring's empty and the accumulators' full
+//     barriers.
+//   warps 2-5 (both CTAs): epilogue of the CTA's 128 rows, through 1 KB
+//     per-warp shared-memory buffers and bulk tensor stores; each warp
+//     releases an accumulator by arriving on the leader's barrier.
+// Every thread of both CTAs reaches both cluster barriers: the skip decision
+// taken from the error word is the leader's, read by the peer, and no role
+// leaves before the final one.  Before a CTA may leave, its producer waits
+// for the last release of every ring stage and the leader's MMA thread for
+// the last release of both accumulators, so no multicast commit or remote
+// arrival is still in flight into a CTA that has exited.
+// Measured against one CTA per 128 x 224 tile, bit-identical output and
+// 3503 against 3321 TFLOP/s at 16384 x 14336 x 4096, 3494 against 3283 at
+// 8192^3; a 256 x 224 pair tile with 7 stages ran at 3362.
+constexpr int kPairBN = 256;
+constexpr int kPairStages = 6;
+using PairSmem = Smem<kPairBN / 2, kPairStages, 2, 4>;
+
+__device__ __forceinline__ bool wait_bounded_cluster(uint64_t* bar, uint32_t parity)
 {
-    using L = Smem<BN, STAGES, 2, 4>;
+    return wait_bounded_err_cluster(bar, parity, &g_dev_error);
+}
+
+template <bool OUT_BF16>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
+    k_gemm_tensor_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       EpiParams p, uint32_t idesc, TileSched sched, const __grid_constant__ CUtensorMap tmD)
+{
+    constexpr int BN = kPairBN, BH = BN / 2, STAGES = kPairStages;
+    using L = PairSmem;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
@@ -263,35 +298,111 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t* afull = empty + STAGES;
     uint64_t* aempty = afull + 2;
     uint64_t* drain = aempty + 2;
-    // two BN-column accumulators; the allocation is a power of two >= 32
-    constexpr uint32_t TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
-    static_assert(2 * BN <= 512, "two accumulators must fit in tensor memory");
-
-    uint32_t tmem_base;
-    if (!gemm_setup<STAGES, 2, 4>(smem, L::BAR_OFF, TMEM_COLS, &tmA, &tmB, tmem_base)) return;
-
+    uint32_t* holder = reinterpret_cast<uint32_t*>(drain + 1);
+    constexpr uint32_t TMEM_COLS = 2 * BN;
+    static_assert(TMEM_COLS <= 512, "two accumulators must fit in tensor memory");
+    __shared__ int s_skip;
+    const uint32_t rank = cluster_ctarank();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        s_skip = rank == 0 ? *reinterpret_cast<volatile int*>(&g_dev_error) : 0;
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);            // the leader's expect_tx arrival (both CTAs' bytes)
+            mbar_init(&empty[s], 1);           // the leader's multicast commit
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&afull[b], 1);           // the leader's multicast commit
+            mbar_init(&aempty[b], 8);          // four epilogue warps of each CTA (used in the leader)
+        }
+        mbar_init(drain, 1);
+        fence_mbar_init();
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    __syncthreads();
+    cluster_sync_all();                        // both CTAs' barriers initialised, the leader's flag written
+    int skip = s_skip;
+    if (rank != 0) skip = (int)ld_shared_cluster_u32(cluster_map(smem_addr(&s_skip), 0));
+    cluster_sync_all();                        // the flag is read before either CTA may leave
+    if (skip) return;                          // the same decision in both CTAs
+    if (warp == 1) {
+        tmem_alloc_pair(holder, TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *holder;
+
     const int num_tiles = sched.num_m * sched.num_n;
     const int nkb = (p.K + BK - 1) / BK;
+    const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
 
     if (warp == 0) {
-        if (lane == 0) producer_loop<BN, STAGES>(smem, full, empty, &tmA, &tmB, sched, num_tiles, nkb);
-    } else if (warp == 1) {
         if (lane == 0) {
+            constexpr uint32_t PAIR_TX = 2u * (uint32_t)L::STAGE;   // bytes landing per stage in the pair
+            const uint32_t full0 = cluster_map(smem_addr(full), 0);
+            int stage = 0, issued = 0;
+            uint32_t phase = 0;
+            bool aborted = false;
+            for (int t = cid; t < num_tiles && !aborted; t += ncl) {
+                int mb, nb;
+                sched.coords(t, mb, nb);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    if (!wait_bounded_cluster(&empty[stage], phase ^ 1u)) {
+                        aborted = true;
+                        break;
+                    }
+                    uint8_t* sa = smem + stage * L::STAGE;
+                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], PAIR_TX);
+                    tma_load_2d_pair(sa, &tmA, kb * BK, mb * 2 * BM + (int)rank * BM, full0 + 8u * stage);
+                    tma_load_2d_pair(sa + A_BYTES, &tmB, kb * BK, nb * BN + (int)rank * BH, full0 + 8u * stage);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!aborted) {
+                for (int i = 0; i < STAGES; ++i) {     // every stage's last release has landed
+                    if (!wait_bounded_cluster(&empty[stage], phase ^ 1u)) break;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            } else if (rank == 0) {
+                // the pair's copies still in flight complete on the leader's barriers
+                int n = issued < STAGES ? issued : STAGES;
+                int s = stage;
+                uint32_t ph = phase;
+                for (int i = 0; i < n; ++i) {
+                    if (--s < 0) {
+                        s = STAGES - 1;
+                        ph ^= 1u;
+                    }
+                    wait_drain(&full[s], ph);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
             int stage = 0, lt = 0;
             uint32_t phase = 0;
             bool aborted = false;
-            for (int t = blockIdx.x; t < num_tiles && !aborted; t += gridDim.x, ++lt) {
+            for (int t = cid; t < num_tiles && !aborted; t += ncl, ++lt) {
                 const int b = lt & 1;
                 const uint32_t u = (uint32_t)(lt >> 1);
-                if (!wait_bounded(&aempty[b], (u & 1u) ^ 1u)) {
+                if (!wait_bounded_cluster(&aempty[b], (u & 1u) ^ 1u)) {
                     aborted = true;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(b * BN);
                 for (int kb = 0; kb < nkb; ++kb) {
-                    if (!wait_bounded(&full[stage], phase)) {
+                    if (!wait_bounded_cluster(&full[stage], phase)) {
                         aborted = true;
                         break;
                     }
@@ -301,17 +412,22 @@ __global__ void __launch_bounds__(192, 1)
                     const uint64_t db = sdesc_kmajor_sw128(sa + A_BYTES);
 #pragma unroll
                     for (int k = 0; k < BK / 32; ++k)
-                        mma_f8f6f4(d, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
-                    mma_commit(&empty[stage]);
+                        mma_pair_f8f6f4(d, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+                    mma_pair_commit(&empty[stage], 3);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
-                if (!aborted) mma_commit(&afull[b]);
+                if (!aborted) mma_pair_commit(&afull[b], 3);
             }
-            if (aborted) {
-                mma_commit(drain);          // completes once every issued MMA is done
+            if (!aborted) {
+                for (int j = 0; j < 2; ++j) {           // both accumulators' last releases have landed
+                    const int l2 = lt + j;
+                    if (!wait_bounded_cluster(&aempty[l2 & 1], ((uint32_t)(l2 >> 1) & 1u) ^ 1u)) break;
+                }
+            } else {
+                mma_pair_commit(drain, 1);              // completes once every issued MMA is done
                 wait_drain(drain, 0);
             }
         }
@@ -320,16 +436,17 @@ __global__ void __launch_bounds__(192, 1)
         const float scale = __ldg(p.sA) * __ldg(p.sB);
         uint8_t* stg = smem + L::STG_OFF + (warp - 2) * kStageBytes;
         constexpr int SC = OUT_BF16 ? 16 : 8;   // columns per 32-byte staged row segment
+        const uint32_t aempty0 = cluster_map(smem_addr(aempty), 0);
         int lt = 0;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++lt) {
+        for (int t = cid; t < num_tiles; t += ncl, ++lt) {
             const int b = lt & 1;
             const uint32_t u = (uint32_t)(lt >> 1);
-            const bool ok = wait_bounded(&afull[b], u & 1u);
+            const bool ok = wait_bounded_cluster(&afull[b], u & 1u);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             tc_fence_after();
             int mb, nb;
             sched.coords(t, mb, nb);
-            const int row0 = mb * BM + quarter * 32;
+            const int row0 = mb * 2 * BM + (int)rank * BM + quarter * 32;
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * BN);
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {
@@ -351,14 +468,15 @@ __global__ void __launch_bounds__(192, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&aempty[b]);
+            if (lane == 0) mbar_arrive_cluster(aempty0 + 8u * b);
         }
         stage_store_drain(lane);
     }
     __syncthreads();
+    cluster_sync_all();                        // nothing is pending into either CTA any more
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
     }
 }
 
@@ -932,16 +1050,38 @@ static bool make_tmap_out(CUtensorMap* m, void* D, int64_t M, int64_t N, bool bf
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Co-resident CTA pairs of the pair kernel on the current device (queried
+// once per device and output type; the kernel's resources never change).
 template <typename KernelT>
-static cudaError_t launch_persistent(KernelT kernel, int threads, int smem_bytes, int num_tiles, int sms,
-                                     cudaStream_t st, const CUtensorMap& ta, const CUtensorMap& tb,
-                                     const EpiParams& p, uint32_t idesc, const TileSched& sched)
+static cudaError_t pair_clusters(KernelT kern, int variant, int smem, int* clusters)
 {
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    static int cache[2][64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    int grid = num_tiles < sms ? num_tiles : sms;
-    kernel<<<grid, threads, smem_bytes, st>>>(ta, tb, p, idesc, sched);
-    return cudaGetLastError();
+    if (dev >= 0 && dev < 64 && cache[variant][dev] > 0) {
+        *clusters = cache[variant][dev];
+        return cudaSuccess;
+    }
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(192, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, (void*)kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) cache[variant][dev] = n;
+    *clusters = n;
+    return cudaSuccess;
 }
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char** why)
@@ -965,10 +1105,8 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
     p.D = g.D;
     CUtensorMap ta, tb;
     if (g.mode == 0) {
-        // 128x224 tiles with a 5-stage ring (225 KB): measured faster than
-        // 128x256 x 4 stages on every FFN shape, and 224 divides 14336
-        constexpr int BN = 224, ST = 5;
-        if (!make_tmap(&ta, g.A, g.K, g.M, BM) || !make_tmap(&tb, g.B, g.K, g.N, BN)) {
+        constexpr int BN = kPairBN;
+        if (!make_tmap(&ta, g.A, g.K, g.M, BM) || !make_tmap(&tb, g.B, g.K, g.N, BN / 2)) {
             *why = "cuTensorMapEncodeTiled failed";
             return cudaErrorInvalidValue;
         }
@@ -977,14 +1115,23 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
             *why = "cuTensorMapEncodeTiled failed (output)";
             return cudaErrorInvalidValue;
         }
-        TileSched sched{(int)((g.M + BM - 1) / BM), (int)((g.N + BN - 1) / BN), 16};
+        TileSched sched{(int)((g.M + 2 * BM - 1) / (2 * BM)), (int)((g.N + BN - 1) / BN), 8};
         const int tiles = sched.num_m * sched.num_n;
-        const uint32_t idesc = make_idesc(g.a_format, g.b_format, BN);
-        const int smem = Smem<BN, ST, 2, 4>::BYTES;
-        auto kern = bf16 ? k_gemm_tensor<BN, ST, true> : k_gemm_tensor<BN, ST, false>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        const int grid = tiles < sms ? tiles : sms;
+        uint32_t idesc = make_idesc(g.a_format, g.b_format, BN);
+        idesc = (idesc & ~(0x1Fu << 24)) | ((uint32_t)((2 * BM) >> 4) << 24);   // M = 256 over the pair
+        const int smem = PairSmem::BYTES;
+        auto kern = bf16 ? k_gemm_tensor_pair<true> : k_gemm_tensor_pair<false>;
+        int clusters = 0;
+        cudaError_t e = pair_clusters(kern, bf16 ? 1 : 0, smem, &clusters);
+        if (e != cudaSuccess) {
+            *why = "cluster occupancy query failed";
+            return e;
+        }
+        if (clusters < 1) {
+            *why = "no CTA pair of this kernel fits on the device";
+            return cudaErrorNotSupported;
+        }
+        const int grid = 2 * (tiles < clusters ? tiles : clusters);
         kern<<<grid, 192, smem, st>>>(ta, tb, p, idesc, sched, td);
         return cudaGetLastError();
     }
