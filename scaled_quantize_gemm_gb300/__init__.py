@@ -75,6 +75,11 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
+def _t():
+    import torch
+    return torch
+
+
 def _ptr(t):
     if t is None:
         return None
@@ -97,6 +102,46 @@ def _check(code: int):
         raise Fp8Error(code, lib().fp8_last_error().decode())
 
 
+def _need(t, name: str, dtype=None, nbytes: int = None):
+    """The C ABI takes raw pointers and cannot see a buffer's size: check here
+    that each tensor is contiguous, of the documented dtype and large enough,
+    so a wrong buffer raises instead of being written out of bounds."""
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, the library expects {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if nbytes is not None and t.numel() * t.element_size() < nbytes:
+        raise ValueError(f"{name}: {t.numel() * t.element_size()} bytes, needs {nbytes}")
+
+
+def _opt(t, name: str, dtype=None, nbytes: int = None):
+    if t is not None:
+        _need(t, name, dtype, nbytes)
+
+
+def _units(gran: int, R: int, C: int) -> int:
+    """number of scaling units of an R x C tensor (include/fp8sq.h)"""
+    if gran == TENSOR:
+        return 1
+    if gran == TILE_1x128:
+        return R * (C // 128)
+    if gran == BLOCK_128x128:
+        return ((R + 127) // 128) * ((C + 127) // 128)
+    if gran == TILE_128x1:
+        return (R // 128) * C
+    return R * C // 32          # MX-32 blocks (and the power-of-two codes in their tiled layout)
+
+
+def _scale_bytes(gran: int, R: int, C: int) -> int:
+    """bytes of the scales fp8_quantize writes: fp32 per unit, or one E8M0
+    byte per 32-element block"""
+    if gran in (TENSOR, TILE_1x128, BLOCK_128x128, TILE_128x1):
+        return 4 * _units(gran, R, C)
+    return R * C // 32
+
+
 def _dtype_code(t) -> int:
     import torch
     if t.dtype == torch.bfloat16:
@@ -109,15 +154,21 @@ def _dtype_code(t) -> int:
 # ---------------------------------------------------------------- entry points
 def fp8_amax(x, gran: int, amax_out, stream=None) -> None:
     R, C = (x.shape[0], x.shape[1]) if x.dim() == 2 else (1, x.numel())
+    _need(x, "x")
+    _need(amax_out, "amax_out", _t().float32, 4 * _units(gran, R, C))
     _check(lib().fp8_amax(_ptr(x), _dtype_code(x), R, C, gran, _ptr(amax_out), _stream(stream)))
 
 
 def fp8_scale_init(states, n_states: int, history_len: int, stream=None) -> None:
+    _need(states, "states", _t().float32, 4 * n_states * (history_len + 2))
     _check(lib().fp8_scale_init(_ptr(states), n_states, history_len, _stream(stream)))
 
 
 def fp8_update_scale(states, n_states: int, history_len: int, formats, algo: int = AMAX_MAX,
                      stream=None) -> None:
+    _need(states, "states", _t().float32, 4 * n_states * (history_len + 2))
+    if len(formats) < n_states:
+        raise ValueError(f"formats: {len(formats)} entries for {n_states} states")
     arr = (ctypes.c_int * max(1, n_states))(*formats)
     _check(lib().fp8_update_scale(_ptr(states), n_states, history_len, arr, algo, _stream(stream)))
 
@@ -125,6 +176,12 @@ def fp8_update_scale(states, n_states: int, history_len: int, formats, algo: int
 def fp8_quantize(x, format: int, gran: int, q, qT=None, scales_out=None, amax_out=None,
                  delayed_state=None, history_len: int = 0, sat_count=None, stream=None) -> None:
     R, C = (x.shape[0], x.shape[1]) if x.dim() == 2 else (1, x.numel())
+    T = _t()
+    _need(x, "x")
+    _opt(q, "q", T.uint8, R * C)
+    _opt(qT, "qT", T.uint8, R * C)
+    _opt(scales_out, "scales_out", None, _scale_bytes(gran, R, C))
+    _opt(delayed_state, "delayed_state", T.float32, 4 * (history_len + 2))
     _check(lib().fp8_quantize(_ptr(x), _dtype_code(x), R, C, format, gran, _ptr(delayed_state), history_len,
                               _ptr(q), _ptr(qT), _ptr(scales_out), _ptr(amax_out), _ptr(sat_count),
                               _stream(stream)))
@@ -135,6 +192,11 @@ def fp8_gemm(A, a_format: int, a_scale, a_gran: int, B, b_format: int, b_scale, 
     M = A.shape[0] if M is None else M
     K = A.shape[1] if K is None else K
     N = B.shape[0] if N is None else N
+    T = _t()
+    _need(A, "A", T.uint8, M * K)
+    _need(B, "B", T.uint8, N * K)
+    _need(D, "D", None, M * N * (2 if D.dtype == T.bfloat16 else 4))
+    _opt(bias, "bias", T.float32, 4 * N)
     _check(lib().fp8_gemm(_ptr(A), a_format, _ptr(a_scale), a_gran, _ptr(B), b_format, _ptr(b_scale), b_gran,
                           M, N, K, _ptr(bias), _ptr(D), _dtype_code(D), _stream(stream)))
 
@@ -147,6 +209,14 @@ def fp8_linear_fwd(x, w, y, workspace, gran: int = TENSOR, recipe: int = RECIPE_
                    x_state=None, w_state=None, history_len: int = 0, bias=None, stream=None) -> None:
     M, K = x.shape
     N = w.shape[0]
+    T = _t()
+    _need(x, "x", T.bfloat16)
+    _need(w, "w", T.bfloat16, 2 * N * K)
+    _need(y, "y", None, M * N * (2 if y.dtype == T.bfloat16 else 4))
+    _need(workspace, "workspace", T.uint8)
+    _opt(x_state, "x_state", T.float32, 4 * (history_len + 2))
+    _opt(w_state, "w_state", T.float32, 4 * (history_len + 2))
+    _opt(bias, "bias", T.float32, 4 * N)
     _check(lib().fp8_linear_fwd(_ptr(x), _ptr(w), M, N, K, gran, recipe, _ptr(x_state), _ptr(w_state),
                                 history_len, _ptr(workspace), workspace.numel() * workspace.element_size(),
                                 _ptr(bias), _ptr(y), _dtype_code(y), _stream(stream)))
@@ -155,6 +225,12 @@ def fp8_linear_fwd(x, w, y, workspace, gran: int = TENSOR, recipe: int = RECIPE_
 def fp8_linear_bwd(dy, dx, dw, workspace, K: int, gran: int = TENSOR, recipe: int = RECIPE_HYBRID,
                    dy_state=None, history_len: int = 0, stream=None) -> None:
     M, N = dy.shape
+    T = _t()
+    _need(dy, "dy", T.bfloat16)
+    _need(dx, "dx", T.bfloat16, 2 * M * K)
+    _need(dw, "dw", T.float32, 4 * N * K)
+    _need(workspace, "workspace", T.uint8)
+    _opt(dy_state, "dy_state", T.float32, 4 * (history_len + 2))
     _check(lib().fp8_linear_bwd(_ptr(dy), M, N, K, gran, recipe, _ptr(dy_state), history_len, _ptr(workspace),
                                 workspace.numel() * workspace.element_size(), _ptr(dx), _ptr(dw),
                                 _stream(stream)))
@@ -163,6 +239,15 @@ def fp8_linear_bwd(dy, dx, dw, workspace, K: int, gran: int = TENSOR, recipe: in
 def fp8_layernorm_quantize(x, gamma, beta, eps: float, format: int, q, qT, mu, rstd, delayed_state,
                            history_len: int, stream=None) -> None:
     M, K = x.shape
+    T = _t()
+    _need(x, "x", T.bfloat16)
+    _need(gamma, "gamma", T.float32, 4 * K)
+    _opt(beta, "beta", T.float32, 4 * K)
+    _opt(q, "q", T.uint8, M * K)
+    _opt(qT, "qT", T.uint8, M * K)
+    _need(mu, "mu", T.float32, 4 * M)
+    _need(rstd, "rstd", T.float32, 4 * M)
+    _opt(delayed_state, "delayed_state", T.float32, 4 * (history_len + 2))
     _check(lib().fp8_layernorm_quantize(_ptr(x), _ptr(gamma), _ptr(beta), eps, M, K, format, _ptr(delayed_state),
                                         history_len, _ptr(q), _ptr(qT), _ptr(mu), _ptr(rstd), _stream(stream)))
 
@@ -171,6 +256,18 @@ def fp8_layernorm_linear_fwd(x, gamma, beta, eps: float, w, y, workspace, mu, rs
                              history_len: int, bias=None, stream=None) -> None:
     M, K = x.shape
     N = w.shape[0]
+    T = _t()
+    _need(x, "x", T.bfloat16)
+    _need(gamma, "gamma", T.float32, 4 * K)
+    _opt(beta, "beta", T.float32, 4 * K)
+    _need(w, "w", T.bfloat16, 2 * N * K)
+    _need(y, "y", None, M * N * (2 if y.dtype == T.bfloat16 else 4))
+    _need(workspace, "workspace", T.uint8)
+    _need(mu, "mu", T.float32, 4 * M)
+    _need(rstd, "rstd", T.float32, 4 * M)
+    _opt(x_state, "x_state", T.float32, 4 * (history_len + 2))
+    _opt(w_state, "w_state", T.float32, 4 * (history_len + 2))
+    _opt(bias, "bias", T.float32, 4 * N)
     _check(lib().fp8_layernorm_linear_fwd(_ptr(x), _ptr(gamma), _ptr(beta), eps, _ptr(w), M, N, K, _ptr(x_state),
                                           _ptr(w_state), history_len, _ptr(workspace),
                                           workspace.numel() * workspace.element_size(), _ptr(mu), _ptr(rstd),
@@ -182,6 +279,11 @@ def fp8_linear_fwd_noalloc(x, w, y, bias=None, stream=None) -> None:
     scratch is the library's static device array (see include/fp8sq.h)."""
     M, K = x.shape
     N = w.shape[0]
+    T = _t()
+    _need(x, "x", T.bfloat16)
+    _need(w, "w", T.bfloat16, 2 * N * K)
+    _need(y, "y", None, M * N * (2 if y.dtype == T.bfloat16 else 4))
+    _opt(bias, "bias", T.float32, 4 * N)
     _check(lib().fp8_linear_fwd_noalloc(_ptr(x), _ptr(w), M, N, K, _ptr(bias), _ptr(y), _dtype_code(y),
                                         _stream(stream)))
 

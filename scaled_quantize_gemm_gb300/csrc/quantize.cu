@@ -162,13 +162,18 @@ __device__ __forceinline__ uint32_t mx_scale_floor(uint32_t amax_bits, float& m)
 
 // cast 8 values with multiplier m; returns 8 codes packed little-endian
 template <int FMT>
-__device__ __forceinline__ uint2 cast8(const float (&f)[8], float m, uint32_t& nsat)
+__device__ __forceinline__ uint2 cast8(const float (&f)[8], float m, uint32_t absbits, uint32_t& nsat)
 {
+    // absbits: fp32 bit pattern of max |f_i|.  rn(|x| m) is monotone in |x|
+    // (m > 0), so no element saturates unless the scaled maximum does; the
+    // elements are counted one by one only then, or when the chunk holds an
+    // inf or NaN (whose bit pattern says nothing about the other elements).
     float p[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        p[i] = __fmul_rn(f[i], m);
-        nsat += (fabsf(p[i]) > Fmt<FMT>::fmax) ? 1u : 0u;
+    for (int i = 0; i < 8; ++i) p[i] = __fmul_rn(f[i], m);
+    if (absbits >= 0x7F800000u || __fmul_rn(__uint_as_float(absbits), m) > Fmt<FMT>::fmax) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) nsat += (fabsf(p[i]) > Fmt<FMT>::fmax) ? 1u : 0u;
     }
     uint32_t lo = cvt_fp8x2<FMT>(p[0], p[1]) | (cvt_fp8x2<FMT>(p[2], p[3]) << 16);
     uint32_t hi = cvt_fp8x2<FMT>(p[4], p[5]) | (cvt_fp8x2<FMT>(p[6], p[7]) << 16);
@@ -269,10 +274,11 @@ __global__ void __launch_bounds__(kFlatThreads) k_cast_tensor(const void* __rest
 #pragma unroll
         for (int u = 0; u < kFlatUnroll; ++u) {
             int64_t c = c0 + u * kFlatThreads + threadIdx.x;
-            if (DELAYED) mx = max(mx, v[u].absmax_bits());
+            const uint32_t ab = v[u].absmax_bits();
+            if (DELAYED) mx = max(mx, ab);
             float f[8];
             v[u].get(f);
-            uint2 codes = cast8<FMT>(f, m, nsat);
+            uint2 codes = cast8<FMT>(f, m, ab, nsat);
             if (c < nch) *reinterpret_cast<uint2*>(q + c * 8) = codes;
         }
     }
@@ -360,10 +366,11 @@ __global__ void __launch_bounds__(256) k_cast_tensor_T(const void* __restrict__ 
     uint2 rows[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        if (DELAYED) mx = max(mx, v[i].absmax_bits());
+        const uint32_t ab = v[i].absmax_bits();
+        if (DELAYED) mx = max(mx, ab);
         float f[8];
         v[i].get(f);
-        rows[i] = cast8<FMT>(f, m, nsat);
+        rows[i] = cast8<FMT>(f, m, ab, nsat);
     }
     if (ok) {
 #pragma unroll
@@ -534,20 +541,23 @@ __global__ void __launch_bounds__(kTThreads, 1)
                 for (int i = 0; i < 8; ++i) {
                     float f[8];
                     v[i].get(f);
+                    uint32_t ab = 0;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         f[j] = __fmaf_rn(__fmul_rn(__fsub_rn(f[j], mu[i]), rs[i]), g[j], be[j]);
-                        if (DELAYED && inside) mx = max(mx, __float_as_uint(f[j]) & 0x7FFFFFFFu);
+                        ab = max(ab, __float_as_uint(f[j]) & 0x7FFFFFFFu);
                     }
-                    rows[i] = cast8<FMT>(f, m, ns);
+                    if (DELAYED && inside) mx = max(mx, ab);
+                    rows[i] = cast8<FMT>(f, m, ab, ns);
                 }
             } else {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    if (DELAYED) mx = max(mx, v[i].absmax_bits());
+                    const uint32_t ab = v[i].absmax_bits();
+                    if (DELAYED) mx = max(mx, ab);
                     float f[8];
                     v[i].get(f);
-                    rows[i] = cast8<FMT>(f, m, ns);
+                    rows[i] = cast8<FMT>(f, m, ab, ns);
                 }
             }
             if (inside) {
@@ -612,6 +622,8 @@ __global__ void __launch_bounds__(kTThreads, 1)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTStages * kTTile);
     uint64_t* empty = full + kTStages;
     __shared__ uint32_t colred[2][4][64];     // [half][quarter][column], 128-row tiles only
+    __shared__ __align__(16) float colm[2][64];           // column multipliers, 128-row tiles
+    __shared__ __align__(16) uint8_t colflag[2][64];      // column may saturate, 128-row tiles
     __shared__ int s_skip;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tiles_c = (int)((C + 127) / 128);
@@ -706,24 +718,46 @@ __global__ void __launch_bounds__(kTThreads, 1)
             a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 16));
             cm[j] = a;
         }
+        const int64_t tr0 = (int64_t)(t / tiles_c) * 128;
+        const int64_t r0 = tr0 + rloc;
+        const int64_t c0 = (int64_t)(t % tiles_c) * 128 + cloc;
+        float m[8];
+        uint32_t code[8];
+        bool maysat = false;      // some column's scaled maximum may exceed fmax
         if (UNIT == 128) {
+            // the tile's 128 column maxima meet in shared memory; thread c < 128
+            // then computes column c's scale once for the whole CTA (and writes
+            // it: 128 consecutive floats), and every thread reads its 8 back
             if (rg == 0) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) colred[h][rq][cg * 8 + j] = cm[j];
             }
             asm volatile("bar.sync 1, 256;" ::: "memory");
+            if (threadIdx.x < 128) {
+                const int hh = threadIdx.x >> 6, cc = threadIdx.x & 63;
+                const uint32_t a = max(max(colred[hh][0][cc], colred[hh][1][cc]),
+                                       max(colred[hh][2][cc], colred[hh][3][cc]));
+                float mm, ss;
+                current_scale<FMT>(a, mm, ss);
+                colm[hh][cc] = mm;
+                colflag[hh][cc] =
+                    (a >= 0x7F800000u || __fmul_rn(__uint_as_float(a), mm) > Fmt<FMT>::fmax) ? 1 : 0;
+                const int64_t c = (int64_t)(t % tiles_c) * 128 + threadIdx.x;
+                if (c < C) static_cast<float*>(scales)[(tr0 / 128) * C + c] = ss;
+            }
+            asm volatile("bar.sync 1, 256;" ::: "memory");   // colm ready; colred free for the next tile
+            const float4 m0 = *reinterpret_cast<const float4*>(&colm[h][cg * 8]);
+            const float4 m1 = *reinterpret_cast<const float4*>(&colm[h][cg * 8 + 4]);
+            m[0] = m0.x; m[1] = m0.y; m[2] = m0.z; m[3] = m0.w;
+            m[4] = m1.x; m[5] = m1.y; m[6] = m1.z; m[7] = m1.w;
+            const uint2 fl = *reinterpret_cast<const uint2*>(&colflag[h][cg * 8]);   // the 8 columns' flags
+            maysat = (fl.x | fl.y) != 0u;
+        } else {
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                cm[j] = max(max(colred[h][0][cg * 8 + j], colred[h][1][cg * 8 + j]),
-                            max(colred[h][2][cg * 8 + j], colred[h][3][cg * 8 + j]));
-            asm volatile("bar.sync 1, 256;" ::: "memory");   // colred is rewritten by the next tile
-        }
-        float m[8], sc[8];
-        uint32_t code[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (UNIT == 32) code[j] = mx_scale<FMT>(cm[j], m[j]);
-            else current_scale<FMT>(cm[j], m[j], sc[j]);
+            for (int j = 0; j < 8; ++j) {
+                code[j] = mx_scale<FMT>(cm[j], m[j]);
+                maysat |= cm[j] >= 0x7F800000u || __fmul_rn(__uint_as_float(cm[j]), m[j]) > Fmt<FMT>::fmax;
+            }
         }
         uint2 rows[8];
         uint32_t ns = 0;
@@ -731,16 +765,14 @@ __global__ void __launch_bounds__(kTThreads, 1)
         for (int i = 0; i < 8; ++i) {
             float p[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                p[j] = __fmul_rn(f[i][j], m[j]);
-                ns += (fabsf(p[j]) > Fmt<FMT>::fmax) ? 1u : 0u;
+            for (int j = 0; j < 8; ++j) p[j] = __fmul_rn(f[i][j], m[j]);
+            if (maysat) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) ns += (fabsf(p[j]) > Fmt<FMT>::fmax) ? 1u : 0u;
             }
             rows[i].x = cvt_fp8x2<FMT>(p[0], p[1]) | (cvt_fp8x2<FMT>(p[2], p[3]) << 16);
             rows[i].y = cvt_fp8x2<FMT>(p[4], p[5]) | (cvt_fp8x2<FMT>(p[6], p[7]) << 16);
         }
-        const int64_t tr0 = (int64_t)(t / tiles_c) * 128;
-        const int64_t r0 = tr0 + rloc;
-        const int64_t c0 = (int64_t)(t % tiles_c) * 128 + cloc;
         if (r0 < R && c0 < C) {
             nsat += ns;
             if (q) {
@@ -751,19 +783,11 @@ __global__ void __launch_bounds__(kTThreads, 1)
             transpose8x8(rows, cols);
 #pragma unroll
             for (int j = 0; j < 8; ++j) *reinterpret_cast<uint2*>(qT + (c0 + j) * R + r0) = cols[j];
-            if (rg == 0) {
-                if (UNIT == 128) {
-                    if (rq == 0) {
-                        float* s_out = static_cast<float*>(scales) + (tr0 / 128) * C + c0;
-                        *reinterpret_cast<float4*>(s_out) = make_float4(sc[0], sc[1], sc[2], sc[3]);
-                        *reinterpret_cast<float4*>(s_out + 4) = make_float4(sc[4], sc[5], sc[6], sc[7]);
-                    }
-                } else {
-                    uint8_t* e = static_cast<uint8_t*>(scales);
-                    const int64_t t32 = (tr0 + rq * 32) / 32;
+            if (UNIT == 32 && rg == 0) {
+                uint8_t* e = static_cast<uint8_t*>(scales);
+                const int64_t t32 = (tr0 + rq * 32) / 32;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) e[mx_tiled_offset(c0 + j, t32, R)] = (uint8_t)code[j];
-                }
+                for (int j = 0; j < 8; ++j) e[mx_tiled_offset(c0 + j, t32, R)] = (uint8_t)code[j];
             }
         }
     }
@@ -881,9 +905,11 @@ int read_device_error_quant(int clear)
 }
 
 // ================================================================== row units
-// 1x128 tiles (UNIT = 128) and MX-32 blocks (UNIT = 32): a unit is UNIT/8
-// consecutive lanes, each holding one 128-bit chunk; units never straddle a
-// row because cols % UNIT == 0, so the tensor is treated as flat.
+// 1x128 tiles (UNIT = 128) and MX-32 blocks (UNIT = 32).  Each lane holds 16
+// consecutive elements (two 128-bit chunks) and a unit is UNIT/16 consecutive
+// lanes; units never straddle a row because cols % UNIT == 0, so the tensor is
+// treated as flat.  Sixteen elements per lane halve the per-element cost of
+// the unit's shuffles and scale computation against eight.
 // WRITE_Q = false computes the unit amaxes only (fp8_amax).
 // RULE: 0 = current fp32 scale (1x128 tiles); 1 = E8M0, smallest power of two
 // that fits (MX-32 blocks, and power-of-two 1x128 tiles); 2 = E8M0 by the
@@ -895,26 +921,33 @@ __global__ void __launch_bounds__(kFlatThreads) k_quant_rowunits(const void* __r
                                                                  float* amax_out, unsigned long long* sat,
                                                                  int64_t cols = 0)
 {
-    constexpr int TPU = UNIT / 8;  // lanes per unit
-    const int64_t nch = n / 8;
+    constexpr int TPU = UNIT / 16;  // lanes per unit
+    const int64_t ng = n / 16;      // 16-element groups
     uint32_t nsat = 0;
     const int64_t stride = (int64_t)gridDim.x * kFlatThreads * kFlatUnroll;
-    for (int64_t c0 = (int64_t)blockIdx.x * kFlatThreads * kFlatUnroll; c0 < nch; c0 += stride) {
-        Vec8<DT> v[kFlatUnroll];
+    for (int64_t g0 = (int64_t)blockIdx.x * kFlatThreads * kFlatUnroll; g0 < ng; g0 += stride) {
+        Vec8<DT> v[kFlatUnroll][2];
 #pragma unroll
         for (int u = 0; u < kFlatUnroll; ++u) {
-            int64_t c = c0 + u * kFlatThreads + threadIdx.x;
-            if (c < nch) v[u].load(x, c * 8); else v[u].zero();
+            const int64_t g = g0 + u * kFlatThreads + threadIdx.x;
+            if (g < ng) {
+                v[u][0].load(x, g * 16);
+                v[u][1].load(x, g * 16 + 8);
+            } else {
+                v[u][0].zero();
+                v[u][1].zero();
+            }
         }
 #pragma unroll
         for (int u = 0; u < kFlatUnroll; ++u) {
-            const int64_t c = c0 + u * kFlatThreads + threadIdx.x;
-            uint32_t a = v[u].absmax_bits();
+            const int64_t g = g0 + u * kFlatThreads + threadIdx.x;
+            const uint32_t b0 = v[u][0].absmax_bits(), b1 = v[u][1].absmax_bits();
+            uint32_t a = max(b0, b1);
 #pragma unroll
             for (int o = TPU / 2; o >= 1; o >>= 1) a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
-            const bool valid = c < nch;            // uniform over a unit's lanes
+            const bool valid = g < ng;             // uniform over a unit's lanes
             const bool leader = (threadIdx.x % TPU) == 0;
-            const int64_t unit = c / TPU;
+            const int64_t unit = g / TPU;
             if (valid && leader && amax_out) amax_out[unit] = __uint_as_float(a);
             if (WRITE_Q) {
                 float m, s = 0.0f;
@@ -923,19 +956,26 @@ __global__ void __launch_bounds__(kFlatThreads) k_quant_rowunits(const void* __r
                 else if (RULE == 2) code = mx_scale_floor<FMT>(a, m);
                 else current_scale<FMT>(a, m, s);
                 float f[8];
-                v[u].get(f);
-                uint32_t ns = 0;
-                uint2 codes = cast8<FMT>(f, m, ns);
+                v[u][0].get(f);
+                const uint2 c0 = cast8<FMT>(f, m, b0, nsat);
+                v[u][1].get(f);
+                const uint2 c1 = cast8<FMT>(f, m, b1, nsat);
                 if (valid) {
-                    nsat += ns;
-                    *reinterpret_cast<uint2*>(q + c * 8) = codes;
+                    *reinterpret_cast<uint4*>(q + g * 16) = make_uint4(c0.x, c0.y, c1.x, c1.y);
                     if (leader) {
                         if (RULE == 0) {
                             static_cast<float*>(scales)[unit] = s;
                         } else if (TILED) {
                             constexpr int SUB = UNIT / 32;      // 32-blocks per unit
                             const int64_t per_row = cols / UNIT;
-                            const int64_t r = unit / per_row, t = unit % per_row;
+                            int64_t r, t;
+                            if ((uint64_t)unit < (1ull << 32)) {     // 32-bit division where it fits
+                                r = (uint32_t)unit / (uint32_t)per_row;
+                                t = (uint32_t)unit - (uint32_t)r * (uint32_t)per_row;
+                            } else {
+                                r = unit / per_row;
+                                t = unit % per_row;
+                            }
 #pragma unroll
                             for (int i = 0; i < SUB; ++i)
                                 static_cast<uint8_t*>(scales)[mx_tiled_offset(r, t * SUB + i, cols)] = (uint8_t)code;
@@ -999,7 +1039,7 @@ __global__ void __launch_bounds__(256) k_quant_block128(const void* __restrict__
     for (int i = 0; i < 8; ++i) {
         float f[8];
         v[i].get(f);
-        rows[i] = cast8<FMT>(f, m, nsat);
+        rows[i] = cast8<FMT>(f, m, v[i].absmax_bits(), nsat);
         *reinterpret_cast<uint2*>(q + (r0 + i) * C + c0) = rows[i];
     }
     if (qT) {
@@ -1064,10 +1104,10 @@ static cudaError_t amax_dt(const QuantArgs& a, cudaStream_t st, int sms)
         if (n > 0) k_amax_tensor<DT><<<flat_grid(n / 8, sms), kFlatThreads, 0, st>>>(a.x, n, a.amax);
         break;
     case kTile:
-        if (n > 0) k_quant_rowunits<DT, kE4M3, 128, false><<<flat_grid(n / 8, sms), kFlatThreads, 0, st>>>(a.x, n, nullptr, nullptr, a.amax, nullptr);
+        if (n > 0) k_quant_rowunits<DT, kE4M3, 128, false><<<flat_grid(n / 16, sms), kFlatThreads, 0, st>>>(a.x, n, nullptr, nullptr, a.amax, nullptr);
         break;
     case kMX:
-        if (n > 0) k_quant_rowunits<DT, kE4M3, 32, false><<<flat_grid(n / 8, sms), kFlatThreads, 0, st>>>(a.x, n, nullptr, nullptr, a.amax, nullptr);
+        if (n > 0) k_quant_rowunits<DT, kE4M3, 32, false><<<flat_grid(n / 16, sms), kFlatThreads, 0, st>>>(a.x, n, nullptr, nullptr, a.amax, nullptr);
         break;
     case kBlock:
         if (n > 0) k_quant_block128<DT, kE4M3, false><<<dim3((unsigned)(a.cols / 128), (unsigned)(a.rows / 128)), 256, 0, st>>>(a.x, a.rows, a.cols, nullptr, nullptr, a.amax, nullptr);
@@ -1136,19 +1176,19 @@ static cudaError_t quant_dt_fmt(const QuantArgs& a, cudaStream_t st, int sms)
     if (n == 0) return cudaSuccess;
     switch (a.gran) {
     case kTile:
-        k_quant_rowunits<DT, FMT, 128, true><<<flat_grid(n / 8, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat);
+        k_quant_rowunits<DT, FMT, 128, true><<<flat_grid(n / 16, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat);
         break;
     case kMX:
-        k_quant_rowunits<DT, FMT, 32, true><<<flat_grid(n / 8, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat);
+        k_quant_rowunits<DT, FMT, 32, true><<<flat_grid(n / 16, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat);
         break;
     case kMXTiled:
-        k_quant_rowunits<DT, FMT, 32, true, true><<<flat_grid(n / 8, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
+        k_quant_rowunits<DT, FMT, 32, true, true><<<flat_grid(n / 16, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
         break;
     case kTilePow2:
-        k_quant_rowunits<DT, FMT, 128, true, true, 1><<<flat_grid(n / 8, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
+        k_quant_rowunits<DT, FMT, 128, true, true, 1><<<flat_grid(n / 16, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
         break;
     case kMXFloor:
-        k_quant_rowunits<DT, FMT, 32, true, true, 2><<<flat_grid(n / 8, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
+        k_quant_rowunits<DT, FMT, 32, true, true, 2><<<flat_grid(n / 16, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
         break;
     case kBlockPow2:
         k_quant_block128<DT, FMT, true, true><<<dim3((unsigned)(a.cols / 128), (unsigned)(a.rows / 128)), 256, 0, st>>>(a.x, a.rows, a.cols, a.q, nullptr, a.amax, a.sat, nullptr, nullptr, static_cast<uint8_t*>(a.scales));
