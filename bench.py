@@ -553,7 +553,8 @@ def kernel_case(case: str, launches: int):
     (k_gemm_tensor_pair), 'cast' = the 16384 x 14336 E5M2 cast with its transposed
     copy (k_cast_T_tma), 'promote' = the 4096^3 1x128 x 128x128 GEMM
     (k_gemm_promote), 'mx' = the 8192^3 MX-32 GEMM (k_gemm_mx), 'fine' = the
-    fine-grained casts (1x128, 128x128, MX-32 tiled, 128x1 columns)."""
+    fine-grained casts (1x128, 128x128, MX-32 tiled, 128x1 columns), 'ln' =
+    the LayerNorm-fused cast of a 16384 x 4096 activation."""
     import scaled_quantize_gemm_gb300 as sq
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -608,6 +609,18 @@ def kernel_case(case: str, launches: int):
             sq.fp8_quantize(w, sq.E4M3, sq.BLOCK_128x128, qw, scales_out=sw)
             sq.fp8_quantize(a4, sq.E4M3, sq.MX32_TILED, qa, scales_out=ea)
             sq.fp8_quantize(dy, sq.E5M2, sq.TILE_128x1, None, qT=qdT, scales_out=sd)
+    elif case == "ln":
+        # LayerNorm fused into the delayed E4M3 cast with the transposed copy,
+        # 16384 x 4096 (k_ln_stats, then k_cast_T_tma in its LayerNorm mode)
+        M, K = 16384, 4096
+        xl = wl.normal((M, K), 2.0, 11, dev)
+        gamma = torch.rand(K, generator=torch.Generator().manual_seed(12)).add_(0.5).to(dev)
+        beta = wl.normal((K,), 0.1, 13, dev, dtype=torch.float32)
+        ql, qlT = torch.empty((M, K), **u8), torch.empty((K, M), **u8)
+        mu = torch.empty(M, dtype=torch.float32, device=dev)
+        rs = torch.empty(M, dtype=torch.float32, device=dev)
+        for _ in range(launches):
+            sq.fp8_layernorm_quantize(xl, gamma, beta, 1e-5, sq.E4M3, ql, qlT, mu, rs, st, H)
     elif case == "promote":
         x, w = wl.w3_operands(dev)
         qx, qw = torch.empty(x.shape, **u8), torch.empty(w.shape, **u8)
@@ -770,6 +783,22 @@ def modes_table(reps: int = 10):
         row(f"fp8_linear_bwd {name} current", "4096^3",
             med(lambda: sq.fp8_linear_bwd(dy, dx, dw, ws, K, gran=gran)), flops=4 * M * N * K)
 
+    # LayerNorm fused into the delayed per-tensor cast (with the transposed
+    # copy): x read twice (statistics, then the normalise-and-cast pass),
+    # codes and transposed codes written = 6 bytes moved per element
+    M, K = 16384, 4096
+    xl = wl.normal((M, K), 2.0, 11, dev)
+    gamma = torch.rand(K, generator=torch.Generator().manual_seed(12)).add_(0.5).to(dev)
+    beta = wl.normal((K,), 0.1, 13, dev, dtype=torch.float32)
+    ql, qlT = torch.empty((M, K), **u8), torch.empty((K, M), **u8)
+    mu, rs = torch.empty(M, **f32), torch.empty(M, **f32)
+    stl = torch.empty(H + 2, **f32)
+    sq.fp8_scale_init(stl, 1, H)
+    row("fp8_layernorm_quantize E4M3 delayed, with qT (6 B moved / element)", f"{M}x{K}",
+        med(lambda: sq.fp8_layernorm_quantize(xl, gamma, beta, 1e-5, sq.E4M3, ql, qlT, mu, rs, stl, H)),
+        nbytes=6 * M * K)
+    del xl, ql, qlT
+
     # workload 4: MX-32, and the per-tensor GEMM on the same operands
     a, b = wl.w4_operands(dev)
     qa, qb = torch.empty(a.shape, **u8), torch.empty(b.shape, **u8)
@@ -789,7 +818,7 @@ def modes_table(reps: int = 10):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel-case", choices=["gemm", "cast", "promote", "mx", "fine"], default=None,
+    ap.add_argument("--kernel-case", choices=["gemm", "cast", "promote", "mx", "fine", "ln"], default=None,
                     help="run a few launches of one kernel (for profiling) and exit")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--modes", action="store_true",

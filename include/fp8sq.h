@@ -273,9 +273,10 @@ FP8SQ_API int fp8_linear_bwd(const void* dy, int64_t M, int64_t N, int64_t K, in
  *   y = (x - mu[r]) * rstd[r] * gamma[c] + beta[c]      (fp32 arithmetic)
  * then q = sat_RNE_fp8(y * m) with delayed per-tensor scaling: m = state[H],
  * amax(|y|) max-combined into state[0] (as fp8_quantize TENSOR + delayed).
- *   gamma, beta  device f32 [K] (beta may be NULL)
+ *   gamma, beta  device f32 [K], 16-byte aligned (beta may be NULL)
  *   q            device u8 [M][K]; qT device u8 [K][M] or NULL
- *   mu_out, rstd_out  device f32 [M], required (the LayerNorm backward needs them)
+ *   mu_out, rstd_out  device f32 [M], 16-byte aligned, required (the LayerNorm
+ *                     backward needs them)
  *   M % 16 == 0, K % 16 == 0; x, q, qT 16-byte aligned.
  * The row statistics are fp32 reductions whose order is this library's; the
  * codes equal those of the exact LayerNorm except where y * m lies within the

@@ -560,8 +560,9 @@ static int validate_ln(const void* x, const float* gamma, const float* beta, int
     if (H < 1 || H > 4096) return fail(FP8SQ_ERR_INVALID_ARG, "layernorm: bad history_len");
     if (!aligned16(x) || !aligned16(q) || (qT && !aligned16(qT)))
         return fail(FP8SQ_ERR_MISALIGNED, "layernorm: x, q, qT must be 16-byte aligned");
-    if (!aligned4(gamma) || (beta && !aligned4(beta)) || !aligned4(state) || !aligned4(mu) || !aligned4(rstd))
-        return fail(FP8SQ_ERR_MISALIGNED, "layernorm: gamma, beta, state, mu, rstd must be 4-byte aligned");
+    if (!aligned16(gamma) || (beta && !aligned16(beta)) || !aligned16(mu) || !aligned16(rstd))
+        return fail(FP8SQ_ERR_MISALIGNED, "layernorm: gamma, beta, mu, rstd must be 16-byte aligned");
+    if (!aligned4(state)) return fail(FP8SQ_ERR_MISALIGNED, "layernorm: state must be 4-byte aligned");
     return FP8SQ_OK;
 }
 

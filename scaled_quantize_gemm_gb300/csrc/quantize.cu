@@ -529,14 +529,23 @@ __global__ void __launch_bounds__(kTThreads, 1)
             uint2 rows[8];
             uint32_t ns = 0;
             if (LN) {
+                // this thread's 8 columns of gamma / beta and 8 rows of mean /
+                // rstd, as 128-bit loads (the buffers are 16-byte aligned and
+                // cols, rows are multiples of 8 inside the tensor)
                 float g[8], be[8], mu[8], rs[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    g[j] = inside ? __ldg(ln.gamma + c0 + j) : 0.0f;
-                    be[j] = (inside && ln.beta) ? __ldg(ln.beta + c0 + j) : 0.0f;
-                    mu[j] = inside ? __ldg(ln.mu + r0 + j) : 0.0f;
-                    rs[j] = inside ? __ldg(ln.rstd + r0 + j) : 0.0f;
-                }
+                const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                const float4* g4 = reinterpret_cast<const float4*>(ln.gamma + c0);
+                const float4* b4 = reinterpret_cast<const float4*>(ln.beta + c0);
+                const float4* m4 = reinterpret_cast<const float4*>(ln.mu + r0);
+                const float4* r4 = reinterpret_cast<const float4*>(ln.rstd + r0);
+                const float4 ga = inside ? __ldg(g4) : z4, gb = inside ? __ldg(g4 + 1) : z4;
+                const float4 ba = (inside && ln.beta) ? __ldg(b4) : z4, bb = (inside && ln.beta) ? __ldg(b4 + 1) : z4;
+                const float4 ma = inside ? __ldg(m4) : z4, mb = inside ? __ldg(m4 + 1) : z4;
+                const float4 ra = inside ? __ldg(r4) : z4, rb = inside ? __ldg(r4 + 1) : z4;
+                g[0] = ga.x; g[1] = ga.y; g[2] = ga.z; g[3] = ga.w; g[4] = gb.x; g[5] = gb.y; g[6] = gb.z; g[7] = gb.w;
+                be[0] = ba.x; be[1] = ba.y; be[2] = ba.z; be[3] = ba.w; be[4] = bb.x; be[5] = bb.y; be[6] = bb.z; be[7] = bb.w;
+                mu[0] = ma.x; mu[1] = ma.y; mu[2] = ma.z; mu[3] = ma.w; mu[4] = mb.x; mu[5] = mb.y; mu[6] = mb.z; mu[7] = mb.w;
+                rs[0] = ra.x; rs[1] = ra.y; rs[2] = ra.z; rs[3] = ra.w; rs[4] = rb.x; rs[5] = rb.y; rs[6] = rb.z; rs[7] = rb.w;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     float f[8];
@@ -794,79 +803,118 @@ __global__ void __launch_bounds__(kTThreads, 1)
     if (sat) add_sat(sat, nsat);
 }
 
-// LayerNorm statistics, one warp per row: mean = sum(x) / K and
-// var = sum((x - mean)^2) / K in fp32 (per-lane running sums, then a warp
-// tree), rstd = 1 / sqrt(var + eps) with IEEE division and square root.
-// Rows of up to 32 x 8 x LN_REG elements (4096 for LN_REG = 16) are read once
-// into registers with all loads in flight; longer rows take two passes.
-constexpr int LN_REG = 16;
+// LayerNorm statistics: mean = sum(x) / K and var = sum((x - mean)^2) / K in
+// fp32, rstd = 1 / sqrt(var + eps) with IEEE division and square root.  Two
+// warps per row, each holding half of the row in registers (rows of up to
+// 2 x 32 x 8 x LN_REG elements, 4096 for LN_REG = 8, are read once); each
+// lane sums its chunks in a tree and over LN_ACC independent accumulators,
+// then a warp tree, then the two warps' partials meet in shared memory (in a
+// fixed order, so both warps hold the same mean).  Longer rows take a
+// two-pass loop.  Half a row per warp and short dependency chains keep the
+// registers low enough for three blocks (24 warps) per SM.
+constexpr int LN_REG = 8;
+constexpr int LN_ACC = 4;
+constexpr int LN_ROWS = 4;       // rows per 256-thread block
 
-__global__ void __launch_bounds__(256) k_ln_stats(const uint16_t* __restrict__ x, int64_t R, int64_t K, float eps,
-                                                  float* __restrict__ mu, float* __restrict__ rstd)
+__device__ __forceinline__ float ln_sum8(const float (&f)[8])
 {
-    const int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (r >= R) return;
-    const uint16_t* row = x + r * K;
-    const int64_t nch = K / 8;
-    float sum = 0.0f, ss = 0.0f, mean;
-    if (nch <= 32 * LN_REG) {
+    return __fadd_rn(__fadd_rn(__fadd_rn(f[0], f[1]), __fadd_rn(f[2], f[3])),
+                     __fadd_rn(__fadd_rn(f[4], f[5]), __fadd_rn(f[6], f[7])));
+}
+__device__ __forceinline__ float ln_sq8(const float (&f)[8], float mean)
+{
+    float d[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) d[j] = __fsub_rn(f[j], mean);
+    float a = __fmul_rn(d[0], d[0]), b = __fmul_rn(d[1], d[1]);
+#pragma unroll
+    for (int j = 2; j < 8; j += 2) {
+        a = __fmaf_rn(d[j], d[j], a);
+        b = __fmaf_rn(d[j + 1], d[j + 1], b);
+    }
+    return __fadd_rn(a, b);
+}
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+__global__ void __launch_bounds__(256, 3) k_ln_stats(const uint16_t* __restrict__ x, int64_t R, int64_t K, float eps,
+                                                     float* __restrict__ mu, float* __restrict__ rstd)
+{
+    __shared__ float part[LN_ROWS][2];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rl = warp >> 1, half = warp & 1;
+    const int64_t r = (int64_t)blockIdx.x * LN_ROWS + rl;
+    const bool live = r < R;                   // whole rows: both warps of a row agree
+    const uint16_t* row = x + (live ? r : 0) * K;
+    const int64_t nch = K / 8;                 // 8-element chunks of the row
+    const int64_t hch = (nch + 1) / 2;         // chunks of the first half
+    const int64_t c0 = half ? hch : 0, c1 = half ? nch : hch;
+    float mean, ss;
+    if (hch <= 32 * LN_REG) {
         Vec8<kBF16> v[LN_REG];
 #pragma unroll
         for (int i = 0; i < LN_REG; ++i) {
-            const int64_t c = lane + 32 * i;
-            if (c < nch) v[i].load(row, c * 8); else v[i].zero();
+            const int64_t c = c0 + lane + 32 * i;
+            if (live && c < c1) v[i].load(row, c * 8); else v[i].zero();
         }
+        float acc[LN_ACC];
+#pragma unroll
+        for (int k = 0; k < LN_ACC; ++k) acc[k] = 0.0f;
 #pragma unroll
         for (int i = 0; i < LN_REG; ++i) {
             float f[8];
             v[i].get(f);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) sum = __fadd_rn(sum, f[j]);
+            acc[i % LN_ACC] = __fadd_rn(acc[i % LN_ACC], ln_sum8(f));
         }
+        float sum = __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3]));
+        sum = warp_sum(sum);
+        if (lane == 0) part[rl][half] = sum;
+        __syncthreads();
+        mean = __fdiv_rn(__fadd_rn(part[rl][0], part[rl][1]), (float)K);
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xFFFFFFFFu, sum, o));
-        mean = __fdiv_rn(sum, (float)K);
+        for (int k = 0; k < LN_ACC; ++k) acc[k] = 0.0f;
 #pragma unroll
         for (int i = 0; i < LN_REG; ++i) {
-            if (lane + 32 * i >= nch) continue;
+            if (c0 + lane + 32 * i >= c1) continue;
             float f[8];
             v[i].get(f);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float d = __fsub_rn(f[j], mean);
-                ss = __fmaf_rn(d, d, ss);
-            }
+            acc[i % LN_ACC] = __fadd_rn(acc[i % LN_ACC], ln_sq8(f, mean));
         }
+        ss = __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3]));
     } else {
-        for (int64_t c = lane; c < nch; c += 32) {
+        float sum = 0.0f;
+        for (int64_t c = c0 + lane; live && c < c1; c += 32) {
             Vec8<kBF16> v;
             v.load(row, c * 8);
             float f[8];
             v.get(f);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) sum = __fadd_rn(sum, f[j]);
+            sum = __fadd_rn(sum, ln_sum8(f));
         }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xFFFFFFFFu, sum, o));
-        mean = __fdiv_rn(sum, (float)K);
-        for (int64_t c = lane; c < nch; c += 32) {
+        sum = warp_sum(sum);
+        if (lane == 0) part[rl][half] = sum;
+        __syncthreads();
+        mean = __fdiv_rn(__fadd_rn(part[rl][0], part[rl][1]), (float)K);
+        ss = 0.0f;
+        for (int64_t c = c0 + lane; live && c < c1; c += 32) {
             Vec8<kBF16> v;
             v.load(row, c * 8);
             float f[8];
             v.get(f);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float d = __fsub_rn(f[j], mean);
-                ss = __fmaf_rn(d, d, ss);
-            }
+            ss = __fadd_rn(ss, ln_sq8(f, mean));
         }
     }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xFFFFFFFFu, ss, o));
-    if (lane == 0) {
+    ss = warp_sum(ss);
+    __syncthreads();                           // every warp has read its row's mean
+    if (lane == 0) part[rl][half] = ss;
+    __syncthreads();
+    if (live && half == 0 && lane == 0) {
         mu[r] = mean;
-        rstd[r] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)K), eps)));
+        const float var = __fdiv_rn(__fadd_rn(part[rl][0], part[rl][1]), (float)K);
+        rstd[r] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
     }
 }
 
@@ -874,7 +922,7 @@ cudaError_t launch_layernorm_quantize(const QuantArgs& a, const float* gamma, co
                                       float* mu, float* rstd, cudaStream_t st, int sms)
 {
     if (a.rows == 0 || a.cols == 0) return cudaSuccess;
-    k_ln_stats<<<(unsigned)((a.rows + 7) / 8), 256, 0, st>>>(static_cast<const uint16_t*>(a.x), a.rows, a.cols, eps, mu, rstd);
+    k_ln_stats<<<(unsigned)((a.rows + LN_ROWS - 1) / LN_ROWS), 256, 0, st>>>(static_cast<const uint16_t*>(a.x), a.rows, a.cols, eps, mu, rstd);
     CUtensorMap tm;
     if (!encode_tmap_2d(&tm, 1, a.x, (uint64_t)a.cols, (uint64_t)a.rows, 64u, 128u)) return cudaErrorInvalidValue;
     const int64_t tiles = ((a.rows + 127) / 128) * ((a.cols + 127) / 128);

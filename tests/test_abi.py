@@ -126,3 +126,16 @@ def test_binding_raises_when_library_missing(monkeypatch, tmp_path):
     monkeypatch.setattr(sq, "_lib", None)
     with pytest.raises(RuntimeError, match="no fallback"):
         sq.lib()
+
+
+def test_layernorm_validation(L):
+    """gamma, beta, mean and rstd are read as 128-bit vectors: 16-byte
+    alignment is required; M, K must be multiples of 16."""
+    P, c = ctypes.c_void_p, ctypes
+    f = P(4096)
+    ln = L.fp8_layernorm_quantize
+    args = lambda gamma, M=32, K=64: (f, gamma, f, c.c_float(1e-5), M, K, sq.E4M3, f, 16, f, f, f, f, None)
+    assert ln(*args(P(4096 + 4))) == sq.ERR_MISALIGNED
+    assert b"16-byte" in L.fp8_last_error()
+    assert ln(*args(f, M=24)) == sq.ERR_UNSUPPORTED
+    assert ln(*args(None)) == sq.ERR_INVALID_ARG
