@@ -152,7 +152,8 @@ FP8SQ_API int fp8_update_scale(float* states, int n_states, int history_len, con
  *   gran, delayed_state:
  *     TENSOR + delayed_state != NULL: delayed scaling.  m = state[H]; the
  *       tensor's amax is max-combined into state[0] (atomic, so several
- *       tensors may share a role).  scales_out is ignored.
+ *       tensors may share a role).  scales_out, if not NULL (1 float),
+ *       receives s = state[H + 1], the dequantisation scale of this cast.
  *     TENSOR + delayed_state == NULL: current scaling, two passes (amax,
  *       then cast).  amax_out (1 float) and scales_out (1 float, receives
  *       s = amax/fmax) are REQUIRED.  m = fmax/amax (amax 0 or non-finite:

@@ -439,11 +439,8 @@ FP8SQ_API int fp8_linear_fwd(const void* x, const void* w, int64_t M, int64_t N,
         qa.state = w_state;
         qa.scales = &scal[1]; qa.amax = delayed ? nullptr : &scal[4];
         if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: quantize w"))) return r;
-        if (delayed) {
-            // keep the dequantisation steps used now for the backward pass
-            if ((r = cuda_status(cudaMemcpyAsync(&scal[0], x_state + H + 1, sizeof(float), cudaMemcpyDeviceToDevice, st), "fp8_linear_fwd: copy s_x"))) return r;
-            if ((r = cuda_status(cudaMemcpyAsync(&scal[1], w_state + H + 1, sizeof(float), cudaMemcpyDeviceToDevice, st), "fp8_linear_fwd: copy s_w"))) return r;
-        }
+        // (delayed: each cast writes the dequantisation scale it used into
+        // scal[], kept for the backward pass)
         g.mode = 0;
         g.a_scale = &scal[0];
         g.b_scale = &scal[1];
@@ -520,9 +517,6 @@ FP8SQ_API int fp8_linear_bwd(const void* dy, int64_t M, int64_t N, int64_t K, in
         qa.state = dy_state; qa.history_len = history_len;
         qa.scales = &scal[2]; qa.amax = dy_state ? nullptr : &scal[5];
         if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_bwd: quantize dy"))) return r;
-        if (dy_state &&
-            (r = cuda_status(cudaMemcpyAsync(&scal[2], dy_state + history_len + 1, sizeof(float), cudaMemcpyDeviceToDevice, st), "fp8_linear_bwd: copy s_dy")))
-            return r;
         dg.mode = wg.mode = 0;
         dg.a_scale = &scal[2]; dg.b_scale = &scal[1];
         wg.a_scale = &scal[2]; wg.b_scale = &scal[0];
@@ -605,13 +599,13 @@ FP8SQ_API int fp8_layernorm_linear_fwd(const void* x, const float* gamma, const 
     fp8sq::QuantArgs qa;
     qa.x = x; qa.x_dtype = fp8sq::kBF16; qa.rows = M; qa.cols = K; qa.format = fp8sq::kE4M3;
     qa.gran = fp8sq::kTensor; qa.state = x_state; qa.history_len = H; qa.q = ws + L.qx; qa.qT = ws + L.qxT;
+    qa.scales = &scal[0];       // receives the dequantisation scale the cast used
     if ((r = cuda_status(fp8sq::launch_layernorm_quantize(qa, gamma, beta, eps, mu_out, rstd_out, st, sms),
                          "fp8_layernorm_linear_fwd: layernorm cast")))
         return r;
     qa.x = w; qa.rows = N; qa.cols = K; qa.state = w_state; qa.q = ws + L.qw; qa.qT = ws + L.qwT;
+    qa.scales = &scal[1];
     if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_layernorm_linear_fwd: quantize w"))) return r;
-    if ((r = cuda_status(cudaMemcpyAsync(&scal[0], x_state + H + 1, sizeof(float), cudaMemcpyDeviceToDevice, st), "copy s_x"))) return r;
-    if ((r = cuda_status(cudaMemcpyAsync(&scal[1], w_state + H + 1, sizeof(float), cudaMemcpyDeviceToDevice, st), "copy s_w"))) return r;
     fp8sq::GemmArgs g;
     g.mode = 0; g.M = M; g.N = N; g.K = K; g.bias = bias; g.D = y; g.d_dtype = y_dtype;
     g.A = ws + L.qx; g.B = ws + L.qw; g.a_scale = &scal[0]; g.b_scale = &scal[1];

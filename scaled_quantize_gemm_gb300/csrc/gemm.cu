@@ -289,6 +289,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     k_gemm_tensor_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        EpiParams p, uint32_t idesc, TileSched sched, const __grid_constant__ CUtensorMap tmD)
 {
+    pdl_enter();
     constexpr int BN = kPairBN, BH = BN / 2, STAGES = kPairStages;
     using L = PairSmem;
     extern __shared__ uint8_t smem_raw[];
@@ -513,6 +514,7 @@ __global__ void __launch_bounds__(320, 1)
     k_gemm_promote(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    EpiParams p, uint32_t idesc, TileSched sched)
 {
+    pdl_enter();
     constexpr int NB = 512 / BN;             // partial buffers
     constexpr int EPI = 8;
     constexpr int COLS = BN / 2;             // columns per epilogue warp
@@ -722,7 +724,7 @@ static cudaError_t launch_promote(const GemmArgs& g, const EpiParams& p, cudaStr
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int grid = tiles < sms ? tiles : sms;
-    kern<<<grid, 320, smem, st>>>(ta, tb, p, idesc, sched);
+    launch_k(kern, grid, 320, smem, st, ta, tb, p, idesc, sched);
     return cudaGetLastError();
 }
 
@@ -777,6 +779,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
     k_gemm_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, EpiParams p,
               uint32_t idesc, TileSched sched, MxParams mx, const __grid_constant__ CUtensorMap tmD)
 {
+    pdl_enter();
     static_assert(EPI <= 8, "staging area holds 8 warps");
     using L = MxLayout<BN, STAGES, NACC>;
     extern __shared__ uint8_t smem_raw[];
@@ -945,6 +948,7 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
 // failure path be exercised without faulting or hanging the GPU.
 __global__ void k_selftest_wait(uint64_t limit_ns, int* waited_out)
 {
+    pdl_enter();
     __shared__ uint64_t bar;
     if (threadIdx.x == 0) {
         mbar_init(&bar, 1);
@@ -956,7 +960,7 @@ __global__ void k_selftest_wait(uint64_t limit_ns, int* waited_out)
 
 cudaError_t launch_selftest_wait(uint64_t limit_ns, int* waited_out, cudaStream_t st)
 {
-    k_selftest_wait<<<1, 32, 0, st>>>(limit_ns, waited_out);
+    launch_k(k_selftest_wait, 1, 32, 0, st, limit_ns, waited_out);
     return cudaGetLastError();
 }
 
@@ -964,6 +968,7 @@ cudaError_t launch_selftest_wait(uint64_t limit_ns, int* waited_out, cudaStream_
 template <bool OUT_BF16>
 __global__ void k_fill_bias(void* D, int64_t M, int64_t N, const float* bias)
 {
+    pdl_enter();
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= M * N) return;
     float v = bias ? bias[i % N] : 0.0f;
@@ -1091,8 +1096,8 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
     const bool bf16 = g.d_dtype == kBF16;
     if (g.K == 0) {
         int64_t n = g.M * g.N;
-        if (bf16) k_fill_bias<true><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(g.D, g.M, g.N, g.bias);
-        else k_fill_bias<false><<<(unsigned)((n + 255) / 256), 256, 0, st>>>(g.D, g.M, g.N, g.bias);
+        if (bf16) launch_k(k_fill_bias<true>, (unsigned)((n + 255) / 256), 256, 0, st, g.D, g.M, g.N, g.bias);
+        else launch_k(k_fill_bias<false>, (unsigned)((n + 255) / 256), 256, 0, st, g.D, g.M, g.N, g.bias);
         return cudaGetLastError();
     }
     EpiParams p;
@@ -1132,7 +1137,7 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
             return cudaErrorNotSupported;
         }
         const int grid = 2 * (tiles < clusters ? tiles : clusters);
-        kern<<<grid, 192, smem, st>>>(ta, tb, p, idesc, sched, td);
+        launch_k(kern, grid, 192, smem, st, ta, tb, p, idesc, sched, td);
         return cudaGetLastError();
     }
     if (g.mode == 1) return launch_promote<1>(g, p, st, sms, why);
@@ -1161,7 +1166,7 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
             return cudaErrorInvalidValue;
         }
         const int grid = tiles < sms ? tiles : sms;
-        kern<<<grid, 64 + 32 * EPI, L::BYTES, st>>>(ta, tb, p, idesc, sched, mx, td);
+        launch_k(kern, grid, 64 + 32 * EPI, L::BYTES, st, ta, tb, p, idesc, sched, mx, td);
         return cudaGetLastError();
     }
     *why = "GEMM mode not built";

@@ -13,6 +13,19 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ------------------------------------------------------------------ launch order
+// Programmatic dependent launch.  Every kernel of this library starts with
+// pdl_enter(): it lets the next kernel on the stream be scheduled now (its
+// launch overlaps this kernel's run) and then waits until every kernel this
+// one depends on has completed with its memory operations visible, so the
+// kernel's reads and writes keep plain stream order.  Both instructions are
+// no-ops for a launch without the programmatic-serialisation attribute.
+__device__ __forceinline__ void pdl_enter()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ FP8 cast
 // cvt.rn.satfinite.{e4m3,e5m2}x2.f32 d, a, b: a goes to the upper byte.
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi)
@@ -336,6 +349,25 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr)
     d |= (uint64_t)1 << 46;
     d |= (uint64_t)2 << 61;
     return d;
+}
+
+// Launch with programmatic stream serialisation allowed (see pdl_enter).
+// Errors are also left for cudaGetLastError, like a <<<>>> launch.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
 }
 
 }  // namespace fp8sq

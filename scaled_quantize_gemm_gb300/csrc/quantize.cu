@@ -217,6 +217,7 @@ template <int DT>
 __global__ void __launch_bounds__(kFlatThreads) k_amax_tensor(const void* __restrict__ x, int64_t n,
                                                               float* __restrict__ amax_out)
 {
+    pdl_enter();
     __shared__ uint32_t red[kFlatThreads / 32];
     const int64_t nch = n / 8;
     uint32_t mx = 0;
@@ -252,11 +253,15 @@ __global__ void __launch_bounds__(kFlatThreads) k_cast_tensor(const void* __rest
                                                               const float* amax_in, float* s_out,
                                                               float* amax_out, unsigned long long* sat)
 {
+    pdl_enter();
     __shared__ uint32_t red[kFlatThreads / 32];
     float m, s;
     if (DELAYED) {
         m = state[H];
         s = 0.0f;
+        // the dequantisation scale this cast uses (the state's s is updated
+        // only at the end of the step)
+        if (blockIdx.x == 0 && threadIdx.x == 0 && s_out) *s_out = state[H + 1];
     } else {
         current_scale<FMT>(__float_as_uint(*amax_in), m, s);
         if (blockIdx.x == 0 && threadIdx.x == 0 && s_out) *s_out = s;
@@ -344,6 +349,7 @@ __global__ void __launch_bounds__(256) k_cast_tensor_T(const void* __restrict__ 
                                                        float* s_out, float* amax_out,
                                                        unsigned long long* sat)
 {
+    pdl_enter();
     __shared__ uint32_t red[8];
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
     const int64_t c0 = (int64_t)blockIdx.x * 128 + ((w & 3) * 4 + (l & 3)) * 8;
@@ -352,6 +358,7 @@ __global__ void __launch_bounds__(256) k_cast_tensor_T(const void* __restrict__ 
     if (DELAYED) {
         m = state[H];
         s = 0.0f;
+        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && s_out) *s_out = state[H + 1];
     } else {
         current_scale<FMT>(__float_as_uint(*amax_in), m, s);
         if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && s_out) *s_out = s;
@@ -438,6 +445,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
                  uint8_t* __restrict__ qT, float* state, int H, const float* amax_in, float* s_out, float* amax_out,
                  unsigned long long* sat, LnParams ln = LnParams())
 {
+    pdl_enter();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTStages * kTTile);
@@ -498,6 +506,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
         if (DELAYED) {
             m = state[H];
             s = 0.0f;
+            if (blockIdx.x == 0 && threadIdx.x == 0 && s_out) *s_out = state[H + 1];
         } else {
             current_scale<FMT>(__float_as_uint(*amax_in), m, s);
             if (blockIdx.x == 0 && threadIdx.x == 0 && s_out) *s_out = s;
@@ -626,6 +635,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
     k_quant_col_tma(const __grid_constant__ CUtensorMap tmX, int64_t R, int64_t C, uint8_t* __restrict__ q,
                     uint8_t* __restrict__ qT, void* scales, unsigned long long* sat)
 {
+    pdl_enter();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTStages * kTTile);
@@ -844,6 +854,7 @@ __device__ __forceinline__ float warp_sum(float v)
 __global__ void __launch_bounds__(256, 3) k_ln_stats(const uint16_t* __restrict__ x, int64_t R, int64_t K, float eps,
                                                      float* __restrict__ mu, float* __restrict__ rstd)
 {
+    pdl_enter();
     __shared__ float part[LN_ROWS][2];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rl = warp >> 1, half = warp & 1;
@@ -922,7 +933,7 @@ cudaError_t launch_layernorm_quantize(const QuantArgs& a, const float* gamma, co
                                       float* mu, float* rstd, cudaStream_t st, int sms)
 {
     if (a.rows == 0 || a.cols == 0) return cudaSuccess;
-    k_ln_stats<<<(unsigned)((a.rows + LN_ROWS - 1) / LN_ROWS), 256, 0, st>>>(static_cast<const uint16_t*>(a.x), a.rows, a.cols, eps, mu, rstd);
+    launch_k(k_ln_stats, (unsigned)((a.rows + LN_ROWS - 1) / LN_ROWS), 256, 0, st, static_cast<const uint16_t*>(a.x), a.rows, a.cols, eps, mu, rstd);
     CUtensorMap tm;
     if (!encode_tmap_2d(&tm, 1, a.x, (uint64_t)a.cols, (uint64_t)a.rows, 64u, 128u)) return cudaErrorInvalidValue;
     const int64_t tiles = ((a.rows + 127) / 128) * ((a.cols + 127) / 128);
@@ -935,7 +946,8 @@ cudaError_t launch_layernorm_quantize(const QuantArgs& a, const float* gamma, co
     auto kern = a.format == kE4M3 ? k_cast_T_tma<kE4M3, true, true> : k_cast_T_tma<kE5M2, true, true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kTThreads, kTSmem, st>>>(tm, a.rows, a.cols, a.q, a.qT, a.state, a.history_len, nullptr, nullptr,
+    launch_k(kern, grid, kTThreads, kTSmem, st, tm, a.rows, a.cols, a.q, a.qT, a.state, a.history_len, nullptr,
+             static_cast<float*>(a.scales),
                                           a.amax, a.sat, ln);
     return cudaGetLastError();
 }
@@ -969,6 +981,7 @@ __global__ void __launch_bounds__(kFlatThreads) k_quant_rowunits(const void* __r
                                                                  float* amax_out, unsigned long long* sat,
                                                                  int64_t cols = 0)
 {
+    pdl_enter();
     constexpr int TPU = UNIT / 16;  // lanes per unit
     const int64_t ng = n / 16;      // 16-element groups
     uint32_t nsat = 0;
@@ -1053,6 +1066,7 @@ __global__ void __launch_bounds__(256) k_quant_block128(const void* __restrict__
                                                         uint8_t* __restrict__ qT = nullptr, float* sT = nullptr,
                                                         uint8_t* e_tiled = nullptr)
 {
+    pdl_enter();
     __shared__ uint32_t red[8];
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
     const int64_t c0 = (int64_t)blockIdx.x * 128 + ((w & 3) * 4 + (l & 3)) * 8;
@@ -1102,6 +1116,7 @@ __global__ void __launch_bounds__(256) k_quant_block128(const void* __restrict__
 // ================================================================== state
 __global__ void k_scale_init(float* states, int n, int H)
 {
+    pdl_enter();
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     int64_t total = (int64_t)n * (H + 2);
     if (i < total) {
@@ -1116,6 +1131,7 @@ struct FormatList {
 
 __global__ void k_update_scale(float* states, int n, int H, FormatList fl, int algo)
 {
+    pdl_enter();
     int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     float* st = states + (int64_t)i * (H + 2);
@@ -1149,16 +1165,17 @@ static cudaError_t amax_dt(const QuantArgs& a, cudaStream_t st, int sms)
     switch (a.gran) {
     case kTensor:
         if (cudaMemsetAsync(a.amax, 0, sizeof(float), st) != cudaSuccess) return cudaGetLastError();
-        if (n > 0) k_amax_tensor<DT><<<flat_grid(n / 8, sms), kFlatThreads, 0, st>>>(a.x, n, a.amax);
+        if (n > 0) launch_k(k_amax_tensor<DT>, flat_grid(n / 8, sms), kFlatThreads, 0, st, a.x, n, a.amax);
         break;
     case kTile:
-        if (n > 0) k_quant_rowunits<DT, kE4M3, 128, false><<<flat_grid(n / 16, sms), kFlatThreads, 0, st>>>(a.x, n, nullptr, nullptr, a.amax, nullptr);
+        if (n > 0) launch_k(k_quant_rowunits<DT, kE4M3, 128, false>, flat_grid(n / 16, sms), kFlatThreads, 0, st, a.x, n, nullptr, nullptr, a.amax, nullptr, (int64_t)0);
         break;
     case kMX:
-        if (n > 0) k_quant_rowunits<DT, kE4M3, 32, false><<<flat_grid(n / 16, sms), kFlatThreads, 0, st>>>(a.x, n, nullptr, nullptr, a.amax, nullptr);
+        if (n > 0) launch_k(k_quant_rowunits<DT, kE4M3, 32, false>, flat_grid(n / 16, sms), kFlatThreads, 0, st, a.x, n, nullptr, nullptr, a.amax, nullptr, (int64_t)0);
         break;
     case kBlock:
-        if (n > 0) k_quant_block128<DT, kE4M3, false><<<dim3((unsigned)(a.cols / 128), (unsigned)(a.rows / 128)), 256, 0, st>>>(a.x, a.rows, a.cols, nullptr, nullptr, a.amax, nullptr);
+        if (n > 0) launch_k(k_quant_block128<DT, kE4M3, false>, dim3((unsigned)(a.cols / 128), (unsigned)(a.rows / 128)), 256, 0, st, a.x, a.rows, a.cols, nullptr, nullptr, a.amax, nullptr,
+                            nullptr, nullptr, nullptr);
         break;
     }
     return cudaGetLastError();
@@ -1195,51 +1212,54 @@ static cudaError_t quant_dt_fmt(const QuantArgs& a, cudaStream_t st, int sms)
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
             if (e != cudaSuccess) return e;
             if (delayed)
-                kern<<<grid, kTThreads, kTSmem, st>>>(tm, a.rows, a.cols, a.q, a.qT, a.state, H, nullptr, nullptr, a.amax, a.sat,
+                launch_k(kern, grid, kTThreads, kTSmem, st, tm, a.rows, a.cols, a.q, a.qT, a.state, H, nullptr, s_out, a.amax, a.sat,
                                                       LnParams());
             else
-                kern<<<grid, kTThreads, kTSmem, st>>>(tm, a.rows, a.cols, a.q, a.qT, nullptr, 0, a.amax, s_out, nullptr, a.sat,
+                launch_k(kern, grid, kTThreads, kTSmem, st, tm, a.rows, a.cols, a.q, a.qT, nullptr, 0, a.amax, s_out, nullptr, a.sat,
                                                       LnParams());
             return cudaGetLastError();
         }
         if (a.qT) {
             if (n == 0) {
-                if (!delayed) k_cast_tensor<DT, FMT, false><<<1, kFlatThreads, 0, st>>>(a.x, 0, a.q, nullptr, 0, a.amax, s_out, nullptr, nullptr);
+                if (!delayed) launch_k(k_cast_tensor<DT, FMT, false>, 1, kFlatThreads, 0, st, a.x, 0, a.q, nullptr, 0, a.amax, s_out, nullptr, nullptr);
+                else if (s_out) launch_k(k_cast_tensor<DT, FMT, true>, 1, kFlatThreads, 0, st, a.x, 0, a.q, a.state, H, nullptr, s_out, a.amax, nullptr);
                 return cudaGetLastError();
             }
             dim3 grid((unsigned)((a.cols + 127) / 128), (unsigned)((a.rows + 127) / 128));
             if (delayed)
-                k_cast_tensor_T<DT, FMT, true><<<grid, 256, 0, st>>>(a.x, a.rows, a.cols, a.q, a.qT, a.state, H, nullptr, nullptr, a.amax, a.sat);
+                launch_k(k_cast_tensor_T<DT, FMT, true>, grid, 256, 0, st, a.x, a.rows, a.cols, a.q, a.qT, a.state, H, nullptr, s_out, a.amax, a.sat);
             else
-                k_cast_tensor_T<DT, FMT, false><<<grid, 256, 0, st>>>(a.x, a.rows, a.cols, a.q, a.qT, nullptr, 0, a.amax, s_out, nullptr, a.sat);
+                launch_k(k_cast_tensor_T<DT, FMT, false>, grid, 256, 0, st, a.x, a.rows, a.cols, a.q, a.qT, nullptr, 0, a.amax, s_out, nullptr, a.sat);
         } else {
             int g = flat_grid(n / 8, sms);
             if (delayed)
-                k_cast_tensor<DT, FMT, true><<<g, kFlatThreads, 0, st>>>(a.x, n, a.q, a.state, H, nullptr, nullptr, a.amax, a.sat);
+                launch_k(k_cast_tensor<DT, FMT, true>, g, kFlatThreads, 0, st, a.x, n, a.q, a.state, H, nullptr, s_out, a.amax, a.sat);
             else
-                k_cast_tensor<DT, FMT, false><<<g, kFlatThreads, 0, st>>>(a.x, n, a.q, nullptr, 0, a.amax, s_out, nullptr, a.sat);
+                launch_k(k_cast_tensor<DT, FMT, false>, g, kFlatThreads, 0, st, a.x, n, a.q, nullptr, 0, a.amax, s_out, nullptr, a.sat);
         }
         return cudaGetLastError();
     }
     if (n == 0) return cudaSuccess;
     switch (a.gran) {
     case kTile:
-        k_quant_rowunits<DT, FMT, 128, true><<<flat_grid(n / 16, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat);
+        launch_k(k_quant_rowunits<DT, FMT, 128, true>, flat_grid(n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat,
+                 (int64_t)0);
         break;
     case kMX:
-        k_quant_rowunits<DT, FMT, 32, true><<<flat_grid(n / 16, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat);
+        launch_k(k_quant_rowunits<DT, FMT, 32, true>, flat_grid(n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat,
+                 (int64_t)0);
         break;
     case kMXTiled:
-        k_quant_rowunits<DT, FMT, 32, true, true><<<flat_grid(n / 16, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
+        launch_k(k_quant_rowunits<DT, FMT, 32, true, true>, flat_grid(n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
         break;
     case kTilePow2:
-        k_quant_rowunits<DT, FMT, 128, true, true, 1><<<flat_grid(n / 16, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
+        launch_k(k_quant_rowunits<DT, FMT, 128, true, true, 1>, flat_grid(n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
         break;
     case kMXFloor:
-        k_quant_rowunits<DT, FMT, 32, true, true, 2><<<flat_grid(n / 16, sms), kFlatThreads, 0, st>>>(a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
+        launch_k(k_quant_rowunits<DT, FMT, 32, true, true, 2>, flat_grid(n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
         break;
     case kBlockPow2:
-        k_quant_block128<DT, FMT, true, true><<<dim3((unsigned)(a.cols / 128), (unsigned)(a.rows / 128)), 256, 0, st>>>(a.x, a.rows, a.cols, a.q, nullptr, a.amax, a.sat, nullptr, nullptr, static_cast<uint8_t*>(a.scales));
+        launch_k(k_quant_block128<DT, FMT, true, true>, dim3((unsigned)(a.cols / 128), (unsigned)(a.rows / 128)), 256, 0, st, a.x, a.rows, a.cols, a.q, nullptr, a.amax, a.sat, nullptr, nullptr, static_cast<uint8_t*>(a.scales));
         break;
     case kTileCol:
     case kMXCol: {
@@ -1250,11 +1270,12 @@ static cudaError_t quant_dt_fmt(const QuantArgs& a, cudaStream_t st, int sms)
         auto kern = a.gran == kTileCol ? k_quant_col_tma<FMT, 128> : k_quant_col_tma<FMT, 32>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
         if (e != cudaSuccess) return e;
-        kern<<<grid, kTThreads, kTSmem, st>>>(tm, a.rows, a.cols, a.q, a.qT, a.scales, a.sat);
+        launch_k(kern, grid, kTThreads, kTSmem, st, tm, a.rows, a.cols, a.q, a.qT, a.scales, a.sat);
         break;
     }
     case kBlock:
-        k_quant_block128<DT, FMT, true><<<dim3((unsigned)(a.cols / 128), (unsigned)(a.rows / 128)), 256, 0, st>>>(a.x, a.rows, a.cols, a.q, static_cast<float*>(a.scales), a.amax, a.sat, a.qT, a.scalesT);
+        launch_k(k_quant_block128<DT, FMT, true>, dim3((unsigned)(a.cols / 128), (unsigned)(a.rows / 128)), 256, 0, st, a.x, a.rows, a.cols, a.q, static_cast<float*>(a.scales), a.amax, a.sat, a.qT, a.scalesT,
+                 nullptr);
         break;
     }
     return cudaGetLastError();
@@ -1270,7 +1291,7 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st, int sms)
 cudaError_t launch_scale_init(float* states, int n, int H, cudaStream_t st)
 {
     int64_t total = (int64_t)n * (H + 2);
-    if (total > 0) k_scale_init<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(states, n, H);
+    if (total > 0) launch_k(k_scale_init, (unsigned)((total + 255) / 256), 256, 0, st, states, n, H);
     return cudaGetLastError();
 }
 
@@ -1278,7 +1299,7 @@ cudaError_t launch_update_scale(float* states, int n, int H, const int* formats,
 {
     FormatList fl;
     for (int i = 0; i < n; ++i) fl.f[i] = (uint8_t)formats[i];
-    if (n > 0) k_update_scale<<<(n + 127) / 128, 128, 0, st>>>(states, n, H, fl, algo);
+    if (n > 0) launch_k(k_update_scale, (n + 127) / 128, 128, 0, st, states, n, H, fl, algo);
     return cudaGetLastError();
 }
 
