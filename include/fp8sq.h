@@ -339,7 +339,11 @@ FP8SQ_API int fp8_linear_fwd_noalloc(const void* x, const void* w, int64_t M, in
  *   cleared.
  * fp8_last_error: message for the calling thread's last non-zero status
  *   (static thread-local storage; never NULL).
- * fp8_abi_version: 2.
+ * fp8_abi_version: 3.  Changes from 2: fp8_selftest_wait_timeout added;
+ *   the LayerNorm entry points need 16-byte aligned gamma, beta, mu, rstd;
+ *   a delayed per-tensor fp8_quantize writes s to a non-NULL scales_out.
+ *   Every kernel is launched with programmatic stream serialisation (the
+ *   next kernel's launch overlaps; memory order on the stream is kept).
  */
 FP8SQ_API int fp8_device_status(int clear);
 FP8SQ_API int fp8_selftest_wait_timeout(int limit_us, int* waited_out, void* stream);

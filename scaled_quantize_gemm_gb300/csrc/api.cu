@@ -148,7 +148,7 @@ int api_check_device(int* sms) { return check_device(sms); }
 
 extern "C" {
 
-FP8SQ_API int fp8_abi_version(void) { return 2; }
+FP8SQ_API int fp8_abi_version(void) { return 3; }
 
 FP8SQ_API const char* fp8_last_error(void) { return g_msg; }
 
