@@ -50,20 +50,20 @@ SAMPLE_TOKENS = 128      # CPU oracle sample: the same step at 128 tokens
 # one ncu capture of each reported kernel, valid only while the kernel's own
 # source text (and the PTX wrappers) still hash to the recorded digest; a
 # changed kernel reports null until it is captured again.  Captured shapes:
-# k_gemm_tensor_pair on the 16384 x 14336 x 4096 forward GEMM, k_cast_T_tma on the
+# k_gemm_tensor_pair on the 16384 x 14336 x 4096 forward GEMM, k_cast_tensor_T on the
 # 16384 x 14336 cast (the captures are summarised under profiles/).
 CSRC = os.path.join(ROOT, "scaled_quantize_gemm_gb300", "csrc")
 KERNEL_SOURCES = {   # file, [(start marker or None = file start, end marker)]: helpers + kernel + launch config
     "k_gemm_tensor_pair": ("gemm.cu", [(None, "// ================================================================== mode 1"),
                                        ("    if (g.mode == 0) {", "    if (g.mode == 1)")]),
-    "k_cast_T_tma": ("quantize.cu", [(None, "// ================================================================== per-tensor\n"),
-                                     ("// ================================================================== per-tensor, TMA-fed",
-                                      "// AND of `v` over the 256 consumer threads"),
-                                     ("        if (a.qT && DT == kBF16 && n > 0) {", "        if (a.qT) {")]),
+    "k_cast_tensor_T": ("quantize.cu", [(None, "// ================================================================== per-tensor\n"),
+                                        ("// Row-wise LayerNorm folded into the cast",
+                                         "// ================================================================== column units"),
+                                        ("        if (a.qT) {", "        } else {")]),
 }
 TRAFFIC = {
-    "k_gemm_tensor_pair": {"sha": "820f53a0c8a7f0e1", "bytes": 973921024},
-    "k_cast_T_tma": {"sha": "59743cdc1cdd4f53", "bytes": 889936640},
+    "k_gemm_tensor_pair": {"sha": "03a352c1142b66c8", "bytes": 973217024},
+    "k_cast_tensor_T": {"sha": "10634066b786eb60", "bytes": 891757312},
 }
 
 
@@ -446,9 +446,9 @@ def run_ours(args, ws, rank, local):
                          "traffic_shape": "16384 x 14336 x 4096 forward GEMM (one ncu capture)",
                          "peak_source": f"2 x bf16_tflops {peak_src} (dense FP8 = 2 x dense BF16)",
                          "flops_per_launch": gemm_flops_launch, "launch_ms": round(gemm_ms, 4)},
-            "roofline_quantize": {"bound": "hbm", "kernel": "k_cast_T_tma (16384 x 14336 casts)",
+            "roofline_quantize": {"bound": "hbm", "kernel": "k_cast_tensor_T (16384 x 14336 casts)",
                                   "achieved": round(big_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                                  "frac": round(big_gbs / hbm_peak, 4), "traffic": kernel_traffic("k_cast_T_tma"),
+                                  "frac": round(big_gbs / hbm_peak, 4), "traffic": kernel_traffic("k_cast_tensor_T"),
                                   "peak_source": f"hbm_gbs {peak_src}",
                                   "bytes_per_launch": big_bytes},
             "quantize": {"GB_per_s_all_casts": round(quant_gbs, 1), "ms_per_step": round(quant_ms_step, 4),
@@ -551,7 +551,7 @@ def kernel_case(case: str, launches: int):
     """A handful of launches of one kernel at the workload's size, for
     profiling a single launch: 'gemm' = the 16384 x 14336 x 4096 forward GEMM
     (k_gemm_tensor_pair), 'cast' = the 16384 x 14336 E5M2 cast with its transposed
-    copy (k_cast_T_tma), 'promote' = the 4096^3 1x128 x 128x128 GEMM
+    copy (k_cast_tensor_T), 'promote' = the 4096^3 1x128 x 128x128 GEMM
     (k_gemm_promote), 'mx' = the 8192^3 MX-32 GEMM (k_gemm_mx), 'fine' = the
     fine-grained casts (1x128, 128x128, MX-32 tiled, 128x1 columns), 'ln' =
     the LayerNorm-fused cast of a 16384 x 4096 activation."""
@@ -611,7 +611,7 @@ def kernel_case(case: str, launches: int):
             sq.fp8_quantize(dy, sq.E5M2, sq.TILE_128x1, None, qT=qdT, scales_out=sd)
     elif case == "ln":
         # LayerNorm fused into the delayed E4M3 cast with the transposed copy,
-        # 16384 x 4096 (k_ln_stats, then k_cast_T_tma in its LayerNorm mode)
+        # 16384 x 4096 (k_ln_stats, then k_cast_tensor_T in its LayerNorm mode)
         M, K = 16384, 4096
         xl = wl.normal((M, K), 2.0, 11, dev)
         gamma = torch.rand(K, generator=torch.Generator().manual_seed(12)).add_(0.5).to(dev)
@@ -782,6 +782,34 @@ def modes_table(reps: int = 10):
             med(lambda: sq.fp8_linear_fwd(x, w, yb, ws, gran=gran)), flops=2 * M * N * K)
         row(f"fp8_linear_bwd {name} current", "4096^3",
             med(lambda: sq.fp8_linear_bwd(dy, dx, dw, ws, K, gran=gran)), flops=4 * M * N * K)
+
+    # the fine-grained casts at a large size (16384 x 14336, the FFN's widest
+    # activation): throughput rather than launch latency
+    R, C = 16384, 14336
+    xb = wl.normal((R, C), 1.0, 21, dev)
+    qb_, qbT = torch.empty((R, C), **u8), torch.empty((C, R), **u8)
+    s_t = torch.empty(R * (C // 128), **f32)
+    s_b = torch.empty((R // 128) * (C // 128), **f32)
+    s_bT = torch.empty((R // 128) * (C // 128), **f32)
+    s_c = torch.empty((R // 128) * C, **f32)
+    e_m = torch.empty(R * C // 32, **u8)
+    big = f"{R}x{C}"
+    row("fp8_quantize TILE_1x128 E4M3", big,
+        med(lambda: sq.fp8_quantize(xb, sq.E4M3, sq.TILE_1x128, qb_, scales_out=s_t)),
+        nbytes=R * C * 3 + 4 * R * (C // 128))
+    row("fp8_quantize BLOCK_128x128 E4M3 with qT", big,
+        med(lambda: sq.fp8_quantize(xb, sq.E4M3, sq.BLOCK_128x128, qb_, qT=qbT, scales_out=s_b)),
+        nbytes=R * C * 4)
+    row("fp8_quantize TILE_128x1 (column tiles) E5M2, qT only", big,
+        med(lambda: sq.fp8_quantize(xb, sq.E5M2, sq.TILE_128x1, None, qT=qbT, scales_out=s_c)),
+        nbytes=R * C * 3 + 4 * (R // 128) * C)
+    row("fp8_quantize MX32_TILED E4M3", big,
+        med(lambda: sq.fp8_quantize(xb, sq.E4M3, sq.MX32_TILED, qb_, scales_out=e_m)),
+        nbytes=R * C * 3 + R * C // 32)
+    row("fp8_quantize MX32_COL_TILED (column blocks) E4M3, qT only", big,
+        med(lambda: sq.fp8_quantize(xb, sq.E4M3, sq.MX32_COL_TILED, None, qT=qbT, scales_out=e_m)),
+        nbytes=R * C * 3 + R * C // 32)
+    del xb, qb_, qbT, s_t, s_b, s_bT, s_c, e_m
 
     # LayerNorm fused into the delayed per-tensor cast (with the transposed
     # copy): x read twice (statistics, then the normalise-and-cast pass),

@@ -28,6 +28,8 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <mutex>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -39,6 +41,31 @@ __device__ int g_dev_error = 0;
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity)
 {
     return wait_bounded_err(bar, parity, &g_dev_error);
+}
+
+// Raises a kernel's dynamic shared-memory limit once per device.  Setting a
+// function attribute on every launch puts a driver call on the launch path
+// that held back back-to-back calls (a fine-grained backward took 279 us in
+// a loop of calls against 238 us replayed from a CUDA graph).
+static cudaError_t smem_attr_once(const void* kern, int bytes)
+{
+    static std::mutex mu;
+    static const void* done_kern[128];
+    static int done_dev[128];
+    static int n_done = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_done; ++i)
+        if (done_kern[i] == kern && done_dev[i] == dev) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && n_done < 128) {
+        done_kern[n_done] = kern;
+        done_dev[n_done] = dev;
+        ++n_done;
+    }
+    return e;
 }
 
 struct TileSched {
@@ -721,7 +748,7 @@ static cudaError_t launch_promote(const GemmArgs& g, const EpiParams& p, cudaStr
     idesc |= (uint32_t)(BM >> 4) << 24;
     const int smem = Smem<BN, ST, 512 / BN>::BYTES;
     auto kern = g.d_dtype == kBF16 ? k_gemm_promote<BN, ST, true, SM> : k_gemm_promote<BN, ST, false, SM>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     const int grid = tiles < sms ? tiles : sms;
     launch_k(kern, grid, 320, smem, st, ta, tb, p, idesc, sched);
@@ -1158,7 +1185,7 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
         // eight epilogue warps drain it in half the time of four
         constexpr int EPI = 8;
         auto kern = bf16 ? k_gemm_mx<BN, ST, NACC, true, EPI> : k_gemm_mx<BN, ST, NACC, false, EPI>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
+        cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(kern), L::BYTES);
         if (e != cudaSuccess) return e;
         CUtensorMap td;
         if (!make_tmap_out(&td, g.D, g.M, g.N, bf16)) {

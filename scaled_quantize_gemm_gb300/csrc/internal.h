@@ -63,9 +63,6 @@ cudaError_t launch_selftest_wait(uint64_t limit_ns, int* waited_out, cudaStream_
 bool encode_tmap_2d(CUtensorMap* m, int u16, const void* ptr, uint64_t inner, uint64_t rows, uint32_t box_inner,
                     uint32_t box_rows);
 
-// quantize.cu
-int read_device_error_quant(int clear);   // 0 or the cast kernels' device error word
-
 // api.cu: the calling thread's error message and the sm_103 device check
 int api_fail(int code, const char* fmt, ...);
 int api_check_device(int* sms);

@@ -337,17 +337,31 @@ __device__ __forceinline__ void transpose8x8(const uint2 (&in)[8], uint2 (&out)[
     }
 }
 
-// Per-tensor cast with a transposed copy: one 128x128 tile per CTA, each
-// thread an 8x8 sub-block (8 rows x one 128-bit load).  Warp layout: 4
-// column groups x 8 row groups, so every load instruction reads 64-byte
-// row segments and every code store writes whole 32-byte sectors, in both q
-// and qT.  Requires rows % 8 == 0, cols % 8 == 0.
-template <int DT, int FMT, bool DELAYED>
+// Row-wise LayerNorm folded into the cast (LN = true): x is replaced by
+// y = (x - mu[r]) * rstd[r] * gamma[c] + beta[c] before the multiplier, the
+// amax is taken over y, and the bf16 LayerNorm output never leaves the SM.
+struct LnParams {
+    const float* mu = nullptr;
+    const float* rstd = nullptr;
+    const float* gamma = nullptr;
+    const float* beta = nullptr;
+};
+
+// Per-tensor cast with a transposed copy: one 128x128 tile per 256-thread
+// CTA, each thread an 8x8 sub-block (8 rows x one 128-bit load), all loads
+// in flight at once.  Warp layout: 4 column groups x 8 row groups, so every
+// load instruction reads 64-byte row segments and every code store writes
+// whole 32-byte sectors, in both q and qT.  Requires rows, cols % 8 == 0
+// (% 16 for the LayerNorm mode).  Three CTAs (24 warps) per SM keep enough
+// loads in flight: measured on the GB300 at 16384 x 14336 (delayed E5M2,
+// identical codes), 144.2 us = 6.5 TB/s against 168.2 us for a persistent
+// TMA-fed ring with 8 consumer warps per SM.
+template <int DT, int FMT, bool DELAYED, bool LN = false>
 __global__ void __launch_bounds__(256) k_cast_tensor_T(const void* __restrict__ x, int64_t R, int64_t C,
                                                        uint8_t* __restrict__ q, uint8_t* __restrict__ qT,
                                                        float* state, int H, const float* amax_in,
                                                        float* s_out, float* amax_out,
-                                                       unsigned long long* sat)
+                                                       unsigned long long* sat, LnParams ln)
 {
     pdl_enter();
     __shared__ uint32_t red[8];
@@ -358,25 +372,55 @@ __global__ void __launch_bounds__(256) k_cast_tensor_T(const void* __restrict__ 
     if (DELAYED) {
         m = state[H];
         s = 0.0f;
+        // the dequantisation scale this cast uses (the state's s is updated
+        // only at the end of the step)
         if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && s_out) *s_out = state[H + 1];
     } else {
         current_scale<FMT>(__float_as_uint(*amax_in), m, s);
         if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && s_out) *s_out = s;
     }
-    const bool ok = (r0 < R) && (c0 < C);
+    const bool ok = (r0 < R) && (c0 < C);    // rows, cols % 16 == 0: whole 8 x 8 groups
     Vec8<DT> v[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         if (ok) v[i].load(x, (r0 + i) * C + c0); else v[i].zero();
     }
+    float g[8], be[8], mu[8], rs[8];
+    if (LN) {
+        // this thread's 8 columns of gamma / beta and 8 rows of mean / rstd as
+        // 128-bit loads (16-byte aligned buffers)
+        const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        const float4* g4 = reinterpret_cast<const float4*>(ln.gamma + c0);
+        const float4* b4 = reinterpret_cast<const float4*>(ln.beta + c0);
+        const float4* m4 = reinterpret_cast<const float4*>(ln.mu + r0);
+        const float4* r4 = reinterpret_cast<const float4*>(ln.rstd + r0);
+        const float4 ga = ok ? __ldg(g4) : z4, gb = ok ? __ldg(g4 + 1) : z4;
+        const float4 ba = (ok && ln.beta) ? __ldg(b4) : z4, bb = (ok && ln.beta) ? __ldg(b4 + 1) : z4;
+        const float4 ma = ok ? __ldg(m4) : z4, mb = ok ? __ldg(m4 + 1) : z4;
+        const float4 ra = ok ? __ldg(r4) : z4, rb = ok ? __ldg(r4 + 1) : z4;
+        g[0] = ga.x; g[1] = ga.y; g[2] = ga.z; g[3] = ga.w; g[4] = gb.x; g[5] = gb.y; g[6] = gb.z; g[7] = gb.w;
+        be[0] = ba.x; be[1] = ba.y; be[2] = ba.z; be[3] = ba.w; be[4] = bb.x; be[5] = bb.y; be[6] = bb.z; be[7] = bb.w;
+        mu[0] = ma.x; mu[1] = ma.y; mu[2] = ma.z; mu[3] = ma.w; mu[4] = mb.x; mu[5] = mb.y; mu[6] = mb.z; mu[7] = mb.w;
+        rs[0] = ra.x; rs[1] = ra.y; rs[2] = ra.z; rs[3] = ra.w; rs[4] = rb.x; rs[5] = rb.y; rs[6] = rb.z; rs[7] = rb.w;
+    }
     uint32_t mx = 0, nsat = 0;
     uint2 rows[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const uint32_t ab = v[i].absmax_bits();
-        if (DELAYED) mx = max(mx, ab);
         float f[8];
         v[i].get(f);
+        uint32_t ab;
+        if (LN) {
+            ab = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                f[j] = __fmaf_rn(__fmul_rn(__fsub_rn(f[j], mu[i]), rs[i]), g[j], be[j]);
+                ab = max(ab, __float_as_uint(f[j]) & 0x7FFFFFFFu);
+            }
+        } else {
+            ab = v[i].absmax_bits();
+        }
+        if (DELAYED) mx = max(mx, ab);
         rows[i] = cast8<FMT>(f, m, ab, nsat);
     }
     if (ok) {
@@ -411,404 +455,116 @@ __device__ __forceinline__ int64_t mx_tiled_offset(int64_t r, int64_t t, int64_t
     return ((r >> 7) * (cols >> 7) + (t >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (t & 3);
 }
 
-// ================================================================== per-tensor, TMA-fed
-// The per-tensor cast with a transposed copy for bf16 inputs, as a persistent
-// pipeline: one CTA per SM; warp 8 streams 128x128 bf16 tiles into a
-// 6-stage shared-memory ring with TMA (two 64-column boxes per tile, 128-byte
-// swizzle, zero fill past the edges); warps 0..7 each take a 32-row x 64-column
-// quarter of a tile, eight rows x 8 columns per thread.  Lane (cg = lane % 8,
-// rg = lane / 8) reads 16-byte chunk cg of its rows, so the eight lanes of a
-// shared-memory phase hit eight different swizzled chunks (no bank
-// conflicts), and every code store (q rows, qT rows) covers whole 32-byte
-// sectors.  The amax is combined over the CTA's whole share of tiles and
-// reaches global memory with one atomic per CTA.
-__device__ int g_dev_error_q = 0;
-
-constexpr int kTStages = 6;
-constexpr int kTTile = 128 * 128 * 2;
-constexpr int kTThreads = 288;
-constexpr int kTSmem = kTStages * kTTile + 2 * kTStages * 8 + 1024;
-
-// Row-wise LayerNorm folded into the cast (LN = true): x is replaced by
-// y = (x - mu[r]) * rstd[r] * gamma[c] + beta[c] before the multiplier, the
-// amax is taken over y, and the bf16 LayerNorm output never leaves the SM.
-struct LnParams {
-    const float* mu = nullptr;
-    const float* rstd = nullptr;
-    const float* gamma = nullptr;
-    const float* beta = nullptr;
-};
-
-template <int FMT, bool DELAYED, bool LN = false>
-__global__ void __launch_bounds__(kTThreads, 1)
-    k_cast_T_tma(const __grid_constant__ CUtensorMap tmX, int64_t R, int64_t C, uint8_t* __restrict__ q,
-                 uint8_t* __restrict__ qT, float* state, int H, const float* amax_in, float* s_out, float* amax_out,
-                 unsigned long long* sat, LnParams ln = LnParams())
-{
-    pdl_enter();
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTStages * kTTile);
-    uint64_t* empty = full + kTStages;
-    __shared__ uint32_t red[8];
-    __shared__ int s_skip;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tiles_c = (int)((C + 127) / 128);
-    const int ntiles = tiles_c * (int)((R + 127) / 128);
-    if (threadIdx.x == 0) {
-        s_skip = *reinterpret_cast<volatile int*>(&g_dev_error_q);
-        for (int i = 0; i < kTStages; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 8);
-        }
-        fence_mbar_init();
-        prefetch_tmap(&tmX);
-    }
-    __syncthreads();
-    if (s_skip) return;
-    uint32_t mx = 0, nsat = 0;
-    if (warp == 8) {
-        if (lane == 0) {
-            int stage = 0, issued = 0;
-            uint32_t phase = 0;
-            bool aborted = false;
-            for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-                if (!wait_bounded_err(&empty[stage], phase ^ 1u, &g_dev_error_q)) {
-                    aborted = true;
-                    break;
-                }
-                const int c0 = (t % tiles_c) * 128, r0 = (t / tiles_c) * 128;
-                uint8_t* dst = smem + stage * kTTile;
-                mbar_arrive_expect_tx(&full[stage], kTTile);
-                tma_load_2d(dst, &tmX, c0, r0, &full[stage]);
-                tma_load_2d(dst + kTTile / 2, &tmX, c0 + 64, r0, &full[stage]);
-                ++issued;
-                if (++stage == kTStages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            }
-            if (aborted) {
-                int n = issued < kTStages ? issued : kTStages;
-                int st = stage;
-                uint32_t ph = phase;
-                for (int i = 0; i < n; ++i) {
-                    if (--st < 0) {
-                        st = kTStages - 1;
-                        ph ^= 1u;
-                    }
-                    wait_drain(&full[st], ph);
-                }
-            }
-        }
-    } else {
-        float m, s;
-        if (DELAYED) {
-            m = state[H];
-            s = 0.0f;
-            if (blockIdx.x == 0 && threadIdx.x == 0 && s_out) *s_out = state[H + 1];
-        } else {
-            current_scale<FMT>(__float_as_uint(*amax_in), m, s);
-            if (blockIdx.x == 0 && threadIdx.x == 0 && s_out) *s_out = s;
-        }
-        const int h = warp >> 2, cg = lane & 7;
-        const int rloc = (warp & 3) * 32 + (lane >> 3) * 8;
-        const int cloc = h * 64 + cg * 8;
-        int stage = 0;
-        uint32_t phase = 0;
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-            const bool ok = wait_bounded_err(&full[stage], phase, &g_dev_error_q);
-            if (!__all_sync(0xFFFFFFFFu, ok)) break;
-            const uint8_t* half = smem + stage * kTTile + h * (kTTile / 2);
-            Vec8<kBF16> v[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = rloc + i;
-                v[i].w = *reinterpret_cast<const uint4*>(half + r * 128 + ((cg ^ (r & 7)) << 4));
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stage]);
-            if (++stage == kTStages) {
-                stage = 0;
-                phase ^= 1u;
-            }
-            const int64_t r0 = (int64_t)(t / tiles_c) * 128 + rloc;
-            const int64_t c0 = (int64_t)(t % tiles_c) * 128 + cloc;
-            const bool inside = r0 < R && c0 < C;
-            uint2 rows[8];
-            uint32_t ns = 0;
-            if (LN) {
-                // this thread's 8 columns of gamma / beta and 8 rows of mean /
-                // rstd, as 128-bit loads (the buffers are 16-byte aligned and
-                // cols, rows are multiples of 8 inside the tensor)
-                float g[8], be[8], mu[8], rs[8];
-                const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                const float4* g4 = reinterpret_cast<const float4*>(ln.gamma + c0);
-                const float4* b4 = reinterpret_cast<const float4*>(ln.beta + c0);
-                const float4* m4 = reinterpret_cast<const float4*>(ln.mu + r0);
-                const float4* r4 = reinterpret_cast<const float4*>(ln.rstd + r0);
-                const float4 ga = inside ? __ldg(g4) : z4, gb = inside ? __ldg(g4 + 1) : z4;
-                const float4 ba = (inside && ln.beta) ? __ldg(b4) : z4, bb = (inside && ln.beta) ? __ldg(b4 + 1) : z4;
-                const float4 ma = inside ? __ldg(m4) : z4, mb = inside ? __ldg(m4 + 1) : z4;
-                const float4 ra = inside ? __ldg(r4) : z4, rb = inside ? __ldg(r4 + 1) : z4;
-                g[0] = ga.x; g[1] = ga.y; g[2] = ga.z; g[3] = ga.w; g[4] = gb.x; g[5] = gb.y; g[6] = gb.z; g[7] = gb.w;
-                be[0] = ba.x; be[1] = ba.y; be[2] = ba.z; be[3] = ba.w; be[4] = bb.x; be[5] = bb.y; be[6] = bb.z; be[7] = bb.w;
-                mu[0] = ma.x; mu[1] = ma.y; mu[2] = ma.z; mu[3] = ma.w; mu[4] = mb.x; mu[5] = mb.y; mu[6] = mb.z; mu[7] = mb.w;
-                rs[0] = ra.x; rs[1] = ra.y; rs[2] = ra.z; rs[3] = ra.w; rs[4] = rb.x; rs[5] = rb.y; rs[6] = rb.z; rs[7] = rb.w;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    float f[8];
-                    v[i].get(f);
-                    uint32_t ab = 0;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        f[j] = __fmaf_rn(__fmul_rn(__fsub_rn(f[j], mu[i]), rs[i]), g[j], be[j]);
-                        ab = max(ab, __float_as_uint(f[j]) & 0x7FFFFFFFu);
-                    }
-                    if (DELAYED && inside) mx = max(mx, ab);
-                    rows[i] = cast8<FMT>(f, m, ab, ns);
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t ab = v[i].absmax_bits();
-                    if (DELAYED) mx = max(mx, ab);
-                    float f[8];
-                    v[i].get(f);
-                    rows[i] = cast8<FMT>(f, m, ab, ns);
-                }
-            }
-            if (inside) {
-                nsat += ns;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(q + (r0 + i) * C + c0) = rows[i];
-                if (qT) {
-                    uint2 cols[8];
-                    transpose8x8(rows, cols);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) *reinterpret_cast<uint2*>(qT + (c0 + j) * R + r0) = cols[j];
-                }
-            }
-        }
-        if (sat) add_sat(sat, nsat);
-        if (DELAYED) {
-            mx = __reduce_max_sync(0xFFFFFFFFu, mx);
-            if (lane == 0) red[warp] = mx;
-        }
-    }
-    __syncthreads();
-    if (DELAYED && threadIdx.x == 0) {
-        uint32_t r = red[0];
-#pragma unroll
-        for (int i = 1; i < 8; ++i) r = max(r, red[i]);
-        atomic_max_bits(&state[0], r);
-        if (amax_out) atomic_max_bits(amax_out, r);
-    }
-}
-
-// AND of `v` over the 256 consumer threads (warps 0..7), at named barrier 1
-__device__ __forceinline__ bool consumers_all(bool v)
-{
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, 256, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v)
-        : "memory");
-    return r != 0;
-}
-
-// ================================================================== column units, TMA-fed
+// ================================================================== column units
 // Column tiles of 128 rows (UNIT = 128, scales f32 [R/128][C]) and column MX
 // blocks of 32 rows (UNIT = 32, E8M0 scales in the tiled layout of the
 // transposed matrix [C][R]): the operands of products that contract over
-// the rows of x.  Same ring and lane map as k_cast_T_tma; each thread's
-// column maxima (8 columns x its 8 rows) are reduced over the 4 lanes that
-// share its columns (a 32-row quarter) and, for 128-row tiles, over the 4
-// quarter warps through shared memory.  Writes the transposed codes qT and,
-// when q is given, the codes in x's layout.
+// the rows of x.  One 128 x 128 tile per 256-thread CTA with the lane map of
+// k_cast_tensor_T: thread (w, l) holds rows r0..r0+7 x columns c0..c0+7,
+// c0 = ((w & 3) * 4 + (l & 3)) * 8 and r0 = ((w >> 2) * 8 + (l >> 2)) * 8.
+// A column's 32 rows are four row groups of one warp (a shuffle over lanes
+// l ^ 4, l ^ 8); its 128 rows are the eight row groups of warps w and w + 4
+// (shuffles, then one exchange through shared memory), after which thread
+// c < 128 computes column c's scale once for the CTA and writes it.  Writes
+// the transposed codes qT and, when q is given, the codes in x's layout.
 template <int FMT, int UNIT>
-__global__ void __launch_bounds__(kTThreads, 1)
-    k_quant_col_tma(const __grid_constant__ CUtensorMap tmX, int64_t R, int64_t C, uint8_t* __restrict__ q,
-                    uint8_t* __restrict__ qT, void* scales, unsigned long long* sat)
+__global__ void __launch_bounds__(256) k_quant_col_block(const void* __restrict__ x, int64_t R, int64_t C,
+                                                         uint8_t* __restrict__ q, uint8_t* __restrict__ qT,
+                                                         void* scales, unsigned long long* sat)
 {
     pdl_enter();
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTStages * kTTile);
-    uint64_t* empty = full + kTStages;
-    __shared__ uint32_t colred[2][4][64];     // [half][quarter][column], 128-row tiles only
-    __shared__ __align__(16) float colm[2][64];           // column multipliers, 128-row tiles
-    __shared__ __align__(16) uint8_t colflag[2][64];      // column may saturate, 128-row tiles
-    __shared__ int s_skip;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tiles_c = (int)((C + 127) / 128);
-    const int ntiles = tiles_c * (int)((R + 127) / 128);
-    if (threadIdx.x == 0) {
-        s_skip = *reinterpret_cast<volatile int*>(&g_dev_error_q);
-        for (int i = 0; i < kTStages; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 8);
-        }
-        fence_mbar_init();
-        prefetch_tmap(&tmX);
-    }
-    __syncthreads();
-    if (s_skip) return;
-    if (warp == 8) {
-        if (lane == 0) {
-            int stage = 0, issued = 0;
-            uint32_t phase = 0;
-            bool aborted = false;
-            for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-                if (!wait_bounded_err(&empty[stage], phase ^ 1u, &g_dev_error_q)) {
-                    aborted = true;
-                    break;
-                }
-                const int c0 = (t % tiles_c) * 128, r0 = (t / tiles_c) * 128;
-                uint8_t* dst = smem + stage * kTTile;
-                mbar_arrive_expect_tx(&full[stage], kTTile);
-                tma_load_2d(dst, &tmX, c0, r0, &full[stage]);
-                tma_load_2d(dst + kTTile / 2, &tmX, c0 + 64, r0, &full[stage]);
-                ++issued;
-                if (++stage == kTStages) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
-            }
-            if (aborted) {
-                int n = issued < kTStages ? issued : kTStages;
-                int st = stage;
-                uint32_t ph = phase;
-                for (int i = 0; i < n; ++i) {
-                    if (--st < 0) {
-                        st = kTStages - 1;
-                        ph ^= 1u;
-                    }
-                    wait_drain(&full[st], ph);
-                }
-            }
-        }
-        return;   // the consumers synchronise among themselves (barrier 1, 256 threads)
-    }
-    const int h = warp >> 2, rq = warp & 3, cg = lane & 7, rg = lane >> 3;
-    const int rloc = rq * 32 + rg * 8;
-    const int cloc = h * 64 + cg * 8;
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t nsat = 0;
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-        const bool ok = wait_bounded_err(&full[stage], phase, &g_dev_error_q);
-        if (UNIT == 128) {
-            // the 8 consumer warps meet at named barrier 1 below, so they
-            // decide together whether to go on (AND over all 256 threads)
-            if (!consumers_all(ok)) break;
-        } else if (!__all_sync(0xFFFFFFFFu, ok)) {
-            break;
-        }
-        const uint8_t* half = smem + stage * kTTile + h * (kTTile / 2);
-        Vec8<kBF16> v[8];
+    __shared__ uint32_t colred[2][128];              // column maxima of the two 64-row halves
+    __shared__ __align__(16) float colm[128];        // column multipliers (128-row tiles)
+    __shared__ __align__(16) uint8_t colflag[128];   // column may saturate (128-row tiles)
+    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+    const int cl = ((w & 3) * 4 + (l & 3)) * 8;      // columns of this thread within the tile
+    const int rl = ((w >> 2) * 8 + (l >> 2)) * 8;    // rows of this thread within the tile
+    const int64_t tr0 = (int64_t)blockIdx.y * 128, tc0 = (int64_t)blockIdx.x * 128;
+    const int64_t r0 = tr0 + rl, c0 = tc0 + cl;
+    const bool ok = r0 < R && c0 < C;                // rows % 128 == 0, cols % 16 == 0
+    Vec8<kBF16> v[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int r = rloc + i;
-            v[i].w = *reinterpret_cast<const uint4*>(half + r * 128 + ((cg ^ (r & 7)) << 4));
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[stage]);
-        if (++stage == kTStages) {
-            stage = 0;
-            phase ^= 1u;
-        }
-        float f[8][8];
+    for (int i = 0; i < 8; ++i) {
+        if (ok) v[i].load(x, (r0 + i) * C + c0); else v[i].zero();
+    }
+    float f[8][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i].get(f[i]);
-        // column maxima of the |x| bit patterns over this thread's 8 rows, then
-        // over the quarter's 32 rows (lanes cg, cg+8, cg+16, cg+24)
-        uint32_t cm[8];
+    for (int i = 0; i < 8; ++i) v[i].get(f[i]);
+    // column maxima of the |x| bit patterns: this thread's 8 rows, then the
+    // row groups of the unit (lanes that share l & 3)
+    uint32_t cm[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t a = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a = max(a, __float_as_uint(f[i][j]) & 0x7FFFFFFFu);
+        a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
+        a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 8));
+        if (UNIT == 128) a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 16));
+        cm[j] = a;
+    }
+    float m[8];
+    uint32_t code[8];
+    bool maysat = false;      // some column's scaled maximum may exceed fmax
+    if (UNIT == 128) {
+        if ((l >> 2) == 0) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) colred[w >> 2][cl + j] = cm[j];
+        }
+        __syncthreads();
+        if (threadIdx.x < 128) {
+            const int c = threadIdx.x;
+            const uint32_t a = max(colred[0][c], colred[1][c]);
+            float mm, ss;
+            current_scale<FMT>(a, mm, ss);
+            colm[c] = mm;
+            colflag[c] = (a >= 0x7F800000u || __fmul_rn(__uint_as_float(a), mm) > Fmt<FMT>::fmax) ? 1 : 0;
+            if (tc0 + c < C) static_cast<float*>(scales)[(tr0 / 128) * C + tc0 + c] = ss;
+        }
+        __syncthreads();
+        const float4 m0 = *reinterpret_cast<const float4*>(&colm[cl]);
+        const float4 m1 = *reinterpret_cast<const float4*>(&colm[cl + 4]);
+        m[0] = m0.x; m[1] = m0.y; m[2] = m0.z; m[3] = m0.w;
+        m[4] = m1.x; m[5] = m1.y; m[6] = m1.z; m[7] = m1.w;
+        const uint2 fl = *reinterpret_cast<const uint2*>(&colflag[cl]);   // the 8 columns' flags
+        maysat = (fl.x | fl.y) != 0u;
+    } else {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            uint32_t a = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) a = max(a, __float_as_uint(f[i][j]) & 0x7FFFFFFFu);
-            a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 8));
-            a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 16));
-            cm[j] = a;
+            code[j] = mx_scale<FMT>(cm[j], m[j]);
+            maysat |= cm[j] >= 0x7F800000u || __fmul_rn(__uint_as_float(cm[j]), m[j]) > Fmt<FMT>::fmax;
         }
-        const int64_t tr0 = (int64_t)(t / tiles_c) * 128;
-        const int64_t r0 = tr0 + rloc;
-        const int64_t c0 = (int64_t)(t % tiles_c) * 128 + cloc;
-        float m[8];
-        uint32_t code[8];
-        bool maysat = false;      // some column's scaled maximum may exceed fmax
-        if (UNIT == 128) {
-            // the tile's 128 column maxima meet in shared memory; thread c < 128
-            // then computes column c's scale once for the whole CTA (and writes
-            // it: 128 consecutive floats), and every thread reads its 8 back
-            if (rg == 0) {
+    }
+    uint2 rows[8];
+    uint32_t nsat = 0;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) colred[h][rq][cg * 8 + j] = cm[j];
-            }
-            asm volatile("bar.sync 1, 256;" ::: "memory");
-            if (threadIdx.x < 128) {
-                const int hh = threadIdx.x >> 6, cc = threadIdx.x & 63;
-                const uint32_t a = max(max(colred[hh][0][cc], colred[hh][1][cc]),
-                                       max(colred[hh][2][cc], colred[hh][3][cc]));
-                float mm, ss;
-                current_scale<FMT>(a, mm, ss);
-                colm[hh][cc] = mm;
-                colflag[hh][cc] =
-                    (a >= 0x7F800000u || __fmul_rn(__uint_as_float(a), mm) > Fmt<FMT>::fmax) ? 1 : 0;
-                const int64_t c = (int64_t)(t % tiles_c) * 128 + threadIdx.x;
-                if (c < C) static_cast<float*>(scales)[(tr0 / 128) * C + c] = ss;
-            }
-            asm volatile("bar.sync 1, 256;" ::: "memory");   // colm ready; colred free for the next tile
-            const float4 m0 = *reinterpret_cast<const float4*>(&colm[h][cg * 8]);
-            const float4 m1 = *reinterpret_cast<const float4*>(&colm[h][cg * 8 + 4]);
-            m[0] = m0.x; m[1] = m0.y; m[2] = m0.z; m[3] = m0.w;
-            m[4] = m1.x; m[5] = m1.y; m[6] = m1.z; m[7] = m1.w;
-            const uint2 fl = *reinterpret_cast<const uint2*>(&colflag[h][cg * 8]);   // the 8 columns' flags
-            maysat = (fl.x | fl.y) != 0u;
-        } else {
+    for (int i = 0; i < 8; ++i) {
+        float p[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                code[j] = mx_scale<FMT>(cm[j], m[j]);
-                maysat |= cm[j] >= 0x7F800000u || __fmul_rn(__uint_as_float(cm[j]), m[j]) > Fmt<FMT>::fmax;
-            }
+        for (int j = 0; j < 8; ++j) p[j] = __fmul_rn(f[i][j], m[j]);
+        if (maysat) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) nsat += (fabsf(p[j]) > Fmt<FMT>::fmax) ? 1u : 0u;
         }
-        uint2 rows[8];
-        uint32_t ns = 0;
+        rows[i].x = cvt_fp8x2<FMT>(p[0], p[1]) | (cvt_fp8x2<FMT>(p[2], p[3]) << 16);
+        rows[i].y = cvt_fp8x2<FMT>(p[4], p[5]) | (cvt_fp8x2<FMT>(p[6], p[7]) << 16);
+    }
+    if (ok) {
+        if (q) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float p[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) p[j] = __fmul_rn(f[i][j], m[j]);
-            if (maysat) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) ns += (fabsf(p[j]) > Fmt<FMT>::fmax) ? 1u : 0u;
-            }
-            rows[i].x = cvt_fp8x2<FMT>(p[0], p[1]) | (cvt_fp8x2<FMT>(p[2], p[3]) << 16);
-            rows[i].y = cvt_fp8x2<FMT>(p[4], p[5]) | (cvt_fp8x2<FMT>(p[6], p[7]) << 16);
+            for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(q + (r0 + i) * C + c0) = rows[i];
         }
-        if (r0 < R && c0 < C) {
-            nsat += ns;
-            if (q) {
+        uint2 cols[8];
+        transpose8x8(rows, cols);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(q + (r0 + i) * C + c0) = rows[i];
-            }
-            uint2 cols[8];
-            transpose8x8(rows, cols);
+        for (int j = 0; j < 8; ++j) *reinterpret_cast<uint2*>(qT + (c0 + j) * R + r0) = cols[j];
+        if (UNIT == 32 && ((l >> 2) & 3) == 0) {     // the first row group of each 32-row block
+            uint8_t* e = static_cast<uint8_t*>(scales);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) *reinterpret_cast<uint2*>(qT + (c0 + j) * R + r0) = cols[j];
-            if (UNIT == 32 && rg == 0) {
-                uint8_t* e = static_cast<uint8_t*>(scales);
-                const int64_t t32 = (tr0 + rq * 32) / 32;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) e[mx_tiled_offset(c0 + j, t32, R)] = (uint8_t)code[j];
-            }
+            for (int j = 0; j < 8; ++j) e[mx_tiled_offset(c0 + j, r0 / 32, R)] = (uint8_t)code[j];
         }
+    } else {
+        nsat = 0;
     }
     if (sat) add_sat(sat, nsat);
 }
@@ -932,36 +688,20 @@ __global__ void __launch_bounds__(256, 3) k_ln_stats(const uint16_t* __restrict_
 cudaError_t launch_layernorm_quantize(const QuantArgs& a, const float* gamma, const float* beta, float eps,
                                       float* mu, float* rstd, cudaStream_t st, int sms)
 {
+    (void)sms;
     if (a.rows == 0 || a.cols == 0) return cudaSuccess;
-    launch_k(k_ln_stats, (unsigned)((a.rows + LN_ROWS - 1) / LN_ROWS), 256, 0, st, static_cast<const uint16_t*>(a.x), a.rows, a.cols, eps, mu, rstd);
-    CUtensorMap tm;
-    if (!encode_tmap_2d(&tm, 1, a.x, (uint64_t)a.cols, (uint64_t)a.rows, 64u, 128u)) return cudaErrorInvalidValue;
-    const int64_t tiles = ((a.rows + 127) / 128) * ((a.cols + 127) / 128);
-    const int grid = (int)(tiles < sms ? tiles : sms);
+    launch_k(k_ln_stats, (unsigned)((a.rows + LN_ROWS - 1) / LN_ROWS), 256, 0, st, static_cast<const uint16_t*>(a.x),
+             a.rows, a.cols, eps, mu, rstd);
     LnParams ln;
     ln.mu = mu;
     ln.rstd = rstd;
     ln.gamma = gamma;
     ln.beta = beta;
-    auto kern = a.format == kE4M3 ? k_cast_T_tma<kE4M3, true, true> : k_cast_T_tma<kE5M2, true, true>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
-    if (e != cudaSuccess) return e;
-    launch_k(kern, grid, kTThreads, kTSmem, st, tm, a.rows, a.cols, a.q, a.qT, a.state, a.history_len, nullptr,
-             static_cast<float*>(a.scales),
-                                          a.amax, a.sat, ln);
+    const dim3 grid((unsigned)((a.cols + 127) / 128), (unsigned)((a.rows + 127) / 128));
+    auto kern = a.format == kE4M3 ? k_cast_tensor_T<kBF16, kE4M3, true, true> : k_cast_tensor_T<kBF16, kE5M2, true, true>;
+    launch_k(kern, grid, 256, 0, st, a.x, a.rows, a.cols, a.q, a.qT, a.state, a.history_len, nullptr,
+             static_cast<float*>(a.scales), a.amax, a.sat, ln);
     return cudaGetLastError();
-}
-
-int read_device_error_quant(int clear)
-{
-    int v = 0;
-    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
-    if (cudaMemcpyFromSymbol(&v, g_dev_error_q, sizeof(int)) != cudaSuccess) return -1;
-    if (clear) {
-        int z = 0;
-        if (cudaMemcpyToSymbol(g_dev_error_q, &z, sizeof(int)) != cudaSuccess) return -1;
-    }
-    return v;
 }
 
 // ================================================================== row units
@@ -1203,22 +943,6 @@ static cudaError_t quant_dt_fmt(const QuantArgs& a, cudaStream_t st, int sms)
             if (cudaMemsetAsync(a.amax, 0, sizeof(float), st) != cudaSuccess) return cudaGetLastError();
         }
         float* s_out = static_cast<float*>(a.scales);
-        if (a.qT && DT == kBF16 && n > 0) {
-            CUtensorMap tm;
-            if (!encode_tmap_2d(&tm, 1, a.x, (uint64_t)a.cols, (uint64_t)a.rows, 64u, 128u)) return cudaErrorInvalidValue;
-            const int64_t tiles = ((a.rows + 127) / 128) * ((a.cols + 127) / 128);
-            const int grid = (int)(tiles < sms ? tiles : sms);
-            auto kern = delayed ? k_cast_T_tma<FMT, true> : k_cast_T_tma<FMT, false>;
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
-            if (e != cudaSuccess) return e;
-            if (delayed)
-                launch_k(kern, grid, kTThreads, kTSmem, st, tm, a.rows, a.cols, a.q, a.qT, a.state, H, nullptr, s_out, a.amax, a.sat,
-                                                      LnParams());
-            else
-                launch_k(kern, grid, kTThreads, kTSmem, st, tm, a.rows, a.cols, a.q, a.qT, nullptr, 0, a.amax, s_out, nullptr, a.sat,
-                                                      LnParams());
-            return cudaGetLastError();
-        }
         if (a.qT) {
             if (n == 0) {
                 if (!delayed) launch_k(k_cast_tensor<DT, FMT, false>, 1, kFlatThreads, 0, st, a.x, 0, a.q, nullptr, 0, a.amax, s_out, nullptr, nullptr);
@@ -1227,9 +951,11 @@ static cudaError_t quant_dt_fmt(const QuantArgs& a, cudaStream_t st, int sms)
             }
             dim3 grid((unsigned)((a.cols + 127) / 128), (unsigned)((a.rows + 127) / 128));
             if (delayed)
-                launch_k(k_cast_tensor_T<DT, FMT, true>, grid, 256, 0, st, a.x, a.rows, a.cols, a.q, a.qT, a.state, H, nullptr, s_out, a.amax, a.sat);
+                launch_k(k_cast_tensor_T<DT, FMT, true>, grid, 256, 0, st, a.x, a.rows, a.cols, a.q, a.qT, a.state, H, nullptr, s_out,
+                         a.amax, a.sat, LnParams());
             else
-                launch_k(k_cast_tensor_T<DT, FMT, false>, grid, 256, 0, st, a.x, a.rows, a.cols, a.q, a.qT, nullptr, 0, a.amax, s_out, nullptr, a.sat);
+                launch_k(k_cast_tensor_T<DT, FMT, false>, grid, 256, 0, st, a.x, a.rows, a.cols, a.q, a.qT, nullptr, 0, a.amax, s_out,
+                         nullptr, a.sat, LnParams());
         } else {
             int g = flat_grid(n / 8, sms);
             if (delayed)
@@ -1263,14 +989,9 @@ static cudaError_t quant_dt_fmt(const QuantArgs& a, cudaStream_t st, int sms)
         break;
     case kTileCol:
     case kMXCol: {
-        CUtensorMap tm;
-        if (!encode_tmap_2d(&tm, 1, a.x, (uint64_t)a.cols, (uint64_t)a.rows, 64u, 128u)) return cudaErrorInvalidValue;
-        const int64_t tiles = ((a.rows + 127) / 128) * ((a.cols + 127) / 128);
-        const int grid = (int)(tiles < sms ? tiles : sms);
-        auto kern = a.gran == kTileCol ? k_quant_col_tma<FMT, 128> : k_quant_col_tma<FMT, 32>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
-        if (e != cudaSuccess) return e;
-        launch_k(kern, grid, kTThreads, kTSmem, st, tm, a.rows, a.cols, a.q, a.qT, a.scales, a.sat);
+        const dim3 grid((unsigned)((a.cols + 127) / 128), (unsigned)(a.rows / 128));
+        auto kern = a.gran == kTileCol ? k_quant_col_block<FMT, 128> : k_quant_col_block<FMT, 32>;
+        launch_k(kern, grid, 256, 0, st, a.x, a.rows, a.cols, a.q, a.qT, a.scales, a.sat);
         break;
     }
     case kBlock:
