@@ -89,12 +89,15 @@ def kernel_traffic(name: str):
 
 
 def _peaks():
+    """(HBM GB/s, bf16 TFLOP/s burst, bf16 TFLOP/s sustained, source): the
+    measured figures, or the fallback ones if the file is missing."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "of measured"
+        burst = float(p["bf16_tflops"])
+        return float(p["hbm_gbs"]), burst, float(p.get("bf16_tflops_sustained", burst)), "of measured"
     except Exception:
-        return 6800.0, 1900.0, "of fallback"
+        return 6800.0, 1900.0, 1700.0, "of fallback"
 
 
 # ---------------------------------------------------------------- distributed
@@ -310,8 +313,9 @@ def run_ours(args, ws, rank, local):
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
-    hbm_peak, bf16_peak, peak_src = _peaks()
+    hbm_peak, bf16_peak, bf16_sust, peak_src = _peaks()
     fp8_peak = 2.0 * bf16_peak          # dense FP8 = 2 x dense BF16 (nominal ratio 4.5 / 2.25)
+    fp8_sust = 2.0 * bf16_sust          # the same under the power cap, for kernels timed inside a long loop
 
     b = FFNStep(device, n_input_sets=min(WK.steps, max(2, args.steps + args.warmup)))
     for s in range(args.warmup):
@@ -441,10 +445,12 @@ def run_ours(args, ws, rank, local):
             "e2e": e2e,
             "gpu_launches": b.KERNELS_PER_STEP * args.steps,
             "roofline": {"bound": "tensor", "kernel": "k_gemm_tensor_pair (tcgen05 .cta_group::2 kind::f8f6f4, 256x256 tile on a CTA pair, 6 stages)",
-                         "achieved": round(achieved, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
-                         "frac": round(achieved / fp8_peak, 4), "traffic": kernel_traffic("k_gemm_tensor_pair"),
+                         "achieved": round(achieved, 1), "peak": round(fp8_sust, 1), "unit": "TFLOP/s",
+                         "frac": round(achieved / fp8_sust, 4), "traffic": kernel_traffic("k_gemm_tensor_pair"),
                          "traffic_shape": "16384 x 14336 x 4096 forward GEMM (one ncu capture)",
-                         "peak_source": f"2 x bf16_tflops {peak_src} (dense FP8 = 2 x dense BF16)",
+                         "peak_source": f"2 x bf16_tflops_sustained {peak_src} (dense FP8 = 2 x dense BF16; the "
+                                        "GEMMs are timed inside the whole K-step loop, under the power cap)",
+                         "peak_burst": round(fp8_peak, 1), "frac_of_burst": round(achieved / fp8_peak, 4),
                          "flops_per_launch": gemm_flops_launch, "launch_ms": round(gemm_ms, 4)},
             "roofline_quantize": {"bound": "hbm", "kernel": "k_cast_tensor_T (16384 x 14336 casts)",
                                   "achieved": round(big_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
@@ -646,7 +652,7 @@ def modes_table(reps: int = 10):
     import scaled_quantize_gemm_gb300 as sq
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    hbm_peak, bf16_peak, src = _peaks()
+    hbm_peak, bf16_peak, _, src = _peaks()
     fp8_peak = 2.0 * bf16_peak
     u8 = dict(dtype=torch.uint8, device=dev)
     f32 = dict(dtype=torch.float32, device=dev)

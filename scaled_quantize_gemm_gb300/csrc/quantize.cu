@@ -468,7 +468,7 @@ __device__ __forceinline__ int64_t mx_tiled_offset(int64_t r, int64_t t, int64_t
 // c < 128 computes column c's scale once for the CTA and writes it.  Writes
 // the transposed codes qT and, when q is given, the codes in x's layout.
 template <int FMT, int UNIT>
-__global__ void __launch_bounds__(256) k_quant_col_block(const void* __restrict__ x, int64_t R, int64_t C,
+__global__ void __launch_bounds__(256, 3) k_quant_col_block(const void* __restrict__ x, int64_t R, int64_t C,
                                                          uint8_t* __restrict__ q, uint8_t* __restrict__ qT,
                                                          void* scales, unsigned long long* sat)
 {
@@ -487,21 +487,31 @@ __global__ void __launch_bounds__(256) k_quant_col_block(const void* __restrict_
     for (int i = 0; i < 8; ++i) {
         if (ok) v[i].load(x, (r0 + i) * C + c0); else v[i].zero();
     }
-    float f[8][8];
+    // column maxima of the |x| bit patterns, kept packed: word k holds columns
+    // 2k (low half) and 2k + 1 (high half) as bf16 patterns (NaN sorts above
+    // inf, so it propagates).  This thread's 8 rows, then the row groups of
+    // the unit (lanes that share l & 3).  Packing keeps the registers low
+    // enough for three CTAs per SM.
+    uint32_t pm[4] = {0u, 0u, 0u, 0u};
+    const uint32_t k7 = 0x7FFF7FFFu;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i].get(f[i]);
-    // column maxima of the |x| bit patterns: this thread's 8 rows, then the
-    // row groups of the unit (lanes that share l & 3)
-    uint32_t cm[8];
+    for (int i = 0; i < 8; ++i) {
+        pm[0] = __vmaxu2(pm[0], v[i].w.x & k7);
+        pm[1] = __vmaxu2(pm[1], v[i].w.y & k7);
+        pm[2] = __vmaxu2(pm[2], v[i].w.z & k7);
+        pm[3] = __vmaxu2(pm[3], v[i].w.w & k7);
+    }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        uint32_t a = 0;
+    for (int k = 0; k < 4; ++k) {
+        pm[k] = __vmaxu2(pm[k], __shfl_xor_sync(0xFFFFFFFFu, pm[k], 4));
+        pm[k] = __vmaxu2(pm[k], __shfl_xor_sync(0xFFFFFFFFu, pm[k], 8));
+        if (UNIT == 128) pm[k] = __vmaxu2(pm[k], __shfl_xor_sync(0xFFFFFFFFu, pm[k], 16));
+    }
+    uint32_t cm[8];                                  // fp32 bit patterns of the column maxima
 #pragma unroll
-        for (int i = 0; i < 8; ++i) a = max(a, __float_as_uint(f[i][j]) & 0x7FFFFFFFu);
-        a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
-        a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 8));
-        if (UNIT == 128) a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 16));
-        cm[j] = a;
+    for (int k = 0; k < 4; ++k) {
+        cm[2 * k] = pm[k] << 16;
+        cm[2 * k + 1] = pm[k] & 0xFFFF0000u;
     }
     float m[8];
     uint32_t code[8];
@@ -539,9 +549,10 @@ __global__ void __launch_bounds__(256) k_quant_col_block(const void* __restrict_
     uint32_t nsat = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        float p[8];
+        float f[8], p[8];
+        v[i].get(f);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) p[j] = __fmul_rn(f[i][j], m[j]);
+        for (int j = 0; j < 8; ++j) p[j] = __fmul_rn(f[j], m[j]);
         if (maysat) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) nsat += (fabsf(p[j]) > Fmt<FMT>::fmax) ? 1u : 0u;
