@@ -750,6 +750,17 @@ def modes_table(reps: int = 10):
         else:
             xs, wsrc = wl.student_t3((M, K), 1, dev), wl.normal((N, K), 0.02, 2, dev)
         qx, sx, qw, sw = quant_tile_block(M, N, K, xs, wsrc)
+        # the power-of-two variant of the same recipe (E8M0 tile and block
+        # scales) runs on the block-scaled MMA with no register promotion
+        qxp, qwp = torch.empty((M, K), **u8), torch.empty((N, K), **u8)
+        exp_, ewp = torch.empty(M * K // 32, **u8), torch.empty(N * K // 32, **u8)
+        sq.fp8_quantize(xs, sq.E4M3, sq.TILE_1x128_POW2, qxp, scales_out=exp_)
+        sq.fp8_quantize(wsrc, sq.E4M3, sq.BLOCK_128x128_POW2, qwp, scales_out=ewp)
+        ybp = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        row("fp8_gemm TILE_1x128_POW2 x BLOCK_128x128_POW2 (k_gemm_mx)", f"{M}x{N}x{K}",
+            med(lambda: sq.fp8_gemm(qxp, sq.E4M3, exp_, sq.TILE_1x128_POW2, qwp, sq.E4M3, ewp,
+                                    sq.BLOCK_128x128_POW2, ybp)), flops=2 * M * N * K)
+        del qxp, qwp, exp_, ewp, ybp
         if M == 4096:
             row("fp8_quantize TILE_1x128 E4M3", "4096x4096",
                 med(lambda: sq.fp8_quantize(xs, sq.E4M3, sq.TILE_1x128, qx, scales_out=sx)),
