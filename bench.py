@@ -826,7 +826,14 @@ def modes_table(reps: int = 10):
     row("fp8_quantize MX32_COL_TILED (column blocks) E4M3, qT only", big,
         med(lambda: sq.fp8_quantize(xb, sq.E4M3, sq.MX32_COL_TILED, None, qT=qbT, scales_out=e_m)),
         nbytes=R * C * 3 + R * C // 32)
-    del xb, qb_, qbT, s_t, s_b, s_bT, s_c, e_m
+    e_m2 = torch.empty(R * C // 32, **u8)
+    row("fp8_quantize_rows_cols TILE_1x128 (1x128 rows + 128x1 columns, one pass)", big,
+        med(lambda: sq.fp8_quantize_rows_cols(xb, sq.E4M3, sq.TILE_1x128, qb_, s_t, qbT, s_c)),
+        nbytes=R * C * 4 + 4 * R * (C // 128) + 4 * (R // 128) * C)
+    row("fp8_quantize_rows_cols MX32_TILED (MX-32 rows + columns, one pass)", big,
+        med(lambda: sq.fp8_quantize_rows_cols(xb, sq.E4M3, sq.MX32_TILED, qb_, e_m, qbT, e_m2)),
+        nbytes=R * C * 4 + 2 * (R * C // 32))
+    del xb, qb_, qbT, s_t, s_b, s_bT, s_c, e_m, e_m2
 
     # LayerNorm fused into the delayed per-tensor cast (with the transposed
     # copy): x read twice (statistics, then the normalise-and-cast pass),

@@ -196,6 +196,26 @@ FP8SQ_API int fp8_quantize(const void* x, int x_dtype, int64_t rows, int64_t col
                            uint8_t* qT, void* scales_out, float* amax_out,
                            unsigned long long* sat_count, void* stream);
 
+/* fp8_quantize_rows_cols: both operands of a fine-grained linear layer's
+ * products from one read of x ([W14] absmax bullet: 1x128 tiles / 32-value
+ * blocks; the column units are the wgrad operands, which contract over the
+ * rows of x).  The result is bit-identical to two fp8_quantize calls:
+ *   unit TILE_1x128:  q, row_scales      = fp8_quantize(TILE_1x128)
+ *                     qT, col_scales     = fp8_quantize(TILE_128x1)
+ *   unit MX32_TILED:  q, row_scales      = fp8_quantize(MX32_TILED)
+ *                     qT, col_scales     = fp8_quantize(MX32_COL_TILED)
+ * with the layouts documented there (f32 [rows][cols/128] and
+ * [rows/128][cols]; or the tiled E8M0 layouts of x and of qT).
+ *   x        device bf16 [rows][cols], 16-byte aligned; rows, cols % 128 == 0
+ *   q        device u8 [rows][cols]; qT device u8 [cols][rows]; 16-byte aligned
+ *   row_scales, col_scales  device, 4-byte aligned (16 for the E8M0 layouts)
+ *   sat_count  device u64 or NULL: the column-unit pass's saturations are
+ *              ADDED to it.
+ */
+FP8SQ_API int fp8_quantize_rows_cols(const void* x, int64_t rows, int64_t cols, int format, int unit,
+                                     uint8_t* q, void* row_scales, uint8_t* qT, void* col_scales,
+                                     unsigned long long* sat_count, void* stream);
+
 /* ---- 4. GEMM ----------------------------------------------------------------
  * D[m][n] = epi( sum_k Ahat[m][k] * Bhat[n][k] ) with Ahat = dec(qA) * sA,
  * Bhat = dec(qB) * sB ([W14] FP8 bullet: matmuls run in FP8 with a wider
@@ -339,7 +359,8 @@ FP8SQ_API int fp8_linear_fwd_noalloc(const void* x, const void* w, int64_t M, in
  *   cleared.
  * fp8_last_error: message for the calling thread's last non-zero status
  *   (static thread-local storage; never NULL).
- * fp8_abi_version: 3.  Changes from 2: fp8_selftest_wait_timeout added;
+ * fp8_abi_version: 4.  Changes from 3: fp8_quantize_rows_cols added.
+ *   Changes from 2 to 3: fp8_selftest_wait_timeout added;
  *   the LayerNorm entry points need 16-byte aligned gamma, beta, mu, rstd;
  *   a delayed per-tensor fp8_quantize writes s to a non-NULL scales_out.
  *   Every kernel is launched with programmatic stream serialisation (the

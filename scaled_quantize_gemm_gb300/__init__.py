@@ -58,6 +58,7 @@ def lib() -> ctypes.CDLL:
                 "fp8_scale_init": (I, [P, I, I, P]),
                 "fp8_update_scale": (I, [P, I, I, P, I, P]),
                 "fp8_quantize": (I, [P, I, I64, I64, I, I, P, I, P, P, P, P, P, P]),
+                "fp8_quantize_rows_cols": (I, [P, I64, I64, I, I, P, P, P, P, P, P]),
                 "fp8_gemm": (I, [P, I, P, I, P, I, P, I, I64, I64, I64, P, P, I, P]),
                 "fp8_linear_workspace_bytes": (Z, [I64, I64, I64, I]),
                 "fp8_linear_fwd": (I, [P, P, I64, I64, I64, I, I, P, P, I, P, Z, P, P, I, P]),
@@ -185,6 +186,20 @@ def fp8_quantize(x, format: int, gran: int, q, qT=None, scales_out=None, amax_ou
     _check(lib().fp8_quantize(_ptr(x), _dtype_code(x), R, C, format, gran, _ptr(delayed_state), history_len,
                               _ptr(q), _ptr(qT), _ptr(scales_out), _ptr(amax_out), _ptr(sat_count),
                               _stream(stream)))
+
+
+def fp8_quantize_rows_cols(x, format: int, unit: int, q, row_scales, qT, col_scales, sat_count=None,
+                           stream=None) -> None:
+    R, C = x.shape
+    T = _t()
+    _need(x, "x", T.bfloat16)
+    _need(q, "q", T.uint8, R * C)
+    _need(qT, "qT", T.uint8, R * C)
+    _need(row_scales, "row_scales", None, _scale_bytes(unit, R, C))
+    _need(col_scales, "col_scales", None,
+          _scale_bytes(TILE_128x1 if unit == TILE_1x128 else MX32_COL_TILED, R, C))
+    _check(lib().fp8_quantize_rows_cols(_ptr(x), R, C, format, unit, _ptr(q), _ptr(row_scales), _ptr(qT),
+                                        _ptr(col_scales), _ptr(sat_count), _stream(stream)))
 
 
 def fp8_gemm(A, a_format: int, a_scale, a_gran: int, B, b_format: int, b_scale, b_gran: int,

@@ -148,7 +148,7 @@ int api_check_device(int* sms) { return check_device(sms); }
 
 extern "C" {
 
-FP8SQ_API int fp8_abi_version(void) { return 3; }
+FP8SQ_API int fp8_abi_version(void) { return 4; }
 
 FP8SQ_API const char* fp8_last_error(void) { return g_msg; }
 
@@ -290,6 +290,38 @@ FP8SQ_API int fp8_quantize(const void* x, int x_dtype, int64_t rows, int64_t col
     a.amax = amax_out;
     a.sat = sat_count;
     return cuda_status(fp8sq::launch_quantize(a, static_cast<cudaStream_t>(stream), sms), "fp8_quantize launch");
+}
+
+FP8SQ_API int fp8_quantize_rows_cols(const void* x, int64_t rows, int64_t cols, int format, int unit,
+                                     uint8_t* q, void* row_scales, uint8_t* qT, void* col_scales,
+                                     unsigned long long* sat_count, void* stream)
+{
+    if ((!x || !q || !qT || !row_scales || !col_scales) && rows * cols != 0)
+        return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize_rows_cols: null pointer");
+    if (!valid_format(format)) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize_rows_cols: bad format");
+    if (unit != FP8SQ_TILE_1x128 && unit != FP8SQ_MX32_TILED)
+        return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize_rows_cols: unit must be TILE_1x128 or MX32_TILED");
+    if (rows < 0 || cols < 0) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize_rows_cols: negative size");
+    if (rows >= kMaxDim || cols >= kMaxDim) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_quantize_rows_cols: dimension too large");
+    if (rows % 128 || cols % 128)
+        return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_quantize_rows_cols: rows, cols %% 128 == 0 (%lld x %lld)",
+                    (long long)rows, (long long)cols);
+    if (!aligned16(x) || !aligned16(q) || !aligned16(qT))
+        return fail(FP8SQ_ERR_MISALIGNED, "fp8_quantize_rows_cols: x, q, qT must be 16-byte aligned");
+    const bool e8m0 = unit == FP8SQ_MX32_TILED;
+    if (e8m0 ? (!aligned16(row_scales) || !aligned16(col_scales)) : (!aligned4(row_scales) || !aligned4(col_scales)))
+        return fail(FP8SQ_ERR_MISALIGNED, "fp8_quantize_rows_cols: scales misaligned");
+    if (sat_count && (reinterpret_cast<uintptr_t>(sat_count) & 7u))
+        return fail(FP8SQ_ERR_MISALIGNED, "fp8_quantize_rows_cols: sat_count must be 8-byte aligned");
+    int sms, r;
+    if ((r = check_device(&sms))) return r;
+    if (rows * cols == 0) return FP8SQ_OK;
+    fp8sq::QuantArgs a;
+    a.x = x; a.x_dtype = fp8sq::kBF16; a.rows = rows; a.cols = cols; a.format = format;
+    a.gran = e8m0 ? fp8sq::kMXRowCol : fp8sq::kTileRowCol;
+    a.q = q; a.qT = qT; a.scales = row_scales; a.col_scales = col_scales; a.sat = sat_count;
+    return cuda_status(fp8sq::launch_quantize(a, static_cast<cudaStream_t>(stream), sms),
+                       "fp8_quantize_rows_cols launch");
 }
 
 static int validate_gemm(const uint8_t* A, int a_format, const void* a_scale, int a_gran, const uint8_t* B,
@@ -444,12 +476,12 @@ FP8SQ_API int fp8_linear_fwd(const void* x, const void* w, int64_t M, int64_t N,
         g.b_scale = &scal[1];
         g.a_format = g.b_format = fp8sq::kE4M3;
     } else if (gran == FP8SQ_TILE_1x128) {
-        // x: 1x128 tiles along K (forward) and 128x1 column tiles along M (wgrad)
-        qa.x = x; qa.rows = M; qa.cols = K; qa.gran = fp8sq::kTile;
-        qa.q = ws + L.qx; qa.scales = ws + L.sx;
+        // x: 1x128 tiles along K (forward) and 128x1 column tiles along M
+        // (wgrad), both from one read of x
+        qa.x = x; qa.rows = M; qa.cols = K; qa.gran = fp8sq::kTileRowCol;
+        qa.q = ws + L.qx; qa.scales = ws + L.sx; qa.qT = ws + L.qxT; qa.col_scales = ws + L.sxT;
         if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: quantize x"))) return r;
-        qa.gran = fp8sq::kTileCol; qa.q = nullptr; qa.qT = ws + L.qxT; qa.scales = ws + L.sxT;
-        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: column-quantize x"))) return r;
+        qa.col_scales = nullptr;
         // W: 128x128 blocks, with the transposed codes and scale grid (dgrad)
         qa.x = w; qa.rows = N; qa.cols = K; qa.gran = fp8sq::kBlock;
         qa.q = ws + L.qw; qa.qT = ws + L.qwT; qa.scales = ws + L.sw;
@@ -459,17 +491,14 @@ FP8SQ_API int fp8_linear_fwd(const void* x, const void* w, int64_t M, int64_t N,
         g.a_scale = ws + L.sx;
         g.b_scale = ws + L.sw;
     } else {
-        // x and W: MX-32 blocks along K (forward) and along their rows (backward)
-        qa.x = x; qa.rows = M; qa.cols = K; qa.gran = fp8sq::kMXTiled;
-        qa.q = ws + L.qx; qa.scales = ws + L.sx;
+        // x and W: MX-32 blocks along K (forward) and along their rows
+        // (backward), each from one read of the operand
+        qa.x = x; qa.rows = M; qa.cols = K; qa.gran = fp8sq::kMXRowCol;
+        qa.q = ws + L.qx; qa.scales = ws + L.sx; qa.qT = ws + L.qxT; qa.col_scales = ws + L.sxT;
         if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: quantize x"))) return r;
-        qa.gran = fp8sq::kMXCol; qa.q = nullptr; qa.qT = ws + L.qxT; qa.scales = ws + L.sxT;
-        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: column-quantize x"))) return r;
-        qa.x = w; qa.rows = N; qa.cols = K; qa.gran = fp8sq::kMXTiled;
-        qa.q = ws + L.qw; qa.qT = nullptr; qa.scales = ws + L.sw;
+        qa.x = w; qa.rows = N; qa.cols = K;
+        qa.q = ws + L.qw; qa.scales = ws + L.sw; qa.qT = ws + L.qwT; qa.col_scales = ws + L.swT;
         if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: quantize w"))) return r;
-        qa.gran = fp8sq::kMXCol; qa.q = nullptr; qa.qT = ws + L.qwT; qa.scales = ws + L.swT;
-        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: column-quantize w"))) return r;
         g.mode = 2;
         g.a_scale = ws + L.sx;
         g.b_scale = ws + L.sw;
@@ -519,19 +548,18 @@ FP8SQ_API int fp8_linear_bwd(const void* dy, int64_t M, int64_t N, int64_t K, in
         dg.a_scale = &scal[2]; dg.b_scale = &scal[1];
         wg.a_scale = &scal[2]; wg.b_scale = &scal[0];
     } else if (gran == FP8SQ_TILE_1x128) {
-        // dy: 1x128 tiles along N (dgrad) and 128x1 column tiles along M (wgrad)
-        qa.gran = fp8sq::kTile; qa.q = ws + L.qdy; qa.scales = ws + L.sdy;
+        // dy: 1x128 tiles along N (dgrad) and 128x1 column tiles along M
+        // (wgrad), both from one read of dy
+        qa.gran = fp8sq::kTileRowCol;
+        qa.q = ws + L.qdy; qa.scales = ws + L.sdy; qa.qT = ws + L.qdyT; qa.col_scales = ws + L.sdyT;
         if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_bwd: quantize dy"))) return r;
-        qa.gran = fp8sq::kTileCol; qa.q = nullptr; qa.qT = ws + L.qdyT; qa.scales = ws + L.sdyT;
-        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_bwd: column-quantize dy"))) return r;
         dg.mode = 1; dg.a_scale = ws + L.sdy; dg.b_scale = ws + L.swT;
         wg.mode = 3; wg.a_scale = ws + L.sdyT; wg.b_scale = ws + L.sxT;
     } else {
-        // dy: MX-32 blocks along N (dgrad) and along M (wgrad)
-        qa.gran = fp8sq::kMXTiled; qa.q = ws + L.qdy; qa.scales = ws + L.sdy;
+        // dy: MX-32 blocks along N (dgrad) and along M (wgrad), from one read
+        qa.gran = fp8sq::kMXRowCol;
+        qa.q = ws + L.qdy; qa.scales = ws + L.sdy; qa.qT = ws + L.qdyT; qa.col_scales = ws + L.sdyT;
         if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_bwd: quantize dy"))) return r;
-        qa.gran = fp8sq::kMXCol; qa.q = nullptr; qa.qT = ws + L.qdyT; qa.scales = ws + L.sdyT;
-        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_bwd: column-quantize dy"))) return r;
         dg.mode = wg.mode = 2;
         dg.a_scale = ws + L.sdy; dg.b_scale = ws + L.swT;
         wg.a_scale = ws + L.sdyT; wg.b_scale = ws + L.sxT;

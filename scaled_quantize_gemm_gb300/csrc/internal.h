@@ -10,7 +10,8 @@ namespace fp8sq {
 enum { kE4M3 = 0, kE5M2 = 1 };
 enum { kBF16 = 0, kF32 = 1 };
 enum { kTensor = 0, kTile = 1, kBlock = 2, kMX = 3, kMXTiled = 4, kTileCol = 5, kMXCol = 6,
-       kTilePow2 = 7, kBlockPow2 = 8, kMXFloor = 9 };
+       kTilePow2 = 7, kBlockPow2 = 8, kMXFloor = 9,
+       kTileRowCol = 10, kMXRowCol = 11 };   // rows and columns in one pass (fp8_quantize_rows_cols)
 
 struct QuantArgs {
     const void* x = nullptr;
@@ -24,6 +25,7 @@ struct QuantArgs {
     uint8_t* qT = nullptr;
     void* scales = nullptr;
     float* scalesT = nullptr;        // 128x128 blocks with qT: the transposed scale grid
+    void* col_scales = nullptr;      // rows and columns in one pass: the column-unit scales
     float* amax = nullptr;
     unsigned long long* sat = nullptr;
     const float* amax_in = nullptr;  // current per-tensor: the amax of pass 1

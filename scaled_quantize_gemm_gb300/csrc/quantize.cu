@@ -467,15 +467,24 @@ __device__ __forceinline__ int64_t mx_tiled_offset(int64_t r, int64_t t, int64_t
 // (shuffles, then one exchange through shared memory), after which thread
 // c < 128 computes column c's scale once for the CTA and writes it.  Writes
 // the transposed codes qT and, when q is given, the codes in x's layout.
-template <int FMT, int UNIT>
-__global__ void __launch_bounds__(256, 3) k_quant_col_block(const void* __restrict__ x, int64_t R, int64_t C,
+// ROWQ: the same pass also quantises the rows in their own units (UNIT = 128:
+// 1x128 tiles, f32 scales [R][C/128] into rscales; UNIT = 32: MX-32 blocks,
+// E8M0 codes in the tiled layout of x [R][C]) and writes q with those row
+// codes: both operands of a fine-grained linear's products from one read of
+// x.  A row's 32 columns are four lanes of one warp; its 128 columns are four
+// warps (shuffles over l ^ 1, l ^ 2, then shared memory), and thread
+// 128 + r computes row r's 1x128 scale.
+template <int FMT, int UNIT, bool ROWQ = false>
+__global__ void __launch_bounds__(256, ROWQ ? 2 : 3) k_quant_col_block(const void* __restrict__ x, int64_t R, int64_t C,
                                                          uint8_t* __restrict__ q, uint8_t* __restrict__ qT,
-                                                         void* scales, unsigned long long* sat)
+                                                         void* scales, void* rscales, unsigned long long* sat)
 {
     pdl_enter();
     __shared__ uint32_t colred[2][128];              // column maxima of the two 64-row halves
     __shared__ __align__(16) float colm[128];        // column multipliers (128-row tiles)
     __shared__ __align__(16) uint8_t colflag[128];   // column may saturate (128-row tiles)
+    __shared__ uint32_t rowred[ROWQ && UNIT == 128 ? 4 : 1][128];   // row maxima of the four 32-column warps
+    __shared__ __align__(16) float rowm[ROWQ && UNIT == 128 ? 128 : 4];
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
     const int cl = ((w & 3) * 4 + (l & 3)) * 8;      // columns of this thread within the tile
     const int rl = ((w >> 2) * 8 + (l >> 2)) * 8;    // rows of this thread within the tile
@@ -513,13 +522,29 @@ __global__ void __launch_bounds__(256, 3) k_quant_col_block(const void* __restri
         cm[2 * k] = pm[k] << 16;
         cm[2 * k + 1] = pm[k] & 0xFFFF0000u;
     }
-    float m[8];
-    uint32_t code[8];
+    // row maxima (ROWQ): this thread's 8 columns of each of its rows, then the
+    // four lanes of the warp that cover 32 columns (l ^ 1, l ^ 2)
+    uint32_t rmax[8];
+    if (ROWQ) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint32_t a = v[i].absmax_bits();
+            a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+            a = max(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+            rmax[i] = a;
+        }
+    }
+    float m[8], rm[8];
+    uint32_t code[8], rcode[8];
     bool maysat = false;      // some column's scaled maximum may exceed fmax
     if (UNIT == 128) {
         if ((l >> 2) == 0) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) colred[w >> 2][cl + j] = cm[j];
+        }
+        if (ROWQ && (l & 3) == 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) rowred[w & 3][rl + i] = rmax[i];
         }
         __syncthreads();
         if (threadIdx.x < 128) {
@@ -530,6 +555,13 @@ __global__ void __launch_bounds__(256, 3) k_quant_col_block(const void* __restri
             colm[c] = mm;
             colflag[c] = (a >= 0x7F800000u || __fmul_rn(__uint_as_float(a), mm) > Fmt<FMT>::fmax) ? 1 : 0;
             if (tc0 + c < C) static_cast<float*>(scales)[(tr0 / 128) * C + tc0 + c] = ss;
+        } else if (ROWQ) {
+            const int r = threadIdx.x - 128;
+            const uint32_t a = max(max(rowred[0][r], rowred[1][r]), max(rowred[2][r], rowred[3][r]));
+            float mm, ss;
+            current_scale<FMT>(a, mm, ss);
+            rowm[r] = mm;
+            if (tr0 + r < R) static_cast<float*>(rscales)[(tr0 + r) * (C / 128) + blockIdx.x] = ss;
         }
         __syncthreads();
         const float4 m0 = *reinterpret_cast<const float4*>(&colm[cl]);
@@ -538,15 +570,25 @@ __global__ void __launch_bounds__(256, 3) k_quant_col_block(const void* __restri
         m[4] = m1.x; m[5] = m1.y; m[6] = m1.z; m[7] = m1.w;
         const uint2 fl = *reinterpret_cast<const uint2*>(&colflag[cl]);   // the 8 columns' flags
         maysat = (fl.x | fl.y) != 0u;
+        if (ROWQ) {
+            const float4 q0 = *reinterpret_cast<const float4*>(&rowm[rl]);
+            const float4 q1 = *reinterpret_cast<const float4*>(&rowm[rl + 4]);
+            rm[0] = q0.x; rm[1] = q0.y; rm[2] = q0.z; rm[3] = q0.w;
+            rm[4] = q1.x; rm[5] = q1.y; rm[6] = q1.z; rm[7] = q1.w;
+        }
     } else {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             code[j] = mx_scale<FMT>(cm[j], m[j]);
             maysat |= cm[j] >= 0x7F800000u || __fmul_rn(__uint_as_float(cm[j]), m[j]) > Fmt<FMT>::fmax;
         }
+        if (ROWQ) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) rcode[i] = mx_scale<FMT>(rmax[i], rm[i]);
+        }
     }
     uint2 rows[8];
-    uint32_t nsat = 0;
+    uint32_t nsat = 0, nsat_r = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         float f[8], p[8];
@@ -559,9 +601,15 @@ __global__ void __launch_bounds__(256, 3) k_quant_col_block(const void* __restri
         }
         rows[i].x = cvt_fp8x2<FMT>(p[0], p[1]) | (cvt_fp8x2<FMT>(p[2], p[3]) << 16);
         rows[i].y = cvt_fp8x2<FMT>(p[4], p[5]) | (cvt_fp8x2<FMT>(p[6], p[7]) << 16);
+        if (ROWQ && ok) {
+            // the row-unit codes of this row go to q (their saturations are
+            // counted separately: sat counts the column-unit pass)
+            *reinterpret_cast<uint2*>(q + (r0 + i) * C + c0) = cast8<FMT>(f, rm[i], v[i].absmax_bits(), nsat_r);
+        }
     }
+    (void)nsat_r;
     if (ok) {
-        if (q) {
+        if (q && !ROWQ) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(q + (r0 + i) * C + c0) = rows[i];
         }
@@ -573,6 +621,11 @@ __global__ void __launch_bounds__(256, 3) k_quant_col_block(const void* __restri
             uint8_t* e = static_cast<uint8_t*>(scales);
 #pragma unroll
             for (int j = 0; j < 8; ++j) e[mx_tiled_offset(c0 + j, r0 / 32, R)] = (uint8_t)code[j];
+        }
+        if (ROWQ && UNIT == 32 && (l & 3) == 0) {    // the first lane of each 32-column block
+            uint8_t* e = static_cast<uint8_t*>(rscales);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) e[mx_tiled_offset(r0 + i, c0 / 32, C)] = (uint8_t)rcode[i];
         }
     } else {
         nsat = 0;
@@ -1002,7 +1055,15 @@ static cudaError_t quant_dt_fmt(const QuantArgs& a, cudaStream_t st, int sms)
     case kMXCol: {
         const dim3 grid((unsigned)((a.cols + 127) / 128), (unsigned)(a.rows / 128));
         auto kern = a.gran == kTileCol ? k_quant_col_block<FMT, 128> : k_quant_col_block<FMT, 32>;
-        launch_k(kern, grid, 256, 0, st, a.x, a.rows, a.cols, a.q, a.qT, a.scales, a.sat);
+        launch_k(kern, grid, 256, 0, st, a.x, a.rows, a.cols, a.q, a.qT, a.scales, nullptr, a.sat);
+        break;
+    }
+    case kTileRowCol:
+    case kMXRowCol: {
+        // rows in their own units into q / scales, columns into qT / col_scales
+        const dim3 grid((unsigned)(a.cols / 128), (unsigned)(a.rows / 128));
+        auto kern = a.gran == kTileRowCol ? k_quant_col_block<FMT, 128, true> : k_quant_col_block<FMT, 32, true>;
+        launch_k(kern, grid, 256, 0, st, a.x, a.rows, a.cols, a.q, a.qT, a.col_scales, a.scales, a.sat);
         break;
     }
     case kBlock:

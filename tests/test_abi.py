@@ -22,7 +22,7 @@ def test_exports_every_declared_symbol(L):
                           "fp8_scale_init", "fp8_linear_workspace_bytes", "fp8_device_status"}
     for n in names:
         assert hasattr(L, n), n
-    assert L.fp8_abi_version() == 3
+    assert L.fp8_abi_version() == 4
 
 
 def test_null_and_enum_validation(L):
@@ -139,3 +139,14 @@ def test_layernorm_validation(L):
     assert b"16-byte" in L.fp8_last_error()
     assert ln(*args(f, M=24)) == sq.ERR_UNSUPPORTED
     assert ln(*args(None)) == sq.ERR_INVALID_ARG
+
+
+def test_rows_cols_validation(L):
+    P = ctypes.c_void_p
+    f = P(4096)
+    rc = L.fp8_quantize_rows_cols
+    assert rc(f, 128, 128, sq.E4M3, sq.TENSOR, f, f, f, f, None, None) == sq.ERR_INVALID_ARG
+    assert rc(f, 128, 96, sq.E4M3, sq.TILE_1x128, f, f, f, f, None, None) == sq.ERR_UNSUPPORTED
+    assert rc(P(4100), 128, 128, sq.E4M3, sq.TILE_1x128, f, f, f, f, None, None) == sq.ERR_MISALIGNED
+    assert rc(f, 128, 128, sq.E4M3, sq.MX32_TILED, f, P(4100), f, f, None, None) == sq.ERR_MISALIGNED
+    assert rc(None, 128, 128, sq.E4M3, sq.TILE_1x128, f, f, f, f, None, None) == sq.ERR_INVALID_ARG

@@ -375,3 +375,48 @@ def test_pow2_tiles_blocks_and_floor_mx(fmt):
     rq, re, rsat = o.quantize_mx32_floor(xf, fmt)
     assert np.array_equal(codes(q), rq) and int(sat.item()) == rsat >= 1
     assert np.array_equal(mx_untile(e.cpu().numpy(), R, C), re)
+
+
+@pytest.mark.parametrize("unit", [sq.TILE_1x128, sq.MX32_TILED])
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape", [(256, 384), (128, 128), (384, 256)])
+def test_rows_cols_one_pass(unit, fmt, shape):
+    """fp8_quantize_rows_cols gives bit-identical results to the two separate
+    casts (row units into q, column units into qT), and matches the oracle's
+    row-unit and column-unit quantisers; an outlier and a NaN are planted."""
+    from _helpers import mx_untile
+    R, C = shape
+    x = wl.student_t3(shape, 81 + R + C)
+    x[3, 130 % C] = 700.0
+    x[R - 1, 5] = float("nan")
+    xd = x.to(DEV)
+    mx = unit == sq.MX32_TILED
+    col_unit = sq.MX32_COL_TILED if mx else sq.TILE_128x1
+    q, qT = _u8(shape), _u8((C, R))
+    if mx:
+        rs, cs = _u8((R * C // 32,)), _u8((R * C // 32,))
+    else:
+        rs, cs = _f32(R * (C // 128)), _f32((R // 128) * C)
+    sq.fp8_quantize_rows_cols(xd, fmt, unit, q, rs, qT, cs)
+    q2, qT2 = _u8(shape), _u8((C, R))
+    rs2, cs2 = torch.empty_like(rs), torch.empty_like(cs)
+    sq.fp8_quantize(xd, fmt, unit, q2, scales_out=rs2)
+    sq.fp8_quantize(xd, fmt, col_unit, None, qT=qT2, scales_out=cs2)
+    torch.cuda.synchronize()
+    assert torch.equal(q, q2) and torch.equal(qT, qT2)
+    assert torch.equal(rs.view(torch.uint8), rs2.view(torch.uint8))
+    assert torch.equal(cs.view(torch.uint8), cs2.view(torch.uint8))
+    # against the oracle
+    xf = np32(x)
+    if mx:
+        rq, re, _, _ = o.quantize_mx32(xf, fmt)
+        cq, ce, _, _ = o.quantize_mx32_col(xf, fmt)
+        assert np.array_equal(mx_untile(rs.cpu().numpy(), R, C), re)
+        assert np.array_equal(mx_untile(cs.cpu().numpy(), C, R), ce.T)
+    else:
+        rq, rsc, _, _ = o.quantize_tile1x128(xf, fmt)
+        cq, csc, _, _ = o.quantize_tile128x1(xf, fmt)
+        assert np.array_equal(rs.cpu().numpy().view(np.uint32), rsc.ravel().view(np.uint32))
+        assert np.array_equal(cs.cpu().numpy().view(np.uint32), csc.ravel().view(np.uint32))
+    assert nan_aware_codes_equal(codes(q), rq, fmt)
+    assert nan_aware_codes_equal(codes(qT), cq.T, fmt)
