@@ -15,7 +15,7 @@
 // Mode 0 (per-tensor scales): two TMEM accumulators of BN columns, so the
 // epilogue of tile i overlaps the MMAs of tile i+1.
 // Mode 1 (1x128 activation tiles x 128x128 weight blocks): the MMAs of each
-// 128-wide K block write a fresh partial into one of four TMEM buffers and
+// 128-wide K block write a fresh partial into one of two TMEM buffers and
 // the epilogue warps promote it into fp32 registers with sA[m][kb] *
 // sB[nb][kb] (the fixed-interval fp32 promotion of the week-14 page,
 // interval = the 128-wide scale block).
@@ -509,47 +509,96 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 }
 
 // ================================================================== mode 1
-// Fine-grained scales with per-K-block promotion.  Tile 128 x BN, 512 / BN
-// TMEM partial buffers of BN columns.  Eight epilogue warps (2..9): warp w
-// reads TMEM lane quarter w % 4 and owns column half (w - 2) / 4 of the tile
-// (COLS = BN / 2 columns).  For every K block it copies its 32 x COLS fp32
-// partial out of tensor memory, frees the buffer after the last copy, and
-// adds partial x scale into its register accumulators, while the MMAs of the
-// next K blocks run into the other buffers.
+// Fine-grained scales with per-K-block promotion.  One CTA per 128 x 256
+// tile; the MMAs of each 128-wide K block write a fresh fp32 partial into one
+// of two 256-column TMEM buffers, and eight epilogue warps promote it into
+// fp32 registers (acc += partial x scale) while the MMAs of the next K block
+// run into the other buffer.
+//   warp 0: TMA producer (48 KB per stage, 4 stages);
+//   warp 1: TMEM allocation (512 columns); one thread issues the MMAs and
+//     one commit per K block, on the buffer's full barrier;
+//   warp 2: stage releaser.  The buffer's full barrier fires only after the
+//     MMAs that read the K block's shared-memory stage have completed, so
+//     one thread waits on it and frees the stage for the producer; the MMA
+//     thread then needs a single commit per K block.  It also counts in the
+//     buffer's release, so the MMAs never run two phases ahead of it;
+//   warp 3: idle (it completes warpgroup 0);
+//   warps 4 .. 11: warp w reads TMEM lane quarter w % 4 and owns the 128
+//     columns (w - 4) / 4 of the tile.  Per K block it copies them out in two
+//     waits of two 32-column chunks, releases the buffer after the second
+//     wait, then does the FMAs (two columns per packed f32x2 FMA).
+// With two buffers the MMAs run one K block ahead of the promotion, so the
+// promotion of a K block (wake-up, the two waits, the release) and the MMA
+// thread's turnaround between K blocks both have to fit in one K block of
+// MMAs.  128 accumulators plus 64 copied registers a thread exceed the 168
+// registers of a 12-warp CTA, so the warpgroups re-split the register file
+// (setmaxnreg): warpgroup 0 drops to kPromoCtlRegs, the two epilogue
+// warpgroups rise to kPromoEpiRegs.
 // SM selects the scale layouts:
-//   1: A in 1x128 tiles sA[M][K/128], B in 128x128 blocks sB[ceil(N/128)][K/128]
-//      (BN = 256): a warp's 128 columns are one weight block, so its scale
-//      is one number per K block, sA[row][kb] * sB[block][kb];
+//   1: A in 1x128 tiles sA[M][K/128], B in 128x128 blocks sB[ceil(N/128)][K/128]:
+//      a warp's 128 columns are one weight block, so its scale is one number
+//      per K block, sA[row][kb] * sB[block][kb];
 //   3: both operands in tiles along K with K-block-major scales sA[K/128][M],
-//      sB[K/128][N] (the transposed codes of column-tile quantisation), BN = 128:
-//      per element sA[kb][row] * sB[kb][col]; the warp's column scales reach
-//      its lanes through a double-buffered shared-memory slot.
-// Measured at 16384 x 14336 x 4096 (bf16 out): per-row scales 1999 TFLOP/s
-// at BN 256 against 1457 at BN 128 (a 256-wide tile halves the A-operand
-// shared-memory reads per FLOP; the tensor-memory drain per FLOP is the same
-// for any width).  Per-column scales stay at BN 128: at 256 their 128
-// accumulators, the partial chunk and the scale operands exceed the 168
-// registers a thread has with ten warps, and the spills cost more than the
-// wider tile gains.  Outputs are written with direct 16-byte stores: staging
-// them through shared memory for bulk tensor stores serialises each warp's
-// stores behind the previous store's read and, with the MMAs at most two
-// K blocks ahead, stalls the tensor pipe (1371 against 1999 TFLOP/s).
-constexpr int kPromoStages(int bn) { return bn == 256 ? 4 : 6; }
+//      sB[K/128][N] (the transposed codes of column-tile quantisation): per
+//      element sA[kb][row] * sB[kb][col]; the warp's column scales reach its
+//      lanes through a double-buffered shared-memory slot.
+// Measured, per-row scales, bf16 out, TFLOP/s at 4096^3 / 16384 x 14336 x
+// 4096 / 8192^3 (bit-identical outputs throughout):
+//   this kernel                                              1832 2188 2421
+//   the same on CTA pairs (256 x 256, cluster-wide handshake) 1716 2115 2348
+//   128 x 192 tiles, all 96 columns copied in one wait       1651 1902 1985
+//   256 x 128 CTA-pair tiles, four 128-column buffers        1335 1440 1525
+//   ten warps, 168 registers, four serial 32-column copies   1633 2002 2182
+// The epilogue's waits stay at CTA scope; with the same handshake across a
+// CTA pair, a release arrival at cluster scope on every K block put a fence
+// behind each K block's scale loads (ncu: membar the dominant stall, 12 %
+// tensor-pipe activity).
+constexpr int kPromoBN = 256;
+constexpr int kPromoStages = 4;
+constexpr int kPromoEpi0 = 4;                        // first epilogue warp (warpgroup 1)
+constexpr int kPromoEpi = 8;                         // epilogue warps
+constexpr int kPromoThreads = 32 * (kPromoEpi0 + kPromoEpi);
+constexpr int kPromoCtlRegs = 48;                    // warpgroup 0 after the re-split
+constexpr int kPromoEpiRegs = 224;                   // epilogue warpgroups after the re-split
+// registers a thread must be launched with for the re-split to fit
+constexpr int kPromoLaunchRegs = (128 * kPromoCtlRegs + 32 * kPromoEpi * kPromoEpiRegs + kPromoThreads - 1) / kPromoThreads;
+using PromoSmem = Smem<kPromoBN, kPromoStages, 2>;
 
-template <int BN, int STAGES, bool OUT_BF16, int SM>
-__global__ void __launch_bounds__(320, 1)
+// acc[0..1] += x[0..1] * s[0..1], both lanes rounded once (the packed
+// f32x2 FMA: bit-identical to two fmaf calls, half the issue slots)
+__device__ __forceinline__ void fma2(float& a0, float& a1, float x0, float x1, float s0, float s1)
+{
+    const float2 r = __ffma2_rn(make_float2(x0, x1), make_float2(s0, s1), make_float2(a0, a1));
+    a0 = r.x;
+    a1 = r.y;
+}
+
+// warpgroup register re-split (every thread of the warpgroup executes it)
+template <int N>
+__device__ __forceinline__ void regs_dec()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <bool OUT_BF16, int SM>
+__global__ void __launch_bounds__(kPromoThreads, 1)
     k_gemm_promote(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    EpiParams p, uint32_t idesc, TileSched sched)
 {
     pdl_enter();
-    constexpr int NB = 512 / BN;             // partial buffers
-    constexpr int EPI = 8;
-    constexpr int COLS = BN / 2;             // columns per epilogue warp
-    constexpr int NLD = COLS / 32;           // 32-column TMEM loads per K block
+    constexpr int BN = kPromoBN, STAGES = kPromoStages, NB = 2, EPI = kPromoEpi;
+    constexpr int COLS = 4 * BN / EPI;       // columns per epilogue warp (128)
+    constexpr int LDF = 2;                   // 32-column copies in flight per wait
+    constexpr int NLD = COLS / 32;           // 32-column copies per K block
     constexpr int CPL = COLS / 32;           // column scales per lane (SM 3)
-    static_assert(BN == 128 || BN == 256, "tile width");
-    static_assert(SM == 1 ? BN == 256 : BN == 128, "scale layout and tile width go together");
-    using L = Smem<BN, STAGES, NB>;
+    static_assert(SM == 1 || SM == 3, "scale layout");
+    static_assert(COLS == 128, "a warp's columns are one weight block");
+    using L = PromoSmem;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
@@ -558,14 +607,17 @@ __global__ void __launch_bounds__(320, 1)
     uint64_t* aempty = afull + NB;
     uint64_t* drain = aempty + NB;
     constexpr uint32_t TMEM_COLS = 512;
+    __shared__ __align__(16) float colbuf[SM == 3 ? EPI : 1][2][SM == 3 ? COLS : 4];
 
     uint32_t tmem_base;
-    if (!gemm_setup<STAGES, NB, EPI>(smem, L::BAR_OFF, TMEM_COLS, &tmA, &tmB, tmem_base)) return;
+    // a buffer is released by the epilogue warps and the stage releaser
+    if (!gemm_setup<STAGES, NB, EPI + 1>(smem, L::BAR_OFF, TMEM_COLS, &tmA, &tmB, tmem_base)) return;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int num_tiles = sched.num_m * sched.num_n;
     const int nkb = p.K / BK;
 
+    if (warp < kPromoEpi0) regs_dec<kPromoCtlRegs>();
     if (warp == 0) {
         if (lane == 0) producer_loop<BN, STAGES>(smem, full, empty, &tmA, &tmB, sched, num_tiles, nkb);
     } else if (warp == 1) {
@@ -588,8 +640,7 @@ __global__ void __launch_bounds__(320, 1)
                     const uint64_t db = sdesc_kmajor_sw128(sa + A_BYTES);
 #pragma unroll
                     for (int k = 0; k < BK / 32; ++k) mma_f8f6f4(d, da + 2 * k, db + 2 * k, idesc, k != 0 ? 1u : 0u);
-                    mma_commit(&empty[stage]);
-                    mma_commit(&afull[b]);
+                    mma_commit(&afull[b]);   // also releases the stage (through warp 2)
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -601,13 +652,29 @@ __global__ void __launch_bounds__(320, 1)
                 wait_drain(drain, 0);
             }
         }
-    } else {
+    } else if (warp == 2) {
+        if (lane == 0) {
+            int it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const int b = it % NB;
+                    if (!wait_bounded(&afull[b], (uint32_t)(it / NB) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive(&empty[it % STAGES]);
+                    mbar_arrive(&aempty[b]);
+                }
+            }
+        }
+    } else if (warp >= kPromoEpi0) {
+        regs_inc<kPromoEpiRegs>();
         const int quarter = warp & 3;
-        const int part = (warp - 2) >> 2;           // column half of the tile
-        const int ew = warp - 2;
+        const int part = (warp - kPromoEpi0) >> 2;  // column half of the tile
+        const int ew = warp - kPromoEpi0;
         const int ksb = p.K / BK;                   // scale blocks along K
         const int nblk = (p.N + 127) / 128;         // weight blocks along N
-        __shared__ __align__(16) float colbuf[SM == 3 ? EPI : 1][2][SM == 3 ? COLS : 4];
         int it = 0;
         bool ok_all = true;
         for (int t = blockIdx.x; t < num_tiles && ok_all; t += gridDim.x) {
@@ -622,7 +689,7 @@ __global__ void __launch_bounds__(320, 1)
             // SM 1: sc = the K block's combined scale (one weight block per warp).
             // SM 3: ra = the row's scale, cb = this lane's CPL column scales.
             const float* sa_row = p.sA + (int64_t)rowc * ksb;
-            int wblk = nb * (BN / 128) + part * (COLS / 128);
+            int wblk = nb * (BN / 128) + part;
             wblk = wblk < nblk ? wblk : nblk - 1;
             const float* sb_row = p.sB + (int64_t)wblk * ksb;
             int cl = col0 + CPL * lane;
@@ -665,38 +732,38 @@ __global__ void __launch_bounds__(320, 1)
                 tc_fence_after();
                 const uint32_t taddr =
                     tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * BN + part * COLS);
-                if constexpr (SM == 1) {
-                    // 128 columns: one 32-column chunk in flight at a time (registers)
 #pragma unroll
-                    for (int l = 0; l < NLD; ++l) {
-                        uint32_t r[32];
-                        tmem_ld_32x32b_x32(taddr + 32 * l, r);
-                        tmem_ld_wait();
-                        if (l == NLD - 1) {
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&aempty[b]);
-                        }
+                for (int g = 0; g < NLD / LDF; ++g) {
+                    uint32_t r[LDF][32];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) acc[32 * l + i] = fmaf(__uint_as_float(r[i]), sc, acc[32 * l + i]);
-                    }
-                } else {
-                    // 64 columns: both chunks loaded, one wait, buffer freed before the FMAs
-                    uint32_t r[NLD][32];
-#pragma unroll
-                    for (int l = 0; l < NLD; ++l) tmem_ld_32x32b_x32(taddr + 32 * l, r[l]);
+                    for (int l = 0; l < LDF; ++l) tmem_ld_32x32b_x32(taddr + 32 * (g * LDF + l), r[l]);
                     tmem_ld_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&aempty[b]);
+                    if (g == NLD / LDF - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&aempty[b]);
+                    }
 #pragma unroll
-                    for (int c4 = 0; c4 < COLS / 4; ++c4) {
-                        const float4 s4 = *reinterpret_cast<const float4*>(cbuf + 4 * c4);
-                        const float s[4] = {s4.x, s4.y, s4.z, s4.w};
+                    for (int l = 0; l < LDF; ++l) {
+                        float* a = acc + 32 * (g * LDF + l);
+                        if constexpr (SM == 1) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int c = 4 * c4 + e;
-                            acc[c] = fmaf(__uint_as_float(r[c / 32][c % 32]), ra * s[e], acc[c]);
+                            for (int c = 0; c < 32; c += 2)
+                                fma2(a[c], a[c + 1], __uint_as_float(r[l][c]), __uint_as_float(r[l][c + 1]), sc, sc);
+                        } else {
+                            // ra x column scale, two columns per packed f32x2 multiply
+                            const float* s32 = cbuf + 32 * (g * LDF + l);
+                            const float2 ra2 = make_float2(ra, ra);
+#pragma unroll
+                            for (int c = 0; c < 32; c += 4) {
+                                const float4 s4 = *reinterpret_cast<const float4*>(s32 + c);
+                                const float2 s01 = __fmul2_rn(ra2, make_float2(s4.x, s4.y));
+                                const float2 s23 = __fmul2_rn(ra2, make_float2(s4.z, s4.w));
+                                fma2(a[c], a[c + 1], __uint_as_float(r[l][c]), __uint_as_float(r[l][c + 1]), s01.x,
+                                     s01.y);
+                                fma2(a[c + 2], a[c + 3], __uint_as_float(r[l][c + 2]), __uint_as_float(r[l][c + 3]),
+                                     s23.x, s23.y);
+                            }
                         }
                     }
                 }
@@ -728,11 +795,37 @@ __global__ void __launch_bounds__(320, 1)
     }
 }
 
-// launches the promotion kernel for scale layout SM (1: BN 256, 3: BN 128)
+// Registers a thread of `kern` is launched with (the compiled count, in the
+// allocation unit of 8), queried once per kernel.
+static cudaError_t launch_regs(const void* kern, int* regs)
+{
+    static std::mutex mu;
+    static const void* done_kern[16];
+    static int done_regs[16];
+    static int n_done = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_done; ++i)
+        if (done_kern[i] == kern) {
+            *regs = done_regs[i];
+            return cudaSuccess;
+        }
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    *regs = (fa.numRegs + 7) & ~7;
+    if (n_done < 16) {
+        done_kern[n_done] = kern;
+        done_regs[n_done] = *regs;
+        ++n_done;
+    }
+    return cudaSuccess;
+}
+
+// launches the promotion kernel for scale layout SM (1 or 3)
 template <int SM>
 static cudaError_t launch_promote(const GemmArgs& g, const EpiParams& p, cudaStream_t st, int sms, const char** why)
 {
-    constexpr int BN = SM == 1 ? 256 : 128, ST = kPromoStages(BN);
+    constexpr int BN = kPromoBN;
     CUtensorMap ta, tb;
     if (!encode_tmap_2d(&ta, 0, g.A, g.K, g.M, 128u, BM) || !encode_tmap_2d(&tb, 0, g.B, g.K, g.N, 128u, BN)) {
         *why = "cuTensorMapEncodeTiled failed";
@@ -746,12 +839,21 @@ static cudaError_t launch_promote(const GemmArgs& g, const EpiParams& p, cudaStr
     idesc |= (uint32_t)g.b_format << 10;
     idesc |= (uint32_t)(BN >> 3) << 17;
     idesc |= (uint32_t)(BM >> 4) << 24;
-    const int smem = Smem<BN, ST, 512 / BN>::BYTES;
-    auto kern = g.d_dtype == kBF16 ? k_gemm_promote<BN, ST, true, SM> : k_gemm_promote<BN, ST, false, SM>;
-    cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(kern), smem);
+    const int smem = PromoSmem::BYTES;
+    auto kern = g.d_dtype == kBF16 ? k_gemm_promote<true, SM> : k_gemm_promote<false, SM>;
+    // the warpgroups' setmaxnreg shares must fit in what the CTA is launched
+    // with, or the raising warpgroups would wait for registers forever
+    int regs = 0;
+    cudaError_t e = launch_regs(reinterpret_cast<const void*>(kern), &regs);
+    if (e != cudaSuccess) return e;
+    if (regs < kPromoLaunchRegs) {
+        *why = "promotion kernel compiled with fewer registers than its warpgroup split needs";
+        return cudaErrorInvalidConfiguration;
+    }
+    e = smem_attr_once(reinterpret_cast<const void*>(kern), smem);
     if (e != cudaSuccess) return e;
     const int grid = tiles < sms ? tiles : sms;
-    launch_k(kern, grid, 320, smem, st, ta, tb, p, idesc, sched);
+    launch_k(kern, grid, kPromoThreads, smem, st, ta, tb, p, idesc, sched);
     return cudaGetLastError();
 }
 
