@@ -1039,15 +1039,22 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
             const int row0 = mb * BM + quarter * 32;
             const uint32_t taddr =
                 tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * BN + part * COLS);
-#pragma unroll 1
-            for (int c = 0; c < COLS; c += 32) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(taddr + (uint32_t)c, r);
-                tmem_ld_wait();
-                float v[32];
-                const int col0 = nb * BN + part * COLS + c;
+            // The whole slice comes out in one wait and the accumulator is
+            // released before any conversion or store: with one accumulator
+            // the next tile's MMAs wait for this release, not for the stores.
+            uint32_t r[COLS / 32][32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+            for (int c = 0; c < COLS / 32; ++c) tmem_ld_32x32b_x32(taddr + (uint32_t)(32 * c), r[c]);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&aempty[b]);
+#pragma unroll
+            for (int c = 0; c < COLS / 32; ++c) {
+                float v[32];
+                const int col0 = nb * BN + part * COLS + 32 * c;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[c][j]);
                 if (p.bias) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
@@ -1057,9 +1064,6 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                 for (int h = 0; h < 32 / SC; ++h)
                     stage_store<OUT_BF16>(stg, &tmD, v + h * SC, col0 + h * SC, row0, p.M, p.N, lane);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&aempty[b]);
         }
         stage_store_drain(lane);
     }
