@@ -2,12 +2,15 @@
 """Benchmark of the FP8 scaled-linear hot path on GB300.
 
 One step = one pass of the whole path over one batch of the large FFN
-training step (M = 16384 tokens, 4096 -> 14336 and 14336 -> 4096 linears,
-HYBRID per-tensor delayed scaling, amax history 16): for each linear,
-quantize x and W (E4M3, with transposed copies), forward GEMM, quantize dy
-(E5M2, with transposed copy), dgrad GEMM, wgrad GEMM; then the end-of-step
-scale update of all six tensor roles.  Every step runs in this library's
-kernels through its C ABI.
+training step (M = 16384 tokens, HYBRID per-tensor delayed scaling, amax
+history 16): x -> linear 0 (4096 -> 14336) -> y0 -> linear 1 (14336 -> 4096)
+-> y1, then back: the upstream gradient dy of y1 -> linear 1's dgrad and
+wgrad -> dx1, which is linear 0's output gradient -> linear 0's dgrad and
+wgrad.  Per linear: quantize its input and W (E4M3, with transposed copies),
+forward GEMM, quantize its output gradient (E5M2, with transposed copy),
+dgrad GEMM, wgrad GEMM; then the end-of-step scale update of all six tensor
+roles.  The step's inputs are x and dy; y0 and dx1 stay on the device.
+Every step runs in this library's kernels through its C ABI.
 
 Metric: FP8 linear TFLOP/s = GEMM FLOPs (2MNK per GEMM, six per step) per
 second of the whole step (quantize + GEMM + scale update), with the inputs
@@ -169,7 +172,11 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- our arm
 class FFNStep:
-    """Device buffers and the timed step of workload 5."""
+    """Device buffers and the timed step of workload 5: one FFN block of two
+    linears, linear 1 reading linear 0's output and linear 0's output
+    gradient being linear 1's dgrad (no activation function between them:
+    the path's arithmetic is the linears').  A step's inputs are x (linear
+    0's input) and dy (the gradient of linear 1's output)."""
 
     def __init__(self, device, n_input_sets: int):
         import scaled_quantize_gemm_gb300 as sq
@@ -179,12 +186,9 @@ class FFNStep:
         self.M = M
         self.lin = [(l.in_features, l.out_features) for l in WK.linears]      # (K, N)
         self.W = [wl.linear_w(5, li, N, K, device) for li, (K, N) in enumerate(self.lin)]
-        self.inputs = []
-        for s in range(n_input_sets):
-            per = []
-            for li, (K, N) in enumerate(self.lin):
-                per.append((wl.linear_x(5, li, s, M, K, device), wl.linear_dy(5, li, s, M, N, device)))
-            self.inputs.append(per)
+        K0, N1 = self.lin[0][0], self.lin[-1][1]
+        self.inputs = [(wl.linear_x(5, 0, s, M, K0, device), wl.linear_dy(5, len(self.lin) - 1, s, M, N1, device))
+                       for s in range(n_input_sets)]
         u8 = dict(dtype=torch.uint8, device=device)
         self.buf = []
         for li, (K, N) in enumerate(self.lin):
@@ -217,9 +221,12 @@ class FFNStep:
 
     def step(self, s: int, ev=None):
         """One pass of the hot path through the granular C-ABI calls; `ev`
-        (a list) receives (kind, start_event, end_event) per call."""
+        (a list) receives (kind, start_event, end_event) per call.  Cast
+        order: x, W0, y0 (linear 1's input), W1, dy, dx1 (linear 0's output
+        gradient)."""
         sq = self.sq
-        inp = self.inputs[s % len(self.inputs)]
+        x, dy = self.inputs[s % len(self.inputs)]
+        L = len(self.lin)
 
         def rec(kind, fn):
             if ev is None:
@@ -231,22 +238,28 @@ class FFNStep:
             b.record()
             ev.append((kind, a, b))
 
-        for li, (K, N) in enumerate(self.lin):
-            x, dy = inp[li]
+        xin = x
+        for li in range(L):                          # forward, first linear first
             B = self.buf[li]
-            sx, sw, sd = 3 * li, 3 * li + 1, 3 * li + 2
-            rec("quant", lambda: sq.fp8_quantize(x, sq.E4M3, sq.TENSOR, B["qx"], qT=B["qxT"],
+            sx, sw = 3 * li, 3 * li + 1
+            rec("quant", lambda: sq.fp8_quantize(xin, sq.E4M3, sq.TENSOR, B["qx"], qT=B["qxT"],
                                                  delayed_state=self.st(sx), history_len=H))
             rec("quant", lambda: sq.fp8_quantize(self.W[li], sq.E4M3, sq.TENSOR, B["qw"], qT=B["qwT"],
                                                  delayed_state=self.st(sw), history_len=H))
             rec("gemm", lambda: sq.fp8_gemm(B["qx"], sq.E4M3, self.s(sx), sq.TENSOR,
                                             B["qw"], sq.E4M3, self.s(sw), sq.TENSOR, B["y"]))
-            rec("quant", lambda: sq.fp8_quantize(dy, sq.E5M2, sq.TENSOR, B["qdy"], qT=B["qdyT"],
+            xin = B["y"]
+        dyin = dy
+        for li in reversed(range(L)):                # backward, last linear first
+            B = self.buf[li]
+            sx, sw, sd = 3 * li, 3 * li + 1, 3 * li + 2
+            rec("quant", lambda: sq.fp8_quantize(dyin, sq.E5M2, sq.TENSOR, B["qdy"], qT=B["qdyT"],
                                                  delayed_state=self.st(sd), history_len=H))
             rec("gemm", lambda: sq.fp8_gemm(B["qdy"], sq.E5M2, self.s(sd), sq.TENSOR,
                                             B["qwT"], sq.E4M3, self.s(sw), sq.TENSOR, B["dx"]))
             rec("gemm", lambda: sq.fp8_gemm(B["qdyT"], sq.E5M2, self.s(sd), sq.TENSOR,
                                             B["qxT"], sq.E4M3, self.s(sx), sq.TENSOR, B["dw"]))
+            dyin = B["dx"]
         rec("update", lambda: sq.fp8_update_scale(self.states, 6, H, self.formats))
 
     KERNELS_PER_STEP = 13   # 6 casts + 6 GEMMs + 1 scale update
@@ -263,23 +276,24 @@ class FFNStep:
         sq = self.sq
         main = torch.cuda.current_stream()
         if not hasattr(self, "_e2e"):
-            dev_in = [[(torch.empty_like(x), torch.empty_like(dy)) for (x, dy) in self.inputs[0]] for _ in range(2)]
+            x0, dy0 = self.inputs[0]
+            dev_in = [(torch.empty_like(x0), torch.empty_like(dy0)) for _ in range(2)]
             self._e2e = (dev_in, torch.cuda.Stream())
         dev_in, copy = self._e2e
         ready = [torch.cuda.Event(), torch.cuda.Event()]
         free = [torch.cuda.Event(), torch.cuda.Event()]
+        L = len(self.lin)
 
         def issue_copy(s):
             buf = s % 2
-            hs = host_sets[s % len(host_sets)]
+            xh, dyh = host_sets[s % len(host_sets)]
             copy.wait_stream(main) if s < 2 else copy.wait_event(free[buf])
             with torch.cuda.stream(copy):
                 if copy_ev is not None:
                     copy_ev.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
                     copy_ev[-1][0].record()
-                for li, (xh, dyh) in enumerate(hs):
-                    dev_in[buf][li][0].copy_(xh, non_blocking=True)
-                    dev_in[buf][li][1].copy_(dyh, non_blocking=True)
+                dev_in[buf][0].copy_(xh, non_blocking=True)
+                dev_in[buf][1].copy_(dyh, non_blocking=True)
                 if copy_ev is not None:
                     copy_ev[-1][1].record()
             ready[buf].record(copy)
@@ -290,13 +304,21 @@ class FFNStep:
             if s + 1 < steps:
                 issue_copy(s + 1)
             main.wait_event(ready[buf])
-            for li, (K, N) in enumerate(self.lin):
-                xd, dyd = dev_in[buf][li]
+            xd, dyd = dev_in[buf]
+            xin = xd
+            for li in range(L):
                 B = self.buf[li]
-                sq.fp8_linear_fwd(xd, self.W[li], B["y"], B["ws"], x_state=self.st(3 * li),
+                sq.fp8_linear_fwd(xin, self.W[li], B["y"], B["ws"], x_state=self.st(3 * li),
                                   w_state=self.st(3 * li + 1), history_len=H)
-                sq.fp8_linear_bwd(dyd, B["dx"], B["dw"], B["ws"], K, dy_state=self.st(3 * li + 2), history_len=H)
-            free[buf].record(main)
+                xin = B["y"]
+            dyin = dyd
+            for li in reversed(range(L)):
+                B = self.buf[li]
+                sq.fp8_linear_bwd(dyin, B["dx"], B["dw"], B["ws"], self.lin[li][0], dy_state=self.st(3 * li + 2),
+                                  history_len=H)
+                if li == L - 1:
+                    free[buf].record(main)           # the step's device inputs are consumed
+                dyin = B["dx"]
             sq.fp8_update_scale(self.states, 6, H, self.formats)
             states_host.copy_(self.states, non_blocking=True)
 
@@ -358,8 +380,9 @@ def run_ours(args, ws, rank, local):
     quant_ms_step = sum(per["quant"]) / args.steps
     qbytes = b.quant_bytes_per_step()
     quant_gbs = qbytes / (quant_ms_step * 1e-3) / 1e9
-    # the largest cast: x of the second linear / dy of the first (16384 x 14336)
-    big = [per["quant"][i] for i in range(len(per["quant"])) if i % 6 in (2, 3)]
+    # the largest casts (16384 x 14336): y0 as linear 1's input, dx1 as linear
+    # 0's output gradient (positions 2 and 5 of the step's six casts)
+    big = [per["quant"][i] for i in range(len(per["quant"])) if i % 6 in (2, 5)]
     big_bytes = 4 * WK.tokens * 14336
     big_gbs = big_bytes / (statistics.mean(big) * 1e-3) / 1e9
 
@@ -368,23 +391,21 @@ def run_ours(args, ws, rank, local):
     if not args.no_e2e:
         host_sets = []
         for s in range(2):
-            host_sets.append([(x.to("cpu").pin_memory(), dy.to("cpu").pin_memory())
-                              for (x, dy) in b.inputs[s % len(b.inputs)]])
+            x, dy = b.inputs[s % len(b.inputs)]
+            host_sets.append((x.to("cpu").pin_memory(), dy.to("cpu").pin_memory()))
         states_host = torch.empty(b.states.shape, dtype=torch.float32).pin_memory()
-        h2d = sum(x.numel() * x.element_size() + dy.numel() * dy.element_size() for (x, dy) in host_sets[0])
+        h2d = sum(t.numel() * t.element_size() for t in host_sets[0])
         d2h = states_host.numel() * 4
         # the host link alone: one step's inputs copied with nothing else running
-        dev_tmp = [(torch.empty_like(x), torch.empty_like(dy)) for (x, dy) in b.inputs[0]]
+        dev_tmp = [torch.empty_like(t) for t in b.inputs[0]]
         for _ in range(2):
-            for (xh, dyh), (xd, dyd) in zip(host_sets[0], dev_tmp):
-                xd.copy_(xh, non_blocking=True)
-                dyd.copy_(dyh, non_blocking=True)
+            for th, td in zip(host_sets[0], dev_tmp):
+                td.copy_(th, non_blocking=True)
         torch.cuda.synchronize()
         l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         l0.record()
-        for (xh, dyh), (xd, dyd) in zip(host_sets[0], dev_tmp):
-            xd.copy_(xh, non_blocking=True)
-            dyd.copy_(dyh, non_blocking=True)
+        for th, td in zip(host_sets[0], dev_tmp):
+            td.copy_(th, non_blocking=True)
         l1.record()
         torch.cuda.synchronize()
         link_gbs = h2d / (l0.elapsed_time(l1) * 1e-3) / 1e9
@@ -436,10 +457,12 @@ def run_ours(args, ws, rank, local):
             "scaling": "weak", "vs_baseline": None, "dtype": "fp8", "data": "synthetic",
             "config": {"workload": WK.name, "tokens": WK.tokens,
                        "linears": [f"{K}->{N}" for (K, N) in b.lin], "history_len": H,
+                       "chain": "x -> linear 0 -> y0 -> linear 1 -> y1; dy -> linear 1 dgrad -> dx1 -> linear 0",
                        "recipe": "HYBRID per-tensor delayed (E4M3 fwd, E5M2 grads), amax_compute_algo=max",
                        "outputs": "y bf16, dx bf16, dW fp32",
-                       "l2": "no flush: every step reads inputs larger than L2 (128-470 MB each, 10 rotating "
-                             "seeded batches)",
+                       "l2": "no flush: every tensor a step reads is 117-470 MB and is touched once per step, "
+                             "and a step moves several GB, so L2 keeps nothing from one use to the next "
+                             "(10 rotating seeded batches of x and dy)",
                        "parallelism": f"replicas x{ws}"},
             "clocks": clk,
             "e2e": e2e,
@@ -470,14 +493,12 @@ def run_ours(args, ws, rank, local):
 
 # ---------------------------------------------------------------- CPU oracle
 def _oracle_sample_inputs(step: int):
-    """The workload's step at SAMPLE_TOKENS tokens (same recipe, CPU-drawn)."""
-    out = []
-    for li, lin in enumerate(WK.linears):
-        K, N = lin.in_features, lin.out_features
-        x = wl.linear_x(5, li, step, SAMPLE_TOKENS, K, "cpu").float().numpy()
-        dy = wl.linear_dy(5, li, step, SAMPLE_TOKENS, N, "cpu").float().numpy()
-        out.append((x, dy))
-    return out
+    """The workload's step inputs (x, dy) at SAMPLE_TOKENS tokens (same
+    recipe, CPU-drawn)."""
+    K0, N1 = WK.linears[0].in_features, WK.linears[-1].out_features
+    x = wl.linear_x(5, 0, step, SAMPLE_TOKENS, K0, "cpu").float().numpy()
+    dy = wl.linear_dy(5, len(WK.linears) - 1, step, SAMPLE_TOKENS, N1, "cpu").float().numpy()
+    return x, dy
 
 
 def _oracle_weights():
@@ -485,18 +506,33 @@ def _oracle_weights():
             for li, l in enumerate(WK.linears)]
 
 
+def _bf16(a):
+    """Round to bf16 (the device path's activation and gradient dtype)."""
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).float().numpy()
+
+
 def oracle_sample_step(o, weights, inputs, states):
     """One step of the workload through the CPU oracle at SAMPLE_TOKENS
-    tokens: quantize x, W, dy (delayed), forward, dgrad, wgrad, update.
-    Returns the GEMM FLOPs processed."""
+    tokens, chained as on the device: forward through both linears (each
+    quantizing its input and W, delayed), then backward from the last linear
+    (quantize the output gradient, dgrad, wgrad), each output rounded to
+    bf16 before it feeds the next linear; then the scale update.  Returns the
+    GEMM FLOPs processed."""
+    x, dy = inputs
     flops = 0
-    for li, (x, dy) in enumerate(inputs):
-        sx, sw, sd = states[3 * li], states[3 * li + 1], states[3 * li + 2]
-        qx, fx, qw, fw, _ = o.linear_fwd_delayed(x, weights[li], sx, sw)
-        o.linear_bwd_delayed(dy, sd, o.E5M2, qx, fx, qw, fw)
-        M, K = x.shape
-        N = weights[li].shape[0]
-        flops += 3 * 2 * M * N * K
+    saved = []
+    xin = x
+    for li, w in enumerate(weights):
+        qx, fx, qw, fw, r = o.linear_fwd_delayed(xin, w, states[3 * li], states[3 * li + 1])
+        saved.append((qx, fx, qw, fw))
+        M, K = xin.shape
+        flops += 3 * 2 * M * w.shape[0] * K
+        xin = _bf16(r)
+    dyin = dy
+    for li in reversed(range(len(weights))):
+        qx, fx, qw, fw = saved[li]
+        _, _, dX, _ = o.linear_bwd_delayed(dyin, states[3 * li + 2], o.E5M2, qx, fx, qw, fw)
+        dyin = _bf16(dX)
     for i, st in enumerate(states):
         o.update_scale(st, o.E5M2 if i % 3 == 2 else o.E4M3)
     return flops
