@@ -66,7 +66,7 @@ KERNEL_SOURCES = {   # file, [(start marker or None = file start, end marker)]: 
 }
 TRAFFIC = {
     "k_gemm_tensor_pair": {"sha": "60e46bcbee106212", "bytes": 971203072},
-    "k_cast_tensor_T": {"sha": "10634066b786eb60", "bytes": 891757312},
+    "k_cast_tensor_T": {"sha": "68f2b59d0aab2c82", "bytes": 892547584},
 }
 
 

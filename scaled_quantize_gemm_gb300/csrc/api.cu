@@ -457,18 +457,17 @@ FP8SQ_API int fp8_linear_fwd(const void* x, const void* w, int64_t M, int64_t N,
     g.B = ws + L.qw;
     if (gran == FP8SQ_TENSOR) {
         float* scal = reinterpret_cast<float*>(ws + L.scal);   // sx, sw, sdy, ax, aw, ady
-        // x
+        // x and W in one launch (current scaling: one more for both amaxes)
         qa.x = x; qa.rows = M; qa.cols = K; qa.gran = fp8sq::kTensor;
         qa.q = ws + L.qx; qa.qT = ws + L.qxT;
         qa.state = x_state; qa.history_len = H;
         qa.scales = &scal[0]; qa.amax = delayed ? nullptr : &scal[3];
-        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: quantize x"))) return r;
-        // W
-        qa.x = w; qa.rows = N; qa.cols = K;
-        qa.q = ws + L.qw; qa.qT = ws + L.qwT;
-        qa.state = w_state;
-        qa.scales = &scal[1]; qa.amax = delayed ? nullptr : &scal[4];
-        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: quantize w"))) return r;
+        fp8sq::QuantArgs qw = qa;
+        qw.x = w; qw.rows = N; qw.cols = K;
+        qw.q = ws + L.qw; qw.qT = ws + L.qwT;
+        qw.state = w_state;
+        qw.scales = &scal[1]; qw.amax = delayed ? nullptr : &scal[4];
+        if ((r = cuda_status(fp8sq::launch_quantize_pair(qa, qw, st, sms), "fp8_linear_fwd: quantize x and w"))) return r;
         // (delayed: each cast writes the dequantisation scale it used into
         // scal[], kept for the backward pass)
         g.mode = 0;

@@ -34,6 +34,9 @@ struct QuantArgs {
 // quantize.cu
 cudaError_t launch_amax(const QuantArgs& a, cudaStream_t st, int sms);    // writes a.amax per unit
 cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st, int sms);
+// two per-tensor casts with transposed copies (same dtype, format and
+// recipe) in one launch; other argument pairs go through launch_quantize twice
+cudaError_t launch_quantize_pair(const QuantArgs& a, const QuantArgs& b, cudaStream_t st, int sms);
 cudaError_t launch_scale_init(float* states, int n, int H, cudaStream_t st);
 cudaError_t launch_update_scale(float* states, int n, int H, const int* formats, int algo, cudaStream_t st);
 // LayerNorm of bf16 x [rows][cols] fused into the delayed per-tensor cast

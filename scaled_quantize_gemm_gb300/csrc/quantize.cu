@@ -213,16 +213,15 @@ __device__ __forceinline__ uint32_t block_max_bits(uint32_t v, uint32_t* red)
 constexpr int kFlatThreads = 256;
 constexpr int kFlatUnroll = 4;
 
+// amax of one tensor over blocks [bid, bid + nblk, ...) of a grid-stride loop
 template <int DT>
-__global__ void __launch_bounds__(kFlatThreads) k_amax_tensor(const void* __restrict__ x, int64_t n,
-                                                              float* __restrict__ amax_out)
+__device__ __forceinline__ void amax_tensor_body(const void* __restrict__ x, int64_t n, float* __restrict__ amax_out,
+                                                 int64_t bid, int64_t nblk, uint32_t* red)
 {
-    pdl_enter();
-    __shared__ uint32_t red[kFlatThreads / 32];
     const int64_t nch = n / 8;
     uint32_t mx = 0;
-    const int64_t stride = (int64_t)gridDim.x * kFlatThreads * kFlatUnroll;
-    for (int64_t c0 = (int64_t)blockIdx.x * kFlatThreads * kFlatUnroll; c0 < nch; c0 += stride) {
+    const int64_t stride = nblk * kFlatThreads * kFlatUnroll;
+    for (int64_t c0 = bid * kFlatThreads * kFlatUnroll; c0 < nch; c0 += stride) {
         Vec8<DT> v[kFlatUnroll];
 #pragma unroll
         for (int u = 0; u < kFlatUnroll; ++u) {
@@ -232,8 +231,8 @@ __global__ void __launch_bounds__(kFlatThreads) k_amax_tensor(const void* __rest
 #pragma unroll
         for (int u = 0; u < kFlatUnroll; ++u) mx = max(mx, v[u].absmax_bits());
     }
-    // ragged tail (n % 8 elements): block 0, first threads
-    if (blockIdx.x == 0 && threadIdx.x < (n & 7)) {
+    // ragged tail (n % 8 elements): the job's first block, first threads
+    if (bid == 0 && threadIdx.x < (n & 7)) {
         int64_t i = nch * 8 + threadIdx.x;
         uint32_t b = (DT == kBF16) ? ((uint32_t)(static_cast<const uint16_t*>(x)[i] & 0x7FFFu) << 16)
                                    : (__float_as_uint(static_cast<const float*>(x)[i]) & 0x7FFFFFFFu);
@@ -241,6 +240,33 @@ __global__ void __launch_bounds__(kFlatThreads) k_amax_tensor(const void* __rest
     }
     uint32_t r = block_max_bits<kFlatThreads / 32>(mx, red);
     if (threadIdx.x == 0) atomic_max_bits(amax_out, r);
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kFlatThreads) k_amax_tensor(const void* __restrict__ x, int64_t n,
+                                                              float* __restrict__ amax_out)
+{
+    pdl_enter();
+    __shared__ uint32_t red[kFlatThreads / 32];
+    amax_tensor_body<DT>(x, n, amax_out, blockIdx.x, gridDim.x, red);
+}
+
+// The amaxes of two tensors in one launch: blocks [0, blocks_a) reduce a,
+// the rest reduce b (a linear layer's x and W under current scaling).
+struct AmaxJob {
+    const void* x;
+    int64_t n;
+    float* amax;
+};
+template <int DT>
+__global__ void __launch_bounds__(kFlatThreads) k_amax_tensor2(AmaxJob a, AmaxJob b, int blocks_a)
+{
+    pdl_enter();
+    __shared__ uint32_t red[kFlatThreads / 32];
+    if ((int)blockIdx.x < blocks_a)
+        amax_tensor_body<DT>(a.x, a.n, a.amax, blockIdx.x, blocks_a, red);
+    else
+        amax_tensor_body<DT>(b.x, b.n, b.amax, blockIdx.x - blocks_a, gridDim.x - blocks_a, red);
 }
 
 // Cast pass of per-tensor scaling without a transposed copy.
@@ -356,28 +382,27 @@ struct LnParams {
 // loads in flight: measured on the GB300 at 16384 x 14336 (delayed E5M2,
 // identical codes), 144.2 us = 6.5 TB/s against 168.2 us for a persistent
 // TMA-fed ring with 8 consumer warps per SM.
-template <int DT, int FMT, bool DELAYED, bool LN = false>
-__global__ void __launch_bounds__(256) k_cast_tensor_T(const void* __restrict__ x, int64_t R, int64_t C,
-                                                       uint8_t* __restrict__ q, uint8_t* __restrict__ qT,
-                                                       float* state, int H, const float* amax_in,
-                                                       float* s_out, float* amax_out,
-                                                       unsigned long long* sat, LnParams ln)
+// One 128 x 128 tile (tile_c, tile_r) of the cast; red: 8 words of shared memory.
+template <int DT, int FMT, bool DELAYED, bool LN>
+__device__ __forceinline__ void cast_tile_T(const void* __restrict__ x, int64_t R, int64_t C,
+                                            uint8_t* __restrict__ q, uint8_t* __restrict__ qT, float* state, int H,
+                                            const float* amax_in, float* s_out, float* amax_out,
+                                            unsigned long long* sat, const LnParams& ln, int64_t tile_c,
+                                            int64_t tile_r, uint32_t* red)
 {
-    pdl_enter();
-    __shared__ uint32_t red[8];
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    const int64_t c0 = (int64_t)blockIdx.x * 128 + ((w & 3) * 4 + (l & 3)) * 8;
-    const int64_t r0 = (int64_t)blockIdx.y * 128 + ((w >> 2) * 8 + (l >> 2)) * 8;
+    const int64_t c0 = tile_c * 128 + ((w & 3) * 4 + (l & 3)) * 8;
+    const int64_t r0 = tile_r * 128 + ((w >> 2) * 8 + (l >> 2)) * 8;
     float m, s;
     if (DELAYED) {
         m = state[H];
         s = 0.0f;
         // the dequantisation scale this cast uses (the state's s is updated
         // only at the end of the step)
-        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && s_out) *s_out = state[H + 1];
+        if (tile_c == 0 && tile_r == 0 && threadIdx.x == 0 && s_out) *s_out = state[H + 1];
     } else {
         current_scale<FMT>(__float_as_uint(*amax_in), m, s);
-        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && s_out) *s_out = s;
+        if (tile_c == 0 && tile_r == 0 && threadIdx.x == 0 && s_out) *s_out = s;
     }
     const bool ok = (r0 < R) && (c0 < C);    // rows, cols % 16 == 0: whole 8 x 8 groups
     Vec8<DT> v[8];
@@ -443,6 +468,50 @@ __global__ void __launch_bounds__(256) k_cast_tensor_T(const void* __restrict__ 
             if (amax_out) atomic_max_bits(amax_out, r);
         }
     }
+}
+
+template <int DT, int FMT, bool DELAYED, bool LN = false>
+__global__ void __launch_bounds__(256) k_cast_tensor_T(const void* __restrict__ x, int64_t R, int64_t C,
+                                                       uint8_t* __restrict__ q, uint8_t* __restrict__ qT,
+                                                       float* state, int H, const float* amax_in,
+                                                       float* s_out, float* amax_out,
+                                                       unsigned long long* sat, LnParams ln)
+{
+    pdl_enter();
+    __shared__ uint32_t red[8];
+    cast_tile_T<DT, FMT, DELAYED, LN>(x, R, C, q, qT, state, H, amax_in, s_out, amax_out, sat, ln, blockIdx.x,
+                                      blockIdx.y, red);
+}
+
+// Two per-tensor casts of the same kind in one launch (a linear layer's x
+// and W): blocks [0, tiles_a) take a's tiles in row-major tile order, the
+// rest b's.  At small layers each cast alone is one partial wave; one launch
+// saves a kernel's prologue and tail.
+struct CastJob {
+    const void* x;
+    int64_t R, C;
+    uint8_t* q;
+    uint8_t* qT;
+    float* state;          // delayed
+    const float* amax_in;  // current
+    float* s_out;
+    float* amax_out;
+};
+template <int DT, int FMT, bool DELAYED>
+__global__ void __launch_bounds__(256) k_cast_tensor_T2(CastJob a, CastJob b, int64_t tiles_a, int H,
+                                                        unsigned long long* sat)
+{
+    pdl_enter();
+    __shared__ uint32_t red[8];
+    // field by field, so the parameters are read in place
+    const bool first = (int64_t)blockIdx.x < tiles_a;
+    const int64_t t = first ? (int64_t)blockIdx.x : (int64_t)blockIdx.x - tiles_a;
+    const int64_t R = first ? a.R : b.R, C = first ? a.C : b.C;
+    const int64_t tiles_c = (C + 127) / 128;
+    cast_tile_T<DT, FMT, DELAYED, false>(first ? a.x : b.x, R, C, first ? a.q : b.q, first ? a.qT : b.qT,
+                                         first ? a.state : b.state, H, first ? a.amax_in : b.amax_in,
+                                         first ? a.s_out : b.s_out, first ? a.amax_out : b.amax_out, sat, LnParams(),
+                                         t % tiles_c, t / tiles_c, red);
 }
 
 // MX scales: the canonical layout is u8 [rows][cols/32]; the tiled layout
@@ -1079,6 +1148,54 @@ cudaError_t launch_quantize(const QuantArgs& a, cudaStream_t st, int sms)
     if (a.x_dtype == kBF16)
         return a.format == kE4M3 ? quant_dt_fmt<kBF16, kE4M3>(a, st, sms) : quant_dt_fmt<kBF16, kE5M2>(a, st, sms);
     return a.format == kE4M3 ? quant_dt_fmt<kF32, kE4M3>(a, st, sms) : quant_dt_fmt<kF32, kE5M2>(a, st, sms);
+}
+
+// Two per-tensor casts with transposed copies in one launch (plus, for
+// current scaling, one launch for both amaxes): a linear layer's x and W.
+template <int DT, int FMT>
+static cudaError_t quant_pair_dt_fmt(const QuantArgs& a, const QuantArgs& b, cudaStream_t st, int sms)
+{
+    const bool delayed = a.state != nullptr;
+    // the amax slots start at zero (one memset when they are adjacent)
+    auto clear = [&](float* pa, float* pb) -> cudaError_t {
+        if (pa && pb && pb == pa + 1) return cudaMemsetAsync(pa, 0, 2 * sizeof(float), st);
+        if (pa && cudaMemsetAsync(pa, 0, sizeof(float), st) != cudaSuccess) return cudaGetLastError();
+        if (pb && cudaMemsetAsync(pb, 0, sizeof(float), st) != cudaSuccess) return cudaGetLastError();
+        return cudaSuccess;
+    };
+    if (clear(a.amax, b.amax) != cudaSuccess) return cudaGetLastError();
+    const int64_t na = a.rows * a.cols, nb = b.rows * b.cols;
+    if (!delayed) {
+        const int ga = flat_grid(na / 8, sms), gb = flat_grid(nb / 8, sms);
+        launch_k(k_amax_tensor2<DT>, ga + gb, kFlatThreads, 0, st, AmaxJob{a.x, na, a.amax}, AmaxJob{b.x, nb, b.amax}, ga);
+    }
+    const int64_t tiles_a = ((a.cols + 127) / 128) * ((a.rows + 127) / 128);
+    const int64_t tiles_b = ((b.cols + 127) / 128) * ((b.rows + 127) / 128);
+    const CastJob ja{a.x, a.rows, a.cols, a.q, a.qT, a.state, delayed ? nullptr : a.amax, static_cast<float*>(a.scales),
+                     delayed ? a.amax : nullptr};
+    const CastJob jb{b.x, b.rows, b.cols, b.q, b.qT, b.state, delayed ? nullptr : b.amax, static_cast<float*>(b.scales),
+                     delayed ? b.amax : nullptr};
+    const unsigned grid = (unsigned)(tiles_a + tiles_b);
+    if (delayed)
+        launch_k(k_cast_tensor_T2<DT, FMT, true>, grid, 256, 0, st, ja, jb, tiles_a, a.history_len, a.sat);
+    else
+        launch_k(k_cast_tensor_T2<DT, FMT, false>, grid, 256, 0, st, ja, jb, tiles_a, 0, a.sat);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_pair(const QuantArgs& a, const QuantArgs& b, cudaStream_t st, int sms)
+{
+    const bool same = a.gran == kTensor && b.gran == kTensor && a.x_dtype == b.x_dtype && a.format == b.format &&
+                      a.qT && b.qT && (a.state != nullptr) == (b.state != nullptr) &&
+                      (!a.state || a.history_len == b.history_len) && (a.state || (a.amax && b.amax)) &&
+                      a.sat == b.sat;
+    if (!same || a.rows * a.cols == 0 || b.rows * b.cols == 0 || a.rows % 8 || a.cols % 8 || b.rows % 8 || b.cols % 8) {
+        cudaError_t e = launch_quantize(a, st, sms);
+        return e != cudaSuccess ? e : launch_quantize(b, st, sms);
+    }
+    if (a.x_dtype == kBF16)
+        return a.format == kE4M3 ? quant_pair_dt_fmt<kBF16, kE4M3>(a, b, st, sms) : quant_pair_dt_fmt<kBF16, kE5M2>(a, b, st, sms);
+    return a.format == kE4M3 ? quant_pair_dt_fmt<kF32, kE4M3>(a, b, st, sms) : quant_pair_dt_fmt<kF32, kE5M2>(a, b, st, sms);
 }
 
 cudaError_t launch_scale_init(float* states, int n, int H, cudaStream_t st)
