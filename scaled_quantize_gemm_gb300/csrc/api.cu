@@ -132,6 +132,53 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int gran)
     return L;
 }
 
+// A non-blocking side stream and its fork / join events, one set per host
+// thread and device: a caller's stream forks work onto it and waits for it
+// again within one call, so no two calls share a set concurrently.  Created
+// on first use outside stream capture (while `st` is being captured, a call
+// without a set yet gets none and runs serially) and kept for the life of the
+// thread.
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+int side_stream(cudaStream_t st, SideStream** out)
+{
+    thread_local SideStream per_dev[64];
+    *out = nullptr;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return fail(FP8SQ_ERR_CUDA, "no usable CUDA device for the side stream");
+    }
+    SideStream& ss = per_dev[dev];
+    if (!ss.s) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+            cudaGetLastError();
+            return FP8SQ_OK;
+        }
+        if (cs != cudaStreamCaptureStatusNone) return FP8SQ_OK;
+        cudaStream_t s = nullptr;
+        cudaEvent_t fork = nullptr, join = nullptr;
+        if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
+            e = cudaGetLastError();
+            if (join) cudaEventDestroy(join);
+            if (fork) cudaEventDestroy(fork);
+            if (s) cudaStreamDestroy(s);
+            return fail(FP8SQ_ERR_CUDA, "cannot create the side stream (%s)", cudaGetErrorString(e));
+        }
+        ss.s = s;
+        ss.fork = fork;
+        ss.join = join;
+    }
+    *out = &ss;
+    return FP8SQ_OK;
+}
+
 }  // namespace
 
 namespace fp8sq {
@@ -144,6 +191,7 @@ int api_fail(int code, const char* fmt, ...)
     return code;
 }
 int api_check_device(int* sms) { return check_device(sms); }
+
 }  // namespace fp8sq
 
 extern "C" {
@@ -562,6 +610,21 @@ FP8SQ_API int fp8_linear_bwd(const void* dy, int64_t M, int64_t N, int64_t K, in
         dg.mode = wg.mode = 2;
         dg.a_scale = ws + L.sdy; dg.b_scale = ws + L.swT;
         wg.a_scale = ws + L.sdyT; wg.b_scale = ws + L.sxT;
+    }
+    // dgrad and wgrad are independent.  When both persistent grids fit on the
+    // device at once (small layers, where each fills only part of the SMs),
+    // wgrad runs on a side stream forked from `st` and joined back into it,
+    // so the two share the device; otherwise they run one after the other.
+    const int cd = fp8sq::gemm_ctas(dg, sms), cw = fp8sq::gemm_ctas(wg, sms);
+    SideStream* side = nullptr;
+    if (cd > 0 && cw > 0 && cd + cw <= sms && (r = side_stream(st, &side))) return r;
+    if (side) {
+        if ((r = cuda_status(cudaEventRecord(side->fork, st), "fp8_linear_bwd: fork"))) return r;
+        if ((r = cuda_status(cudaStreamWaitEvent(side->s, side->fork, 0), "fp8_linear_bwd: fork"))) return r;
+        if ((r = cuda_status(fp8sq::launch_gemm(dg, st, sms, &why), why ? why : "fp8_linear_bwd: dgrad"))) return r;
+        if ((r = cuda_status(fp8sq::launch_gemm(wg, side->s, sms, &why), why ? why : "fp8_linear_bwd: wgrad"))) return r;
+        if ((r = cuda_status(cudaEventRecord(side->join, side->s), "fp8_linear_bwd: join"))) return r;
+        return cuda_status(cudaStreamWaitEvent(st, side->join, 0), "fp8_linear_bwd: join");
     }
     if ((r = cuda_status(fp8sq::launch_gemm(dg, st, sms, &why), why ? why : "fp8_linear_bwd: dgrad"))) return r;
     return cuda_status(fp8sq::launch_gemm(wg, st, sms, &why), why ? why : "fp8_linear_bwd: wgrad");

@@ -1222,6 +1222,29 @@ static cudaError_t pair_clusters(KernelT kern, int variant, int smem, int* clust
     return cudaSuccess;
 }
 
+// SMs a launch of g occupies (its persistent grid: one CTA per SM), -1 if
+// that cannot be determined.  Lets a caller run two independent GEMMs side by
+// side when both grids fit on the device at once.
+int gemm_ctas(const GemmArgs& g, int sms)
+{
+    if (g.M == 0 || g.N == 0 || g.K == 0) return 0;
+    const bool pair = g.mode == 0;   // the per-tensor kernel runs on CTA pairs
+    if (pair) {
+        const int64_t tiles = ((g.M + 2 * BM - 1) / (2 * BM)) * ((g.N + kPairBN - 1) / kPairBN);
+        const bool bf16 = g.d_dtype == kBF16;
+        int clusters = 0;
+        if (pair_clusters(bf16 ? k_gemm_tensor_pair<true> : k_gemm_tensor_pair<false>, bf16 ? 1 : 0,
+                          PairSmem::BYTES, &clusters) != cudaSuccess || clusters < 1) {
+            cudaGetLastError();
+            return -1;
+        }
+        return 2 * (int)(tiles < clusters ? tiles : clusters);
+    }
+    // the promotion and MX kernels: one CTA per 128 x 256 tile
+    const int64_t tiles = ((g.M + BM - 1) / BM) * ((g.N + 255) / 256);
+    return (int)(tiles < sms ? tiles : sms);
+}
+
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char** why)
 {
     *why = nullptr;

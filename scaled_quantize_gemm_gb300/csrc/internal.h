@@ -60,6 +60,7 @@ struct GemmArgs {
 
 // gemm.cu
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char** why);
+int gemm_ctas(const GemmArgs& g, int sms);   // SMs its persistent grid occupies, -1 if unknown
 int read_device_error(int clear);   // 0 or the GEMM kernels' device error word
 // launches a kernel whose bounded wait is made to run out (failure-path test)
 cudaError_t launch_selftest_wait(uint64_t limit_ns, int* waited_out, cudaStream_t st);
