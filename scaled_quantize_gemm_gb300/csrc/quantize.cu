@@ -542,9 +542,10 @@ __device__ __forceinline__ int64_t mx_tiled_offset(int64_t r, int64_t t, int64_t
 // codes: both operands of a fine-grained linear's products from one read of
 // x.  A row's 32 columns are four lanes of one warp; its 128 columns are four
 // warps (shuffles over l ^ 1, l ^ 2, then shared memory), and thread
-// 128 + r computes row r's 1x128 scale.
+// 128 + r computes row r's 1x128 scale.  Three CTAs per SM (80 registers),
+// except ROWQ with MX-32 rows: two (128 registers; at three it spills).
 template <int FMT, int UNIT, bool ROWQ = false>
-__global__ void __launch_bounds__(256, ROWQ ? 2 : 3) k_quant_col_block(const void* __restrict__ x, int64_t R, int64_t C,
+__global__ void __launch_bounds__(256, ROWQ && UNIT == 32 ? 2 : 3) k_quant_col_block(const void* __restrict__ x, int64_t R, int64_t C,
                                                          uint8_t* __restrict__ q, uint8_t* __restrict__ qT,
                                                          void* scales, void* rscales, unsigned long long* sat)
 {
@@ -639,12 +640,6 @@ __global__ void __launch_bounds__(256, ROWQ ? 2 : 3) k_quant_col_block(const voi
         m[4] = m1.x; m[5] = m1.y; m[6] = m1.z; m[7] = m1.w;
         const uint2 fl = *reinterpret_cast<const uint2*>(&colflag[cl]);   // the 8 columns' flags
         maysat = (fl.x | fl.y) != 0u;
-        if (ROWQ) {
-            const float4 q0 = *reinterpret_cast<const float4*>(&rowm[rl]);
-            const float4 q1 = *reinterpret_cast<const float4*>(&rowm[rl + 4]);
-            rm[0] = q0.x; rm[1] = q0.y; rm[2] = q0.z; rm[3] = q0.w;
-            rm[4] = q1.x; rm[5] = q1.y; rm[6] = q1.z; rm[7] = q1.w;
-        }
     } else {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -672,8 +667,11 @@ __global__ void __launch_bounds__(256, ROWQ ? 2 : 3) k_quant_col_block(const voi
         rows[i].y = cvt_fp8x2<FMT>(p[4], p[5]) | (cvt_fp8x2<FMT>(p[6], p[7]) << 16);
         if (ROWQ && ok) {
             // the row-unit codes of this row go to q (their saturations are
-            // counted separately: sat counts the column-unit pass)
-            *reinterpret_cast<uint2*>(q + (r0 + i) * C + c0) = cast8<FMT>(f, rm[i], v[i].absmax_bits(), nsat_r);
+            // counted separately: sat counts the column-unit pass); 1x128
+            // tiles read the row's multiplier from shared memory row by row,
+            // which keeps the kernel within three CTAs' registers
+            const float rmi = UNIT == 128 ? rowm[rl + i] : rm[i];
+            *reinterpret_cast<uint2*>(q + (r0 + i) * C + c0) = cast8<FMT>(f, rmi, v[i].absmax_bits(), nsat_r);
         }
     }
     (void)nsat_r;
