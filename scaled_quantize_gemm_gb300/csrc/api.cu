@@ -1,6 +1,7 @@
 // api.cu -- the extern "C" boundary declared in include/fp8sq.h.
 // Validates every argument on the host before anything is enqueued, checks
 // that the current device is sm_103, then hands off to the launchers.
+#include <atomic>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -25,10 +26,10 @@ int fail(int code, const char* fmt, ...)
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-struct DevInfo {
-    int checked = 0, ok = 0, sms = 0, major = 0, minor = 0;
-};
-DevInfo g_dev[64];
+// Per-device facts, queried once.  `packed` is 0 until the first query has
+// finished, then (major << 24) | (minor << 16) | sms, published with one
+// atomic store so concurrent callers see either nothing or all of it.
+std::atomic<uint32_t> g_dev[64];
 
 // current device must be sm_103; returns its SM count through *sms
 int check_device(int* sms)
@@ -39,19 +40,22 @@ int check_device(int* sms)
         cudaGetLastError();
         return fail(FP8SQ_ERR_CUDA, "no usable CUDA device (%s)", cudaGetErrorString(e));
     }
-    DevInfo& d = g_dev[dev];
-    if (!d.checked) {
-        if (cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    uint32_t packed = g_dev[dev].load(std::memory_order_acquire);
+    if (packed == 0) {
+        int major = 0, minor = 0, n = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
             cudaGetLastError();
             return fail(FP8SQ_ERR_CUDA, "cannot query device %d", dev);
         }
-        d.ok = (d.major == 10 && d.minor == 3);
-        d.checked = 1;
+        packed = ((uint32_t)major << 24) | ((uint32_t)(minor & 0xFF) << 16) | ((uint32_t)n & 0xFFFFu);
+        g_dev[dev].store(packed, std::memory_order_release);
     }
-    if (!d.ok) return fail(FP8SQ_ERR_WRONG_ARCH, "device %d is sm_%d%d; this library is built for sm_103a only", dev, d.major, d.minor);
-    *sms = d.sms;
+    const int major = (int)(packed >> 24), minor = (int)((packed >> 16) & 0xFF);
+    if (!(major == 10 && minor == 3))
+        return fail(FP8SQ_ERR_WRONG_ARCH, "device %d is sm_%d%d; this library is built for sm_103a only", dev, major, minor);
+    *sms = (int)(packed & 0xFFFFu);
     return FP8SQ_OK;
 }
 

@@ -1110,17 +1110,20 @@ __global__ void k_fill_bias(void* D, int64_t M, int64_t N, const float* bias)
 }
 
 // ================================================================== host
+// the driver's tensor-map encoder, resolved once (thread-safe static
+// initialisation); null if the driver does not provide it
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        cudaGetLastError();
+        return nullptr;
+    }();
     return fn;
 }
 
@@ -1190,16 +1193,21 @@ static bool make_tmap_out(CUtensorMap* m, void* D, int64_t M, int64_t N, bool bf
 
 // Co-resident CTA pairs of the pair kernel on the current device (queried
 // once per device and output type; the kernel's resources never change).
+// The cache entries are atomics: concurrent first calls may both query and
+// store, always the same value.
 template <typename KernelT>
 static cudaError_t pair_clusters(KernelT kern, int variant, int smem, int* clusters)
 {
-    static int cache[2][64] = {};
+    static std::atomic<int> cache[2][64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && cache[variant][dev] > 0) {
-        *clusters = cache[variant][dev];
-        return cudaSuccess;
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[variant][dev].load(std::memory_order_relaxed);
+        if (c > 0) {
+            *clusters = c;
+            return cudaSuccess;
+        }
     }
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
@@ -1217,7 +1225,7 @@ static cudaError_t pair_clusters(KernelT kern, int variant, int smem, int* clust
     int n = 0;
     e = cudaOccupancyMaxActiveClusters(&n, (void*)kern, &cfg);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) cache[variant][dev] = n;
+    if (dev >= 0 && dev < 64) cache[variant][dev].store(n, std::memory_order_relaxed);
     *clusters = n;
     return cudaSuccess;
 }

@@ -1,6 +1,7 @@
 // internal.h -- host-side launcher interface between the C-ABI layer
 // (api.cu) and the kernel translation units.  Not installed, not part of the ABI.
 #pragma once
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
