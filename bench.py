@@ -594,7 +594,8 @@ def kernel_case(case: str, launches: int):
     profiling a single launch: 'gemm' = the 16384 x 14336 x 4096 forward GEMM
     (k_gemm_tensor_pair), 'cast' = the 16384 x 14336 E5M2 cast with its transposed
     copy (k_cast_tensor_T), 'promote' = the 4096^3 1x128 x 128x128 GEMM
-    (k_gemm_promote), 'mx' = the 8192^3 MX-32 GEMM (k_gemm_mx), 'fine' = the
+    (k_gemm_promote), 'wgrad' = the 4096^3 column-tile GEMM (k_gemm_promote, per-column
+    scales, fp32 out), 'mx' = the 8192^3 MX-32 GEMM (k_gemm_mx), 'fine' = the
     fine-grained casts (1x128, 128x128, MX-32 tiled, 128x1 columns), 'ln' =
     the LayerNorm-fused cast of a 16384 x 4096 activation."""
     import scaled_quantize_gemm_gb300 as sq
@@ -673,6 +674,19 @@ def kernel_case(case: str, launches: int):
         y = torch.empty((4096, 4096), dtype=torch.bfloat16, device=dev)
         for _ in range(launches):
             sq.fp8_gemm(qx, sq.E4M3, sx, sq.TILE_1x128, qw, sq.E4M3, sw, sq.BLOCK_128x128, y)
+    elif case == "wgrad":
+        # the fine-grained wgrad at 4096^3: dy (E5M2) and x (E4M3) in 128x1
+        # column tiles, their transposed codes as the GEMM's operands
+        x, _ = wl.w3_operands(dev)
+        dy = wl.normal((4096, 4096), 1e-3, 3, dev)
+        qdT, qxT = torch.empty((4096, 4096), **u8), torch.empty((4096, 4096), **u8)
+        sd = torch.empty(32 * 4096, dtype=torch.float32, device=dev)
+        sx = torch.empty(32 * 4096, dtype=torch.float32, device=dev)
+        sq.fp8_quantize(dy, sq.E5M2, sq.TILE_128x1, None, qT=qdT, scales_out=sd)
+        sq.fp8_quantize(x, sq.E4M3, sq.TILE_128x1, None, qT=qxT, scales_out=sx)
+        dw = torch.empty((4096, 4096), dtype=torch.float32, device=dev)
+        for _ in range(launches):
+            sq.fp8_gemm(qdT, sq.E5M2, sd, sq.TILE_128x1, qxT, sq.E4M3, sx, sq.TILE_128x1, dw)
     torch.cuda.synchronize()
     if sq.fp8_device_status(True) != 0:
         raise RuntimeError("device status error")
@@ -916,7 +930,7 @@ def modes_table(reps: int = 10):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel-case", choices=["gemm", "cast", "promote", "mx", "fine", "ln"], default=None,
+    ap.add_argument("--kernel-case", choices=["gemm", "cast", "promote", "wgrad", "mx", "fine", "ln"], default=None,
                     help="run a few launches of one kernel (for profiling) and exit")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--modes", action="store_true",
