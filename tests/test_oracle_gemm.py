@@ -101,3 +101,34 @@ def test_epilogue_rounding():
     b = o.epilogue(r, out_bf16=True)
     assert b.dtype == np.uint16
     assert o.bf16_bits_to_f32(b).tolist() == [[256.0, 1.0, -3.0]]
+
+
+def test_linear_delayed_exact_on_representable_inputs():
+    """The delayed linear layer end to end.  Each role's state gets its own
+    power-of-two multiplier m and scale s = 1/m (x: 2, W: 4, dy: 8), and the
+    inputs are small integers, so every scaled value is exact in its format:
+    x*2 within +-16 in E4M3, W*4 multiples of 4 within +-32 in E4M3, dy*8
+    multiples of 8 within +-32 in E5M2.  The forward, dgrad and wgrad must
+    then be the exact integer products R = x W^T, dX = dy W, dW = dy^T x, on
+    non-square shapes where a transposed operand, a scale taken from the
+    wrong role or the wrong format would show.  Each cast also records its
+    tensor's amax in history slot 0."""
+    rng = np.random.default_rng(5)
+    M, K, N, H = 6, 5, 7, 4
+    xi = rng.integers(-8, 9, (M, K))
+    wi = rng.integers(-8, 9, (N, K))
+    di = rng.integers(-4, 5, (M, N))
+    states = []
+    for m in (2.0, 4.0, 8.0):
+        st = o.state_init(H)
+        st[H], st[H + 1] = m, 1.0 / m
+        states.append(st)
+    sx, sw, sd = states
+    qx, fx, qw, fw, r = o.linear_fwd_delayed(xi.astype(np.float32), wi.astype(np.float32), sx, sw)
+    assert (fx, fw) == (0.5, 0.25)
+    _, fd, dX, dW = o.linear_bwd_delayed(di.astype(np.float32), sd, o.E5M2, qx, fx, qw, fw)
+    assert fd == 0.125
+    assert np.array_equal(r, xi @ wi.T)
+    assert np.array_equal(dX, di @ wi)
+    assert np.array_equal(dW, di.T @ xi)
+    assert (sx[0], sw[0], sd[0]) == (np.abs(xi).max(), np.abs(wi).max(), np.abs(di).max())
