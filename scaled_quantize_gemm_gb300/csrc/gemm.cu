@@ -543,12 +543,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 //      element sA[kb][row] * sB[kb][col]; the warp's column scales reach its
 //      lanes through a double-buffered shared-memory slot.
 // Measured, per-row scales, bf16 out, TFLOP/s at 4096^3 / 16384 x 14336 x
-// 4096 / 8192^3 (bit-identical outputs throughout):
-//   this kernel                                              1832 2188 2421
+// 4096 / 8192^3, outputs bit-identical throughout.  This kernel, through the
+// library: 1848-1871 / 2080-2133 / 2270-2351.  Timed side by side in one
+// process (the first row is this design while an epilogue warp still freed
+// the stages):
+//   one CTA per 128 x 256 tile                               1832 2188 2421
 //   the same on CTA pairs (256 x 256, cluster-wide handshake) 1716 2115 2348
 //   128 x 192 tiles, all 96 columns copied in one wait       1651 1902 1985
+// From separate runs:
 //   256 x 128 CTA-pair tiles, four 128-column buffers        1335 1440 1525
-//   ten warps, 168 registers, four serial 32-column copies   1633 2002 2182
+//   ten warps, 168 registers, four serial 32-column copies   1633-1676 1961-2002 2103-2182
 // The epilogue's waits stay at CTA scope; with the same handshake across a
 // CTA pair, a release arrival at cluster scope on every K block put a fence
 // behind each K block's scale loads (ncu: membar the dominant stall, 12 %
