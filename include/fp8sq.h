@@ -334,17 +334,22 @@ FP8SQ_API int fp8_layernorm_linear_fwd(const void* x, const float* gamma, const 
  * per-tensor scaling (x, W cast to E4M3 with m = 448/amax; y = acc * s_x *
  * s_w + bias).  Its scratch -- the codes of x and W and four fp32 scalars --
  * is a file-scope device array of FP8SQ_NOALLOC_SCRATCH_BYTES (32 MiB) that
- * every GPU which loads this library holds until the process exits.  The call
- * itself allocates nothing (no cudaMalloc, cudaFree or allocating library
- * routine).
+ * every GPU on which this library's device code is loaded holds until the
+ * process exits.  The call allocates nothing itself (no cudaMalloc, cudaFree
+ * or allocating library routine).
+ *   M, N, K must each be below 2^31 (checked before any product is formed).
  *   x  device bf16 [M][K], w device bf16 [N][K], y device bf16 / f32 [M][N],
  *      bias device f32 [N] or NULL; x, w, y 16-byte aligned.
  *   Needs N % 8 == 0, K % 16 == 0 and round256(M*K) + round256(N*K) + 256 <=
  *   FP8SQ_NOALLOC_SCRATCH_BYTES; larger sizes return FP8SQ_ERR_UNSUPPORTED
  *   with a message giving the bytes needed.
  * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) for that device; make that first call before any
- * stream capture.  All calls share the one array and it keeps the last
+ * (cudaGetSymbolAddress) for that device.  Under CUDA's lazy module loading
+ * (the default) that lookup may be what loads the library's device code onto
+ * the device and places the array there, so the first call can reserve the
+ * 32 MiB and can fail with FP8SQ_ERR_CUDA (out of memory).  Make that first
+ * call at set-up time, before any stream capture; later calls on the device
+ * reserve nothing.  All calls share the one array and it keeps the last
  * call's contents (the amax slots are cleared by every call), so calls whose
  * work overlaps on the GPU -- on different streams, or from several threads
  * -- race on it and must be serialised by the caller.

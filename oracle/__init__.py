@@ -419,23 +419,45 @@ def linear_fine_fwd(x, w, gran: int):
     return {"x": x, "w": w}, r
 
 
-def linear_fine_bwd(st, dy, gran: int, dy_fmt: int = E4M3):
-    """-> (dX, dW) float64 for the fine-grained recipes."""
+def linear_fine_bwd_operands(st, dy, gran: int, dy_fmt: int = E4M3):
+    """The four operands of the fine-grained backward, each quantised along
+    its own GEMM's contraction dimension.  Returns {name: (codes, scales,
+    dequantised float64)} with every matrix in its original orientation
+    (dy [M][N], W [N][K], x [M][K]):
+      dgrad_dy  dy in units along N   (1x128 tiles [M][N/128] / MX-32 [M][N/32])
+      dgrad_w   W in units along N    (the forward's 128x128 blocks [N/128][K/128] /
+                                       MX-32 column blocks [N/32][K])
+      wgrad_dy  dy in units along M   (128x1 column tiles [M/128][N] / [M/32][N])
+      wgrad_x   x in units along M    (128x1 column tiles [M/128][K] / [M/32][K])"""
     x, w = st["x"], st["w"]
     if gran == GRAN_TILE_1x128:
-        qd, sd, _, _ = quantize_tile1x128(dy, dy_fmt)                      # along N
-        wh = dequantize(st["qw"], E4M3, GRAN_BLOCK_128x128, st["sw"])       # blocks, same codes
-        dX = gemm_ref(dequantize(qd, dy_fmt, GRAN_TILE_1x128, sd), wh.T)
-        qdc, sdc, _, _ = quantize_tile128x1(dy, dy_fmt)                    # along M
+        qd, sd, _, _ = quantize_tile1x128(dy, dy_fmt)
+        qdc, sdc, _, _ = quantize_tile128x1(dy, dy_fmt)
         qxc, sxc, _, _ = quantize_tile128x1(x, E4M3)
-        dW = gemm_ref(dequantize(qdc, dy_fmt, GRAN_TILE_128x1, sdc).T, dequantize(qxc, E4M3, GRAN_TILE_128x1, sxc).T)
-        return dX, dW
-    qd, ed, _, _ = quantize_mx32(dy, dy_fmt)                               # along N
-    qwc, ewc, _, _ = quantize_mx32_col(w, E4M3)                            # W along N
-    dX = gemm_ref(dequantize(qd, dy_fmt, GRAN_MX32, ed), dequantize(qwc, E4M3, GRAN_MX32_COL, ewc).T)
-    qdc, edc, _, _ = quantize_mx32_col(dy, dy_fmt)                         # along M
+        return {
+            "dgrad_dy": (qd, sd, dequantize(qd, dy_fmt, GRAN_TILE_1x128, sd)),
+            "dgrad_w": (st["qw"], st["sw"], dequantize(st["qw"], E4M3, GRAN_BLOCK_128x128, st["sw"])),
+            "wgrad_dy": (qdc, sdc, dequantize(qdc, dy_fmt, GRAN_TILE_128x1, sdc)),
+            "wgrad_x": (qxc, sxc, dequantize(qxc, E4M3, GRAN_TILE_128x1, sxc)),
+        }
+    qd, ed, _, _ = quantize_mx32(dy, dy_fmt)
+    qwc, ewc, _, _ = quantize_mx32_col(w, E4M3)
+    qdc, edc, _, _ = quantize_mx32_col(dy, dy_fmt)
     qxc, exc, _, _ = quantize_mx32_col(x, E4M3)
-    dW = gemm_ref(dequantize(qdc, dy_fmt, GRAN_MX32_COL, edc).T, dequantize(qxc, E4M3, GRAN_MX32_COL, exc).T)
+    return {
+        "dgrad_dy": (qd, ed, dequantize(qd, dy_fmt, GRAN_MX32, ed)),
+        "dgrad_w": (qwc, ewc, dequantize(qwc, E4M3, GRAN_MX32_COL, ewc)),
+        "wgrad_dy": (qdc, edc, dequantize(qdc, dy_fmt, GRAN_MX32_COL, edc)),
+        "wgrad_x": (qxc, exc, dequantize(qxc, E4M3, GRAN_MX32_COL, exc)),
+    }
+
+
+def linear_fine_bwd(st, dy, gran: int, dy_fmt: int = E4M3):
+    """-> (dX, dW) float64 for the fine-grained recipes: dX = dy W over N,
+    dW = dy^T x over M, on the operands of linear_fine_bwd_operands."""
+    ops = linear_fine_bwd_operands(st, dy, gran, dy_fmt)
+    dX = gemm_ref(ops["dgrad_dy"][2], ops["dgrad_w"][2].T)
+    dW = gemm_ref(ops["wgrad_dy"][2].T, ops["wgrad_x"][2].T)
     return dX, dW
 
 

@@ -12,6 +12,7 @@
 namespace {
 
 constexpr size_t kScratchBytes = FP8SQ_NOALLOC_SCRATCH_BYTES;
+constexpr int64_t kMaxDim = (int64_t)1 << 31;
 
 // Held by every GPU that loads this library, until the process exits.  In
 // host code `g_noalloc_scratch` only names the symbol; its device address
@@ -54,6 +55,9 @@ extern "C" FP8SQ_API int fp8_linear_fwd_noalloc(const void* x, const void* w, in
 {
     using fp8sq::api_fail;
     if (M < 0 || N < 0 || K < 0) return api_fail(FP8SQ_ERR_INVALID_ARG, "fp8_linear_fwd_noalloc: negative size");
+    // bound each dimension before any product is formed (GEMM / TMA coordinates are 32-bit)
+    if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim)
+        return api_fail(FP8SQ_ERR_UNSUPPORTED, "fp8_linear_fwd_noalloc: dimension too large");
     if ((!x && M * K) || (!w && N * K) || (!y && M * N))
         return api_fail(FP8SQ_ERR_INVALID_ARG, "fp8_linear_fwd_noalloc: null pointer");
     if (y_dtype != FP8SQ_BF16 && y_dtype != FP8SQ_F32)
@@ -102,6 +106,8 @@ extern "C" FP8SQ_API int fp8_linear_fwd_noalloc(const void* x, const void* w, in
     g.bias = bias; g.D = y; g.d_dtype = y_dtype;
     const char* why = nullptr;
     e = fp8sq::launch_gemm(g, st, sms, &why);
+    if (e == cudaErrorNotSupported)
+        return api_fail(FP8SQ_ERR_UNSUPPORTED, "fp8_linear_fwd_noalloc: %s", why ? why : "GEMM not supported");
     if (e != cudaSuccess) {
         cudaGetLastError();
         return api_fail(FP8SQ_ERR_CUDA, "fp8_linear_fwd_noalloc: GEMM launch: %s", why ? why : cudaGetErrorString(e));

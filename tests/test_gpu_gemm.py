@@ -178,21 +178,29 @@ def _sample_rows(M, n, seed):
 
 def test_w3_full_size_sampled_rows():
     """Workload 3 at full size (M=N=K=4096, bf16 out) in the launch
-    configuration the bench times; 256 sampled rows checked against the oracle."""
+    configuration the bench times.  The reference is built from the oracle's
+    own 1x128 / 128x128 quantisation of the inputs (which must equal the
+    GPU's codes and scales); 256 sampled rows of the product checked."""
     x, w = wl.w3_operands(DEV)
     qx, sx, qw, sw = _quant_tile_block(x, w)
     D = torch.empty((4096, 4096), dtype=torch.bfloat16, device=DEV)
     sq.fp8_gemm(qx, sq.E4M3, sx, sq.TILE_1x128, qw, sq.E4M3, sw, sq.BLOCK_128x128, D)
     torch.cuda.synchronize()
+    rqx, rsx, _, _ = o.quantize_tile1x128(np32(x), o.E4M3)
+    rqw, rsw, _, _ = o.quantize_block128(np32(w), o.E4M3)
+    assert np.array_equal(codes(qx), rqx) and np.array_equal(sx.cpu().numpy(), rsx.ravel())
+    assert np.array_equal(codes(qw), rqw) and np.array_equal(sw.cpu().numpy(), rsw.ravel())
     rows = _sample_rows(4096, 256, 3)
-    ah = o.dequantize(codes(qx[rows]), 0, o.GRAN_TILE_1x128, sx.view(4096, 32)[rows].cpu().numpy())
-    bh = o.dequantize(codes(qw), 0, o.GRAN_BLOCK_128x128, sw.view(32, 32).cpu().numpy())
+    ah = o.dequantize(rqx[rows], 0, o.GRAN_TILE_1x128, rsx[rows])
+    bh = o.dequantize(rqw, 0, o.GRAN_BLOCK_128x128, rsw)
     assert_gemm_close(D[rows], o.gemm_ref(ah, bh))
 
 
 def test_w5_forward_gemm_full_size_sampled_rows():
     """The FFN up-projection of workload 5 (M=16384, K=4096, N=14336, bf16
-    out) at full size; 128 sampled rows against the oracle."""
+    out) at full size, current per-tensor scaling; the reference comes from
+    the oracle's own quantisation of x and W (equal to the GPU's codes and
+    scales); 128 sampled rows against it."""
     M, K, N = 16384, 4096, 14336
     x = wl.linear_x(5, 0, 0, M, K, DEV)
     w = wl.linear_w(5, 0, N, K, DEV)
@@ -201,9 +209,13 @@ def test_w5_forward_gemm_full_size_sampled_rows():
     D = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
     sq.fp8_gemm(qx, sq.E4M3, sx, sq.TENSOR, qw, sq.E4M3, sw, sq.TENSOR, D)
     torch.cuda.synchronize()
+    rqx, _, rsx, _ = o.quantize_tensor_current(np32(x), o.E4M3)
+    rqw, _, rsw, _ = o.quantize_tensor_current(np32(w), o.E4M3)
+    assert np.array_equal(codes(qx), rqx) and np.float32(sx.item()) == rsx
+    assert np.array_equal(codes(qw), rqw) and np.float32(sw.item()) == rsw
     rows = _sample_rows(M, 128, 5)
-    ah = o.dequantize(codes(qx[rows]), 0, 0, sx.item())
-    bh = o.dequantize(codes(qw), 0, 0, sw.item())
+    ah = o.dequantize(rqx[rows], 0, 0, rsx)
+    bh = o.dequantize(rqw, 0, 0, rsw)
     assert_gemm_close(D[rows], o.gemm_ref(ah, bh))
 
 
@@ -303,18 +315,22 @@ def test_mx_vs_oracle(M, N, K, out):
 
 def test_w4_mx_full_size_sampled_rows():
     """Workload 4 at full size: A, B 8192 x 8192 with 0.1 % of entries x100,
-    MX-32 E4M3, bf16 out; 128 sampled rows against the oracle."""
+    MX-32 E4M3, bf16 out.  The reference comes from the oracle's own MX-32
+    quantisation of A and B (equal to the GPU's codes and, untiled, its E8M0
+    scales); 128 sampled rows against it."""
     from _helpers import mx_untile
     a, b = wl.w4_operands(DEV)
     qa, ea = _quant_mx(a)
     qb, eb = _quant_mx(b)
-    del a, b
     D = _mx_gemm(qa, ea, qb, eb, torch.bfloat16)
+    rqa, rea, _, _ = o.quantize_mx32(np32(a), o.E4M3)
+    rqb, reb, _, _ = o.quantize_mx32(np32(b), o.E4M3)
+    del a, b
+    assert np.array_equal(codes(qa), rqa) and np.array_equal(mx_untile(ea.cpu().numpy(), 8192, 8192), rea)
+    assert np.array_equal(codes(qb), rqb) and np.array_equal(mx_untile(eb.cpu().numpy(), 8192, 8192), reb)
     rows = _sample_rows(8192, 128, 9)
-    ea_c = mx_untile(ea.cpu().numpy(), 8192, 8192)
-    eb_c = mx_untile(eb.cpu().numpy(), 8192, 8192)
-    ah = o.dequantize(codes(qa[rows]), 0, o.GRAN_MX32, ea_c[rows])
-    bh = o.dequantize(codes(qb), 0, o.GRAN_MX32, eb_c)
+    ah = o.dequantize(rqa[rows], 0, o.GRAN_MX32, rea[rows])
+    bh = o.dequantize(rqb, 0, o.GRAN_MX32, reb)
     assert_gemm_close(D[rows], o.gemm_ref(ah, bh))
 
 

@@ -42,7 +42,9 @@ def _check_ln_codes(x, gamma, beta, q, mu, rstd, m, fmt):
     assert np.all(np.abs(rs_g / rs_o - 1.0) <= 2e-5)
     t = (xf.astype(np.float64) - mu_o[:, None]) * rs_o[:, None]
     g64, b64 = gamma.numpy().astype(np.float64), beta.numpy().astype(np.float64)
-    delta = 2.0 ** -14 * (np.abs(t * g64) + np.abs(g64) + np.abs(b64))
+    # + 2^-20 |y|: room for a multiplier a few ulps away from m (the GPU's
+    # own, derived from its fp32 amax history)
+    delta = 2.0 ** -14 * (np.abs(t * g64) + np.abs(g64) + np.abs(b64)) + 2.0 ** -20 * np.abs(y)
     near, lo, hi = o.ln_acceptable_codes(y, delta, m, fmt)
     gq = codes(q)
     r = o.code_rank
@@ -69,8 +71,17 @@ def test_layernorm_fused_cast(fmt, M, K):
 
 
 def test_layernorm_linear_forward_and_backward():
-    """LayerNormLinear forward (LN cast, W cast, GEMM) over three delayed
-    steps, then the linear backward from the same workspace."""
+    """LayerNormLinear forward (LN cast, W cast, GEMM) then the linear
+    backward from the same workspace, over four delayed steps.
+
+    The W and dy states are bit-exact against the oracle's every step.  The x
+    state follows the exact (float64) LayerNorm's amax: every history entry
+    within 1e-5 of the oracle's, and the update rule applied exactly to the
+    GPU's own history.  The LayerNorm codes (re-derived by the same cast on a
+    copy of the pre-step state) sit inside the reachable bracket of the exact
+    LayerNorm under the oracle's multiplier; y, dx and dW are then compared
+    with the oracle's float64 products of those codes, the oracle's W codes
+    and the oracle's own dy codes."""
     M, K, N, H = 256, 768, 512, 16
     w = wl.normal((N, K), 0.02, 3).to(DEV)
     states = torch.empty(3 * (H + 2), device=DEV)
@@ -81,23 +92,52 @@ def test_layernorm_linear_forward_and_backward():
     dx = torch.empty((M, K), dtype=torch.bfloat16, device=DEV)
     dw = torch.empty((N, K), dtype=torch.float32, device=DEV)
     mu, rstd = torch.empty(M, device=DEV), torch.empty(M, device=DEV)
-    ref_w = o.state_init(H)
-    for step in range(3):
+    qln, qlnT = torch.empty((M, K), dtype=torch.uint8, device=DEV), torch.empty((K, M), dtype=torch.uint8, device=DEV)
+    mu2, rstd2 = torch.empty(M, device=DEV), torch.empty(M, device=DEV)
+    ref_x, ref_w, ref_dy = o.state_init(H), o.state_init(H), o.state_init(H)
+    wf = np32(w)
+    for step in range(4):
         x, gamma, beta = _inputs(M, K, 30 + step)
-        dy = wl.normal((M, N), 1e-3, 40 + step).to(DEV)
-        m_x = float(st[0][H].item())
-        s_x = np.float32(st[0][H + 1].item())
-        sq.fp8_layernorm_linear_fwd(x.to(DEV), gamma.to(DEV), beta.to(DEV), EPS, w, y, ws, mu, rstd, st[0], st[1], H)
+        # a gradient spike at step 2 moves the dy scale through its history
+        dy = wl.normal((M, N), 1e-3 * (30.0 if step == 2 else 1.0), 40 + step).to(DEV)
+        xd, gd, bd = x.to(DEV), gamma.to(DEV), beta.to(DEV)
+        pre_x = st[0].clone()
+        sq.fp8_layernorm_linear_fwd(xd, gd, bd, EPS, w, y, ws, mu, rstd, st[0], st[1], H)
         sq.fp8_linear_bwd(dy, dx, dw, ws, K, dy_state=st[2], history_len=H)
+        # the LayerNorm codes the forward used: the same cast, from a copy of
+        # the pre-step x state
+        sq.fp8_layernorm_quantize(xd, gd, bd, EPS, sq.E4M3, qln, qlnT, mu2, rstd2, pre_x, H)
         torch.cuda.synchronize()
-        # LayerNorm codes of x, checked against the exact LayerNorm
-        yln, _, _ = o.layernorm(np32(x), gamma.numpy(), beta.numpy(), EPS)
-        near, _, _ = o.ln_acceptable_codes(yln, np.zeros_like(yln), m_x, o.E4M3)
-        qw, _ = o.quantize_delayed(np32(w), o.E4M3, ref_w)
+        m_x_gpu = np.float32(st[0][H].item())
+        s_x_gpu = np.float32(st[0][H + 1].item())
+        m_x, s_x = np.float32(ref_x[H]), np.float32(ref_x[H + 1])
+        assert abs(m_x_gpu / m_x - 1.0) <= 1e-5 and abs(s_x_gpu / s_x - 1.0) <= 1e-5, step
+        yln = _check_ln_codes(x, gamma, beta, qln, mu, rstd, m_x, o.E4M3)
+        assert np.array_equal(codes(mu2.view(torch.uint8)), codes(mu.view(torch.uint8)))
+        # oracle: W and dy codes and their states (bit-exact below)
+        qw, _ = o.quantize_delayed(wf, o.E4M3, ref_w)
         s_w = np.float32(ref_w[H + 1])
-        R = o.gemm_ref(o.dequantize(near, o.E4M3, 0, s_x), o.dequantize(qw, o.E4M3, 0, s_w))
-        assert_gemm_close(y, R)
+        qd, _ = o.quantize_delayed(np32(dy), o.E5M2, ref_dy)
+        s_d = np.float32(ref_dy[H + 1])
+        ref_x[0] = np.float32(np.max(np.abs(yln)))
+        xh = o.dequantize(codes(qln), o.E4M3, o.GRAN_TENSOR, s_x_gpu)
+        wh = o.dequantize(qw, o.E4M3, o.GRAN_TENSOR, s_w)
+        dh = o.dequantize(qd, o.E5M2, o.GRAN_TENSOR, s_d)
+        assert_gemm_close(y, o.gemm_ref(xh, wh))
+        assert_gemm_close(dx, o.gemm_ref(dh, wh.T))
+        assert_gemm_close(dw, o.gemm_ref(dh.T, xh.T))
+        # end of step: update, then compare the states
+        gpu_x_before = st[0].cpu().numpy().copy()
         sq.fp8_update_scale(states, 3, H, [sq.E4M3, sq.E4M3, sq.E5M2])
-        o.update_scale(ref_w, o.E4M3)
+        for ref, fmt in ((ref_x, o.E4M3), (ref_w, o.E4M3), (ref_dy, o.E5M2)):
+            o.update_scale(ref, fmt)
+        o.update_scale(gpu_x_before, o.E4M3)
         torch.cuda.synchronize()
-        assert np.all(np.isfinite(dx.float().cpu().numpy())) and np.all(np.isfinite(dw.cpu().numpy()))
+        got = states.cpu().numpy()
+        gx, gw, gd_ = got[:H + 2], got[H + 2:2 * (H + 2)], got[2 * (H + 2):]
+        assert gw.tobytes() == ref_w.tobytes(), step
+        assert gd_.tobytes() == ref_dy.tobytes(), step
+        assert gx.tobytes() == gpu_x_before.tobytes(), step          # the update rule, exactly
+        nz = ref_x[:H] > 0
+        assert np.array_equal(gx[:H] > 0, nz)
+        assert np.all(np.abs(gx[:H][nz] / ref_x[:H][nz] - 1.0) <= 1e-5), step

@@ -9,7 +9,7 @@ import oracle as o
 import scaled_quantize_gemm_gb300 as sq
 from scaled_quantize_gemm_gb300 import workloads as wl
 
-from _helpers import assert_gemm_close, np32
+from _helpers import assert_gemm_close, codes, np32
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -30,19 +30,21 @@ class Layer:
     def st(self, i):
         return self.states[i * (self.H + 2):(i + 1) * (self.H + 2)]
 
-    def step(self, x, w, dy):
-        sq.fp8_linear_fwd(x, w, self.y, self.ws, x_state=self.st(0), w_state=self.st(1), history_len=self.H)
-        sq.fp8_linear_bwd(dy, self.dx, self.dw, self.ws, self.K, dy_state=self.st(2), history_len=self.H)
+    def step(self, x, w, dy, recipe=sq.RECIPE_HYBRID):
+        sq.fp8_linear_fwd(x, w, self.y, self.ws, recipe=recipe, x_state=self.st(0), w_state=self.st(1),
+                          history_len=self.H)
+        sq.fp8_linear_bwd(dy, self.dx, self.dw, self.ws, self.K, recipe=recipe, dy_state=self.st(2),
+                          history_len=self.H)
 
 
 FORMATS = [sq.E4M3, sq.E4M3, sq.E5M2]       # x, W, dy under HYBRID
 
 
-def _oracle_step(ref, x, w, dy, rows=None, wrows=None):
+def _oracle_step(ref, x, w, dy, rows=None, wrows=None, dy_fmt=o.E5M2):
     qx, sx, qw, sw, Y = o.linear_fwd_delayed(np32(x), np32(w), ref[0], ref[1])
     if rows is not None:
         Y = Y[rows]
-    _, _, dX, dW = o.linear_bwd_delayed(np32(dy), ref[2], o.E5M2, qx, sx, qw, sw, rows=rows, wrows=wrows)
+    _, _, dX, dW = o.linear_bwd_delayed(np32(dy), ref[2], dy_fmt, qx, sx, qw, sw, rows=rows, wrows=wrows)
     return Y, dX, dW
 
 
@@ -59,6 +61,32 @@ def test_delayed_hybrid_steps(M, K, N):
         sq.fp8_update_scale(L.states, 3, 16, FORMATS)
         for r in range(3):
             o.update_scale(ref[r], FORMATS[r])
+        torch.cuda.synchronize()
+        assert_gemm_close(L.y, Y)
+        assert_gemm_close(L.dx, dX)
+        assert_gemm_close(L.dw, dW)
+        assert L.states.cpu().numpy().tobytes() == np.concatenate(ref).tobytes(), step
+
+
+@pytest.mark.parametrize("M,K,N", [(256, 384, 512), (272, 144, 400)])
+def test_delayed_e4m3_only_recipe(M, K, N):
+    """The E4M3-only recipe (Transformer Engine tutorial, closing suggestions:
+    Format.E4M3 instead of HYBRID) under delayed scaling: the gradient's state
+    is an E4M3 state (fmax 448) too.  Six steps with H = 16, a gradient spike
+    at step 3; all three histories bit-exact every step."""
+    H = 16
+    L = Layer(M, K, N, H)
+    ref = [o.state_init(H) for _ in range(3)]
+    fmts = [sq.E4M3, sq.E4M3, sq.E4M3]
+    w = wl.normal((N, K), 0.02, 13).to(DEV)
+    for step in range(6):
+        x = wl.normal((M, K), 1.0 + 0.5 * step, 110 + step).to(DEV)
+        dy = wl.normal((M, N), 1e-3 * (20.0 if step == 3 else 1.0), 120 + step).to(DEV)
+        L.step(x, w, dy, recipe=sq.RECIPE_E4M3)
+        Y, dX, dW = _oracle_step(ref, x, w, dy, dy_fmt=o.E4M3)
+        sq.fp8_update_scale(L.states, 3, H, fmts)
+        for r in range(3):
+            o.update_scale(ref[r], o.E4M3)
         torch.cuda.synchronize()
         assert_gemm_close(L.y, Y)
         assert_gemm_close(L.dx, dX)
@@ -135,12 +163,94 @@ def test_w2_minigpt_20_steps():
             assert layers[li].states.cpu().numpy().tobytes() == np.concatenate(refs[li]).tobytes(), (step, li)
 
 
+def _u8(shape):
+    return torch.empty(shape, dtype=torch.uint8, device=DEV)
+
+
 def test_w5_ffn_step_full_size():
-    """Workload 5 at full size (M = 16384, 4096 -> 14336 -> 4096), two steps of
-    forward + backward + update in the launch configuration the bench times;
-    histories bit-exact, 32 sampled rows of y, dx and dW per linear."""
+    """Workload 5 at full size, all 10 steps, in the launch configuration the
+    bench times: the granular calls chained as in a training step (x ->
+    linear 0 -> y0 -> linear 1; dy -> linear 1's dgrad and wgrad -> dx1 ->
+    linear 0's dgrad and wgrad), HYBRID delayed scaling, H = 16.
+
+    Every step: the codes and transposed codes of all six casts equal the
+    oracle's over the whole tensor, all six histories are bit-exact after the
+    update, and y, dx and dW are compared with the oracle on 32 sampled rows
+    per GEMM.  Each linear's input is the GPU's own output of the previous
+    linear (checked there), as in the bench."""
     wk = wl.WORKLOADS[5]
+    M, H = wk.tokens, wk.history_len
+    lin = [(l.in_features, l.out_features) for l in wk.linears]
+    W = [wl.linear_w(5, li, N, K, DEV) for li, (K, N) in enumerate(lin)]
+    Wf = [np32(w) for w in W]
+    states = torch.empty(6 * (H + 2), dtype=torch.float32, device=DEV)
+    sq.fp8_scale_init(states, 6, H)
+    st = [states[i * (H + 2):(i + 1) * (H + 2)] for i in range(6)]
+    sc = [states[i * (H + 2) + H + 1:i * (H + 2) + H + 2] for i in range(6)]
+    ref = [o.state_init(H) for _ in range(6)]
+    fmts = [sq.E4M3, sq.E4M3, sq.E5M2] * 2
+    buf = [dict(qx=_u8((M, K)), qxT=_u8((K, M)), qw=_u8((N, K)), qwT=_u8((K, N)), qdy=_u8((M, N)),
+                qdyT=_u8((N, M)), y=torch.empty((M, N), dtype=torch.bfloat16, device=DEV),
+                dx=torch.empty((M, K), dtype=torch.bfloat16, device=DEV),
+                dw=torch.empty((N, K), dtype=torch.float32, device=DEV)) for (K, N) in lin]
     rng = np.random.default_rng(1)
+
+    def cast(src, fmt, si, q, qT):
+        sq.fp8_quantize(src, fmt, sq.TENSOR, q, qT=qT, delayed_state=st[si], history_len=H)
+        torch.cuda.synchronize()
+        s_used = np.float32(ref[si][H + 1])                      # the oracle state's scale before the cast
+        rq, _ = o.quantize_delayed(np32(src), fmt, ref[si])
+        assert np.array_equal(codes(q), rq), ("codes", si)
+        assert np.array_equal(codes(qT), rq.T), ("transposed codes", si)
+        assert np.float32(sc[si].item()) == s_used
+        return rq, s_used
+
+    for step in range(wk.steps):
+        saved = []
+        xin = wl.linear_x(5, 0, step, M, lin[0][0], DEV)
+        for li, (K, N) in enumerate(lin):                            # forward
+            B = buf[li]
+            qx, sx = cast(xin, sq.E4M3, 3 * li, B["qx"], B["qxT"])
+            qw, sw = cast(W[li], sq.E4M3, 3 * li + 1, B["qw"], B["qwT"])
+            sq.fp8_gemm(B["qx"], sq.E4M3, sc[3 * li], sq.TENSOR, B["qw"], sq.E4M3, sc[3 * li + 1], sq.TENSOR, B["y"])
+            torch.cuda.synchronize()
+            rows = np.sort(rng.choice(M, 32, replace=False))
+            wh = o.dequantize(qw, o.E4M3, o.GRAN_TENSOR, sw)
+            assert_gemm_close(B["y"][rows], o.gemm_ref(o.dequantize(qx[rows], o.E4M3, o.GRAN_TENSOR, sx), wh))
+            saved.append((qx, sx, wh))
+            xin = B["y"]
+        dyin = wl.linear_dy(5, len(lin) - 1, step, M, lin[-1][1], DEV)
+        for li in reversed(range(len(lin))):                         # backward
+            K, N = lin[li]
+            B = buf[li]
+            qx, sx, wh = saved[li]
+            qd, sd = cast(dyin, sq.E5M2, 3 * li + 2, B["qdy"], B["qdyT"])
+            sq.fp8_gemm(B["qdy"], sq.E5M2, sc[3 * li + 2], sq.TENSOR, B["qwT"], sq.E4M3, sc[3 * li + 1], sq.TENSOR,
+                        B["dx"])
+            sq.fp8_gemm(B["qdyT"], sq.E5M2, sc[3 * li + 2], sq.TENSOR, B["qxT"], sq.E4M3, sc[3 * li], sq.TENSOR,
+                        B["dw"])
+            torch.cuda.synchronize()
+            rows = np.sort(rng.choice(M, 32, replace=False))
+            wrows = np.sort(rng.choice(N, 32, replace=False))
+            assert_gemm_close(B["dx"][rows], o.gemm_ref(o.dequantize(qd[rows], o.E5M2, o.GRAN_TENSOR, sd), wh.T))
+            dcols = o.dequantize(np.ascontiguousarray(qd[:, wrows].T), o.E5M2, o.GRAN_TENSOR, sd)
+            xh = o.dequantize(qx, o.E4M3, o.GRAN_TENSOR, sx)
+            assert_gemm_close(B["dw"][wrows], o.gemm_ref(dcols, xh.T))
+            del xh, dcols
+            dyin = B["dx"]
+        sq.fp8_update_scale(states, 6, H, fmts)
+        for i in range(6):
+            o.update_scale(ref[i], fmts[i])
+        torch.cuda.synchronize()
+        assert states.cpu().numpy().tobytes() == np.concatenate(ref).tobytes(), step
+
+
+def test_w5_linear_api_full_size():
+    """Workload 5 at full size through fp8_linear_fwd / fp8_linear_bwd (the
+    calls the end-to-end leg of the bench times), two steps; histories
+    bit-exact, 32 sampled rows of y, dx and dW per linear."""
+    wk = wl.WORKLOADS[5]
+    rng = np.random.default_rng(2)
     layers, refs, ws_ = [], [], []
     for li, lin in enumerate(wk.linears):
         layers.append(Layer(wk.tokens, lin.in_features, lin.out_features, wk.history_len))
