@@ -369,6 +369,11 @@ def run_ours(args, ws, rank, local):
         raise RuntimeError(f"device status {rc} after the timed steps")
 
     ms_step = total_ms / args.steps
+    # the burst peak applies to a timed region of well under a second (the
+    # power cap has not pulled the clock down yet); the sustained one to a
+    # region of seconds
+    long_region = total_ms >= 2000.0
+    gemm_peak = fp8_sust if long_region else fp8_peak
     flops = b.gemm_flops_per_step()
     value = _replica_throughput(flops, ms_step, ws)
     per = {"gemm": [], "quant": [], "update": []}
@@ -414,10 +419,10 @@ def run_ours(args, ws, rank, local):
         torch.cuda.synchronize()
         if ws > 1:
             torch.distributed.barrier()
-        # three timed windows of K steps each; the fastest is reported and all
-        # are listed.  Intermittent host-link stalls on the shared host (one
-        # copy of 40-60 ms among 5.7 ms ones, in some windows and not others,
-        # with no matching host-side delay) would otherwise decide the number.
+        # three timed windows of K steps each; the median is reported and all
+        # are listed, with the median and maximum single-step copy time (the
+        # shared host's link stalls intermittently: one copy of 40-60 ms among
+        # 5.7 ms ones, in some windows and not others).
         rep_ms, copy_ms = [], []
         for _ in range(3):
             e0 = torch.cuda.Event(enable_timing=True)
@@ -432,19 +437,23 @@ def run_ours(args, ws, rank, local):
             torch.cuda.synchronize()
             copy_ms += [a.elapsed_time(z) for a, z in cev]
             rep_ms.append(_barrier_max(e0.elapsed_time(e1), ws, device) / args.steps)
-        e2e_ms = min(rep_ms)
+        e2e_ms = statistics.median(rep_ms)
         e2e = {"value": round(_replica_throughput(flops, e2e_ms, ws), 2), "unit": UNIT,
                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "h2d_link_gbs": round(link_gbs, 1),
                "h2d_bound_ms": round(h2d / (link_gbs * 1e9) * 1e3, 4),
                "h2d_copy_ms": {"median": round(statistics.median(copy_ms), 4), "max": round(max(copy_ms), 4)},
                "windows_ms_per_step": [round(v, 4) for v in rep_ms],
-               "window_rule": "fastest of 3 timed windows of K steps (all listed; h2d_copy_ms.max shows a stall)",
+               "window_rule": "median of 3 timed windows of K steps (all listed; h2d_copy_ms.max shows a stall)",
                "api": "fp8_linear_fwd / fp8_linear_bwd / fp8_update_scale; each step's x and dy copied "
                       "from pinned host memory (next step's copies overlap this step's compute), scale states "
                       "read back every step"}
         if b.sq.fp8_device_status(True) != 0:
             raise RuntimeError("device status error in the end-to-end leg")
+
+    cfgs = None
+    if rank == 0 and not args.no_per_config:
+        cfgs = per_config(device, with_oracle=(ws == 1 and not args.no_cpu_baseline))
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -468,12 +477,15 @@ def run_ours(args, ws, rank, local):
             "e2e": e2e,
             "gpu_launches": b.KERNELS_PER_STEP * args.steps,
             "roofline": {"bound": "tensor", "kernel": "k_gemm_tensor_pair (tcgen05 .cta_group::2 kind::f8f6f4, 256x256 tile on a CTA pair, 6 stages)",
-                         "achieved": round(achieved, 1), "peak": round(fp8_sust, 1), "unit": "TFLOP/s",
-                         "frac": round(achieved / fp8_sust, 4), "traffic": kernel_traffic("k_gemm_tensor_pair"),
+                         "achieved": round(achieved, 1), "peak": round(gemm_peak, 1), "unit": "TFLOP/s",
+                         "frac": round(achieved / gemm_peak, 4), "traffic": kernel_traffic("k_gemm_tensor_pair"),
                          "traffic_shape": "16384 x 14336 x 4096 forward GEMM (one ncu capture)",
-                         "peak_source": f"2 x bf16_tflops_sustained {peak_src} (dense FP8 = 2 x dense BF16; the "
-                                        "GEMMs are timed inside the whole K-step loop, under the power cap)",
+                         "peak_source": (f"2 x bf16_tflops_sustained {peak_src} (timed region {total_ms:.0f} ms, "
+                                         "seconds long: under the power cap)") if long_region else
+                                        (f"2 x bf16_tflops (burst) {peak_src} (timed region {total_ms:.0f} ms; "
+                                         "dense FP8 = 2 x dense BF16)"),
                          "peak_burst": round(fp8_peak, 1), "frac_of_burst": round(achieved / fp8_peak, 4),
+                         "peak_sustained": round(fp8_sust, 1), "frac_of_sustained": round(achieved / fp8_sust, 4),
                          "flops_per_launch": gemm_flops_launch, "launch_ms": round(gemm_ms, 4)},
             "roofline_quantize": {"bound": "hbm", "kernel": "k_cast_tensor_T (16384 x 14336 casts)",
                                   "achieved": round(big_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
@@ -485,10 +497,239 @@ def run_ours(args, ws, rank, local):
             "gemm": {"ms_per_step": round(sum(per["gemm"]) / args.steps, 4),
                      "tflops_per_s": round(achieved, 1)},
             "cpu_baseline": cpu,
+            "per_config": cfgs,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+# ---------------------------------------------------------------- workloads 1-4
+class _L2Flush:
+    """Writes a buffer larger than L2 (129 MB) before each timed iteration of
+    the smaller workloads, so no iteration reads what the previous one left in
+    L2."""
+
+    def __init__(self, device):
+        self.buf = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    def __call__(self):
+        self.buf.fill_(1)
+
+
+def _time_flushed(fn, flush, iters: int = 15, warm: int = 3) -> float:
+    """median ms of one call of fn, L2 flushed before every timed call; CUDA
+    events on the current stream (the library's calls are queued on it)."""
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(iters):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def _time_cpu(fn, reps: int = 1) -> float:
+    """seconds of one call of fn on the host cores (best of reps, after one
+    untimed call)."""
+    fn()
+    best = None
+    for _ in range(reps):
+        t = time.perf_counter()
+        fn()
+        dt = time.perf_counter() - t
+        best = dt if best is None else min(best, dt)
+    return best
+
+
+def per_config(device, with_oracle: bool = True) -> dict:
+    """Workloads 1-4 timed in the bench's process: each row's GPU time (median
+    of flushed single calls, CUDA events), its throughput and fraction of the
+    burst peaks, and the oracle's time for the same work (or a stated sample
+    of it) on the host cores."""
+    import scaled_quantize_gemm_gb300 as sq
+    hbm, bf16_burst, _, src = _peaks()
+    fp8 = 2.0 * bf16_burst
+    flush = _L2Flush(device)
+    u8 = dict(dtype=torch.uint8, device=device)
+    f32 = dict(dtype=torch.float32, device=device)
+    o = None
+    if with_oracle:
+        import oracle as o
+        o.build()
+    cores = len(os.sched_getaffinity(0))
+
+    def gemm_row(ms, flops, extra=None):
+        r = {"ms": round(ms, 5), "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1)}
+        r["frac"] = round(r["TFLOP/s"] / fp8, 4)
+        r.update(extra or {})
+        return r
+
+    def bytes_row(ms, nbytes, extra=None):
+        r = {"ms": round(ms, 5), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+        r["frac"] = round(r["GB/s"] / hbm, 4)
+        r.update(extra or {})
+        return r
+
+    out = {"peaks": {"fp8_tflops": round(fp8, 1), "hbm_gbs": hbm,
+                     "source": f"burst: 2 x bf16_tflops and hbm_gbs {src}"},
+           "timing": "median of 15 single calls, L2 flushed (256 MB write) before each, CUDA events",
+           "oracle_cores": cores}
+
+    # ---- workload 1: per-tensor current scaling, 256^3, fp32 in and out
+    a, b = wl.w1_operands(device)
+    qa, qb = torch.empty((256, 256), **u8), torch.empty((256, 256), **u8)
+    sa, sb, aa, ab = (torch.empty(1, **f32) for _ in range(4))
+    y1 = torch.empty((256, 256), **f32)
+
+    def lin1():
+        sq.fp8_quantize(a, sq.E4M3, sq.TENSOR, qa, scales_out=sa, amax_out=aa)
+        sq.fp8_quantize(b, sq.E4M3, sq.TENSOR, qb, scales_out=sb, amax_out=ab)
+        sq.fp8_gemm(qa, sq.E4M3, sa, sq.TENSOR, qb, sq.E4M3, sb, sq.TENSOR, y1)
+    row = gemm_row(_time_flushed(lin1, flush), 2 * 256 ** 3,
+                   {"what": "current-scaled linear: quantize A, B (amax + cast each) + GEMM, fp32 out"})
+    if o is not None:
+        an, bn = a.cpu().numpy(), b.cpu().numpy()
+
+        def olin1():
+            qa_, _, sa_, _ = o.quantize_tensor_current(an, o.E4M3)
+            qb_, _, sb_, _ = o.quantize_tensor_current(bn, o.E4M3)
+            return o.gemm_ref(o.dequantize(qa_, 0, 0, sa_), o.dequantize(qb_, 0, 0, sb_))
+        row["oracle_ms"] = round(_time_cpu(olin1, 3) * 1e3, 3)
+    out["1"] = {"workload": wl.WORKLOADS[1].name, "linear": row}
+    del a, b, qa, qb, y1
+
+    # ---- workload 2: MiniGPT linears, one training step of all three
+    W2 = wl.WORKLOADS[2]
+    lay = []
+    flops2 = 0
+    for li, lin in enumerate(W2.linears):
+        M, K, N = W2.tokens, lin.in_features, lin.out_features
+        st = torch.empty(3 * (H + 2), **f32)
+        sq.fp8_scale_init(st, 3, H)
+        lay.append(dict(M=M, K=K, N=N, x=wl.linear_x(2, li, 0, M, K, device), w=wl.linear_w(2, li, N, K, device),
+                        dy=wl.linear_dy(2, li, 0, M, N, device), st=st,
+                        ws=torch.empty(sq.fp8_linear_workspace_bytes(M, N, K), **u8),
+                        y=torch.empty((M, N), dtype=torch.bfloat16, device=device),
+                        dx=torch.empty((M, K), dtype=torch.bfloat16, device=device),
+                        dw=torch.empty((N, K), **f32)))
+        flops2 += 6 * M * N * K
+    fm2 = [sq.E4M3, sq.E4M3, sq.E5M2]
+
+    def step2():
+        for L in lay:
+            s_ = [L["st"][i * (H + 2):(i + 1) * (H + 2)] for i in range(3)]
+            sq.fp8_linear_fwd(L["x"], L["w"], L["y"], L["ws"], x_state=s_[0], w_state=s_[1], history_len=H)
+            sq.fp8_linear_bwd(L["dy"], L["dx"], L["dw"], L["ws"], L["K"], dy_state=s_[2], history_len=H)
+            sq.fp8_update_scale(L["st"], 3, H, fm2)
+    row = gemm_row(_time_flushed(step2, flush), flops2,
+                   {"what": "one training step of the three linears (fwd + dgrad + wgrad + scale update, "
+                            "delayed HYBRID), eager calls"})
+    if o is not None:
+        host = [(L["x"].float().cpu().numpy(), L["w"].float().cpu().numpy(), L["dy"].float().cpu().numpy())
+                for L in lay]
+        ost = [[o.state_init(H) for _ in range(3)] for _ in lay]
+
+        def ostep2():
+            for (xn, wn, dn), s_ in zip(host, ost):
+                qx, sx, qw, sw, _ = o.linear_fwd_delayed(xn, wn, s_[0], s_[1])
+                o.linear_bwd_delayed(dn, s_[2], o.E5M2, qx, sx, qw, sw)
+                for r, f in zip(s_, (o.E4M3, o.E4M3, o.E5M2)):
+                    o.update_scale(r, f)
+        row["oracle_ms"] = round(_time_cpu(ostep2) * 1e3, 1)
+    out["2"] = {"workload": W2.name, "step": row}
+    del lay
+
+    # ---- workload 3: fine-grained current scaling, 4096^3
+    x3, w3 = wl.w3_operands(device)
+    dy3 = wl.normal((4096, 4096), 1e-3, wl.seed_of(3, 0, wl.ROLE_DY), device)
+    n3 = 4096
+    ws3 = torch.empty(sq.fp8_linear_workspace_bytes(n3, n3, n3, sq.TILE_1x128), **u8)
+    y3 = torch.empty((n3, n3), dtype=torch.bfloat16, device=device)
+    dx3 = torch.empty((n3, n3), dtype=torch.bfloat16, device=device)
+    dw3 = torch.empty((n3, n3), **f32)
+    qx3, qw3 = torch.empty((n3, n3), **u8), torch.empty((n3, n3), **u8)
+    sx3, sw3 = torch.empty(n3 * 32, **f32), torch.empty(32 * 32, **f32)
+    fl3 = 2 * n3 ** 3
+    r3 = {}
+    r3["quantize_x_1x128"] = bytes_row(
+        _time_flushed(lambda: sq.fp8_quantize(x3, sq.E4M3, sq.TILE_1x128, qx3, scales_out=sx3), flush),
+        n3 * n3 * 3 + 4 * n3 * 32, {"kernel": "k_quant_rowunits<128>"})
+    r3["quantize_w_128x128"] = bytes_row(
+        _time_flushed(lambda: sq.fp8_quantize(w3, sq.E4M3, sq.BLOCK_128x128, qw3, scales_out=sw3), flush),
+        n3 * n3 * 3 + 4 * 32 * 32, {"kernel": "k_quant_block128"})
+    r3["gemm"] = gemm_row(
+        _time_flushed(lambda: sq.fp8_gemm(qx3, sq.E4M3, sx3, sq.TILE_1x128, qw3, sq.E4M3, sw3, sq.BLOCK_128x128, y3),
+                      flush), fl3, {"kernel": "k_gemm_promote (1x128 x 128x128, promotion per 128 K)"})
+    r3["linear_fwd"] = gemm_row(
+        _time_flushed(lambda: sq.fp8_linear_fwd(x3, w3, y3, ws3, gran=sq.TILE_1x128), flush), fl3,
+        {"what": "fp8_linear_fwd TILE_1x128: x rows + columns in one pass, W blocks + transpose, GEMM"})
+    r3["linear_bwd"] = gemm_row(
+        _time_flushed(lambda: sq.fp8_linear_bwd(dy3, dx3, dw3, ws3, n3, gran=sq.TILE_1x128), flush), 2 * fl3,
+        {"what": "fp8_linear_bwd TILE_1x128: dy rows + columns, dgrad (promotion) + wgrad (column tiles)"})
+    if o is not None:
+        rows = 256
+        xn, wn = x3.float().cpu().numpy(), w3.float().cpu().numpy()
+
+        def olin3():
+            qx_, sx_, _, _ = o.quantize_tile1x128(xn[:rows], o.E4M3)
+            qw_, sw_, _, _ = o.quantize_block128(wn, o.E4M3)
+            return o.gemm_ref(o.dequantize(qx_, 0, o.GRAN_TILE_1x128, sx_),
+                              o.dequantize(qw_, 0, o.GRAN_BLOCK_128x128, sw_))
+        t = _time_cpu(olin3)
+        r3["linear_fwd"]["oracle_ms"] = round(t * 1e3, 1)
+        r3["linear_fwd"]["oracle_sample"] = f"{rows} of 4096 rows of x (all of W quantised)"
+        r3["linear_fwd"]["oracle_TFLOP/s"] = round(2 * rows * n3 * n3 / t / 1e12, 6)
+    out["3"] = {"workload": wl.WORKLOADS[3].name, **r3}
+    del x3, w3, dy3, ws3, y3, dx3, dw3, qx3, qw3
+    torch.cuda.empty_cache()
+
+    # ---- workload 4: MX-32, 8192^3
+    a4, b4 = wl.w4_operands(device)
+    n4 = 8192
+    qa4, qb4 = torch.empty((n4, n4), **u8), torch.empty((n4, n4), **u8)
+    ea4, eb4 = torch.empty(n4 * n4 // 32, **u8), torch.empty(n4 * n4 // 32, **u8)
+    y4 = torch.empty((n4, n4), dtype=torch.bfloat16, device=device)
+    fl4 = 2 * n4 ** 3
+    r4 = {}
+    r4["quantize_mx32"] = bytes_row(
+        _time_flushed(lambda: sq.fp8_quantize(a4, sq.E4M3, sq.MX32_TILED, qa4, scales_out=ea4), flush),
+        n4 * n4 * 3 + n4 * n4 // 32, {"kernel": "k_quant_rowunits<32>"})
+    sq.fp8_quantize(b4, sq.E4M3, sq.MX32_TILED, qb4, scales_out=eb4)
+    r4["gemm"] = gemm_row(
+        _time_flushed(lambda: sq.fp8_gemm(qa4, sq.E4M3, ea4, sq.MX32_TILED, qb4, sq.E4M3, eb4, sq.MX32_TILED, y4),
+                      flush), fl4, {"kernel": "k_gemm_mx (kind::mxf8f6f4.block_scale)"})
+
+    def lin4():
+        sq.fp8_quantize(a4, sq.E4M3, sq.MX32_TILED, qa4, scales_out=ea4)
+        sq.fp8_quantize(b4, sq.E4M3, sq.MX32_TILED, qb4, scales_out=eb4)
+        sq.fp8_gemm(qa4, sq.E4M3, ea4, sq.MX32_TILED, qb4, sq.E4M3, eb4, sq.MX32_TILED, y4)
+    r4["linear"] = gemm_row(_time_flushed(lin4, flush), fl4,
+                            {"what": "quantize A, B (MX-32) + block-scaled GEMM, bf16 out"})
+    if o is not None:
+        rows = 64
+        an, bn = a4.float().cpu().numpy(), b4.float().cpu().numpy()
+
+        def olin4():
+            qa_, ea_, _, _ = o.quantize_mx32(an[:rows], o.E4M3)
+            qb_, eb_, _, _ = o.quantize_mx32(bn, o.E4M3)
+            return o.gemm_ref(o.dequantize(qa_, 0, o.GRAN_MX32, ea_), o.dequantize(qb_, 0, o.GRAN_MX32, eb_))
+        t = _time_cpu(olin4)
+        r4["linear"]["oracle_ms"] = round(t * 1e3, 1)
+        r4["linear"]["oracle_sample"] = f"{rows} of 8192 rows of A (all of B quantised)"
+        r4["linear"]["oracle_TFLOP/s"] = round(2 * rows * n4 * n4 / t / 1e12, 6)
+    out["4"] = {"workload": wl.WORKLOADS[4].name, **r4}
+    del a4, b4, qa4, qb4, ea4, eb4, y4, flush
+    torch.cuda.empty_cache()
+    if sq.fp8_device_status(True) != 0:
+        raise RuntimeError("device status error in the per-workload rows")
+    return out
 
 
 # ---------------------------------------------------------------- CPU oracle
@@ -941,6 +1182,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the rows of workloads 1-4 (timed after the headline step)")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     args = ap.parse_args()
     if args.warmup < 3:

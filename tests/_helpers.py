@@ -2,7 +2,7 @@
 
 GEMM tolerance (the 1e-3 bound on maximum relative error): for fp32 output,
 max|C - R| <= 1e-3 * max|R|, R the oracle's float64 result.  For bf16 output
-the output rounding itself is up to half a bf16 ulp (2^-9 relative), so each
+the output rounding itself is up to half a bf16 ulp (2^-8 relative), so each
 element must satisfy |C - R| <= 1e-3 * max|R| + ulp_bf16(C) / 2: C is the
 bf16 rounding of a value within the 1e-3 bound.
 
@@ -11,7 +11,7 @@ error max |C_ij - R_ij| / |R_ij| over the elements with |R_ij| >= 1e-2 max|R|
 (small outputs, which the norm bound barely constrains: it lets an element at
 1e-2 max|R| be 10 % off).  It must stay within ELEM_TOL_F32 for fp32 outputs
 (fp32 accumulation error only) and within ELEM_TOL_BF16 for bf16 outputs
-(half a bf16 ulp, 2^-9, plus the same accumulation slack).  With SQ_ERR_REPORT=<path> set, each check appends one
+(half a bf16 ulp, 2^-8 of the value, plus the same accumulation slack).  With SQ_ERR_REPORT=<path> set, each check appends one
 JSON line (test, shape, dtype, both errors) to that file.
 """
 import json
@@ -46,10 +46,12 @@ def gemm_error(C: torch.Tensor, R: np.ndarray) -> float:
 
 
 ELEM_FLOOR = 1e-2          # elements with |R_ij| >= ELEM_FLOOR * max|R| enter the elementwise error
-# fp32 summation of K products: the rounding error grows like 2^-24 sqrt(K)
-# relative to a typical |R_ij|, i.e. up to ~6e-4 at 1e-2 max|R| for K = 16384
-ELEM_TOL_F32 = 2e-3
-ELEM_TOL_BF16 = 2.0 ** -9 + 2e-3
+# fp32 accumulation error only: measured at most 3.8e-5 (K = 16384, the FFN
+# wgrad) and below 8e-6 for K <= 4096 on the GB300
+ELEM_TOL_F32 = 1e-4
+# the bf16 output rounding is up to half an ulp, 2^-8 of the value, plus the
+# same accumulation slack
+ELEM_TOL_BF16 = 2.0 ** -8 + 1e-4
 
 
 def elementwise_rel_error(c: np.ndarray, R: np.ndarray, floor: float = ELEM_FLOOR) -> float:
