@@ -259,14 +259,6 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cl_addr)
 {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr) : "memory");
 }
-// relaxed arrive on an mbarrier of any CTA of the cluster: no release fence.
-// For a thread that only read tensor memory (and waited for those reads with
-// tcgen05.wait::ld) before arriving, nothing needs publishing: the reads are
-// complete when the arrival is issued.
-__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cl_addr)
-{
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr) : "memory");
-}
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
