@@ -1,0 +1,174 @@
+"""Tensor-parallel column-parallel FP8 linear ("Transformer Scaling",
+Part 03 and "04 · Put it back into code -- Program model": each TP rank
+computes a local linear, launches an all-gather of its output asynchronously,
+runs independent work in the window, and waits at the first consumer of the
+gathered result).
+
+W [N][K] is sharded along N: rank r owns rows [r N/P, (r+1) N/P).  Per step,
+with per-tensor delayed scaling under the HYBRID recipe:
+
+  forward   y_r = x W_r^T          (x replicated; the rank's own FP8 GEMM on
+                                    local operands only)
+            y   = all-gather_r(y_r) (asynchronous; a handle is returned)
+  backward  dx  = sum_r dy_r W_r    (dy_r = the rank's N-columns of dy; the
+                                    partial products are all-reduced, summed)
+            dW_r = dy_r^T x         (local, no exchange)
+  step end  the amax just recorded in each state's history slot 0 is
+            all-reduced (max) before the scale update, so every rank's
+            x, W and dy states stay bit-identical, and equal to the states of
+            the unsharded layer (the amax of a sharded tensor is the max of
+            its shards' amaxes).
+
+The exchange steps are torch.distributed collectives on the given process
+group; the arithmetic of each rank runs in `ops`.  The default `ops`
+(LibraryOps) is this library's CUDA path through the C ABI; a caller may
+pass another implementation of the same five methods (the tests drive the
+orchestration on CPU ranks this way).
+"""
+from __future__ import annotations
+
+import torch
+import torch.distributed as dist
+
+
+def shard_rows(w: torch.Tensor, rank: int, world: int) -> torch.Tensor:
+    """Rows [rank N/P, (rank+1) N/P) of w [N][K] (N % P == 0), contiguous."""
+    n = w.shape[0]
+    if n % world:
+        raise ValueError(f"N = {n} is not divisible by the tensor-parallel size {world}")
+    step = n // world
+    return w[rank * step:(rank + 1) * step].contiguous()
+
+
+def shard_cols(t: torch.Tensor, rank: int, world: int) -> torch.Tensor:
+    """Columns [rank N/P, (rank+1) N/P) of t [M][N], contiguous (the rank's
+    part of the output gradient of a column-parallel linear)."""
+    n = t.shape[1]
+    if n % world:
+        raise ValueError(f"N = {n} is not divisible by the tensor-parallel size {world}")
+    step = n // world
+    return t[:, rank * step:(rank + 1) * step].contiguous()
+
+
+class GatherHandle:
+    """An all-gather in flight: `wait()` blocks (on the host for CPU
+    collectives, on the current stream for device ones) until the gathered
+    output may be read, and returns it as y [M][N]."""
+
+    def __init__(self, work, parts: torch.Tensor, M: int, N: int):
+        self._work = work
+        self._parts = parts          # [P][M][N/P], rank-major
+        self._M, self._N = M, N
+        self._out = None
+
+    def wait(self) -> torch.Tensor:
+        if self._out is None:
+            if self._work is not None:
+                self._work.wait()
+            # rank-major [P][M][N/P] -> [M][N]: rank r's block is columns [r N/P, (r+1) N/P)
+            self._out = self._parts.permute(1, 0, 2).reshape(self._M, self._N)
+        return self._out
+
+
+class LibraryOps:
+    """Per-rank arithmetic on this library's CUDA path: per-tensor delayed
+    casts (with transposed copies) and FP8 GEMMs through the C ABI, states in
+    one device block of three (x, W, dy)."""
+
+    def __init__(self, M: int, N_local: int, K: int, history_len: int, device, recipe_e4m3: bool = False):
+        import scaled_quantize_gemm_gb300 as sq
+        self.sq = sq
+        self.H = history_len
+        self.M, self.N, self.K = M, N_local, K
+        u8 = dict(dtype=torch.uint8, device=device)
+        self.qx, self.qxT = torch.empty((M, K), **u8), torch.empty((K, M), **u8)
+        self.qw, self.qwT = torch.empty((N_local, K), **u8), torch.empty((K, N_local), **u8)
+        self.qdy, self.qdyT = torch.empty((M, N_local), **u8), torch.empty((N_local, M), **u8)
+        self.states = torch.empty(3 * (history_len + 2), dtype=torch.float32, device=device)
+        sq.fp8_scale_init(self.states, 3, history_len)
+        self.dy_fmt = sq.E4M3 if recipe_e4m3 else sq.E5M2
+        self.formats = [sq.E4M3, sq.E4M3, self.dy_fmt]
+
+    def _st(self, i):
+        return self.states[i * (self.H + 2):(i + 1) * (self.H + 2)]
+
+    def _s(self, i):
+        j = i * (self.H + 2) + self.H + 1
+        return self.states[j:j + 1]
+
+    def forward(self, x: torch.Tensor, w_local: torch.Tensor) -> torch.Tensor:
+        sq, H = self.sq, self.H
+        sq.fp8_quantize(x, sq.E4M3, sq.TENSOR, self.qx, qT=self.qxT, delayed_state=self._st(0), history_len=H)
+        sq.fp8_quantize(w_local, sq.E4M3, sq.TENSOR, self.qw, qT=self.qwT, delayed_state=self._st(1),
+                        history_len=H)
+        y = torch.empty((self.M, self.N), dtype=torch.bfloat16, device=x.device)
+        sq.fp8_gemm(self.qx, sq.E4M3, self._s(0), sq.TENSOR, self.qw, sq.E4M3, self._s(1), sq.TENSOR, y)
+        return y
+
+    def backward(self, dy_local: torch.Tensor):
+        """-> (dx partial fp32 [M][K], dW_local fp32 [N/P][K])"""
+        sq, H = self.sq, self.H
+        sq.fp8_quantize(dy_local, self.dy_fmt, sq.TENSOR, self.qdy, qT=self.qdyT, delayed_state=self._st(2),
+                        history_len=H)
+        dx = torch.empty((self.M, self.K), dtype=torch.float32, device=dy_local.device)
+        dw = torch.empty((self.N, self.K), dtype=torch.float32, device=dy_local.device)
+        sq.fp8_gemm(self.qdy, self.dy_fmt, self._s(2), sq.TENSOR, self.qwT, sq.E4M3, self._s(1), sq.TENSOR, dx)
+        sq.fp8_gemm(self.qdyT, self.dy_fmt, self._s(2), sq.TENSOR, self.qxT, sq.E4M3, self._s(0), sq.TENSOR, dw)
+        return dx, dw
+
+    def recorded_amax(self) -> torch.Tensor:
+        """history slot 0 of the x, W and dy states (3 floats, a copy)"""
+        H = self.H
+        return self.states[0::H + 2][:3].clone()
+
+    def set_recorded_amax(self, a: torch.Tensor) -> None:
+        H = self.H
+        self.states[0::H + 2][:3].copy_(a)
+
+    def update_scale(self) -> None:
+        self.sq.fp8_update_scale(self.states, 3, self.H, self.formats)
+
+
+class ColumnParallelFP8Linear:
+    """One column-parallel FP8 linear of a TP group (see the module text).
+
+    w_local: this rank's rows of W ([N/P][K]).  `ops` defaults to LibraryOps
+    on w_local's device."""
+
+    def __init__(self, w_local: torch.Tensor, M: int, history_len: int = 16, group=None, ops=None,
+                 recipe_e4m3: bool = False):
+        self.group = group
+        self.world = dist.get_world_size(group)
+        self.rank = dist.get_rank(group)
+        self.w = w_local
+        self.M = M
+        self.N_local, self.K = w_local.shape
+        self.N = self.N_local * self.world
+        self.ops = ops if ops is not None else LibraryOps(M, self.N_local, self.K, history_len, w_local.device,
+                                                          recipe_e4m3)
+
+    def forward_async(self, x: torch.Tensor) -> GatherHandle:
+        """Local linear, then an asynchronous all-gather of its output along
+        N; run independent work before calling wait() on the handle."""
+        y_local = self.ops.forward(x, self.w)
+        # rank-major concatenation along the first dimension: [P M][N/P]
+        parts = torch.empty((self.world * self.M, self.N_local), dtype=y_local.dtype, device=y_local.device)
+        work = dist.all_gather_into_tensor(parts, y_local.contiguous(), group=self.group, async_op=True)
+        return GatherHandle(work, parts.view(self.world, self.M, self.N_local), self.M, self.N)
+
+    def backward(self, dy: torch.Tensor):
+        """dy: the full output gradient [M][N] (replicated) or this rank's
+        columns [M][N/P].  Returns (dx fp32 [M][K], summed over the group;
+        dW_local fp32 [N/P][K])."""
+        dy_local = dy if dy.shape[1] == self.N_local else shard_cols(dy, self.rank, self.world)
+        dx, dw = self.ops.backward(dy_local)
+        dist.all_reduce(dx, op=dist.ReduceOp.SUM, group=self.group)
+        return dx, dw
+
+    def end_step(self) -> None:
+        """All-reduce (max) the amaxes the step recorded, then update the
+        scales: every rank ends the step with the same x, W and dy states."""
+        a = self.ops.recorded_amax()
+        dist.all_reduce(a, op=dist.ReduceOp.MAX, group=self.group)
+        self.ops.set_recorded_amax(a)
+        self.ops.update_scale()

@@ -1,0 +1,59 @@
+"""The column-parallel FP8 linear's per-rank path on the GPU (LibraryOps:
+delayed per-tensor casts and FP8 GEMMs through the C ABI), in a
+tensor-parallel group of one rank on NCCL: the gathered output, the input
+gradient (fp32, all-reduced) and the weight gradient against the oracle,
+histories bit-exact every step.  The two-rank exchange logic is covered on
+CPU ranks (tests/test_tp_gloo.py); this run uses one GPU."""
+import datetime
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+
+import oracle as o
+import scaled_quantize_gemm_gb300 as sq
+from scaled_quantize_gemm_gb300 import tp
+from scaled_quantize_gemm_gb300 import workloads as wl
+
+from _helpers import assert_gemm_close, np32
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def test_column_parallel_linear_one_rank_matches_oracle():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1,
+                            timeout=datetime.timedelta(seconds=120), device_id=torch.device(DEV, 0))
+    try:
+        M, K, N, H = 256, 384, 512, 16
+        w = wl.normal((N, K), 0.02, 71).to(DEV)
+        layer = tp.ColumnParallelFP8Linear(tp.shard_rows(w, 0, 1), M, history_len=H)
+        ref = [o.state_init(H) for _ in range(3)]
+        qo, so = torch.empty((128, K), dtype=torch.uint8, device=DEV), torch.empty(1, device=DEV)
+        ao = torch.empty(1, device=DEV)
+        for step in range(4):
+            x = wl.normal((M, K), 1.0 + step, 72 + step).to(DEV)
+            dy = wl.normal((M, N), 1e-3 * (30.0 if step == 2 else 1.0), 80 + step).to(DEV)
+            handle = layer.forward_async(x)
+            # independent work in the window: another cast of the same input
+            sq.fp8_quantize(x[:128], sq.E4M3, sq.TENSOR, qo, scales_out=so, amax_out=ao)
+            y = handle.wait()
+            dx, dw = layer.backward(dy)
+            layer.end_step()
+            torch.cuda.synchronize()
+            qx, sx, qw, sw, Y = o.linear_fwd_delayed(np32(x), np32(w), ref[0], ref[1])
+            _, _, dX, dW = o.linear_bwd_delayed(np32(dy), ref[2], o.E5M2, qx, sx, qw, sw)
+            for r, f in zip(ref, (o.E4M3, o.E4M3, o.E5M2)):
+                o.update_scale(r, f)
+            assert_gemm_close(y, Y)
+            assert_gemm_close(dx, dX)
+            assert_gemm_close(dw, dW)
+            assert layer.ops.states.cpu().numpy().tobytes() == np.concatenate(ref).tobytes(), step
+        assert sq.fp8_device_status(True) == 0
+    finally:
+        dist.destroy_process_group()
