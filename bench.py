@@ -6,10 +6,10 @@ training step (M = 16384 tokens, HYBRID per-tensor delayed scaling, amax
 history 16): x -> linear 0 (4096 -> 14336) -> y0 -> linear 1 (14336 -> 4096)
 -> y1, then back: the upstream gradient dy of y1 -> linear 1's dgrad and
 wgrad -> dx1, which is linear 0's output gradient -> linear 0's dgrad and
-wgrad.  Per linear: quantize its input and W (E4M3, with transposed copies),
-forward GEMM, quantize its output gradient (E5M2, with transposed copy),
-dgrad GEMM, wgrad GEMM; then the end-of-step scale update of all six tensor
-roles.  The step's inputs are x and dy; y0 and dx1 stay on the device.
+wgrad.  Per linear: quantize its input and W (E4M3), forward GEMM, quantize
+its output gradient (E5M2), dgrad and wgrad GEMMs (which read the codes
+MN-major, so no cast writes a transposed copy); then the end-of-step scale
+update of all six tensor roles.  The step's inputs are x and dy; y0 and dx1 stay on the device.
 Every step runs in this library's kernels through its C ABI.
 
 Metric: FP8 linear TFLOP/s = GEMM FLOPs (2MNK per GEMM, six per step) per
@@ -59,14 +59,14 @@ CSRC = os.path.join(ROOT, "scaled_quantize_gemm_gb300", "csrc")
 KERNEL_SOURCES = {   # file, [(start marker or None = file start, end marker)]: helpers + kernel + launch config
     "k_gemm_tensor_pair": ("gemm.cu", [(None, "// ================================================================== mode 1"),
                                        ("    if (g.mode == 0) {", "    if (g.mode == 1)")]),
-    "k_cast_tensor_T": ("quantize.cu", [(None, "// ================================================================== per-tensor\n"),
-                                        ("// Row-wise LayerNorm folded into the cast",
-                                         "// ================================================================== column units"),
-                                        ("        if (a.qT) {", "        } else {")]),
+    "k_cast_tensor": ("quantize.cu", [(None, "// ================================================================== per-tensor\n"),
+                                      ("// Cast pass of per-tensor scaling without a transposed copy",
+                                       "// 8x8 byte transpose"),
+                                      ("            int g = flat_grid(n / 8, sms);", "        return cudaGetLastError();")]),
 }
 TRAFFIC = {
-    "k_gemm_tensor_pair": {"sha": "60e46bcbee106212", "bytes": 971203072},
-    "k_cast_tensor_T": {"sha": "68f2b59d0aab2c82", "bytes": 892547584},
+    "k_gemm_tensor_pair": {"sha": None, "bytes": None},
+    "k_cast_tensor": {"sha": None, "bytes": None},
 }
 
 
@@ -193,9 +193,7 @@ class FFNStep:
         self.buf = []
         for li, (K, N) in enumerate(self.lin):
             self.buf.append(dict(
-                qx=torch.empty((M, K), **u8), qxT=torch.empty((K, M), **u8),
-                qw=torch.empty((N, K), **u8), qwT=torch.empty((K, N), **u8),
-                qdy=torch.empty((M, N), **u8), qdyT=torch.empty((N, M), **u8),
+                qx=torch.empty((M, K), **u8), qw=torch.empty((N, K), **u8), qdy=torch.empty((M, N), **u8),
                 y=torch.empty((M, N), dtype=torch.bfloat16, device=device),
                 dx=torch.empty((M, K), dtype=torch.bfloat16, device=device),
                 dw=torch.empty((N, K), dtype=torch.float32, device=device),
@@ -215,9 +213,10 @@ class FFNStep:
         return sum(3 * 2 * M * N * K for (K, N) in self.lin)
 
     def quant_bytes_per_step(self):
-        # bf16 read + code write + transposed code write, per element
+        # bf16 read + code write per element (the backward GEMMs read the
+        # codes MN-major: no transposed copy)
         M = self.M
-        return sum(4 * (M * K + N * K + M * N) for (K, N) in self.lin)
+        return sum(3 * (M * K + N * K + M * N) for (K, N) in self.lin)
 
     def step(self, s: int, ev=None):
         """One pass of the hot path through the granular C-ABI calls; `ev`
@@ -239,12 +238,14 @@ class FFNStep:
             ev.append((kind, a, b))
 
         xin = x
+        K_, MN_ = sq.K_MAJOR, sq.MN_MAJOR
         for li in range(L):                          # forward, first linear first
             B = self.buf[li]
+            K, N = self.lin[li]
             sx, sw = 3 * li, 3 * li + 1
-            rec("quant", lambda: sq.fp8_quantize(xin, sq.E4M3, sq.TENSOR, B["qx"], qT=B["qxT"],
+            rec("quant", lambda: sq.fp8_quantize(xin, sq.E4M3, sq.TENSOR, B["qx"],
                                                  delayed_state=self.st(sx), history_len=H))
-            rec("quant", lambda: sq.fp8_quantize(self.W[li], sq.E4M3, sq.TENSOR, B["qw"], qT=B["qwT"],
+            rec("quant", lambda: sq.fp8_quantize(self.W[li], sq.E4M3, sq.TENSOR, B["qw"],
                                                  delayed_state=self.st(sw), history_len=H))
             rec("gemm", lambda: sq.fp8_gemm(B["qx"], sq.E4M3, self.s(sx), sq.TENSOR,
                                             B["qw"], sq.E4M3, self.s(sw), sq.TENSOR, B["y"]))
@@ -252,13 +253,16 @@ class FFNStep:
         dyin = dy
         for li in reversed(range(L)):                # backward, last linear first
             B = self.buf[li]
+            K, N = self.lin[li]
             sx, sw, sd = 3 * li, 3 * li + 1, 3 * li + 2
-            rec("quant", lambda: sq.fp8_quantize(dyin, sq.E5M2, sq.TENSOR, B["qdy"], qT=B["qdyT"],
+            rec("quant", lambda: sq.fp8_quantize(dyin, sq.E5M2, sq.TENSOR, B["qdy"],
                                                  delayed_state=self.st(sd), history_len=H))
-            rec("gemm", lambda: sq.fp8_gemm(B["qdy"], sq.E5M2, self.s(sd), sq.TENSOR,
-                                            B["qwT"], sq.E4M3, self.s(sw), sq.TENSOR, B["dx"]))
-            rec("gemm", lambda: sq.fp8_gemm(B["qdyT"], sq.E5M2, self.s(sd), sq.TENSOR,
-                                            B["qxT"], sq.E4M3, self.s(sx), sq.TENSOR, B["dw"]))
+            # dgrad dx[M][K] = dy W: B = W's codes [N][K], MN-major
+            rec("gemm", lambda: sq.fp8_gemm_layout(B["qdy"], sq.E5M2, self.s(sd), K_, B["qw"], sq.E4M3, self.s(sw),
+                                                   MN_, B["dx"], self.M, K, N))
+            # wgrad dW[N][K] = dy^T x: A = dy's codes [M][N], B = x's codes [M][K], both MN-major
+            rec("gemm", lambda: sq.fp8_gemm_layout(B["qdy"], sq.E5M2, self.s(sd), MN_, B["qx"], sq.E4M3, self.s(sx),
+                                                   MN_, B["dw"], N, K, self.M))
             dyin = B["dx"]
         rec("update", lambda: sq.fp8_update_scale(self.states, 6, H, self.formats))
 
@@ -388,7 +392,7 @@ def run_ours(args, ws, rank, local):
     # the largest casts (16384 x 14336): y0 as linear 1's input, dx1 as linear
     # 0's output gradient (positions 2 and 5 of the step's six casts)
     big = [per["quant"][i] for i in range(len(per["quant"])) if i % 6 in (2, 5)]
-    big_bytes = 4 * WK.tokens * 14336
+    big_bytes = 3 * WK.tokens * 14336
     big_gbs = big_bytes / (statistics.mean(big) * 1e-3) / 1e9
 
     # ---- end to end through the linear API with pinned host buffers
@@ -487,9 +491,9 @@ def run_ours(args, ws, rank, local):
                          "peak_burst": round(fp8_peak, 1), "frac_of_burst": round(achieved / fp8_peak, 4),
                          "peak_sustained": round(fp8_sust, 1), "frac_of_sustained": round(achieved / fp8_sust, 4),
                          "flops_per_launch": gemm_flops_launch, "launch_ms": round(gemm_ms, 4)},
-            "roofline_quantize": {"bound": "hbm", "kernel": "k_cast_tensor_T (16384 x 14336 casts)",
+            "roofline_quantize": {"bound": "hbm", "kernel": "k_cast_tensor (16384 x 14336 casts)",
                                   "achieved": round(big_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                                  "frac": round(big_gbs / hbm_peak, 4), "traffic": kernel_traffic("k_cast_tensor_T"),
+                                  "frac": round(big_gbs / hbm_peak, 4), "traffic": kernel_traffic("k_cast_tensor"),
                                   "peak_source": f"hbm_gbs {peak_src}",
                                   "bytes_per_launch": big_bytes},
             "quantize": {"GB_per_s_all_casts": round(quant_gbs, 1), "ms_per_step": round(quant_ms_step, 4),
@@ -833,8 +837,8 @@ def run_reference(args, ws, rank, local):
 def kernel_case(case: str, launches: int):
     """A handful of launches of one kernel at the workload's size, for
     profiling a single launch: 'gemm' = the 16384 x 14336 x 4096 forward GEMM
-    (k_gemm_tensor_pair), 'cast' = the 16384 x 14336 E5M2 cast with its transposed
-    copy (k_cast_tensor_T), 'promote' = the 4096^3 1x128 x 128x128 GEMM
+    (k_gemm_tensor_pair), 'cast' = the 16384 x 14336 E5M2 delayed cast
+    (k_cast_tensor), 'promote' = the 4096^3 1x128 x 128x128 GEMM
     (k_gemm_promote), 'wgrad' = the 4096^3 column-tile GEMM (k_gemm_promote, per-column
     scales, fp32 out), 'mx' = the 8192^3 MX-32 GEMM (k_gemm_mx), 'fine' = the
     fine-grained casts (1x128, 128x128, MX-32 tiled, 128x1 columns), 'ln' =
@@ -848,9 +852,9 @@ def kernel_case(case: str, launches: int):
     if case == "cast":
         M, N = WK.tokens, 14336
         dy = wl.linear_dy(5, 0, 0, M, N, dev)
-        q, qT = torch.empty((M, N), **u8), torch.empty((N, M), **u8)
+        q = torch.empty((M, N), **u8)
         for _ in range(launches):
-            sq.fp8_quantize(dy, sq.E5M2, sq.TENSOR, q, qT=qT, delayed_state=st, history_len=H)
+            sq.fp8_quantize(dy, sq.E5M2, sq.TENSOR, q, delayed_state=st, history_len=H)
     elif case == "gemm":
         M, K, N = WK.tokens, 4096, 14336
         x = wl.linear_x(5, 0, 0, M, K, dev)

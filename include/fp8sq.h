@@ -252,6 +252,25 @@ FP8SQ_API int fp8_gemm(const uint8_t* A, int a_format, const void* a_scale, int 
                        int64_t M, int64_t N, int64_t K, const float* bias, void* D, int d_dtype,
                        void* stream);
 
+/* fp8_gemm_layout: fp8_gemm with per-tensor scales (a_gran = b_gran =
+ * TENSOR) whose operands may also be stored MN-major:
+ *   a_major K_MAJOR: A [M][K] (K contiguous);  MN_MAJOR: A [K][M] (M contiguous)
+ *   b_major K_MAJOR: B [N][K] (K contiguous);  MN_MAJOR: B [K][N] (N contiguous)
+ * The linear layer's backward products read the forward codes as they are
+ * ([W14] FP8 bullet; [TS] core vocabulary: a scaling scheme should not add
+ * passes over the tensor): dgrad dx = dy W takes B = the codes of W [N][K]
+ * MN-major, wgrad dW = dy^T x takes A = the codes of dy [M][N] and B = the
+ * codes of x [M][K], both MN-major, so no transposed copy is written.
+ * Needs M % 16 == 0 for an MN-major A and N % 16 == 0 for an MN-major B (row
+ * pitch a multiple of 16 bytes), K % 16 == 0; otherwise as fp8_gemm.
+ * FP8SQ_ERR_UNSUPPORTED for other granularities with an MN-major operand. */
+#define FP8SQ_K_MAJOR 0
+#define FP8SQ_MN_MAJOR 1
+FP8SQ_API int fp8_gemm_layout(const uint8_t* A, int a_format, const void* a_scale, int a_major,
+                              const uint8_t* B, int b_format, const void* b_scale, int b_major,
+                              int64_t M, int64_t N, int64_t K, const float* bias, void* D, int d_dtype,
+                              void* stream);
+
 /* ---- 5. linear layer ---------------------------------------------------------
  * [TE] te.Linear under fp8_autocast; [TS] Part 01 (HYBRID).
  * Forward  y[M][N]  = x[M][K] W[N][K]^T      (x, W quantised in E4M3)
@@ -261,8 +280,9 @@ FP8SQ_API int fp8_gemm(const uint8_t* A, int a_format, const void* a_scale, int 
  * x, w, dy: device bf16.  y: bf16 or f32.  dx: bf16.  dw: f32.
  * gran TENSOR: delayed scaling when x_state / w_state / dy_state are given
  *   (each a state block of history_len), current scaling when all are NULL.
- *   The forward keeps the codes of x and W (and their transposes) in the
- *   workspace; the backward reads them and adds dy's codes.
+ *   The forward keeps the codes of x and W in the workspace; the backward
+ *   adds dy's codes and reads all three as they are (dgrad and wgrad take
+ *   them as MN-major operands, see fp8_gemm_layout): no transposed copy.
  * gran TILE_1x128: x in 1x128 tiles, W in 128x128 blocks, current scaling
  *   ([W14] absmax bullet, the DeepSeek-V3 granularity).  Backward: dy in
  *   1x128 tiles along N for dgrad (B = W^T codes, its blocks transposed); dy
@@ -372,7 +392,11 @@ FP8SQ_API int fp8_linear_fwd_noalloc(const void* x, const void* w, int64_t M, in
  *   cleared.
  * fp8_last_error: message for the calling thread's last non-zero status
  *   (static thread-local storage; never NULL).
- * fp8_abi_version: 4.  Changes from 3: fp8_quantize_rows_cols added.
+ * fp8_abi_version: 5.  Changes from 4: fp8_gemm_layout added (MN-major
+ *   operands); the per-tensor linear layer keeps no transposed codes (its
+ *   backward reads the forward's codes MN-major), so
+ *   fp8_linear_workspace_bytes(TENSOR) is smaller.
+ *   Changes from 3 to 4: fp8_quantize_rows_cols added.
  *   Changes from 2 to 3: fp8_selftest_wait_timeout added;
  *   the LayerNorm entry points need 16-byte aligned gamma, beta, mu, rstd;
  *   a delayed per-tensor fp8_quantize writes s to a non-NULL scales_out.

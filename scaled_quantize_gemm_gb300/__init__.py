@@ -18,6 +18,7 @@ TENSOR, TILE_1x128, BLOCK_128x128, MX32, MX32_TILED, TILE_128x1, MX32_COL_TILED 
 TILE_1x128_POW2, BLOCK_128x128_POW2, MX32_FLOOR_TILED = 7, 8, 9
 AMAX_MAX, AMAX_MOST_RECENT = 0, 1
 RECIPE_HYBRID, RECIPE_E4M3 = 0, 1
+K_MAJOR, MN_MAJOR = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_MISALIGNED, ERR_WRONG_ARCH, ERR_CUDA, ERR_TIMEOUT = 0, -1, -2, -3, -4, -5, -6
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -60,6 +61,7 @@ def lib() -> ctypes.CDLL:
                 "fp8_quantize": (I, [P, I, I64, I64, I, I, P, I, P, P, P, P, P, P]),
                 "fp8_quantize_rows_cols": (I, [P, I64, I64, I, I, P, P, P, P, P, P]),
                 "fp8_gemm": (I, [P, I, P, I, P, I, P, I, I64, I64, I64, P, P, I, P]),
+                "fp8_gemm_layout": (I, [P, I, P, I, P, I, P, I, I64, I64, I64, P, P, I, P]),
                 "fp8_linear_workspace_bytes": (Z, [I64, I64, I64, I]),
                 "fp8_linear_fwd": (I, [P, P, I64, I64, I64, I, I, P, P, I, P, Z, P, P, I, P]),
                 "fp8_linear_bwd": (I, [P, I64, I64, I64, I, I, P, I, P, Z, P, P, P]),
@@ -214,6 +216,21 @@ def fp8_gemm(A, a_format: int, a_scale, a_gran: int, B, b_format: int, b_scale, 
     _opt(bias, "bias", T.float32, 4 * N)
     _check(lib().fp8_gemm(_ptr(A), a_format, _ptr(a_scale), a_gran, _ptr(B), b_format, _ptr(b_scale), b_gran,
                           M, N, K, _ptr(bias), _ptr(D), _dtype_code(D), _stream(stream)))
+
+
+def fp8_gemm_layout(A, a_format: int, a_scale, a_major: int, B, b_format: int, b_scale, b_major: int,
+                    D, M: int, N: int, K: int, bias=None, stream=None) -> None:
+    """Per-tensor-scaled GEMM with K-major or MN-major operands: A [M][K]
+    or [K][M], B [N][K] or [K][N] (a_major / b_major K_MAJOR or MN_MAJOR)."""
+    T = _t()
+    _need(A, "A", T.uint8, M * K)
+    _need(B, "B", T.uint8, N * K)
+    _need(D, "D", None, M * N * (2 if D.dtype == T.bfloat16 else 4))
+    _need(a_scale, "a_scale", T.float32, 4)
+    _need(b_scale, "b_scale", T.float32, 4)
+    _opt(bias, "bias", T.float32, 4 * N)
+    _check(lib().fp8_gemm_layout(_ptr(A), a_format, _ptr(a_scale), a_major, _ptr(B), b_format, _ptr(b_scale),
+                                 b_major, M, N, K, _ptr(bias), _ptr(D), _dtype_code(D), _stream(stream)))
 
 
 def fp8_linear_workspace_bytes(M: int, N: int, K: int, gran: int = TENSOR) -> int:

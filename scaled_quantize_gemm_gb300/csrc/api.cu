@@ -100,9 +100,11 @@ struct WsLayout {
     size_t sx = 0, sxT = 0, sw = 0, swT = 0, sdy = 0, sdyT = 0, scal = 0, total = 0;
 };
 size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
-// TENSOR: codes of x, W, dy and their transposes + 8 scalars.
-// TILE_1x128: x tiles [M][K/128] and column tiles [M/128][K]; W blocks and
-//   their transpose; dy tiles [M][N/128] and column tiles [M/128][N].
+// TENSOR: codes of x, W, dy + 8 scalars (the backward GEMMs read the codes
+//   MN-major, so no transposed copies are kept).
+// TILE_1x128: codes and their transposed or column-unit counterparts; x
+//   tiles [M][K/128] and column tiles [M/128][K]; W blocks and their
+//   transpose; dy tiles [M][N/128] and column tiles [M/128][N].
 // MX32: x, W, dy in row blocks and column blocks, tiled E8M0 scales.
 WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int gran)
 {
@@ -111,10 +113,12 @@ WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int gran)
     auto take = [&](size_t bytes) { size_t o = off; off += al256(bytes); return o; };
     L.qx = take((size_t)(M * K));
     L.qw = take((size_t)(N * K));
-    L.qxT = take((size_t)(M * K));
-    L.qwT = take((size_t)(N * K));
     L.qdy = take((size_t)(M * N));
-    L.qdyT = take((size_t)(M * N));
+    if (gran != FP8SQ_TENSOR) {
+        L.qxT = take((size_t)(M * K));
+        L.qwT = take((size_t)(N * K));
+        L.qdyT = take((size_t)(M * N));
+    }
     if (gran == FP8SQ_TENSOR) {
         L.scal = take(8 * sizeof(float));   // sx, sw, sdy, ax, aw, ady
     } else if (gran == FP8SQ_TILE_1x128) {
@@ -200,7 +204,7 @@ int api_check_device(int* sms) { return check_device(sms); }
 
 extern "C" {
 
-FP8SQ_API int fp8_abi_version(void) { return 4; }
+FP8SQ_API int fp8_abi_version(void) { return 5; }
 
 FP8SQ_API const char* fp8_last_error(void) { return g_msg; }
 
@@ -449,6 +453,38 @@ FP8SQ_API int fp8_gemm(const uint8_t* A, int a_format, const void* a_scale, int 
     return cuda_status(e, "fp8_gemm launch");
 }
 
+FP8SQ_API int fp8_gemm_layout(const uint8_t* A, int a_format, const void* a_scale, int a_major, const uint8_t* B,
+                              int b_format, const void* b_scale, int b_major, int64_t M, int64_t N, int64_t K,
+                              const float* bias, void* D, int d_dtype, void* stream)
+{
+    if ((a_major != FP8SQ_K_MAJOR && a_major != FP8SQ_MN_MAJOR) || (b_major != FP8SQ_K_MAJOR && b_major != FP8SQ_MN_MAJOR))
+        return fail(FP8SQ_ERR_INVALID_ARG, "fp8_gemm_layout: a_major / b_major must be K_MAJOR or MN_MAJOR");
+    int mode = 0;
+    int r = validate_gemm(A, a_format, a_scale, FP8SQ_TENSOR, B, b_format, b_scale, FP8SQ_TENSOR, M, N, K, bias, D,
+                          d_dtype, &mode);
+    if (r) return r;
+    if (a_major == FP8SQ_MN_MAJOR && M % 16)
+        return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_gemm_layout: an MN-major A needs M %% 16 == 0");
+    if (b_major == FP8SQ_MN_MAJOR && N % 16)
+        return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_gemm_layout: an MN-major B needs N %% 16 == 0");
+    int sms;
+    if ((r = check_device(&sms))) return r;
+    fp8sq::GemmArgs g;
+    g.A = A; g.B = B; g.a_format = a_format; g.b_format = b_format; g.mode = 0;
+    g.a_scale = a_scale; g.b_scale = b_scale; g.M = M; g.N = N; g.K = K;
+    g.bias = bias; g.D = D; g.d_dtype = d_dtype;
+    g.a_mn = a_major == FP8SQ_MN_MAJOR;
+    g.b_mn = b_major == FP8SQ_MN_MAJOR;
+    const char* why = nullptr;
+    cudaError_t e = fp8sq::launch_gemm(g, static_cast<cudaStream_t>(stream), sms, &why);
+    if (e == cudaErrorNotSupported) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_gemm_layout: %s", why ? why : "not supported");
+    if (e != cudaSuccess && why) {
+        cudaGetLastError();
+        return fail(FP8SQ_ERR_CUDA, "fp8_gemm_layout: %s", why);
+    }
+    return cuda_status(e, "fp8_gemm_layout launch");
+}
+
 FP8SQ_API size_t fp8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int gran)
 {
     if (M < 0 || N < 0 || K < 0 || !(gran == FP8SQ_TENSOR || gran == FP8SQ_TILE_1x128 || gran == FP8SQ_MX32)) return 0;
@@ -509,14 +545,15 @@ FP8SQ_API int fp8_linear_fwd(const void* x, const void* w, int64_t M, int64_t N,
     g.B = ws + L.qw;
     if (gran == FP8SQ_TENSOR) {
         float* scal = reinterpret_cast<float*>(ws + L.scal);   // sx, sw, sdy, ax, aw, ady
-        // x and W in one launch (current scaling: one more for both amaxes)
+        // x and W in one launch (current scaling: one more for both amaxes);
+        // no transposed copies, the backward reads these codes MN-major
         qa.x = x; qa.rows = M; qa.cols = K; qa.gran = fp8sq::kTensor;
-        qa.q = ws + L.qx; qa.qT = ws + L.qxT;
+        qa.q = ws + L.qx; qa.qT = nullptr;
         qa.state = x_state; qa.history_len = H;
         qa.scales = &scal[0]; qa.amax = delayed ? nullptr : &scal[3];
         fp8sq::QuantArgs qw = qa;
         qw.x = w; qw.rows = N; qw.cols = K;
-        qw.q = ws + L.qw; qw.qT = ws + L.qwT;
+        qw.q = ws + L.qw; qw.qT = nullptr;
         qw.state = w_state;
         qw.scales = &scal[1]; qw.amax = delayed ? nullptr : &scal[4];
         if ((r = cuda_status(fp8sq::launch_quantize_pair(qa, qw, st, sms), "fp8_linear_fwd: quantize x and w"))) return r;
@@ -591,13 +628,18 @@ FP8SQ_API int fp8_linear_bwd(const void* dy, int64_t M, int64_t N, int64_t K, in
     if (gran == FP8SQ_TENSOR) {
         float* scal = reinterpret_cast<float*>(ws + L.scal);
         qa.gran = fp8sq::kTensor;
-        qa.q = ws + L.qdy; qa.qT = ws + L.qdyT;
+        qa.q = ws + L.qdy; qa.qT = nullptr;
         qa.state = dy_state; qa.history_len = history_len;
         qa.scales = &scal[2]; qa.amax = dy_state ? nullptr : &scal[5];
         if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_bwd: quantize dy"))) return r;
         dg.mode = wg.mode = 0;
         dg.a_scale = &scal[2]; dg.b_scale = &scal[1];
         wg.a_scale = &scal[2]; wg.b_scale = &scal[0];
+        // the forward's codes as they are: dgrad's B = W [N][K] and wgrad's
+        // A = dy [M][N], B = x [M][K] are MN-major operands
+        dg.B = ws + L.qw; dg.b_mn = true;
+        wg.A = ws + L.qdy; wg.a_mn = true;
+        wg.B = ws + L.qx; wg.b_mn = true;
     } else if (gran == FP8SQ_TILE_1x128) {
         // dy: 1x128 tiles along N (dgrad) and 128x1 column tiles along M
         // (wgrad), both from one read of dy
@@ -679,7 +721,7 @@ FP8SQ_API int fp8_layernorm_linear_fwd(const void* x, const float* gamma, const 
     if (r) return r;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     const WsLayout L = ws_layout(M, N, K, FP8SQ_TENSOR);
-    r = validate_ln(x, gamma, beta, M, K, FP8SQ_E4M3, x_state, history_len, ws + L.qx, ws + L.qxT, mu_out, rstd_out);
+    r = validate_ln(x, gamma, beta, M, K, FP8SQ_E4M3, x_state, history_len, ws + L.qx, nullptr, mu_out, rstd_out);
     if (r) return r;
     if (!aligned16(w) || !aligned16(y)) return fail(FP8SQ_ERR_MISALIGNED, "fp8_layernorm_linear_fwd: w, y must be 16-byte aligned");
     if ((bias && !aligned4(bias)) || !aligned4(w_state)) return fail(FP8SQ_ERR_MISALIGNED, "fp8_layernorm_linear_fwd: bias / w_state alignment");
@@ -690,12 +732,12 @@ FP8SQ_API int fp8_layernorm_linear_fwd(const void* x, const float* gamma, const 
     float* scal = reinterpret_cast<float*>(ws + L.scal);
     fp8sq::QuantArgs qa;
     qa.x = x; qa.x_dtype = fp8sq::kBF16; qa.rows = M; qa.cols = K; qa.format = fp8sq::kE4M3;
-    qa.gran = fp8sq::kTensor; qa.state = x_state; qa.history_len = H; qa.q = ws + L.qx; qa.qT = ws + L.qxT;
+    qa.gran = fp8sq::kTensor; qa.state = x_state; qa.history_len = H; qa.q = ws + L.qx; qa.qT = nullptr;
     qa.scales = &scal[0];       // receives the dequantisation scale the cast used
     if ((r = cuda_status(fp8sq::launch_layernorm_quantize(qa, gamma, beta, eps, mu_out, rstd_out, st, sms),
                          "fp8_layernorm_linear_fwd: layernorm cast")))
         return r;
-    qa.x = w; qa.rows = N; qa.cols = K; qa.state = w_state; qa.q = ws + L.qw; qa.qT = ws + L.qwT;
+    qa.x = w; qa.rows = N; qa.cols = K; qa.state = w_state; qa.q = ws + L.qw; qa.qT = nullptr;
     qa.scales = &scal[1];
     if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_layernorm_linear_fwd: quantize w"))) return r;
     fp8sq::GemmArgs g;

@@ -314,7 +314,8 @@ __device__ __forceinline__ bool wait_bounded_cluster(uint64_t* bar, uint32_t par
 template <bool OUT_BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     k_gemm_tensor_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                       EpiParams p, uint32_t idesc, TileSched sched, const __grid_constant__ CUtensorMap tmD)
+                       EpiParams p, uint32_t idesc, TileSched sched, const __grid_constant__ CUtensorMap tmD,
+                       int layout)
 {
     pdl_enter();
     constexpr int BN = kPairBN, BH = BN / 2, STAGES = kPairStages;
@@ -332,6 +333,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     __shared__ int s_skip;
     const uint32_t rank = cluster_ctarank();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool a_mn = (layout & 1) != 0, b_mn = (layout & 2) != 0;   // MN-major operands
 
     if (threadIdx.x == 0) {
         s_skip = rank == 0 ? *reinterpret_cast<volatile int*>(&g_dev_error) : 0;
@@ -384,8 +386,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     }
                     uint8_t* sa = smem + stage * L::STAGE;
                     if (rank == 0) mbar_arrive_expect_tx(&full[stage], PAIR_TX);
-                    tma_load_2d_pair(sa, &tmA, kb * BK, mb * 2 * BM + (int)rank * BM, full0 + 8u * stage);
-                    tma_load_2d_pair(sa + A_BYTES, &tmB, kb * BK, nb * BN + (int)rank * BH, full0 + 8u * stage);
+                    const int ar = mb * 2 * BM + (int)rank * BM, br = nb * BN + (int)rank * BH;
+                    // K-major boxes are (k, row); MN-major ones (row, k)
+                    tma_load_2d_pair(sa, &tmA, a_mn ? ar : kb * BK, a_mn ? kb * BK : ar, full0 + 8u * stage);
+                    tma_load_2d_pair(sa + A_BYTES, &tmB, b_mn ? br : kb * BK, b_mn ? kb * BK : br,
+                                     full0 + 8u * stage);
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -436,11 +441,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     }
                     tc_fence_after();
                     const uint32_t sa = smem_addr(smem + stage * L::STAGE);
-                    const uint64_t da = sdesc_kmajor_sw128(sa);
-                    const uint64_t db = sdesc_kmajor_sw128(sa + A_BYTES);
+                    // K = 32 slice k: 32 bytes further along a K-major row, or
+                    // 32 rows (4 atoms, 4 KB) further down an MN-major tile
 #pragma unroll
-                    for (int k = 0; k < BK / 32; ++k)
-                        mma_pair_f8f6f4(d, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+                    for (int k = 0; k < BK / 32; ++k) {
+                        const uint64_t da = a_mn ? sdesc_mn_sw128(sa + 4096u * k) : sdesc_kmajor_sw128(sa) + 2 * k;
+                        const uint64_t db = b_mn ? sdesc_mn_sw128(sa + A_BYTES + 4096u * k)
+                                                 : sdesc_kmajor_sw128(sa + A_BYTES) + 2 * k;
+                        mma_pair_f8f6f4(d, da, db, idesc, (kb | k) != 0 ? 1u : 0u);
+                    }
                     mma_pair_commit(&empty[stage], 3);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -1279,7 +1288,11 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
     CUtensorMap ta, tb;
     if (g.mode == 0) {
         constexpr int BN = kPairBN;
-        if (!make_tmap(&ta, g.A, g.K, g.M, BM) || !make_tmap(&tb, g.B, g.K, g.N, BN / 2)) {
+        // K-major: [rows][K] in boxes of 128 rows x 128 K; MN-major: [K][rows]
+        // in boxes of 128 K rows x 128 along M / N
+        const bool ok_a = g.a_mn ? make_tmap(&ta, g.A, g.M, g.K, BK) : make_tmap(&ta, g.A, g.K, g.M, BM);
+        const bool ok_b = g.b_mn ? make_tmap(&tb, g.B, g.N, g.K, BK) : make_tmap(&tb, g.B, g.K, g.N, BN / 2);
+        if (!ok_a || !ok_b) {
             *why = "cuTensorMapEncodeTiled failed";
             return cudaErrorInvalidValue;
         }
@@ -1292,6 +1305,8 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
         const int tiles = sched.num_m * sched.num_n;
         uint32_t idesc = make_idesc(g.a_format, g.b_format, BN);
         idesc = (idesc & ~(0x1Fu << 24)) | ((uint32_t)((2 * BM) >> 4) << 24);   // M = 256 over the pair
+        if (g.a_mn) idesc |= 1u << 15;          // A MN-major
+        if (g.b_mn) idesc |= 1u << 16;          // B MN-major
         const int smem = PairSmem::BYTES;
         auto kern = bf16 ? k_gemm_tensor_pair<true> : k_gemm_tensor_pair<false>;
         int clusters = 0;
@@ -1305,7 +1320,7 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
             return cudaErrorNotSupported;
         }
         const int grid = 2 * (tiles < clusters ? tiles : clusters);
-        launch_k(kern, grid, 192, smem, st, ta, tb, p, idesc, sched, td);
+        launch_k(kern, grid, 192, smem, st, ta, tb, p, idesc, sched, td, (g.a_mn ? 1 : 0) | (g.b_mn ? 2 : 0));
         return cudaGetLastError();
     }
     if (g.mode == 1) return launch_promote<1>(g, p, st, sms, why);

@@ -57,6 +57,9 @@ struct GemmArgs {
     const float* bias = nullptr;
     void* D = nullptr;
     int d_dtype = kBF16;
+    // operand storage (mode 0 only): K-major A [M][K] / B [N][K], or
+    // MN-major A [K][M] / B [K][N]
+    bool a_mn = false, b_mn = false;
 };
 
 // gemm.cu

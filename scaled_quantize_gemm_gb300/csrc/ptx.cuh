@@ -356,6 +356,24 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr)
     return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand (128-byte swizzle):
+// the tile is stored as K rows of 128 bytes along M (or N), 8-row x 128-byte
+// atoms stacked along K every 1024 bytes (stride byte offset); the leading
+// byte offset is the distance between 128-byte-wide atom columns along M/N
+// (16 KB, the size of one 128 x 128 box; a tile here is one column wide).
+// Probed on the GB300 with integer operands for 8-bit A and B: exact with
+// these offsets, wrong with the two swapped.
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)(16384 >> 4) << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
 // Launch with programmatic stream serialisation allowed (see pdl_enter).
 // Errors are also left for cudaGetLastError, like a <<<>>> launch.
 template <typename... KArgs, typename... Args>

@@ -22,6 +22,7 @@
 //    ("Transformer Scaling", delayed scaling; the Transformer Engine
 //    tutorial's DelayedScaling recipe).
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -269,33 +270,32 @@ __global__ void __launch_bounds__(kFlatThreads) k_amax_tensor2(AmaxJob a, AmaxJo
         amax_tensor_body<DT>(b.x, b.n, b.amax, blockIdx.x - blocks_a, gridDim.x - blocks_a, red);
 }
 
-// Cast pass of per-tensor scaling without a transposed copy.
+// Cast pass of per-tensor scaling without a transposed copy, over blocks
+// [bid, bid + nblk, ...) of a grid-stride loop.
 //   DELAYED: m = state[H]; the tensor's amax is max-combined into state[0]
 //            (and into amax_out if given).
-//   current: m, s from *amax_in; block 0 writes s.
+//   current: m, s from *amax_in; the job's block 0 writes s.
 template <int DT, int FMT, bool DELAYED>
-__global__ void __launch_bounds__(kFlatThreads) k_cast_tensor(const void* __restrict__ x, int64_t n,
-                                                              uint8_t* __restrict__ q, float* state, int H,
-                                                              const float* amax_in, float* s_out,
-                                                              float* amax_out, unsigned long long* sat)
+__device__ __forceinline__ void cast_tensor_body(const void* __restrict__ x, int64_t n, uint8_t* __restrict__ q,
+                                                 float* state, int H, const float* amax_in, float* s_out,
+                                                 float* amax_out, unsigned long long* sat, int64_t bid,
+                                                 int64_t nblk, uint32_t* red)
 {
-    pdl_enter();
-    __shared__ uint32_t red[kFlatThreads / 32];
     float m, s;
     if (DELAYED) {
         m = state[H];
         s = 0.0f;
         // the dequantisation scale this cast uses (the state's s is updated
         // only at the end of the step)
-        if (blockIdx.x == 0 && threadIdx.x == 0 && s_out) *s_out = state[H + 1];
+        if (bid == 0 && threadIdx.x == 0 && s_out) *s_out = state[H + 1];
     } else {
         current_scale<FMT>(__float_as_uint(*amax_in), m, s);
-        if (blockIdx.x == 0 && threadIdx.x == 0 && s_out) *s_out = s;
+        if (bid == 0 && threadIdx.x == 0 && s_out) *s_out = s;
     }
     const int64_t nch = n / 8;
     uint32_t mx = 0, nsat = 0;
-    const int64_t stride = (int64_t)gridDim.x * kFlatThreads * kFlatUnroll;
-    for (int64_t c0 = (int64_t)blockIdx.x * kFlatThreads * kFlatUnroll; c0 < nch; c0 += stride) {
+    const int64_t stride = nblk * kFlatThreads * kFlatUnroll;
+    for (int64_t c0 = bid * kFlatThreads * kFlatUnroll; c0 < nch; c0 += stride) {
         Vec8<DT> v[kFlatUnroll];
 #pragma unroll
         for (int u = 0; u < kFlatUnroll; ++u) {
@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(kFlatThreads) k_cast_tensor(const void* __rest
             if (c < nch) *reinterpret_cast<uint2*>(q + c * 8) = codes;
         }
     }
-    if (blockIdx.x == 0 && threadIdx.x < (n & 7)) {
+    if (bid == 0 && threadIdx.x < (n & 7)) {
         int64_t i = nch * 8 + threadIdx.x;
         float f = (DT == kBF16) ? __uint_as_float((uint32_t)static_cast<const uint16_t*>(x)[i] << 16)
                                 : static_cast<const float*>(x)[i];
@@ -330,6 +330,42 @@ __global__ void __launch_bounds__(kFlatThreads) k_cast_tensor(const void* __rest
             if (amax_out) atomic_max_bits(amax_out, r);
         }
     }
+}
+
+template <int DT, int FMT, bool DELAYED>
+__global__ void __launch_bounds__(kFlatThreads) k_cast_tensor(const void* __restrict__ x, int64_t n,
+                                                              uint8_t* __restrict__ q, float* state, int H,
+                                                              const float* amax_in, float* s_out,
+                                                              float* amax_out, unsigned long long* sat)
+{
+    pdl_enter();
+    __shared__ uint32_t red[kFlatThreads / 32];
+    cast_tensor_body<DT, FMT, DELAYED>(x, n, q, state, H, amax_in, s_out, amax_out, sat, blockIdx.x, gridDim.x, red);
+}
+
+// Two per-tensor casts without transposed copies in one launch (a linear
+// layer's x and W): blocks [0, blocks_a) cast a, the rest cast b.
+struct FlatCastJob {
+    const void* x;
+    int64_t n;
+    uint8_t* q;
+    float* state;
+    const float* amax_in;
+    float* s_out;
+    float* amax_out;
+};
+template <int DT, int FMT, bool DELAYED>
+__global__ void __launch_bounds__(kFlatThreads) k_cast_tensor2(FlatCastJob a, FlatCastJob b, int blocks_a, int H,
+                                                               unsigned long long* sat)
+{
+    pdl_enter();
+    __shared__ uint32_t red[kFlatThreads / 32];
+    if ((int)blockIdx.x < blocks_a)
+        cast_tensor_body<DT, FMT, DELAYED>(a.x, a.n, a.q, a.state, H, a.amax_in, a.s_out, a.amax_out, sat, blockIdx.x,
+                                           blocks_a, red);
+    else
+        cast_tensor_body<DT, FMT, DELAYED>(b.x, b.n, b.q, b.state, H, b.amax_in, b.s_out, b.amax_out, sat,
+                                           blockIdx.x - blocks_a, gridDim.x - blocks_a, red);
 }
 
 // 8x8 byte transpose: in[i] holds row i (bytes = columns 0..7); out[j] holds
@@ -1020,13 +1056,68 @@ __global__ void k_update_scale(float* states, int n, int H, FormatList fl, int a
 }
 
 // ================================================================== launchers
-static int flat_grid(int64_t nch, int sms)
+// CTAs of a flat kernel (kFlatThreads threads, no dynamic shared memory)
+// that fit on one SM at once, queried once per kernel and device.
+static int resident_per_sm(const void* kern)
 {
-    int64_t per_block = (int64_t)kFlatThreads * kFlatUnroll;
-    int64_t need = (nch + per_block - 1) / per_block;
-    int64_t cap = (int64_t)sms * 8;     // 8 x 256 threads resident per SM
-    int64_t g = need < cap ? need : cap;
+    static std::mutex mu;
+    static const void* keys[128];
+    static int devs[128], vals[128];
+    static int n = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 1;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n; ++i)
+        if (keys[i] == kern && devs[i] == dev) return vals[i];
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, kFlatThreads, 0) != cudaSuccess || b < 1) {
+        cudaGetLastError();
+        b = 1;
+    }
+    if (n < 128) {
+        keys[n] = kern;
+        devs[n] = dev;
+        vals[n] = b;
+        ++n;
+    }
+    return b;
+}
+
+// Grid of a grid-stride flat kernel over nch work items (kFlatUnroll per
+// thread per pass): no more CTAs than fit on the device at once.  A grid
+// larger than that runs its last CTAs as a second, mostly empty wave (a
+// 16384 x 14336 cast ran at 0.80 of HBM with 8 CTAs per SM requested and 6
+// resident).
+template <typename K>
+static int flat_grid(K kern, int64_t nch, int sms)
+{
+    const int64_t per_block = (int64_t)kFlatThreads * kFlatUnroll;
+    const int64_t need = (nch + per_block - 1) / per_block;
+    const int64_t cap = (int64_t)sms * resident_per_sm(reinterpret_cast<const void*>(kern));
+    const int64_t g = need < cap ? need : cap;
     return g < 1 ? 1 : (int)g;
+}
+
+// The grids of the two jobs of a two-tensor flat kernel: each job's own need
+// when both fit at once, else the resident capacity split in proportion to
+// the jobs' sizes (at least one CTA each).
+template <typename K>
+static void flat_grid2(K kern, int64_t na, int64_t nb, int sms, int& ga, int& gb)
+{
+    const int64_t per_block = (int64_t)kFlatThreads * kFlatUnroll;
+    const int64_t need_a = (na + per_block - 1) / per_block, need_b = (nb + per_block - 1) / per_block;
+    const int64_t cap = (int64_t)sms * resident_per_sm(reinterpret_cast<const void*>(kern));
+    int64_t a = need_a < 1 ? 1 : need_a, b = need_b < 1 ? 1 : need_b;
+    if (a + b > cap) {
+        a = (int64_t)((double)cap * (double)na / (double)(na + nb) + 0.5);
+        a = a < 1 ? 1 : (a > cap - 1 ? cap - 1 : a);
+        b = cap - a < 1 ? 1 : cap - a;
+    }
+    ga = (int)a;
+    gb = (int)b;
 }
 
 template <int DT>
@@ -1036,13 +1127,13 @@ static cudaError_t amax_dt(const QuantArgs& a, cudaStream_t st, int sms)
     switch (a.gran) {
     case kTensor:
         if (cudaMemsetAsync(a.amax, 0, sizeof(float), st) != cudaSuccess) return cudaGetLastError();
-        if (n > 0) launch_k(k_amax_tensor<DT>, flat_grid(n / 8, sms), kFlatThreads, 0, st, a.x, n, a.amax);
+        if (n > 0) launch_k(k_amax_tensor<DT>, flat_grid(k_amax_tensor<DT>, n / 8, sms), kFlatThreads, 0, st, a.x, n, a.amax);
         break;
     case kTile:
-        if (n > 0) launch_k(k_quant_rowunits<DT, kE4M3, 128, false>, flat_grid(n / 16, sms), kFlatThreads, 0, st, a.x, n, nullptr, nullptr, a.amax, nullptr, (int64_t)0);
+        if (n > 0) launch_k(k_quant_rowunits<DT, kE4M3, 128, false>, flat_grid(k_quant_rowunits<DT, kE4M3, 128, false>, n / 16, sms), kFlatThreads, 0, st, a.x, n, nullptr, nullptr, a.amax, nullptr, (int64_t)0);
         break;
     case kMX:
-        if (n > 0) launch_k(k_quant_rowunits<DT, kE4M3, 32, false>, flat_grid(n / 16, sms), kFlatThreads, 0, st, a.x, n, nullptr, nullptr, a.amax, nullptr, (int64_t)0);
+        if (n > 0) launch_k(k_quant_rowunits<DT, kE4M3, 32, false>, flat_grid(k_quant_rowunits<DT, kE4M3, 32, false>, n / 16, sms), kFlatThreads, 0, st, a.x, n, nullptr, nullptr, a.amax, nullptr, (int64_t)0);
         break;
     case kBlock:
         if (n > 0) launch_k(k_quant_block128<DT, kE4M3, false>, dim3((unsigned)(a.cols / 128), (unsigned)(a.rows / 128)), 256, 0, st, a.x, a.rows, a.cols, nullptr, nullptr, a.amax, nullptr,
@@ -1088,7 +1179,8 @@ static cudaError_t quant_dt_fmt(const QuantArgs& a, cudaStream_t st, int sms)
                 launch_k(k_cast_tensor_T<DT, FMT, false>, grid, 256, 0, st, a.x, a.rows, a.cols, a.q, a.qT, nullptr, 0, a.amax, s_out,
                          nullptr, a.sat, LnParams());
         } else {
-            int g = flat_grid(n / 8, sms);
+            int g = delayed ? flat_grid(k_cast_tensor<DT, FMT, true>, n / 8, sms)
+                            : flat_grid(k_cast_tensor<DT, FMT, false>, n / 8, sms);
             if (delayed)
                 launch_k(k_cast_tensor<DT, FMT, true>, g, kFlatThreads, 0, st, a.x, n, a.q, a.state, H, nullptr, s_out, a.amax, a.sat);
             else
@@ -1099,21 +1191,21 @@ static cudaError_t quant_dt_fmt(const QuantArgs& a, cudaStream_t st, int sms)
     if (n == 0) return cudaSuccess;
     switch (a.gran) {
     case kTile:
-        launch_k(k_quant_rowunits<DT, FMT, 128, true>, flat_grid(n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat,
+        launch_k(k_quant_rowunits<DT, FMT, 128, true>, flat_grid(k_quant_rowunits<DT, FMT, 128, true>, n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat,
                  (int64_t)0);
         break;
     case kMX:
-        launch_k(k_quant_rowunits<DT, FMT, 32, true>, flat_grid(n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat,
+        launch_k(k_quant_rowunits<DT, FMT, 32, true>, flat_grid(k_quant_rowunits<DT, FMT, 32, true>, n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat,
                  (int64_t)0);
         break;
     case kMXTiled:
-        launch_k(k_quant_rowunits<DT, FMT, 32, true, true>, flat_grid(n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
+        launch_k(k_quant_rowunits<DT, FMT, 32, true, true>, flat_grid(k_quant_rowunits<DT, FMT, 32, true, true>, n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
         break;
     case kTilePow2:
-        launch_k(k_quant_rowunits<DT, FMT, 128, true, true, 1>, flat_grid(n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
+        launch_k(k_quant_rowunits<DT, FMT, 128, true, true, 1>, flat_grid(k_quant_rowunits<DT, FMT, 128, true, true, 1>, n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
         break;
     case kMXFloor:
-        launch_k(k_quant_rowunits<DT, FMT, 32, true, true, 2>, flat_grid(n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
+        launch_k(k_quant_rowunits<DT, FMT, 32, true, true, 2>, flat_grid(k_quant_rowunits<DT, FMT, 32, true, true, 2>, n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
         break;
     case kBlockPow2:
         launch_k(k_quant_block128<DT, FMT, true, true>, dim3((unsigned)(a.cols / 128), (unsigned)(a.rows / 128)), 256, 0, st, a.x, a.rows, a.cols, a.q, nullptr, a.amax, a.sat, nullptr, nullptr, static_cast<uint8_t*>(a.scales));
@@ -1164,7 +1256,8 @@ static cudaError_t quant_pair_dt_fmt(const QuantArgs& a, const QuantArgs& b, cud
     if (clear(a.amax, b.amax) != cudaSuccess) return cudaGetLastError();
     const int64_t na = a.rows * a.cols, nb = b.rows * b.cols;
     if (!delayed) {
-        const int ga = flat_grid(na / 8, sms), gb = flat_grid(nb / 8, sms);
+        int ga, gb;
+        flat_grid2(k_amax_tensor2<DT>, na / 8, nb / 8, sms, ga, gb);
         launch_k(k_amax_tensor2<DT>, ga + gb, kFlatThreads, 0, st, AmaxJob{a.x, na, a.amax}, AmaxJob{b.x, nb, b.amax}, ga);
     }
     const int64_t tiles_a = ((a.cols + 127) / 128) * ((a.rows + 127) / 128);
@@ -1181,15 +1274,53 @@ static cudaError_t quant_pair_dt_fmt(const QuantArgs& a, const QuantArgs& b, cud
     return cudaGetLastError();
 }
 
+// The same without transposed copies: the flat cast over both tensors.
+template <int DT, int FMT>
+static cudaError_t quant_pair_flat_dt_fmt(const QuantArgs& a, const QuantArgs& b, cudaStream_t st, int sms)
+{
+    const bool delayed = a.state != nullptr;
+    const int64_t na = a.rows * a.cols, nb = b.rows * b.cols;
+    if (a.amax && b.amax && b.amax == a.amax + 1) {
+        if (cudaMemsetAsync(a.amax, 0, 2 * sizeof(float), st) != cudaSuccess) return cudaGetLastError();
+    } else {
+        if (a.amax && cudaMemsetAsync(a.amax, 0, sizeof(float), st) != cudaSuccess) return cudaGetLastError();
+        if (b.amax && cudaMemsetAsync(b.amax, 0, sizeof(float), st) != cudaSuccess) return cudaGetLastError();
+    }
+    if (!delayed) {
+        int ga, gb;
+        flat_grid2(k_amax_tensor2<DT>, na / 8, nb / 8, sms, ga, gb);
+        launch_k(k_amax_tensor2<DT>, ga + gb, kFlatThreads, 0, st, AmaxJob{a.x, na, a.amax}, AmaxJob{b.x, nb, b.amax}, ga);
+    }
+    int ga, gb;
+    if (delayed) flat_grid2(k_cast_tensor2<DT, FMT, true>, na / 8, nb / 8, sms, ga, gb);
+    else flat_grid2(k_cast_tensor2<DT, FMT, false>, na / 8, nb / 8, sms, ga, gb);
+    const FlatCastJob ja{a.x, na, a.q, a.state, delayed ? nullptr : a.amax, static_cast<float*>(a.scales),
+                         delayed ? a.amax : nullptr};
+    const FlatCastJob jb{b.x, nb, b.q, b.state, delayed ? nullptr : b.amax, static_cast<float*>(b.scales),
+                         delayed ? b.amax : nullptr};
+    if (delayed)
+        launch_k(k_cast_tensor2<DT, FMT, true>, ga + gb, kFlatThreads, 0, st, ja, jb, ga, a.history_len, a.sat);
+    else
+        launch_k(k_cast_tensor2<DT, FMT, false>, ga + gb, kFlatThreads, 0, st, ja, jb, ga, 0, a.sat);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_quantize_pair(const QuantArgs& a, const QuantArgs& b, cudaStream_t st, int sms)
 {
     const bool same = a.gran == kTensor && b.gran == kTensor && a.x_dtype == b.x_dtype && a.format == b.format &&
-                      a.qT && b.qT && (a.state != nullptr) == (b.state != nullptr) &&
+                      (a.qT != nullptr) == (b.qT != nullptr) && (a.state != nullptr) == (b.state != nullptr) &&
                       (!a.state || a.history_len == b.history_len) && (a.state || (a.amax && b.amax)) &&
                       a.sat == b.sat;
     if (!same || a.rows * a.cols == 0 || b.rows * b.cols == 0 || a.rows % 8 || a.cols % 8 || b.rows % 8 || b.cols % 8) {
         cudaError_t e = launch_quantize(a, st, sms);
         return e != cudaSuccess ? e : launch_quantize(b, st, sms);
+    }
+    if (!a.qT) {
+        if (a.x_dtype == kBF16)
+            return a.format == kE4M3 ? quant_pair_flat_dt_fmt<kBF16, kE4M3>(a, b, st, sms)
+                                     : quant_pair_flat_dt_fmt<kBF16, kE5M2>(a, b, st, sms);
+        return a.format == kE4M3 ? quant_pair_flat_dt_fmt<kF32, kE4M3>(a, b, st, sms)
+                                 : quant_pair_flat_dt_fmt<kF32, kE5M2>(a, b, st, sms);
     }
     if (a.x_dtype == kBF16)
         return a.format == kE4M3 ? quant_pair_dt_fmt<kBF16, kE4M3>(a, b, st, sms) : quant_pair_dt_fmt<kBF16, kE5M2>(a, b, st, sms);

@@ -72,8 +72,8 @@ class GatherHandle:
 
 class LibraryOps:
     """Per-rank arithmetic on this library's CUDA path: per-tensor delayed
-    casts (with transposed copies) and FP8 GEMMs through the C ABI, states in
-    one device block of three (x, W, dy)."""
+    casts and FP8 GEMMs through the C ABI (the backward reads the codes
+    MN-major), states in one device block of three (x, W, dy)."""
 
     def __init__(self, M: int, N_local: int, K: int, history_len: int, device, recipe_e4m3: bool = False):
         import scaled_quantize_gemm_gb300 as sq
@@ -81,9 +81,9 @@ class LibraryOps:
         self.H = history_len
         self.M, self.N, self.K = M, N_local, K
         u8 = dict(dtype=torch.uint8, device=device)
-        self.qx, self.qxT = torch.empty((M, K), **u8), torch.empty((K, M), **u8)
-        self.qw, self.qwT = torch.empty((N_local, K), **u8), torch.empty((K, N_local), **u8)
-        self.qdy, self.qdyT = torch.empty((M, N_local), **u8), torch.empty((N_local, M), **u8)
+        self.qx = torch.empty((M, K), **u8)
+        self.qw = torch.empty((N_local, K), **u8)
+        self.qdy = torch.empty((M, N_local), **u8)
         self.states = torch.empty(3 * (history_len + 2), dtype=torch.float32, device=device)
         sq.fp8_scale_init(self.states, 3, history_len)
         self.dy_fmt = sq.E4M3 if recipe_e4m3 else sq.E5M2
@@ -98,9 +98,8 @@ class LibraryOps:
 
     def forward(self, x: torch.Tensor, w_local: torch.Tensor) -> torch.Tensor:
         sq, H = self.sq, self.H
-        sq.fp8_quantize(x, sq.E4M3, sq.TENSOR, self.qx, qT=self.qxT, delayed_state=self._st(0), history_len=H)
-        sq.fp8_quantize(w_local, sq.E4M3, sq.TENSOR, self.qw, qT=self.qwT, delayed_state=self._st(1),
-                        history_len=H)
+        sq.fp8_quantize(x, sq.E4M3, sq.TENSOR, self.qx, delayed_state=self._st(0), history_len=H)
+        sq.fp8_quantize(w_local, sq.E4M3, sq.TENSOR, self.qw, delayed_state=self._st(1), history_len=H)
         y = torch.empty((self.M, self.N), dtype=torch.bfloat16, device=x.device)
         sq.fp8_gemm(self.qx, sq.E4M3, self._s(0), sq.TENSOR, self.qw, sq.E4M3, self._s(1), sq.TENSOR, y)
         return y
@@ -108,12 +107,14 @@ class LibraryOps:
     def backward(self, dy_local: torch.Tensor):
         """-> (dx partial fp32 [M][K], dW_local fp32 [N/P][K])"""
         sq, H = self.sq, self.H
-        sq.fp8_quantize(dy_local, self.dy_fmt, sq.TENSOR, self.qdy, qT=self.qdyT, delayed_state=self._st(2),
-                        history_len=H)
+        sq.fp8_quantize(dy_local, self.dy_fmt, sq.TENSOR, self.qdy, delayed_state=self._st(2), history_len=H)
         dx = torch.empty((self.M, self.K), dtype=torch.float32, device=dy_local.device)
         dw = torch.empty((self.N, self.K), dtype=torch.float32, device=dy_local.device)
-        sq.fp8_gemm(self.qdy, self.dy_fmt, self._s(2), sq.TENSOR, self.qwT, sq.E4M3, self._s(1), sq.TENSOR, dx)
-        sq.fp8_gemm(self.qdyT, self.dy_fmt, self._s(2), sq.TENSOR, self.qxT, sq.E4M3, self._s(0), sq.TENSOR, dw)
+        # the forward's codes as they are: W and (for wgrad) dy and x MN-major
+        sq.fp8_gemm_layout(self.qdy, self.dy_fmt, self._s(2), sq.K_MAJOR, self.qw, sq.E4M3, self._s(1), sq.MN_MAJOR,
+                           dx, self.M, self.K, self.N)
+        sq.fp8_gemm_layout(self.qdy, self.dy_fmt, self._s(2), sq.MN_MAJOR, self.qx, sq.E4M3, self._s(0), sq.MN_MAJOR,
+                           dw, self.N, self.K, self.M)
         return dx, dw
 
     def recorded_amax(self) -> torch.Tensor:

@@ -22,7 +22,7 @@ def test_exports_every_declared_symbol(L):
                           "fp8_scale_init", "fp8_linear_workspace_bytes", "fp8_device_status"}
     for n in names:
         assert hasattr(L, n), n
-    assert L.fp8_abi_version() == 4
+    assert L.fp8_abi_version() == 5
 
 
 def test_null_and_enum_validation(L):
@@ -81,9 +81,12 @@ def test_linear_validation_and_workspace(L):
     P = ctypes.c_void_p
     f = P(4096)
     ws = sq.fp8_linear_workspace_bytes(256, 512, 384)
-    # q_x, q_w, their transposes, dy codes and transpose (+ scalars), 256-byte aligned
-    assert ws >= 2 * 256 * 384 + 2 * 512 * 384 + 2 * 256 * 512
+    # per tensor: the codes of x, W and dy (+ scalars), 256-byte aligned; the
+    # backward reads them MN-major, so no transposed copies are kept
+    assert 256 * 384 + 512 * 384 + 256 * 512 <= ws < 2 * (256 * 384 + 512 * 384 + 256 * 512)
     assert ws % 256 == 0
+    # the fine-grained layouts also keep the column-unit codes
+    assert sq.fp8_linear_workspace_bytes(256, 512, 384, sq.TILE_1x128) >= 2 * (256 * 384 + 512 * 384 + 256 * 512)
     assert sq.fp8_linear_workspace_bytes(256, 512, 384, sq.BLOCK_128x128) == 0
     fwd = L.fp8_linear_fwd
     assert fwd(f, f, 256, 512, 384, 0, 0, f, None, 16, f, ws, None, f, 0, None) == sq.ERR_INVALID_ARG  # one state

@@ -384,3 +384,53 @@ def test_pow2_tiles_blocks_on_block_scaled_mma(M, N, K):
     ah = o.dequantize(rqx[rows], o.E4M3, o.GRAN_TILE_POW2, rex[rows])
     bh = o.dequantize(rqw, o.E4M3, o.GRAN_BLOCK_POW2, rew)
     assert_gemm_close(D[rows], o.gemm_ref(ah, bh))
+
+
+# ---------------------------------------------------------------- MN-major operands
+@pytest.mark.parametrize("a_mn,b_mn", [(False, True), (True, False), (True, True)])
+@pytest.mark.parametrize("M,N,K,with_bias", [(256, 384, 512, False), (272, 400, 144, True), (128, 128, 16, False),
+                                             (528, 256, 1040, True)])
+@pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
+def test_mn_major_operands(a_mn, b_mn, M, N, K, with_bias, out):
+    """fp8_gemm_layout with A stored [K][M] and/or B stored [K][N]: bit-identical
+    to fp8_gemm on the same codes stored K-major, and within tolerance of the
+    oracle's product (ragged tiles in M, N and K, with and without bias)."""
+    a = wl.normal((M, K), 1.0, 131 + M, dtype=torch.float32)
+    b = wl.normal((N, K), 1.0, 132 + N, dtype=torch.float32)
+    qa, sa = _quant_tensor(a, sq.E5M2)
+    qb, sb = _quant_tensor(b, sq.E4M3)
+    bias = wl.normal((N,), 1.0, 133 + N, dtype=torch.float32).to(DEV) if with_bias else None
+    ref = _gemm_t(qa, sq.E5M2, sa, qb, sq.E4M3, sb, out, bias=bias)
+    A = qa.t().contiguous() if a_mn else qa
+    B = qb.t().contiguous() if b_mn else qb
+    D = torch.empty((M, N), dtype=out, device=DEV)
+    sq.fp8_gemm_layout(A, sq.E5M2, sa, sq.MN_MAJOR if a_mn else sq.K_MAJOR, B, sq.E4M3, sb,
+                       sq.MN_MAJOR if b_mn else sq.K_MAJOR, D, M, N, K, bias=bias)
+    torch.cuda.synchronize()
+    assert torch.equal(D.view(torch.uint8), ref.view(torch.uint8))
+    R = o.gemm_ref(o.dequantize(codes(qa), o.E5M2, 0, sa.item()), o.dequantize(codes(qb), o.E4M3, 0, sb.item()),
+                   bias=None if bias is None else bias.cpu().numpy())
+    assert_gemm_close(D, R)
+
+
+def test_mn_major_integer_operands_exact():
+    """Integer-valued codes, unit scales, both operands MN-major: the int64
+    product exactly."""
+    rng = np.random.default_rng(12)
+    M, N, K = 256, 512, 384
+    va, qa = _int_codes(rng, (M, K), o.E4M3, -8, 8)
+    vb, qb = _int_codes(rng, (N, K), o.E5M2, -8, 8)
+    D = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    sq.fp8_gemm_layout(torch.from_numpy(np.ascontiguousarray(qa.T)).to(DEV), sq.E4M3, _one(), sq.MN_MAJOR,
+                       torch.from_numpy(np.ascontiguousarray(qb.T)).to(DEV), sq.E5M2, _one(), sq.MN_MAJOR, D, M, N, K)
+    torch.cuda.synchronize()
+    assert np.array_equal(D.cpu().numpy(), (va.astype(np.int64) @ vb.astype(np.int64).T).astype(np.float32))
+
+
+def test_mn_major_rejects_unaligned_rows():
+    qa = torch.zeros((64, 40), dtype=torch.uint8, device=DEV)      # A [K][M] with M = 40
+    qb = torch.zeros((64, 32), dtype=torch.uint8, device=DEV)
+    D = torch.empty((40, 32), dtype=torch.float32, device=DEV)
+    with pytest.raises(sq.Fp8Error) as e:
+        sq.fp8_gemm_layout(qa, sq.E4M3, _one(), sq.MN_MAJOR, qb, sq.E4M3, _one(), sq.MN_MAJOR, D, 40, 32, 64)
+    assert e.value.code == sq.ERR_UNSUPPORTED
