@@ -163,86 +163,59 @@ def test_w2_minigpt_20_steps():
             assert layers[li].states.cpu().numpy().tobytes() == np.concatenate(refs[li]).tobytes(), (step, li)
 
 
-def _u8(shape):
-    return torch.empty(shape, dtype=torch.uint8, device=DEV)
-
-
 def test_w5_ffn_step_full_size():
-    """Workload 5 at full size, all 10 steps, in the launch configuration the
-    bench times: the granular calls chained as in a training step (x ->
+    """Workload 5 at full size, all 10 steps, through the bench's own step
+    (bench.FFNStep: the granular calls chained as in a training step, x ->
     linear 0 -> y0 -> linear 1; dy -> linear 1's dgrad and wgrad -> dx1 ->
-    linear 0's dgrad and wgrad), HYBRID delayed scaling, H = 16.
+    linear 0's dgrad and wgrad, with W1, dy and dx1 cast on the side stream
+    beside the GEMMs), HYBRID delayed scaling, H = 16.
 
-    Every step: the codes of all six casts equal the oracle's over the whole
-    tensor (the backward GEMMs read them MN-major), all six histories are bit-exact after the
-    update, and y, dx and dW are compared with the oracle on 32 sampled rows
-    per GEMM.  Each linear's input is the GPU's own output of the previous
-    linear (checked there), as in the bench."""
+    After every step: the codes of all six casts equal the oracle's over the
+    whole tensor, y, dx and dW match the oracle on 32 sampled rows per GEMM,
+    and all six histories are bit-exact after the update.  Each linear's
+    input is the GPU's own output of the previous linear (checked there)."""
+    import bench
     wk = wl.WORKLOADS[5]
     M, H = wk.tokens, wk.history_len
-    lin = [(l.in_features, l.out_features) for l in wk.linears]
-    W = [wl.linear_w(5, li, N, K, DEV) for li, (K, N) in enumerate(lin)]
-    Wf = [np32(w) for w in W]
-    states = torch.empty(6 * (H + 2), dtype=torch.float32, device=DEV)
-    sq.fp8_scale_init(states, 6, H)
-    st = [states[i * (H + 2):(i + 1) * (H + 2)] for i in range(6)]
-    sc = [states[i * (H + 2) + H + 1:i * (H + 2) + H + 2] for i in range(6)]
+    step = bench.FFNStep(torch.device(DEV), n_input_sets=wk.steps)
+    (K0, N0), (K1, N1) = step.lin
+    B0, B1 = step.buf
+    Wf = [np32(w) for w in step.W]
     ref = [o.state_init(H) for _ in range(6)]
-    fmts = [sq.E4M3, sq.E4M3, sq.E5M2] * 2
-    buf = [dict(qx=_u8((M, K)), qw=_u8((N, K)), qdy=_u8((M, N)),
-                y=torch.empty((M, N), dtype=torch.bfloat16, device=DEV),
-                dx=torch.empty((M, K), dtype=torch.bfloat16, device=DEV),
-                dw=torch.empty((N, K), dtype=torch.float32, device=DEV)) for (K, N) in lin]
+    fmts = [o.E4M3, o.E4M3, o.E5M2] * 2
     rng = np.random.default_rng(1)
 
-    def cast(src, fmt, si, q):
-        sq.fp8_quantize(src, fmt, sq.TENSOR, q, delayed_state=st[si], history_len=H)
-        torch.cuda.synchronize()
-        s_used = np.float32(ref[si][H + 1])                      # the oracle state's scale before the cast
+    def check_cast(src, fmt, si, q):
+        s_used = np.float32(ref[si][H + 1])              # the state's scale before the cast
         rq, _ = o.quantize_delayed(np32(src), fmt, ref[si])
         assert np.array_equal(codes(q), rq), ("codes", si)
-        assert np.float32(sc[si].item()) == s_used
         return rq, s_used
 
-    for step in range(wk.steps):
-        saved = []
-        xin = wl.linear_x(5, 0, step, M, lin[0][0], DEV)
-        for li, (K, N) in enumerate(lin):                            # forward
-            B = buf[li]
-            qx, sx = cast(xin, sq.E4M3, 3 * li, B["qx"])
-            qw, sw = cast(W[li], sq.E4M3, 3 * li + 1, B["qw"])
-            sq.fp8_gemm(B["qx"], sq.E4M3, sc[3 * li], sq.TENSOR, B["qw"], sq.E4M3, sc[3 * li + 1], sq.TENSOR, B["y"])
-            torch.cuda.synchronize()
-            rows = np.sort(rng.choice(M, 32, replace=False))
-            wh = o.dequantize(qw, o.E4M3, o.GRAN_TENSOR, sw)
-            assert_gemm_close(B["y"][rows], o.gemm_ref(o.dequantize(qx[rows], o.E4M3, o.GRAN_TENSOR, sx), wh))
-            saved.append((qx, sx, wh))
-            xin = B["y"]
-        dyin = wl.linear_dy(5, len(lin) - 1, step, M, lin[-1][1], DEV)
-        for li in reversed(range(len(lin))):                         # backward
-            K, N = lin[li]
-            B = buf[li]
-            qx, sx, wh = saved[li]
-            qd, sd = cast(dyin, sq.E5M2, 3 * li + 2, B["qdy"])
-            # dgrad reads W's codes and wgrad dy's and x's codes MN-major
-            sq.fp8_gemm_layout(B["qdy"], sq.E5M2, sc[3 * li + 2], sq.K_MAJOR, B["qw"], sq.E4M3, sc[3 * li + 1],
-                               sq.MN_MAJOR, B["dx"], M, K, N)
-            sq.fp8_gemm_layout(B["qdy"], sq.E5M2, sc[3 * li + 2], sq.MN_MAJOR, B["qx"], sq.E4M3, sc[3 * li],
-                               sq.MN_MAJOR, B["dw"], N, K, M)
-            torch.cuda.synchronize()
+    for s_ in range(wk.steps):
+        step.step(s_)
+        torch.cuda.synchronize()
+        x, dy = step.inputs[s_]
+        qx0, sx0 = check_cast(x, o.E4M3, 0, B0["qx"])
+        qw0, sw0 = check_cast(step.W[0], o.E4M3, 1, B0["qw"])
+        qw1, sw1 = check_cast(step.W[1], o.E4M3, 4, B1["qw"])
+        qd1, sd1 = check_cast(dy, o.E5M2, 5, B1["qdy"])
+        qx1, sx1 = check_cast(B0["y"], o.E4M3, 3, B1["qx"])
+        qd0, sd0 = check_cast(B1["dx"], o.E5M2, 2, B0["qdy"])
+        for (B, qx, sx, qw, sw, qd, sd, K, N) in ((B0, qx0, sx0, qw0, sw0, qd0, sd0, K0, N0),
+                                                  (B1, qx1, sx1, qw1, sw1, qd1, sd1, K1, N1)):
             rows = np.sort(rng.choice(M, 32, replace=False))
             wrows = np.sort(rng.choice(N, 32, replace=False))
+            wh = o.dequantize(qw, o.E4M3, o.GRAN_TENSOR, sw)
+            assert_gemm_close(B["y"][rows], o.gemm_ref(o.dequantize(qx[rows], o.E4M3, o.GRAN_TENSOR, sx), wh))
             assert_gemm_close(B["dx"][rows], o.gemm_ref(o.dequantize(qd[rows], o.E5M2, o.GRAN_TENSOR, sd), wh.T))
             dcols = o.dequantize(np.ascontiguousarray(qd[:, wrows].T), o.E5M2, o.GRAN_TENSOR, sd)
             xh = o.dequantize(qx, o.E4M3, o.GRAN_TENSOR, sx)
             assert_gemm_close(B["dw"][wrows], o.gemm_ref(dcols, xh.T))
             del xh, dcols
-            dyin = B["dx"]
-        sq.fp8_update_scale(states, 6, H, fmts)
         for i in range(6):
             o.update_scale(ref[i], fmts[i])
-        torch.cuda.synchronize()
-        assert states.cpu().numpy().tobytes() == np.concatenate(ref).tobytes(), step
+        assert step.states.cpu().numpy().tobytes() == np.concatenate(ref).tobytes(), s_
+    assert sq.fp8_device_status(True) == 0
 
 
 def test_w5_linear_api_full_size():
