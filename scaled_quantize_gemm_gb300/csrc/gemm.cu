@@ -311,11 +311,12 @@ __device__ __forceinline__ bool wait_bounded_cluster(uint64_t* bar, uint32_t par
     return wait_bounded_err_cluster(bar, parity, &g_dev_error);
 }
 
-template <bool OUT_BF16>
+// LAYOUT bit 0: A MN-major, bit 1: B MN-major (compile-time, so the
+// K-major instantiation issues its MMAs from hoisted descriptors)
+template <bool OUT_BF16, int LAYOUT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     k_gemm_tensor_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                       EpiParams p, uint32_t idesc, TileSched sched, const __grid_constant__ CUtensorMap tmD,
-                       int layout)
+                       EpiParams p, uint32_t idesc, TileSched sched, const __grid_constant__ CUtensorMap tmD)
 {
     pdl_enter();
     constexpr int BN = kPairBN, BH = BN / 2, STAGES = kPairStages;
@@ -333,7 +334,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     __shared__ int s_skip;
     const uint32_t rank = cluster_ctarank();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool a_mn = (layout & 1) != 0, b_mn = (layout & 2) != 0;   // MN-major operands
+    constexpr bool a_mn = (LAYOUT & 1) != 0, b_mn = (LAYOUT & 2) != 0;   // MN-major operands
 
     if (threadIdx.x == 0) {
         s_skip = rank == 0 ? *reinterpret_cast<volatile int*>(&g_dev_error) : 0;
@@ -443,13 +444,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     const uint32_t sa = smem_addr(smem + stage * L::STAGE);
                     // K = 32 slice k: 32 bytes further along a K-major row, or
                     // 32 rows (4 atoms, 4 KB) further down an MN-major tile
+                    // (start address in 16-byte units: +2 or +256)
+                    const uint64_t da = a_mn ? sdesc_mn_sw128(sa) : sdesc_kmajor_sw128(sa);
+                    const uint64_t db = b_mn ? sdesc_mn_sw128(sa + A_BYTES) : sdesc_kmajor_sw128(sa + A_BYTES);
+                    constexpr uint64_t sta = a_mn ? 256 : 2, stb = b_mn ? 256 : 2;
 #pragma unroll
-                    for (int k = 0; k < BK / 32; ++k) {
-                        const uint64_t da = a_mn ? sdesc_mn_sw128(sa + 4096u * k) : sdesc_kmajor_sw128(sa) + 2 * k;
-                        const uint64_t db = b_mn ? sdesc_mn_sw128(sa + A_BYTES + 4096u * k)
-                                                 : sdesc_kmajor_sw128(sa + A_BYTES) + 2 * k;
-                        mma_pair_f8f6f4(d, da, db, idesc, (kb | k) != 0 ? 1u : 0u);
-                    }
+                    for (int k = 0; k < BK / 32; ++k)
+                        mma_pair_f8f6f4(d, da + sta * k, db + stb * k, idesc, (kb | k) != 0 ? 1u : 0u);
                     mma_pair_commit(&empty[stage], 3);
                     if (++stage == STAGES) {
                         stage = 0;
@@ -1254,7 +1255,7 @@ int gemm_ctas(const GemmArgs& g, int sms)
         const int64_t tiles = ((g.M + 2 * BM - 1) / (2 * BM)) * ((g.N + kPairBN - 1) / kPairBN);
         const bool bf16 = g.d_dtype == kBF16;
         int clusters = 0;
-        if (pair_clusters(bf16 ? k_gemm_tensor_pair<true> : k_gemm_tensor_pair<false>, bf16 ? 1 : 0,
+        if (pair_clusters(bf16 ? k_gemm_tensor_pair<true, 0> : k_gemm_tensor_pair<false, 0>, bf16 ? 1 : 0,
                           PairSmem::BYTES, &clusters) != cudaSuccess || clusters < 1) {
             cudaGetLastError();
             return -1;
@@ -1308,9 +1309,19 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
         if (g.a_mn) idesc |= 1u << 15;          // A MN-major
         if (g.b_mn) idesc |= 1u << 16;          // B MN-major
         const int smem = PairSmem::BYTES;
-        auto kern = bf16 ? k_gemm_tensor_pair<true> : k_gemm_tensor_pair<false>;
+        const int layout = (g.a_mn ? 1 : 0) | (g.b_mn ? 2 : 0);
+        using PairKern = decltype(&k_gemm_tensor_pair<true, 0>);
+        static const PairKern kerns[2][4] = {
+            {k_gemm_tensor_pair<false, 0>, k_gemm_tensor_pair<false, 1>, k_gemm_tensor_pair<false, 2>,
+             k_gemm_tensor_pair<false, 3>},
+            {k_gemm_tensor_pair<true, 0>, k_gemm_tensor_pair<true, 1>, k_gemm_tensor_pair<true, 2>,
+             k_gemm_tensor_pair<true, 3>}};
+        auto kern = kerns[bf16 ? 1 : 0][layout];
         int clusters = 0;
+        // every layout instantiation has the same resources: one cached query
+        // per output type (and the shared-memory attribute set for this one)
         cudaError_t e = pair_clusters(kern, bf16 ? 1 : 0, smem, &clusters);
+        if (e == cudaSuccess) e = smem_attr_once(reinterpret_cast<const void*>(kern), smem);
         if (e != cudaSuccess) {
             *why = "cluster occupancy query failed";
             return e;
@@ -1320,7 +1331,7 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
             return cudaErrorNotSupported;
         }
         const int grid = 2 * (tiles < clusters ? tiles : clusters);
-        launch_k(kern, grid, 192, smem, st, ta, tb, p, idesc, sched, td, (g.a_mn ? 1 : 0) | (g.b_mn ? 2 : 0));
+        launch_k(kern, grid, 192, smem, st, ta, tb, p, idesc, sched, td);
         return cudaGetLastError();
     }
     if (g.mode == 1) return launch_promote<1>(g, p, st, sms, why);
