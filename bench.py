@@ -215,23 +215,26 @@ class FFNStep:
         return sum(3 * 2 * M * N * K for (K, N) in self.lin)
 
     def quant_bytes_per_step(self):
-        # bf16 read + code write per element (the backward GEMMs read the
-        # codes MN-major: no transposed copy)
+        # the four separate casts (x, W0, W1, dy): bf16 read + code write per
+        # element (no transposed copy: the backward GEMMs read the codes
+        # MN-major).  y0's and dx1's codes come out of GEMM epilogues.
+        (K0, N0), (K1, N1) = self.lin
         M = self.M
-        return sum(3 * (M * K + N * K + M * N) for (K, N) in self.lin)
+        return 3 * (M * K0 + N0 * K0 + N1 * K1 + M * N1)
 
     def step(self, s: int, ev=None, inputs=None, consumed=None):
         """One pass of the hot path through the granular C-ABI calls; `ev`
         (a list) receives (kind, start_event, end_event) per call.
 
-        Schedule: the six casts are HBM-bound and the six GEMMs tensor-bound,
-        so the casts no GEMM is waiting for run on a side stream, concurrently
-        with the GEMMs: W1 and the step's output gradient dy (which depend on
-        nothing in the step) while linear 0's forward GEMM runs, and linear
-        0's output gradient dx1 while linear 1's wgrad runs.  x, W0 and y0 are
-        cast on the main stream, in front of the GEMM that needs them.  The
-        side stream starts each step behind the previous step's scale update
-        and is joined back before this step's update.  `inputs` replaces the
+        Schedule: the casts are HBM-bound and the GEMMs tensor-bound.  The
+        casts of y0 (linear 1's input) and dx1 (linear 0's output gradient)
+        ride on the GEMMs that produce them (fp8_gemm_cast: the epilogue
+        writes the codes beside the bf16 output).  W1 and the step's output
+        gradient dy, which depend on nothing in the step, are cast on a side
+        stream while linear 0's forward GEMM runs.  x and W0 are cast on the
+        main stream in front of that GEMM, alone on the device: the side
+        stream starts behind them and is joined back before linear 1's
+        forward GEMM.  `inputs` replaces the
         resident (x, dy) of step s; `consumed` (an event) is recorded on the
         main stream once both have been cast."""
         sq = self.sq
@@ -256,46 +259,54 @@ class FFNStep:
         def cast(src, fmt, q, si):
             rec("quant", lambda: sq.fp8_quantize(src, fmt, sq.TENSOR, q, delayed_state=self.st(si), history_len=H))
 
-        def fwd(B, li):
-            rec("gemm", lambda: sq.fp8_gemm(B["qx"], sq.E4M3, self.s(3 * li), sq.TENSOR,
-                                            B["qw"], sq.E4M3, self.s(3 * li + 1), sq.TENSOR, B["y"]))
+        def fwd(B, li, K, N, cast_to=None):
+            if cast_to is None:
+                rec("gemm", lambda: sq.fp8_gemm(B["qx"], sq.E4M3, self.s(3 * li), sq.TENSOR,
+                                                B["qw"], sq.E4M3, self.s(3 * li + 1), sq.TENSOR, B["y"]))
+            else:                   # y's codes for the next linear, in the epilogue
+                q, si = cast_to
+                rec("gemm", lambda: sq.fp8_gemm_cast(B["qx"], sq.E4M3, self.s(3 * li), K_, B["qw"], sq.E4M3,
+                                                     self.s(3 * li + 1), K_, B["y"], M, N, K, q, sq.E4M3,
+                                                     self.st(si), H))
 
-        def dgrad(B, li, K, N):     # dx[M][K] = dy W: B = W's codes [N][K], MN-major
-            rec("gemm", lambda: sq.fp8_gemm_layout(B["qdy"], sq.E5M2, self.s(3 * li + 2), K_, B["qw"], sq.E4M3,
-                                                   self.s(3 * li + 1), MN_, B["dx"], M, K, N))
+        def dgrad(B, li, K, N, cast_to=None):     # dx[M][K] = dy W: B = W's codes [N][K], MN-major
+            if cast_to is None:
+                rec("gemm", lambda: sq.fp8_gemm_layout(B["qdy"], sq.E5M2, self.s(3 * li + 2), K_, B["qw"], sq.E4M3,
+                                                       self.s(3 * li + 1), MN_, B["dx"], M, K, N))
+            else:                   # dx's codes for the previous linear's backward, in the epilogue
+                q, si = cast_to
+                rec("gemm", lambda: sq.fp8_gemm_cast(B["qdy"], sq.E5M2, self.s(3 * li + 2), K_, B["qw"], sq.E4M3,
+                                                     self.s(3 * li + 1), MN_, B["dx"], M, K, N, q, sq.E5M2,
+                                                     self.st(si), H))
 
         def wgrad(B, li, K, N):     # dW[N][K] = dy^T x: dy's [M][N] and x's [M][K] codes, MN-major
             rec("gemm", lambda: sq.fp8_gemm_layout(B["qdy"], sq.E5M2, self.s(3 * li + 2), MN_, B["qx"], sq.E4M3,
                                                    self.s(3 * li), MN_, B["dw"], N, K, M))
 
         # forward
-        side.wait_stream(main)                       # behind the previous step's update
         cast(x, sq.E4M3, B0["qx"], 0)
         cast(self.W[0], sq.E4M3, B0["qw"], 1)
+        # the side stream starts behind x's and W0's casts (and so behind the
+        # previous step's update): those two are on the critical path and
+        # get the HBM to themselves
+        side.wait_stream(main)
         with torch.cuda.stream(side):
             cast(self.W[1], sq.E4M3, B1["qw"], 4)
             cast(dy, sq.E5M2, B1["qdy"], 5)
             self.ev_side.record(side)
-        fwd(B0, 0)
-        cast(B0["y"], sq.E4M3, B1["qx"], 3)
+        fwd(B0, 0, K0, N0, cast_to=(B1["qx"], 3))          # y0 and linear 1's input codes
         main.wait_event(self.ev_side)
         if consumed is not None:
             consumed.record(main)                   # x and dy have been cast
-        fwd(B1, 1)
+        fwd(B1, 1, K1, N1)
         # backward, last linear first
-        dgrad(B1, 1, K1, N1)
-        self.ev_main.record(main)
-        with torch.cuda.stream(side):
-            side.wait_event(self.ev_main)
-            cast(B1["dx"], sq.E5M2, B0["qdy"], 2)
-            self.ev_side.record(side)
+        dgrad(B1, 1, K1, N1, cast_to=(B0["qdy"], 2))        # dx1 and linear 0's output-gradient codes
         wgrad(B1, 1, K1, N1)
-        main.wait_event(self.ev_side)
         dgrad(B0, 0, K0, N0)
         wgrad(B0, 0, K0, N0)
         rec("update", lambda: sq.fp8_update_scale(self.states, 6, H, self.formats))
 
-    KERNELS_PER_STEP = 13   # 6 casts + 6 GEMMs + 1 scale update
+    KERNELS_PER_STEP = 11   # 4 casts + 6 GEMMs (two with the output cast) + 1 scale update
 
     def e2e_run(self, host_sets, steps: int, states_host, copy_ev=None, linear_api: bool = False):
         """`steps` steps with host buffers: each step's x and dy come from
@@ -418,22 +429,22 @@ def run_ours(args, ws, rank, local):
     per = {"gemm": [], "quant": [], "update": []}
     for kind, a, e in ev:
         per[kind].append(a.elapsed_time(e))
-    # the kernel's roofline from the GEMMs that run alone on the device:
-    # positions 1, 2, 4, 5 of the step's six (fwd1, dgrad1, dgrad0, wgrad0);
-    # fwd0 and wgrad1 share the device with the side stream's casts
+    # the kernel's roofline from the GEMMs that run alone on the device with
+    # a plain epilogue: positions 1, 3, 4, 5 of the step's six (fwd1, wgrad1,
+    # dgrad0, wgrad0); fwd0 shares the device with the side stream's casts,
+    # and fwd0 and dgrad1 also cast their outputs in the epilogue
     gemm_ms_all = statistics.mean(per["gemm"])
-    gemm_ms = statistics.mean(per["gemm"][i] for i in range(len(per["gemm"])) if i % 6 in (1, 2, 4, 5))
+    gemm_ms = statistics.mean(per["gemm"][i] for i in range(len(per["gemm"])) if i % 6 in (1, 3, 4, 5))
     gemm_flops_launch = flops / 6
     achieved = gemm_flops_launch / (gemm_ms * 1e-3) / 1e12
     quant_ms_step = sum(per["quant"]) / args.steps
     qbytes = b.quant_bytes_per_step()
     quant_gbs = qbytes / (quant_ms_step * 1e-3) / 1e9
-    # the 16384 x 14336 cast of y0 (linear 1's input): on the main stream,
-    # alone on the device (position 4 of the step's six casts in issue order:
-    # x0, W0, W1, dy, y0, dx1); dx1's cast of the same size runs beside
-    # linear 1's wgrad and is not a kernel-alone figure
-    big = [per["quant"][i] for i in range(len(per["quant"])) if i % 6 == 4]
-    big_bytes = 3 * WK.tokens * 14336
+    # the cast of x (16384 x 4096) on the main stream, alone on the device
+    # (position 0 of the step's four casts in issue order: x, W0, W1, dy;
+    # W1 and dy run beside linear 0's forward GEMM)
+    big = [per["quant"][i] for i in range(len(per["quant"])) if i % 4 == 0]
+    big_bytes = 3 * WK.tokens * WK.linears[0].in_features
     big_gbs = big_bytes / (statistics.mean(big) * 1e-3) / 1e9
 
     # ---- end to end through the linear API with pinned host buffers
@@ -523,8 +534,9 @@ def run_ours(args, ws, rank, local):
             "config": {"workload": WK.name, "tokens": WK.tokens,
                        "linears": [f"{K}->{N}" for (K, N) in b.lin], "history_len": H,
                        "chain": "x -> linear 0 -> y0 -> linear 1 -> y1; dy -> linear 1 dgrad -> dx1 -> linear 0",
-                       "schedule": "W1 and dy cast on a side stream during linear 0's forward GEMM, dx1 cast "
-                                   "during linear 1's wgrad; the rest in order on one stream",
+                       "schedule": "y0's and dx1's casts in the epilogues of the GEMMs that produce them; W1 and "
+                                   "dy cast on a side stream during linear 0's forward GEMM; the rest in order on "
+                                   "one stream",
                        "recipe": "HYBRID per-tensor delayed (E4M3 fwd, E5M2 grads), amax_compute_algo=max",
                        "outputs": "y bf16, dx bf16, dW fp32",
                        "l2": "no flush: every tensor a step reads is 117-470 MB and is touched once per step, "
@@ -545,18 +557,19 @@ def run_ours(args, ws, rank, local):
                          "peak_burst": round(fp8_peak, 1), "frac_of_burst": round(achieved / fp8_peak, 4),
                          "peak_sustained": round(fp8_sust, 1), "frac_of_sustained": round(achieved / fp8_sust, 4),
                          "flops_per_launch": gemm_flops_launch, "launch_ms": round(gemm_ms, 4),
-                         "launch_ms_rule": "mean of the step's four GEMMs that run alone on the device (fwd1, "
-                                           "dgrad1, dgrad0, wgrad0)",
+                         "launch_ms_rule": "mean of the step's four GEMMs that run alone on the device with a "
+                                           "plain epilogue (fwd1, wgrad1, dgrad0, wgrad0)",
                          "launch_ms_all_six": round(gemm_ms_all, 4)},
-            "roofline_quantize": {"bound": "hbm", "kernel": "k_cast_tensor (the 16384 x 14336 cast of y0, alone on the device)",
+            "roofline_quantize": {"bound": "hbm", "kernel": "k_cast_tensor (the 16384 x 4096 cast of x, alone on the device)",
                                   "achieved": round(big_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                                   "frac": round(big_gbs / hbm_peak, 4), "traffic": kernel_traffic("k_cast_tensor"),
                                   "peak_source": f"hbm_gbs {peak_src}",
                                   "bytes_per_launch": big_bytes},
             "quantize": {"GB_per_s_all_casts": round(quant_gbs, 1), "ms_per_step": round(quant_ms_step, 4),
                          "bytes_per_step": qbytes,
-                         "note": "sum of the six casts' own durations; W1, dy and dx1 run on a side stream beside "
-                                 "the GEMMs, so this is not their share of the step time"},
+                         "note": "the four separate casts (x, W0, W1, dy): the sum of their own durations; W1 "
+                                 "and dy run on a side stream beside a GEMM, so this is not their share of the step "
+                                 "time.  y0's and dx1's codes are written by the GEMM epilogues (fp8_gemm_cast)"},
             "gemm": {"ms_per_step": round(sum(per["gemm"]) / args.steps, 4),
                      "tflops_per_s_alone": round(achieved, 1),
                      "tflops_per_s_all_six": round(gemm_flops_launch / (gemm_ms_all * 1e-3) / 1e12, 1)},

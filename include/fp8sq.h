@@ -271,6 +271,25 @@ FP8SQ_API int fp8_gemm_layout(const uint8_t* A, int a_format, const void* a_scal
                               int64_t M, int64_t N, int64_t K, const float* bias, void* D, int d_dtype,
                               void* stream);
 
+/* fp8_gemm_cast: fp8_gemm_layout with a bf16 output D that also casts D, as
+ * stored, to FP8 in the GEMM's epilogue with delayed per-tensor scaling
+ * ([TS] delayed scaling; [W14] FP8 bullet): the result is the same as
+ *   fp8_gemm_layout(..., D, FP8SQ_BF16, ...);
+ *   fp8_quantize(D, FP8SQ_BF16, M, N, q_format, FP8SQ_TENSOR, q_state,
+ *                q_history_len, q_out, NULL, NULL, NULL, NULL, stream);
+ * (q_out[m][n] = sat_rne(fp32(D[m][n]) * q_state[H]), max|D| max-combined
+ * into q_state[0]) without reading D back: the next linear layer's input
+ * cast (or the previous layer's output-gradient cast) rides on this GEMM.
+ *   q_out     device u8 [M][N], 16-byte aligned; q_state device f32 state
+ *             block of q_history_len; q_format E4M3 or E5M2.
+ *   Needs K > 0, N % 16 == 0 (and the fp8_gemm_layout shape rules).
+ *   Saturations are not counted. */
+FP8SQ_API int fp8_gemm_cast(const uint8_t* A, int a_format, const void* a_scale, int a_major,
+                            const uint8_t* B, int b_format, const void* b_scale, int b_major,
+                            int64_t M, int64_t N, int64_t K, const float* bias, void* D,
+                            uint8_t* q_out, int q_format, float* q_state, int q_history_len,
+                            void* stream);
+
 /* ---- 5. linear layer ---------------------------------------------------------
  * [TE] te.Linear under fp8_autocast; [TS] Part 01 (HYBRID).
  * Forward  y[M][N]  = x[M][K] W[N][K]^T      (x, W quantised in E4M3)
@@ -392,7 +411,9 @@ FP8SQ_API int fp8_linear_fwd_noalloc(const void* x, const void* w, int64_t M, in
  *   cleared.
  * fp8_last_error: message for the calling thread's last non-zero status
  *   (static thread-local storage; never NULL).
- * fp8_abi_version: 5.  Changes from 4: fp8_gemm_layout added (MN-major
+ * fp8_abi_version: 6.  Changes from 5: fp8_gemm_cast added (the GEMM's
+ *   epilogue casts its bf16 output to FP8 with delayed scaling).
+ *   Changes from 4 to 5: fp8_gemm_layout added (MN-major
  *   operands); the per-tensor linear layer keeps no transposed codes (its
  *   backward reads the forward's codes MN-major), so
  *   fp8_linear_workspace_bytes(TENSOR) is smaller.

@@ -62,6 +62,7 @@ def lib() -> ctypes.CDLL:
                 "fp8_quantize_rows_cols": (I, [P, I64, I64, I, I, P, P, P, P, P, P]),
                 "fp8_gemm": (I, [P, I, P, I, P, I, P, I, I64, I64, I64, P, P, I, P]),
                 "fp8_gemm_layout": (I, [P, I, P, I, P, I, P, I, I64, I64, I64, P, P, I, P]),
+                "fp8_gemm_cast": (I, [P, I, P, I, P, I, P, I, I64, I64, I64, P, P, P, I, P, I, P]),
                 "fp8_linear_workspace_bytes": (Z, [I64, I64, I64, I]),
                 "fp8_linear_fwd": (I, [P, P, I64, I64, I64, I, I, P, P, I, P, Z, P, P, I, P]),
                 "fp8_linear_bwd": (I, [P, I64, I64, I64, I, I, P, I, P, Z, P, P, P]),
@@ -231,6 +232,25 @@ def fp8_gemm_layout(A, a_format: int, a_scale, a_major: int, B, b_format: int, b
     _opt(bias, "bias", T.float32, 4 * N)
     _check(lib().fp8_gemm_layout(_ptr(A), a_format, _ptr(a_scale), a_major, _ptr(B), b_format, _ptr(b_scale),
                                  b_major, M, N, K, _ptr(bias), _ptr(D), _dtype_code(D), _stream(stream)))
+
+
+def fp8_gemm_cast(A, a_format: int, a_scale, a_major: int, B, b_format: int, b_scale, b_major: int,
+                  D, M: int, N: int, K: int, q_out, q_format: int, q_state, history_len: int, bias=None,
+                  stream=None) -> None:
+    """fp8_gemm_layout with a bf16 D whose epilogue also casts D to FP8
+    codes q_out [M][N] with the delayed per-tensor state q_state."""
+    T = _t()
+    _need(A, "A", T.uint8, M * K)
+    _need(B, "B", T.uint8, N * K)
+    _need(D, "D", T.bfloat16, 2 * M * N)
+    _need(a_scale, "a_scale", T.float32, 4)
+    _need(b_scale, "b_scale", T.float32, 4)
+    _need(q_out, "q_out", T.uint8, M * N)
+    _need(q_state, "q_state", T.float32, 4 * (history_len + 2))
+    _opt(bias, "bias", T.float32, 4 * N)
+    _check(lib().fp8_gemm_cast(_ptr(A), a_format, _ptr(a_scale), a_major, _ptr(B), b_format, _ptr(b_scale),
+                               b_major, M, N, K, _ptr(bias), _ptr(D), _ptr(q_out), q_format, _ptr(q_state),
+                               history_len, _stream(stream)))
 
 
 def fp8_linear_workspace_bytes(M: int, N: int, K: int, gran: int = TENSOR) -> int:

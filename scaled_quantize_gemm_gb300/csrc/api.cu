@@ -204,7 +204,7 @@ int api_check_device(int* sms) { return check_device(sms); }
 
 extern "C" {
 
-FP8SQ_API int fp8_abi_version(void) { return 5; }
+FP8SQ_API int fp8_abi_version(void) { return 6; }
 
 FP8SQ_API const char* fp8_last_error(void) { return g_msg; }
 
@@ -483,6 +483,47 @@ FP8SQ_API int fp8_gemm_layout(const uint8_t* A, int a_format, const void* a_scal
         return fail(FP8SQ_ERR_CUDA, "fp8_gemm_layout: %s", why);
     }
     return cuda_status(e, "fp8_gemm_layout launch");
+}
+
+FP8SQ_API int fp8_gemm_cast(const uint8_t* A, int a_format, const void* a_scale, int a_major, const uint8_t* B,
+                            int b_format, const void* b_scale, int b_major, int64_t M, int64_t N, int64_t K,
+                            const float* bias, void* D, uint8_t* q_out, int q_format, float* q_state,
+                            int q_history_len, void* stream)
+{
+    if ((a_major != FP8SQ_K_MAJOR && a_major != FP8SQ_MN_MAJOR) || (b_major != FP8SQ_K_MAJOR && b_major != FP8SQ_MN_MAJOR))
+        return fail(FP8SQ_ERR_INVALID_ARG, "fp8_gemm_cast: a_major / b_major must be K_MAJOR or MN_MAJOR");
+    if (!valid_format(q_format)) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_gemm_cast: bad q_format");
+    if ((!q_out && M * N != 0) || !q_state) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_gemm_cast: null q_out or q_state");
+    if (q_history_len < 1 || q_history_len > 4096) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_gemm_cast: bad q_history_len");
+    int mode = 0;
+    int r = validate_gemm(A, a_format, a_scale, FP8SQ_TENSOR, B, b_format, b_scale, FP8SQ_TENSOR, M, N, K, bias, D,
+                          FP8SQ_BF16, &mode);
+    if (r) return r;
+    if (K == 0) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_gemm_cast: K == 0");
+    if (N % 16) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_gemm_cast: N %% 16 != 0");
+    if (a_major == FP8SQ_MN_MAJOR && M % 16)
+        return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_gemm_cast: an MN-major A needs M %% 16 == 0");
+    if (b_major == FP8SQ_MN_MAJOR && N % 16)
+        return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_gemm_cast: an MN-major B needs N %% 16 == 0");
+    if (!aligned16(q_out)) return fail(FP8SQ_ERR_MISALIGNED, "fp8_gemm_cast: q_out must be 16-byte aligned");
+    if (!aligned4(q_state)) return fail(FP8SQ_ERR_MISALIGNED, "fp8_gemm_cast: q_state must be 4-byte aligned");
+    int sms;
+    if ((r = check_device(&sms))) return r;
+    fp8sq::GemmArgs g;
+    g.A = A; g.B = B; g.a_format = a_format; g.b_format = b_format; g.mode = 0;
+    g.a_scale = a_scale; g.b_scale = b_scale; g.M = M; g.N = N; g.K = K;
+    g.bias = bias; g.D = D; g.d_dtype = fp8sq::kBF16;
+    g.a_mn = a_major == FP8SQ_MN_MAJOR;
+    g.b_mn = b_major == FP8SQ_MN_MAJOR;
+    g.q_out = q_out; g.q_state = q_state; g.q_history_len = q_history_len; g.q_format = q_format;
+    const char* why = nullptr;
+    cudaError_t e = fp8sq::launch_gemm(g, static_cast<cudaStream_t>(stream), sms, &why);
+    if (e == cudaErrorNotSupported) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_gemm_cast: %s", why ? why : "not supported");
+    if (e != cudaSuccess && why) {
+        cudaGetLastError();
+        return fail(FP8SQ_ERR_CUDA, "fp8_gemm_cast: %s", why);
+    }
+    return cuda_status(e, "fp8_gemm_cast launch");
 }
 
 FP8SQ_API size_t fp8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int gran)

@@ -88,6 +88,12 @@ struct EpiParams {
     const float* sB;     // mode 0: 1 float; mode 1: [N/128][K/128]
     const float* bias;   // [N] or null
     void* D;
+    // mode 0 with the output cast (QOUT): codes of D as stored, delayed
+    // per-tensor scaling with the state qstate (m = qstate[qH], max|D| into
+    // qstate[0])
+    uint8_t* Q = nullptr;
+    float* qstate = nullptr;
+    int qH = 0, qfmt = 0;
 };
 
 constexpr int BM = 128;
@@ -312,8 +318,12 @@ __device__ __forceinline__ bool wait_bounded_cluster(uint64_t* bar, uint32_t par
 }
 
 // LAYOUT bit 0: A MN-major, bit 1: B MN-major (compile-time, so the
-// K-major instantiation issues its MMAs from hoisted descriptors)
-template <bool OUT_BF16, int LAYOUT>
+// K-major instantiation issues its MMAs from hoisted descriptors).
+// QOUT (bf16 output only): the epilogue also casts the output, as stored in
+// bf16, to FP8 with the delayed per-tensor scale of p.qstate -- the codes
+// fp8_quantize would produce from D -- and max-combines max|D| into
+// p.qstate[0], so the next layer's cast never reads D back.
+template <bool OUT_BF16, int LAYOUT, bool QOUT = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     k_gemm_tensor_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        EpiParams p, uint32_t idesc, TileSched sched, const __grid_constant__ CUtensorMap tmD)
@@ -475,6 +485,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
         uint8_t* stg = smem + L::STG_OFF + (warp - 2) * kStageBytes;
         constexpr int SC = OUT_BF16 ? 16 : 8;   // columns per 32-byte staged row segment
         const uint32_t aempty0 = cluster_map(smem_addr(aempty), 0);
+        static_assert(!QOUT || OUT_BF16, "the output cast takes the bf16 output");
+        float qm = 1.0f;
+        uint32_t qmax = 0;                  // packed pair of |bf16| maxima
+        if constexpr (QOUT) qm = p.qstate[p.qH];
         int lt = 0;
         for (int t = cid; t < num_tiles; t += ncl, ++lt) {
             const int b = lt & 1;
@@ -503,12 +517,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
 #pragma unroll
                 for (int h = 0; h < 32 / SC; ++h)
                     stage_store<OUT_BF16>(stg, &tmD, v + h * SC, colc + h * SC, row0, p.M, p.N, lane);
+                if constexpr (QOUT) {
+                    // the codes of this lane's 32 outputs as rounded to bf16:
+                    // q = sat_rne(fp32(bf16(v)) * m), as the cast of D would
+                    uint32_t w[8];
+                    const int row = row0 + lane;
+                    // only outputs inside the matrix enter the maximum (a row
+                    // past M holds the bias; columns past N hold zeros)
+                    const uint32_t keep = row < p.M ? 0x7FFF7FFFu : 0u;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        __nv_bfloat162 h0 = __floats2bfloat162_rn(v[j], v[j + 1]);
+                        __nv_bfloat162 h1 = __floats2bfloat162_rn(v[j + 2], v[j + 3]);
+                        const uint32_t b0 = *reinterpret_cast<uint32_t*>(&h0), b1 = *reinterpret_cast<uint32_t*>(&h1);
+                        qmax = __vmaxu2(qmax, __vmaxu2(b0 & keep, b1 & keep));
+                        const float f0 = __fmul_rn(__uint_as_float(b0 << 16), qm);
+                        const float f1 = __fmul_rn(__uint_as_float(b0 & 0xFFFF0000u), qm);
+                        const float f2 = __fmul_rn(__uint_as_float(b1 << 16), qm);
+                        const float f3 = __fmul_rn(__uint_as_float(b1 & 0xFFFF0000u), qm);
+                        w[j / 4] = p.qfmt == kE4M3 ? (cvt_e4m3x2(f0, f1) | (cvt_e4m3x2(f2, f3) << 16))
+                                                   : (cvt_e5m2x2(f0, f1) | (cvt_e5m2x2(f2, f3) << 16));
+                    }
+                    if (row < p.M) {
+                        uint8_t* qrow = p.Q + (int64_t)row * p.N + colc;
+                        if (colc + 32 <= p.N) {
+                            *reinterpret_cast<uint4*>(qrow) = make_uint4(w[0], w[1], w[2], w[3]);
+                            *reinterpret_cast<uint4*>(qrow + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+                        } else {
+#pragma unroll
+                            for (int g8 = 0; g8 < 4; ++g8)
+                                if (colc + 8 * g8 + 8 <= p.N)
+                                    *reinterpret_cast<uint2*>(qrow + 8 * g8) = make_uint2(w[2 * g8], w[2 * g8 + 1]);
+                        }
+                    }
+                }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(aempty0 + 8u * b);
         }
         stage_store_drain(lane);
+        if constexpr (QOUT) {
+            uint32_t a = max(qmax & 0xFFFFu, qmax >> 16) << 16;
+            a = __reduce_max_sync(0xFFFFFFFFu, a);
+            if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(p.qstate), a);
+        }
     }
     __syncthreads();
     cluster_sync_all();                        // nothing is pending into either CTA any more
@@ -1311,12 +1364,22 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
         const int smem = PairSmem::BYTES;
         const int layout = (g.a_mn ? 1 : 0) | (g.b_mn ? 2 : 0);
         using PairKern = decltype(&k_gemm_tensor_pair<true, 0>);
-        static const PairKern kerns[2][4] = {
+        static const PairKern kerns[3][4] = {
             {k_gemm_tensor_pair<false, 0>, k_gemm_tensor_pair<false, 1>, k_gemm_tensor_pair<false, 2>,
              k_gemm_tensor_pair<false, 3>},
             {k_gemm_tensor_pair<true, 0>, k_gemm_tensor_pair<true, 1>, k_gemm_tensor_pair<true, 2>,
-             k_gemm_tensor_pair<true, 3>}};
-        auto kern = kerns[bf16 ? 1 : 0][layout];
+             k_gemm_tensor_pair<true, 3>},
+            {k_gemm_tensor_pair<true, 0, true>, k_gemm_tensor_pair<true, 1, true>,
+             k_gemm_tensor_pair<true, 2, true>, k_gemm_tensor_pair<true, 3, true>}};
+        if (g.q_out && !bf16) {
+            *why = "the fused output cast takes a bf16 output";
+            return cudaErrorNotSupported;
+        }
+        p.Q = g.q_out;
+        p.qstate = g.q_state;
+        p.qH = g.q_history_len;
+        p.qfmt = g.q_format;
+        auto kern = kerns[g.q_out ? 2 : (bf16 ? 1 : 0)][layout];
         int clusters = 0;
         // every layout instantiation has the same resources: one cached query
         // per output type (and the shared-memory attribute set for this one)

@@ -60,6 +60,11 @@ struct GemmArgs {
     // operand storage (mode 0 only): K-major A [M][K] / B [N][K], or
     // MN-major A [K][M] / B [K][N]
     bool a_mn = false, b_mn = false;
+    // mode 0, bf16 D only: also cast D to FP8 codes q_out [M][N] with the
+    // delayed per-tensor state q_state (history q_history_len)
+    uint8_t* q_out = nullptr;
+    float* q_state = nullptr;
+    int q_history_len = 0, q_format = kE4M3;
 };
 
 // gemm.cu

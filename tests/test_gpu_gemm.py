@@ -434,3 +434,57 @@ def test_mn_major_rejects_unaligned_rows():
     with pytest.raises(sq.Fp8Error) as e:
         sq.fp8_gemm_layout(qa, sq.E4M3, _one(), sq.MN_MAJOR, qb, sq.E4M3, _one(), sq.MN_MAJOR, D, 40, 32, 64)
     assert e.value.code == sq.ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------- GEMM with the output cast fused
+@pytest.mark.parametrize("a_mn,b_mn", [(False, False), (False, True), (True, True)])
+@pytest.mark.parametrize("M,N,K,with_bias", [(256, 384, 512, False), (272, 400, 144, True), (528, 256, 1040, True)])
+@pytest.mark.parametrize("qfmt", [sq.E4M3, sq.E5M2])
+def test_gemm_cast_equals_gemm_then_cast(a_mn, b_mn, M, N, K, with_bias, qfmt):
+    """fp8_gemm_cast: D bit-identical to fp8_gemm_layout's, the codes and the
+    delayed state bit-identical to fp8_quantize (TENSOR, delayed) of that D
+    run afterwards -- including a ragged M with bias, whose rows past M must
+    not enter the amax."""
+    H = 16
+    a = wl.normal((M, K), 1.0, 141 + M, dtype=torch.float32)
+    b = wl.normal((N, K), 1.0, 142 + N, dtype=torch.float32)
+    qa, sa = _quant_tensor(a, sq.E4M3)
+    qb, sb = _quant_tensor(b, sq.E4M3)
+    bias = wl.normal((N,), 3.0, 143 + N, dtype=torch.float32).to(DEV) if with_bias else None
+    A = qa.t().contiguous() if a_mn else qa
+    B = qb.t().contiguous() if b_mn else qb
+    la, lb = (sq.MN_MAJOR if a_mn else sq.K_MAJOR), (sq.MN_MAJOR if b_mn else sq.K_MAJOR)
+    st0 = torch.tensor(o.state_init(H), device=DEV)
+    st0[H] = 448.0 / 7.0 if qfmt == sq.E4M3 else 57344.0 / 7.0     # a multiplier under which some outputs saturate
+    st0[3] = 2.5                                                     # older history entries stay put
+    # reference: the GEMM, then the delayed cast of its bf16 output
+    D_ref = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    sq.fp8_gemm_layout(A, sq.E4M3, sa, la, B, sq.E4M3, sb, lb, D_ref, M, N, K, bias=bias)
+    st_ref = st0.clone()
+    q_ref = torch.empty((M, N), dtype=torch.uint8, device=DEV)
+    sq.fp8_quantize(D_ref, qfmt, sq.TENSOR, q_ref, delayed_state=st_ref, history_len=H)
+    # fused
+    D = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    q = torch.empty((M, N), dtype=torch.uint8, device=DEV)
+    st = st0.clone()
+    sq.fp8_gemm_cast(A, sq.E4M3, sa, la, B, sq.E4M3, sb, lb, D, M, N, K, q, qfmt, st, H, bias=bias)
+    torch.cuda.synchronize()
+    assert torch.equal(D.view(torch.int16), D_ref.view(torch.int16))
+    assert torch.equal(q, q_ref)
+    assert st.cpu().numpy().tobytes() == st_ref.cpu().numpy().tobytes()
+    # and against the oracle's cast of the same bf16 output
+    rst = st0.cpu().numpy().copy()
+    rq, _ = o.quantize_delayed(np32(D), qfmt, rst)
+    assert np.array_equal(codes(q), rq) and rst.tobytes() == st.cpu().numpy().tobytes()
+
+
+def test_gemm_cast_rejects_n_not_multiple_of_16():
+    qa = torch.zeros((64, 32), dtype=torch.uint8, device=DEV)
+    qb = torch.zeros((40, 32), dtype=torch.uint8, device=DEV)     # N = 40: not a multiple of 16
+    D = torch.empty((64, 40), dtype=torch.bfloat16, device=DEV)
+    q = torch.empty((64, 40), dtype=torch.uint8, device=DEV)
+    st = torch.tensor(o.state_init(16), device=DEV)
+    with pytest.raises(sq.Fp8Error) as e:
+        sq.fp8_gemm_cast(qa, sq.E4M3, _one(), sq.K_MAJOR, qb, sq.E4M3, _one(), sq.K_MAJOR, D, 64, 40, 32, q, sq.E4M3,
+                         st, 16)
+    assert e.value.code == sq.ERR_UNSUPPORTED
