@@ -578,10 +578,15 @@ __device__ __forceinline__ int64_t mx_tiled_offset(int64_t r, int64_t t, int64_t
 // codes: both operands of a fine-grained linear's products from one read of
 // x.  A row's 32 columns are four lanes of one warp; its 128 columns are four
 // warps (shuffles over l ^ 1, l ^ 2, then shared memory), and thread
-// 128 + r computes row r's 1x128 scale.  Three CTAs per SM (80 registers),
-// except ROWQ with MX-32 rows: two (128 registers; at three it spills).
+// 128 + r computes row r's 1x128 scale.  The CTA's loads are all issued at
+// its start and nothing is loaded while it reduces and casts, so the SM's
+// memory pipe needs several CTAs: 128-row tiles run four per SM (64
+// registers; at three, 80 registers, 16384 x 14336 column tiles took 131.5
+// against 117.3 us), 32-row blocks three (at four they spill and were
+// slower: 139 against 133 us; with row units too, 80 registers and a few
+// spilled bytes, 227 against 231 us at two).
 template <int FMT, int UNIT, bool ROWQ = false>
-__global__ void __launch_bounds__(256, ROWQ && UNIT == 32 ? 2 : 3) k_quant_col_block(const void* __restrict__ x, int64_t R, int64_t C,
+__global__ void __launch_bounds__(256, UNIT == 32 ? 3 : 4) k_quant_col_block(const void* __restrict__ x, int64_t R, int64_t C,
                                                          uint8_t* __restrict__ q, uint8_t* __restrict__ qT,
                                                          void* scales, void* rscales, unsigned long long* sat)
 {
@@ -1086,17 +1091,27 @@ static int resident_per_sm(const void* kern)
     return b;
 }
 
+// CTAs a grid-stride flat kernel is launched with per SM: a whole number of
+// the CTAs that fit at once, about eight.  A grid that is not a whole
+// number of resident waves runs its last CTAs as a partial wave (a 16384 x
+// 14336 cast ran at 0.80 of HBM with 8 CTAs per SM requested and 6
+// resident, 0.91 with 6); two full waves of 4 (the 64-register row-unit
+// casts) time slightly better than one.
+static int64_t flat_cap(const void* kern, int sms)
+{
+    const int per_sm = resident_per_sm(kern);
+    const int waves = per_sm >= 8 ? 1 : 8 / per_sm;
+    return (int64_t)sms * per_sm * waves;
+}
+
 // Grid of a grid-stride flat kernel over nch work items (kFlatUnroll per
-// thread per pass): no more CTAs than fit on the device at once.  A grid
-// larger than that runs its last CTAs as a second, mostly empty wave (a
-// 16384 x 14336 cast ran at 0.80 of HBM with 8 CTAs per SM requested and 6
-// resident).
+// thread per pass).
 template <typename K>
 static int flat_grid(K kern, int64_t nch, int sms)
 {
     const int64_t per_block = (int64_t)kFlatThreads * kFlatUnroll;
     const int64_t need = (nch + per_block - 1) / per_block;
-    const int64_t cap = (int64_t)sms * resident_per_sm(reinterpret_cast<const void*>(kern));
+    const int64_t cap = flat_cap(reinterpret_cast<const void*>(kern), sms);
     const int64_t g = need < cap ? need : cap;
     return g < 1 ? 1 : (int)g;
 }
@@ -1109,7 +1124,7 @@ static void flat_grid2(K kern, int64_t na, int64_t nb, int sms, int& ga, int& gb
 {
     const int64_t per_block = (int64_t)kFlatThreads * kFlatUnroll;
     const int64_t need_a = (na + per_block - 1) / per_block, need_b = (nb + per_block - 1) / per_block;
-    const int64_t cap = (int64_t)sms * resident_per_sm(reinterpret_cast<const void*>(kern));
+    const int64_t cap = flat_cap(reinterpret_cast<const void*>(kern), sms);
     int64_t a = need_a < 1 ? 1 : need_a, b = need_b < 1 ? 1 : need_b;
     if (a + b > cap) {
         a = (int64_t)((double)cap * (double)na / (double)(na + nb) + 0.5);
