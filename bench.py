@@ -970,9 +970,11 @@ def kernel_case(case: str, launches: int):
             sq.fp8_quantize(w, sq.E4M3, sq.BLOCK_128x128, qw, scales_out=sw)
             sq.fp8_quantize(a4, sq.E4M3, sq.MX32_TILED, qa, scales_out=ea)
             sq.fp8_quantize(dy, sq.E5M2, sq.TILE_128x1, None, qT=qdT, scales_out=sd)
-    elif case == "ln":
-        # LayerNorm fused into the delayed E4M3 cast with the transposed copy,
-        # 16384 x 4096 (k_ln_stats, then k_cast_tensor_T in its LayerNorm mode)
+    elif case in ("ln", "ln1"):
+        # LayerNorm fused into the delayed E4M3 cast, 16384 x 4096: "ln" with
+        # the transposed copy (k_ln_rows for the statistics, then
+        # k_cast_tensor_T in its LayerNorm mode), "ln1" without it
+        # (k_ln_rows, one pass)
         M, K = 16384, 4096
         xl = wl.normal((M, K), 2.0, 11, dev)
         gamma = torch.rand(K, generator=torch.Generator().manual_seed(12)).add_(0.5).to(dev)
@@ -981,7 +983,8 @@ def kernel_case(case: str, launches: int):
         mu = torch.empty(M, dtype=torch.float32, device=dev)
         rs = torch.empty(M, dtype=torch.float32, device=dev)
         for _ in range(launches):
-            sq.fp8_layernorm_quantize(xl, gamma, beta, 1e-5, sq.E4M3, ql, qlT, mu, rs, st, H)
+            sq.fp8_layernorm_quantize(xl, gamma, beta, 1e-5, sq.E4M3, ql, qlT if case == "ln" else None, mu, rs,
+                                      st, H)
     elif case == "promote":
         x, w = wl.w3_operands(dev)
         qx, qw = torch.empty(x.shape, **u8), torch.empty(w.shape, **u8)
@@ -1217,6 +1220,11 @@ def modes_table(reps: int = 10):
     row("fp8_layernorm_quantize E4M3 delayed, with qT (6 B moved / element)", f"{M}x{K}",
         med(lambda: sq.fp8_layernorm_quantize(xl, gamma, beta, 1e-5, sq.E4M3, ql, qlT, mu, rs, stl, H)),
         nbytes=6 * M * K)
+    # without the transposed copy: one pass (k_ln_rows), x read once and the
+    # codes written = 3 bytes moved per element
+    row("fp8_layernorm_quantize E4M3 delayed, no qT (one pass, 3 B moved / element)", f"{M}x{K}",
+        med(lambda: sq.fp8_layernorm_quantize(xl, gamma, beta, 1e-5, sq.E4M3, ql, None, mu, rs, stl, H)),
+        nbytes=3 * M * K)
     del xl, ql, qlT
 
     # workload 4: MX-32, and the per-tensor GEMM on the same operands
@@ -1248,7 +1256,7 @@ def modes_table(reps: int = 10):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel-case", choices=["gemm", "cast", "promote", "wgrad", "mx", "fine", "ln"], default=None,
+    ap.add_argument("--kernel-case", choices=["gemm", "cast", "promote", "wgrad", "mx", "fine", "ln", "ln1"], default=None,
                     help="run a few launches of one kernel (for profiling) and exit")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--modes", action="store_true",

@@ -47,7 +47,7 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity)
 // function attribute on every launch puts a driver call on the launch path
 // that held back back-to-back calls (a fine-grained backward took 279 us in
 // a loop of calls against 238 us replayed from a CUDA graph).
-static cudaError_t smem_attr_once(const void* kern, int bytes)
+cudaError_t smem_attr_once(const void* kern, int bytes)
 {
     static std::mutex mu;
     static const void* done_kern[128];

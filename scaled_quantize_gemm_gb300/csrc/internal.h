@@ -69,6 +69,8 @@ struct GemmArgs {
 
 // gemm.cu
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char** why);
+// Raises a kernel's dynamic shared-memory limit to `bytes`, once per device.
+cudaError_t smem_attr_once(const void* kern, int bytes);
 int gemm_ctas(const GemmArgs& g, int sms);   // SMs its persistent grid occupies, -1 if unknown
 int read_device_error(int clear);   // 0 or the GEMM kernels' device error word
 // launches a kernel whose bounded wait is made to run out (failure-path test)

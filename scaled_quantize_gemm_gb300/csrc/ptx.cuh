@@ -52,6 +52,15 @@ __device__ __forceinline__ uint32_t cvt_fp8x2(float lo, float hi)
     else return cvt_e5m2x2(lo, hi);
 }
 
+// ------------------------------------------------------------------ cp.async
+// 16-byte global -> shared copies (L2 only), completed per thread by groups
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
 {

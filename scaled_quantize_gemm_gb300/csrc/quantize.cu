@@ -742,128 +742,350 @@ __global__ void __launch_bounds__(256, UNIT == 32 ? 3 : 4) k_quant_col_block(con
 }
 
 // LayerNorm statistics: mean = sum(x) / K and var = sum((x - mean)^2) / K in
-// fp32, rstd = 1 / sqrt(var + eps) with IEEE division and square root.  Two
-// warps per row, each holding half of the row in registers (rows of up to
-// 2 x 32 x 8 x LN_REG elements, 4096 for LN_REG = 8, are read once); each
-// lane sums its chunks in a tree and over LN_ACC independent accumulators,
-// then a warp tree, then the two warps' partials meet in shared memory (in a
-// fixed order, so both warps hold the same mean).  Longer rows take a
-// two-pass loop.  Half a row per warp and short dependency chains keep the
-// registers low enough for three blocks (24 warps) per SM.
-constexpr int LN_REG = 8;
-constexpr int LN_ACC = 4;
-constexpr int LN_ROWS = 4;       // rows per 256-thread block
+// fp32, rstd = 1 / sqrt(var + eps) with IEEE division and square root.  One
+// reduction order serves every LayerNorm kernel, so the statistics (and hence
+// the codes) do not depend on which kernel produced them: a 256-thread CTA
+// takes LN_RB rows at a time, thread t owns the 8-element chunks t, t + 256,
+// ... of every row and sums them in that order (each chunk as a tree of
+// (even, odd) element pairs; the pair's two partials added last), then the
+// warp reduction of warp_sum4, then the eight warps' partials in a fixed
+// tree; one lane per row divides, and broadcasts the result.
+constexpr int LN_RB = 4;         // rows per CTA iteration
+constexpr int LN_CT = 2;         // chunks per thread held in registers: K <= 256 x 8 x LN_CT
 
-__device__ __forceinline__ float ln_sum8(const float (&f)[8])
+// The arithmetic below works on (even, odd) element pairs with the packed
+// fp32x2 instructions; each lane of a pair is an IEEE round-to-nearest fp32
+// operation, so the pairing changes only how many instructions run.
+__device__ __forceinline__ void bf16x8_pairs(const uint4& w, float2 (&p)[4])
 {
-    return __fadd_rn(__fadd_rn(__fadd_rn(f[0], f[1]), __fadd_rn(f[2], f[3])),
-                     __fadd_rn(__fadd_rn(f[4], f[5]), __fadd_rn(f[6], f[7])));
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) p[k] = make_float2(__uint_as_float(ws[k] << 16), __uint_as_float(ws[k] & 0xFFFF0000u));
 }
-__device__ __forceinline__ float ln_sq8(const float (&f)[8], float mean)
+// acc + the chunk's sum, as (even, odd) partials: ((p0 + p1) + (p2 + p3))
+__device__ __forceinline__ float2 ln_sum8(const float2 (&p)[4], float2 acc)
 {
-    float d[8];
+    return __fadd2_rn(acc, __fadd2_rn(__fadd2_rn(p[0], p[1]), __fadd2_rn(p[2], p[3])));
+}
+// acc + the chunk's squared deviations from the mean (nm = -mean), in order
+__device__ __forceinline__ float2 ln_sq8(const float2 (&p)[4], float2 nm, float2 acc)
+{
 #pragma unroll
-    for (int j = 0; j < 8; ++j) d[j] = __fsub_rn(f[j], mean);
-    float a = __fmul_rn(d[0], d[0]), b = __fmul_rn(d[1], d[1]);
-#pragma unroll
-    for (int j = 2; j < 8; j += 2) {
-        a = __fmaf_rn(d[j], d[j], a);
-        b = __fmaf_rn(d[j + 1], d[j + 1], b);
+    for (int k = 0; k < 4; ++k) {
+        const float2 d = __fadd2_rn(p[k], nm);
+        acc = __ffma2_rn(d, d, acc);
     }
-    return __fadd_rn(a, b);
+    return acc;
 }
-__device__ __forceinline__ float warp_sum(float v)
+// NaN-propagating max of a and |b| (|x| orders like its fp32 bit pattern,
+// and every NaN an fp32 operation returns is the canonical 0x7FFFFFFF, the
+// largest |x| pattern: the same result as the integer max of the patterns)
+__device__ __forceinline__ float max_abs_nan(float a, float b)
 {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(fabsf(b)));
+    return d;
+}
+// The LayerNorm of a chunk, y = (x - mean) rstd gamma + beta, its |y| max
+// into amax, and its codes under the multiplier m (the arithmetic of cast8).
+template <int FMT>
+__device__ __forceinline__ uint2 ln_cast8(const float2 (&p)[4], float2 nm, float2 rs, const float2 (&g)[4],
+                                          const float2 (&be)[4], float m, float& amax, uint32_t& nsat)
+{
+    float2 y[4];
+    float a = 0.0f;
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    for (int k = 0; k < 4; ++k) {
+        y[k] = __ffma2_rn(__fmul2_rn(__fadd2_rn(p[k], nm), rs), g[k], be[k]);
+        a = max_abs_nan(max_abs_nan(a, y[k].x), y[k].y);
+    }
+    amax = max_abs_nan(amax, a);
+    const float2 m2 = make_float2(m, m);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) y[k] = __fmul2_rn(y[k], m2);
+    if (__float_as_uint(a) >= 0x7F800000u || __fmul_rn(a, m) > Fmt<FMT>::fmax) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            nsat += (fabsf(y[k].x) > Fmt<FMT>::fmax ? 1u : 0u) + (fabsf(y[k].y) > Fmt<FMT>::fmax ? 1u : 0u);
+    }
+    return make_uint2(cvt_fp8x2<FMT>(y[0].x, y[0].y) | (cvt_fp8x2<FMT>(y[1].x, y[1].y) << 16),
+                      cvt_fp8x2<FMT>(y[2].x, y[2].y) | (cvt_fp8x2<FMT>(y[3].x, y[3].y) << 16));
+}
+
+// The warp sums of LN_RB = 4 per-lane values (one per row) in six shuffles:
+// a reduce-scatter over lane bits 4 and 3 (lanes 0-15 keep rows 0-1, lanes
+// 8-15 and 24-31 then keep the odd row), then a butterfly over bits 2-0.
+// Lane l returns the sum of row l >> 3, the same value in all eight lanes of
+// its group.
+__device__ __forceinline__ float warp_sum4(const float (&s)[LN_RB], int lane)
+{
+    const bool b4 = lane & 16, b3 = lane & 8;
+    const float u0 = __fadd_rn(b4 ? s[2] : s[0], __shfl_xor_sync(0xFFFFFFFFu, b4 ? s[0] : s[2], 16));
+    const float u1 = __fadd_rn(b4 ? s[3] : s[1], __shfl_xor_sync(0xFFFFFFFFu, b4 ? s[1] : s[3], 16));
+    float v = __fadd_rn(b3 ? u1 : u0, __shfl_xor_sync(0xFFFFFFFFu, b3 ? u0 : u1, 8));
+#pragma unroll
+    for (int o = 4; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
     return v;
 }
+// The eight warps' partials of row j, in a fixed tree.
+__device__ __forceinline__ float ln_tree8(const float (*p)[LN_RB], int j)
+{
+    return __fadd_rn(__fadd_rn(__fadd_rn(p[0][j], p[1][j]), __fadd_rn(p[2][j], p[3][j])),
+                     __fadd_rn(__fadd_rn(p[4][j], p[5][j]), __fadd_rn(p[6][j], p[7][j])));
+}
+// One reduction of the LN_RB rows over the CTA: the warp sums (lanes 0, 8,
+// 16, 24 store theirs), a barrier, then every lane takes the CTA total of
+// row lane % LN_RB.  The caller must not write p again before every warp has
+// passed a later barrier.
+__device__ __forceinline__ float cta_rows_sum(const float (&s)[LN_RB], float (*p)[LN_RB], int warp, int lane)
+{
+    const float v = warp_sum4(s, lane);
+    if ((lane & 7) == 0) p[warp][lane >> 3] = v;
+    __syncthreads();
+    return ln_tree8(p, lane & (LN_RB - 1));
+}
 
-__global__ void __launch_bounds__(256, 3) k_ln_stats(const uint16_t* __restrict__ x, int64_t R, int64_t K, float eps,
-                                                     float* __restrict__ mu, float* __restrict__ rstd)
+// Rows of up to 4096 elements, held in registers from the statistics to the
+// codes (CAST = true: LayerNorm fused into the delayed per-tensor cast, x
+// read once, 3 B moved per element; CAST = false: the statistics alone, for
+// the two-pass cast with a transposed copy).  The CTAs (as many as fit at
+// once) walk groups of LN_RB rows.  Each thread copies its own chunks of the
+// next group into a shared-memory stage (cp.async) as soon as its sums have
+// consumed the current group's, so the next group's loads are in flight
+// while the current one is reduced, normalised and cast; no barrier guards
+// the stage, as a thread reads back only what it copied.  gamma and beta are
+// staged once per CTA as four arrays of 16-byte halves, so that the warp's
+// reads of a chunk's gamma / beta halves are consecutive 16-byte words (no
+// bank conflicts); a thread applies them to the LN_RB rows of a group.
+template <bool CAST>
+__host__ __device__ constexpr int ln_rows_smem(int K)
+{
+    return (CAST ? 2 * K * 4 : 0) + LN_RB * K * 2;    // gamma and beta (fp32), then the row stage (bf16)
+}
+
+template <bool CAST, int FMT>
+__global__ void __launch_bounds__(256, 3) k_ln_rows(const uint16_t* __restrict__ x, int64_t R, int K, float eps,
+                                                    const float* __restrict__ gamma, const float* __restrict__ beta,
+                                                    float* __restrict__ mu, float* __restrict__ rstd,
+                                                    uint8_t* __restrict__ q, float* state, int H, float* s_out,
+                                                    unsigned long long* sat)
 {
     pdl_enter();
-    __shared__ float part[LN_ROWS][2];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rl = warp >> 1, half = warp & 1;
-    const int64_t r = (int64_t)blockIdx.x * LN_ROWS + rl;
-    const bool live = r < R;                   // whole rows: both warps of a row agree
-    const uint16_t* row = x + (live ? r : 0) * K;
-    const int64_t nch = K / 8;                 // 8-element chunks of the row
-    const int64_t hch = (nch + 1) / 2;         // chunks of the first half
-    const int64_t c0 = half ? hch : 0, c1 = half ? nch : hch;
-    float mean, ss;
-    if (hch <= 32 * LN_REG) {
-        Vec8<kBF16> v[LN_REG];
+    extern __shared__ __align__(16) uint8_t ln_smem[];
+    __shared__ float part[2][8][LN_RB];        // sums, then squared deviations
+    __shared__ uint32_t red[8];
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int nch = K / 8;
+    float4* gb4 = reinterpret_cast<float4*>(ln_smem);          // CAST: gamma lo, gamma hi, beta lo, beta hi [nch]
+    uint4* xs = reinterpret_cast<uint4*>(ln_smem + (CAST ? 2 * K * 4 : 0));   // [LN_RB][nch] chunks
+    const int64_t stride = (int64_t)gridDim.x * LN_RB;
+    auto stage = [&](int64_t r0) {
 #pragma unroll
-        for (int i = 0; i < LN_REG; ++i) {
-            const int64_t c = c0 + lane + 32 * i;
-            if (live && c < c1) v[i].load(row, c * 8); else v[i].zero();
+        for (int j = 0; j < LN_RB; ++j) {
+            if (r0 + j >= R) continue;
+            const uint16_t* row = x + (r0 + j) * (int64_t)K;
+#pragma unroll
+            for (int i = 0; i < LN_CT; ++i) {
+                const int c = t + 256 * i;
+                if (c < nch) cp_async16(&xs[j * nch + c], row + c * 8);
+            }
         }
-        float acc[LN_ACC];
-#pragma unroll
-        for (int k = 0; k < LN_ACC; ++k) acc[k] = 0.0f;
-#pragma unroll
-        for (int i = 0; i < LN_REG; ++i) {
-            float f[8];
-            v[i].get(f);
-            acc[i % LN_ACC] = __fadd_rn(acc[i % LN_ACC], ln_sum8(f));
+        cp_async_commit();
+    };
+    stage((int64_t)blockIdx.x * LN_RB);
+    float m = 0.0f;
+    if (CAST) {
+        const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int c = t; c < nch; c += 256) {
+            const float4* g = reinterpret_cast<const float4*>(gamma) + 2 * c;
+            const float4* b = reinterpret_cast<const float4*>(beta) + 2 * c;
+            gb4[c] = g[0];
+            gb4[nch + c] = g[1];
+            gb4[2 * nch + c] = beta ? b[0] : z4;
+            gb4[3 * nch + c] = beta ? b[1] : z4;
         }
-        float sum = __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3]));
-        sum = warp_sum(sum);
-        if (lane == 0) part[rl][half] = sum;
         __syncthreads();
-        mean = __fdiv_rn(__fadd_rn(part[rl][0], part[rl][1]), (float)K);
+        m = state[H];
+        if (blockIdx.x == 0 && t == 0 && s_out) *s_out = state[H + 1];
+    }
+    float amax = 0.0f;
+    uint32_t nsat = 0;
+    for (int64_t r0 = (int64_t)blockIdx.x * LN_RB; r0 < R; r0 += stride) {
+        cp_async_wait_all();
+        Vec8<kBF16> v[LN_RB][LN_CT];
 #pragma unroll
-        for (int k = 0; k < LN_ACC; ++k) acc[k] = 0.0f;
+        for (int j = 0; j < LN_RB; ++j) {
 #pragma unroll
-        for (int i = 0; i < LN_REG; ++i) {
-            if (c0 + lane + 32 * i >= c1) continue;
-            float f[8];
-            v[i].get(f);
-            acc[i % LN_ACC] = __fadd_rn(acc[i % LN_ACC], ln_sq8(f, mean));
+            for (int i = 0; i < LN_CT; ++i) {
+                const int c = t + 256 * i;
+                if (r0 + j < R && c < nch) v[j][i].w = xs[j * nch + c]; else v[j][i].zero();
+            }
         }
-        ss = __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3]));
-    } else {
-        float sum = 0.0f;
-        for (int64_t c = c0 + lane; live && c < c1; c += 32) {
+        float s[LN_RB];
+#pragma unroll
+        for (int j = 0; j < LN_RB; ++j) {
+            float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int i = 0; i < LN_CT; ++i) {
+                if (t + 256 * i >= nch) continue;
+                float2 p[4];
+                bf16x8_pairs(v[j][i].w, p);
+                acc = ln_sum8(p, acc);
+            }
+            s[j] = __fadd_rn(acc.x, acc.y);
+        }
+        // the sums have consumed this group's chunks: start the next group's
+        stage(r0 + stride);
+        // lane l: the mean of row l % LN_RB, then every row's by broadcast
+        const float mean_l = __fdiv_rn(cta_rows_sum(s, part[0], warp, lane), (float)K);
+        float mean[LN_RB];
+#pragma unroll
+        for (int j = 0; j < LN_RB; ++j) mean[j] = __shfl_sync(0xFFFFFFFFu, mean_l, j);
+#pragma unroll
+        for (int j = 0; j < LN_RB; ++j) {
+            float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int i = 0; i < LN_CT; ++i) {
+                if (t + 256 * i >= nch) continue;
+                float2 p[4];
+                bf16x8_pairs(v[j][i].w, p);
+                acc = ln_sq8(p, make_float2(-mean[j], -mean[j]), acc);
+            }
+            s[j] = __fadd_rn(acc.x, acc.y);
+        }
+        // (part[0] of the next group is written only after every warp has
+        // passed the barrier in this call, i.e. has read this group's sums)
+        const float var_l = __fdiv_rn(cta_rows_sum(s, part[1], warp, lane), (float)K);
+        const float rs_l = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var_l, eps)));
+        if (warp == 0 && lane < LN_RB && r0 + lane < R) {
+            mu[r0 + lane] = mean_l;
+            rstd[r0 + lane] = rs_l;
+        }
+        float rs[LN_RB];
+#pragma unroll
+        for (int j = 0; j < LN_RB; ++j) rs[j] = __shfl_sync(0xFFFFFFFFu, rs_l, j);
+        if (CAST) {
+#pragma unroll
+            for (int i = 0; i < LN_CT; ++i) {
+                const int c = t + 256 * i;
+                if (c >= nch) continue;
+                const float4 ga = gb4[c], gh = gb4[nch + c], ba = gb4[2 * nch + c], bh = gb4[3 * nch + c];
+                const float2 g[4] = {make_float2(ga.x, ga.y), make_float2(ga.z, ga.w), make_float2(gh.x, gh.y),
+                                     make_float2(gh.z, gh.w)};
+                const float2 be[4] = {make_float2(ba.x, ba.y), make_float2(ba.z, ba.w), make_float2(bh.x, bh.y),
+                                      make_float2(bh.z, bh.w)};
+#pragma unroll
+                for (int j = 0; j < LN_RB; ++j) {
+                    if (r0 + j >= R) continue;
+                    float2 p[4];
+                    bf16x8_pairs(v[j][i].w, p);
+                    *reinterpret_cast<uint2*>(q + (r0 + j) * (int64_t)K + c * 8) =
+                        ln_cast8<FMT>(p, make_float2(-mean[j], -mean[j]), make_float2(rs[j], rs[j]), g, be, m, amax,
+                                      nsat);
+                }
+            }
+        }
+        // (part[1] of the next group is written only after every warp has
+        // passed the next group's first barrier, i.e. has read these sums)
+    }
+    if (CAST) {
+        if (sat) add_sat(sat, nsat);
+        const uint32_t b = block_max_bits<8>(__float_as_uint(amax), red);
+        if (t == 0) atomic_max_bits(&state[0], b);
+    }
+}
+
+// The statistics of rows longer than 4096 elements, in the same order as
+// k_ln_rows, streaming each row twice (through L2) instead of holding it.
+__global__ void __launch_bounds__(256) k_ln_stats_long(const uint16_t* __restrict__ x, int64_t R, int K, float eps,
+                                                       float* __restrict__ mu, float* __restrict__ rstd)
+{
+    pdl_enter();
+    __shared__ float part[2][8][LN_RB];
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int nch = K / 8;
+    const int64_t r0 = (int64_t)blockIdx.x * LN_RB;
+    float s[LN_RB];
+#pragma unroll
+    for (int j = 0; j < LN_RB; ++j) {
+        const bool live = r0 + j < R;
+        const uint16_t* row = x + (live ? r0 + j : 0) * (int64_t)K;
+        float2 acc = make_float2(0.0f, 0.0f);
+        for (int c = t; live && c < nch; c += 256) {
             Vec8<kBF16> v;
             v.load(row, c * 8);
-            float f[8];
-            v.get(f);
-            sum = __fadd_rn(sum, ln_sum8(f));
+            float2 p[4];
+            bf16x8_pairs(v.w, p);
+            acc = ln_sum8(p, acc);
         }
-        sum = warp_sum(sum);
-        if (lane == 0) part[rl][half] = sum;
-        __syncthreads();
-        mean = __fdiv_rn(__fadd_rn(part[rl][0], part[rl][1]), (float)K);
-        ss = 0.0f;
-        for (int64_t c = c0 + lane; live && c < c1; c += 32) {
+        s[j] = __fadd_rn(acc.x, acc.y);
+    }
+    const float mean_l = __fdiv_rn(cta_rows_sum(s, part[0], warp, lane), (float)K);
+#pragma unroll
+    for (int j = 0; j < LN_RB; ++j) {
+        const float mean = __shfl_sync(0xFFFFFFFFu, mean_l, j);
+        const bool live = r0 + j < R;
+        const uint16_t* row = x + (live ? r0 + j : 0) * (int64_t)K;
+        float2 acc = make_float2(0.0f, 0.0f);
+        for (int c = t; live && c < nch; c += 256) {
             Vec8<kBF16> v;
             v.load(row, c * 8);
-            float f[8];
-            v.get(f);
-            ss = __fadd_rn(ss, ln_sq8(f, mean));
+            float2 p[4];
+            bf16x8_pairs(v.w, p);
+            acc = ln_sq8(p, make_float2(-mean, -mean), acc);
         }
+        s[j] = __fadd_rn(acc.x, acc.y);
     }
-    ss = warp_sum(ss);
-    __syncthreads();                           // every warp has read its row's mean
-    if (lane == 0) part[rl][half] = ss;
-    __syncthreads();
-    if (live && half == 0 && lane == 0) {
-        mu[r] = mean;
-        const float var = __fdiv_rn(__fadd_rn(part[rl][0], part[rl][1]), (float)K);
-        rstd[r] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
+    const float var_l = __fdiv_rn(cta_rows_sum(s, part[1], warp, lane), (float)K);
+    if (warp == 0 && lane < LN_RB && r0 + lane < R) {
+        mu[r0 + lane] = mean_l;
+        rstd[r0 + lane] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var_l, eps)));
     }
+}
+
+// CTAs for a k_ln_rows launch over R rows: the groups of LN_RB rows, capped
+// at the CTAs resident at once (each CTA then walks several groups).
+template <typename Kern>
+static unsigned ln_grid(Kern kern, int64_t R, int smem, int sms)
+{
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem) != cudaSuccess || per_sm < 1) {
+        cudaGetLastError();
+        per_sm = 1;
+    }
+    const int64_t groups = (R + LN_RB - 1) / LN_RB;
+    const int64_t cap = (int64_t)sms * per_sm;
+    return (unsigned)(groups < cap ? groups : cap);
 }
 
 cudaError_t launch_layernorm_quantize(const QuantArgs& a, const float* gamma, const float* beta, float eps,
                                       float* mu, float* rstd, cudaStream_t st, int sms)
 {
-    (void)sms;
     if (a.rows == 0 || a.cols == 0) return cudaSuccess;
-    launch_k(k_ln_stats, (unsigned)((a.rows + LN_ROWS - 1) / LN_ROWS), 256, 0, st, static_cast<const uint16_t*>(a.x),
-             a.rows, a.cols, eps, mu, rstd);
+    const int K = (int)a.cols;
+    const bool in_regs = a.cols <= 256 * 8 * LN_CT;
+    if (!a.qT && !a.amax && in_regs) {
+        // one pass: statistics, normalisation and cast from registers
+        auto kern = a.format == kE4M3 ? k_ln_rows<true, kE4M3> : k_ln_rows<true, kE5M2>;
+        const int smem = ln_rows_smem<true>(K);                 // up to 64 KB
+        cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(kern), ln_rows_smem<true>(256 * 8 * LN_CT));
+        if (e != cudaSuccess) return e;
+        launch_k(kern, ln_grid(kern, a.rows, smem, sms), 256, smem, st, static_cast<const uint16_t*>(a.x), a.rows, K,
+                 eps, gamma, beta, mu, rstd, a.q, a.state, a.history_len, static_cast<float*>(a.scales), a.sat);
+        return cudaGetLastError();
+    }
+    // two passes: the statistics, then the tiled cast in its LayerNorm mode
+    // (which also writes the transposed copy)
+    if (in_regs) {
+        auto kern = k_ln_rows<false, kE4M3>;
+        const int smem = ln_rows_smem<false>(K);                // up to 32 KB
+        launch_k(kern, ln_grid(kern, a.rows, smem, sms), 256, smem, st, static_cast<const uint16_t*>(a.x), a.rows, K, eps,
+                 gamma, beta, mu, rstd, (uint8_t*)nullptr, (float*)nullptr, 0, (float*)nullptr,
+                 (unsigned long long*)nullptr);
+    } else {
+        launch_k(k_ln_stats_long, (unsigned)((a.rows + LN_RB - 1) / LN_RB), 256, 0, st,
+                 static_cast<const uint16_t*>(a.x), a.rows, K, eps, mu, rstd);
+    }
     LnParams ln;
     ln.mu = mu;
     ln.rstd = rstd;

@@ -141,3 +141,44 @@ def test_layernorm_linear_forward_and_backward():
         nz = ref_x[:H] > 0
         assert np.array_equal(gx[:H] > 0, nz)
         assert np.all(np.abs(gx[:H][nz] / ref_x[:H][nz] - 1.0) <= 1e-5), step
+
+
+@pytest.mark.parametrize("fmt", [sq.E4M3, sq.E5M2])
+@pytest.mark.parametrize("M,K,with_beta", [(272, 144, True), (4096, 4096, True), (2064, 1040, False),
+                                           (64, 4112, True)])
+def test_layernorm_single_pass_matches_two_pass(fmt, M, K, with_beta):
+    """Without a transposed copy the LayerNorm cast runs in one pass (each
+    row held in registers from the statistics to the codes, rows of up to
+    4096); with one it runs as a statistics kernel and a tiled cast.  Both
+    take the same fp32 reductions in the same order and the same per-element
+    arithmetic, so the codes, mean, rstd, the recorded amax and the reported
+    scale are bit-identical.  The shapes: an odd number of 8-element chunks
+    per row (144), the largest single-pass row (4096) over more rows than
+    one wave of CTAs holds, no beta, and a row too long for the single pass
+    (4112, both calls take the two-pass path)."""
+    x, gamma, beta = _inputs(M, K, 90 + K)
+    beta = beta if with_beta else None
+    H = 16
+    xd, gd = x.to(DEV), gamma.to(DEV)
+    bd = beta.to(DEV) if beta is not None else None
+    out = []
+    for with_qT in (False, True):
+        st = torch.tensor(o.state_init(H), device=DEV)
+        st[H] = float(np.float32(17.25))
+        st[H + 1] = float(np.float32(1.0 / 17.25))
+        q = torch.full((M, K), 0x55, dtype=torch.uint8, device=DEV)
+        qT = torch.empty((K, M), dtype=torch.uint8, device=DEV) if with_qT else None
+        mu, rstd = torch.full((M,), 7.0, device=DEV), torch.full((M,), 7.0, device=DEV)
+        sq.fp8_layernorm_quantize(xd, gd, bd, EPS, fmt, q, qT, mu, rstd, st, H)
+        torch.cuda.synchronize()
+        out.append((codes(q), mu.cpu().numpy().tobytes(), rstd.cpu().numpy().tobytes(), st.cpu().numpy().tobytes()))
+    for a, b in zip(out[0], out[1]):
+        assert np.array_equal(a, b) if isinstance(a, np.ndarray) else a == b
+    # and the single pass against the exact LayerNorm, as for the two-pass
+    # cast (on the first and last 256 rows)
+    rows = torch.cat([torch.arange(min(M, 256)), torch.arange(max(M - 256, min(M, 256)), M)])
+    beta_c = beta if beta is not None else torch.zeros(K)
+    q1 = torch.from_numpy(out[0][0])[rows]
+    mu1 = torch.from_numpy(np.frombuffer(out[0][1], dtype=np.float32).copy())[rows]
+    rs1 = torch.from_numpy(np.frombuffer(out[0][2], dtype=np.float32).copy())[rows]
+    _check_ln_codes(x[rows], gamma, beta_c, q1, mu1, rs1, np.float32(17.25), fmt)
