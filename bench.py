@@ -65,7 +65,7 @@ KERNEL_SOURCES = {   # file, [(start marker or None = file start, end marker)]: 
                                       ("            int g = delayed ? flat_grid(", "        return cudaGetLastError();")]),
 }
 TRAFFIC = {
-    "k_gemm_tensor_pair": {"sha": "327d3b6212be741d", "bytes": 978102528},
+    "k_gemm_tensor_pair": {"sha": "0c2f56cddf535029", "bytes": 673217792},
     "k_cast_tensor": {"sha": "9ca10da12c8e431d", "bytes": 143839232},
 }
 
