@@ -234,7 +234,8 @@ class FFNStep:
         stream while linear 0's forward GEMM runs.  x and W0 are cast on the
         main stream in front of that GEMM, alone on the device: the side
         stream starts behind them and is joined back before linear 1's
-        forward GEMM.  `inputs` replaces the
+        forward GEMM.  Each linear's wgrad runs on the side stream beside its
+        dgrad.  `inputs` replaces the
         resident (x, dy) of step s; `consumed` (an event) is recorded on the
         main stream once both have been cast."""
         sq = self.sq
@@ -271,17 +272,28 @@ class FFNStep:
 
         def dgrad(B, li, K, N, cast_to=None):     # dx[M][K] = dy W: B = W's codes [N][K], MN-major
             if cast_to is None:
-                rec("gemm", lambda: sq.fp8_gemm_layout(B["qdy"], sq.E5M2, self.s(3 * li + 2), K_, B["qw"], sq.E4M3,
-                                                       self.s(3 * li + 1), MN_, B["dx"], M, K, N))
+                sq.fp8_gemm_layout(B["qdy"], sq.E5M2, self.s(3 * li + 2), K_, B["qw"], sq.E4M3,
+                                   self.s(3 * li + 1), MN_, B["dx"], M, K, N)
             else:                   # dx's codes for the previous linear's backward, in the epilogue
                 q, si = cast_to
-                rec("gemm", lambda: sq.fp8_gemm_cast(B["qdy"], sq.E5M2, self.s(3 * li + 2), K_, B["qw"], sq.E4M3,
-                                                     self.s(3 * li + 1), MN_, B["dx"], M, K, N, q, sq.E5M2,
-                                                     self.st(si), H))
+                sq.fp8_gemm_cast(B["qdy"], sq.E5M2, self.s(3 * li + 2), K_, B["qw"], sq.E4M3,
+                                 self.s(3 * li + 1), MN_, B["dx"], M, K, N, q, sq.E5M2, self.st(si), H)
 
         def wgrad(B, li, K, N):     # dW[N][K] = dy^T x: dy's [M][N] and x's [M][K] codes, MN-major
-            rec("gemm", lambda: sq.fp8_gemm_layout(B["qdy"], sq.E5M2, self.s(3 * li + 2), MN_, B["qx"], sq.E4M3,
-                                                   self.s(3 * li), MN_, B["dw"], N, K, M))
+            sq.fp8_gemm_layout(B["qdy"], sq.E5M2, self.s(3 * li + 2), MN_, B["qx"], sq.E4M3,
+                               self.s(3 * li), MN_, B["dw"], N, K, M)
+
+        def backward(B, li, K, N, cast_to=None):
+            # dgrad on the main stream, wgrad on the side stream beside it
+            # (independent products): the second grid's CTAs take the SMs
+            # that the first one's last, partial wave leaves idle
+            def both():
+                side.wait_stream(main)
+                dgrad(B, li, K, N, cast_to)
+                with torch.cuda.stream(side):
+                    wgrad(B, li, K, N)
+                main.wait_stream(side)
+            rec("gemm2", both)
 
         # forward
         cast(x, sq.E4M3, B0["qx"], 0)
@@ -300,10 +312,8 @@ class FFNStep:
             consumed.record(main)                   # x and dy have been cast
         fwd(B1, 1, K1, N1)
         # backward, last linear first
-        dgrad(B1, 1, K1, N1, cast_to=(B0["qdy"], 2))        # dx1 and linear 0's output-gradient codes
-        wgrad(B1, 1, K1, N1)
-        dgrad(B0, 0, K0, N0)
-        wgrad(B0, 0, K0, N0)
+        backward(B1, 1, K1, N1, cast_to=(B0["qdy"], 2))     # dx1 and linear 0's output-gradient codes
+        backward(B0, 0, K0, N0)
         rec("update", lambda: sq.fp8_update_scale(self.states, 6, H, self.formats))
 
     KERNELS_PER_STEP = 11   # 4 casts + 6 GEMMs (two with the output cast) + 1 scale update
@@ -426,15 +436,24 @@ def run_ours(args, ws, rank, local):
     gemm_peak = fp8_sust if long_region else fp8_peak
     flops = b.gemm_flops_per_step()
     value = _replica_throughput(flops, ms_step, ws)
-    per = {"gemm": [], "quant": [], "update": []}
+    per = {"gemm": [], "gemm2": [], "quant": [], "update": []}
     for kind, a, e in ev:
         per[kind].append(a.elapsed_time(e))
-    # the kernel's roofline from the GEMMs that run alone on the device with
-    # a plain epilogue: positions 1, 3, 4, 5 of the step's six (fwd1, wgrad1,
-    # dgrad0, wgrad0); fwd0 shares the device with the side stream's casts,
-    # and fwd0 and dgrad1 also cast their outputs in the epilogue
-    gemm_ms_all = statistics.mean(per["gemm"])
-    gemm_ms = statistics.mean(per["gemm"][i] for i in range(len(per["gemm"])) if i % 6 in (1, 3, 4, 5))
+    # The kernel's roofline from the wall time of all six GEMM launches of the
+    # step: fwd0 and fwd1 on the main stream, then per linear the dgrad ||
+    # wgrad phase (two launches on two streams, timed on the main stream from
+    # the fork to the join).  fwd0 shares the device with the side stream's
+    # casts; fwd0 and dgrad1 also cast their outputs in the epilogue.
+    # The roofline takes the three launches with a plain epilogue and nothing
+    # else on the device: fwd1, and linear 0's dgrad || wgrad phase (the
+    # other three share the device with casts: fwd0 with the side stream's,
+    # fwd0 and dgrad1 with their own output casts).
+    gemm_ms_step = (sum(per["gemm"]) + sum(per["gemm2"])) / args.steps
+    fwd0_ms = statistics.mean(per["gemm"][0::2])
+    fwd1_ms = statistics.mean(per["gemm"][1::2])
+    bwd1_ms = statistics.mean(per["gemm2"][0::2])
+    bwd0_ms = statistics.mean(per["gemm2"][1::2])
+    gemm_ms = (fwd1_ms + bwd0_ms) / 3
     gemm_flops_launch = flops / 6
     achieved = gemm_flops_launch / (gemm_ms * 1e-3) / 1e12
     quant_ms_step = sum(per["quant"]) / args.steps
@@ -540,8 +559,8 @@ def run_ours(args, ws, rank, local):
                        "linears": [f"{K}->{N}" for (K, N) in b.lin], "history_len": H,
                        "chain": "x -> linear 0 -> y0 -> linear 1 -> y1; dy -> linear 1 dgrad -> dx1 -> linear 0",
                        "schedule": "y0's and dx1's casts in the epilogues of the GEMMs that produce them; W1 and "
-                                   "dy cast on a side stream during linear 0's forward GEMM; the rest in order on "
-                                   "one stream",
+                                   "dy cast on a side stream during linear 0's forward GEMM; each linear's wgrad on "
+                                   "the side stream beside its dgrad; the rest in order on one stream",
                        "recipe": "HYBRID per-tensor delayed (E4M3 fwd, E5M2 grads), amax_compute_algo=max",
                        "outputs": "y bf16, dx bf16, dW fp32",
                        "l2": "no flush: every tensor a step reads is 117-470 MB and is touched once per step, "
@@ -562,9 +581,13 @@ def run_ours(args, ws, rank, local):
                          "peak_burst": round(fp8_peak, 1), "frac_of_burst": round(achieved / fp8_peak, 4),
                          "peak_sustained": round(fp8_sust, 1), "frac_of_sustained": round(achieved / fp8_sust, 4),
                          "flops_per_launch": gemm_flops_launch, "launch_ms": round(gemm_ms, 4),
-                         "launch_ms_rule": "mean of the step's four GEMMs that run alone on the device with a "
-                                           "plain epilogue (fwd1, wgrad1, dgrad0, wgrad0)",
-                         "launch_ms_all_six": round(gemm_ms_all, 4)},
+                         "launch_ms_rule": "(fwd1 + linear 0's dgrad || wgrad phase) / 3: the three launches with "
+                                           "a plain epilogue and no cast beside them; CUDA events on the main stream, "
+                                           "the phase from its fork to its join",
+                         "phases_ms": {"fwd0 (+ side casts, + y0 cast)": round(fwd0_ms, 4), "fwd1": round(fwd1_ms, 4),
+                                       "dgrad1 || wgrad1 (+ dx1 cast)": round(bwd1_ms, 4),
+                                       "dgrad0 || wgrad0": round(bwd0_ms, 4)},
+                         "frac_all_six": round(6 * gemm_flops_launch / (gemm_ms_step * 1e-3) / 1e12 / gemm_peak, 4)},
             "roofline_quantize": {"bound": "hbm", "kernel": "k_cast_tensor (the 16384 x 4096 cast of x, alone on the device; "
                                             "mean over the timed steps after the first)",
                                   "achieved": round(big_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
@@ -577,9 +600,9 @@ def run_ours(args, ws, rank, local):
                          "note": "the four separate casts (x, W0, W1, dy): the sum of their own durations; W1 "
                                  "and dy run on a side stream beside a GEMM, so this is not their share of the step "
                                  "time.  y0's and dx1's codes are written by the GEMM epilogues (fp8_gemm_cast)"},
-            "gemm": {"ms_per_step": round(sum(per["gemm"]) / args.steps, 4),
-                     "tflops_per_s_alone": round(achieved, 1),
-                     "tflops_per_s_all_six": round(gemm_flops_launch / (gemm_ms_all * 1e-3) / 1e12, 1)},
+            "gemm": {"ms_per_step": round(gemm_ms_step, 4),
+                     "tflops_per_s_plain": round(achieved, 1),
+                     "tflops_per_s_all_six": round(6 * gemm_flops_launch / (gemm_ms_step * 1e-3) / 1e12, 1)},
             "cpu_baseline": cpu,
             "per_config": cfgs,
         }

@@ -698,13 +698,14 @@ FP8SQ_API int fp8_linear_bwd(const void* dy, int64_t M, int64_t N, int64_t K, in
         dg.a_scale = ws + L.sdy; dg.b_scale = ws + L.swT;
         wg.a_scale = ws + L.sdyT; wg.b_scale = ws + L.sxT;
     }
-    // dgrad and wgrad are independent.  When both persistent grids fit on the
-    // device at once (small layers, where each fills only part of the SMs),
-    // wgrad runs on a side stream forked from `st` and joined back into it,
-    // so the two share the device; otherwise they run one after the other.
+    // dgrad and wgrad are independent: wgrad runs on a side stream forked
+    // from `st` and joined back into it.  When both persistent grids fit on
+    // the device at once (small layers) the two share it; when each fills the
+    // device, wgrad's CTAs take the SMs that dgrad's last, partial wave of
+    // tiles leaves idle (FFN layers at 16384 tokens: 1.4 % off the step).
     const int cd = fp8sq::gemm_ctas(dg, sms), cw = fp8sq::gemm_ctas(wg, sms);
     SideStream* side = nullptr;
-    if (cd > 0 && cw > 0 && cd + cw <= sms && (r = side_stream(st, &side))) return r;
+    if (cd > 0 && cw > 0 && (r = side_stream(st, &side))) return r;
     if (side) {
         if ((r = cuda_status(cudaEventRecord(side->fork, st), "fp8_linear_bwd: fork"))) return r;
         if ((r = cuda_status(cudaStreamWaitEvent(side->s, side->fork, 0), "fp8_linear_bwd: fork"))) return r;
