@@ -578,15 +578,17 @@ __device__ __forceinline__ int64_t mx_tiled_offset(int64_t r, int64_t t, int64_t
 // codes: both operands of a fine-grained linear's products from one read of
 // x.  A row's 32 columns are four lanes of one warp; its 128 columns are four
 // warps (shuffles over l ^ 1, l ^ 2, then shared memory), and thread
-// 128 + r computes row r's 1x128 scale.  The CTA's loads are all issued at
-// its start and nothing is loaded while it reduces and casts, so the SM's
-// memory pipe needs several CTAs: 128-row tiles run four per SM (64
-// registers; at three, 80 registers, 16384 x 14336 column tiles took 131.5
-// against 117.3 us), 32-row blocks three (at four they spill and were
-// slower: 139 against 133 us; with row units too, 80 registers and a few
-// spilled bytes, 227 against 231 us at two).
+// 128 + r computes row r's 1x128 scale.  For MX-32 units the four lanes that
+// share a unit's maxima each compute two of its eight E8M0 scales and pass
+// the multipliers on by shuffles (16384 x 14336: column blocks 133 -> 117 us,
+// rows + columns 226 -> 167 us, against every lane computing all sixteen).
+// The CTA's loads are all issued at its start and nothing is loaded while it
+// reduces and casts, so the SM's memory pipe needs several CTAs: four per SM
+// (64 registers; 128-row column tiles at three, 80 registers, took 131.5
+// against 117.3 us), except MX-32 rows + columns, three (80 registers; at
+// four they spill).
 template <int FMT, int UNIT, bool ROWQ = false>
-__global__ void __launch_bounds__(256, UNIT == 32 ? 3 : 4) k_quant_col_block(const void* __restrict__ x, int64_t R, int64_t C,
+__global__ void __launch_bounds__(256, UNIT == 32 && ROWQ ? 3 : 4) k_quant_col_block(const void* __restrict__ x, int64_t R, int64_t C,
                                                          uint8_t* __restrict__ q, uint8_t* __restrict__ qT,
                                                          void* scales, void* rscales, unsigned long long* sat)
 {
@@ -646,7 +648,6 @@ __global__ void __launch_bounds__(256, UNIT == 32 ? 3 : 4) k_quant_col_block(con
         }
     }
     float m[8], rm[8];
-    uint32_t code[8], rcode[8];
     bool maysat = false;      // some column's scaled maximum may exceed fmax
     if (UNIT == 128) {
         if ((l >> 2) == 0) {
@@ -682,14 +683,48 @@ __global__ void __launch_bounds__(256, UNIT == 32 ? 3 : 4) k_quant_col_block(con
         const uint2 fl = *reinterpret_cast<const uint2*>(&colflag[cl]);   // the 8 columns' flags
         maysat = (fl.x | fl.y) != 0u;
     } else {
+        // The four lanes that share a unit's maxima split its scale work:
+        // lane g of the column group (l bits 2-3) takes columns 2g, 2g + 1,
+        // lane h of the row group (l bits 0-1) rows 2h, 2h + 1; the
+        // multipliers reach the other lanes by shuffles, and each lane stores
+        // its own two E8M0 codes at once.
+        const int g = (l >> 2) & 3, h = l & 3;
+        const uint32_t ca = g == 0 ? cm[0] : g == 1 ? cm[2] : g == 2 ? cm[4] : cm[6];
+        const uint32_t cb = g == 0 ? cm[1] : g == 1 ? cm[3] : g == 2 ? cm[5] : cm[7];
+        float ma, mb;
+        const uint32_t ka = mx_scale<FMT>(ca, ma), kb = mx_scale<FMT>(cb, mb);
+        int flag = (ca >= 0x7F800000u || __fmul_rn(__uint_as_float(ca), ma) > Fmt<FMT>::fmax ||
+                    cb >= 0x7F800000u || __fmul_rn(__uint_as_float(cb), mb) > Fmt<FMT>::fmax) ? 1 : 0;
+        flag |= __shfl_xor_sync(0xFFFFFFFFu, flag, 4);
+        flag |= __shfl_xor_sync(0xFFFFFFFFu, flag, 8);
+        maysat = flag != 0;
+        const int cbase = l & ~12;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            code[j] = mx_scale<FMT>(cm[j], m[j]);
-            maysat |= cm[j] >= 0x7F800000u || __fmul_rn(__uint_as_float(cm[j]), m[j]) > Fmt<FMT>::fmax;
+        for (int j = 0; j < 8; j += 2) {
+            m[j] = __shfl_sync(0xFFFFFFFFu, ma, cbase | ((j >> 1) << 2));
+            m[j + 1] = __shfl_sync(0xFFFFFFFFu, mb, cbase | ((j >> 1) << 2));
+        }
+        if (ok) {
+            uint8_t* e = static_cast<uint8_t*>(scales);
+            e[mx_tiled_offset(c0 + 2 * g, r0 / 32, R)] = (uint8_t)ka;
+            e[mx_tiled_offset(c0 + 2 * g + 1, r0 / 32, R)] = (uint8_t)kb;
         }
         if (ROWQ) {
+            const uint32_t ra = h == 0 ? rmax[0] : h == 1 ? rmax[2] : h == 2 ? rmax[4] : rmax[6];
+            const uint32_t rb = h == 0 ? rmax[1] : h == 1 ? rmax[3] : h == 2 ? rmax[5] : rmax[7];
+            float rma, rmb;
+            const uint32_t qa = mx_scale<FMT>(ra, rma), qb = mx_scale<FMT>(rb, rmb);
+            const int rbase = l & ~3;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) rcode[i] = mx_scale<FMT>(rmax[i], rm[i]);
+            for (int i = 0; i < 8; i += 2) {
+                rm[i] = __shfl_sync(0xFFFFFFFFu, rma, rbase | (i >> 1));
+                rm[i + 1] = __shfl_sync(0xFFFFFFFFu, rmb, rbase | (i >> 1));
+            }
+            if (ok) {
+                uint8_t* e = static_cast<uint8_t*>(rscales);
+                e[mx_tiled_offset(r0 + 2 * h, c0 / 32, C)] = (uint8_t)qa;
+                e[mx_tiled_offset(r0 + 2 * h + 1, c0 / 32, C)] = (uint8_t)qb;
+            }
         }
     }
     uint2 rows[8];
@@ -725,16 +760,6 @@ __global__ void __launch_bounds__(256, UNIT == 32 ? 3 : 4) k_quant_col_block(con
         transpose8x8(rows, cols);
 #pragma unroll
         for (int j = 0; j < 8; ++j) *reinterpret_cast<uint2*>(qT + (c0 + j) * R + r0) = cols[j];
-        if (UNIT == 32 && ((l >> 2) & 3) == 0) {     // the first row group of each 32-row block
-            uint8_t* e = static_cast<uint8_t*>(scales);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) e[mx_tiled_offset(c0 + j, r0 / 32, R)] = (uint8_t)code[j];
-        }
-        if (ROWQ && UNIT == 32 && (l & 3) == 0) {    // the first lane of each 32-column block
-            uint8_t* e = static_cast<uint8_t*>(rscales);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) e[mx_tiled_offset(r0 + i, c0 / 32, C)] = (uint8_t)rcode[i];
-        }
     } else {
         nsat = 0;
     }
