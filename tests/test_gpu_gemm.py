@@ -47,6 +47,22 @@ def test_integer_operands_exact(fa, fb):
     assert np.array_equal(D.cpu().numpy(), exact)
 
 
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 128), (4096, 5120, 128)])
+def test_multi_wave_exact(M, N, K):
+    """Several waves of 256x256 tiles on the persistent CTA pairs, with a
+    last, partial wave (4096^2: 256 tiles, 28 left after three waves of 76
+    pairs; 4096 x 5120: 320 tiles, 16 left).  Integer operands and unit
+    scales make every output exact, so a tile scheduled onto the wrong pair,
+    rows or columns shows."""
+    rng = np.random.default_rng(7)
+    va, qa = _int_codes(rng, (M, K), sq.E4M3, -8, 8)
+    vb, qb = _int_codes(rng, (N, K), sq.E4M3, -8, 8)
+    D = _gemm_t(torch.from_numpy(qa).to(DEV), sq.E4M3, _one(), torch.from_numpy(qb).to(DEV), sq.E4M3, _one(),
+                torch.float32)
+    exact = va.astype(np.float64) @ vb.astype(np.float64).T      # integers far below 2^53
+    assert np.array_equal(D.cpu().numpy().astype(np.float64), exact)
+
+
 def test_identity_b():
     rng = np.random.default_rng(2)
     M, K = 384, 256
