@@ -42,6 +42,8 @@ def state_floats(history_len: int) -> int:
 def lib() -> ctypes.CDLL:
     """Load libfp8sq.so (raises if it has not been built)."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(LIB_PATH):
@@ -79,9 +81,33 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
+_torch = None
+_raw_stream = None
+
+
 def _t():
-    import torch
-    return torch
+    global _torch
+    if _torch is None:
+        import torch
+        _torch = torch
+    return _torch
+
+
+def _current_stream() -> int:
+    """The current CUDA stream of the current device as a raw handle.  The
+    binding asks for it on every call, so it takes torch's direct accessor
+    (a fraction of a microsecond) where torch has it, else the public one."""
+    global _raw_stream
+    if _raw_stream is None:
+        torch = _t()
+        torch.cuda.init()
+        C = torch._C
+        if hasattr(C, "_cuda_getCurrentRawStream") and hasattr(C, "_cuda_getDevice"):
+            get, dev = C._cuda_getCurrentRawStream, C._cuda_getDevice
+            _raw_stream = lambda: get(dev())
+        else:
+            _raw_stream = lambda: torch.cuda.current_stream().cuda_stream
+    return _raw_stream()
 
 
 def _ptr(t):
@@ -94,8 +120,7 @@ def _ptr(t):
 
 def _stream(stream):
     if stream is None:
-        import torch
-        return torch.cuda.current_stream().cuda_stream
+        return _current_stream()
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
@@ -147,7 +172,7 @@ def _scale_bytes(gran: int, R: int, C: int) -> int:
 
 
 def _dtype_code(t) -> int:
-    import torch
+    torch = _t()
     if t.dtype == torch.bfloat16:
         return BF16
     if t.dtype == torch.float32:
