@@ -738,6 +738,17 @@ def per_config(device, with_oracle: bool = True) -> dict:
     row = gemm_row(_time_flushed(step2, flush), flops2,
                    {"what": "one training step of the three linears (fwd + dgrad + wgrad + scale update, "
                             "delayed HYBRID), eager calls"})
+    # the same step captured once and replayed from a CUDA graph: the device
+    # time without the host's per-call cost (the path does not synchronise
+    # or allocate, so it captures as is)
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2):
+        step2()
+    ms_g = _time_flushed(g2.replay, flush)
+    row["graph_ms"] = round(ms_g, 5)
+    row["graph_TFLOP/s"] = round(flops2 / (ms_g * 1e-3) / 1e12, 1)
+    row["graph_frac"] = round(flops2 / (ms_g * 1e-3) / 1e12 / fp8, 4)
+    del g2
     if o is not None:
         host = [(L["x"].float().cpu().numpy(), L["w"].float().cpu().numpy(), L["dy"].float().cpu().numpy())
                 for L in lay]
