@@ -145,7 +145,7 @@ def test_layernorm_linear_forward_and_backward():
 
 @pytest.mark.parametrize("fmt", [sq.E4M3, sq.E5M2])
 @pytest.mark.parametrize("M,K,with_beta", [(272, 144, True), (4096, 4096, True), (2064, 1040, False),
-                                           (64, 4112, True)])
+                                           (64, 4112, True), (48, 16, True), (32, 2064, False)])
 def test_layernorm_single_pass_matches_two_pass(fmt, M, K, with_beta):
     """Without a transposed copy the LayerNorm cast runs in one pass (each
     row held in registers from the statistics to the codes, rows of up to
@@ -154,8 +154,9 @@ def test_layernorm_single_pass_matches_two_pass(fmt, M, K, with_beta):
     arithmetic, so the codes, mean, rstd, the recorded amax and the reported
     scale are bit-identical.  The shapes: an odd number of 8-element chunks
     per row (144), the largest single-pass row (4096) over more rows than
-    one wave of CTAs holds, no beta, and a row too long for the single pass
-    (4112, both calls take the two-pass path)."""
+    one wave of CTAs holds, no beta, a row too long for the single pass
+    (4112, both calls take the two-pass path), a row of two chunks (16) and
+    one where a few threads hold a second chunk (2064)."""
     x, gamma, beta = _inputs(M, K, 90 + K)
     beta = beta if with_beta else None
     H = 16
@@ -182,3 +183,32 @@ def test_layernorm_single_pass_matches_two_pass(fmt, M, K, with_beta):
     mu1 = torch.from_numpy(np.frombuffer(out[0][1], dtype=np.float32).copy())[rows]
     rs1 = torch.from_numpy(np.frombuffer(out[0][2], dtype=np.float32).copy())[rows]
     _check_ln_codes(x[rows], gamma, beta_c, q1, mu1, rs1, np.float32(17.25), fmt)
+
+
+def test_layernorm_non_finite_rows_agree():
+    """A row holding an inf (its mean is inf, its variance NaN) and a row
+    holding a NaN normalise to NaN everywhere: both LayerNorm paths must give
+    the same codes, statistics and recorded amax (the NaN), bit for bit, and
+    the finite rows must be unaffected."""
+    M, K, H = 64, 768, 16
+    x, gamma, beta = _inputs(M, K, 5)
+    x[3, 17] = float("inf")
+    x[40, 5] = float("nan")
+    xd, gd, bd = x.to(DEV), gamma.to(DEV), beta.to(DEV)
+    out = []
+    for with_qT in (False, True):
+        st = torch.tensor(o.state_init(H), device=DEV)
+        q = torch.empty((M, K), dtype=torch.uint8, device=DEV)
+        qT = torch.empty((K, M), dtype=torch.uint8, device=DEV) if with_qT else None
+        mu, rstd = torch.empty(M, device=DEV), torch.empty(M, device=DEV)
+        sq.fp8_layernorm_quantize(xd, gd, bd, EPS, sq.E4M3, q, qT, mu, rstd, st, H)
+        torch.cuda.synchronize()
+        out.append((codes(q), mu.cpu().numpy().tobytes(), rstd.cpu().numpy().tobytes(), st.cpu().numpy().tobytes()))
+    for a, b in zip(out[0], out[1]):
+        assert np.array_equal(a, b) if isinstance(a, np.ndarray) else a == b
+    st = np.frombuffer(out[0][3], dtype=np.float32)
+    assert np.isnan(st[0])
+    q = out[0][0]
+    assert np.all((q[3] & 0x7F) == 0x7F) and np.all((q[40] & 0x7F) == 0x7F)     # NaN codes
+    finite = [r for r in range(M) if r not in (3, 40)]
+    assert np.all((q[finite] & 0x7F) != 0x7F)
