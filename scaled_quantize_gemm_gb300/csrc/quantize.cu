@@ -1068,19 +1068,140 @@ __global__ void __launch_bounds__(256) k_ln_stats_long(const uint16_t* __restric
     }
 }
 
-// CTAs for a k_ln_rows launch over R rows: the groups of LN_RB rows, capped
-// at the CTAs resident at once (each CTA then walks several groups).
+// Rows of up to 32 x 8 x CT elements (CT = 4: 1024, CT = 8: 2048), one warp
+// per RBW rows at a time: lane l owns the 8-element chunks l, l + 32, ... of
+// its rows, sums them in that order (pairs as above), and a warp butterfly
+// (the same sum in every lane) completes the row; no barrier and no shared
+// memory reduction.  Short rows would leave most of k_ln_rows' 256 threads
+// idle (96 chunks of a 768-wide row) and pay a CTA-wide reduction per four
+// rows.  CAST as for k_ln_rows; the statistics-only instantiation serves the
+// two-pass cast at these widths, so both paths share the reduction order.
+__device__ __forceinline__ float ln_warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+template <bool CAST, int FMT, int CT, int RBW>
+__global__ void __launch_bounds__(256, 3) k_ln_warp(const uint16_t* __restrict__ x, int64_t R, int K, float eps,
+                                                    const float* __restrict__ gamma, const float* __restrict__ beta,
+                                                    float* __restrict__ mu, float* __restrict__ rstd,
+                                                    uint8_t* __restrict__ q, float* state, int H, float* s_out,
+                                                    unsigned long long* sat)
+{
+    pdl_enter();
+    extern __shared__ __align__(16) uint8_t ln_smem[];
+    __shared__ uint32_t red[8];
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int nch = K / 8;
+    float4* gb4 = reinterpret_cast<float4*>(ln_smem);          // CAST: gamma lo, gamma hi, beta lo, beta hi [nch]
+    float m = 0.0f;
+    if (CAST) {
+        const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int c = t; c < nch; c += 256) {
+            const float4* g = reinterpret_cast<const float4*>(gamma) + 2 * c;
+            const float4* b = reinterpret_cast<const float4*>(beta) + 2 * c;
+            gb4[c] = g[0];
+            gb4[nch + c] = g[1];
+            gb4[2 * nch + c] = beta ? b[0] : z4;
+            gb4[3 * nch + c] = beta ? b[1] : z4;
+        }
+        __syncthreads();
+        m = state[H];
+        if (blockIdx.x == 0 && t == 0 && s_out) *s_out = state[H + 1];
+    }
+    float amax = 0.0f;
+    uint32_t nsat = 0;
+    const int64_t stride = (int64_t)gridDim.x * 8 * RBW;
+    for (int64_t r0 = ((int64_t)blockIdx.x * 8 + warp) * RBW; r0 < R; r0 += stride) {
+        Vec8<kBF16> v[RBW][CT];
+#pragma unroll
+        for (int j = 0; j < RBW; ++j) {
+            const bool live = r0 + j < R;
+            const uint16_t* row = x + (live ? r0 + j : 0) * (int64_t)K;
+#pragma unroll
+            for (int i = 0; i < CT; ++i) {
+                const int c = lane + 32 * i;
+                if (live && c < nch) v[j][i].load(row, c * 8); else v[j][i].zero();
+            }
+        }
+        float mean[RBW], rs[RBW];
+#pragma unroll
+        for (int j = 0; j < RBW; ++j) {
+            float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int i = 0; i < CT; ++i) {
+                if (lane + 32 * i >= nch) continue;
+                float2 p[4];
+                bf16x8_pairs(v[j][i].w, p);
+                acc = ln_sum8(p, acc);
+            }
+            mean[j] = __fdiv_rn(ln_warp_sum(__fadd_rn(acc.x, acc.y)), (float)K);
+        }
+#pragma unroll
+        for (int j = 0; j < RBW; ++j) {
+            float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int i = 0; i < CT; ++i) {
+                if (lane + 32 * i >= nch) continue;
+                float2 p[4];
+                bf16x8_pairs(v[j][i].w, p);
+                acc = ln_sq8(p, make_float2(-mean[j], -mean[j]), acc);
+            }
+            const float var = __fdiv_rn(ln_warp_sum(__fadd_rn(acc.x, acc.y)), (float)K);
+            rs[j] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
+            if (lane == 0 && r0 + j < R) {
+                mu[r0 + j] = mean[j];
+                rstd[r0 + j] = rs[j];
+            }
+        }
+        if (CAST) {
+#pragma unroll
+            for (int i = 0; i < CT; ++i) {
+                const int c = lane + 32 * i;
+                if (c >= nch) continue;
+                const float4 ga = gb4[c], gh = gb4[nch + c], ba = gb4[2 * nch + c], bh = gb4[3 * nch + c];
+                const float2 g[4] = {make_float2(ga.x, ga.y), make_float2(ga.z, ga.w), make_float2(gh.x, gh.y),
+                                     make_float2(gh.z, gh.w)};
+                const float2 be[4] = {make_float2(ba.x, ba.y), make_float2(ba.z, ba.w), make_float2(bh.x, bh.y),
+                                      make_float2(bh.z, bh.w)};
+#pragma unroll
+                for (int j = 0; j < RBW; ++j) {
+                    if (r0 + j >= R) continue;
+                    float2 p[4];
+                    bf16x8_pairs(v[j][i].w, p);
+                    *reinterpret_cast<uint2*>(q + (r0 + j) * (int64_t)K + c * 8) =
+                        ln_cast8<FMT>(p, make_float2(-mean[j], -mean[j]), make_float2(rs[j], rs[j]), g, be, m, amax,
+                                      nsat);
+                }
+            }
+        }
+    }
+    if (CAST) {
+        if (sat) add_sat(sat, nsat);
+        const uint32_t b = block_max_bits<8>(__float_as_uint(amax), red);
+        if (t == 0) atomic_max_bits(&state[0], b);
+    }
+}
+
+// One LayerNorm-kernel launch: KERN is a k_ln_warp or k_ln_rows
+// instantiation, `rows_per_cta` the rows one CTA takes per iteration;
+// CAST launches pass the codes and state.
 template <typename Kern>
-static unsigned ln_grid(Kern kern, int64_t R, int smem, int sms)
+static void launch_ln(Kern kern, int rows_per_cta, int smem, const QuantArgs& a, const float* gamma,
+                      const float* beta, float eps, float* mu, float* rstd, cudaStream_t st, int sms, bool cast)
 {
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem) != cudaSuccess || per_sm < 1) {
         cudaGetLastError();
         per_sm = 1;
     }
-    const int64_t groups = (R + LN_RB - 1) / LN_RB;
+    const int64_t groups = (a.rows + rows_per_cta - 1) / rows_per_cta;
     const int64_t cap = (int64_t)sms * per_sm;
-    return (unsigned)(groups < cap ? groups : cap);
+    const unsigned grid = (unsigned)(groups < cap ? groups : cap);
+    launch_k(kern, grid, 256, smem, st, static_cast<const uint16_t*>(a.x), a.rows, (int)a.cols, eps, gamma, beta, mu,
+             rstd, cast ? a.q : (uint8_t*)nullptr, cast ? a.state : (float*)nullptr, cast ? a.history_len : 0,
+             cast ? static_cast<float*>(a.scales) : (float*)nullptr, cast ? a.sat : (unsigned long long*)nullptr);
 }
 
 cudaError_t launch_layernorm_quantize(const QuantArgs& a, const float* gamma, const float* beta, float eps,
@@ -1088,36 +1209,51 @@ cudaError_t launch_layernorm_quantize(const QuantArgs& a, const float* gamma, co
 {
     if (a.rows == 0 || a.cols == 0) return cudaSuccess;
     const int K = (int)a.cols;
-    const bool in_regs = a.cols <= 256 * 8 * LN_CT;
-    if (!a.qT && !a.amax && in_regs) {
-        // one pass: statistics, normalisation and cast from registers
-        auto kern = a.format == kE4M3 ? k_ln_rows<true, kE4M3> : k_ln_rows<true, kE5M2>;
-        const int smem = ln_rows_smem<true>(K);                 // up to 64 KB
-        cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(kern), ln_rows_smem<true>(256 * 8 * LN_CT));
-        if (e != cudaSuccess) return e;
-        launch_k(kern, ln_grid(kern, a.rows, smem, sms), 256, smem, st, static_cast<const uint16_t*>(a.x), a.rows, K,
-                 eps, gamma, beta, mu, rstd, a.q, a.state, a.history_len, static_cast<float*>(a.scales), a.sat);
-        return cudaGetLastError();
-    }
-    // two passes: the statistics, then the tiled cast in its LayerNorm mode
-    // (which also writes the transposed copy)
-    if (in_regs) {
-        auto kern = k_ln_rows<false, kE4M3>;
-        const int smem = ln_rows_smem<false>(K);                // up to 32 KB
-        launch_k(kern, ln_grid(kern, a.rows, smem, sms), 256, smem, st, static_cast<const uint16_t*>(a.x), a.rows, K, eps,
-                 gamma, beta, mu, rstd, (uint8_t*)nullptr, (float*)nullptr, 0, (float*)nullptr,
-                 (unsigned long long*)nullptr);
+    // row width -> kernel: up to 1024 a warp per two rows, up to 2048 a warp
+    // per row, up to 4096 a CTA per four rows (all held in registers); wider
+    // rows stream their statistics and always take two passes
+    const int width = K <= 1024 ? 0 : K <= 2048 ? 1 : K <= 256 * 8 * LN_CT ? 2 : 3;
+    const bool one_pass = !a.qT && !a.amax && width < 3;
+    const bool e4 = a.format == kE4M3;
+    const int gb_smem = 2 * K * 4;                                   // gamma and beta
+    if (width == 0) {
+        if (one_pass) {
+            launch_ln(e4 ? k_ln_warp<true, kE4M3, 4, 2> : k_ln_warp<true, kE5M2, 4, 2>, 16, gb_smem, a, gamma, beta,
+                      eps, mu, rstd, st, sms, true);
+            return cudaGetLastError();
+        }
+        launch_ln(k_ln_warp<false, kE4M3, 4, 2>, 16, 0, a, gamma, beta, eps, mu, rstd, st, sms, false);
+    } else if (width == 1) {
+        if (one_pass) {
+            launch_ln(e4 ? k_ln_warp<true, kE4M3, 8, 1> : k_ln_warp<true, kE5M2, 8, 1>, 8, gb_smem, a, gamma, beta,
+                      eps, mu, rstd, st, sms, true);
+            return cudaGetLastError();
+        }
+        launch_ln(k_ln_warp<false, kE4M3, 8, 1>, 8, 0, a, gamma, beta, eps, mu, rstd, st, sms, false);
+    } else if (width == 2) {
+        if (one_pass) {
+            // one pass: statistics, normalisation and cast from registers
+            auto kern = e4 ? k_ln_rows<true, kE4M3> : k_ln_rows<true, kE5M2>;
+            cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(kern), ln_rows_smem<true>(256 * 8 * LN_CT));
+            if (e != cudaSuccess) return e;
+            launch_ln(kern, LN_RB, ln_rows_smem<true>(K), a, gamma, beta, eps, mu, rstd, st, sms, true);
+            return cudaGetLastError();
+        }
+        launch_ln(k_ln_rows<false, kE4M3>, LN_RB, ln_rows_smem<false>(K), a, gamma, beta, eps, mu, rstd, st, sms,
+                  false);
     } else {
         launch_k(k_ln_stats_long, (unsigned)((a.rows + LN_RB - 1) / LN_RB), 256, 0, st,
                  static_cast<const uint16_t*>(a.x), a.rows, K, eps, mu, rstd);
     }
+    // two passes: the statistics above, then the tiled cast in its LayerNorm
+    // mode (which also writes the transposed copy)
     LnParams ln;
     ln.mu = mu;
     ln.rstd = rstd;
     ln.gamma = gamma;
     ln.beta = beta;
     const dim3 grid((unsigned)((a.cols + 127) / 128), (unsigned)((a.rows + 127) / 128));
-    auto kern = a.format == kE4M3 ? k_cast_tensor_T<kBF16, kE4M3, true, true> : k_cast_tensor_T<kBF16, kE5M2, true, true>;
+    auto kern = e4 ? k_cast_tensor_T<kBF16, kE4M3, true, true> : k_cast_tensor_T<kBF16, kE5M2, true, true>;
     launch_k(kern, grid, 256, 0, st, a.x, a.rows, a.cols, a.q, a.qT, a.state, a.history_len, nullptr,
              static_cast<float*>(a.scales), a.amax, a.sat, ln);
     return cudaGetLastError();
