@@ -678,7 +678,6 @@ __global__ void __launch_bounds__(kPromoThreads, 1)
     pdl_enter();
     constexpr int BN = kPromoBN, STAGES = kPromoStages, NB = 2, EPI = kPromoEpi;
     constexpr int COLS = 4 * BN / EPI;       // columns per epilogue warp (128)
-    constexpr int LDF = 2;                   // 32-column copies in flight per wait
     constexpr int NLD = COLS / 32;           // 32-column copies per K block
     constexpr int CPL = COLS / 32;           // column scales per lane (SM 3)
     static_assert(SM == 1 || SM == 3, "scale layout");
@@ -817,39 +816,63 @@ __global__ void __launch_bounds__(kPromoThreads, 1)
                 tc_fence_after();
                 const uint32_t taddr =
                     tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * BN + part * COLS);
+                // Per-column scales (SM 3): the four 32-column copies are
+                // pipelined with the FMAs -- the copy of chunk g + 1 is in
+                // flight while chunk g is promoted, and the buffer is released
+                // right after the last copy lands (two 32-register copy
+                // buffers beside the 128 accumulators): 3 % faster at 8192^3
+                // and 14336 x 4096 x 16384.
+                auto promote32 = [&](float* a, const uint32_t (&r)[32], int chunk) {
+                    if constexpr (SM == 1) {
 #pragma unroll
-                for (int g = 0; g < NLD / LDF; ++g) {
-                    uint32_t r[LDF][32];
+                        for (int c = 0; c < 32; c += 2)
+                            fma2(a[c], a[c + 1], __uint_as_float(r[c]), __uint_as_float(r[c + 1]), sc, sc);
+                    } else {
+                        // ra x column scale, two columns per packed f32x2 multiply
+                        const float* s32 = cbuf + 32 * chunk;
+                        const float2 ra2 = make_float2(ra, ra);
 #pragma unroll
-                    for (int l = 0; l < LDF; ++l) tmem_ld_32x32b_x32(taddr + 32 * (g * LDF + l), r[l]);
-                    tmem_ld_wait();
-                    if (g == NLD / LDF - 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&aempty[b]);
-                    }
-#pragma unroll
-                    for (int l = 0; l < LDF; ++l) {
-                        float* a = acc + 32 * (g * LDF + l);
-                        if constexpr (SM == 1) {
-#pragma unroll
-                            for (int c = 0; c < 32; c += 2)
-                                fma2(a[c], a[c + 1], __uint_as_float(r[l][c]), __uint_as_float(r[l][c + 1]), sc, sc);
-                        } else {
-                            // ra x column scale, two columns per packed f32x2 multiply
-                            const float* s32 = cbuf + 32 * (g * LDF + l);
-                            const float2 ra2 = make_float2(ra, ra);
-#pragma unroll
-                            for (int c = 0; c < 32; c += 4) {
-                                const float4 s4 = *reinterpret_cast<const float4*>(s32 + c);
-                                const float2 s01 = __fmul2_rn(ra2, make_float2(s4.x, s4.y));
-                                const float2 s23 = __fmul2_rn(ra2, make_float2(s4.z, s4.w));
-                                fma2(a[c], a[c + 1], __uint_as_float(r[l][c]), __uint_as_float(r[l][c + 1]), s01.x,
-                                     s01.y);
-                                fma2(a[c + 2], a[c + 3], __uint_as_float(r[l][c + 2]), __uint_as_float(r[l][c + 3]),
-                                     s23.x, s23.y);
-                            }
+                        for (int c = 0; c < 32; c += 4) {
+                            const float4 s4 = *reinterpret_cast<const float4*>(s32 + c);
+                            const float2 s01 = __fmul2_rn(ra2, make_float2(s4.x, s4.y));
+                            const float2 s23 = __fmul2_rn(ra2, make_float2(s4.z, s4.w));
+                            fma2(a[c], a[c + 1], __uint_as_float(r[c]), __uint_as_float(r[c + 1]), s01.x, s01.y);
+                            fma2(a[c + 2], a[c + 3], __uint_as_float(r[c + 2]), __uint_as_float(r[c + 3]), s23.x,
+                                 s23.y);
                         }
+                    }
+                };
+                if constexpr (SM == 3) {
+                    uint32_t ra_[32], rb_[32];
+                    tmem_ld_32x32b_x32(taddr, ra_);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int g = 0; g < NLD; ++g) {
+                        if (g + 1 < NLD) tmem_ld_32x32b_x32(taddr + 32 * (g + 1), (g & 1) ? ra_ : rb_);
+                        promote32(acc + 32 * g, (g & 1) ? rb_ : ra_, g);
+                        if (g + 1 < NLD) tmem_ld_wait();
+                        if (g + 2 == NLD) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&aempty[b]);
+                        }
+                    }
+                } else {
+                    // per-row scales: two copies per wait, then their FMAs
+                    // (the pipelined order above measured 1.5 % slower here)
+#pragma unroll
+                    for (int g = 0; g < NLD / 2; ++g) {
+                        uint32_t r[2][32];
+                        tmem_ld_32x32b_x32(taddr + 64 * g, r[0]);
+                        tmem_ld_32x32b_x32(taddr + 64 * g + 32, r[1]);
+                        tmem_ld_wait();
+                        if (g == NLD / 2 - 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&aempty[b]);
+                        }
+                        promote32(acc + 64 * g, r[0], 2 * g);
+                        promote32(acc + 64 * g + 32, r[1], 2 * g + 1);
                     }
                 }
                 if constexpr (SM == 1) {
