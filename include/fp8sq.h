@@ -315,12 +315,13 @@ FP8SQ_API int fp8_gemm_cast(const uint8_t* A, int a_format, const void* a_scale,
  * Shapes: M, N, K % 128 == 0 (TENSOR: M % 16, N % 16, K % 16).
  * fp8_linear_bwd takes the forward's gran and workspace.  Under the HYBRID
  * recipe dy is cast to E5M2, under RECIPE_E4M3 to E4M3.
- * Streams: all work is ordered on `stream`.  When the dgrad and wgrad GEMMs
- *   fit on the device together (small layers), fp8_linear_bwd runs wgrad on a
+ * Streams: all work is ordered on `stream`.  fp8_linear_bwd runs wgrad on a
  *   library-owned non-blocking stream (one per host thread and device, kept
- *   for the thread's life), forked from `stream` by an event and joined back
- *   into it by another before the call returns; work queued on `stream` after
- *   the call sees both results.  Under stream capture this records two
+ *   for the thread's life) beside dgrad, forked from `stream` by an event and
+ *   joined back into it by another before the call returns; work queued on
+ *   `stream` after the call sees both results.  (Small layers' two grids
+ *   share the device; large layers' wgrad takes the SMs that dgrad's last
+ *   wave of tiles leaves idle.)  Under stream capture this records two
  *   parallel branches; the library's stream is created only outside capture
  *   (a call captured before one exists runs both GEMMs on `stream`).
  */
