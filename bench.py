@@ -65,7 +65,7 @@ KERNEL_SOURCES = {   # file, [(start marker or None = file start, end marker)]: 
                                       ("            int g = delayed ? flat_grid(", "        return cudaGetLastError();")]),
 }
 TRAFFIC = {
-    "k_gemm_tensor_pair": {"sha": "0c2f56cddf535029", "bytes": 673217792},
+    "k_gemm_tensor_pair": {"sha": "15529b129fb3a50e", "bytes": 669804544},
     "k_cast_tensor": {"sha": "9ca10da12c8e431d", "bytes": 143839232},
 }
 
@@ -951,7 +951,8 @@ def run_reference(args, ws, rank, local):
 def kernel_case(case: str, launches: int):
     """A handful of launches of one kernel at the workload's size, for
     profiling a single launch: 'gemm' = the 16384 x 14336 x 4096 forward GEMM
-    (k_gemm_tensor_pair), 'cast' = the 16384 x 14336 E5M2 delayed cast
+    (k_gemm_tensor_pair), 'gemm_cast' = the same with y's codes written by its
+    epilogue, 'cast' = the 16384 x 14336 E5M2 delayed cast
     (k_cast_tensor), 'castx' = the 16384 x 4096 E4M3 delayed cast of x (k_cast_tensor,
     the step's reported cast), 'promote' = the 4096^3 1x128 x 128x128 GEMM
     (k_gemm_promote), 'wgrad' = the 4096^3 column-tile GEMM (k_gemm_promote, per-column
@@ -977,7 +978,7 @@ def kernel_case(case: str, launches: int):
         q = torch.empty((M, K), **u8)
         for _ in range(launches):
             sq.fp8_quantize(x, sq.E4M3, sq.TENSOR, q, delayed_state=st, history_len=H)
-    elif case == "gemm":
+    elif case in ("gemm", "gemm_cast"):
         M, K, N = WK.tokens, 4096, 14336
         x = wl.linear_x(5, 0, 0, M, K, dev)
         w = wl.linear_w(5, 0, N, K, dev)
@@ -988,8 +989,16 @@ def kernel_case(case: str, launches: int):
         sq.fp8_quantize(w, sq.E4M3, sq.TENSOR, qw, delayed_state=sw, history_len=H)
         del x, w
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        for _ in range(launches):
-            sq.fp8_gemm(qx, sq.E4M3, st[H + 1:], sq.TENSOR, qw, sq.E4M3, sw[H + 1:], sq.TENSOR, y)
+        if case == "gemm":
+            for _ in range(launches):
+                sq.fp8_gemm(qx, sq.E4M3, st[H + 1:], sq.TENSOR, qw, sq.E4M3, sw[H + 1:], sq.TENSOR, y)
+        else:               # the same GEMM writing y's E4M3 codes in its epilogue
+            qy = torch.empty((M, N), **u8)
+            sy = torch.empty(H + 2, dtype=torch.float32, device=dev)
+            sq.fp8_scale_init(sy, 1, H)
+            for _ in range(launches):
+                sq.fp8_gemm_cast(qx, sq.E4M3, st[H + 1:], sq.K_MAJOR, qw, sq.E4M3, sw[H + 1:], sq.K_MAJOR, y,
+                                 M, N, K, qy, sq.E4M3, sy, H)
     elif case == "mx":
         a, b = wl.w4_operands(dev)
         qa, qb = torch.empty(a.shape, **u8), torch.empty(b.shape, **u8)
@@ -1305,7 +1314,7 @@ def modes_table(reps: int = 10):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel-case", choices=["gemm", "cast", "castx", "promote", "wgrad", "mx", "fine", "ln", "ln1"], default=None,
+    ap.add_argument("--kernel-case", choices=["gemm", "gemm_cast", "cast", "castx", "promote", "wgrad", "mx", "fine", "ln", "ln1"], default=None,
                     help="run a few launches of one kernel (for profiling) and exit")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--modes", action="store_true",

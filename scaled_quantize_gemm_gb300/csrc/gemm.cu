@@ -199,6 +199,39 @@ __device__ __forceinline__ void stage_store(uint8_t* buf, const CUtensorMap* tmD
         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
     }
 }
+// One lane's 32-byte staging row: 16 bf16 or 8 fp32 outputs.
+template <bool OUT_BF16>
+__device__ __forceinline__ void stage_row(uint8_t* rowp, const float* v)
+{
+    if (OUT_BF16) {
+#pragma unroll
+        for (int q4 = 0; q4 < 2; ++q4) {
+            uint4 w4;
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(v[8 * q4 + 0], v[8 * q4 + 1]);
+            __nv_bfloat162 h1 = __floats2bfloat162_rn(v[8 * q4 + 2], v[8 * q4 + 3]);
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(v[8 * q4 + 4], v[8 * q4 + 5]);
+            __nv_bfloat162 h3 = __floats2bfloat162_rn(v[8 * q4 + 6], v[8 * q4 + 7]);
+            w4.x = *reinterpret_cast<uint32_t*>(&h0);
+            w4.y = *reinterpret_cast<uint32_t*>(&h1);
+            w4.z = *reinterpret_cast<uint32_t*>(&h2);
+            w4.w = *reinterpret_cast<uint32_t*>(&h3);
+            *reinterpret_cast<uint4*>(rowp + 16 * q4) = w4;
+        }
+    } else {
+        *reinterpret_cast<float4*>(rowp) = make_float4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<float4*>(rowp + 16) = make_float4(v[4], v[5], v[6], v[7]);
+    }
+}
+// Bulk tensor store of a 32 x 32-byte staging buffer (one bulk group per call
+// site's commit).
+__device__ __forceinline__ void bulk_store_2d(const CUtensorMap* m, int x, int y, const uint8_t* buf)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y), "r"(smem_addr(buf))
+                 : "memory");
+}
+
 __device__ __forceinline__ void stage_store_drain(int lane)
 {
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -328,7 +361,7 @@ __device__ __forceinline__ void producer_loop(uint8_t* smem, uint64_t* full, uin
 // 8192^3; a 256 x 224 pair tile with 7 stages ran at 3362.
 constexpr int kPairBN = 256;
 constexpr int kPairStages = 6;
-using PairSmem = Smem<kPairBN / 2, kPairStages, 2, 4>;
+using PairSmem = Smem<kPairBN / 2, kPairStages, 2, 16>;  // per epilogue warp: four 1 KB staging buffers
 
 __device__ __forceinline__ bool wait_bounded_cluster(uint64_t* bar, uint32_t parity)
 {
@@ -344,7 +377,8 @@ __device__ __forceinline__ bool wait_bounded_cluster(uint64_t* bar, uint32_t par
 template <bool OUT_BF16, int LAYOUT, bool QOUT = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     k_gemm_tensor_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                       EpiParams p, uint32_t idesc, TileSched sched, const __grid_constant__ CUtensorMap tmD)
+                       EpiParams p, uint32_t idesc, TileSched sched, const __grid_constant__ CUtensorMap tmD,
+                       const __grid_constant__ CUtensorMap tmQ)
 {
     pdl_enter();
     constexpr int BN = kPairBN, BH = BN / 2, STAGES = kPairStages;
@@ -500,7 +534,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
     } else {
         const int quarter = warp & 3;       // the TMEM lane quarter this warp may read
         const float scale = __ldg(p.sA) * __ldg(p.sB);
-        uint8_t* stg = smem + L::STG_OFF + (warp - 2) * kStageBytes;
+        // four 1 KB staging buffers per warp: a chunk's 32 output columns (two
+        // bf16 or four fp32 row segments of 32 bytes) and, with QOUT, its codes
+        uint8_t* stg = smem + L::STG_OFF + (warp - 2) * 4 * kStageBytes;
+        uint8_t* qstg = stg + 2 * kStageBytes;
         constexpr int SC = OUT_BF16 ? 16 : 8;   // columns per 32-byte staged row segment
         const uint32_t aempty0 = cluster_map(smem_addr(aempty), 0);
         static_assert(!QOUT || OUT_BF16, "the output cast takes the bf16 output");
@@ -532,9 +569,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                     for (int j = 0; j < 32; ++j)
                         if (colc + j < p.N) v[j] += __ldg(p.bias + colc + j);
                 }
+                // the previous chunk's bulk stores have read their buffers
+                // (one wait per chunk: they had the whole chunk to do so)
+                if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                __syncwarp();
 #pragma unroll
-                for (int h = 0; h < 32 / SC; ++h)
-                    stage_store<OUT_BF16>(stg, &tmD, v + h * SC, colc + h * SC, row0, p.M, p.N, lane);
+                for (int h = 0; h < 32 / SC; ++h) stage_row<OUT_BF16>(stg + h * kStageBytes + 32 * lane, v + h * SC);
                 if constexpr (QOUT) {
                     // the codes of this lane's 32 outputs as rounded to bf16:
                     // q = sat_rne(fp32(bf16(v)) * m), as the cast of D would
@@ -556,18 +596,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(192, 1)
                         w[j / 4] = p.qfmt == kE4M3 ? (cvt_e4m3x2(f0, f1) | (cvt_e4m3x2(f2, f3) << 16))
                                                    : (cvt_e5m2x2(f0, f1) | (cvt_e5m2x2(f2, f3) << 16));
                     }
-                    if (row < p.M) {
-                        uint8_t* qrow = p.Q + (int64_t)row * p.N + colc;
-                        if (colc + 32 <= p.N) {
-                            *reinterpret_cast<uint4*>(qrow) = make_uint4(w[0], w[1], w[2], w[3]);
-                            *reinterpret_cast<uint4*>(qrow + 16) = make_uint4(w[4], w[5], w[6], w[7]);
-                        } else {
+                    // the warp's 32 rows x 32 codes: whole 32-byte rows
+                    *reinterpret_cast<uint4*>(qstg + 32 * lane) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4*>(qstg + 32 * lane + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                // one lane issues the chunk's bulk tensor stores (the tensor
+                // maps clip rows past M and columns past N)
+                if (lane == 0 && row0 < p.M) {
 #pragma unroll
-                            for (int g8 = 0; g8 < 4; ++g8)
-                                if (colc + 8 * g8 + 8 <= p.N)
-                                    *reinterpret_cast<uint2*>(qrow + 8 * g8) = make_uint2(w[2 * g8], w[2 * g8 + 1]);
-                        }
-                    }
+                    for (int h = 0; h < 32 / SC; ++h)
+                        if (colc + h * SC < p.N) bulk_store_2d(&tmD, colc + h * SC, row0, stg + h * kStageBytes);
+                    if (QOUT && colc < p.N) bulk_store_2d(&tmQ, colc, row0, qstg);
+                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
                 }
             }
             tc_fence_before();
@@ -1285,6 +1327,21 @@ static uint32_t make_idesc_mx(int a_fmt, int b_fmt, int n)
 
 // 2-D tensor map of the output D [M][N] for the staged epilogue stores: box
 // 32 rows x 32 bytes, no swizzle (stores clip at the matrix edge)
+// 2-D tensor map of 8-bit codes Q [M][N] for the staged code stores: box
+// 32 rows x 32 bytes, no swizzle
+static bool make_tmap_codes(CUtensorMap* m, void* Q, int64_t M, int64_t N)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)N};
+    cuuint32_t box[2] = {32u, 32u};
+    cuuint32_t estr[2] = {1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, Q, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 static bool make_tmap_out(CUtensorMap* m, void* D, int64_t M, int64_t N, bool bf16)
 {
     auto fn = encode_fn();
@@ -1416,6 +1473,11 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
             *why = "the fused output cast takes a bf16 output";
             return cudaErrorNotSupported;
         }
+        CUtensorMap tq = td;                   // unused unless the epilogue casts
+        if (g.q_out && !make_tmap_codes(&tq, g.q_out, g.M, g.N)) {
+            *why = "cuTensorMapEncodeTiled failed (codes)";
+            return cudaErrorInvalidValue;
+        }
         p.Q = g.q_out;
         p.qstate = g.q_state;
         p.qH = g.q_history_len;
@@ -1436,7 +1498,7 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
         }
         const int grid = 2 * (tiles < clusters ? tiles : clusters);
         sched.group = raster_group(g.K, 2 * BM, BN, grid / 2);
-        launch_k(kern, grid, 192, smem, st, ta, tb, p, idesc, sched, td);
+        launch_k(kern, grid, 192, smem, st, ta, tb, p, idesc, sched, td, tq);
         return cudaGetLastError();
     }
     if (g.mode == 1) return launch_promote<1>(g, p, st, sms, why);
