@@ -615,13 +615,17 @@ def run_ours(args, ws, rank, local):
 class _L2Flush:
     """Writes a buffer larger than L2 (129 MB) before each timed iteration of
     the smaller workloads, so no iteration reads what the previous one left in
-    L2."""
+    L2; then reads a second such buffer, so that the dirty lines of the write
+    are written back before the timed call instead of during it (L2 is left
+    holding clean lines that no timed call reads)."""
 
     def __init__(self, device):
         self.buf = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+        self.clean = torch.zeros(64 << 20, dtype=torch.float32, device=device)
 
     def __call__(self):
         self.buf.fill_(1)
+        self.clean.sum()
 
 
 def _time_flushed(fn, flush, iters: int = 15, warm: int = 3) -> float:
@@ -686,7 +690,7 @@ def per_config(device, with_oracle: bool = True) -> dict:
 
     out = {"peaks": {"fp8_tflops": round(fp8, 1), "hbm_gbs": hbm,
                      "source": f"burst: 2 x bf16_tflops and hbm_gbs {src}"},
-           "timing": "median of 15 single calls, L2 flushed (256 MB write) before each, CUDA events",
+           "timing": "median of 15 single calls, L2 flushed before each (a 256 MB write, then a 256 MB read so the write-backs happen before the timed call), CUDA events",
            "oracle_cores": cores}
 
     # ---- workload 1: per-tensor current scaling, 256^3, fp32 in and out
