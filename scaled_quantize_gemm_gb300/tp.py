@@ -19,6 +19,18 @@ with per-tensor delayed scaling under the HYBRID recipe:
             the unsharded layer (the amax of a sharded tensor is the max of
             its shards' amaxes).
 
+Row-parallel (RowParallelFP8Linear), the partner of a column-parallel
+layer: W [N][K] sharded along K, rank r owning columns [r K/P, (r+1) K/P),
+and the input arriving sharded the same way (the column-parallel layer's
+output columns):
+
+  forward   y = sum_r x_r W_r^T   (each rank's product in fp32, then one
+                                   all-reduce (sum) of the partial outputs)
+  backward  dx_r = dy W_r         (dy replicated; local, no exchange)
+            dW_r = dy^T x_r       (local)
+  step end  the same amax all-reduce (max) as above: x_r and W_r are shards
+            of x and W, and dy is the same on every rank.
+
 The exchange steps are torch.distributed collectives on the given process
 group; the arithmetic of each rank runs in `ops`.  The default `ops`
 (LibraryOps) is this library's CUDA path through the C ABI; a caller may
@@ -96,13 +108,18 @@ class LibraryOps:
         j = i * (self.H + 2) + self.H + 1
         return self.states[j:j + 1]
 
-    def forward(self, x: torch.Tensor, w_local: torch.Tensor) -> torch.Tensor:
+    def forward(self, x: torch.Tensor, w_local: torch.Tensor, out_dtype=torch.bfloat16) -> torch.Tensor:
         sq, H = self.sq, self.H
         sq.fp8_quantize(x, sq.E4M3, sq.TENSOR, self.qx, delayed_state=self._st(0), history_len=H)
         sq.fp8_quantize(w_local, sq.E4M3, sq.TENSOR, self.qw, delayed_state=self._st(1), history_len=H)
-        y = torch.empty((self.M, self.N), dtype=torch.bfloat16, device=x.device)
+        y = torch.empty((self.M, self.N), dtype=out_dtype, device=x.device)
         sq.fp8_gemm(self.qx, sq.E4M3, self._s(0), sq.TENSOR, self.qw, sq.E4M3, self._s(1), sq.TENSOR, y)
         return y
+
+    def forward_partial(self, x_local: torch.Tensor, w_local: torch.Tensor) -> torch.Tensor:
+        """The rank's partial output of a row-parallel linear, fp32 (summed
+        across the group afterwards)."""
+        return self.forward(x_local, w_local, out_dtype=torch.float32)
 
     def backward(self, dy_local: torch.Tensor):
         """-> (dx partial fp32 [M][K], dW_local fp32 [N/P][K])"""
@@ -165,6 +182,47 @@ class ColumnParallelFP8Linear:
         dx, dw = self.ops.backward(dy_local)
         dist.all_reduce(dx, op=dist.ReduceOp.SUM, group=self.group)
         return dx, dw
+
+    def end_step(self) -> None:
+        """All-reduce (max) the amaxes the step recorded, then update the
+        scales: every rank ends the step with the same x, W and dy states."""
+        a = self.ops.recorded_amax()
+        dist.all_reduce(a, op=dist.ReduceOp.MAX, group=self.group)
+        self.ops.set_recorded_amax(a)
+        self.ops.update_scale()
+
+
+class RowParallelFP8Linear:
+    """One row-parallel FP8 linear of a TP group (see the module text).
+
+    w_local: this rank's columns of W ([N][K/P]); the forward takes this
+    rank's columns of x ([M][K/P]).  `ops` defaults to LibraryOps on
+    w_local's device (its N is the full N, its K the local K/P)."""
+
+    def __init__(self, w_local: torch.Tensor, M: int, history_len: int = 16, group=None, ops=None,
+                 recipe_e4m3: bool = False):
+        self.group = group
+        self.world = dist.get_world_size(group)
+        self.rank = dist.get_rank(group)
+        self.w = w_local
+        self.M = M
+        self.N, self.K_local = w_local.shape
+        self.K = self.K_local * self.world
+        self.ops = ops if ops is not None else LibraryOps(M, self.N, self.K_local, history_len, w_local.device,
+                                                          recipe_e4m3)
+
+    def forward(self, x_local: torch.Tensor, async_op: bool = False):
+        """The rank's partial product, then an all-reduce (sum) of it: y
+        [M][N] fp32 on every rank.  With async_op the all-reduce is left in
+        flight and (work, y) is returned; y may be read after work.wait()."""
+        y = self.ops.forward_partial(x_local, self.w)
+        work = dist.all_reduce(y, op=dist.ReduceOp.SUM, group=self.group, async_op=async_op)
+        return (work, y) if async_op else y
+
+    def backward(self, dy: torch.Tensor):
+        """dy: the full output gradient [M][N] (the same on every rank).
+        Returns (dx_local fp32 [M][K/P], dW_local fp32 [N][K/P]); no exchange."""
+        return self.ops.backward(dy)
 
     def end_step(self) -> None:
         """All-reduce (max) the amaxes the step recorded, then update the

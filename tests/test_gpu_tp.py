@@ -57,3 +57,40 @@ def test_column_parallel_linear_one_rank_matches_oracle():
         assert sq.fp8_device_status(True) == 0
     finally:
         dist.destroy_process_group()
+
+
+def test_row_parallel_linear_one_rank_matches_oracle():
+    """The row-parallel linear's per-rank path (fp32 partial output through
+    the library's GEMM, then the all-reduce) in a group of one rank on NCCL:
+    the output, the input gradient and the weight gradient against the
+    oracle, histories bit-exact every step."""
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1,
+                            timeout=datetime.timedelta(seconds=120), device_id=torch.device(DEV, 0))
+    try:
+        M, K, N, H = 256, 512, 384, 16
+        w = wl.normal((N, K), 0.02, 91).to(DEV)
+        layer = tp.RowParallelFP8Linear(tp.shard_cols(w, 0, 1), M, history_len=H)
+        ref = [o.state_init(H) for _ in range(3)]
+        for step in range(4):
+            x = wl.normal((M, K), 1.0 + step, 92 + step).to(DEV)
+            dy = wl.normal((M, N), 1e-3 * (30.0 if step == 1 else 1.0), 96 + step).to(DEV)
+            work, y = layer.forward(tp.shard_cols(x, 0, 1), async_op=True)
+            work.wait()
+            dx, dw = layer.backward(dy)
+            layer.end_step()
+            torch.cuda.synchronize()
+            assert y.dtype == torch.float32
+            qx, sx, qw, sw, Y = o.linear_fwd_delayed(np32(x), np32(w), ref[0], ref[1])
+            _, _, dX, dW = o.linear_bwd_delayed(np32(dy), ref[2], o.E5M2, qx, sx, qw, sw)
+            for r, f in zip(ref, (o.E4M3, o.E4M3, o.E5M2)):
+                o.update_scale(r, f)
+            assert_gemm_close(y, Y)
+            assert_gemm_close(dx, dX)
+            assert_gemm_close(dw, dW)
+            assert layer.ops.states.cpu().numpy().tobytes() == np.concatenate(ref).tobytes(), step
+        assert sq.fp8_device_status(True) == 0
+    finally:
+        dist.destroy_process_group()

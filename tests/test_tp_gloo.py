@@ -44,6 +44,9 @@ class OracleOps:
         self.wh = o.dequantize(qw, o.E4M3, o.GRAN_TENSOR, sw)
         return torch.from_numpy(o.gemm_ref(self.xh, self.wh))
 
+    def forward_partial(self, x, w):
+        return self.forward(x, w)
+
     def backward(self, dy):
         o, H = self.o, self.H
         sd = np.float32(self.st[2][H + 1])
@@ -187,3 +190,107 @@ def test_shard_helpers():
     assert torch.equal(torch.cat([tp.shard_cols(t, r, 2) for r in range(2)], dim=1), t)
     parts = torch.stack([tp.shard_cols(t, r, 3) for r in range(3)])
     assert torch.equal(tp.GatherHandle(None, parts, 4, 6).wait(), t)
+
+
+# ---------------------------------------------------------------- row-parallel
+def _row_inputs(step):
+    g = torch.Generator().manual_seed(50 + step)
+    x = (torch.randn((M, N), generator=g) * (1.0 + step)).to(torch.bfloat16).float()   # the layer's K = N here
+    x[5, N - 3] = 40.0 * (1.0 + step)                 # the second rank's shard of x holds the largest entry
+    dy = (torch.randn((M, K), generator=g) * 1e-3).to(torch.bfloat16).float()
+    return x, dy
+
+
+def _row_weights():
+    g = torch.Generator().manual_seed(4)
+    w = (torch.randn((K, N), generator=g) * 0.02)
+    w[3, 2] = 0.7                                     # the first rank's shard of W holds the largest entry
+    return w.to(torch.bfloat16).float()
+
+
+def _row_worker(rank, ws, port, sync, out):
+    try:
+        os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        sys.path.insert(0, ROOT)
+        from scaled_quantize_gemm_gb300 import tp
+        dist.init_process_group("gloo", rank=rank, world_size=ws, timeout=__import__("datetime").timedelta(seconds=60))
+        try:
+            w = _row_weights()
+            ops = OracleOps(H)
+            layer = tp.RowParallelFP8Linear(tp.shard_cols(w, rank, ws), M, history_len=H, ops=ops)
+            rec = []
+            for step in range(STEPS):
+                x, dy = _row_inputs(step)
+                work, y = layer.forward(tp.shard_cols(x, rank, ws), async_op=True)
+                work.wait()
+                dx, dw = layer.backward(dy)
+                if sync:
+                    layer.end_step()
+                else:
+                    ops.update_scale()
+                rec.append((y.numpy().copy(), dx.numpy(), dw.numpy(), ops.state_bytes()))
+            out.put((rank, rec))
+        finally:
+            dist.destroy_process_group()
+    except BaseException as e:
+        import traceback
+        out.put((rank, "error: " + "".join(traceback.format_exception(e))))
+        raise
+
+
+def _row_run(sync):
+    ctx = mp.get_context("spawn")
+    out = ctx.Queue()
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    procs = [ctx.Process(target=_row_worker, args=(r, 2, port, sync, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = {}
+    for _ in range(2):
+        rank, rec = out.get(timeout=180)
+        assert not isinstance(rec, str), rec
+        res[rank] = rec
+    for p in procs:
+        p.join(60)
+    assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+    return res
+
+
+def _row_unsharded():
+    w = _row_weights()
+    ops = OracleOps(H)
+    rec = []
+    for step in range(STEPS):
+        x, dy = _row_inputs(step)
+        y = ops.forward(x, w)
+        dx, dw = ops.backward(dy)
+        ops.update_scale()
+        rec.append((y.numpy(), dx.numpy(), dw.numpy(), ops.state_bytes()))
+    return rec
+
+
+def test_row_parallel_matches_unsharded_layer():
+    """Row-parallel (W [K_out][N] sharded along its input dimension, x
+    sharded the same way): the all-reduced output, each rank's input- and
+    weight-gradient columns, and the delayed-scaling states (bit-identical
+    to the unsharded layer's, through the amax all-reduce)."""
+    res = _row_run(sync=True)
+    ref = _row_unsharded()
+    half = N // 2
+    for step in range(STEPS):
+        y_r, dx_r, dw_r, st_r = ref[step]
+        for rank in range(2):
+            y, dx, dw, st = res[rank][step]
+            assert st == st_r, (step, rank)
+            assert _close(y, y_r), (step, rank)
+            assert _close(dx, dx_r[:, rank * half:(rank + 1) * half]), (step, rank)
+            assert _close(dw, dw_r[:, rank * half:(rank + 1) * half]), (step, rank)
+
+
+def test_row_parallel_without_amax_allreduce_diverges():
+    res = _row_run(sync=False)
+    ref = _row_unsharded()
+    assert res[0][0][3] != res[1][0][3]
+    assert res[0][0][3] != ref[0][3] or res[1][0][3] != ref[0][3]
