@@ -31,6 +31,14 @@ output columns):
   step end  the same amax all-reduce (max) as above: x_r and W_r are shards
             of x and W, and dy is the same on every rank.
 
+Data-parallel (DataParallelFP8Linear): W replicated, the batch sharded along
+M (rank r owns rows [r M/P, (r+1) M/P) of x and dy):
+
+  forward   y_r = x_r W^T         (local)
+  backward  dx_r = dy_r W         (local)
+            dW = sum_r dy_r^T x_r (the local products all-reduced, sum)
+  step end  the amax all-reduce (max): x and dy are sharded, W identical.
+
 The exchange steps are torch.distributed collectives on the given process
 group; the arithmetic of each rank runs in `ops`.  The default `ops`
 (LibraryOps) is this library's CUDA path through the C ABI; a caller may
@@ -223,6 +231,42 @@ class RowParallelFP8Linear:
         """dy: the full output gradient [M][N] (the same on every rank).
         Returns (dx_local fp32 [M][K/P], dW_local fp32 [N][K/P]); no exchange."""
         return self.ops.backward(dy)
+
+    def end_step(self) -> None:
+        """All-reduce (max) the amaxes the step recorded, then update the
+        scales: every rank ends the step with the same x, W and dy states."""
+        a = self.ops.recorded_amax()
+        dist.all_reduce(a, op=dist.ReduceOp.MAX, group=self.group)
+        self.ops.set_recorded_amax(a)
+        self.ops.update_scale()
+
+
+class DataParallelFP8Linear:
+    """One data-parallel FP8 linear (see the module text): every rank holds
+    all of W [N][K] and its own M_local rows of the batch.  `ops` defaults to
+    LibraryOps on w's device (its M is the local batch)."""
+
+    def __init__(self, w: torch.Tensor, M_local: int, history_len: int = 16, group=None, ops=None,
+                 recipe_e4m3: bool = False):
+        self.group = group
+        self.world = dist.get_world_size(group)
+        self.rank = dist.get_rank(group)
+        self.w = w
+        self.N, self.K = w.shape
+        self.ops = ops if ops is not None else LibraryOps(M_local, self.N, self.K, history_len, w.device,
+                                                          recipe_e4m3)
+
+    def forward(self, x_local: torch.Tensor) -> torch.Tensor:
+        """y_local [M_local][N] (bf16 on the library path); no exchange."""
+        return self.ops.forward(x_local, self.w)
+
+    def backward(self, dy_local: torch.Tensor, async_op: bool = False):
+        """dx_local [M_local][K] (local) and dW [N][K] fp32 summed over the
+        group.  With async_op the all-reduce of dW is left in flight and
+        (dx_local, dW, work) is returned; dW may be read after work.wait()."""
+        dx, dw = self.ops.backward(dy_local)
+        work = dist.all_reduce(dw, op=dist.ReduceOp.SUM, group=self.group, async_op=async_op)
+        return (dx, dw, work) if async_op else (dx, dw)
 
     def end_step(self) -> None:
         """All-reduce (max) the amaxes the step recorded, then update the

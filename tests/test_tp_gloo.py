@@ -294,3 +294,95 @@ def test_row_parallel_without_amax_allreduce_diverges():
     ref = _row_unsharded()
     assert res[0][0][3] != res[1][0][3]
     assert res[0][0][3] != ref[0][3] or res[1][0][3] != ref[0][3]
+
+
+# ---------------------------------------------------------------- data-parallel
+def _dp_worker(rank, ws, port, sync, out):
+    try:
+        os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        sys.path.insert(0, ROOT)
+        from scaled_quantize_gemm_gb300 import tp
+        dist.init_process_group("gloo", rank=rank, world_size=ws, timeout=__import__("datetime").timedelta(seconds=60))
+        try:
+            w = _weights()
+            ops = OracleOps(H)
+            layer = tp.DataParallelFP8Linear(w, M // ws, history_len=H, ops=ops)
+            rows = slice(rank * (M // ws), (rank + 1) * (M // ws))
+            rec = []
+            for step in range(STEPS):
+                x, dy = _inputs(step)
+                if step == 1:
+                    x[M - 2, 9] = 300.0                   # only the second rank's rows hold this spike
+                y = layer.forward(x[rows].contiguous())
+                dx, dw, work = layer.backward(dy[rows].contiguous(), async_op=True)
+                work.wait()
+                if sync:
+                    layer.end_step()
+                else:
+                    ops.update_scale()
+                rec.append((y.numpy(), dx.numpy(), dw.numpy().copy(), ops.state_bytes()))
+            out.put((rank, rec))
+        finally:
+            dist.destroy_process_group()
+    except BaseException as e:
+        import traceback
+        out.put((rank, "error: " + "".join(traceback.format_exception(e))))
+        raise
+
+
+def _dp_run(sync):
+    ctx = mp.get_context("spawn")
+    out = ctx.Queue()
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    procs = [ctx.Process(target=_dp_worker, args=(r, 2, port, sync, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = {}
+    for _ in range(2):
+        rank, rec = out.get(timeout=180)
+        assert not isinstance(rec, str), rec
+        res[rank] = rec
+    for p in procs:
+        p.join(60)
+    assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+    return res
+
+
+def _dp_unsharded():
+    w = _weights()
+    ops = OracleOps(H)
+    rec = []
+    for step in range(STEPS):
+        x, dy = _inputs(step)
+        if step == 1:
+            x[M - 2, 9] = 300.0
+        y = ops.forward(x, w)
+        dx, dw = ops.backward(dy)
+        ops.update_scale()
+        rec.append((y.numpy(), dx.numpy(), dw.numpy(), ops.state_bytes()))
+    return rec
+
+
+def test_data_parallel_matches_unsharded_layer():
+    """Data-parallel (W replicated, batch rows sharded): each rank's output
+    and input-gradient rows, the all-reduced weight gradient, and the
+    states bit-identical to the full-batch layer's through the amax
+    all-reduce (a spike in the second rank's rows moves the x history)."""
+    res = _dp_run(sync=True)
+    ref = _dp_unsharded()
+    half = M // 2
+    for step in range(STEPS):
+        y_r, dx_r, dw_r, st_r = ref[step]
+        for rank in range(2):
+            y, dx, dw, st = res[rank][step]
+            assert st == st_r, (step, rank)
+            assert _close(y, y_r[rank * half:(rank + 1) * half]), (step, rank)
+            assert _close(dx, dx_r[rank * half:(rank + 1) * half]), (step, rank)
+            assert _close(dw, dw_r), (step, rank)
+
+
+def test_data_parallel_without_amax_allreduce_diverges():
+    res = _dp_run(sync=False)
+    assert res[0][1][3] != res[1][1][3]
