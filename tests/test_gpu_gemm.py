@@ -315,7 +315,8 @@ def test_mx_power_of_two_scales_select_the_right_block():
     assert np.array_equal(D.cpu().numpy().astype(np.float64), ah @ bh.T)
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 384, 512), (384, 256, 1024), (256, 384, 1536)])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (256, 384, 512), (384, 256, 1024), (256, 384, 1536),
+                                   (640, 256, 1536), (384, 640, 1152)])
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
 def test_mx_vs_oracle(M, N, K, out):
     from _helpers import mx_untile
