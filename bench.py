@@ -1034,9 +1034,9 @@ def kernel_case(case: str, launches: int):
             sq.fp8_quantize(dy, sq.E5M2, sq.TILE_128x1, None, qT=qdT, scales_out=sd)
     elif case in ("ln", "ln1"):
         # LayerNorm fused into the delayed E4M3 cast, 16384 x 4096: "ln" with
-        # the transposed copy (k_ln_rows for the statistics, then
+        # the transposed copy (k_ln_warp for the statistics, then
         # k_cast_tensor_T in its LayerNorm mode), "ln1" without it
-        # (k_ln_rows, one pass)
+        # (k_ln_warp, one pass)
         M, K = 16384, 4096
         xl = wl.normal((M, K), 2.0, 11, dev)
         gamma = torch.rand(K, generator=torch.Generator().manual_seed(12)).add_(0.5).to(dev)
@@ -1282,7 +1282,7 @@ def modes_table(reps: int = 10):
     row("fp8_layernorm_quantize E4M3 delayed, with qT (6 B moved / element)", f"{M}x{K}",
         med(lambda: sq.fp8_layernorm_quantize(xl, gamma, beta, 1e-5, sq.E4M3, ql, qlT, mu, rs, stl, H)),
         nbytes=6 * M * K)
-    # without the transposed copy: one pass (k_ln_rows), x read once and the
+    # without the transposed copy: one pass (k_ln_warp), x read once and the
     # codes written = 3 bytes moved per element
     row("fp8_layernorm_quantize E4M3 delayed, no qT (one pass, 3 B moved / element)", f"{M}x{K}",
         med(lambda: sq.fp8_layernorm_quantize(xl, gamma, beta, 1e-5, sq.E4M3, ql, None, mu, rs, stl, H)),

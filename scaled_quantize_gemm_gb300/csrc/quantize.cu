@@ -767,16 +767,17 @@ __global__ void __launch_bounds__(256, UNIT == 32 && ROWQ ? 3 : 4) k_quant_col_b
 }
 
 // LayerNorm statistics: mean = sum(x) / K and var = sum((x - mean)^2) / K in
-// fp32, rstd = 1 / sqrt(var + eps) with IEEE division and square root.  One
-// reduction order serves every LayerNorm kernel, so the statistics (and hence
-// the codes) do not depend on which kernel produced them: a 256-thread CTA
-// takes LN_RB rows at a time, thread t owns the 8-element chunks t, t + 256,
-// ... of every row and sums them in that order (each chunk as a tree of
-// (even, odd) element pairs; the pair's two partials added last), then the
-// warp reduction of warp_sum4, then the eight warps' partials in a fixed
-// tree; one lane per row divides, and broadcasts the result.
-constexpr int LN_RB = 4;         // rows per CTA iteration
-constexpr int LN_CT = 2;         // chunks per thread held in registers: K <= 256 x 8 x LN_CT
+// fp32, rstd = 1 / sqrt(var + eps) with IEEE division and square root.  The
+// reduction order is a function of the row width alone, so the statistics
+// (and hence the codes) do not depend on whether the one-pass or the
+// two-pass path produced them.  Rows of up to 4096 elements: one warp per
+// row (k_ln_warp).  Longer rows (two passes only): a 256-thread CTA takes
+// LN_RB rows at a time, thread t owns the 8-element chunks t, t + 256, ...
+// of every row and sums them in that order (each chunk as a tree of (even,
+// odd) element pairs; the pair's two partials added last), then the warp
+// reduction of warp_sum4, then the eight warps' partials in a fixed tree;
+// one lane per row divides, and broadcasts the result.
+constexpr int LN_RB = 4;         // rows per CTA iteration of the long-row kernel
 
 // The arithmetic below works on (even, odd) element pairs with the packed
 // fp32x2 instructions; each lane of a pair is an IEEE round-to-nearest fp32
@@ -870,158 +871,8 @@ __device__ __forceinline__ float cta_rows_sum(const float (&s)[LN_RB], float (*p
     return ln_tree8(p, lane & (LN_RB - 1));
 }
 
-// Rows of up to 4096 elements, held in registers from the statistics to the
-// codes (CAST = true: LayerNorm fused into the delayed per-tensor cast, x
-// read once, 3 B moved per element; CAST = false: the statistics alone, for
-// the two-pass cast with a transposed copy).  The CTAs (as many as fit at
-// once) walk groups of LN_RB rows.  Each thread copies its own chunks of the
-// next group into a shared-memory stage (cp.async) as soon as its sums have
-// consumed the current group's, so the next group's loads are in flight
-// while the current one is reduced, normalised and cast; no barrier guards
-// the stage, as a thread reads back only what it copied.  gamma and beta are
-// staged once per CTA as four arrays of 16-byte halves, so that the warp's
-// reads of a chunk's gamma / beta halves are consecutive 16-byte words (no
-// bank conflicts); a thread applies them to the LN_RB rows of a group.
-template <bool CAST>
-__host__ __device__ constexpr int ln_rows_smem(int K)
-{
-    return (CAST ? 2 * K * 4 : 0) + LN_RB * K * 2;    // gamma and beta (fp32), then the row stage (bf16)
-}
-
-template <bool CAST, int FMT>
-__global__ void __launch_bounds__(256, 3) k_ln_rows(const uint16_t* __restrict__ x, int64_t R, int K, float eps,
-                                                    const float* __restrict__ gamma, const float* __restrict__ beta,
-                                                    float* __restrict__ mu, float* __restrict__ rstd,
-                                                    uint8_t* __restrict__ q, float* state, int H, float* s_out,
-                                                    unsigned long long* sat)
-{
-    pdl_enter();
-    extern __shared__ __align__(16) uint8_t ln_smem[];
-    __shared__ float part[2][8][LN_RB];        // sums, then squared deviations
-    __shared__ uint32_t red[8];
-    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const int nch = K / 8;
-    float4* gb4 = reinterpret_cast<float4*>(ln_smem);          // CAST: gamma lo, gamma hi, beta lo, beta hi [nch]
-    uint4* xs = reinterpret_cast<uint4*>(ln_smem + (CAST ? 2 * K * 4 : 0));   // [LN_RB][nch] chunks
-    const int64_t stride = (int64_t)gridDim.x * LN_RB;
-    auto stage = [&](int64_t r0) {
-#pragma unroll
-        for (int j = 0; j < LN_RB; ++j) {
-            if (r0 + j >= R) continue;
-            const uint16_t* row = x + (r0 + j) * (int64_t)K;
-#pragma unroll
-            for (int i = 0; i < LN_CT; ++i) {
-                const int c = t + 256 * i;
-                if (c < nch) cp_async16(&xs[j * nch + c], row + c * 8);
-            }
-        }
-        cp_async_commit();
-    };
-    stage((int64_t)blockIdx.x * LN_RB);
-    float m = 0.0f;
-    if (CAST) {
-        const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        for (int c = t; c < nch; c += 256) {
-            const float4* g = reinterpret_cast<const float4*>(gamma) + 2 * c;
-            const float4* b = reinterpret_cast<const float4*>(beta) + 2 * c;
-            gb4[c] = g[0];
-            gb4[nch + c] = g[1];
-            gb4[2 * nch + c] = beta ? b[0] : z4;
-            gb4[3 * nch + c] = beta ? b[1] : z4;
-        }
-        __syncthreads();
-        m = state[H];
-        if (blockIdx.x == 0 && t == 0 && s_out) *s_out = state[H + 1];
-    }
-    float amax = 0.0f;
-    uint32_t nsat = 0;
-    for (int64_t r0 = (int64_t)blockIdx.x * LN_RB; r0 < R; r0 += stride) {
-        cp_async_wait_all();
-        Vec8<kBF16> v[LN_RB][LN_CT];
-#pragma unroll
-        for (int j = 0; j < LN_RB; ++j) {
-#pragma unroll
-            for (int i = 0; i < LN_CT; ++i) {
-                const int c = t + 256 * i;
-                if (r0 + j < R && c < nch) v[j][i].w = xs[j * nch + c]; else v[j][i].zero();
-            }
-        }
-        float s[LN_RB];
-#pragma unroll
-        for (int j = 0; j < LN_RB; ++j) {
-            float2 acc = make_float2(0.0f, 0.0f);
-#pragma unroll
-            for (int i = 0; i < LN_CT; ++i) {
-                if (t + 256 * i >= nch) continue;
-                float2 p[4];
-                bf16x8_pairs(v[j][i].w, p);
-                acc = ln_sum8(p, acc);
-            }
-            s[j] = __fadd_rn(acc.x, acc.y);
-        }
-        // the sums have consumed this group's chunks: start the next group's
-        stage(r0 + stride);
-        // lane l: the mean of row l % LN_RB, then every row's by broadcast
-        const float mean_l = __fdiv_rn(cta_rows_sum(s, part[0], warp, lane), (float)K);
-        float mean[LN_RB];
-#pragma unroll
-        for (int j = 0; j < LN_RB; ++j) mean[j] = __shfl_sync(0xFFFFFFFFu, mean_l, j);
-#pragma unroll
-        for (int j = 0; j < LN_RB; ++j) {
-            float2 acc = make_float2(0.0f, 0.0f);
-#pragma unroll
-            for (int i = 0; i < LN_CT; ++i) {
-                if (t + 256 * i >= nch) continue;
-                float2 p[4];
-                bf16x8_pairs(v[j][i].w, p);
-                acc = ln_sq8(p, make_float2(-mean[j], -mean[j]), acc);
-            }
-            s[j] = __fadd_rn(acc.x, acc.y);
-        }
-        // (part[0] of the next group is written only after every warp has
-        // passed the barrier in this call, i.e. has read this group's sums)
-        const float var_l = __fdiv_rn(cta_rows_sum(s, part[1], warp, lane), (float)K);
-        const float rs_l = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var_l, eps)));
-        if (warp == 0 && lane < LN_RB && r0 + lane < R) {
-            mu[r0 + lane] = mean_l;
-            rstd[r0 + lane] = rs_l;
-        }
-        float rs[LN_RB];
-#pragma unroll
-        for (int j = 0; j < LN_RB; ++j) rs[j] = __shfl_sync(0xFFFFFFFFu, rs_l, j);
-        if (CAST) {
-#pragma unroll
-            for (int i = 0; i < LN_CT; ++i) {
-                const int c = t + 256 * i;
-                if (c >= nch) continue;
-                const float4 ga = gb4[c], gh = gb4[nch + c], ba = gb4[2 * nch + c], bh = gb4[3 * nch + c];
-                const float2 g[4] = {make_float2(ga.x, ga.y), make_float2(ga.z, ga.w), make_float2(gh.x, gh.y),
-                                     make_float2(gh.z, gh.w)};
-                const float2 be[4] = {make_float2(ba.x, ba.y), make_float2(ba.z, ba.w), make_float2(bh.x, bh.y),
-                                      make_float2(bh.z, bh.w)};
-#pragma unroll
-                for (int j = 0; j < LN_RB; ++j) {
-                    if (r0 + j >= R) continue;
-                    float2 p[4];
-                    bf16x8_pairs(v[j][i].w, p);
-                    *reinterpret_cast<uint2*>(q + (r0 + j) * (int64_t)K + c * 8) =
-                        ln_cast8<FMT>(p, make_float2(-mean[j], -mean[j]), make_float2(rs[j], rs[j]), g, be, m, amax,
-                                      nsat);
-                }
-            }
-        }
-        // (part[1] of the next group is written only after every warp has
-        // passed the next group's first barrier, i.e. has read these sums)
-    }
-    if (CAST) {
-        if (sat) add_sat(sat, nsat);
-        const uint32_t b = block_max_bits<8>(__float_as_uint(amax), red);
-        if (t == 0) atomic_max_bits(&state[0], b);
-    }
-}
-
-// The statistics of rows longer than 4096 elements, in the same order as
-// k_ln_rows, streaming each row twice (through L2) instead of holding it.
+// The statistics of rows longer than 4096 elements (the CTA-wide order
+// above), streaming each row twice (through L2) instead of holding it.
 __global__ void __launch_bounds__(256) k_ln_stats_long(const uint16_t* __restrict__ x, int64_t R, int K, float eps,
                                                        float* __restrict__ mu, float* __restrict__ rstd)
 {
@@ -1068,22 +919,33 @@ __global__ void __launch_bounds__(256) k_ln_stats_long(const uint16_t* __restric
     }
 }
 
-// Rows of up to 32 x 8 x CT elements (CT = 4: 1024, CT = 8: 2048), one warp
-// per RBW rows at a time: lane l owns the 8-element chunks l, l + 32, ... of
-// its rows, sums them in that order (pairs as above), and a warp butterfly
-// (the same sum in every lane) completes the row; no barrier and no shared
-// memory reduction.  Short rows would leave most of k_ln_rows' 256 threads
-// idle (96 chunks of a 768-wide row) and pay a CTA-wide reduction per four
-// rows.  CAST as for k_ln_rows; the statistics-only instantiation serves the
-// two-pass cast at these widths, so both paths share the reduction order.
+// Rows of up to 32 x 8 x CT elements (CT = 4: 1024, CT = 8: 2048, CT = 16:
+// 4096), one warp per RBW rows at a time: lane l owns the 8-element chunks
+// l, l + 32, ... of its rows, sums them in that order (pairs as above), and
+// a warp butterfly (the same sum in every lane) completes the row; no
+// barrier and no shared memory reduction.  Each lane copies its chunks of the
+// warp's next rows into the warp's shared-memory stage (cp.async) once its
+// sums have consumed the current ones, so the next rows' loads are in flight
+// while the current rows are reduced, normalised and cast (no barrier guards
+// the stage: a lane reads back only what it copied).  CAST = true: the
+// LayerNorm fused into the delayed per-tensor cast, x read once, 3 B moved
+// per element (gamma and beta staged once per CTA as four arrays of 16-byte
+// halves, so a warp's reads of a chunk's halves are consecutive 16-byte
+// words); CAST = false: the statistics alone, which serve the two-pass cast
+// at these widths, so both paths share the reduction order.
 __device__ __forceinline__ float ln_warp_sum(float v)
 {
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
     return v;
 }
+template <bool CAST, int CT, int RBW>
+__host__ __device__ constexpr int ln_warp_smem(int K)
+{
+    return (CAST ? 2 * K * 4 : 0) + 8 * RBW * CT * 32 * 16;   // gamma and beta (fp32), then eight warps' stages
+}
 template <bool CAST, int FMT, int CT, int RBW>
-__global__ void __launch_bounds__(256, 3) k_ln_warp(const uint16_t* __restrict__ x, int64_t R, int K, float eps,
+__global__ void __launch_bounds__(256, CT >= 16 ? 2 : 3) k_ln_warp(const uint16_t* __restrict__ x, int64_t R, int K, float eps,
                                                     const float* __restrict__ gamma, const float* __restrict__ beta,
                                                     float* __restrict__ mu, float* __restrict__ rstd,
                                                     uint8_t* __restrict__ q, float* state, int H, float* s_out,
@@ -1095,6 +957,23 @@ __global__ void __launch_bounds__(256, 3) k_ln_warp(const uint16_t* __restrict__
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int nch = K / 8;
     float4* gb4 = reinterpret_cast<float4*>(ln_smem);          // CAST: gamma lo, gamma hi, beta lo, beta hi [nch]
+    // this warp's stage: [RBW rows][CT chunks][32 lanes] of 16 bytes
+    uint4* xs = reinterpret_cast<uint4*>(ln_smem + (CAST ? 2 * K * 4 : 0)) + warp * (RBW * CT * 32);
+    const int64_t stride = (int64_t)gridDim.x * 8 * RBW;
+    auto stage = [&](int64_t r0) {
+#pragma unroll
+        for (int j = 0; j < RBW; ++j) {
+            if (r0 + j >= R) continue;
+            const uint16_t* row = x + (r0 + j) * (int64_t)K;
+#pragma unroll
+            for (int i = 0; i < CT; ++i) {
+                const int c = lane + 32 * i;
+                if (c < nch) cp_async16(&xs[(j * CT + i) * 32 + lane], row + c * 8);
+            }
+        }
+        cp_async_commit();
+    };
+    stage(((int64_t)blockIdx.x * 8 + warp) * RBW);
     float m = 0.0f;
     if (CAST) {
         const float4 z4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -1112,20 +991,19 @@ __global__ void __launch_bounds__(256, 3) k_ln_warp(const uint16_t* __restrict__
     }
     float amax = 0.0f;
     uint32_t nsat = 0;
-    const int64_t stride = (int64_t)gridDim.x * 8 * RBW;
     for (int64_t r0 = ((int64_t)blockIdx.x * 8 + warp) * RBW; r0 < R; r0 += stride) {
+        cp_async_wait_all();
         Vec8<kBF16> v[RBW][CT];
 #pragma unroll
         for (int j = 0; j < RBW; ++j) {
-            const bool live = r0 + j < R;
-            const uint16_t* row = x + (live ? r0 + j : 0) * (int64_t)K;
 #pragma unroll
             for (int i = 0; i < CT; ++i) {
                 const int c = lane + 32 * i;
-                if (live && c < nch) v[j][i].load(row, c * 8); else v[j][i].zero();
+                if (r0 + j < R && c < nch) v[j][i].w = xs[(j * CT + i) * 32 + lane]; else v[j][i].zero();
             }
         }
         float mean[RBW], rs[RBW];
+        float s0[RBW];
 #pragma unroll
         for (int j = 0; j < RBW; ++j) {
             float2 acc = make_float2(0.0f, 0.0f);
@@ -1136,8 +1014,12 @@ __global__ void __launch_bounds__(256, 3) k_ln_warp(const uint16_t* __restrict__
                 bf16x8_pairs(v[j][i].w, p);
                 acc = ln_sum8(p, acc);
             }
-            mean[j] = __fdiv_rn(ln_warp_sum(__fadd_rn(acc.x, acc.y)), (float)K);
+            s0[j] = __fadd_rn(acc.x, acc.y);
         }
+        // the sums have consumed this warp's stage: start the next rows'
+        stage(r0 + stride);
+#pragma unroll
+        for (int j = 0; j < RBW; ++j) mean[j] = __fdiv_rn(ln_warp_sum(s0[j]), (float)K);
 #pragma unroll
         for (int j = 0; j < RBW; ++j) {
             float2 acc = make_float2(0.0f, 0.0f);
@@ -1184,8 +1066,8 @@ __global__ void __launch_bounds__(256, 3) k_ln_warp(const uint16_t* __restrict__
     }
 }
 
-// One LayerNorm-kernel launch: KERN is a k_ln_warp or k_ln_rows
-// instantiation, `rows_per_cta` the rows one CTA takes per iteration;
+// One LayerNorm-kernel launch: KERN is a k_ln_warp instantiation,
+// `rows_per_cta` the rows one CTA takes per iteration;
 // CAST launches pass the codes and state.
 template <typename Kern>
 static void launch_ln(Kern kern, int rows_per_cta, int smem, const QuantArgs& a, const float* gamma,
@@ -1204,47 +1086,48 @@ static void launch_ln(Kern kern, int rows_per_cta, int smem, const QuantArgs& a,
              cast ? static_cast<float*>(a.scales) : (float*)nullptr, cast ? a.sat : (unsigned long long*)nullptr);
 }
 
+// A k_ln_warp launch: its shared memory (gamma and beta for CAST, the warps'
+// stages) allowed once at the largest width it serves.
+template <bool CAST, int FMT, int CT, int RBW>
+static cudaError_t launch_ln_warp(const QuantArgs& a, const float* gamma, const float* beta, float eps, float* mu,
+                                  float* rstd, cudaStream_t st, int sms)
+{
+    auto kern = k_ln_warp<CAST, FMT, CT, RBW>;
+    cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(kern), ln_warp_smem<CAST, CT, RBW>(32 * 8 * CT));
+    if (e != cudaSuccess) return e;
+    launch_ln(kern, 8 * RBW, ln_warp_smem<CAST, CT, RBW>((int)a.cols), a, gamma, beta, eps, mu, rstd, st, sms, CAST);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_layernorm_quantize(const QuantArgs& a, const float* gamma, const float* beta, float eps,
                                       float* mu, float* rstd, cudaStream_t st, int sms)
 {
     if (a.rows == 0 || a.cols == 0) return cudaSuccess;
     const int K = (int)a.cols;
-    // row width -> kernel: up to 1024 a warp per two rows, up to 2048 a warp
-    // per row, up to 4096 a CTA per four rows (all held in registers); wider
-    // rows stream their statistics and always take two passes
-    const int width = K <= 1024 ? 0 : K <= 2048 ? 1 : K <= 256 * 8 * LN_CT ? 2 : 3;
+    // row width -> kernel: up to 1024 a warp per two rows, up to 4096 a warp
+    // per row (all held in registers); wider rows stream their statistics and
+    // always take two passes
+    const int width = K <= 1024 ? 0 : K <= 2048 ? 1 : K <= 4096 ? 2 : 3;
     const bool one_pass = !a.qT && !a.amax && width < 3;
     const bool e4 = a.format == kE4M3;
-    const int gb_smem = 2 * K * 4;                                   // gamma and beta
+    cudaError_t e = cudaSuccess;
     if (width == 0) {
-        if (one_pass) {
-            launch_ln(e4 ? k_ln_warp<true, kE4M3, 4, 2> : k_ln_warp<true, kE5M2, 4, 2>, 16, gb_smem, a, gamma, beta,
-                      eps, mu, rstd, st, sms, true);
-            return cudaGetLastError();
-        }
-        launch_ln(k_ln_warp<false, kE4M3, 4, 2>, 16, 0, a, gamma, beta, eps, mu, rstd, st, sms, false);
+        if (one_pass) return e4 ? launch_ln_warp<true, kE4M3, 4, 2>(a, gamma, beta, eps, mu, rstd, st, sms)
+                                : launch_ln_warp<true, kE5M2, 4, 2>(a, gamma, beta, eps, mu, rstd, st, sms);
+        e = launch_ln_warp<false, kE4M3, 4, 2>(a, gamma, beta, eps, mu, rstd, st, sms);
     } else if (width == 1) {
-        if (one_pass) {
-            launch_ln(e4 ? k_ln_warp<true, kE4M3, 8, 1> : k_ln_warp<true, kE5M2, 8, 1>, 8, gb_smem, a, gamma, beta,
-                      eps, mu, rstd, st, sms, true);
-            return cudaGetLastError();
-        }
-        launch_ln(k_ln_warp<false, kE4M3, 8, 1>, 8, 0, a, gamma, beta, eps, mu, rstd, st, sms, false);
+        if (one_pass) return e4 ? launch_ln_warp<true, kE4M3, 8, 1>(a, gamma, beta, eps, mu, rstd, st, sms)
+                                : launch_ln_warp<true, kE5M2, 8, 1>(a, gamma, beta, eps, mu, rstd, st, sms);
+        e = launch_ln_warp<false, kE4M3, 8, 1>(a, gamma, beta, eps, mu, rstd, st, sms);
     } else if (width == 2) {
-        if (one_pass) {
-            // one pass: statistics, normalisation and cast from registers
-            auto kern = e4 ? k_ln_rows<true, kE4M3> : k_ln_rows<true, kE5M2>;
-            cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(kern), ln_rows_smem<true>(256 * 8 * LN_CT));
-            if (e != cudaSuccess) return e;
-            launch_ln(kern, LN_RB, ln_rows_smem<true>(K), a, gamma, beta, eps, mu, rstd, st, sms, true);
-            return cudaGetLastError();
-        }
-        launch_ln(k_ln_rows<false, kE4M3>, LN_RB, ln_rows_smem<false>(K), a, gamma, beta, eps, mu, rstd, st, sms,
-                  false);
+        if (one_pass) return e4 ? launch_ln_warp<true, kE4M3, 16, 1>(a, gamma, beta, eps, mu, rstd, st, sms)
+                                : launch_ln_warp<true, kE5M2, 16, 1>(a, gamma, beta, eps, mu, rstd, st, sms);
+        e = launch_ln_warp<false, kE4M3, 16, 1>(a, gamma, beta, eps, mu, rstd, st, sms);
     } else {
         launch_k(k_ln_stats_long, (unsigned)((a.rows + LN_RB - 1) / LN_RB), 256, 0, st,
                  static_cast<const uint16_t*>(a.x), a.rows, K, eps, mu, rstd);
     }
+    if (e != cudaSuccess) return e;
     // two passes: the statistics above, then the tiled cast in its LayerNorm
     // mode (which also writes the transposed copy)
     LnParams ln;
