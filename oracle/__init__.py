@@ -37,6 +37,7 @@ ALGO_MAX, ALGO_MOST_RECENT = 0, 1
 GRAN_TENSOR, GRAN_TILE_1x128, GRAN_BLOCK_128x128, GRAN_MX32 = 0, 1, 2, 3
 GRAN_TILE_128x1, GRAN_MX32_COL = 4, 5   # column units (128 or 32 consecutive rows of a column)
 GRAN_TILE_POW2, GRAN_BLOCK_POW2 = 6, 7   # 1x128 / 128x128 units with power-of-two (E8M0) scales
+GRAN_TILE_COL_POW2 = 8                   # 128x1 column units with power-of-two (E8M0) scales
 FMAX = {E4M3: 448.0, E5M2: 57344.0}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -86,6 +87,7 @@ def _load():
                 "orc_layernorm": (None, [P, c.c_int64, c.c_int64, P, P, c.c_double, P, P, P]),
                 "orc_quantize_mx32_floor": (c.c_int64, [P, c.c_int64, c.c_int64, c.c_int, P, P]),
                 "orc_quantize_tile1x128_pow2": (c.c_int64, [P, c.c_int64, c.c_int64, c.c_int, P, P]),
+                "orc_quantize_tile128x1_pow2": (c.c_int64, [P, c.c_int64, c.c_int64, c.c_int, P, P]),
                 "orc_quantize_block128_pow2": (c.c_int64, [P, c.c_int64, c.c_int64, c.c_int, P, P]),
                 "orc_quantize_mx32_col": (c.c_int64, [P, c.c_int64, c.c_int64, c.c_int, P, P, P]),
                 "orc_quantize_mx32": (c.c_int64, [P, c.c_int64, c.c_int64, c.c_int, P, P, P]),
@@ -277,6 +279,7 @@ def _e8m0_quantizer(name, shape_fn):
 quantize_mx32_floor = _e8m0_quantizer("orc_quantize_mx32_floor", lambda R, C: (R, C // 32))
 quantize_tile1x128_pow2 = _e8m0_quantizer("orc_quantize_tile1x128_pow2", lambda R, C: (R, C // 128))
 quantize_block128_pow2 = _e8m0_quantizer("orc_quantize_block128_pow2", lambda R, C: (R // 128, C // 128))
+quantize_tile128x1_pow2 = _e8m0_quantizer("orc_quantize_tile128x1_pow2", lambda R, C: (R // 128, C))
 
 
 def layernorm(x, gamma, beta=None, eps: float = 1e-5):
@@ -339,7 +342,7 @@ def update_scale(state: np.ndarray, fmt: int, algo: int = ALGO_MAX) -> None:
 def dequantize(q: np.ndarray, fmt: int, gran: int, scales) -> np.ndarray:
     q = np.ascontiguousarray(q, dtype=np.uint8)
     R, C = q.shape
-    if gran in (GRAN_MX32, GRAN_MX32_COL, GRAN_TILE_POW2, GRAN_BLOCK_POW2):
+    if gran in (GRAN_MX32, GRAN_MX32_COL, GRAN_TILE_POW2, GRAN_BLOCK_POW2, GRAN_TILE_COL_POW2):
         sc = np.ascontiguousarray(scales, dtype=np.uint8)
     else:
         sc = np.ascontiguousarray(np.atleast_1d(np.asarray(scales, dtype=np.float32)))
@@ -406,13 +409,19 @@ def linear_bwd_delayed(dy, dy_state, dy_fmt, qx, sx, qw, sw, rows=None, wrows=No
 # 128x128 blocks of W^T are W's blocks transposed, and MX W is re-quantised
 # in column blocks), wgrad over the tokens M (dy and x in column units).
 def linear_fine_fwd(x, w, gran: int):
-    """gran GRAN_TILE_1x128 (x tiles, W blocks) or GRAN_MX32 -> (state, R) with
-    state holding what the backward needs (the forward's W codes / scales)."""
+    """gran GRAN_TILE_1x128 (x tiles, W blocks), GRAN_TILE_POW2 (the same
+    units with power-of-two scales) or GRAN_MX32 -> (state, R) with state
+    holding what the backward needs (the forward's W codes / scales)."""
     if gran == GRAN_TILE_1x128:
         qx, sx, _, _ = quantize_tile1x128(x, E4M3)
         qw, sw, _, _ = quantize_block128(w, E4M3)
         r = gemm_ref(dequantize(qx, E4M3, GRAN_TILE_1x128, sx), dequantize(qw, E4M3, GRAN_BLOCK_128x128, sw))
         return {"x": x, "qw": qw, "sw": sw, "w": w}, r
+    if gran == GRAN_TILE_POW2:
+        qx, ex, _ = quantize_tile1x128_pow2(x, E4M3)
+        qw, ew, _ = quantize_block128_pow2(w, E4M3)
+        r = gemm_ref(dequantize(qx, E4M3, GRAN_TILE_POW2, ex), dequantize(qw, E4M3, GRAN_BLOCK_POW2, ew))
+        return {"x": x, "qw": qw, "sw": ew, "w": w}, r
     qx, ex, _, _ = quantize_mx32(x, E4M3)
     qw, ew, _, _ = quantize_mx32(w, E4M3)
     r = gemm_ref(dequantize(qx, E4M3, GRAN_MX32, ex), dequantize(qw, E4M3, GRAN_MX32, ew))
@@ -430,6 +439,16 @@ def linear_fine_bwd_operands(st, dy, gran: int, dy_fmt: int = E4M3):
       wgrad_dy  dy in units along M   (128x1 column tiles [M/128][N] / [M/32][N])
       wgrad_x   x in units along M    (128x1 column tiles [M/128][K] / [M/32][K])"""
     x, w = st["x"], st["w"]
+    if gran == GRAN_TILE_POW2:
+        qd, ed, _ = quantize_tile1x128_pow2(dy, dy_fmt)
+        qdc, edc, _ = quantize_tile128x1_pow2(dy, dy_fmt)
+        qxc, exc, _ = quantize_tile128x1_pow2(x, E4M3)
+        return {
+            "dgrad_dy": (qd, ed, dequantize(qd, dy_fmt, GRAN_TILE_POW2, ed)),
+            "dgrad_w": (st["qw"], st["sw"], dequantize(st["qw"], E4M3, GRAN_BLOCK_POW2, st["sw"])),
+            "wgrad_dy": (qdc, edc, dequantize(qdc, dy_fmt, GRAN_TILE_COL_POW2, edc)),
+            "wgrad_x": (qxc, exc, dequantize(qxc, E4M3, GRAN_TILE_COL_POW2, exc)),
+        }
     if gran == GRAN_TILE_1x128:
         qd, sd, _, _ = quantize_tile1x128(dy, dy_fmt)
         qdc, sdc, _, _ = quantize_tile128x1(dy, dy_fmt)

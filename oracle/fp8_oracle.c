@@ -389,6 +389,27 @@ int64_t orc_quantize_tile128x1(const float* x, int64_t R, int64_t C, int fmt, ui
     return sat;
 }
 
+/* Power-of-two column tiles (the recipe variant of tile128x1): the MX rule's
+ * power of two for each 128 consecutive values of a column; E8M0 codes
+ * e[R/128][C]. */
+int64_t orc_quantize_tile128x1_pow2(const float* x, int64_t R, int64_t C, int fmt, uint8_t* q, uint8_t* e_out)
+{
+    int64_t RB = R / 128, sat = 0;
+    #pragma omp parallel for reduction(+:sat) schedule(static)
+    for (int64_t c = 0; c < C; ++c) {
+        for (int64_t rb = 0; rb < RB; ++rb) {
+            float a = 0.0f;
+            for (int64_t r = rb * 128; r < rb * 128 + 128; ++r)
+                a = amax2(a, fabsf(x[r * C + c]));
+            uint8_t code = orc_mx_scale_code(a, fmt);
+            float m = (code == 0xFF) ? 1.0f : (float)ldexp(1.0, -((int)code - 127));
+            e_out[rb * C + c] = code;
+            sat += quant_run(x + rb * 128 * C + c, 128, C, m, fmt, q + rb * 128 * C + c, C);
+        }
+    }
+    return sat;
+}
+
 int64_t orc_quantize_mx32_col(const float* x, int64_t R, int64_t C, int fmt, uint8_t* q,
                               uint8_t* e8m0_out, float* amax_out)
 {
@@ -487,7 +508,8 @@ void orc_update_scale(float* state, int H, int fmt, int algo)
  * (s[R/128][C/128]), 3 MX-32 (E8M0 codes u8[R][C/32]), 4 column tile 128x1
  * (s[R/128][C]), 5 column MX-32 (E8M0 codes u8[R/32][C]), 6 power-of-two 1x128
  * tiles (E8M0 codes u8[R][C/128]), 7 power-of-two 128x128 blocks (E8M0 codes
- * u8[R/128][C/128]).
+ * u8[R/128][C/128]), 8 power-of-two 128x1 column tiles (E8M0 codes
+ * u8[R/128][C]).
  * ---------------------------------------------------------------------- */
 void orc_dequantize(const uint8_t* q, int64_t R, int64_t C, int fmt, int gran,
                     const void* scales, double* out)
@@ -500,8 +522,9 @@ void orc_dequantize(const uint8_t* q, int64_t R, int64_t C, int fmt, int gran,
             else if (gran == 1) s = ((const float*)scales)[r * (C / 128) + c / 128];
             else if (gran == 2) s = ((const float*)scales)[(r / 128) * (C / 128) + c / 128];
             else if (gran == 4) s = ((const float*)scales)[(r / 128) * C + c];
-            else if (gran == 5) {
-                uint8_t code = ((const uint8_t*)scales)[(r / 32) * C + c];
+            else if (gran == 5 || gran == 8) {
+                uint8_t code = (gran == 5) ? ((const uint8_t*)scales)[(r / 32) * C + c]
+                                           : ((const uint8_t*)scales)[(r / 128) * C + c];
                 s = (code == 0xFF) ? NAN : ldexp(1.0, (int)code - 127);
             } else if (gran == 6 || gran == 7) {
                 uint8_t code = (gran == 6) ? ((const uint8_t*)scales)[r * (C / 128) + c / 128]

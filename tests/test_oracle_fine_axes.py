@@ -32,6 +32,9 @@ def _operands(x, w, dy, gran):
     if gran == o.GRAN_TILE_1x128:
         qw, sw, _, _ = o.quantize_block128(w, o.E4M3)
         st = {"x": x, "w": w, "qw": qw, "sw": sw}
+    elif gran == o.GRAN_TILE_POW2:
+        qw, ew, _ = o.quantize_block128_pow2(w, o.E4M3)
+        st = {"x": x, "w": w, "qw": qw, "sw": ew}
     else:
         st = {"x": x, "w": w}
     return o.linear_fine_bwd_operands(st, dy, gran, o.E5M2)
@@ -49,6 +52,12 @@ EXPECTED = {
         "wgrad_dy": ((M // 128, N), {(DY_AT[0] // 128, DY_AT[1])}),          # 128x1 along M
         "wgrad_x": ((M // 128, K), {(X_AT[0] // 128, X_AT[1])}),             # 128x1 along M
     },
+    o.GRAN_TILE_POW2: {      # the same units, power-of-two scales
+        "dgrad_dy": ((M, N // 128), {(DY_AT[0], DY_AT[1] // 128)}),
+        "dgrad_w": ((N // 128, K // 128), {(W_AT[0] // 128, W_AT[1] // 128)}),
+        "wgrad_dy": ((M // 128, N), {(DY_AT[0] // 128, DY_AT[1])}),
+        "wgrad_x": ((M // 128, K), {(X_AT[0] // 128, X_AT[1])}),
+    },
     o.GRAN_MX32: {
         "dgrad_dy": ((M, N // 32), {(DY_AT[0], DY_AT[1] // 32)}),            # 32 along N
         "dgrad_w": ((N // 32, K), {(W_AT[0] // 32, W_AT[1])}),               # W, 32 along N
@@ -58,7 +67,7 @@ EXPECTED = {
 }
 
 
-@pytest.mark.parametrize("gran", [o.GRAN_TILE_1x128, o.GRAN_MX32])
+@pytest.mark.parametrize("gran", [o.GRAN_TILE_1x128, o.GRAN_TILE_POW2, o.GRAN_MX32])
 def test_one_outlier_changes_exactly_its_unit_per_operand(gran):
     x, w, dy = _inputs(1)
     base = _operands(x, w, dy, gran)
@@ -78,7 +87,7 @@ def test_one_outlier_changes_exactly_its_unit_per_operand(gran):
         assert o.decode(fmt, int(spiked[name][0][at])) >= fmax / 2, name
 
 
-@pytest.mark.parametrize("gran", [o.GRAN_TILE_1x128, o.GRAN_MX32])
+@pytest.mark.parametrize("gran", [o.GRAN_TILE_1x128, o.GRAN_TILE_POW2, o.GRAN_MX32])
 def test_backward_products_use_those_operands(gran):
     x, w, dy = _inputs(2)
     st, _ = o.linear_fine_fwd(x, w, gran)

@@ -260,6 +260,26 @@ def test_pow2_tiles_and_blocks(fmt):
                           np.repeat(np.repeat(2.0 ** (eb.astype(np.float64) - 127), 128, 0), 128, 1))
 
 
+@pytest.mark.parametrize("fmt", [o.E4M3, o.E5M2])
+def test_pow2_column_tiles(fmt):
+    """A power-of-two 128x1 column tile's code is the largest of the four
+    column MX-32 codes it covers; the codes are the row tiles of x^T (the
+    same rule on 128 consecutive values of a column); dequantising the code
+    of 1.0 gives the tile's power of two."""
+    rng = np.random.default_rng(16)
+    x = (rng.standard_normal((256, 384)) * np.exp(rng.standard_normal((1, 384)))).astype(np.float32)
+    x[200, 3] = 9000.0
+    q, e, sat = o.quantize_tile128x1_pow2(x, fmt)
+    _, emx, _, _ = o.quantize_mx32_col(x, fmt)
+    assert e.shape == (2, 384) and sat == 0
+    assert np.array_equal(e, emx.reshape(2, 4, 384).max(axis=1))
+    qt, et, _ = o.quantize_tile1x128_pow2(np.ascontiguousarray(x.T), fmt)
+    assert np.array_equal(q, qt.T) and np.array_equal(e, et.T)
+    one = o.encode(fmt, 1.0)
+    assert np.array_equal(o.dequantize(np.full((256, 384), one, np.uint8), fmt, o.GRAN_TILE_COL_POW2, e),
+                          np.repeat(2.0 ** (e.astype(np.float64) - 127), 128, 0))
+
+
 def test_layernorm_closed_forms():
     """Standardised output: every row has mean 0 and variance var/(var+eps)
     before the affine part; gamma scales and beta shifts column-wise; a
