@@ -795,6 +795,17 @@ def per_config(device, with_oracle: bool = True) -> dict:
     r3["linear_bwd"] = gemm_row(
         _time_flushed(lambda: sq.fp8_linear_bwd(dy3, dx3, dw3, ws3, n3, gran=sq.TILE_1x128), flush), 2 * fl3,
         {"what": "fp8_linear_bwd TILE_1x128: dy rows + columns, dgrad (promotion) + wgrad (column tiles)"})
+    # the recipe variant with the same units and power-of-two scales: every
+    # GEMM on the block-scaled MMA, no promotion
+    ws3p = torch.empty(sq.fp8_linear_workspace_bytes(n3, n3, n3, sq.TILE_1x128_POW2), **u8)
+    r3["linear_fwd_pow2"] = gemm_row(
+        _time_flushed(lambda: sq.fp8_linear_fwd(x3, w3, y3, ws3p, gran=sq.TILE_1x128_POW2), flush), fl3,
+        {"what": "recipe variant, fp8_linear_fwd TILE_1x128_POW2: the same units with power-of-two (E8M0) "
+                 "scales, block-scaled GEMM"})
+    r3["linear_bwd_pow2"] = gemm_row(
+        _time_flushed(lambda: sq.fp8_linear_bwd(dy3, dx3, dw3, ws3p, n3, gran=sq.TILE_1x128_POW2), flush), 2 * fl3,
+        {"what": "recipe variant, fp8_linear_bwd TILE_1x128_POW2: dgrad and wgrad block-scaled"})
+    del ws3p
     if o is not None:
         rows = 256
         xn, wn = x3.float().cpu().numpy(), w3.float().cpu().numpy()
@@ -1221,7 +1232,8 @@ def modes_table(reps: int = 10):
         del qdT, qxT, yb
         torch.cuda.empty_cache()
     M = N = K = 4096
-    for gran, name in [(sq.TILE_1x128, "TILE_1x128 / BLOCK_128x128"), (sq.MX32, "MX32")]:
+    for gran, name in [(sq.TILE_1x128, "TILE_1x128 / BLOCK_128x128"),
+                       (sq.TILE_1x128_POW2, "TILE_1x128_POW2 (power-of-two tiles / blocks)"), (sq.MX32, "MX32")]:
         x, w = wl.student_t3((M, K), 1, dev), wl.normal((N, K), 0.02, 2, dev)
         dy = wl.normal((M, N), 1e-3, 3, dev)
         ws = torch.empty(sq.fp8_linear_workspace_bytes(M, N, K, gran), **u8)

@@ -206,6 +206,12 @@ FP8SQ_API int fp8_quantize(const void* x, int x_dtype, int64_t rows, int64_t col
  *                     qT, col_scales     = fp8_quantize(MX32_COL_TILED)
  * with the layouts documented there (f32 [rows][cols/128] and
  * [rows/128][cols]; or the tiled E8M0 layouts of x and of qT).
+ *   unit TILE_1x128_POW2: q, row_scales = fp8_quantize(TILE_1x128_POW2)
+ *                     (power-of-two 1x128 tiles, tiled E8M0 layout of x);
+ *                     qT, col_scales: power-of-two 128x1 column tiles, the
+ *                     same rule on 128 consecutive values of a column, each
+ *                     code in the four 32-row blocks it covers of the tiled
+ *                     E8M0 layout of qT (as MX32_COL_TILED lays them out).
  *   x        device bf16 [rows][cols], 16-byte aligned; rows, cols % 128 == 0
  *   q        device u8 [rows][cols]; qT device u8 [cols][rows]; 16-byte aligned
  *   row_scales, col_scales  device, 4-byte aligned (16 for the E8M0 layouts)
@@ -307,6 +313,10 @@ FP8SQ_API int fp8_gemm_cast(const uint8_t* A, int a_format, const void* a_scale,
  *   1x128 tiles along N for dgrad (B = W^T codes, its blocks transposed); dy
  *   and x in 128x1 column tiles along M for wgrad (both operands promoted per
  *   128 tokens).  The forward also casts x in column tiles for the backward.
+ * gran TILE_1x128_POW2: the units of TILE_1x128 with power-of-two scales
+ *   (the MX rule on each 1x128 tile, 128x128 block and 128x1 column tile,
+ *   stored as tiled E8M0 codes): every GEMM runs on the block-scaled MMA,
+ *   with no promotion.  dgrad's B is W^T with W's blocks transposed.
  * gran MX32: every operand in MX-32 blocks along its contraction dimension:
  *   x, W along K (forward), dy along N and W along N (dgrad), dy and x along
  *   M (wgrad); the forward also writes the column-block codes of x and W.

@@ -106,6 +106,9 @@ size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
 //   tiles [M][K/128] and column tiles [M/128][K]; W blocks and their
 //   transpose; dy tiles [M][N/128] and column tiles [M/128][N].
 // MX32: x, W, dy in row blocks and column blocks, tiled E8M0 scales.
+// TILE_1x128_POW2: as MX32 in size and layout: x and dy in power-of-two
+//   1x128 tiles and 128x1 column tiles, W in power-of-two 128x128 blocks
+//   and their transpose, every scale as tiled E8M0 codes.
 WsLayout ws_layout(int64_t M, int64_t N, int64_t K, int gran)
 {
     WsLayout L;
@@ -355,8 +358,8 @@ FP8SQ_API int fp8_quantize_rows_cols(const void* x, int64_t rows, int64_t cols, 
     if ((!x || !q || !qT || !row_scales || !col_scales) && rows * cols != 0)
         return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize_rows_cols: null pointer");
     if (!valid_format(format)) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize_rows_cols: bad format");
-    if (unit != FP8SQ_TILE_1x128 && unit != FP8SQ_MX32_TILED)
-        return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize_rows_cols: unit must be TILE_1x128 or MX32_TILED");
+    if (unit != FP8SQ_TILE_1x128 && unit != FP8SQ_MX32_TILED && unit != FP8SQ_TILE_1x128_POW2)
+        return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize_rows_cols: unit must be TILE_1x128, TILE_1x128_POW2 or MX32_TILED");
     if (rows < 0 || cols < 0) return fail(FP8SQ_ERR_INVALID_ARG, "fp8_quantize_rows_cols: negative size");
     if (rows >= kMaxDim || cols >= kMaxDim) return fail(FP8SQ_ERR_UNSUPPORTED, "fp8_quantize_rows_cols: dimension too large");
     if (rows % 128 || cols % 128)
@@ -364,7 +367,7 @@ FP8SQ_API int fp8_quantize_rows_cols(const void* x, int64_t rows, int64_t cols, 
                     (long long)rows, (long long)cols);
     if (!aligned16(x) || !aligned16(q) || !aligned16(qT))
         return fail(FP8SQ_ERR_MISALIGNED, "fp8_quantize_rows_cols: x, q, qT must be 16-byte aligned");
-    const bool e8m0 = unit == FP8SQ_MX32_TILED;
+    const bool e8m0 = unit == FP8SQ_MX32_TILED || unit == FP8SQ_TILE_1x128_POW2;
     if (e8m0 ? (!aligned16(row_scales) || !aligned16(col_scales)) : (!aligned4(row_scales) || !aligned4(col_scales)))
         return fail(FP8SQ_ERR_MISALIGNED, "fp8_quantize_rows_cols: scales misaligned");
     if (sat_count && (reinterpret_cast<uintptr_t>(sat_count) & 7u))
@@ -374,7 +377,8 @@ FP8SQ_API int fp8_quantize_rows_cols(const void* x, int64_t rows, int64_t cols, 
     if (rows * cols == 0) return FP8SQ_OK;
     fp8sq::QuantArgs a;
     a.x = x; a.x_dtype = fp8sq::kBF16; a.rows = rows; a.cols = cols; a.format = format;
-    a.gran = e8m0 ? fp8sq::kMXRowCol : fp8sq::kTileRowCol;
+    a.gran = unit == FP8SQ_MX32_TILED ? fp8sq::kMXRowCol
+             : unit == FP8SQ_TILE_1x128_POW2 ? fp8sq::kTileRowColPow2 : fp8sq::kTileRowCol;
     a.q = q; a.qT = qT; a.scales = row_scales; a.col_scales = col_scales; a.sat = sat_count;
     return cuda_status(fp8sq::launch_quantize(a, static_cast<cudaStream_t>(stream), sms),
                        "fp8_quantize_rows_cols launch");
@@ -528,7 +532,9 @@ FP8SQ_API int fp8_gemm_cast(const uint8_t* A, int a_format, const void* a_scale,
 
 FP8SQ_API size_t fp8_linear_workspace_bytes(int64_t M, int64_t N, int64_t K, int gran)
 {
-    if (M < 0 || N < 0 || K < 0 || !(gran == FP8SQ_TENSOR || gran == FP8SQ_TILE_1x128 || gran == FP8SQ_MX32)) return 0;
+    if (M < 0 || N < 0 || K < 0 ||
+        !(gran == FP8SQ_TENSOR || gran == FP8SQ_TILE_1x128 || gran == FP8SQ_MX32 || gran == FP8SQ_TILE_1x128_POW2))
+        return 0;
     return ws_layout(M, N, K, gran).total;
 }
 
@@ -538,10 +544,10 @@ static int check_linear_shape(int64_t M, int64_t N, int64_t K, int gran, const v
     if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) return fail(FP8SQ_ERR_UNSUPPORTED, "linear: dimension too large");
     if (gran == FP8SQ_TENSOR) {
         if (M % 16 || N % 16 || K % 16) return fail(FP8SQ_ERR_UNSUPPORTED, "linear: per-tensor needs M, N, K %% 16 == 0");
-    } else if (gran == FP8SQ_TILE_1x128 || gran == FP8SQ_MX32) {
+    } else if (gran == FP8SQ_TILE_1x128 || gran == FP8SQ_MX32 || gran == FP8SQ_TILE_1x128_POW2) {
         if (M % 128 || N % 128 || K % 128) return fail(FP8SQ_ERR_UNSUPPORTED, "linear: block scaling needs M, N, K %% 128 == 0");
     } else {
-        return fail(FP8SQ_ERR_INVALID_ARG, "linear: granularity must be TENSOR, TILE_1x128 or MX32");
+        return fail(FP8SQ_ERR_INVALID_ARG, "linear: granularity must be TENSOR, TILE_1x128, TILE_1x128_POW2 or MX32");
     }
     if (!ws) return fail(FP8SQ_ERR_INVALID_ARG, "linear: null workspace");
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(FP8SQ_ERR_MISALIGNED, "linear: workspace must be 256-byte aligned");
@@ -619,6 +625,22 @@ FP8SQ_API int fp8_linear_fwd(const void* x, const void* w, int64_t M, int64_t N,
         g.mode = 1;
         g.a_scale = ws + L.sx;
         g.b_scale = ws + L.sw;
+    } else if (gran == FP8SQ_TILE_1x128_POW2) {
+        // the same units with power-of-two scales, as tiled E8M0 codes: the
+        // GEMMs run on the block-scaled MMA with no promotion.  x: 1x128
+        // tiles (forward) and 128x1 column tiles (wgrad) from one read.
+        qa.x = x; qa.rows = M; qa.cols = K; qa.gran = fp8sq::kTileRowColPow2;
+        qa.q = ws + L.qx; qa.scales = ws + L.sx; qa.qT = ws + L.qxT; qa.col_scales = ws + L.sxT;
+        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: quantize x"))) return r;
+        qa.col_scales = nullptr;
+        // W: 128x128 blocks, with the transposed codes and W^T's codes (dgrad)
+        qa.x = w; qa.rows = N; qa.cols = K; qa.gran = fp8sq::kBlockPow2;
+        qa.q = ws + L.qw; qa.qT = ws + L.qwT; qa.scales = ws + L.sw;
+        qa.scalesT = reinterpret_cast<float*>(ws + L.swT);
+        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_fwd: quantize w"))) return r;
+        g.mode = 2;
+        g.a_scale = ws + L.sx;
+        g.b_scale = ws + L.sw;
     } else {
         // x and W: MX-32 blocks along K (forward) and along their rows
         // (backward), each from one read of the operand
@@ -689,6 +711,15 @@ FP8SQ_API int fp8_linear_bwd(const void* dy, int64_t M, int64_t N, int64_t K, in
         if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_bwd: quantize dy"))) return r;
         dg.mode = 1; dg.a_scale = ws + L.sdy; dg.b_scale = ws + L.swT;
         wg.mode = 3; wg.a_scale = ws + L.sdyT; wg.b_scale = ws + L.sxT;
+    } else if (gran == FP8SQ_TILE_1x128_POW2) {
+        // dy: power-of-two 1x128 tiles along N (dgrad) and 128x1 column tiles
+        // along M (wgrad), from one read; both GEMMs on the block-scaled MMA
+        qa.gran = fp8sq::kTileRowColPow2;
+        qa.q = ws + L.qdy; qa.scales = ws + L.sdy; qa.qT = ws + L.qdyT; qa.col_scales = ws + L.sdyT;
+        if ((r = cuda_status(fp8sq::launch_quantize(qa, st, sms), "fp8_linear_bwd: quantize dy"))) return r;
+        dg.mode = wg.mode = 2;
+        dg.a_scale = ws + L.sdy; dg.b_scale = ws + L.swT;
+        wg.a_scale = ws + L.sdyT; wg.b_scale = ws + L.sxT;
     } else {
         // dy: MX-32 blocks along N (dgrad) and along M (wgrad), from one read
         qa.gran = fp8sq::kMXRowCol;

@@ -12,7 +12,8 @@ enum { kE4M3 = 0, kE5M2 = 1 };
 enum { kBF16 = 0, kF32 = 1 };
 enum { kTensor = 0, kTile = 1, kBlock = 2, kMX = 3, kMXTiled = 4, kTileCol = 5, kMXCol = 6,
        kTilePow2 = 7, kBlockPow2 = 8, kMXFloor = 9,
-       kTileRowCol = 10, kMXRowCol = 11 };   // rows and columns in one pass (fp8_quantize_rows_cols)
+       kTileRowCol = 10, kMXRowCol = 11,     // rows and columns in one pass (fp8_quantize_rows_cols)
+       kTileRowColPow2 = 12 };               // the same for power-of-two 1x128 / 128x1 tiles, tiled E8M0 codes
 
 struct QuantArgs {
     const void* x = nullptr;
@@ -25,7 +26,8 @@ struct QuantArgs {
     uint8_t* q = nullptr;            // may be null only for amax-only launches
     uint8_t* qT = nullptr;
     void* scales = nullptr;
-    float* scalesT = nullptr;        // 128x128 blocks with qT: the transposed scale grid
+    float* scalesT = nullptr;        // 128x128 blocks with qT: the transposed scale grid (power-of-two
+                                     // blocks: the tiled E8M0 codes of x^T, as bytes)
     void* col_scales = nullptr;      // rows and columns in one pass: the column-unit scales
     float* amax = nullptr;
     unsigned long long* sat = nullptr;

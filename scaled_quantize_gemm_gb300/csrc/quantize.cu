@@ -587,7 +587,7 @@ __device__ __forceinline__ int64_t mx_tiled_offset(int64_t r, int64_t t, int64_t
 // (64 registers; 128-row column tiles at three, 80 registers, took 131.5
 // against 117.3 us), except MX-32 rows + columns, three (80 registers; at
 // four they spill).
-template <int FMT, int UNIT, bool ROWQ = false>
+template <int FMT, int UNIT, bool ROWQ = false, bool POW2 = false>
 __global__ void __launch_bounds__(256, UNIT == 32 && ROWQ ? 3 : 4) k_quant_col_block(const void* __restrict__ x, int64_t R, int64_t C,
                                                          uint8_t* __restrict__ q, uint8_t* __restrict__ qT,
                                                          void* scales, void* rscales, unsigned long long* sat)
@@ -663,17 +663,39 @@ __global__ void __launch_bounds__(256, UNIT == 32 && ROWQ ? 3 : 4) k_quant_col_b
             const int c = threadIdx.x;
             const uint32_t a = max(colred[0][c], colred[1][c]);
             float mm, ss;
-            current_scale<FMT>(a, mm, ss);
+            if (POW2) {
+                // power-of-two column tile: its E8M0 code fills the four
+                // 32-row blocks it covers in the tiled layout of x^T
+                const uint32_t code = mx_scale<FMT>(a, mm);
+                if (tc0 + c < C) {
+                    uint8_t* e = static_cast<uint8_t*>(scales);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) e[mx_tiled_offset(tc0 + c, tr0 / 32 + k, R)] = (uint8_t)code;
+                }
+            } else {
+                current_scale<FMT>(a, mm, ss);
+                if (tc0 + c < C) static_cast<float*>(scales)[(tr0 / 128) * C + tc0 + c] = ss;
+            }
             colm[c] = mm;
             colflag[c] = (a >= 0x7F800000u || __fmul_rn(__uint_as_float(a), mm) > Fmt<FMT>::fmax) ? 1 : 0;
-            if (tc0 + c < C) static_cast<float*>(scales)[(tr0 / 128) * C + tc0 + c] = ss;
         } else if (ROWQ) {
             const int r = threadIdx.x - 128;
             const uint32_t a = max(max(rowred[0][r], rowred[1][r]), max(rowred[2][r], rowred[3][r]));
             float mm, ss;
-            current_scale<FMT>(a, mm, ss);
+            if (POW2) {
+                // power-of-two 1x128 tile: its code fills the four 32-column
+                // blocks it covers in the tiled layout of x
+                const uint32_t code = mx_scale<FMT>(a, mm);
+                if (tr0 + r < R) {
+                    uint8_t* e = static_cast<uint8_t*>(rscales);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) e[mx_tiled_offset(tr0 + r, tc0 / 32 + k, C)] = (uint8_t)code;
+                }
+            } else {
+                current_scale<FMT>(a, mm, ss);
+                if (tr0 + r < R) static_cast<float*>(rscales)[(tr0 + r) * (C / 128) + blockIdx.x] = ss;
+            }
             rowm[r] = mm;
-            if (tr0 + r < R) static_cast<float*>(rscales)[(tr0 + r) * (C / 128) + blockIdx.x] = ss;
         }
         __syncthreads();
         const float4 m0 = *reinterpret_cast<const float4*>(&colm[cl]);
@@ -1242,7 +1264,7 @@ __global__ void __launch_bounds__(256) k_quant_block128(const void* __restrict__
                                                         uint8_t* __restrict__ q, float* s_out,
                                                         float* amax_out, unsigned long long* sat,
                                                         uint8_t* __restrict__ qT = nullptr, float* sT = nullptr,
-                                                        uint8_t* e_tiled = nullptr)
+                                                        uint8_t* e_tiled = nullptr, uint8_t* eT_tiled = nullptr)
 {
     pdl_enter();
     __shared__ uint32_t red[8];
@@ -1263,6 +1285,10 @@ __global__ void __launch_bounds__(256) k_quant_block128(const void* __restrict__
         if (WRITE_Q) {
             const uint16_t two = (uint16_t)(code | (code << 8));
             reinterpret_cast<uint16_t*>(e_tiled + unit * 512)[threadIdx.x] = two;
+            // the same block of x^T: chunk (column block, row block) of its layout
+            if (eT_tiled)
+                reinterpret_cast<uint16_t*>(eT_tiled + ((int64_t)blockIdx.x * gridDim.y + blockIdx.y) * 512)[threadIdx.x] =
+                    two;
         }
     } else {
         current_scale<FMT>(a, m, s);
@@ -1418,7 +1444,7 @@ static cudaError_t amax_dt(const QuantArgs& a, cudaStream_t st, int sms)
         break;
     case kBlock:
         if (n > 0) launch_k(k_quant_block128<DT, kE4M3, false>, dim3((unsigned)(a.cols / 128), (unsigned)(a.rows / 128)), 256, 0, st, a.x, a.rows, a.cols, nullptr, nullptr, a.amax, nullptr,
-                            nullptr, nullptr, nullptr);
+                            nullptr, nullptr, nullptr, nullptr);
         break;
     }
     return cudaGetLastError();
@@ -1489,7 +1515,10 @@ static cudaError_t quant_dt_fmt(const QuantArgs& a, cudaStream_t st, int sms)
         launch_k(k_quant_rowunits<DT, FMT, 32, true, true, 2>, flat_grid(k_quant_rowunits<DT, FMT, 32, true, true, 2>, n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
         break;
     case kBlockPow2:
-        launch_k(k_quant_block128<DT, FMT, true, true>, dim3((unsigned)(a.cols / 128), (unsigned)(a.rows / 128)), 256, 0, st, a.x, a.rows, a.cols, a.q, nullptr, a.amax, a.sat, nullptr, nullptr, static_cast<uint8_t*>(a.scales));
+        // (qT and scalesT: the transposed codes and the tiled E8M0 codes of
+        // x^T, for a linear layer's dgrad)
+        launch_k(k_quant_block128<DT, FMT, true, true>, dim3((unsigned)(a.cols / 128), (unsigned)(a.rows / 128)), 256, 0, st, a.x, a.rows, a.cols, a.q, nullptr, a.amax, a.sat, a.qT, nullptr, static_cast<uint8_t*>(a.scales),
+                 reinterpret_cast<uint8_t*>(a.scalesT));
         break;
     case kTileCol:
     case kMXCol: {
@@ -1499,16 +1528,19 @@ static cudaError_t quant_dt_fmt(const QuantArgs& a, cudaStream_t st, int sms)
         break;
     }
     case kTileRowCol:
+    case kTileRowColPow2:
     case kMXRowCol: {
         // rows in their own units into q / scales, columns into qT / col_scales
         const dim3 grid((unsigned)(a.cols / 128), (unsigned)(a.rows / 128));
-        auto kern = a.gran == kTileRowCol ? k_quant_col_block<FMT, 128, true> : k_quant_col_block<FMT, 32, true>;
+        auto kern = a.gran == kTileRowCol       ? k_quant_col_block<FMT, 128, true>
+                    : a.gran == kTileRowColPow2 ? k_quant_col_block<FMT, 128, true, true>
+                                                : k_quant_col_block<FMT, 32, true>;
         launch_k(kern, grid, 256, 0, st, a.x, a.rows, a.cols, a.q, a.qT, a.col_scales, a.scales, a.sat);
         break;
     }
     case kBlock:
         launch_k(k_quant_block128<DT, FMT, true>, dim3((unsigned)(a.cols / 128), (unsigned)(a.rows / 128)), 256, 0, st, a.x, a.rows, a.cols, a.q, static_cast<float*>(a.scales), a.amax, a.sat, a.qT, a.scalesT,
-                 nullptr);
+                 nullptr, nullptr);
         break;
     }
     return cudaGetLastError();

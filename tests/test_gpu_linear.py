@@ -266,11 +266,12 @@ def test_mx_linear_forward():
     assert_gemm_close(y, R)
 
 
-@pytest.mark.parametrize("gran", [sq.TILE_1x128, sq.MX32])
+@pytest.mark.parametrize("gran", [sq.TILE_1x128, sq.TILE_1x128_POW2, sq.MX32])
 @pytest.mark.parametrize("recipe", [sq.RECIPE_E4M3, sq.RECIPE_HYBRID])
 def test_fine_grained_linear_forward_and_backward(gran, recipe):
-    """1x128 / 128x128 (and MX-32) forward, dgrad and wgrad, each operand
-    quantised along its own contraction dimension, against the oracle."""
+    """1x128 / 128x128 (with fp32 or power-of-two scales, and MX-32) forward,
+    dgrad and wgrad, each operand quantised along its own contraction
+    dimension, against the oracle."""
     M, K, N = 256, 384, 512
     x = wl.student_t3((M, K), 101).to(DEV)
     w = wl.normal((N, K), 0.02, 102).to(DEV)
@@ -282,7 +283,7 @@ def test_fine_grained_linear_forward_and_backward(gran, recipe):
     sq.fp8_linear_fwd(x, w, y, ws, gran=gran)
     sq.fp8_linear_bwd(dy, dx, dw, ws, K, gran=gran, recipe=recipe)
     torch.cuda.synchronize()
-    og = o.GRAN_TILE_1x128 if gran == sq.TILE_1x128 else o.GRAN_MX32
+    og = {sq.TILE_1x128: o.GRAN_TILE_1x128, sq.TILE_1x128_POW2: o.GRAN_TILE_POW2, sq.MX32: o.GRAN_MX32}[gran]
     st, Y = o.linear_fine_fwd(np32(x), np32(w), og)
     dX, dW = o.linear_fine_bwd(st, np32(dy), og, o.E5M2 if recipe == sq.RECIPE_HYBRID else o.E4M3)
     assert_gemm_close(y, Y)

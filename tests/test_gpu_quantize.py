@@ -379,6 +379,32 @@ def test_pow2_tiles_blocks_and_floor_mx(fmt):
     assert np.array_equal(mx_untile(e.cpu().numpy(), R, C), re)
 
 
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("shape", [(256, 384), (128, 128), (384, 256)])
+def test_rows_cols_pow2_tiles(fmt, shape):
+    """Power-of-two 1x128 row tiles and 128x1 column tiles in one pass: codes
+    bit-exact against the oracle's power-of-two quantisers; each tile's E8M0
+    code fills the four 32-blocks it covers in the tiled layouts of x and
+    x^T; an outlier and a NaN are planted."""
+    from _helpers import mx_untile
+    R, C = shape
+    x = wl.student_t3(shape, 91 + R + C)
+    x[3, 130 % C] = 700.0
+    x[R - 1, 5] = float("nan")
+    xd = x.to(DEV)
+    q, qT = _u8(shape), _u8((C, R))
+    rs, cs = _u8((R * C // 32,)), _u8((R * C // 32,))
+    sq.fp8_quantize_rows_cols(xd, fmt, sq.TILE_1x128_POW2, q, rs, qT, cs)
+    torch.cuda.synchronize()
+    xf = np32(x)
+    rq, re, _ = o.quantize_tile1x128_pow2(xf, fmt)
+    cq, ce, _ = o.quantize_tile128x1_pow2(xf, fmt)
+    assert np.array_equal(mx_untile(rs.cpu().numpy(), R, C), np.repeat(re, 4, axis=1))
+    assert np.array_equal(mx_untile(cs.cpu().numpy(), C, R), np.repeat(ce.T, 4, axis=1))
+    assert nan_aware_codes_equal(codes(q), rq, fmt)
+    assert nan_aware_codes_equal(codes(qT), cq.T, fmt)
+
+
 @pytest.mark.parametrize("unit", [sq.TILE_1x128, sq.MX32_TILED])
 @pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("shape", [(256, 384), (128, 128), (384, 256)])
