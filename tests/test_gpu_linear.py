@@ -289,3 +289,48 @@ def test_fine_grained_linear_forward_and_backward(gran, recipe):
     assert_gemm_close(y, Y)
     assert_gemm_close(dx, dX)
     assert_gemm_close(dw, dW)
+
+
+def _fine_forward_operands(x, w, og):
+    """The oracle's forward operands of the fine-grained recipes, dequantised,
+    and the backward state (W's codes and scales for the tile recipes)."""
+    if og == o.GRAN_TILE_1x128:
+        qx, sx, _, _ = o.quantize_tile1x128(x, o.E4M3)
+        qw, sw, _, _ = o.quantize_block128(w, o.E4M3)
+        return (o.dequantize(qx, o.E4M3, og, sx), o.dequantize(qw, o.E4M3, o.GRAN_BLOCK_128x128, sw),
+                {"x": x, "w": w, "qw": qw, "sw": sw})
+    if og == o.GRAN_TILE_POW2:
+        qx, ex, _ = o.quantize_tile1x128_pow2(x, o.E4M3)
+        qw, ew, _ = o.quantize_block128_pow2(w, o.E4M3)
+        return (o.dequantize(qx, o.E4M3, og, ex), o.dequantize(qw, o.E4M3, o.GRAN_BLOCK_POW2, ew),
+                {"x": x, "w": w, "qw": qw, "sw": ew})
+    qx, ex, _, _ = o.quantize_mx32(x, o.E4M3)
+    qw, ew, _, _ = o.quantize_mx32(w, o.E4M3)
+    return o.dequantize(qx, o.E4M3, og, ex), o.dequantize(qw, o.E4M3, og, ew), {"x": x, "w": w}
+
+
+@pytest.mark.parametrize("gran", [sq.TILE_1x128, sq.TILE_1x128_POW2, sq.MX32])
+def test_fine_grained_linear_full_size_sampled_rows(gran):
+    """Workload 3's shapes and data (M = N = K = 4096: Student-t x, N(0, 0.02)
+    W, N(0, 1e-3) dy) through fp8_linear_fwd / fp8_linear_bwd in the launch
+    configuration the bench times: y, dx and dW on 32 sampled rows each
+    against the oracle's products of its own operands (HYBRID: dy in E5M2)."""
+    n = 4096
+    x, w = wl.w3_operands(DEV)
+    dy = wl.normal((n, n), 1e-3, wl.seed_of(3, 0, wl.ROLE_DY), DEV)
+    ws = torch.empty(sq.fp8_linear_workspace_bytes(n, n, n, gran), dtype=torch.uint8, device=DEV)
+    y = torch.empty((n, n), dtype=torch.bfloat16, device=DEV)
+    dx = torch.empty((n, n), dtype=torch.bfloat16, device=DEV)
+    dw = torch.empty((n, n), dtype=torch.float32, device=DEV)
+    sq.fp8_linear_fwd(x, w, y, ws, gran=gran)
+    sq.fp8_linear_bwd(dy, dx, dw, ws, n, gran=gran)
+    torch.cuda.synchronize()
+    og = {sq.TILE_1x128: o.GRAN_TILE_1x128, sq.TILE_1x128_POW2: o.GRAN_TILE_POW2, sq.MX32: o.GRAN_MX32}[gran]
+    xh, wh, st = _fine_forward_operands(np32(x), np32(w), og)
+    ops = o.linear_fine_bwd_operands(st, np32(dy), og, o.E5M2)
+    rng = np.random.default_rng(33)
+    ry, rx, rw = (np.sort(rng.choice(n, size=32, replace=False)) for _ in range(3))
+    assert_gemm_close(y[ry], o.gemm_ref(xh[ry], wh))
+    assert_gemm_close(dx[rx], ops["dgrad_dy"][2][rx] @ ops["dgrad_w"][2])
+    assert_gemm_close(dw[rw], ops["wgrad_dy"][2][:, rw].T @ ops["wgrad_x"][2])
+    assert sq.fp8_device_status(True) == 0
