@@ -1009,42 +1009,36 @@ static cudaError_t launch_promote(const GemmArgs& g, const EpiParams& p, cudaStr
 
 // ================================================================== mode 2
 // MX-32 block scaling on the block-scaled tensor-core path
-// (tcgen05.mma kind::mxf8f6f4.block_scale, E8M0 scale factors).  Each stage
-// carries, next to the A and B tiles, the 512-byte scale chunks of its 128
-// rows x 128 K (one per 128 rows of B), copied from global memory by bulk
-// copies (the chunks are contiguous in the tiled scale layout of
-// fp8_quantize) and into tensor memory by tcgen05.cp.32x128b.warpx4.  Every
-// ring stage has its own scale-factor columns, so a stage's columns are
-// rewritten only after the MMAs that read them have completed (their
-// commit released the stage).  MMA j (K = 32 slice j of the stage) selects
-// byte j of each scale word through the descriptor's scale-factor ids.
+// (tcgen05.mma kind::mxf8f6f4.block_scale, E8M0 scale factors).  The ring
+// stages carry only the A and B tiles.  The scale factors reach tensor
+// memory on their own path: a warpgroup of writers (one warp per TMEM lane
+// quarter) reads the 512-byte scale chunks of eight K blocks at a time (one
+// per 128 rows x 128 K of A, and of each 128 rows of B; contiguous in the
+// tiled scale layout of fp8_quantize) from global memory into registers and
+// writes them with tcgen05.st into one of two scale-factor slots, each
+// quarter the same 32 lanes x 4 columns per chunk (the layout the
+// replicating 32x128b.warpx4 copy gives).  A slot is rewritten only after
+// the MMAs that read it have completed (one commit per group), so the MMA
+// queue holds MMAs only and the writers run up to a group ahead.  MMA j
+// (K = 32 slice j of a K block) selects byte j of each scale word through
+// the descriptor's scale-factor ids.
 template <int BN, int STAGES, int NACC>
 struct MxLayout {
     static constexpr int CH = BN / 128;                  // 128-row scale chunks of B
     static constexpr int B_BYTES = BN * BK;
     static constexpr int STAGE = A_BYTES + B_BYTES;
-    static constexpr int SF_STAGE = 512 * (1 + CH);
-    static constexpr int SF_OFF = STAGES * STAGE;
-    static constexpr int BAR_OFF = SF_OFF + STAGES * SF_STAGE;
-    static constexpr int NBARS = 2 * STAGES + 2 * NACC + 1;
+    static constexpr int BAR_OFF = STAGES * STAGE;
+    static constexpr int SFBAR_OFF = BAR_OFF + 256;      // scale-factor slot full[2], empty[2]
     static constexpr int STG_OFF = BAR_OFF + 512;        // epilogue staging, 1 KB per warp
     static constexpr int BYTES = STG_OFF + 8 * kStageBytes + 1024;
+    static constexpr int SF_G = 8;                       // K blocks per scale-factor group
+    static constexpr int SF_KB_COLS = 16;                // TMEM columns per K block: A 4, B 4 per chunk, padding
     static constexpr int SF_COL0 = NACC * BN;            // first scale-factor TMEM column
-    static constexpr int SF_COLS = 4 * (1 + CH);         // per stage
-    static_assert(SF_COL0 + STAGES * SF_COLS <= 512, "tensor memory budget");
+    static constexpr int SF_SLOT_COLS = SF_G * SF_KB_COLS;
+    static_assert(4 * (1 + CH) <= SF_KB_COLS, "scale columns of a K block");
+    static_assert(SF_COL0 + 2 * SF_SLOT_COLS <= 512, "tensor memory budget");
+    static_assert(2 * STAGES + 2 * NACC + 2 <= 32, "barriers below the scale-factor barriers");
 };
-
-// descriptor of a 32-row x 16-byte scale chunk in shared memory (rows
-// contiguous, no swizzle; 8-row groups 128 bytes apart)
-__device__ __forceinline__ uint64_t sdesc_sf_chunk(uint32_t saddr)
-{
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
-    d |= (uint64_t)(128 >> 4) << 16;
-    d |= (uint64_t)(128 >> 4) << 32;
-    d |= (uint64_t)1 << 46;
-    return d;
-}
 
 struct MxParams {
     const uint8_t* sfa;   // tiled E8M0 scales of A
@@ -1053,14 +1047,22 @@ struct MxParams {
     int nchunks_b;        // N / 128
 };
 
-template <int BN, int STAGES, int NACC, bool OUT_BF16, int EPI = 4>
-__global__ void __launch_bounds__(64 + 32 * EPI, 1)
+// warpgroups: 0 producer / MMA (two idle warps), 1-2 epilogue (two warps per
+// lane quarter), 3 scale-factor writers.  Registers are re-split with
+// setmaxnreg: 56 / 184 / 80 of the 128 a thread is launched with.
+constexpr int kMxThreads = 512;
+constexpr int kMxCtlRegs = 56, kMxEpiRegs = 184, kMxSfRegs = 80;
+constexpr int kMxLaunchRegs = (128 * kMxCtlRegs + 256 * kMxEpiRegs + 128 * kMxSfRegs + kMxThreads - 1) / kMxThreads;
+
+template <int BN, int STAGES, int NACC, bool OUT_BF16>
+__global__ void __launch_bounds__(kMxThreads, 1)
     k_gemm_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, EpiParams p,
               uint32_t idesc, TileSched sched, MxParams mx, const __grid_constant__ CUtensorMap tmD)
 {
     pdl_enter();
-    static_assert(EPI <= 8, "staging area holds 8 warps");
+    constexpr int EPI = 8;
     using L = MxLayout<BN, STAGES, NACC>;
+    constexpr int G = L::SF_G;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
@@ -1068,9 +1070,17 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
     uint64_t* afull = empty + STAGES;
     uint64_t* aempty = afull + NACC;
     uint64_t* drain = aempty + NACC;
-    uint8_t* sf_smem = smem + L::SF_OFF;
+    uint64_t* sf_full = reinterpret_cast<uint64_t*>(smem + L::SFBAR_OFF);
+    uint64_t* sf_empty = sf_full + 2;
     constexpr uint32_t TMEM_COLS = 512;
 
+    if (threadIdx.x == 0) {
+        // initialised before gemm_setup's fence and barrier
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&sf_full[s], 4);     // the four writer warps
+            mbar_init(&sf_empty[s], 1);    // the MMA thread's commit
+        }
+    }
     uint32_t tmem_base;
     if (!gemm_setup<STAGES, NACC, EPI>(smem, L::BAR_OFF, TMEM_COLS, &tmA, &tmB, tmem_base)) return;
 
@@ -1078,31 +1088,24 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
     const int num_tiles = sched.num_m * sched.num_n;
     const int nkb = p.K / BK;
 
-    if (warp == 0) {
-        if (lane == 0) {
+    if (warp < 4) {
+        regs_dec<kMxCtlRegs>();
+        if (warp == 0 && lane == 0) {
             int stage = 0, issued = 0;
             uint32_t phase = 0;
             bool aborted = false;
             for (int t = blockIdx.x; t < num_tiles && !aborted; t += gridDim.x) {
                 int mb, nb;
                 sched.coords(t, mb, nb);
-                int nch = mx.nchunks_b - nb * L::CH;
-                nch = nch < L::CH ? nch : L::CH;
-                const uint32_t bytes = L::STAGE + 512u * (uint32_t)(1 + nch);
                 for (int kb = 0; kb < nkb; ++kb) {
                     if (!wait_bounded(&empty[stage], phase ^ 1u)) {
                         aborted = true;
                         break;
                     }
                     uint8_t* sa = smem + stage * L::STAGE;
-                    uint8_t* sf = sf_smem + stage * L::SF_STAGE;
-                    mbar_arrive_expect_tx(&full[stage], bytes);
+                    mbar_arrive_expect_tx(&full[stage], (uint32_t)L::STAGE);
                     tma_load_2d(sa, &tmA, kb * BK, mb * BM, &full[stage]);
                     tma_load_2d(sa + A_BYTES, &tmB, kb * BK, nb * BN, &full[stage]);
-                    bulk_load_1d(sf, mx.sfa + ((int64_t)mb * mx.kb128 + kb) * 512, 512, &full[stage]);
-                    for (int c = 0; c < nch; ++c)
-                        bulk_load_1d(sf + 512 * (1 + c), mx.sfb + ((int64_t)(nb * L::CH + c) * mx.kb128 + kb) * 512,
-                                     512, &full[stage]);
                     ++issued;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -1122,10 +1125,8 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                     wait_drain(&full[s], ph);
                 }
             }
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            int stage = 0, lt = 0;
+        } else if (warp == 1 && lane == 0) {
+            int stage = 0, lt = 0, cw = 0;
             uint32_t phase = 0;
             bool aborted = false;
             for (int t = blockIdx.x; t < num_tiles && !aborted; t += gridDim.x, ++lt) {
@@ -1137,19 +1138,25 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(b * BN);
+                uint32_t sf0 = 0;
                 for (int kb = 0; kb < nkb; ++kb) {
+                    const int j = kb % G;
+                    if (j == 0) {
+                        if (!wait_bounded(&sf_full[cw & 1], (uint32_t)(cw >> 1) & 1u)) {
+                            aborted = true;
+                            break;
+                        }
+                        tc_fence_after();
+                        sf0 = tmem_base + (uint32_t)(L::SF_COL0 + (cw & 1) * L::SF_SLOT_COLS);
+                    }
                     if (!wait_bounded(&full[stage], phase)) {
                         aborted = true;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t sa = smem_addr(smem + stage * L::STAGE);
-                    const uint32_t sf = smem_addr(sf_smem + stage * L::SF_STAGE);
-                    const uint32_t sfa_t = tmem_base + (uint32_t)(L::SF_COL0 + stage * L::SF_COLS);
+                    const uint32_t sfa_t = sf0 + (uint32_t)(j * L::SF_KB_COLS);
                     const uint32_t sfb_t = sfa_t + 4;
-                    tmem_cp_32x128b_warpx4(sfa_t, sdesc_sf_chunk(sf));
-#pragma unroll
-                    for (int c = 0; c < L::CH; ++c) tmem_cp_32x128b_warpx4(sfb_t + 4 * c, sdesc_sf_chunk(sf + 512 * (1 + c)));
                     const uint64_t da = sdesc_kmajor_sw128(sa);
                     const uint64_t db = sdesc_kmajor_sw128(sa + A_BYTES);
 #pragma unroll
@@ -1157,6 +1164,10 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                         mma_mxf8f6f4(d, da + 2 * k, db + 2 * k, idesc | ((uint32_t)k << 29) | ((uint32_t)k << 4),
                                      sfa_t, sfb_t, (kb | k) != 0 ? 1u : 0u);
                     mma_commit(&empty[stage]);
+                    if (j == G - 1 || kb == nkb - 1) {
+                        mma_commit(&sf_empty[cw & 1]);   // the group's MMAs have read its slot
+                        ++cw;
+                    }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -1169,13 +1180,13 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
                 wait_drain(drain, 0);
             }
         }
-    } else {
-        // EPI / 4 warps per TMEM lane quarter split the BN columns
-        constexpr int PARTS = EPI / 4;
-        constexpr int COLS = BN / PARTS;
+    } else if (warp < 12) {
+        regs_inc<kMxEpiRegs>();
+        // two warps per TMEM lane quarter split the BN columns
+        constexpr int COLS = BN / 2;
         const int quarter = warp & 3;
-        const int part = (warp - 2) >> 2;
-        uint8_t* stg = smem + L::STG_OFF + (warp - 2) * kStageBytes;
+        const int part = (warp - 4) >> 2;
+        uint8_t* stg = smem + L::STG_OFF + (warp - 4) * kStageBytes;
         constexpr int SC = OUT_BF16 ? 16 : 8;
         int lt = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++lt) {
@@ -1216,6 +1227,66 @@ __global__ void __launch_bounds__(64 + 32 * EPI, 1)
             }
         }
         stage_store_drain(lane);
+    } else {
+        regs_dec<kMxSfRegs>();
+        // scale-factor writers: warp (12 + q) fills lane quarter q of every
+        // group's slot, four K blocks per round of loads
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const int cpt = (nkb + G - 1) / G;                   // groups per tile
+        int wi = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            int mb, nb;
+            sched.coords(t, mb, nb);
+            int nch = mx.nchunks_b - nb * L::CH;
+            nch = nch < L::CH ? nch : L::CH;
+            for (int g = 0; g < cpt; ++g, ++wi) {
+                const int slot = wi & 1;
+                const bool okw = wait_bounded(&sf_empty[slot], ((uint32_t)(wi >> 1) & 1u) ^ 1u);
+                if (!__all_sync(0xFFFFFFFFu, okw)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t col0 = tmem_base + lane_base + (uint32_t)(L::SF_COL0 + slot * L::SF_SLOT_COLS);
+#pragma unroll
+                for (int h = 0; h < G / 4; ++h) {
+                    uint32_t r[4][16];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int kb = g * G + h * 4 + i;
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) r[i][c] = 0u;
+                        if (kb < nkb) {
+                            const uint4 a = __ldg(reinterpret_cast<const uint4*>(
+                                mx.sfa + ((int64_t)mb * mx.kb128 + kb) * 512 + 16 * lane));
+                            r[i][0] = a.x;
+                            r[i][1] = a.y;
+                            r[i][2] = a.z;
+                            r[i][3] = a.w;
+#pragma unroll
+                            for (int c = 0; c < L::CH; ++c)
+                                if (c < nch) {
+                                    const uint4 q = __ldg(reinterpret_cast<const uint4*>(
+                                        mx.sfb + ((int64_t)(nb * L::CH + c) * mx.kb128 + kb) * 512 + 16 * lane));
+                                    r[i][4 + 4 * c] = q.x;
+                                    r[i][5 + 4 * c] = q.y;
+                                    r[i][6 + 4 * c] = q.z;
+                                    r[i][7 + 4 * c] = q.w;
+                                }
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (g * G + h * 4 + i < nkb)
+                            tmem_st_32x32b_x16(col0 + (uint32_t)((h * 4 + i) * L::SF_KB_COLS), r[i]);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sf_full[slot]);
+            }
+        }
     }
     __syncthreads();
     if (warp == 1) {
@@ -1515,11 +1586,17 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
         MxParams mx{static_cast<const uint8_t*>(g.a_scale), static_cast<const uint8_t*>(g.b_scale), (int)(g.K / 128),
                     (int)(g.N / 128)};
         const uint32_t idesc = make_idesc_mx(g.a_format, g.b_format, BN);
-        // one accumulator (the scale factors take the other TMEM columns), so
-        // eight epilogue warps drain it in half the time of four
-        constexpr int EPI = 8;
-        auto kern = bf16 ? k_gemm_mx<BN, ST, NACC, true, EPI> : k_gemm_mx<BN, ST, NACC, false, EPI>;
-        cudaError_t e = smem_attr_once(reinterpret_cast<const void*>(kern), L::BYTES);
+        auto kern = bf16 ? k_gemm_mx<BN, ST, NACC, true> : k_gemm_mx<BN, ST, NACC, false>;
+        // the warpgroups' setmaxnreg shares must fit in what the CTA is
+        // launched with, or the raising warpgroup would wait forever
+        int regs = 0;
+        cudaError_t e = launch_regs(reinterpret_cast<const void*>(kern), &regs);
+        if (e != cudaSuccess) return e;
+        if (regs < kMxLaunchRegs) {
+            *why = "MX kernel compiled with fewer registers than its warpgroup split needs";
+            return cudaErrorInvalidConfiguration;
+        }
+        e = smem_attr_once(reinterpret_cast<const void*>(kern), L::BYTES);
         if (e != cudaSuccess) return e;
         CUtensorMap td;
         if (!make_tmap_out(&td, g.D, g.M, g.N, bf16)) {
@@ -1528,7 +1605,7 @@ cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t st, int sms, const char*
         }
         const int grid = tiles < sms ? tiles : sms;
         sched.group = raster_group(g.K, BM, BN, grid);
-        launch_k(kern, grid, 64 + 32 * EPI, L::BYTES, st, ta, tb, p, idesc, sched, mx, td);
+        launch_k(kern, grid, kMxThreads, L::BYTES, st, ta, tb, p, idesc, sched, mx, td);
         return cudaGetLastError();
     }
     *why = "GEMM mode not built";
