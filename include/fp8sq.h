@@ -422,7 +422,10 @@ FP8SQ_API int fp8_linear_fwd_noalloc(const void* x, const void* w, int64_t M, in
  *   cleared.
  * fp8_last_error: message for the calling thread's last non-zero status
  *   (static thread-local storage; never NULL).
- * fp8_abi_version: 6.  Changes from 5: fp8_gemm_cast added (the GEMM's
+ * fp8_abi_version: 7.  Changes from 6: fp8_linear_fwd / fp8_linear_bwd,
+ *   fp8_linear_workspace_bytes and fp8_quantize_rows_cols accept
+ *   TILE_1x128_POW2 (the fine-grained units with power-of-two scales).
+ *   Changes from 5 to 6: fp8_gemm_cast added (the GEMM's
  *   epilogue casts its bf16 output to FP8 with delayed scaling).
  *   Changes from 4 to 5: fp8_gemm_layout added (MN-major
  *   operands); the per-tensor linear layer keeps no transposed codes (its

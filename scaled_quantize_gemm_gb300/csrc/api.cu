@@ -207,7 +207,7 @@ int api_check_device(int* sms) { return check_device(sms); }
 
 extern "C" {
 
-FP8SQ_API int fp8_abi_version(void) { return 6; }
+FP8SQ_API int fp8_abi_version(void) { return 7; }
 
 FP8SQ_API const char* fp8_last_error(void) { return g_msg; }
 

@@ -22,7 +22,7 @@ def test_exports_every_declared_symbol(L):
                           "fp8_scale_init", "fp8_linear_workspace_bytes", "fp8_device_status"}
     for n in names:
         assert hasattr(L, n), n
-    assert L.fp8_abi_version() == 6
+    assert L.fp8_abi_version() == 7
 
 
 def test_null_and_enum_validation(L):
