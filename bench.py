@@ -65,8 +65,8 @@ KERNEL_SOURCES = {   # file, [(start marker or None = file start, end marker)]: 
                                       ("            int g = delayed ? flat_grid(", "        return cudaGetLastError();")]),
 }
 TRAFFIC = {
-    "k_gemm_tensor_pair": {"sha": "15529b129fb3a50e", "bytes": 669804544},
-    "k_cast_tensor": {"sha": "9ca10da12c8e431d", "bytes": 143839232},
+    "k_gemm_tensor_pair": {"sha": "db87dc145773aece", "bytes": 665896448},
+    "k_cast_tensor": {"sha": "4156e299acff17f4", "bytes": 144140800},
 }
 
 
