@@ -720,10 +720,13 @@ def per_config(device, with_oracle: bool = True) -> dict:
     W2 = wl.WORKLOADS[2]
     lay = []
     flops2 = 0
+    # the nine delayed states (x, W, dy of each linear) in one buffer, so the
+    # step ends with one scale update for all of them
+    states2 = torch.empty(3 * len(W2.linears) * (H + 2), **f32)
+    sq.fp8_scale_init(states2, 3 * len(W2.linears), H)
     for li, lin in enumerate(W2.linears):
         M, K, N = W2.tokens, lin.in_features, lin.out_features
-        st = torch.empty(3 * (H + 2), **f32)
-        sq.fp8_scale_init(st, 3, H)
+        st = states2[3 * li * (H + 2):3 * (li + 1) * (H + 2)]
         lay.append(dict(M=M, K=K, N=N, x=wl.linear_x(2, li, 0, M, K, device), w=wl.linear_w(2, li, N, K, device),
                         dy=wl.linear_dy(2, li, 0, M, N, device), st=st,
                         ws=torch.empty(sq.fp8_linear_workspace_bytes(M, N, K), **u8),
@@ -738,10 +741,10 @@ def per_config(device, with_oracle: bool = True) -> dict:
             s_ = [L["st"][i * (H + 2):(i + 1) * (H + 2)] for i in range(3)]
             sq.fp8_linear_fwd(L["x"], L["w"], L["y"], L["ws"], x_state=s_[0], w_state=s_[1], history_len=H)
             sq.fp8_linear_bwd(L["dy"], L["dx"], L["dw"], L["ws"], L["K"], dy_state=s_[2], history_len=H)
-            sq.fp8_update_scale(L["st"], 3, H, fm2)
+        sq.fp8_update_scale(states2, 3 * len(lay), H, fm2 * len(lay))
     row = gemm_row(_time_flushed(step2, flush), flops2,
-                   {"what": "one training step of the three linears (fwd + dgrad + wgrad + scale update, "
-                            "delayed HYBRID), eager calls"})
+                   {"what": "one training step of the three linears (fwd + dgrad + wgrad of each, one scale "
+                            "update of all nine states, delayed HYBRID), eager calls"})
     # the same step captured once and replayed from a CUDA graph: the device
     # time without the host's per-call cost (the path does not synchronise
     # or allocate, so it captures as is)

@@ -587,6 +587,9 @@ __device__ __forceinline__ int64_t mx_tiled_offset(int64_t r, int64_t t, int64_t
 // (64 registers; 128-row column tiles at three, 80 registers, took 131.5
 // against 117.3 us), except MX-32 rows + columns, three (80 registers; at
 // four they spill).
+// POW2 (UNIT = 128): power-of-two tiles by the MX rule; each tile's E8M0
+// code fills the four 32-blocks it covers in the tiled layouts (rows: of x,
+// columns: of x^T), the layouts the block-scaled GEMM reads.
 template <int FMT, int UNIT, bool ROWQ = false, bool POW2 = false>
 __global__ void __launch_bounds__(256, UNIT == 32 && ROWQ ? 3 : 4) k_quant_col_block(const void* __restrict__ x, int64_t R, int64_t C,
                                                          uint8_t* __restrict__ q, uint8_t* __restrict__ qT,
