@@ -80,3 +80,53 @@ def test_linear_step_graph_replay_matches_eager(M, K, N):
         assert torch.equal(g_step.dw, dw), s
         assert np.array_equal(g_step.states.cpu().numpy().view(np.uint32), st.cpu().numpy().view(np.uint32)), s
     assert sq.fp8_device_status(True) == sq.OK
+
+
+@pytest.mark.parametrize("gran", [sq.TILE_1x128, sq.TILE_1x128_POW2, sq.MX32])
+def test_fine_grained_linear_graph_replay_matches_eager(gran):
+    """The fine-grained recipes (current scaling per unit, fp32 or
+    power-of-two tile scales, MX-32) captured once: replays on fresh inputs
+    give bit-identical y, dx and dW to eager calls."""
+    M, K, N = 256, 384, 512
+    steps = 3
+    ws = torch.empty(sq.fp8_linear_workspace_bytes(M, N, K, gran), dtype=torch.uint8, device=DEV)
+    x = torch.empty((M, K), dtype=torch.bfloat16, device=DEV)
+    w = torch.empty((N, K), dtype=torch.bfloat16, device=DEV)
+    dy = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device=DEV)
+    dw = torch.empty((N, K), dtype=torch.float32, device=DEV)
+
+    def run():
+        sq.fp8_linear_fwd(x, w, y, ws, gran=gran)
+        sq.fp8_linear_bwd(dy, dx, dw, ws, K, gran=gran)
+
+    def inputs(s):
+        return (wl.student_t3((M, K), 600 + s, DEV), wl.normal((N, K), 0.02, 700 + s, DEV),
+                wl.normal((M, N), 1e-3, 800 + s, DEV))
+
+    outs = []
+    for s in range(steps):
+        a, b, c = inputs(s)
+        x.copy_(a); w.copy_(b); dy.copy_(c)
+        run()
+        outs.append((y.clone(), dx.clone(), dw.clone()))
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):          # first calls (one-time queries) outside the capture
+        run()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run()
+    for s in range(steps):
+        a, b, c = inputs(s)
+        x.copy_(a); w.copy_(b); dy.copy_(c)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y, outs[s][0]), s
+        assert torch.equal(dx, outs[s][1]), s
+        assert torch.equal(dw, outs[s][2]), s
+    assert sq.fp8_device_status(True) == sq.OK
