@@ -58,7 +58,7 @@ def test_every_bf16_pattern_every_multiplier(fmt, m):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
-@pytest.mark.parametrize("shape", [(256, 256), (1000, 37), (1, 5), (3, 1024)])
+@pytest.mark.parametrize("shape", [(256, 256), (1000, 37), (1, 5), (3, 1024), (513, 256), (1024, 1031)])
 def test_tensor_current(fmt, shape):
     a, _ = wl.w1_operands()
     x = torch.randn(shape, generator=torch.Generator().manual_seed(sum(shape)), dtype=torch.float32)
@@ -72,7 +72,11 @@ def test_tensor_current(fmt, shape):
     torch.cuda.synchronize()
     rq, ra, rs, rsat = o.quantize_tensor_current(x.numpy(), fmt)
     assert np.array_equal(codes(q), rq)
-    assert amax.item() == ra and s.item() == rs and int(sat.item()) == rsat == 0
+    # amax * fp32(fmax / amax) can round one ulp above fmax, so current
+    # scaling may saturate the elements equal to the amax (and only those):
+    # the same count on both sides
+    assert amax.item() == ra and s.item() == rs and int(sat.item()) == rsat
+    assert rsat <= int(np.sum(np.abs(x.numpy()) == ra))
 
 
 @pytest.mark.parametrize("fmt", FMTS)
