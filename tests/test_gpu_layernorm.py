@@ -143,9 +143,16 @@ def test_layernorm_linear_forward_and_backward():
         assert np.all(np.abs(gx[:H][nz] / ref_x[:H][nz] - 1.0) <= 1e-5), step
 
 
+def _random_ln_shapes(seed, n):
+    """seeded (rows, width) pairs, both multiples of 16, widths up to 6000"""
+    rng = np.random.default_rng(seed)
+    return [(int(rng.integers(1, 129)) * 16, int(rng.integers(1, 376)) * 16, bool(i % 2)) for i in range(n)]
+
+
 @pytest.mark.parametrize("fmt", [sq.E4M3, sq.E5M2])
 @pytest.mark.parametrize("M,K,with_beta", [(272, 144, True), (4096, 4096, True), (2064, 1040, False),
-                                           (64, 4112, True), (48, 16, True), (32, 2064, False)])
+                                           (64, 4112, True), (48, 16, True), (32, 2064, False)]
+                         + _random_ln_shapes(5, 4))
 def test_layernorm_single_pass_matches_two_pass(fmt, M, K, with_beta):
     """Without a transposed copy the LayerNorm cast runs in one pass (each
     row held in registers from the statistics to the codes, rows of up to
