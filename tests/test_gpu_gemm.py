@@ -406,7 +406,7 @@ def test_pow2_tiles_blocks_on_block_scaled_mma(M, N, K):
 # ---------------------------------------------------------------- MN-major operands
 @pytest.mark.parametrize("a_mn,b_mn", [(False, True), (True, False), (True, True)])
 @pytest.mark.parametrize("M,N,K,with_bias", [(256, 384, 512, False), (272, 400, 144, True), (128, 128, 16, False),
-                                             (528, 256, 1040, True)])
+                                             (528, 256, 1040, True), (720, 592, 1328, True), (96, 1008, 416, False)])
 @pytest.mark.parametrize("out", [torch.float32, torch.bfloat16])
 def test_mn_major_operands(a_mn, b_mn, M, N, K, with_bias, out):
     """fp8_gemm_layout with A stored [K][M] and/or B stored [K][N]: bit-identical
@@ -455,13 +455,14 @@ def test_mn_major_rejects_unaligned_rows():
 
 # ---------------------------------------------------------------- GEMM with the output cast fused
 @pytest.mark.parametrize("a_mn,b_mn", [(False, False), (False, True), (True, True)])
-@pytest.mark.parametrize("M,N,K,with_bias", [(256, 384, 512, False), (272, 400, 144, True), (528, 256, 1040, True)])
+@pytest.mark.parametrize("M,N,K,with_bias", [(256, 384, 512, False), (272, 400, 144, True), (528, 256, 1040, True)]
+                         + [(432, 896, 1488, False), (304, 128, 928, True), (688, 800, 992, False)])
 @pytest.mark.parametrize("qfmt", [sq.E4M3, sq.E5M2])
 def test_gemm_cast_equals_gemm_then_cast(a_mn, b_mn, M, N, K, with_bias, qfmt):
     """fp8_gemm_cast: D bit-identical to fp8_gemm_layout's, the codes and the
     delayed state bit-identical to fp8_quantize (TENSOR, delayed) of that D
     run afterwards -- including a ragged M with bias, whose rows past M must
-    not enter the amax."""
+    not enter the amax (the last three shapes: seeded random draws)."""
     H = 16
     a = wl.normal((M, K), 1.0, 141 + M, dtype=torch.float32)
     b = wl.normal((N, K), 1.0, 142 + N, dtype=torch.float32)
