@@ -48,7 +48,7 @@ def _oracle_step(ref, x, w, dy, rows=None, wrows=None, dy_fmt=o.E5M2):
     return Y, dX, dW
 
 
-@pytest.mark.parametrize("M,K,N", [(256, 384, 512), (128, 128, 128), (272, 144, 400)])
+@pytest.mark.parametrize("M,K,N", [(256, 384, 512), (128, 128, 128), (272, 144, 400), (848, 1232, 688), (64, 2048, 96)])
 def test_delayed_hybrid_steps(M, K, N):
     L = Layer(M, K, N)
     ref = [o.state_init(16) for _ in range(3)]

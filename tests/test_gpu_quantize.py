@@ -384,7 +384,7 @@ def test_pow2_tiles_blocks_and_floor_mx(fmt):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
-@pytest.mark.parametrize("shape", [(256, 384), (128, 128), (384, 256)])
+@pytest.mark.parametrize("shape", [(256, 384), (128, 128), (384, 256), (640, 1152), (1152, 512)])
 def test_rows_cols_pow2_tiles(fmt, shape):
     """Power-of-two 1x128 row tiles and 128x1 column tiles in one pass: codes
     bit-exact against the oracle's power-of-two quantisers; each tile's E8M0
@@ -411,7 +411,7 @@ def test_rows_cols_pow2_tiles(fmt, shape):
 
 @pytest.mark.parametrize("unit", [sq.TILE_1x128, sq.MX32_TILED])
 @pytest.mark.parametrize("fmt", FMTS)
-@pytest.mark.parametrize("shape", [(256, 384), (128, 128), (384, 256)])
+@pytest.mark.parametrize("shape", [(256, 384), (128, 128), (384, 256), (640, 1152), (1152, 512)])
 def test_rows_cols_one_pass(unit, fmt, shape):
     """fp8_quantize_rows_cols gives bit-identical results to the two separate
     casts (row units into q, column units into qT), and matches the oracle's
