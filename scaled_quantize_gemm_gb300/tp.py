@@ -39,6 +39,15 @@ M (rank r owns rows [r M/P, (r+1) M/P) of x and dy):
             dW = sum_r dy_r^T x_r (the local products all-reduced, sum)
   step end  the amax all-reduce (max): x and dy are sharded, W identical.
 
+The data-parallel linear also runs the fine-grained recipes (FineOps:
+current scaling per 1x128 tile / 128x128 block, with fp32 or power-of-two
+scales, or per MX-32 block).  Every unit lies inside one rank's rows (1x128
+tiles and MX blocks along a row; wgrad's 128-row column tiles and 32-row
+column blocks inside the rank's M_local rows, a multiple of 128) or is the
+same on every rank (W's blocks), so each rank computes exactly the scales and
+codes of the full-batch layer and there is no amax to exchange; dW is summed
+as above.
+
 The exchange steps are torch.distributed collectives on the given process
 group; the arithmetic of each rank runs in `ops`.  The default `ops`
 (LibraryOps) is this library's CUDA path through the C ABI; a caller may
@@ -155,6 +164,45 @@ class LibraryOps:
         self.sq.fp8_update_scale(self.states, 3, self.H, self.formats)
 
 
+class FineOps:
+    """Per-rank arithmetic of a data-parallel linear under a fine-grained
+    recipe (gran TILE_1x128, TILE_1x128_POW2 or MX32; current scaling per
+    unit) through fp8_linear_fwd / fp8_linear_bwd: y and dx bf16, dW fp32.
+    There is no delayed state, so nothing is recorded or exchanged at the
+    step's end."""
+
+    def __init__(self, M: int, N: int, K: int, gran: int, device, recipe_e4m3: bool = False):
+        import scaled_quantize_gemm_gb300 as sq
+        self.sq = sq
+        self.M, self.N, self.K, self.gran = M, N, K, gran
+        self.recipe = sq.RECIPE_E4M3 if recipe_e4m3 else sq.RECIPE_HYBRID
+        nbytes = sq.fp8_linear_workspace_bytes(M, N, K, gran)
+        if nbytes == 0:
+            raise ValueError(f"granularity {gran} is not a linear-layer recipe")
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+    def forward(self, x: torch.Tensor, w: torch.Tensor, out_dtype=torch.bfloat16) -> torch.Tensor:
+        y = torch.empty((self.M, self.N), dtype=out_dtype, device=x.device)
+        self.sq.fp8_linear_fwd(x, w, y, self.ws, gran=self.gran, recipe=self.recipe)
+        return y
+
+    def backward(self, dy: torch.Tensor):
+        """-> (dx bf16 [M][K], dW fp32 [N][K])"""
+        dx = torch.empty((self.M, self.K), dtype=torch.bfloat16, device=dy.device)
+        dw = torch.empty((self.N, self.K), dtype=torch.float32, device=dy.device)
+        self.sq.fp8_linear_bwd(dy, dx, dw, self.ws, self.K, gran=self.gran, recipe=self.recipe)
+        return dx, dw
+
+    def recorded_amax(self) -> torch.Tensor:
+        return torch.zeros(0, dtype=torch.float32, device=self.ws.device)
+
+    def set_recorded_amax(self, a: torch.Tensor) -> None:
+        pass
+
+    def update_scale(self) -> None:
+        pass
+
+
 class ColumnParallelFP8Linear:
     """One column-parallel FP8 linear of a TP group (see the module text).
 
@@ -244,17 +292,20 @@ class RowParallelFP8Linear:
 class DataParallelFP8Linear:
     """One data-parallel FP8 linear (see the module text): every rank holds
     all of W [N][K] and its own M_local rows of the batch.  `ops` defaults to
-    LibraryOps on w's device (its M is the local batch)."""
+    LibraryOps on w's device (its M is the local batch), or FineOps when a
+    fine-grained `gran` is given."""
 
     def __init__(self, w: torch.Tensor, M_local: int, history_len: int = 16, group=None, ops=None,
-                 recipe_e4m3: bool = False):
+                 recipe_e4m3: bool = False, gran: int = 0):
         self.group = group
         self.world = dist.get_world_size(group)
         self.rank = dist.get_rank(group)
         self.w = w
         self.N, self.K = w.shape
-        self.ops = ops if ops is not None else LibraryOps(M_local, self.N, self.K, history_len, w.device,
-                                                          recipe_e4m3)
+        if ops is None:
+            ops = (LibraryOps(M_local, self.N, self.K, history_len, w.device, recipe_e4m3) if gran == 0
+                   else FineOps(M_local, self.N, self.K, gran, w.device, recipe_e4m3))
+        self.ops = ops
 
     def forward(self, x_local: torch.Tensor) -> torch.Tensor:
         """y_local [M_local][N] (bf16 on the library path); no exchange."""
@@ -270,8 +321,10 @@ class DataParallelFP8Linear:
 
     def end_step(self) -> None:
         """All-reduce (max) the amaxes the step recorded, then update the
-        scales: every rank ends the step with the same x, W and dy states."""
+        scales: every rank ends the step with the same x, W and dy states
+        (a fine-grained recipe records none)."""
         a = self.ops.recorded_amax()
-        dist.all_reduce(a, op=dist.ReduceOp.MAX, group=self.group)
-        self.ops.set_recorded_amax(a)
+        if a.numel():
+            dist.all_reduce(a, op=dist.ReduceOp.MAX, group=self.group)
+            self.ops.set_recorded_amax(a)
         self.ops.update_scale()

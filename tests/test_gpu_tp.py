@@ -94,3 +94,36 @@ def test_row_parallel_linear_one_rank_matches_oracle():
         assert sq.fp8_device_status(True) == 0
     finally:
         dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("gran,og", [(sq.TILE_1x128, o.GRAN_TILE_1x128), (sq.TILE_1x128_POW2, o.GRAN_TILE_POW2),
+                                     (sq.MX32, o.GRAN_MX32)])
+def test_data_parallel_fine_grained_one_rank_matches_oracle(gran, og):
+    """The data-parallel linear's per-rank path under a fine-grained recipe
+    (FineOps: fp8_linear_fwd / fp8_linear_bwd) in a group of one rank on
+    NCCL: y, dx and the all-reduced dW against the oracle."""
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1,
+                            timeout=datetime.timedelta(seconds=120), device_id=torch.device(DEV, 0))
+    try:
+        M, K, N = 256, 384, 512
+        w = wl.normal((N, K), 0.02, 191).to(DEV)
+        layer = tp.DataParallelFP8Linear(w, M, gran=gran)
+        assert isinstance(layer.ops, tp.FineOps)
+        for step in range(2):
+            x = wl.student_t3((M, K), 192 + step).to(DEV)
+            dy = wl.normal((M, N), 1e-3, 196 + step).to(DEV)
+            y = layer.forward(x)
+            dx, dw = layer.backward(dy)
+            layer.end_step()
+            torch.cuda.synchronize()
+            st, Y = o.linear_fine_fwd(np32(x), np32(w), og)
+            dX, dW = o.linear_fine_bwd(st, np32(dy), og, o.E5M2)
+            assert_gemm_close(y, Y)
+            assert_gemm_close(dx, dX)
+            assert_gemm_close(dw, dW)
+        assert sq.fp8_device_status(True) == 0
+    finally:
+        dist.destroy_process_group()

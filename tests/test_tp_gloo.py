@@ -15,6 +15,7 @@ import socket
 import sys
 
 import numpy as np
+import pytest
 import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
@@ -386,3 +387,104 @@ def test_data_parallel_matches_unsharded_layer():
 def test_data_parallel_without_amax_allreduce_diverges():
     res = _dp_run(sync=False)
     assert res[0][1][3] != res[1][1][3]
+
+
+# ---------------------------------------------------------------- data-parallel, fine-grained recipes
+class OracleFineOps:
+    """The per-rank operations of a data-parallel linear under a
+    fine-grained recipe on the CPU oracle (current scaling per unit, float64
+    products of the dequantised operands); no delayed state."""
+
+    def __init__(self, gran):
+        import oracle as o
+        self.o, self.gran = o, gran
+
+    def forward(self, x, w):
+        self.st, r = self.o.linear_fine_fwd(x.numpy(), w.numpy(), self.gran)
+        return torch.from_numpy(r)
+
+    def backward(self, dy):
+        dX, dW = self.o.linear_fine_bwd(self.st, dy.numpy(), self.gran, self.o.E5M2)
+        return torch.from_numpy(dX), torch.from_numpy(dW)
+
+    def recorded_amax(self):
+        return torch.zeros(0, dtype=torch.float32)
+
+    def set_recorded_amax(self, a):
+        pass
+
+    def update_scale(self):
+        pass
+
+
+FM, FK, FN = 256, 384, 256      # fine-grained units need multiples of 128 (128 batch rows per rank)
+
+
+def _fine_inputs(step):
+    g = torch.Generator().manual_seed(50 + step)
+    x = (torch.randn((FM, FK), generator=g) * (1.0 + step)).to(torch.bfloat16).float()
+    x[FM - 3, 17] = 90.0 * (step + 1)            # an outlier in the second rank's rows
+    dy = (torch.randn((FM, FN), generator=g) * 1e-3).to(torch.bfloat16).float()
+    w = (torch.randn((FN, FK), generator=torch.Generator().manual_seed(51)) * 0.02).to(torch.bfloat16).float()
+    return x, w, dy
+
+
+def _fine_dp_worker(rank, ws, port, gran, out):
+    try:
+        os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        sys.path.insert(0, ROOT)
+        from scaled_quantize_gemm_gb300 import tp
+        dist.init_process_group("gloo", rank=rank, world_size=ws, timeout=__import__("datetime").timedelta(seconds=60))
+        try:
+            rows = slice(rank * (FM // ws), (rank + 1) * (FM // ws))
+            rec = []
+            for step in range(2):
+                x, w, dy = _fine_inputs(step)
+                layer = tp.DataParallelFP8Linear(w, FM // ws, ops=OracleFineOps(gran))
+                y = layer.forward(x[rows].contiguous())
+                dx, dw = layer.backward(dy[rows].contiguous())
+                layer.end_step()
+                rec.append((y.numpy(), dx.numpy(), dw.numpy().copy()))
+            out.put((rank, rec))
+        finally:
+            dist.destroy_process_group()
+    except BaseException as e:
+        import traceback
+        out.put((rank, "error: " + "".join(traceback.format_exception(e))))
+        raise
+
+
+@pytest.mark.parametrize("gran_name", ["GRAN_TILE_1x128", "GRAN_TILE_POW2", "GRAN_MX32"])
+def test_data_parallel_fine_grained_matches_full_batch(gran_name):
+    """Data-parallel under the fine-grained recipes: each rank's output and
+    input-gradient rows and the summed weight gradient equal the full-batch
+    layer's (every quantisation unit lies inside one rank's rows or is the
+    same on every rank, so the codes and scales are the full batch's)."""
+    import oracle as o
+    gran = getattr(o, gran_name)
+    ctx = mp.get_context("spawn")
+    out = ctx.Queue()
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    procs = [ctx.Process(target=_fine_dp_worker, args=(r, 2, port, gran, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = {}
+    for _ in range(2):
+        rank, rec = out.get(timeout=180)
+        assert not isinstance(rec, str), rec
+        res[rank] = rec
+    for p in procs:
+        p.join(60)
+    assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+    half = FM // 2
+    for step in range(2):
+        x, w, dy = _fine_inputs(step)
+        st, Y = o.linear_fine_fwd(x.numpy(), w.numpy(), gran)
+        dX, dW = o.linear_fine_bwd(st, dy.numpy(), gran, o.E5M2)
+        for rank in range(2):
+            y, dx, dw = res[rank][step]
+            assert np.array_equal(y, Y[rank * half:(rank + 1) * half]), (step, rank)
+            assert np.array_equal(dx, dX[rank * half:(rank + 1) * half]), (step, rank)
+            assert _close(dw, dW), (step, rank)
