@@ -39,14 +39,17 @@ M (rank r owns rows [r M/P, (r+1) M/P) of x and dy):
             dW = sum_r dy_r^T x_r (the local products all-reduced, sum)
   step end  the amax all-reduce (max): x and dy are sharded, W identical.
 
-The data-parallel linear also runs the fine-grained recipes (FineOps:
+The data-parallel and row-parallel linears also run the fine-grained
+recipes (FineOps:
 current scaling per 1x128 tile / 128x128 block, with fp32 or power-of-two
 scales, or per MX-32 block).  Every unit lies inside one rank's rows (1x128
 tiles and MX blocks along a row; wgrad's 128-row column tiles and 32-row
 column blocks inside the rank's M_local rows, a multiple of 128) or is the
 same on every rank (W's blocks), so each rank computes exactly the scales and
 codes of the full-batch layer and there is no amax to exchange; dW is summed
-as above.
+as above.  Row-parallel likewise, with K/P a multiple of 128 (x's tiles and
+W's blocks inside one rank's columns, dy the same everywhere); the fp32
+partial outputs are summed as above.
 
 The exchange steps are torch.distributed collectives on the given process
 group; the arithmetic of each rank runs in `ops`.  The default `ops`
@@ -186,6 +189,11 @@ class FineOps:
         self.sq.fp8_linear_fwd(x, w, y, self.ws, gran=self.gran, recipe=self.recipe)
         return y
 
+    def forward_partial(self, x_local: torch.Tensor, w_local: torch.Tensor) -> torch.Tensor:
+        """The rank's partial output of a row-parallel linear, fp32 (summed
+        across the group afterwards)."""
+        return self.forward(x_local, w_local, out_dtype=torch.float32)
+
     def backward(self, dy: torch.Tensor):
         """-> (dx bf16 [M][K], dW fp32 [N][K])"""
         dx = torch.empty((self.M, self.K), dtype=torch.bfloat16, device=dy.device)
@@ -253,10 +261,13 @@ class RowParallelFP8Linear:
 
     w_local: this rank's columns of W ([N][K/P]); the forward takes this
     rank's columns of x ([M][K/P]).  `ops` defaults to LibraryOps on
-    w_local's device (its N is the full N, its K the local K/P)."""
+    w_local's device (its N is the full N, its K the local K/P), or FineOps
+    when a fine-grained `gran` is given (K/P a multiple of 128: every 1x128
+    tile of x and 128x128 block of W then lies inside one rank's columns, and
+    dy's units are the same on every rank)."""
 
     def __init__(self, w_local: torch.Tensor, M: int, history_len: int = 16, group=None, ops=None,
-                 recipe_e4m3: bool = False):
+                 recipe_e4m3: bool = False, gran: int = 0):
         self.group = group
         self.world = dist.get_world_size(group)
         self.rank = dist.get_rank(group)
@@ -264,8 +275,10 @@ class RowParallelFP8Linear:
         self.M = M
         self.N, self.K_local = w_local.shape
         self.K = self.K_local * self.world
-        self.ops = ops if ops is not None else LibraryOps(M, self.N, self.K_local, history_len, w_local.device,
-                                                          recipe_e4m3)
+        if ops is None:
+            ops = (LibraryOps(M, self.N, self.K_local, history_len, w_local.device, recipe_e4m3) if gran == 0
+                   else FineOps(M, self.N, self.K_local, gran, w_local.device, recipe_e4m3))
+        self.ops = ops
 
     def forward(self, x_local: torch.Tensor, async_op: bool = False):
         """The rank's partial product, then an all-reduce (sum) of it: y
@@ -277,15 +290,18 @@ class RowParallelFP8Linear:
 
     def backward(self, dy: torch.Tensor):
         """dy: the full output gradient [M][N] (the same on every rank).
-        Returns (dx_local fp32 [M][K/P], dW_local fp32 [N][K/P]); no exchange."""
+        Returns (dx_local [M][K/P], fp32 under the per-tensor recipe, bf16
+        under a fine-grained one; dW_local fp32 [N][K/P]); no exchange."""
         return self.ops.backward(dy)
 
     def end_step(self) -> None:
         """All-reduce (max) the amaxes the step recorded, then update the
-        scales: every rank ends the step with the same x, W and dy states."""
+        scales: every rank ends the step with the same x, W and dy states
+        (a fine-grained recipe records none)."""
         a = self.ops.recorded_amax()
-        dist.all_reduce(a, op=dist.ReduceOp.MAX, group=self.group)
-        self.ops.set_recorded_amax(a)
+        if a.numel():
+            dist.all_reduce(a, op=dist.ReduceOp.MAX, group=self.group)
+            self.ops.set_recorded_amax(a)
         self.ops.update_scale()
 
 

@@ -127,3 +127,38 @@ def test_data_parallel_fine_grained_one_rank_matches_oracle(gran, og):
         assert sq.fp8_device_status(True) == 0
     finally:
         dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("gran,og", [(sq.TILE_1x128, o.GRAN_TILE_1x128), (sq.TILE_1x128_POW2, o.GRAN_TILE_POW2),
+                                     (sq.MX32, o.GRAN_MX32)])
+def test_row_parallel_fine_grained_one_rank_matches_oracle(gran, og):
+    """The row-parallel linear's per-rank path under a fine-grained recipe
+    (FineOps: fp32 partial output, then the all-reduce) in a group of one
+    rank on NCCL: y, dx and dW against the oracle."""
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1,
+                            timeout=datetime.timedelta(seconds=120), device_id=torch.device(DEV, 0))
+    try:
+        M, K, N = 256, 512, 384
+        w = wl.normal((N, K), 0.02, 291).to(DEV)
+        layer = tp.RowParallelFP8Linear(tp.shard_cols(w, 0, 1), M, gran=gran)
+        assert isinstance(layer.ops, tp.FineOps)
+        for step in range(2):
+            x = wl.student_t3((M, K), 292 + step).to(DEV)
+            dy = wl.normal((M, N), 1e-3, 296 + step).to(DEV)
+            work, y = layer.forward(tp.shard_cols(x, 0, 1), async_op=True)
+            work.wait()
+            dx, dw = layer.backward(dy)
+            layer.end_step()
+            torch.cuda.synchronize()
+            assert y.dtype == torch.float32
+            st, Y = o.linear_fine_fwd(np32(x), np32(w), og)
+            dX, dW = o.linear_fine_bwd(st, np32(dy), og, o.E5M2)
+            assert_gemm_close(y, Y)
+            assert_gemm_close(dx, dX)
+            assert_gemm_close(dw, dW)
+        assert sq.fp8_device_status(True) == 0
+    finally:
+        dist.destroy_process_group()

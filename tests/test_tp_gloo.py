@@ -403,6 +403,9 @@ class OracleFineOps:
         self.st, r = self.o.linear_fine_fwd(x.numpy(), w.numpy(), self.gran)
         return torch.from_numpy(r)
 
+    def forward_partial(self, x, w):
+        return self.forward(x, w)
+
     def backward(self, dy):
         dX, dW = self.o.linear_fine_bwd(self.st, dy.numpy(), self.gran, self.o.E5M2)
         return torch.from_numpy(dX), torch.from_numpy(dW)
@@ -488,3 +491,78 @@ def test_data_parallel_fine_grained_matches_full_batch(gran_name):
             assert np.array_equal(y, Y[rank * half:(rank + 1) * half]), (step, rank)
             assert np.array_equal(dx, dX[rank * half:(rank + 1) * half]), (step, rank)
             assert _close(dw, dW), (step, rank)
+
+
+# ---------------------------------------------------------------- row-parallel, fine-grained recipes
+RM, RK, RN = 128, 512, 256      # each rank's K/P = 256 columns: whole 1x128 tiles and 128x128 blocks
+
+
+def _fine_row_inputs(step):
+    g = torch.Generator().manual_seed(70 + step)
+    x = (torch.randn((RM, RK), generator=g) * (1.0 + step)).to(torch.bfloat16).float()
+    x[9, RK - 5] = 70.0 * (step + 1)             # an outlier in the second rank's columns
+    dy = (torch.randn((RM, RN), generator=g) * 1e-3).to(torch.bfloat16).float()
+    w = (torch.randn((RN, RK), generator=torch.Generator().manual_seed(71)) * 0.02).to(torch.bfloat16).float()
+    return x, w, dy
+
+
+def _fine_row_worker(rank, ws, port, gran, out):
+    try:
+        os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        sys.path.insert(0, ROOT)
+        from scaled_quantize_gemm_gb300 import tp
+        dist.init_process_group("gloo", rank=rank, world_size=ws, timeout=__import__("datetime").timedelta(seconds=60))
+        try:
+            rec = []
+            for step in range(2):
+                x, w, dy = _fine_row_inputs(step)
+                layer = tp.RowParallelFP8Linear(tp.shard_cols(w, rank, ws), RM, ops=OracleFineOps(gran))
+                y = layer.forward(tp.shard_cols(x, rank, ws))
+                dx, dw = layer.backward(dy)
+                layer.end_step()
+                rec.append((y.numpy().copy(), dx.numpy(), dw.numpy()))
+            out.put((rank, rec))
+        finally:
+            dist.destroy_process_group()
+    except BaseException as e:
+        import traceback
+        out.put((rank, "error: " + "".join(traceback.format_exception(e))))
+        raise
+
+
+@pytest.mark.parametrize("gran_name", ["GRAN_TILE_1x128", "GRAN_TILE_POW2", "GRAN_MX32"])
+def test_row_parallel_fine_grained_matches_full_layer(gran_name):
+    """Row-parallel under the fine-grained recipes with K/P a multiple of
+    128: the summed partial outputs equal the full layer's output up to the
+    order of the sum over K, and each rank's input- and weight-gradient
+    columns equal the full layer's exactly (the contraction of dgrad runs
+    over N and that of wgrad over M, neither sharded; every unit of x and W
+    lies inside one rank's columns and dy is the same on every rank)."""
+    import oracle as o
+    gran = getattr(o, gran_name)
+    ctx = mp.get_context("spawn")
+    out = ctx.Queue()
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    procs = [ctx.Process(target=_fine_row_worker, args=(r, 2, port, gran, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = {}
+    for _ in range(2):
+        rank, rec = out.get(timeout=180)
+        assert not isinstance(rec, str), rec
+        res[rank] = rec
+    for p in procs:
+        p.join(60)
+    assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+    half = RK // 2
+    for step in range(2):
+        x, w, dy = _fine_row_inputs(step)
+        st, Y = o.linear_fine_fwd(x.numpy(), w.numpy(), gran)
+        dX, dW = o.linear_fine_bwd(st, dy.numpy(), gran, o.E5M2)
+        for rank in range(2):
+            y, dx, dw = res[rank][step]
+            assert _close(y, Y), (step, rank)
+            assert np.array_equal(dx, dX[:, rank * half:(rank + 1) * half]), (step, rank)
+            assert np.array_equal(dw, dW[:, rank * half:(rank + 1) * half]), (step, rank)
