@@ -828,6 +828,25 @@ __device__ __forceinline__ float2 ln_sq8(const float2 (&p)[4], float2 nm, float2
     }
     return acc;
 }
+// (even, odd) bf16 elements of w, each widened exactly and added to its half
+// of c with one fp32 rounding (the mixed-precision add): the value of
+// widening first and then adding, in one instruction per element.
+__device__ __forceinline__ float2 bf16x2_add(uint32_t w, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %3;\n\tadd.rn.f32.bf16 %1, hi, %4;\n\t}"
+        : "=f"(d.x), "=f"(d.y) : "r"(w), "f"(c.x), "f"(c.y));
+    return d;
+}
+// The chunk's elements minus the mean (nm = -mean), as (even, odd) pairs.
+__device__ __forceinline__ void ln_dev8(const uint4& w, float2 nm, float2 (&d)[4])
+{
+    d[0] = bf16x2_add(w.x, nm);
+    d[1] = bf16x2_add(w.y, nm);
+    d[2] = bf16x2_add(w.z, nm);
+    d[3] = bf16x2_add(w.w, nm);
+}
 // NaN-propagating max of a and |b| (|x| orders like its fp32 bit pattern,
 // and every NaN an fp32 operation returns is the canonical 0x7FFFFFFF, the
 // largest |x| pattern: the same result as the integer max of the patterns)
@@ -839,15 +858,16 @@ __device__ __forceinline__ float max_abs_nan(float a, float b)
 }
 // The LayerNorm of a chunk, y = (x - mean) rstd gamma + beta, its |y| max
 // into amax, and its codes under the multiplier m (the arithmetic of cast8).
+// d: the chunk's deviations from the mean (x - mean, rounded once).
 template <int FMT>
-__device__ __forceinline__ uint2 ln_cast8(const float2 (&p)[4], float2 nm, float2 rs, const float2 (&g)[4],
+__device__ __forceinline__ uint2 ln_cast8(const float2 (&d)[4], float2 rs, const float2 (&g)[4],
                                           const float2 (&be)[4], float m, float& amax, uint32_t& nsat)
 {
     float2 y[4];
     float a = 0.0f;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        y[k] = __ffma2_rn(__fmul2_rn(__fadd2_rn(p[k], nm), rs), g[k], be[k]);
+        y[k] = __ffma2_rn(__fmul2_rn(d[k], rs), g[k], be[k]);
         a = max_abs_nan(max_abs_nan(a, y[k].x), y[k].y);
     }
     amax = max_abs_nan(amax, a);
@@ -946,9 +966,12 @@ __global__ void __launch_bounds__(256) k_ln_stats_long(const uint16_t* __restric
 
 // Rows of up to 32 x 8 x CT elements (CT = 4: 1024, CT = 8: 2048, CT = 16:
 // 4096), one warp per RBW rows at a time: lane l owns the 8-element chunks
-// l, l + 32, ... of its rows, sums them in that order (pairs as above), and
-// a warp butterfly (the same sum in every lane) completes the row; no
-// barrier and no shared memory reduction.  Each lane copies its chunks of the
+// l, l + 32, ... of its rows and sums them in that order into eight
+// partials, one per element position of a chunk (mixed-precision adds, no
+// separate widening), which it combines as ((p0 + p1) + (p2 + p3)) over the
+// (even, odd) pairs and then even + odd; the squared deviations take the
+// (even, odd) pairs as above.  A warp butterfly (the same sum in every lane)
+// completes the row; no barrier and no shared memory reduction.  Each lane copies its chunks of the
 // warp's next rows into the warp's shared-memory stage (cp.async) once its
 // sums have consumed the current ones, so the next rows' loads are in flight
 // while the current rows are reduced, normalised and cast (no barrier guards
@@ -1031,15 +1054,18 @@ __global__ void __launch_bounds__(256, CT >= 16 ? 2 : 3) k_ln_warp(const uint16_
         float s0[RBW];
 #pragma unroll
         for (int j = 0; j < RBW; ++j) {
-            float2 acc = make_float2(0.0f, 0.0f);
+            float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                             make_float2(0.0f, 0.0f)};
 #pragma unroll
             for (int i = 0; i < CT; ++i) {
                 if (lane + 32 * i >= nch) continue;
-                float2 p[4];
-                bf16x8_pairs(v[j][i].w, p);
-                acc = ln_sum8(p, acc);
+                acc[0] = bf16x2_add(v[j][i].w.x, acc[0]);
+                acc[1] = bf16x2_add(v[j][i].w.y, acc[1]);
+                acc[2] = bf16x2_add(v[j][i].w.z, acc[2]);
+                acc[3] = bf16x2_add(v[j][i].w.w, acc[3]);
             }
-            s0[j] = __fadd_rn(acc.x, acc.y);
+            const float2 t = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+            s0[j] = __fadd_rn(t.x, t.y);
         }
         // the sums have consumed this warp's stage: start the next rows'
         stage(r0 + stride);
@@ -1051,9 +1077,10 @@ __global__ void __launch_bounds__(256, CT >= 16 ? 2 : 3) k_ln_warp(const uint16_
 #pragma unroll
             for (int i = 0; i < CT; ++i) {
                 if (lane + 32 * i >= nch) continue;
-                float2 p[4];
-                bf16x8_pairs(v[j][i].w, p);
-                acc = ln_sq8(p, make_float2(-mean[j], -mean[j]), acc);
+                float2 d[4];
+                ln_dev8(v[j][i].w, make_float2(-mean[j], -mean[j]), d);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) acc = __ffma2_rn(d[k], d[k], acc);
             }
             const float var = __fdiv_rn(ln_warp_sum(__fadd_rn(acc.x, acc.y)), (float)K);
             rs[j] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, eps)));
@@ -1075,11 +1102,10 @@ __global__ void __launch_bounds__(256, CT >= 16 ? 2 : 3) k_ln_warp(const uint16_
 #pragma unroll
                 for (int j = 0; j < RBW; ++j) {
                     if (r0 + j >= R) continue;
-                    float2 p[4];
-                    bf16x8_pairs(v[j][i].w, p);
+                    float2 d[4];
+                    ln_dev8(v[j][i].w, make_float2(-mean[j], -mean[j]), d);
                     *reinterpret_cast<uint2*>(q + (r0 + j) * (int64_t)K + c * 8) =
-                        ln_cast8<FMT>(p, make_float2(-mean[j], -mean[j]), make_float2(rs[j], rs[j]), g, be, m, amax,
-                                      nsat);
+                        ln_cast8<FMT>(d, make_float2(rs[j], rs[j]), g, be, m, amax, nsat);
                 }
             }
         }
