@@ -213,6 +213,16 @@ __device__ __forceinline__ uint32_t block_max_bits(uint32_t v, uint32_t* red)
 // over 8-element chunks, 4 independent 128-bit loads in flight per thread.
 constexpr int kFlatThreads = 256;
 constexpr int kFlatUnroll = 4;
+// 16-element groups per thread per pass of the row-unit kernels: two for
+// 1x128 tiles, four for MX-32 blocks.  Measured on the GB300 (interleaved,
+// L2 flushed): 1x128 at 16384 x 14336 110.6 -> 108.2-108.5 us with two
+// against four; MX-32 with two was faster at 4096 x 4096 but slower at
+// 8192 x 8192 (34.8 against 34.1 us); eight was slower at every size.
+template <int UNIT>
+__host__ __device__ constexpr int row_unroll()
+{
+    return UNIT == 32 ? 4 : 2;
+}
 
 // amax of one tensor over blocks [bid, bid + nblk, ...) of a grid-stride loop
 template <int DT>
@@ -1212,13 +1222,14 @@ __global__ void __launch_bounds__(kFlatThreads) k_quant_rowunits(const void* __r
 {
     pdl_enter();
     constexpr int TPU = UNIT / 16;  // lanes per unit
+    constexpr int U = row_unroll<UNIT>();
     const int64_t ng = n / 16;      // 16-element groups
     uint32_t nsat = 0;
-    const int64_t stride = (int64_t)gridDim.x * kFlatThreads * kFlatUnroll;
-    for (int64_t g0 = (int64_t)blockIdx.x * kFlatThreads * kFlatUnroll; g0 < ng; g0 += stride) {
-        Vec8<DT> v[kFlatUnroll][2];
+    const int64_t stride = (int64_t)gridDim.x * kFlatThreads * U;
+    for (int64_t g0 = (int64_t)blockIdx.x * kFlatThreads * U; g0 < ng; g0 += stride) {
+        Vec8<DT> v[U][2];
 #pragma unroll
-        for (int u = 0; u < kFlatUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int64_t g = g0 + u * kFlatThreads + threadIdx.x;
             if (g < ng) {
                 v[u][0].load(x, g * 16);
@@ -1229,7 +1240,7 @@ __global__ void __launch_bounds__(kFlatThreads) k_quant_rowunits(const void* __r
             }
         }
 #pragma unroll
-        for (int u = 0; u < kFlatUnroll; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int64_t g = g0 + u * kFlatThreads + threadIdx.x;
             const uint32_t b0 = v[u][0].absmax_bits(), b1 = v[u][1].absmax_bits();
             uint32_t a = max(b0, b1);
@@ -1437,6 +1448,17 @@ static int flat_grid(K kern, int64_t nch, int sms)
     return g < 1 ? 1 : (int)g;
 }
 
+// The same for the row-unit kernels (U groups per thread per pass).
+template <int U, typename K>
+static int flat_grid_u(K kern, int64_t nch, int sms)
+{
+    const int64_t per_block = (int64_t)kFlatThreads * U;
+    const int64_t need = (nch + per_block - 1) / per_block;
+    const int64_t cap = flat_cap(reinterpret_cast<const void*>(kern), sms);
+    const int64_t g = need < cap ? need : cap;
+    return g < 1 ? 1 : (int)g;
+}
+
 // The grids of the two jobs of a two-tensor flat kernel: each job's own need
 // when both fit at once, else the resident capacity split in proportion to
 // the jobs' sizes (at least one CTA each).
@@ -1466,10 +1488,10 @@ static cudaError_t amax_dt(const QuantArgs& a, cudaStream_t st, int sms)
         if (n > 0) launch_k(k_amax_tensor<DT>, flat_grid(k_amax_tensor<DT>, n / 8, sms), kFlatThreads, 0, st, a.x, n, a.amax);
         break;
     case kTile:
-        if (n > 0) launch_k(k_quant_rowunits<DT, kE4M3, 128, false>, flat_grid(k_quant_rowunits<DT, kE4M3, 128, false>, n / 16, sms), kFlatThreads, 0, st, a.x, n, nullptr, nullptr, a.amax, nullptr, (int64_t)0);
+        if (n > 0) launch_k(k_quant_rowunits<DT, kE4M3, 128, false>, flat_grid_u<row_unroll<128>()>(k_quant_rowunits<DT, kE4M3, 128, false>, n / 16, sms), kFlatThreads, 0, st, a.x, n, nullptr, nullptr, a.amax, nullptr, (int64_t)0);
         break;
     case kMX:
-        if (n > 0) launch_k(k_quant_rowunits<DT, kE4M3, 32, false>, flat_grid(k_quant_rowunits<DT, kE4M3, 32, false>, n / 16, sms), kFlatThreads, 0, st, a.x, n, nullptr, nullptr, a.amax, nullptr, (int64_t)0);
+        if (n > 0) launch_k(k_quant_rowunits<DT, kE4M3, 32, false>, flat_grid_u<row_unroll<32>()>(k_quant_rowunits<DT, kE4M3, 32, false>, n / 16, sms), kFlatThreads, 0, st, a.x, n, nullptr, nullptr, a.amax, nullptr, (int64_t)0);
         break;
     case kBlock:
         if (n > 0) launch_k(k_quant_block128<DT, kE4M3, false>, dim3((unsigned)(a.cols / 128), (unsigned)(a.rows / 128)), 256, 0, st, a.x, a.rows, a.cols, nullptr, nullptr, a.amax, nullptr,
@@ -1527,21 +1549,21 @@ static cudaError_t quant_dt_fmt(const QuantArgs& a, cudaStream_t st, int sms)
     if (n == 0) return cudaSuccess;
     switch (a.gran) {
     case kTile:
-        launch_k(k_quant_rowunits<DT, FMT, 128, true>, flat_grid(k_quant_rowunits<DT, FMT, 128, true>, n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat,
+        launch_k(k_quant_rowunits<DT, FMT, 128, true>, flat_grid_u<row_unroll<128>()>(k_quant_rowunits<DT, FMT, 128, true>, n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat,
                  (int64_t)0);
         break;
     case kMX:
-        launch_k(k_quant_rowunits<DT, FMT, 32, true>, flat_grid(k_quant_rowunits<DT, FMT, 32, true>, n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat,
+        launch_k(k_quant_rowunits<DT, FMT, 32, true>, flat_grid_u<row_unroll<32>()>(k_quant_rowunits<DT, FMT, 32, true>, n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat,
                  (int64_t)0);
         break;
     case kMXTiled:
-        launch_k(k_quant_rowunits<DT, FMT, 32, true, true>, flat_grid(k_quant_rowunits<DT, FMT, 32, true, true>, n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
+        launch_k(k_quant_rowunits<DT, FMT, 32, true, true>, flat_grid_u<row_unroll<32>()>(k_quant_rowunits<DT, FMT, 32, true, true>, n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
         break;
     case kTilePow2:
-        launch_k(k_quant_rowunits<DT, FMT, 128, true, true, 1>, flat_grid(k_quant_rowunits<DT, FMT, 128, true, true, 1>, n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
+        launch_k(k_quant_rowunits<DT, FMT, 128, true, true, 1>, flat_grid_u<row_unroll<128>()>(k_quant_rowunits<DT, FMT, 128, true, true, 1>, n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
         break;
     case kMXFloor:
-        launch_k(k_quant_rowunits<DT, FMT, 32, true, true, 2>, flat_grid(k_quant_rowunits<DT, FMT, 32, true, true, 2>, n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
+        launch_k(k_quant_rowunits<DT, FMT, 32, true, true, 2>, flat_grid_u<row_unroll<32>()>(k_quant_rowunits<DT, FMT, 32, true, true, 2>, n / 16, sms), kFlatThreads, 0, st, a.x, n, a.q, a.scales, a.amax, a.sat, a.cols);
         break;
     case kBlockPow2:
         // (qT and scalesT: the transposed codes and the tiled E8M0 codes of
