@@ -1299,8 +1299,11 @@ __global__ void __launch_bounds__(kFlatThreads) k_quant_rowunits(const void* __r
 // POW2: the block scale is the smallest power of two that fits (E8M0); its
 // code fills the block's whole 512-byte chunk of the tiled MX layout (all 128
 // rows x four 32-blocks), so the block feeds the block-scaled GEMM directly.
+// Four CTAs per SM (64 registers, no spills): measured on the GB300 against
+// three (80 registers), L2 flushed, identical codes: 16384 x 14336 106.5 ->
+// 100.4 us (with qT 141.6 -> 139.3), 8192 x 8192 32.3 -> 28.7 us.
 template <int DT, int FMT, bool WRITE_Q, bool POW2 = false>
-__global__ void __launch_bounds__(256) k_quant_block128(const void* __restrict__ x, int64_t R, int64_t C,
+__global__ void __launch_bounds__(256, 4) k_quant_block128(const void* __restrict__ x, int64_t R, int64_t C,
                                                         uint8_t* __restrict__ q, float* s_out,
                                                         float* amax_out, unsigned long long* sat,
                                                         uint8_t* __restrict__ qT = nullptr, float* sT = nullptr,
